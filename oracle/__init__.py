@@ -1,0 +1,192 @@
+"""CPU oracle for decode-step token selection -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg may import this package. The product path (the CUDA library and its
+Python binding) never imports it, and the two share no code.
+
+The arithmetic lives in ``sel_oracle.c`` (plain C, double precision). This
+module compiles it with gcc on first use, loads it with ctypes and converts
+numpy arrays. See the C file's header for the definitions and the page
+passages each routine follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import tempfile
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sel_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libsel_oracle.so")
+
+INVALID_ID = 0xFFFFFFFF
+
+# -ffp-contract=off: no fused multiply-add, so x86 and Arm hosts round alike.
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared"]
+
+
+def compile_oracle(src: str = _SRC, out: str = _LIB_PATH,
+                   extra_flags: tuple[str, ...] = ()) -> str:
+    """Compile ``src`` into the shared library ``out`` (atomic replace)."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=os.path.dirname(out))
+    os.close(fd)
+    try:
+        subprocess.run(["gcc", *CFLAGS, *extra_flags, "-o", tmp, src, "-lm"],
+                       check=True, capture_output=True, text=True)
+        os.replace(tmp, out)
+    finally:
+        if os.path.exists(tmp):
+            os.unlink(tmp)
+    return out
+
+
+def build() -> str:
+    """Compile the oracle if the library is missing or older than its source."""
+    if (not os.path.exists(_LIB_PATH)
+            or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)):
+        compile_oracle()
+    return _LIB_PATH
+
+
+_f32p = ctypes.POINTER(ctypes.c_float)
+_u32p = ctypes.POINTER(ctypes.c_uint32)
+_f64p = ctypes.POINTER(ctypes.c_double)
+_u32 = ctypes.c_uint32
+
+
+def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
+    lib.orc_argmax_row.argtypes = [_f32p, _u32]
+    lib.orc_argmax_row.restype = _u32
+    lib.orc_argmax.argtypes = [_f32p, _u32, _u32, _u32p]
+    lib.orc_argmax.restype = None
+    lib.orc_topk.argtypes = [_f32p, _u32, _u32, _u32, _f32p, _u32p]
+    lib.orc_topk.restype = None
+    lib.orc_sample.argtypes = [_f32p, _u32, _u32, ctypes.c_double, _u32,
+                               ctypes.c_double, ctypes.c_double, ctypes.c_int,
+                               _f32p, _u32p, _f64p, _f64p]
+    lib.orc_sample.restype = ctypes.c_int
+    lib.orc_spec_accept.argtypes = [_f32p, _f32p, _u32p, _u32, _u32, _u32,
+                                    ctypes.c_double, ctypes.c_int, _f32p,
+                                    _f32p, _u32p, _u32p, _f64p, _f64p]
+    lib.orc_spec_accept.restype = ctypes.c_int
+    lib.orc_softmax_row.argtypes = [_f32p, _u32, ctypes.c_double, _f64p]
+    lib.orc_softmax_row.restype = None
+    return lib
+
+
+def load(path: str | None = None) -> "Oracle":
+    """Load the oracle library (building it first when ``path`` is None)."""
+    return Oracle(_declare(ctypes.CDLL(path or build())))
+
+
+def _f32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def _ptr(a: np.ndarray, ctype):
+    return a.ctypes.data_as(ctype)
+
+
+@dataclass
+class SampleResult:
+    ids: np.ndarray      # uint32 [rows]
+    probs: np.ndarray    # float64 [rows], probability of the drawn id
+    margin: np.ndarray   # float64 [rows], nearest decision's distance to its threshold
+
+
+@dataclass
+class SpecResult:
+    accepted: np.ndarray       # uint32 [S]
+    emitted: np.ndarray        # uint32 [S, K+1]
+    margin_accept: np.ndarray  # float64 [S], min |u q - p| / max(p, q) over tested positions
+    margin_draw: np.ndarray    # float64 [S], min |u - C_i| of the final draw
+
+
+class Oracle:
+    """Thin numpy wrapper over the C oracle. ctypes calls release the GIL,
+    so rows can be spread over Python threads."""
+
+    def __init__(self, lib: ctypes.CDLL):
+        self.lib = lib
+
+    def argmax(self, logits) -> np.ndarray:
+        x = _f32(logits)
+        rows, V = x.shape
+        out = np.empty(rows, dtype=np.uint32)
+        self.lib.orc_argmax(_ptr(x, _f32p), rows, V, _ptr(out, _u32p))
+        return out
+
+    def topk(self, logits, k: int) -> tuple[np.ndarray, np.ndarray]:
+        x = _f32(logits)
+        rows, V = x.shape
+        vals = np.empty((rows, k), dtype=np.float32)
+        ids = np.empty((rows, k), dtype=np.uint32)
+        self.lib.orc_topk(_ptr(x, _f32p), rows, V, k, _ptr(vals, _f32p),
+                          _ptr(ids, _u32p))
+        return vals, ids
+
+    def sample(self, logits, uniforms, temperature: float, top_k: int,
+               top_p: float, min_p: float, temp_last: bool = False) -> SampleResult:
+        x = _f32(logits)
+        rows, V = x.shape
+        u = _f32(uniforms).reshape(rows)
+        ids = np.empty(rows, dtype=np.uint32)
+        probs = np.empty(rows, dtype=np.float64)
+        margin = np.empty(rows, dtype=np.float64)
+        self.lib.orc_sample(_ptr(x, _f32p), rows, V, float(temperature),
+                            int(top_k), float(top_p), float(min_p),
+                            int(bool(temp_last)), _ptr(u, _f32p),
+                            _ptr(ids, _u32p), _ptr(probs, _f64p),
+                            _ptr(margin, _f64p))
+        return SampleResult(ids, probs, margin)
+
+    def spec_accept(self, target, draft, draft_tokens, temperature: float,
+                    mode: int, u_acc=None, u_fin=None) -> SpecResult:
+        """target [S, K+1, V], draft [S, K, V] (None allowed for mode 1),
+        draft_tokens [S, K]; mode 0 = rejection sampling, 1 = argmax rule."""
+        t = _f32(target)
+        S, K1, V = t.shape
+        K = K1 - 1
+        tok = np.ascontiguousarray(draft_tokens, dtype=np.uint32).reshape(S, K)
+        d = None if draft is None else _f32(draft).reshape(S, K, V)
+        if mode == 0 and d is None:
+            raise ValueError("rejection mode needs draft logits")
+        ua = None if u_acc is None else _f32(u_acc).reshape(S, K)
+        uf = None if u_fin is None else _f32(u_fin).reshape(S)
+        if mode == 0 and temperature != 0.0 and (ua is None or uf is None):
+            raise ValueError("rejection mode needs u_acc and u_fin")
+        acc = np.empty(S, dtype=np.uint32)
+        emi = np.empty((S, K + 1), dtype=np.uint32)
+        ma = np.empty(S, dtype=np.float64)
+        md = np.empty(S, dtype=np.float64)
+        self.lib.orc_spec_accept(
+            _ptr(t, _f32p), None if d is None else _ptr(d, _f32p),
+            _ptr(tok, _u32p), S, K, V, float(temperature), int(mode),
+            None if ua is None else _ptr(ua, _f32p),
+            None if uf is None else _ptr(uf, _f32p),
+            _ptr(acc, _u32p), _ptr(emi, _u32p), _ptr(ma, _f64p),
+            _ptr(md, _f64p))
+        return SpecResult(acc, emi, ma, md)
+
+    def softmax_row(self, x, temperature: float = 1.0) -> np.ndarray:
+        x = _f32(x).reshape(-1)
+        p = np.empty(x.size, dtype=np.float64)
+        self.lib.orc_softmax_row(_ptr(x, _f32p), x.size, float(temperature),
+                                 _ptr(p, _f64p))
+        return p
+
+
+_default: Oracle | None = None
+
+
+def default() -> Oracle:
+    global _default
+    if _default is None:
+        _default = load()
+    return _default

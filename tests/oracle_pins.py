@@ -1,0 +1,429 @@
+"""Pins for the CPU oracle: checks that tie the oracle to what the pages and
+the mathematics fix, independently of the oracle's own code.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError
+on a violation. The test files run every pin on the real oracle; the mutant
+test compiles copies of the oracle with a planted mistake and requires that
+at least one pin fails for each copy.
+
+Kinds of pin used here:
+  * values the pages print (the tie rule, the 202,048 partition, the
+    p(a)=0.3 / q(a)=0.95 ceiling example, the chi-square recipe);
+  * closed forms derived by hand (tests/golden/*.json);
+  * brute force on tiny inputs (rank counting for top-k, a characterisation
+    of the first maximum);
+  * library routines for special cases (numpy's first-occurrence argmax,
+    numpy's lexsort ordering);
+  * statistical laws: acceptance -> sum min(p, q), emitted stream -> p.
+"""
+from __future__ import annotations
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+INVALID = 0xFFFFFFFF
+NEG = -1e30  # a finite logit whose probability is exactly 0 in double
+
+
+def golden(name: str):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _logits_from(case_or_probs) -> np.ndarray:
+    if isinstance(case_or_probs, dict):
+        if "logits" in case_or_probs:
+            return np.asarray(case_or_probs["logits"], dtype=np.float32)
+        case_or_probs = case_or_probs["probs"]
+    p = np.asarray(case_or_probs, dtype=np.float64)
+    with np.errstate(divide="ignore"):
+        lg = np.where(p > 0, np.log(np.where(p > 0, p, 1.0)), NEG)
+    return lg.astype(np.float32)
+
+
+# ---------------------------------------------------------------------------
+# argmax
+# ---------------------------------------------------------------------------
+
+def _is_first_max(x: np.ndarray, i: int) -> bool:
+    """i attains the maximum and no earlier index does."""
+    return bool(np.all(x[i] >= x) and np.all(x[:i] < x[i]))
+
+
+def pin_argmax_ties(orc):
+    """Ch 21, 21.3: strict '>' keeps the lower index on ties. Planted equal
+    maxima (the planted-argmax workload's recipe) -> lowest planted id."""
+    rng = np.random.default_rng(123)
+    for V in (7, 1000, 202048):
+        x = rng.normal(0, 3, size=V).astype(np.float32)
+        ids = np.sort(rng.choice(V, size=3, replace=False))
+        x[ids] = x.max() + np.float32(1.0)
+        got = int(orc.argmax(x[None])[0])
+        assert got == ids[0], (V, got, ids)
+    # -0.0 and +0.0 compare equal: the lower index wins
+    x = np.array([-1.0, -0.0, 0.0, -2.0], dtype=np.float32)
+    assert int(orc.argmax(x[None])[0]) == 1
+    x = np.array([-1.0, 0.0, -0.0], dtype=np.float32)
+    assert int(orc.argmax(x[None])[0]) == 1
+
+
+def pin_argmax_bruteforce(orc):
+    """Every row over the alphabet {0, 1, 2} up to length 6: the result is the
+    unique first maximum (characterised, not recomputed by a scan)."""
+    for V in range(1, 7):
+        rows = np.array(list(itertools.product((0.0, 1.0, 2.0), repeat=V)),
+                        dtype=np.float32)
+        got = orc.argmax(rows)
+        for r in range(rows.shape[0]):
+            assert _is_first_max(rows[r], int(got[r])), (rows[r], got[r])
+
+
+def pin_argmax_numpy(orc):
+    """numpy.argmax documents first-occurrence; on finite rows it must agree.
+    Rows drawn from a small integer set so ties are frequent."""
+    rng = np.random.default_rng(7)
+    x = rng.integers(0, 5, size=(64, 333)).astype(np.float32)
+    assert np.array_equal(orc.argmax(x), np.argmax(x, axis=1).astype(np.uint32))
+    x = rng.normal(size=(16, 5000)).astype(np.float32)
+    assert np.array_equal(orc.argmax(x), np.argmax(x, axis=1).astype(np.uint32))
+
+
+def pin_argmax_partition(orc):
+    """Ch 21, Figure 21.1: V = 202,048 = 197 x 1,024 + 320. The maximum placed
+    at each chunk edge and in the ragged tail is found."""
+    g = golden("argmax_partition.json")
+    V, chunk = g["V"], g["chunk"]
+    assert g["full_chunks"] * chunk + g["tail"] == V
+    assert math.ceil(V / chunk) == g["chunks"]
+    base = np.random.default_rng(0).normal(0, 3, size=V).astype(np.float32)
+    for pos in g["positions"]:
+        x = base.copy()
+        x[pos] = x.max() + np.float32(1.0)
+        assert int(orc.argmax(x[None])[0]) == pos, pos
+    for V in (1, 2, 3, 5, 1023, 1024, 1025, 202047):
+        x = np.random.default_rng(V).normal(size=V).astype(np.float32)
+        for pos in {0, V // 2, V - 1}:
+            y = x.copy()
+            y[pos] = 100.0
+            assert int(orc.argmax(y[None])[0]) == pos, (V, pos)
+
+
+def pin_argmax_nonfinite(orc):
+    """Ch 21, 21.4 / 21.6: any NaN or +-Inf makes the row fail closed."""
+    for bad in (np.nan, np.inf, -np.inf):
+        for pos in (0, 17, 99):
+            x = np.zeros((1, 100), dtype=np.float32)
+            x[0, pos] = bad
+            assert int(orc.argmax(x)[0]) == INVALID, (bad, pos)
+
+
+# ---------------------------------------------------------------------------
+# top-k
+# ---------------------------------------------------------------------------
+
+def _rank_topk(x: np.ndarray, k: int):
+    """O(V^2) rank counting: rank_i = #{j : x_j > x_i or (x_j == x_i, j < i)}."""
+    V = x.size
+    rank = np.array([sum(1 for j in range(V)
+                         if x[j] > x[i] or (x[j] == x[i] and j < i))
+                     for i in range(V)])
+    ids = np.argsort(rank)[:k]
+    return ids
+
+
+def pin_topk_bruteforce(orc):
+    rng = np.random.default_rng(11)
+    for V in range(1, 17):
+        for _ in range(6):
+            x = rng.integers(-3, 4, size=V).astype(np.float32)
+            for k in sorted({1, (V + 1) // 2, V}):
+                vals, ids = orc.topk(x[None], k)
+                want = _rank_topk(x, k)
+                assert np.array_equal(ids[0], want.astype(np.uint32)), (x, k, ids, want)
+                assert np.array_equal(vals[0], x[want]), (x, k)
+
+
+def pin_topk_lexsort(orc):
+    """numpy.lexsort orders by (-value, id): an independent library route."""
+    rng = np.random.default_rng(12)
+    x = rng.integers(0, 50, size=(8, 3000)).astype(np.float32)
+    vals, ids = orc.topk(x, 84)
+    for r in range(x.shape[0]):
+        order = np.lexsort((np.arange(x.shape[1]), -x[r].astype(np.float64)))
+        assert np.array_equal(ids[r], order[:84].astype(np.uint32))
+
+
+def pin_topk_special(orc):
+    rng = np.random.default_rng(13)
+    x = rng.normal(size=(5, 999)).astype(np.float32)
+    _, ids1 = orc.topk(x, 1)
+    assert np.array_equal(ids1[:, 0], orc.argmax(x))      # k = 1 is argmax
+    eq = np.full((1, 50), 2.5, dtype=np.float32)           # all equal: ids 0..k-1
+    _, ids = orc.topk(eq, 7)
+    assert np.array_equal(ids[0], np.arange(7, dtype=np.uint32))
+    vals, ids = orc.topk(x, 999)                            # k = V: full order
+    assert np.all(np.diff(vals, axis=1) <= 0)
+    assert np.array_equal(np.sort(ids, axis=1),
+                          np.tile(np.arange(999, dtype=np.uint32), (5, 1)))
+    bad = x.copy()
+    bad[2, 500] = np.nan
+    vals, ids = orc.topk(bad, 3)
+    assert np.all(ids[2] == INVALID) and np.all(np.isnan(vals[2]))
+    assert np.all(ids[[0, 1, 3, 4]] != INVALID)
+
+
+# ---------------------------------------------------------------------------
+# filtered sampling
+# ---------------------------------------------------------------------------
+
+def pin_sample_closed_forms(orc):
+    g = golden("sample_closed_forms.json")
+    for case in g["cases"]:
+        x = _logits_from(case)[None]
+        for u, want_id, want_p in case["draws"]:
+            r = orc.sample(x, [u], case["T"], case["top_k"], case["top_p"],
+                           case["min_p"], case["temp_last"])
+            assert int(r.ids[0]) == want_id, (case["name"], u, r.ids[0])
+            assert abs(r.probs[0] - want_p) <= 1e-6 * max(1.0, want_p), \
+                (case["name"], u, r.probs[0], want_p)
+
+
+def pin_sample_cdf_grid(orc):
+    """Sweep u over a 10^5-point grid on a row with hand-chosen probabilities:
+    the share of grid points mapped to each id equals its probability."""
+    P = np.array([0.05, 0.4, 0.15, 0.1, 0.3])  # order by P: ids 1, 4, 2, 3, 0
+    x = np.tile(_logits_from(P), (100_000, 1))
+    u = ((np.arange(100_000) + 0.5) / 100_000).astype(np.float32)
+    r = orc.sample(x, u, 1.0, 0, 1.0, 0.0)
+    share = np.bincount(r.ids.astype(np.int64), minlength=5) / 100_000
+    assert np.allclose(share, P, atol=2e-5), share
+    # the map is monotone in u along the (P desc, id asc) order
+    rank_of = {1: 0, 4: 1, 2: 2, 3: 3, 0: 4}
+    ranks = np.array([rank_of[int(i)] for i in r.ids])
+    assert np.all(np.diff(ranks) >= 0)
+    # each drawn id's reported probability is its own
+    assert np.allclose(r.probs, P[r.ids.astype(np.int64)], rtol=1e-6)
+
+
+def pin_sample_support(orc):
+    """Zero tolerance on support: every draw lies in the top_k set, and with
+    top_p = 1, min_p = 0 every top_k id is reachable."""
+    rng = np.random.default_rng(21)
+    x = np.tile(rng.normal(0, 2, size=300).astype(np.float32), (4000, 1))
+    u = rng.random(4000, dtype=np.float32)
+    _, top = orc.topk(x[:1], 8)
+    r = orc.sample(x, u, 0.8, 8, 1.0, 0.0)
+    assert set(r.ids.tolist()) <= set(top[0].tolist())
+    assert set(r.ids.tolist()) == set(top[0].tolist())
+
+
+def pin_sample_invalid(orc):
+    x = np.zeros((4, 10), dtype=np.float32)
+    x[3, 2] = np.inf
+    r = orc.sample(x, np.array([1.0, -0.25, np.nan, 0.5], dtype=np.float32),
+                   1.0, 0, 1.0, 0.0)
+    assert np.all(r.ids == INVALID) and np.all(np.isnan(r.probs))
+
+
+# ---------------------------------------------------------------------------
+# speculative acceptance
+# ---------------------------------------------------------------------------
+
+def _spec_case_arrays(g, case):
+    rows = {k: _logits_from(v) for k, v in g["rows"].items()}
+    target = np.stack([rows[n] for n in case["target"]])[None]
+    draft = None if case["draft"] is None else np.stack([rows[n] for n in case["draft"]])[None]
+    return target, draft
+
+
+def pin_spec_closed_forms(orc):
+    g = golden("spec_closed_forms.json")
+    for case in g["cases"]:
+        target, draft = _spec_case_arrays(g, case)
+        mode = 0 if case["mode"] == "rejection" else 1
+        K = len(case["tokens"])
+        r = orc.spec_accept(target, draft, np.array([case["tokens"]]),
+                            case.get("T", 1.0), mode,
+                            np.array([case.get("u_acc", [0.0] * K)], dtype=np.float32),
+                            np.array([case.get("u_fin", 0.0)], dtype=np.float32))
+        want = [INVALID if e is None else e for e in case["emitted"]]
+        assert int(r.accepted[0]) == case["accepted"], (case["name"], r.accepted)
+        assert r.emitted[0].tolist() == want, (case["name"], r.emitted[0])
+
+
+def _draws_from(rng, P, n):
+    return rng.choice(P.size, size=n, p=P / P.sum())
+
+
+def _spec_rounds(orc, p, q, n, seed, mode=0, K=1, bonus=None):
+    """n independent single-sequence rounds with draft tokens drawn from q."""
+    rng = np.random.default_rng(seed)
+    V = p.size
+    lp, lq = _logits_from(p), _logits_from(q)
+    lb = _logits_from(p if bonus is None else bonus)
+    target = np.empty((n, K + 1, V), dtype=np.float32)
+    target[:, :K] = lp
+    target[:, K] = lb
+    draft = np.empty((n, K, V), dtype=np.float32)
+    draft[:] = lq
+    tokens = _draws_from(rng, q, n * K).reshape(n, K)
+    u_acc = rng.random((n, K), dtype=np.float32)
+    u_fin = rng.random(n, dtype=np.float32)
+    return orc.spec_accept(target, draft, tokens, 1.0, mode, u_acc, u_fin)
+
+
+def pin_spec_ceiling_example(orc):
+    """mlxcel, The acceptance ceiling: argmax rule 0.95 vs ceiling 0.30."""
+    g = golden("spec_ceiling_example.json")
+    p, q = np.array(g["p"]), np.array(g["q"])
+    n = 20_000
+    assert abs(np.minimum(p, q).sum() - g["accept_rejection_rule"]) < 1e-12
+    assert abs(q[np.argmax(p)] - g["accept_argmax_rule"]) < 1e-12
+    for mode, want in ((0, g["accept_rejection_rule"]), (1, g["accept_argmax_rule"])):
+        r = _spec_rounds(orc, p, q, n, seed=31 + mode, mode=mode)
+        rate = float(np.mean(r.accepted == 1))
+        sd = math.sqrt(want * (1 - want) / n)
+        assert abs(rate - want) < 5 * sd, (mode, rate, want)
+
+
+def pin_spec_acceptance_law(orc):
+    """Per-position acceptance converges to sum_x min(p, q) (the rule's
+    closed form) and not to sum_x p q (sampler-match)."""
+    rng = np.random.default_rng(41)
+    for trial in range(3):
+        p = rng.dirichlet(np.ones(6))
+        q = rng.dirichlet(np.ones(6))
+        n = 20_000
+        r = _spec_rounds(orc, p, q, n, seed=50 + trial)
+        rate = float(np.mean(r.accepted == 1))
+        smin = float(np.minimum(p, q).sum())
+        sd = math.sqrt(smin * (1 - smin) / n)
+        assert abs(rate - smin) < 5 * sd, (rate, smin)
+
+
+def chi_square(counts: np.ndarray, probs: np.ndarray) -> float:
+    expected = probs * counts.sum()
+    return float(np.sum((counts - expected) ** 2 / expected))
+
+
+def pin_spec_stream_is_target(orc):
+    """mlxcel, Regression guards: the emitted stream matches the target's
+    exact categorical by chi-square (12000 tokens, dof 5, reject > 25.7448)."""
+    g = golden("chi_square_recipe.json")
+    rng = np.random.default_rng(61)
+    p = rng.dirichlet(np.ones(6) * 2)
+    q = rng.dirichlet(np.ones(6) * 2)
+    r = _spec_rounds(orc, p, q, g["samples"], seed=62)
+    counts = np.bincount(r.emitted[:, 0].astype(np.int64), minlength=6)
+    stat = chi_square(counts, p)
+    assert stat <= g["critical"], stat
+
+
+def pin_spec_support(orc):
+    """mlxcel, Regression guards: with a top_k = 2 target no emitted token
+    ever lies outside the target's support (accepted drafts, residual draws
+    and bonus draws alike)."""
+    rng = np.random.default_rng(71)
+    p = np.array([0.0, 0.6, 0.0, 0.4, 0.0, 0.0])
+    q = rng.dirichlet(np.ones(6))
+    r = _spec_rounds(orc, p, q, 5000, seed=72, bonus=p)
+    first = r.emitted[:, 0]
+    bonus = r.emitted[:, 1][r.accepted == 1]
+    assert set(first.tolist()) <= {1, 3}, set(first.tolist())
+    assert set(bonus.tolist()) <= {1, 3}, set(bonus.tolist())
+    assert bonus.size > 0 and np.any(r.accepted == 0)
+
+
+def pin_spec_regimes(orc):
+    """q = p accepts every draft (u < 1) and draws the bonus from p_K;
+    disjoint supports reject at position 0 and draw the residual = p."""
+    rng = np.random.default_rng(81)
+    p = rng.dirichlet(np.ones(5))
+    pb = rng.dirichlet(np.ones(5))
+    n = 3000
+    r = _spec_rounds(orc, p, p, n, seed=82, K=3, bonus=pb)
+    assert np.all(r.accepted == 3)
+    counts = np.bincount(r.emitted[:, 3].astype(np.int64), minlength=5)
+    assert chi_square(counts, pb) < 25.0
+    pd = np.array([0.5, 0.5, 0.0, 0.0, 0.0])
+    qd = np.array([0.0, 0.0, 0.2, 0.3, 0.5])
+    r = _spec_rounds(orc, pd, qd, n, seed=83, K=2)
+    assert np.all(r.accepted == 0)
+    assert set(r.emitted[:, 0].tolist()) <= {0, 1}
+    share0 = float(np.mean(r.emitted[:, 0] == 0))
+    assert abs(share0 - 0.5) < 5 * math.sqrt(0.25 / n)
+
+
+def pin_spec_greedy(orc):
+    """mlxcel, RNG dependency / Regression guards: temperature 0 is the argmax
+    rule, byte-identical to greedy target decoding, whatever the uniforms."""
+    rng = np.random.default_rng(91)
+    S, K, V = 50, 4, 40
+    target = rng.normal(size=(S, K + 1, V)).astype(np.float32)
+    draft = rng.normal(size=(S, K, V)).astype(np.float32)
+    greedy = np.argmax(target, axis=2)
+    tokens = np.where(rng.random((S, K)) < 0.7, greedy[:, :K],
+                      rng.integers(0, V, size=(S, K)))
+    r0 = orc.spec_accept(target, draft, tokens, 0.0, 0,
+                         rng.random((S, K), dtype=np.float32),
+                         rng.random(S, dtype=np.float32))
+    r1 = orc.spec_accept(target, None, tokens, 1.0, 1)
+    assert np.array_equal(r0.accepted, r1.accepted)
+    assert np.array_equal(r0.emitted, r1.emitted)
+    for s in range(S):
+        n = int(r1.accepted[s])
+        assert np.array_equal(r1.emitted[s, :n + 1], greedy[s, :n + 1])
+
+
+def pin_spec_invalid(orc):
+    rng = np.random.default_rng(95)
+    target = rng.normal(size=(3, 3, 8)).astype(np.float32)
+    draft = rng.normal(size=(3, 2, 8)).astype(np.float32)
+    tokens = np.array([[1, 2], [8, 0], [0, 1]])
+    target[2, 2, 5] = np.nan
+    r = orc.spec_accept(target, draft, tokens, 1.0, 0,
+                        np.full((3, 2), 0.5, dtype=np.float32),
+                        np.full(3, 0.5, dtype=np.float32))
+    assert r.accepted[0] != INVALID
+    assert r.accepted[1] == INVALID and np.all(r.emitted[1] == INVALID)
+    assert r.accepted[2] == INVALID and np.all(r.emitted[2] == INVALID)
+
+
+ALL_PINS = [
+    pin_argmax_ties, pin_argmax_bruteforce, pin_argmax_numpy,
+    pin_argmax_partition, pin_argmax_nonfinite,
+    pin_topk_bruteforce, pin_topk_lexsort, pin_topk_special,
+    pin_sample_closed_forms, pin_sample_cdf_grid, pin_sample_support,
+    pin_sample_invalid,
+    pin_spec_closed_forms, pin_spec_ceiling_example, pin_spec_acceptance_law,
+    pin_spec_stream_is_target, pin_spec_support, pin_spec_regimes,
+    pin_spec_greedy, pin_spec_invalid,
+]
+
+
+def _main(argv):
+    """Run the pins against the oracle library at argv[1]; print the first
+    failing pin's name and exit 1, or exit 0 if every pin holds. Used by the
+    mutant test in a child process, so a planted mistake that crashes the
+    library cannot take the test runner down."""
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(GOLDEN)))
+    import oracle
+    orc = oracle.load(argv[1])
+    for pin in ALL_PINS:
+        try:
+            pin(orc)
+        except AssertionError:
+            print("FAIL", pin.__name__, flush=True)
+            return 1
+    return 0
+
+
+if __name__ == "__main__":
+    import sys
+    sys.exit(_main(sys.argv))
