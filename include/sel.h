@@ -1,0 +1,244 @@
+/*
+ * sel.h -- C ABI of the GB300 (sm_103a) decode-step token-selection library.
+ *
+ * Four operations over batched fp32 logits rows of a vocabulary of V entries:
+ * argmax, exact top-k, filtered sampling and speculative acceptance. Every
+ * entry point takes device pointers, sizes, the policy parameters, a
+ * caller-owned workspace and a cudaStream_t, validates its arguments on the
+ * host, enqueues its kernels on that stream and returns. It never allocates,
+ * never synchronises and never touches another stream.
+ *
+ * Conventions shared by every entry point
+ *  - Memory. All pointers except the parameter structs are device pointers
+ *    owned by the caller. Logits are row-major: row r starts at
+ *    logits + r * V (a row stride of exactly V floats). The vector path needs
+ *    logits 16-byte aligned and V % 4 == 0; any other 4-byte-aligned layout
+ *    takes the scalar path, with identical results.
+ *  - Workspace. d_ws holds per-row partial results and the counters that
+ *    let the last block of a row combine them. Size it with
+ *    sel_workspace_bytes() for the largest call it will serve, zero it once
+ *    with sel_workspace_init() after allocating it, then reuse it: every call
+ *    leaves its counters at zero again. Calls that may run concurrently (on
+ *    different streams) need separate workspaces. d_ws must be 256-byte
+ *    aligned.
+ *  - Errors. The return value reports what the host can see: bad arguments
+ *    (SEL_EINVAL), a workspace too small (SEL_EWORKSPACE), an unsupported
+ *    size (SEL_EUNSUPPORTED) or a launch failure (SEL_ECUDA). rows == 0 (or
+ *    S == 0) is a no-op returning SEL_OK. Data errors found on the device do
+ *    not fail the call: they make that row's (sequence's) ids
+ *    SEL_INVALID_ID, with NaN values and probabilities. A row is invalid when
+ *    it holds a NaN or +-Inf logit, or when its uniform lies outside [0, 1)
+ *    (fail closed: the greedy serving variant of the Muser book's argmax
+ *    latches nonfinite logits and returns 0xffffffff, "Ch 21 -- Sampling,
+ *    argmax, and grammar", 21.4 and 21.6).
+ *  - Ids are 31-bit: V must be below 2^31 (bit 31 of an id is the
+ *    nonfinite flag of that design).
+ *  - Determinism. Results do not depend on block scheduling: every combine
+ *    runs in a fixed order, and ties between equal logits always go to the
+ *    lower token id.
+ */
+#ifndef SEL_H
+#define SEL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sel_status {
+    SEL_OK = 0,
+    SEL_EINVAL = 1,       /* null/misaligned pointer, bad size or parameter */
+    SEL_EWORKSPACE = 2,   /* ws_bytes below sel_workspace_bytes() */
+    SEL_ECUDA = 3,        /* a CUDA call or kernel launch failed */
+    SEL_EUNSUPPORTED = 4  /* valid request outside what the kernels cover */
+} sel_status;
+
+#define SEL_INVALID_ID 0xFFFFFFFFu  /* per-row (per-sequence) error sentinel */
+#define SEL_MAX_K 1024u             /* largest k of sel_topk / top_k of sel_sample */
+#define SEL_MAX_V 0x7FFFFFFFu       /* V must be <= SEL_MAX_V (31-bit ids) */
+#define SEL_WS_ALIGN 256u
+
+/* Operation codes for sel_workspace_bytes. */
+enum { SEL_OP_ARGMAX = 0, SEL_OP_TOPK = 1, SEL_OP_SAMPLE = 2, SEL_OP_SPEC = 3 };
+
+/* Order of temperature and filters in sel_sample. */
+enum {
+    SEL_ORDER_TEMP_FIRST = 0, /* scale by 1/T, then top-k, top-p, min-p */
+    SEL_ORDER_TEMP_LAST = 1   /* top-k, top-p, min-p on the untempered
+                                 distribution; temperature only in the draw
+                                 ("Speculative-decoding acceptance rules",
+                                 The rules: filtering on the untempered
+                                 distribution, temperature scaling last) */
+};
+
+/* Acceptance rule of spec_accept. */
+enum {
+    SPEC_MODE_REJECTION = 0, /* modified rejection sampling (lossless) */
+    SPEC_MODE_ARGMAX = 1     /* argmax-against-argmax (greedy stream) */
+};
+
+/*
+ * Bytes of workspace an operation needs.
+ *   op SEL_OP_ARGMAX: rows, V (k ignored)
+ *   op SEL_OP_TOPK:   rows, V, k
+ *   op SEL_OP_SAMPLE: rows, V, k = the policy's top_k
+ *   op SEL_OP_SPEC:   rows = S (sequences), V, k = K (draft positions)
+ * The size depends only on these arguments, not on the device. Returns 0
+ * when the arguments are invalid (the entry point would refuse them anyway).
+ */
+size_t sel_workspace_bytes(int op, uint32_t rows, uint32_t V, uint32_t k);
+
+/*
+ * Zero a freshly allocated workspace: one cudaMemsetAsync on `stream`.
+ * Needed once per allocation; the entry points keep it zeroed afterwards.
+ */
+sel_status sel_workspace_init(void *d_ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * sel_argmax -- per row, the lowest index attaining the maximum logit.
+ *
+ * Defined by the Muser book chapter "Ch 21 -- Sampling, argmax, and
+ * grammar": 21.3 (a reduction of each row to one (value, index) pair; the
+ * comparison is strictly greater, so a tie keeps the lower index), 21.4 (the
+ * greedy serving variant: any NaN/Inf latches a flag and the result is
+ * 0xffffffff), 21.5 ("encode_argmax_f32_rows": one winner per row of a
+ * logits matrix).
+ *
+ *   d_logits   [rows][V] f32, device
+ *   d_out_ids  [rows] u32, device: the winning id, or SEL_INVALID_ID when the
+ *              row holds a nonfinite logit
+ *   d_ws       workspace of sel_workspace_bytes(SEL_OP_ARGMAX, rows, V, 0)
+ */
+sel_status sel_argmax(const float *d_logits, uint32_t rows, uint32_t V,
+                      uint32_t *d_out_ids, void *d_ws, size_t ws_bytes,
+                      cudaStream_t stream);
+
+/*
+ * sel_topk -- per row, the k largest logits with their token ids, sorted by
+ * value descending, equal values by lower id; only these k entries per row
+ * leave the kernel.
+ *
+ * Defined by the llama.cpp pull request 49 ("Change": llama_set_logits_topk
+ * runs top_k on the logits so only the k candidates per row are copied, and
+ * the candidates hold the k largest logits of each row with their tokens and
+ * values), with the lower-id tie rule of the Muser book, 21.3.
+ *
+ *   d_logits    [rows][V] f32, device
+ *   k           1 <= k <= min(V, SEL_MAX_K)
+ *   d_out_vals  [rows][k] f32, device: the values (copies of the logits);
+ *               NaN for an invalid row
+ *   d_out_ids   [rows][k] u32, device: their ids; SEL_INVALID_ID for an
+ *               invalid row
+ *   d_ws        workspace of sel_workspace_bytes(SEL_OP_TOPK, rows, V, k)
+ */
+sel_status sel_topk(const float *d_logits, uint32_t rows, uint32_t V,
+                    uint32_t k, float *d_out_vals, uint32_t *d_out_ids,
+                    void *d_ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Sampling policy.
+ *   temperature  >= 0; 0 means greedy (the argmax, probability 1)
+ *   top_k        1 <= top_k <= SEL_MAX_K (top_k > V means V); 0 (no
+ *                truncation) returns SEL_EUNSUPPORTED unless temperature == 0
+ *   top_p        (0, 1]; 1 disables it
+ *   min_p        [0, 1); 0 disables it
+ *   order        SEL_ORDER_TEMP_FIRST or SEL_ORDER_TEMP_LAST
+ */
+typedef struct sel_sample_params {
+    float temperature;
+    uint32_t top_k;
+    float top_p;
+    float min_p;
+    int32_t order;
+} sel_sample_params;
+
+/*
+ * sel_sample -- per row, one token drawn by inverse CDF from the filtered,
+ * temperature-scaled softmax, with a caller-supplied uniform.
+ *
+ * Steps (TEMP_FIRST): z = x / T; the top_k candidates of z (the sel_topk
+ * definition); P = softmax over the candidates; top-p keeps the shortest
+ * prefix, in (P desc, id asc) order, whose cumulative P reaches top_p (the
+ * crossing token included); min-p keeps candidates with P >= min_p * P_max;
+ * Q = P renormalised over the survivors; the draw is the first survivor, in
+ * the same order, whose cumulative Q exceeds u (the last survivor if
+ * rounding leaves none). TEMP_LAST computes the filters with T = 1 and Q with
+ * the tempered weights.
+ * Sources: Muser book 21.1 (temperature-scaled softmax, then a draw
+ * restricted to top-k / top-p candidates) and 21.7 (top-k truncation before
+ * the top-p cutoff); llama.cpp pull 49, "Change" (a chain with top-k first
+ * needs only the k candidates; top-p and min-p then act on them);
+ * "Speculative-decoding acceptance rules", The rules (the temperature-last
+ * order).
+ *
+ *   d_uniforms  [rows] f32, device: u in [0, 1); anything else (NaN
+ *               included) makes the row invalid
+ *   d_out_ids   [rows] u32, device: the drawn id or SEL_INVALID_ID
+ *   d_out_probs [rows] f32, device: Q of the drawn id (1 for greedy), NaN
+ *               for an invalid row
+ *   d_ws        workspace of sel_workspace_bytes(SEL_OP_SAMPLE, rows, V, top_k)
+ */
+sel_status sel_sample(const float *d_logits, uint32_t rows, uint32_t V,
+                      const sel_sample_params *params,
+                      const float *d_uniforms, uint32_t *d_out_ids,
+                      float *d_out_probs, void *d_ws, size_t ws_bytes,
+                      cudaStream_t stream);
+
+/*
+ * Speculative-acceptance policy.
+ *   temperature  >= 0; p and q are softmax(logits / T); 0 selects the argmax
+ *                rule whatever the mode (greedy draws nothing)
+ *   mode         SPEC_MODE_REJECTION or SPEC_MODE_ARGMAX
+ */
+typedef struct spec_params {
+    float temperature;
+    int32_t mode;
+} spec_params;
+
+/*
+ * spec_accept -- verify K draft tokens per sequence against the target.
+ *
+ * SPEC_MODE_REJECTION ("Speculative-decoding acceptance rules", Modified
+ * rejection sampling, steps 1-3; Muser book 21.9): for j = 0..K-1, accept
+ * draft token t_j iff u_acc[j] * q_j(t_j) <= p_j(t_j); at the first
+ * rejection j* draw one token with u_fin from normalize(max(p_j* - q_j*, 0))
+ * (from p_j* if that residual sums to <= 0) and stop; if all K are accepted
+ * draw a bonus token with u_fin from p_K. Draws walk the vocabulary in
+ * ascending token id.
+ * SPEC_MODE_ARGMAX (same page, Argmax-against-argmax): accept t_j iff it
+ * equals argmax(target_j); emit that argmax at the first mismatch, or the
+ * bonus argmax(target_K) when all match. d_draft and the uniforms may be
+ * NULL.
+ *
+ *   d_target        [S][K+1][V] f32, device
+ *   d_draft         [S][K][V] f32, device (rejection mode)
+ *   d_draft_tokens  [S][K] u32, device
+ *   d_u_acc         [S][K] f32, device: one uniform per draft position
+ *   d_u_fin         [S] f32, device: one uniform for the final draw
+ *   d_accepted      [S] u32, device: accepted count n, or SEL_INVALID_ID
+ *   d_emitted       [S][K+1] u32, device: t_0..t_{n-1}, the drawn token,
+ *                   then SEL_INVALID_ID
+ *   d_ws            workspace of sel_workspace_bytes(SEL_OP_SPEC, S, V, K)
+ * A sequence is invalid (accepted and emitted all SEL_INVALID_ID) when any
+ * of its rows holds a nonfinite logit, a draft token is >= V, or (rejection
+ * mode) a uniform lies outside [0, 1).
+ */
+sel_status spec_accept(const float *d_target, const float *d_draft,
+                       const uint32_t *d_draft_tokens, uint32_t S,
+                       uint32_t K, uint32_t V, const spec_params *params,
+                       const float *d_u_acc, const float *d_u_fin,
+                       uint32_t *d_accepted, uint32_t *d_emitted, void *d_ws,
+                       size_t ws_bytes, cudaStream_t stream);
+
+/* Static description of a status code. */
+const char *sel_status_string(sel_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SEL_H */

@@ -1,0 +1,206 @@
+"""Python binding of the C-ABI library (``include/sel.h``).
+
+Argument marshalling only: torch CUDA tensors supply device pointers and the
+current (or given) CUDA stream; every step of the selection path runs in the
+library's kernels. The functions carry the C names. A missing or unloadable
+library raises immediately -- there is no fallback implementation.
+
+Ids are 32-bit unsigned on the device; torch tensors of dtype int32 or
+uint32 are accepted for them (SEL_INVALID_ID reads as -1 through int32).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+from . import build as _build
+
+SEL_OK, SEL_EINVAL, SEL_EWORKSPACE, SEL_ECUDA, SEL_EUNSUPPORTED = range(5)
+SEL_INVALID_ID = 0xFFFFFFFF
+SEL_MAX_K = 1024
+SEL_OP_ARGMAX, SEL_OP_TOPK, SEL_OP_SAMPLE, SEL_OP_SPEC = range(4)
+SEL_ORDER_TEMP_FIRST, SEL_ORDER_TEMP_LAST = 0, 1
+SPEC_MODE_REJECTION, SPEC_MODE_ARGMAX = 0, 1
+
+EXPORTED = ("sel_workspace_bytes", "sel_workspace_init", "sel_argmax", "sel_topk",
+            "sel_sample", "spec_accept", "sel_status_string")
+
+
+class SelError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+class SampleParams(ctypes.Structure):
+    """struct sel_sample_params"""
+    _fields_ = [("temperature", ctypes.c_float), ("top_k", ctypes.c_uint32),
+                ("top_p", ctypes.c_float), ("min_p", ctypes.c_float),
+                ("order", ctypes.c_int32)]
+
+
+class SpecParams(ctypes.Structure):
+    """struct spec_params"""
+    _fields_ = [("temperature", ctypes.c_float), ("mode", ctypes.c_int32)]
+
+
+_vp = ctypes.c_void_p
+_u32 = ctypes.c_uint32
+_sz = ctypes.c_size_t
+_lib: ctypes.CDLL | None = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libsel.so (once). Raises if it has not been built."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or library_path()
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is not built: run `python -m sampling_row_fp32_gb300.build` "
+                           "(or __graft_entry__.build()) first")
+    lib = ctypes.CDLL(p)
+    lib.sel_workspace_bytes.argtypes = [ctypes.c_int, _u32, _u32, _u32]
+    lib.sel_workspace_bytes.restype = _sz
+    lib.sel_workspace_init.argtypes = [_vp, _sz, _vp]
+    lib.sel_workspace_init.restype = ctypes.c_int
+    lib.sel_argmax.argtypes = [_vp, _u32, _u32, _vp, _vp, _sz, _vp]
+    lib.sel_argmax.restype = ctypes.c_int
+    lib.sel_topk.argtypes = [_vp, _u32, _u32, _u32, _vp, _vp, _vp, _sz, _vp]
+    lib.sel_topk.restype = ctypes.c_int
+    lib.sel_sample.argtypes = [_vp, _u32, _u32, ctypes.POINTER(SampleParams), _vp, _vp, _vp,
+                               _vp, _sz, _vp]
+    lib.sel_sample.restype = ctypes.c_int
+    lib.spec_accept.argtypes = [_vp, _vp, _vp, _u32, _u32, _u32, ctypes.POINTER(SpecParams),
+                                _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+    lib.spec_accept.restype = ctypes.c_int
+    lib.sel_status_string.argtypes = [ctypes.c_int]
+    lib.sel_status_string.restype = ctypes.c_char_p
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().sel_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != SEL_OK:
+        raise SelError(status, what)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("tensors passed to the selection library must be CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the selection library must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check_f32(t, name):
+    if t is not None and not isinstance(t, int) and t.dtype != torch.float32:
+        raise ValueError(f"{name} must be float32")
+
+
+def _check_ids(t, name):
+    if t is not None and not isinstance(t, int) and t.dtype not in (torch.int32, torch.uint32):
+        raise ValueError(f"{name} must be int32 or uint32")
+
+
+def _nbytes(ws) -> int:
+    return 0 if ws is None else ws.numel() * ws.element_size()
+
+
+# ---------------------------------------------------------------------------
+# entry points (C names)
+# ---------------------------------------------------------------------------
+
+def sel_workspace_bytes(op: int, rows: int, V: int, k: int = 0) -> int:
+    return int(load().sel_workspace_bytes(op, rows, V, k))
+
+
+def sel_workspace_init(ws, stream=None) -> None:
+    _check(load().sel_workspace_init(_ptr(ws), _nbytes(ws), _stream(stream)), "sel_workspace_init")
+
+
+def sel_argmax(logits, out_ids, ws=None, stream=None) -> None:
+    _check_f32(logits, "logits")
+    _check_ids(out_ids, "out_ids")
+    rows, V = logits.shape
+    _check(load().sel_argmax(_ptr(logits), rows, V, _ptr(out_ids), _ptr(ws), _nbytes(ws),
+                             _stream(stream)), "sel_argmax")
+
+
+def sel_topk(logits, k: int, out_vals, out_ids, ws=None, stream=None) -> None:
+    _check_f32(logits, "logits")
+    _check_f32(out_vals, "out_vals")
+    _check_ids(out_ids, "out_ids")
+    rows, V = logits.shape
+    _check(load().sel_topk(_ptr(logits), rows, V, k, _ptr(out_vals), _ptr(out_ids), _ptr(ws),
+                           _nbytes(ws), _stream(stream)), "sel_topk")
+
+
+def sel_sample(logits, params: SampleParams, uniforms, out_ids, out_probs, ws=None,
+               stream=None) -> None:
+    _check_f32(logits, "logits")
+    _check_f32(uniforms, "uniforms")
+    _check_f32(out_probs, "out_probs")
+    _check_ids(out_ids, "out_ids")
+    rows, V = logits.shape
+    _check(load().sel_sample(_ptr(logits), rows, V, ctypes.byref(params), _ptr(uniforms),
+                             _ptr(out_ids), _ptr(out_probs), _ptr(ws), _nbytes(ws),
+                             _stream(stream)), "sel_sample")
+
+
+def spec_accept(target, draft, draft_tokens, params: SpecParams, u_acc, u_fin, accepted,
+                emitted, ws=None, stream=None) -> None:
+    """target [S, K+1, V], draft [S, K, V] (or None), draft_tokens [S, K]."""
+    _check_f32(target, "target")
+    _check_f32(draft, "draft")
+    _check_ids(draft_tokens, "draft_tokens")
+    S, K1, V = target.shape
+    _check(load().spec_accept(_ptr(target), _ptr(draft), _ptr(draft_tokens), S, K1 - 1, V,
+                              ctypes.byref(params), _ptr(u_acc), _ptr(u_fin), _ptr(accepted),
+                              _ptr(emitted), _ptr(ws), _nbytes(ws), _stream(stream)),
+           "spec_accept")
+
+
+# ---------------------------------------------------------------------------
+# allocation helpers (torch owns the memory)
+# ---------------------------------------------------------------------------
+
+def workspace(op: int, rows: int, V: int, k: int = 0, device="cuda", stream=None):
+    """A zeroed workspace tensor sized for (op, rows, V, k), or None if the
+    operation needs none. torch's allocator returns 512-byte aligned blocks."""
+    n = sel_workspace_bytes(op, rows, V, k)
+    if n == 0:
+        return None
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    sel_workspace_init(ws, stream)
+    return ws
+
+
+def ids_to_numpy(t):
+    """Device ids (int32/uint32) as a numpy uint32 array."""
+    import numpy as np
+    return t.detach().cpu().contiguous().view(torch.int32).numpy().view(np.uint32)

@@ -1,0 +1,148 @@
+// sel_common.cuh -- device helpers shared by the selection kernels.
+//
+// Row streaming: every logits row is read exactly once with 128-bit
+// non-caching loads (ld.global.nc.L1::no_allocate.v4) when the row is
+// 16-byte aligned, or with scalar loads otherwise; each block owns one
+// contiguous chunk of one row. Cross-block combines use a per-row arrival
+// counter in the caller's workspace: the last block of a row to arrive
+// merges the row's partial results in chunk order and resets the counter.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "sel.h"
+
+namespace sel {
+
+constexpr uint32_t kFull = 0xffffffffu;
+
+// ---------------------------------------------------------------------------
+// loads
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float4 ld_stream4(const float* p) {
+    float4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+        : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float ld_stream1(const float* p) {
+    float v;
+    asm("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+// Load the 4 consecutive elements [e, e+4) of a row, clipped to [.., hi):
+// elements at or past hi are not read and come back as `fill`.
+template <bool kVec>
+__device__ __forceinline__ float4 ld_quad(const float* row, uint32_t e,
+                                          uint32_t hi, float fill) {
+    if (kVec) {
+        // vector path: e and hi are multiples of 4, so a quad is all-in or all-out
+        if (e < hi) return ld_stream4(row + e);
+        return make_float4(fill, fill, fill, fill);
+    } else {
+        float4 v;
+        v.x = e + 0 < hi ? ld_stream1(row + e + 0) : fill;
+        v.y = e + 1 < hi ? ld_stream1(row + e + 1) : fill;
+        v.z = e + 2 < hi ? ld_stream1(row + e + 2) : fill;
+        v.w = e + 3 < hi ? ld_stream1(row + e + 3) : fill;
+        return v;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// order-preserving keys
+// ---------------------------------------------------------------------------
+// key(a) > key(b) iff a > b for all non-NaN floats; -0.0 is first turned into
+// +0.0 (x + 0.0f), so the two zeros get one key and tie by id like the
+// floating-point comparison does. Finite floats map into
+// [kKeyMinFinite, kKeyMaxFinite]; +-Inf and NaN land outside it. Key 0 is
+// below every key a float can take except the all-ones NaN pattern, and
+// marks "no element".
+
+constexpr uint32_t kKeyMinFinite = 0x00800000u;  // key(-FLT_MAX)
+constexpr uint32_t kKeyMaxFinite = 0xFF7FFFFFu;  // key(+FLT_MAX)
+
+__device__ __forceinline__ uint32_t f2key(float f) {
+    uint32_t u = __float_as_uint(f + 0.0f);
+    return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
+}
+
+__device__ __forceinline__ float key2f(uint32_t k) {
+    uint32_t u = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+    return __uint_as_float(u);
+}
+
+__device__ __forceinline__ bool key_nonfinite(uint32_t kmin, uint32_t kmax) {
+    return kmin < kKeyMinFinite || kmax > kKeyMaxFinite;
+}
+
+// Candidate = (key << 32) | ~id: a larger candidate is a larger value, or the
+// same value at a lower id. 0 means "empty".
+__device__ __forceinline__ uint64_t make_cand(uint32_t key, uint32_t id) {
+    return (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(~id);
+}
+__device__ __forceinline__ uint32_t cand_key(uint64_t c) { return static_cast<uint32_t>(c >> 32); }
+__device__ __forceinline__ uint32_t cand_id(uint64_t c) { return ~static_cast<uint32_t>(c); }
+
+// ---------------------------------------------------------------------------
+// warp helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint64_t shfl_xor64(uint64_t v, int m) {
+    uint32_t lo = __shfl_xor_sync(kFull, static_cast<uint32_t>(v), m);
+    uint32_t hi = __shfl_xor_sync(kFull, static_cast<uint32_t>(v >> 32), m);
+    return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+__device__ __forceinline__ uint64_t shfl64(uint64_t v, int src) {
+    uint32_t lo = __shfl_sync(kFull, static_cast<uint32_t>(v), src);
+    uint32_t hi = __shfl_sync(kFull, static_cast<uint32_t>(v >> 32), src);
+    return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+// Bitonic sort of one value per lane across the warp, descending
+// (lane 0 gets the largest).
+template <typename T>
+__device__ __forceinline__ T warp_sort_desc(T v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            T o;
+            if constexpr (sizeof(T) == 8) o = shfl_xor64(v, stride);
+            else o = __shfl_xor_sync(kFull, v, stride);
+            // descending blocks when (lane & size) == 0; lower lane keeps the max
+            bool lower = (lane & stride) == 0;
+            bool desc = (lane & size) == 0;
+            bool take_max = lower == desc;
+            v = take_max ? (o > v ? o : v) : (o < v ? o : v);
+        }
+    }
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+// last-block-of-row arrival
+// ---------------------------------------------------------------------------
+// Called by one thread after the block's partial result is stored. Makes the
+// partial visible device-wide, then takes a ticket; the block that draws the
+// last ticket of the row (chunks - 1) resets the counter for the next call
+// and returns true.
+__device__ __forceinline__ bool arrive_is_last(uint32_t* counter, uint32_t chunks) {
+    __threadfence();
+    uint32_t t = atomicAdd(counter, 1u);
+    bool last = (t == chunks - 1);
+    if (last) {
+        *counter = 0u;
+        __threadfence();
+    }
+    return last;
+}
+
+}  // namespace sel

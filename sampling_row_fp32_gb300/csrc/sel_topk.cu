@@ -1,0 +1,557 @@
+// sel_topk.cu -- exact per-row top-k, and filtered sampling built on it.
+//
+// Top-k computes what the llama.cpp pull request 49 ("Change") ships to the
+// host instead of whole rows: the k largest logits of each row with their
+// token ids, sorted by value descending, equal values by lower id (the tie
+// rule of the Muser book, "Ch 21 -- Sampling, argmax, and grammar", 21.3).
+// Sampling follows the Muser chain (21.1, 21.7: temperature-scaled softmax,
+// top-k before top-p) with min-p, and the observation of the same pull
+// request that a chain with top-k first needs only the k candidates.
+//
+// Design (sm_103a). The page's implementation is a ggml graph op (TOP_K +
+// get_rows) whose kernel is not shown; this one is a single launch that
+// reads each row once:
+//  1. Each block streams one chunk of one row in tiles of 8,192 elements
+//     (8 x 128-bit loads per thread, all in flight) and turns each float into
+//     an order-preserving 32-bit key in registers.
+//  2. A cheap exact filter: each warp sorts its 32 lane maxima (shuffle
+//     bitonic sort) and takes the ceil(k/8)-th; the minimum over the 8 warps
+//     is a key that at least k elements of the tile reach, so nothing below
+//     it can be in the top k. Survivors (typically ~1.5 k per tile) go to a
+//     shared-memory buffer as 64-bit candidates (key << 32 | ~id), which
+//     order exactly like (value desc, id asc).
+//  3. The block selects its chunk's top k from the buffer (rank counting for
+//     small buffers, bitonic sort otherwise) and stores them, sorted, in the
+//     workspace. A buffer overflow (adversarial rows such as all-equal
+//     values) falls back to appending 1,024 elements at a time with a
+//     selection in between, which is exact for any input.
+//  4. The last block of the row to arrive merges the per-chunk lists: a
+//     bound taken from the lists' r-th entries (the m-th largest of the
+//     chunks' r-th entries, m * r >= k) discards almost every entry, and the
+//     survivors are selected exactly. Sampling then runs its softmax,
+//     top-p, min-p and inverse-CDF draw on the k candidates in one warp.
+#include <cfloat>
+
+#include "sel_common.cuh"
+#include "sel_plan.h"
+
+namespace sel {
+namespace {
+
+constexpr int kNT = 256;
+constexpr int kWarps = kNT / 32;
+constexpr int kVPT = 8;
+constexpr uint32_t kTile = 4u * kNT * kVPT;  // 8,192 elements per tile
+constexpr uint32_t kGrain = 4u * kNT;        // chunk sizes are multiples of 1,024
+constexpr uint32_t kMaxChunks = 32;          // merge input <= 32 lists
+constexpr uint32_t kCap = 2048;              // candidate buffer (>= SEL_MAX_K + 4 * kNT)
+constexpr uint32_t kOverhead = 2048;         // per-block cost, in elements
+constexpr uint32_t kRankMax = 512;           // rank counting up to this many candidates
+
+static_assert(kCap >= SEL_MAX_K + 4 * kNT, "a slot of 1,024 must fit after a selection");
+
+struct TopkShared {
+    uint64_t buf[kCap];          // candidate buffer
+    uint64_t sorted[SEL_MAX_K];  // selection output, descending
+    uint64_t warp_cand[kWarps];
+    uint32_t warp_val[kWarps];
+    uint32_t count;              // entries appended to buf
+    uint32_t tau_key;            // key of the k-th candidate once buf held k
+    uint32_t flag;
+    uint32_t total;
+    bool last;
+};
+
+struct SampleArgs {
+    const float* uniforms;  // [rows]
+    float* out_probs;       // [rows]
+    float temperature;
+    float top_p;
+    float min_p;
+    int order;
+};
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    return (1u << (threadIdx.x & 31)) - 1u;
+}
+
+// Append `cand` for every lane with p set; every lane of the warp must call.
+__device__ __forceinline__ void warp_append(TopkShared& s, bool p, uint64_t cand) {
+    const uint32_t m = __ballot_sync(kFull, p);
+    if (m) {
+        const int leader = __ffs(m) - 1;
+        uint32_t base = 0;
+        if ((threadIdx.x & 31) == leader) base = atomicAdd(&s.count, static_cast<uint32_t>(__popc(m)));
+        base = __shfl_sync(kFull, base, leader);
+        if (p) {
+            const uint32_t slot = base + __popc(m & lanemask_lt());
+            if (slot < kCap) s.buf[slot] = cand;
+        }
+    }
+}
+
+// The min(n, k) largest of buf[0..n) (distinct, non-zero) into out[], in
+// descending order. All threads call; buf may be reordered. Ends synced.
+__device__ void block_select_sorted(uint64_t* buf, uint32_t n, uint32_t k, uint64_t* out) {
+    const uint32_t tid = threadIdx.x;
+    if (n <= kRankMax) {
+        // rank = number of larger candidates; candidates are distinct
+        for (uint32_t i = tid; i < n; i += kNT) {
+            const uint64_t c = buf[i];
+            uint32_t rank = 0;
+            for (uint32_t j = 0; j < n; ++j) rank += buf[j] > c ? 1u : 0u;
+            if (rank < k) out[rank] = c;
+        }
+    } else {
+        uint32_t m = 1;
+        while (m < n) m <<= 1;
+        for (uint32_t i = n + tid; i < m; i += kNT) buf[i] = 0;
+        __syncthreads();
+        for (uint32_t size = 2; size <= m; size <<= 1) {
+            for (uint32_t stride = size >> 1; stride > 0; stride >>= 1) {
+                for (uint32_t i = tid; i < m / 2; i += kNT) {
+                    const uint32_t a = 2 * stride * (i / stride) + (i % stride);
+                    const uint32_t b = a + stride;
+                    const bool desc = (a & size) == 0;
+                    const uint64_t x = buf[a], y = buf[b];
+                    if ((x < y) == desc) { buf[a] = y; buf[b] = x; }
+                }
+                __syncthreads();
+            }
+        }
+        const uint32_t kk = n < k ? n : k;
+        for (uint32_t i = tid; i < kk; i += kNT) out[i] = buf[i];
+    }
+    __syncthreads();
+}
+
+// Shrink the buffer to its top min(count, k); record the k-th key.
+__device__ __noinline__ void reduce_buffer(TopkShared& s, uint32_t k) {
+    const uint32_t n = min(s.count, kCap);
+    block_select_sorted(s.buf, n, k, s.sorted);
+    const uint32_t kk = n < k ? n : k;
+    for (uint32_t i = threadIdx.x; i < kk; i += kNT) s.buf[i] = s.sorted[i];
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        s.count = kk;
+        if (kk == k) s.tau_key = cand_key(s.sorted[k - 1]);
+    }
+    __syncthreads();
+}
+
+// Sampling epilogue on the sorted candidates s.sorted[0..n): one warp.
+__device__ void sample_epilogue(const TopkShared& s, uint32_t n, uint32_t row, bool nonfinite,
+                                const SampleArgs& sa, uint32_t* out_ids) {
+    const int lane = threadIdx.x & 31;
+    const float u = sa.uniforms[row];
+    const bool valid = !nonfinite && u >= 0.0f && u < 1.0f;
+    if (!valid) {
+        if (lane == 0) { out_ids[row] = SEL_INVALID_ID; sa.out_probs[row] = __uint_as_float(0x7fc00000u); }
+        return;
+    }
+    if (sa.temperature == 0.0f || n == 1) {  // greedy, or a single candidate
+        if (lane == 0) { out_ids[row] = cand_id(s.sorted[0]); sa.out_probs[row] = 1.0f; }
+        return;
+    }
+    const float x0 = key2f(cand_key(s.sorted[0]));
+    const float T = sa.temperature;
+    const bool temp_last = sa.order == SEL_ORDER_TEMP_LAST;
+    // filter weights wf (T = 1 when temperature comes last) and draw weights wd;
+    // the largest candidate has weight exactly 1.
+    float sum_f = 0.0f;
+    for (uint32_t b = 0; b < n; b += 32) {
+        const uint32_t j = b + lane;
+        float wf = 0.0f;
+        if (j < n) {
+            const float d = key2f(cand_key(s.sorted[j])) - x0;
+            wf = temp_last ? expf(d) : expf(d / T);
+        }
+        float t = wf;
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) t += __shfl_xor_sync(kFull, t, m);
+        sum_f += t;
+    }
+    // top-p: the shortest prefix whose cumulative P reaches top_p
+    uint32_t ns = n;
+    if (sa.top_p < 1.0f) {
+        float cum = 0.0f;
+        ns = 0;
+        for (uint32_t b = 0; b < n && ns == 0; b += 32) {
+            const uint32_t j = b + lane;
+            float p = 0.0f;
+            if (j < n) {
+                const float d = key2f(cand_key(s.sorted[j])) - x0;
+                p = (temp_last ? expf(d) : expf(d / T)) / sum_f;
+            }
+            float incl = p;
+#pragma unroll
+            for (int m = 1; m < 32; m <<= 1) {
+                const float o = __shfl_up_sync(kFull, incl, m);
+                if (lane >= m) incl += o;
+            }
+            incl += cum;
+            const uint32_t hit = __ballot_sync(kFull, j < n && incl >= sa.top_p);
+            if (hit) ns = b + __ffs(hit);
+            cum = __shfl_sync(kFull, incl, 31);
+        }
+        if (ns == 0) ns = n;  // rounding kept the total below top_p
+    }
+    // min-p: keep P_j >= min_p * P_max, i.e. wf_j >= min_p (wf_0 = 1)
+    if (sa.min_p > 0.0f) {
+        uint32_t keep = 1;
+        for (uint32_t b = 0; b < ns; b += 32) {
+            const uint32_t j = b + lane;
+            bool ok = false;
+            if (j < ns && j > 0) {
+                const float d = key2f(cand_key(s.sorted[j])) - x0;
+                const float wf = temp_last ? expf(d) : expf(d / T);
+                ok = wf >= sa.min_p;
+            }
+            const uint32_t m = __ballot_sync(kFull, ok);
+            if (m) keep = b + 32 - __clz(m);  // survivors form a prefix
+        }
+        ns = keep;
+    }
+    // renormalise the draw weights over the survivors and invert the CDF
+    float sum_d = 0.0f;
+    for (uint32_t b = 0; b < ns; b += 32) {
+        const uint32_t j = b + lane;
+        float wd = 0.0f;
+        if (j < ns) wd = expf((key2f(cand_key(s.sorted[j])) - x0) / T);
+        float t = wd;
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) t += __shfl_xor_sync(kFull, t, m);
+        sum_d += t;
+    }
+    uint32_t pick = ns - 1;
+    float pick_w = 0.0f;
+    bool found = false;
+    float cum = 0.0f;
+    for (uint32_t b = 0; b < ns && !found; b += 32) {
+        const uint32_t j = b + lane;
+        float wd = 0.0f;
+        if (j < ns) wd = expf((key2f(cand_key(s.sorted[j])) - x0) / T);
+        float incl = wd;
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+            const float o = __shfl_up_sync(kFull, incl, m);
+            if (lane >= m) incl += o;
+        }
+        incl += cum;
+        const uint32_t hit = __ballot_sync(kFull, j < ns && u < incl / sum_d);
+        if (hit) {
+            const int l = __ffs(hit) - 1;
+            pick = b + l;
+            pick_w = __shfl_sync(kFull, wd, l);
+            found = true;
+        }
+        cum = __shfl_sync(kFull, incl, 31);
+    }
+    if (!found) pick_w = expf((key2f(cand_key(s.sorted[pick])) - x0) / T);
+    if (lane == 0) {
+        out_ids[row] = cand_id(s.sorted[pick]);
+        sa.out_probs[row] = pick_w / sum_d;
+    }
+}
+
+template <bool kVec, bool kSample>
+__global__ void __launch_bounds__(kNT, 3) topk_rows_kernel(
+    const float* __restrict__ logits, uint32_t V, uint32_t k, uint32_t chunks,
+    uint32_t chunk_elems, float* __restrict__ out_vals, uint32_t* __restrict__ out_ids,
+    uint32_t* __restrict__ counters, uint32_t* __restrict__ chunk_flags,
+    uint64_t* __restrict__ lists, uint32_t list_stride, SampleArgs sa) {
+    __shared__ TopkShared s;
+
+    const uint32_t row = blockIdx.x / chunks;
+    const uint32_t chunk = blockIdx.x - row * chunks;
+    const float* x = logits + static_cast<size_t>(row) * V;
+    const uint32_t lo = chunk * chunk_elems;
+    const uint32_t hi = min(V, lo + chunk_elems);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    if (tid == 0) { s.count = 0; s.tau_key = 0; }
+    uint32_t kmin = 0xffffffffu, kmax = 0u;  // finite check over real elements
+
+    for (uint32_t tile_lo = lo; tile_lo < hi; tile_lo += kTile) {
+        uint32_t key[kVPT][4];
+        uint32_t tmax = 0;
+        {
+            float4 q[kVPT];
+#pragma unroll
+            for (int sl = 0; sl < kVPT; ++sl) q[sl] = ld_quad<kVec>(x, tile_lo + 4u * (tid + kNT * sl), hi, 0.0f);
+#pragma unroll
+            for (int sl = 0; sl < kVPT; ++sl) {
+                const uint32_t e = tile_lo + 4u * (tid + kNT * sl);
+                const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const bool in = kVec ? (e < hi) : (e + j < hi);
+                    uint32_t kk = f2key(f[j]);
+                    kmin = in ? min(kmin, kk) : kmin;
+                    kk = in ? kk : 0u;
+                    kmax = max(kmax, kk);
+                    tmax = max(tmax, kk);
+                    key[sl][j] = kk;
+                }
+            }
+        }
+        // tile bound: >= k elements of this tile have key >= tau_tile
+        if (k <= 32u * kWarps) {
+            const uint32_t v = warp_sort_desc(tmax);
+            const uint32_t r = (k + kWarps - 1) / kWarps;
+            const uint32_t wv = __shfl_sync(kFull, v, r - 1);
+            if (lane == 0) s.warp_val[warp] = wv;
+        }
+        __syncthreads();
+        uint32_t tau_tile = 0;
+        if (k <= 32u * kWarps) {
+            tau_tile = s.warp_val[0];
+#pragma unroll
+            for (int w = 1; w < kWarps; ++w) tau_tile = min(tau_tile, s.warp_val[w]);
+        }
+        const uint32_t pre = s.count;
+        // later elements have higher ids: an equal key cannot displace the k-th
+        uint32_t thr = max(tau_tile, s.tau_key + 1u);
+        if (__any_sync(kFull, tmax >= thr)) {
+#pragma unroll
+            for (int sl = 0; sl < kVPT; ++sl) {
+                const uint32_t e = tile_lo + 4u * (tid + kNT * sl);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) warp_append(s, key[sl][j] >= thr, make_cand(key[sl][j], e + j));
+            }
+        }
+        __syncthreads();
+        const uint32_t appended = s.count;
+        if (appended > kCap) {
+            // overflow (adversarial rows): redo this tile slot by slot,
+            // selecting in between; the slot is re-read from memory so the
+            // common path keeps its keys in registers only
+            __syncthreads();
+            if (tid == 0) s.count = pre;
+            __syncthreads();
+#pragma unroll 1
+            for (int sl = 0; sl < kVPT; ++sl) {
+                if (s.count + 4u * kNT > kCap) reduce_buffer(s, k);
+                thr = max(tau_tile, s.tau_key + 1u);
+                const uint32_t e = tile_lo + 4u * (tid + kNT * sl);
+                const float4 q = ld_quad<kVec>(x, e, hi, 0.0f);
+                const float f[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const bool in = kVec ? (e < hi) : (e + j < hi);
+                    const uint32_t kk = in ? f2key(f[j]) : 0u;
+                    warp_append(s, kk >= thr, make_cand(kk, e + j));
+                }
+                __syncthreads();
+            }
+        }
+        if (tile_lo + kTile < hi && s.count > k) reduce_buffer(s, k);
+    }
+
+    // the chunk's top k, sorted
+    const uint32_t n = min(s.count, kCap);
+    block_select_sorted(s.buf, n, k, s.sorted);
+    const uint32_t have = n < k ? n : k;
+    const uint32_t nf_local = key_nonfinite(__reduce_min_sync(kFull, kmin), __reduce_max_sync(kFull, kmax)) ? 1u : 0u;
+    if (lane == 0) s.warp_val[warp] = nf_local;
+    __syncthreads();
+    uint32_t nf = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) nf |= s.warp_val[w];
+
+    if (chunks == 1) {
+        if constexpr (kSample) {
+            if (warp == 0) sample_epilogue(s, have, row, nf != 0, sa, out_ids);
+        } else {
+            for (uint32_t j = tid; j < k; j += kNT) {
+                const bool ok = !nf && j < have;
+                out_vals[static_cast<size_t>(row) * k + j] = ok ? key2f(cand_key(s.sorted[j])) : __uint_as_float(0x7fc00000u);
+                out_ids[static_cast<size_t>(row) * k + j] = ok ? cand_id(s.sorted[j]) : SEL_INVALID_ID;
+            }
+        }
+        return;
+    }
+
+    // publish the sorted list (padded with empty candidates) and arrive
+    uint64_t* my_list = lists + (static_cast<size_t>(row) * list_stride + chunk) * k;
+    for (uint32_t j = tid; j < k; j += kNT) my_list[j] = j < have ? s.sorted[j] : 0ull;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        chunk_flags[static_cast<size_t>(row) * list_stride + chunk] = nf;
+        s.last = arrive_is_last(&counters[row], chunks);
+    }
+    __syncthreads();
+    if (!s.last) return;
+
+    // ---- last block of the row: merge the chunk lists ----
+    const uint64_t* L = lists + static_cast<size_t>(row) * list_stride * k;
+    nf = 0;
+    for (uint32_t c = lane; c < chunks; c += 32) nf |= __ldcg(chunk_flags + static_cast<size_t>(row) * list_stride + c);
+    nf = __reduce_or_sync(kFull, nf);
+
+    // bound: for m lists and r = ceil(k / m), the m-th largest of the lists'
+    // r-th entries is reached by at least m * r >= k entries
+    {
+        const uint32_t m = max(1u, chunks >> warp);
+        const uint32_t r = (k + m - 1) / m;
+        uint64_t v = 0;
+        if (static_cast<uint32_t>(lane) < chunks) v = __ldcg(reinterpret_cast<const unsigned long long*>(L + static_cast<size_t>(lane) * k + (r - 1)));
+        v = warp_sort_desc(v);
+        const uint64_t b = shfl64(v, static_cast<int>(m - 1));
+        if (lane == 0) s.warp_cand[warp] = b;
+    }
+    if (tid == 0) { s.count = 0; s.tau_key = 0; s.total = 0; }
+    __syncthreads();
+    uint64_t tau_m = s.warp_cand[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) tau_m = s.warp_cand[w] > tau_m ? s.warp_cand[w] : tau_m;
+
+    // count the survivors first; append in one pass if they fit
+    const uint32_t total_entries = chunks * k;
+    uint32_t mine = 0;
+    for (uint32_t i = tid; i < total_entries; i += kNT) {
+        const uint64_t v = __ldcg(reinterpret_cast<const unsigned long long*>(L + i));
+        mine += (v != 0 && v >= tau_m) ? 1u : 0u;
+    }
+    mine = __reduce_add_sync(kFull, mine);
+    if (lane == 0) atomicAdd(&s.total, mine);
+    __syncthreads();
+    if (s.total <= kCap) {
+        for (uint32_t i0 = 0; i0 < total_entries; i0 += kNT) {
+            const uint32_t i = i0 + tid;
+            uint64_t v = 0;
+            if (i < total_entries) v = __ldcg(reinterpret_cast<const unsigned long long*>(L + i));
+            warp_append(s, v != 0 && v >= tau_m, v);
+        }
+        __syncthreads();
+        block_select_sorted(s.buf, min(s.count, kCap), k, s.sorted);
+    } else {
+        // list by list, keeping the buffer at its top k in between
+        uint64_t floor_c = tau_m;
+#pragma unroll 1
+        for (uint32_t c = 0; c < chunks; ++c) {
+            for (uint32_t j0 = 0; j0 < k; j0 += kNT) {
+                const uint32_t j = j0 + tid;
+                uint64_t v = 0;
+                if (j < k) v = __ldcg(reinterpret_cast<const unsigned long long*>(L + static_cast<size_t>(c) * k + j));
+                warp_append(s, v != 0 && v >= floor_c, v);
+            }
+            __syncthreads();
+            if (s.count > k) {
+                block_select_sorted(s.buf, s.count, k, s.sorted);
+                for (uint32_t i = tid; i < k; i += kNT) s.buf[i] = s.sorted[i];
+                __syncthreads();
+                floor_c = s.sorted[k - 1] > floor_c ? s.sorted[k - 1] : floor_c;
+                if (tid == 0) s.count = k;
+                __syncthreads();
+            }
+        }
+        block_select_sorted(s.buf, s.count, k, s.sorted);
+    }
+
+    if constexpr (kSample) {
+        if (warp == 0) sample_epilogue(s, k, row, nf != 0, sa, out_ids);
+    } else {
+        for (uint32_t j = tid; j < k; j += kNT) {
+            const bool ok = !nf;
+            out_vals[static_cast<size_t>(row) * k + j] = ok ? key2f(cand_key(s.sorted[j])) : __uint_as_float(0x7fc00000u);
+            out_ids[static_cast<size_t>(row) * k + j] = ok ? cand_id(s.sorted[j]) : SEL_INVALID_ID;
+        }
+    }
+}
+
+struct TopkLayout {
+    size_t counters, flags, lists, total;
+    uint32_t cmax;
+};
+
+TopkLayout topk_layout(uint32_t rows, uint32_t V, uint32_t k) {
+    TopkLayout l{};
+    l.cmax = max_chunks_bound(V, kGrain, kMaxChunks);
+    if (l.cmax <= 1) return l;  // one block per row: no workspace
+    l.counters = 0;
+    l.flags = ws_counters_bytes(rows);
+    l.lists = l.flags + align_up(static_cast<size_t>(rows) * l.cmax * 4u, 256);
+    l.total = l.lists + static_cast<size_t>(rows) * l.cmax * k * 8u;
+    return l;
+}
+
+template <bool kSample>
+sel_status launch_topk(const float* d_logits, uint32_t rows, uint32_t V, uint32_t k,
+                       float* d_out_vals, uint32_t* d_out_ids, void* d_ws, size_t ws_bytes,
+                       const SampleArgs& sa, cudaStream_t stream) {
+    const TopkLayout l = topk_layout(rows, V, k);
+    if (l.total > 0) {
+        if (!d_ws) return SEL_EINVAL;
+        if (reinterpret_cast<uintptr_t>(d_ws) % SEL_WS_ALIGN) return SEL_EINVAL;
+        if (ws_bytes < l.total) return SEL_EWORKSPACE;
+    }
+    const int sms = device_sms();
+    if (sms <= 0) return SEL_ECUDA;
+    static const int res = resident_blocks(topk_rows_kernel<true, kSample>, kNT);
+    const RowPlan plan = plan_rows(rows, V, sms, kGrain, kMaxChunks, kOverhead, res, kTile);
+    char* ws = static_cast<char*>(d_ws);
+    uint32_t* counters = l.total ? reinterpret_cast<uint32_t*>(ws + l.counters) : nullptr;
+    uint32_t* flags = l.total ? reinterpret_cast<uint32_t*>(ws + l.flags) : nullptr;
+    uint64_t* lists = l.total ? reinterpret_cast<uint64_t*>(ws + l.lists) : nullptr;
+    const bool vec = (reinterpret_cast<uintptr_t>(d_logits) % 16 == 0) && (V % 4 == 0);
+    const dim3 grid(rows * plan.chunks);
+    if (vec)
+        topk_rows_kernel<true, kSample><<<grid, kNT, 0, stream>>>(d_logits, V, k, plan.chunks, plan.chunk_elems,
+                                                                  d_out_vals, d_out_ids, counters, flags, lists,
+                                                                  l.cmax, sa);
+    else
+        topk_rows_kernel<false, kSample><<<grid, kNT, 0, stream>>>(d_logits, V, k, plan.chunks, plan.chunk_elems,
+                                                                   d_out_vals, d_out_ids, counters, flags, lists,
+                                                                   l.cmax, sa);
+    return cudaGetLastError() == cudaSuccess ? SEL_OK : SEL_ECUDA;
+}
+
+}  // namespace
+
+size_t topk_ws_bytes(uint32_t rows, uint32_t V, uint32_t k) { return topk_layout(rows, V, k).total; }
+
+}  // namespace sel
+
+using namespace sel;
+
+extern "C" sel_status sel_topk(const float* d_logits, uint32_t rows, uint32_t V, uint32_t k,
+                               float* d_out_vals, uint32_t* d_out_ids, void* d_ws, size_t ws_bytes,
+                               cudaStream_t stream) {
+    if (V == 0 || V > SEL_MAX_V || k == 0 || k > V) return SEL_EINVAL;
+    if (k > SEL_MAX_K) return SEL_EUNSUPPORTED;
+    if (rows == 0) return SEL_OK;
+    if (!d_logits || !d_out_vals || !d_out_ids) return SEL_EINVAL;
+    if (reinterpret_cast<uintptr_t>(d_logits) % 4 || reinterpret_cast<uintptr_t>(d_out_vals) % 4 ||
+        reinterpret_cast<uintptr_t>(d_out_ids) % 4)
+        return SEL_EINVAL;
+    if (rows > 0x7fffffffu / kMaxChunks) return SEL_EUNSUPPORTED;
+    SampleArgs sa{};
+    return launch_topk<false>(d_logits, rows, V, k, d_out_vals, d_out_ids, d_ws, ws_bytes, sa, stream);
+}
+
+extern "C" sel_status sel_sample(const float* d_logits, uint32_t rows, uint32_t V,
+                                 const sel_sample_params* p, const float* d_uniforms,
+                                 uint32_t* d_out_ids, float* d_out_probs, void* d_ws, size_t ws_bytes,
+                                 cudaStream_t stream) {
+    if (!p || V == 0 || V > SEL_MAX_V) return SEL_EINVAL;
+    const float T = p->temperature;
+    if (!(T >= 0.0f) || !(T < INFINITY)) return SEL_EINVAL;  // rejects NaN too
+    if (!(p->top_p > 0.0f && p->top_p <= 1.0f)) return SEL_EINVAL;
+    if (!(p->min_p >= 0.0f && p->min_p < 1.0f)) return SEL_EINVAL;
+    if (p->order != SEL_ORDER_TEMP_FIRST && p->order != SEL_ORDER_TEMP_LAST) return SEL_EINVAL;
+    uint32_t k = p->top_k;
+    if (T == 0.0f) k = 1;  // greedy: the top-1 candidate is the argmax
+    if (k == 0) return SEL_EUNSUPPORTED;
+    if (k > V) k = V;
+    if (k > SEL_MAX_K) return SEL_EUNSUPPORTED;
+    if (rows == 0) return SEL_OK;
+    if (!d_logits || !d_uniforms || !d_out_ids || !d_out_probs) return SEL_EINVAL;
+    if (reinterpret_cast<uintptr_t>(d_logits) % 4 || reinterpret_cast<uintptr_t>(d_uniforms) % 4 ||
+        reinterpret_cast<uintptr_t>(d_out_ids) % 4 || reinterpret_cast<uintptr_t>(d_out_probs) % 4)
+        return SEL_EINVAL;
+    if (rows > 0x7fffffffu / kMaxChunks) return SEL_EUNSUPPORTED;
+    SampleArgs sa{d_uniforms, d_out_probs, T, p->top_p, p->min_p, p->order};
+    return launch_topk<true>(d_logits, rows, V, k, nullptr, d_out_ids, d_ws, ws_bytes, sa, stream);
+}

@@ -1,0 +1,99 @@
+"""The C-ABI library builds, loads and exports what include/sel.h declares;
+host-side argument checks answer without touching a GPU (no GPU needed)."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sel.h")
+
+pytestmark = pytest.mark.skipif(shutil.which("nvcc") is None and
+                                not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                                reason="nvcc is needed to build the library")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:sel_status|size_t|const char\s*\*)\s*(\w+)\s*\(",
+                                 text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sampling_row_fp32_gb300 import binding, build
+    build.build()
+    return binding.load()
+
+
+def test_header_declares_the_four_operations():
+    names = declared_functions()
+    for n in ("sel_argmax", "sel_topk", "sel_sample", "spec_accept",
+              "sel_workspace_bytes", "sel_workspace_init", "sel_status_string"):
+        assert n in names, names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(lib._name)
+    for name in declared_functions():
+        assert hasattr(raw, name), name
+    from sampling_row_fp32_gb300 import binding
+    assert sorted(binding.EXPORTED) == declared_functions()
+
+
+def test_status_strings(lib):
+    from sampling_row_fp32_gb300 import binding as B
+    for s in range(5):
+        assert B.status_string(s).startswith("SEL_")
+
+
+def test_workspace_sizes_are_host_only_and_monotone(lib):
+    from sampling_row_fp32_gb300 import binding as B
+    a = B.sel_workspace_bytes(B.SEL_OP_ARGMAX, 49, 248_320)
+    assert a > 0 and a % 8 == 0
+    assert B.sel_workspace_bytes(B.SEL_OP_ARGMAX, 98, 248_320) > a
+    assert B.sel_workspace_bytes(B.SEL_OP_ARGMAX, 4, 1000) == 0      # one block per row
+    t20 = B.sel_workspace_bytes(B.SEL_OP_TOPK, 49, 248_320, 20)
+    t84 = B.sel_workspace_bytes(B.SEL_OP_TOPK, 49, 248_320, 84)
+    assert 0 < t20 < t84
+    assert B.sel_workspace_bytes(B.SEL_OP_TOPK, 49, 248_320, 0) == 0  # invalid k
+    assert B.sel_workspace_bytes(B.SEL_OP_TOPK, 1, 10, 11) == 0       # k > V
+    assert B.sel_workspace_bytes(B.SEL_OP_SAMPLE, 64, 202_048, 40) == \
+        B.sel_workspace_bytes(B.SEL_OP_TOPK, 64, 202_048, 40)
+    assert B.sel_workspace_bytes(7, 1, 10, 1) == 0                    # unknown op
+
+
+def test_host_validation_needs_no_gpu(lib):
+    """Arguments the host can reject are rejected before any CUDA call."""
+    from sampling_row_fp32_gb300 import binding as B
+    vp = ctypes.c_void_p
+    fake = vp(0x10000)   # never dereferenced: every call below fails validation first
+    assert lib.sel_argmax(fake, 1, 0, fake, None, 0, None) == B.SEL_EINVAL          # V = 0
+    assert lib.sel_argmax(fake, 1, 0x80000000, fake, None, 0, None) == B.SEL_EINVAL  # V >= 2^31
+    assert lib.sel_argmax(None, 1, 10, fake, None, 0, None) == B.SEL_EINVAL          # null logits
+    assert lib.sel_argmax(vp(0x10002), 1, 10, fake, None, 0, None) == B.SEL_EINVAL   # misaligned
+    assert lib.sel_argmax(None, 0, 10, None, None, 0, None) == B.SEL_OK              # rows = 0
+    assert lib.sel_argmax(fake, 3, 300_000, fake, None, 0, None) == B.SEL_EINVAL     # ws missing
+    assert lib.sel_argmax(fake, 3, 300_000, fake, fake, 16, None) == B.SEL_EWORKSPACE
+    assert lib.sel_argmax(fake, 3, 300_000, fake, vp(0x10010), 1 << 30, None) == B.SEL_EINVAL
+    assert lib.sel_topk(fake, 1, 10, 11, fake, fake, None, 0, None) == B.SEL_EINVAL  # k > V
+    assert lib.sel_topk(fake, 1, 10, 0, fake, fake, None, 0, None) == B.SEL_EINVAL   # k = 0
+    assert lib.sel_topk(fake, 1, 5000, 1025, fake, fake, None, 0, None) == B.SEL_EUNSUPPORTED
+
+    def sample(T, k, p, m, order=0):
+        prm = B.SampleParams(T, k, p, m, order)
+        return lib.sel_sample(fake, 1, 10, ctypes.byref(prm), fake, fake, fake, None, 0, None)
+    assert sample(float("nan"), 5, 1.0, 0.0) == B.SEL_EINVAL
+    assert sample(-1.0, 5, 1.0, 0.0) == B.SEL_EINVAL
+    assert sample(1.0, 5, 0.0, 0.0) == B.SEL_EINVAL
+    assert sample(1.0, 5, 1.5, 0.0) == B.SEL_EINVAL
+    assert sample(1.0, 5, 1.0, 1.0) == B.SEL_EINVAL
+    assert sample(1.0, 5, 1.0, -0.1) == B.SEL_EINVAL
+    assert sample(1.0, 5, 1.0, 0.0, order=2) == B.SEL_EINVAL
+    assert sample(1.0, 0, 1.0, 0.0) == B.SEL_EUNSUPPORTED    # full-row sampling
+    prm = B.SampleParams(1.0, 5, 1.0, 0.0, 0)
+    assert lib.sel_sample(fake, 1, 10, None, fake, fake, fake, None, 0, None) == B.SEL_EINVAL
+    assert lib.sel_sample(fake, 0, 10, ctypes.byref(prm), None, None, None, None, 0, None) == B.SEL_OK
