@@ -3,208 +3,204 @@
 // Computes what "Ch 21 -- Sampling, argmax, and grammar" (Muser book)
 // defines in 21.3-21.5: per row, the (value, index) of the maximum under a
 // strict '>' comparison (a tie keeps the lower index), with the greedy
-// serving variant's fail-closed latch (any NaN/Inf -> 0xffffffff).
+// serving variant's fail-closed latch (any NaN/Inf -> 0xffffffff), over
+// every row of a logits matrix.
 //
 // Design (sm_103a). The page's Metal version is a two-dispatch tree: one
 // 1,024-thread threadgroup per 1,024-element chunk writes a partial, an
 // explicit barrier orders the hazard, and a second dispatch reduces the
-// partials. Here one launch does both: each block streams one chunk of one
-// row with 128-bit loads (8 in flight per thread), keeps a running
-// (value, index) per thread, merges across the warp with shuffles and across
-// warps through shared memory, stores its partial, and the last block of the
-// row to arrive merges the row's partials and writes the id. The chunk size
-// is planned so that every SM streams the same number of bytes.
-#include <cfloat>
-
-#include "sel_common.cuh"
+// partials. Here one launch does both. Persistent blocks stream contiguous
+// runs of 32 KB row chunks through a TMA bulk-copy ring (sel_stream.cuh) and
+// keep a running (value, index) per thread across the chunks of a row; when
+// a block leaves a row it merges across the warp with shuffles and across
+// warps through shared memory and publishes one partial for its segment of
+// the row; the block that publishes a row's last segment merges that row's
+// partials with one warp and writes the id. (value desc, id asc) is a total
+// order, so the merge order cannot change the result.
 #include "sel_plan.h"
+#include "sel_stream.cuh"
 
 namespace sel {
 namespace {
 
-constexpr int kNT = 256;      // threads per block
-constexpr int kVPT = 8;       // float4 loads in flight per thread
-constexpr uint32_t kGrain = 4u * kNT;         // 1,024 elements
-constexpr uint32_t kMaxChunks = 4096;
-constexpr uint32_t kOverhead = 1024;          // per-block cost, in elements
-constexpr uint32_t kNoIdx = 0x7fffffffu;      // "no element" (loses every tie)
+constexpr int kNT = 256;                        // threads per block
+constexpr int kVPT = 8;                         // float4 per thread per unit
+constexpr int kStages = 4;                      // units in flight per block
+constexpr uint32_t kUnitMax = 4u * kNT * kVPT;  // 8,192 elements (32 KB)
+constexpr uint32_t kUnitMin = 1024u;
+constexpr uint32_t kNoIdx = 0x7fffffffu;        // "no element": loses every tie
 constexpr uint32_t kNonfiniteBit = 0x80000000u;
 
 struct alignas(8) ArgPair {
     float v;
-    uint32_t i;  // id, bit 31 = nonfinite seen
+    uint32_t i;  // id; bit 31 = a nonfinite logit was seen
 };
 
-// (v, i) beats (w, j): larger value, or the same value at a lower id.
 __device__ __forceinline__ bool beats(float v, uint32_t i, float w, uint32_t j) {
     return v > w || (v == w && i < j);
 }
 
-template <bool kVec>
-__global__ void __launch_bounds__(kNT) argmax_rows_kernel(
-    const float* __restrict__ logits, uint32_t V, uint32_t chunks,
-    uint32_t chunk_elems, uint32_t* __restrict__ out_ids,
-    uint32_t* __restrict__ counters, ArgPair* __restrict__ partials,
-    uint32_t partial_stride) {
+__device__ __forceinline__ void warp_argmax(float& v, uint32_t& i, uint32_t& nf) {
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) {
+        const float ov = __shfl_xor_sync(kFull, v, m);
+        const uint32_t oi = __shfl_xor_sync(kFull, i, m);
+        if (beats(ov, oi, v, i)) { v = ov; i = oi; }
+    }
+    nf = __reduce_or_sync(kFull, nf);
+}
+
+struct ArgmaxArgs {
+    const float* logits;
+    uint32_t* out_ids;
+    uint32_t* counters;  // [rows]
+    ArgPair* partials;   // [rows][stride]
+    uint32_t stride;
+    uint32_t* err;
+    StreamCfg cfg;
+};
+
+template <bool kTma>
+__global__ void __launch_bounds__(kNT) argmax_kernel(ArgmaxArgs a) {
+    extern __shared__ float4 stages[];
+    __shared__ uint64_t full[kStages];
     __shared__ float s_v[kNT / 32];
     __shared__ uint32_t s_i[kNT / 32];
     __shared__ uint32_t s_nf[kNT / 32];
-    __shared__ bool s_last;
 
-    const uint32_t row = blockIdx.x / chunks;
-    const uint32_t chunk = blockIdx.x - row * chunks;
-    const float* x = logits + static_cast<size_t>(row) * V;
-    const uint32_t lo = chunk * chunk_elems;
-    const uint32_t hi = min(V, lo + chunk_elems);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t V = a.cfg.V;
+    auto row_ptr = [&](uint32_t r) { return a.logits + static_cast<size_t>(r) * V; };
 
-    // -inf loses to every finite logit; a row holding -inf fails closed anyway
-    float best = -INFINITY;
+    // running (value, id) and finite check of this thread over the segment
+    float best = -INFINITY;  // loses to every finite logit (a row with -inf fails closed)
     uint32_t bidx = kNoIdx;
-    uint32_t absmax = 0;  // max |bits|: >= 0x7f800000 means NaN/Inf seen
+    uint32_t absmax = 0;     // max |bits| over real elements: >= Inf bits means NaN/Inf
 
-    for (uint32_t base = lo + 4u * tid; base < hi; base += 4u * kNT * kVPT) {
-        float4 q[kVPT];
-#pragma unroll
-        for (int s = 0; s < kVPT; ++s) q[s] = ld_quad<kVec>(x, base + 4u * kNT * s, hi, -INFINITY);
+    auto accum = [&](const Unit& t, float4 (&q)[kVPT]) {
 #pragma unroll
         for (int s = 0; s < kVPT; ++s) {
-            const uint32_t e = base + 4u * kNT * s;
-            const bool quad_in = e < hi;
+            const uint32_t e = t.lo + 4u * (tid + kNT * s);
             const float f[4] = {q[s].x, q[s].y, q[s].z, q[s].w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const bool in = kVec ? quad_in : (e + j < hi);
-                if (in) {
+                if (e + j < t.hi) {
                     absmax = max(absmax, __float_as_uint(f[j]) & 0x7fffffffu);
-                    // ids rise along the thread's walk, so '>' keeps the lowest
-                    if (f[j] > best) {
+                    if (f[j] > best) {  // ids rise along the walk: '>' keeps the lowest
                         best = f[j];
                         bidx = e + j;
                     }
                 }
             }
         }
-    }
-    uint32_t nf = absmax >= 0x7f800000u ? kNonfiniteBit : 0u;
-    if (nf) { best = -INFINITY; bidx = kNoIdx; }  // the row fails closed
+    };
 
-    // warp merge
-#pragma unroll
-    for (int m = 16; m > 0; m >>= 1) {
-        float ov = __shfl_xor_sync(kFull, best, m);
-        uint32_t oi = __shfl_xor_sync(kFull, bidx, m);
-        if (beats(ov, oi, best, bidx)) { best = ov; bidx = oi; }
-    }
-    nf = __reduce_or_sync(kFull, nf);
-    if (lane == 0) { s_v[warp] = best; s_i[warp] = bidx; s_nf[warp] = nf; }
-    __syncthreads();
-
-    if (warp == 0) {
-        best = lane < kNT / 32 ? s_v[lane] : -INFINITY;
-        bidx = lane < kNT / 32 ? s_i[lane] : kNoIdx;
-        nf = lane < kNT / 32 ? s_nf[lane] : 0u;
-#pragma unroll
-        for (int m = 16; m > 0; m >>= 1) {
-            float ov = __shfl_xor_sync(kFull, best, m);
-            uint32_t oi = __shfl_xor_sync(kFull, bidx, m);
-            if (beats(ov, oi, best, bidx)) { best = ov; bidx = oi; }
-        }
-        nf = __reduce_or_sync(kFull, nf);
-        if (lane == 0) {
-            if (chunks == 1) {
-                out_ids[row] = nf ? SEL_INVALID_ID : bidx;
-                s_last = false;
-            } else {
-                partials[static_cast<size_t>(row) * partial_stride + chunk] = ArgPair{best, bidx | nf};
-                s_last = arrive_is_last(&counters[row], chunks);
+    auto flush = [&](const Segment& g) {
+        uint32_t nf = absmax >= 0x7f800000u ? kNonfiniteBit : 0u;
+        float v = nf ? -INFINITY : best;
+        uint32_t i = nf ? kNoIdx : bidx;
+        best = -INFINITY;
+        bidx = kNoIdx;
+        absmax = 0;
+        warp_argmax(v, i, nf);
+        if (lane == 0) { s_v[warp] = v; s_i[warp] = i; s_nf[warp] = nf; }
+        __syncthreads();
+        if (warp == 0) {
+            v = lane < kNT / 32 ? s_v[lane] : -INFINITY;
+            i = lane < kNT / 32 ? s_i[lane] : kNoIdx;
+            nf = lane < kNT / 32 ? s_nf[lane] : 0u;
+            warp_argmax(v, i, nf);
+            bool last = true;
+            if (g.count > 1) {
+                uint32_t flag = 0;
+                if (lane == 0) {
+                    a.partials[static_cast<size_t>(g.row) * a.stride + g.index] = ArgPair{v, i | nf};
+                    flag = segment_arrive(&a.counters[g.row], g.count) ? 1u : 0u;
+                }
+                last = __shfl_sync(kFull, flag, 0) != 0;
+                if (last) {
+                    // merge the row's segments (any order gives the same answer)
+                    __threadfence();
+                    v = -INFINITY;
+                    i = kNoIdx;
+                    nf = 0;
+                    const ArgPair* part = a.partials + static_cast<size_t>(g.row) * a.stride;
+                    for (uint32_t c = lane; c < g.count; c += 32) {
+                        const uint64_t raw = ld_gpu_u64(part + c);
+                        const float pv = __uint_as_float(static_cast<uint32_t>(raw));
+                        const uint32_t hi = static_cast<uint32_t>(raw >> 32);
+                        const uint32_t pi = hi & ~kNonfiniteBit;
+                        nf |= hi & kNonfiniteBit;
+                        if (beats(pv, pi, v, i)) { v = pv; i = pi; }
+                    }
+                    warp_argmax(v, i, nf);
+                }
             }
+            if (last && lane == 0) a.out_ids[g.row] = nf ? SEL_INVALID_ID : i;
         }
-    }
-    __syncthreads();
-    if (!s_last) return;
+        __syncthreads();
+    };
 
-    // last block of the row: merge the partials (max is order-free: the
-    // (value desc, id asc) order is total, so the result is deterministic)
-    best = -INFINITY;
-    bidx = kNoIdx;
-    nf = 0u;
-    const ArgPair* part = partials + static_cast<size_t>(row) * partial_stride;
-    for (uint32_t c = tid; c < chunks; c += kNT) {
-        uint2 raw = __ldcg(reinterpret_cast<const uint2*>(part + c));
-        float v = __uint_as_float(raw.x);
-        uint32_t i = raw.y & ~kNonfiniteBit;
-        nf |= raw.y & kNonfiniteBit;
-        if (beats(v, i, best, bidx)) { best = v; bidx = i; }
-    }
-#pragma unroll
-    for (int m = 16; m > 0; m >>= 1) {
-        float ov = __shfl_xor_sync(kFull, best, m);
-        uint32_t oi = __shfl_xor_sync(kFull, bidx, m);
-        if (beats(ov, oi, best, bidx)) { best = ov; bidx = oi; }
-    }
-    nf = __reduce_or_sync(kFull, nf);
-    __syncthreads();
-    if (lane == 0) { s_v[warp] = best; s_i[warp] = bidx; s_nf[warp] = nf; }
-    __syncthreads();
-    if (warp == 0) {
-        best = lane < kNT / 32 ? s_v[lane] : -INFINITY;
-        bidx = lane < kNT / 32 ? s_i[lane] : kNoIdx;
-        nf = lane < kNT / 32 ? s_nf[lane] : 0u;
-#pragma unroll
-        for (int m = 16; m > 0; m >>= 1) {
-            float ov = __shfl_xor_sync(kFull, best, m);
-            uint32_t oi = __shfl_xor_sync(kFull, bidx, m);
-            if (beats(ov, oi, best, bidx)) { best = ov; bidx = oi; }
-        }
-        nf = __reduce_or_sync(kFull, nf);
-        if (lane == 0) out_ids[row] = nf ? SEL_INVALID_ID : bidx;
-    }
+    stream_segments<kTma, kNT, kVPT, kStages>(a.cfg, row_ptr, accum, flush, stages, full, a.err);
+}
+
+struct ArgmaxLayout {
+    size_t counters, partials, total;
+    uint32_t stride;
+};
+
+ArgmaxLayout argmax_layout(uint32_t rows, uint32_t V) {
+    ArgmaxLayout l{};
+    l.stride = ceil_div(V, kUnitMin);  // most chunks any plan uses
+    l.counters = kWsHeaderBytes;
+    l.partials = l.counters + ws_counters_bytes(rows);
+    l.total = l.partials + static_cast<size_t>(rows) * l.stride * sizeof(ArgPair);
+    return l;
 }
 
 }  // namespace
 
-size_t argmax_ws_bytes(uint32_t rows, uint32_t V) {
-    uint32_t cmax = max_chunks_bound(V, kGrain, kMaxChunks);
-    if (cmax <= 1) return 0;
-    return ws_counters_bytes(rows) + static_cast<size_t>(rows) * cmax * sizeof(ArgPair);
-}
+size_t argmax_ws_bytes(uint32_t rows, uint32_t V) { return argmax_layout(rows, V).total; }
 
 }  // namespace sel
 
 using namespace sel;
 
-extern "C" sel_status sel_argmax(const float* d_logits, uint32_t rows, uint32_t V,
-                                 uint32_t* d_out_ids, void* d_ws, size_t ws_bytes,
-                                 cudaStream_t stream) {
+extern "C" sel_status sel_argmax(const float* d_logits, uint32_t rows, uint32_t V, uint32_t* d_out_ids, void* d_ws,
+                                 size_t ws_bytes, cudaStream_t stream) {
     if (V == 0 || V > SEL_MAX_V) return SEL_EINVAL;
     if (rows == 0) return SEL_OK;
     if (!d_logits || !d_out_ids) return SEL_EINVAL;
-    if (reinterpret_cast<uintptr_t>(d_logits) % 4 || reinterpret_cast<uintptr_t>(d_out_ids) % 4)
-        return SEL_EINVAL;
+    if (reinterpret_cast<uintptr_t>(d_logits) % 4 || reinterpret_cast<uintptr_t>(d_out_ids) % 4) return SEL_EINVAL;
     if (rows > 0x7fffffffu) return SEL_EUNSUPPORTED;
-    const size_t need = argmax_ws_bytes(rows, V);
-    if (need > 0) {
-        if (!d_ws) return SEL_EINVAL;
-        if (reinterpret_cast<uintptr_t>(d_ws) % SEL_WS_ALIGN) return SEL_EINVAL;
-        if (ws_bytes < need) return SEL_EWORKSPACE;
-    }
+    const ArgmaxLayout l = argmax_layout(rows, V);
+    if (!d_ws) return SEL_EINVAL;
+    if (reinterpret_cast<uintptr_t>(d_ws) % SEL_WS_ALIGN) return SEL_EINVAL;
+    if (ws_bytes < l.total) return SEL_EWORKSPACE;
     const int sms = device_sms();
     if (sms <= 0) return SEL_ECUDA;
-    static const int res_vec = resident_blocks(argmax_rows_kernel<true>, kNT);
-    static const int res_sca = resident_blocks(argmax_rows_kernel<false>, kNT);
-    const bool vec = (reinterpret_cast<uintptr_t>(d_logits) % 16 == 0) && (V % 4 == 0);
-    const RowPlan plan = plan_rows(rows, V, sms, kGrain, kMaxChunks, kOverhead, vec ? res_vec : res_sca);
-    const uint32_t cmax = max_chunks_bound(V, kGrain, kMaxChunks);
-    uint32_t* counters = static_cast<uint32_t*>(d_ws);
-    ArgPair* partials = need ? reinterpret_cast<ArgPair*>(static_cast<char*>(d_ws) + ws_counters_bytes(rows))
-                             : nullptr;
-    const dim3 grid(rows * plan.chunks);
-    if (vec)
-        argmax_rows_kernel<true><<<grid, kNT, 0, stream>>>(d_logits, V, plan.chunks, plan.chunk_elems,
-                                                            d_out_ids, counters, partials, cmax);
+
+    const bool tma = (reinterpret_cast<uintptr_t>(d_logits) % 16 == 0) && (V % 4 == 0);
+    constexpr size_t kDyn = stage_bytes<kNT, kVPT, kStages>();
+    static const bool attr_ok = set_dynamic_smem(argmax_kernel<true>, kDyn);
+    static const int res_tma = resident_blocks_dyn(argmax_kernel<true>, kNT, kDyn);
+    static const int res_sca = resident_blocks_dyn(argmax_kernel<false>, kNT, 0);
+    if (!attr_ok) return SEL_ECUDA;
+    const int res = tma ? res_tma : res_sca;
+    const StreamPlan sp = plan_stream(rows, V, sms, res, kUnitMin, kUnitMax);
+
+    char* ws = static_cast<char*>(d_ws);
+    ArgmaxArgs a{};
+    a.logits = d_logits;
+    a.out_ids = d_out_ids;
+    a.counters = reinterpret_cast<uint32_t*>(ws + l.counters);
+    a.partials = reinterpret_cast<ArgPair*>(ws + l.partials);
+    a.stride = l.stride;
+    a.err = reinterpret_cast<uint32_t*>(ws);
+    a.cfg = StreamCfg{rows * sp.chunks, sp.chunks, sp.chunk_elems, V};
+    if (tma)
+        argmax_kernel<true><<<sp.grid, kNT, kDyn, stream>>>(a);
     else
-        argmax_rows_kernel<false><<<grid, kNT, 0, stream>>>(d_logits, V, plan.chunks, plan.chunk_elems,
-                                                             d_out_ids, counters, partials, cmax);
+        argmax_kernel<false><<<sp.grid, kNT, 0, stream>>>(a);
     return cudaGetLastError() == cudaSuccess ? SEL_OK : SEL_ECUDA;
 }

@@ -1,11 +1,9 @@
 // sel_common.cuh -- device helpers shared by the selection kernels.
 //
-// Row streaming: every logits row is read exactly once with 128-bit
-// non-caching loads (ld.global.nc.L1::no_allocate.v4) when the row is
-// 16-byte aligned, or with scalar loads otherwise; each block owns one
-// contiguous chunk of one row. Cross-block combines use a per-row arrival
-// counter in the caller's workspace: the last block of a row to arrive
-// merges the row's partial results in chunk order and resets the counter.
+// Keys and candidates for exact ordering, warp sorts, non-caching loads,
+// and the cross-block hand-off: blocks publish per-row partial results in
+// the caller's workspace and bump a per-row arrival counter; the block that
+// arrives last merges the row's partials and resets the counter.
 #pragma once
 
 #include <cstdint>
@@ -126,6 +124,27 @@ __device__ __forceinline__ T warp_sort_desc(T v) {
     }
     return v;
 }
+
+// ---------------------------------------------------------------------------
+// cross-block hand-off
+// ---------------------------------------------------------------------------
+// Results one block publishes for another (per-chunk partials, candidate
+// lists, flags) are read with strong relaxed loads at GPU scope, after a
+// fence in the reading thread; the publishing threads fence before the
+// arrival counter is bumped.
+
+__device__ __forceinline__ uint64_t ld_gpu_u64(const void* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_gpu_u32(const void* p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ float ld_gpu_f32(const void* p) { return __uint_as_float(ld_gpu_u32(p)); }
+__device__ __forceinline__ double ld_gpu_f64(const void* p) { return __longlong_as_double(static_cast<long long>(ld_gpu_u64(p))); }
 
 // ---------------------------------------------------------------------------
 // last-block-of-row arrival

@@ -82,7 +82,32 @@ size_t argmax_ws_bytes(uint32_t rows, uint32_t V);
 size_t topk_ws_bytes(uint32_t rows, uint32_t V, uint32_t k);
 size_t spec_ws_bytes(uint32_t S, uint32_t V, uint32_t K);
 
-// Workspace: a per-row arrival counter array, then the per-op payload.
+// Workspace: a 256-byte header (word 0: error flags the kernels raise), a
+// per-row arrival counter array, then the per-op payload.
+constexpr size_t kWsHeaderBytes = 256;
 inline size_t ws_counters_bytes(uint32_t rows) { return align_up(static_cast<size_t>(rows) * 4u, 256); }
+
+// Plan of a persistent streaming launch: rows are cut into `chunks` units of
+// `chunk_elems` elements (a multiple of 1,024, at most unit_max); `grid`
+// blocks take the units round-robin. Units are as large as possible while
+// still giving every resident block slot about two units or more, so the
+// bulk-copy ring stays full and the last wave is short.
+struct StreamPlan {
+    uint32_t chunks, chunk_elems, grid;
+};
+
+inline StreamPlan plan_stream(uint32_t rows, uint32_t V, int sms, int resident, uint32_t unit_min,
+                              uint32_t unit_max) {
+    const uint64_t slots = static_cast<uint64_t>(sms > 0 ? sms : 1) * (resident > 0 ? resident : 1);
+    uint32_t ce = unit_max;
+    while (ce > unit_min && static_cast<uint64_t>(rows) * ceil_div(V, ce) < 2 * slots) ce -= 1024u;
+    if (ce < unit_min) ce = unit_min;
+    StreamPlan p;
+    p.chunks = ceil_div(V, ce);
+    p.chunk_elems = ce;
+    const uint64_t units = static_cast<uint64_t>(rows) * p.chunks;
+    p.grid = static_cast<uint32_t>(units < slots ? units : slots);
+    return p;
+}
 
 }  // namespace sel

@@ -32,8 +32,8 @@
 // threads, blocks and chunks, so the CDF is accurate to ~1e-7 of its total.
 #include <cfloat>
 
-#include "sel_common.cuh"
 #include "sel_plan.h"
+#include "sel_stream.cuh"
 
 namespace sel {
 namespace {
@@ -41,6 +41,9 @@ namespace {
 constexpr int kNT = 256;
 constexpr int kWarps = kNT / 32;
 constexpr int kVPT = 8;
+constexpr int kStages = 3;
+constexpr uint32_t kUnitMax = 4u * kNT * kVPT;  // 8,192 elements per unit
+constexpr uint32_t kUnitMin = 1024u;
 constexpr uint32_t kGrain = 4u * kNT;
 constexpr uint32_t kMaxChunks = 4096;
 constexpr uint32_t kOverhead = 1024;
@@ -74,9 +77,9 @@ struct SpecLayout {
 SpecLayout spec_layout(uint32_t S, uint32_t V, uint32_t K) {
     SpecLayout l{};
     l.rows_a = S * (2u * K + 1u);
-    l.cmax_a = max_chunks_bound(V, kGrain, kMaxChunks);
+    l.cmax_a = ceil_div(V, kUnitMin);
     l.cmax_b = l.cmax_a;
-    size_t o = 0;
+    size_t o = kWsHeaderBytes;
     l.row_ctr = o;   o += align_up(static_cast<size_t>(l.rows_a) * 4u, 256);
     l.seq_ctr_a = o; o += align_up(static_cast<size_t>(S) * 4u, 256);
     l.seq_ctr_b = o; o += align_up(static_cast<size_t>(S) * 4u, 256);
@@ -98,8 +101,8 @@ struct SpecArgs {
     uint32_t* emitted;
     uint32_t S, K, V;
     float T;
-    uint32_t chunks;       // phase-1 chunks per row
-    uint32_t chunk_elems;
+    StreamCfg cfg;         // phase-1 units over all rows
+    uint32_t* err;
     uint32_t* row_ctr;
     uint32_t* seq_ctr;
     RowPart* row_parts;    // [rows_a][cmax_a]
@@ -163,11 +166,11 @@ __device__ void decide_sequence(const SpecArgs& a, uint32_t s) {
     Decision d{0u, kDrawNone, 0u, 0u};
 
     bool valid = true;
-    for (uint32_t j = 0; j <= K; ++j) valid &= !(__ldcg(&tstat[j].idx) & kNonfiniteBit);
+    for (uint32_t j = 0; j <= K; ++j) valid &= !(ld_gpu_u32(&tstat[j].idx) & kNonfiniteBit);
     for (uint32_t j = 0; j < K; ++j) valid &= tok[j] < V;
     if (kRej) {
         for (uint32_t j = 0; j < K; ++j) {
-            valid &= !(__ldcg(&dstat[j].idx) & kNonfiniteBit);
+            valid &= !(ld_gpu_u32(&dstat[j].idx) & kNonfiniteBit);
             const float u = a.u_acc[static_cast<size_t>(s) * K + j];
             valid &= u >= 0.0f && u < 1.0f;
         }
@@ -182,9 +185,9 @@ __device__ void decide_sequence(const SpecArgs& a, uint32_t s) {
     }
     uint32_t n = 0;
     if (!kRej) {
-        while (n < K && tok[n] == (__ldcg(&tstat[n].idx) & ~kNonfiniteBit)) ++n;
+        while (n < K && tok[n] == (ld_gpu_u32(&tstat[n].idx) & ~kNonfiniteBit)) ++n;
         for (uint32_t j = 0; j < n; ++j) em[j] = tok[j];
-        em[n] = __ldcg(&tstat[n].idx) & ~kNonfiniteBit;
+        em[n] = ld_gpu_u32(&tstat[n].idx) & ~kNonfiniteBit;
         for (uint32_t j = n + 1; j <= K; ++j) em[j] = SEL_INVALID_ID;
         a.accepted[s] = n;
         a.decisions[s] = d;
@@ -195,8 +198,8 @@ __device__ void decide_sequence(const SpecArgs& a, uint32_t s) {
         const uint32_t t = tok[n];
         const float* trow = a.target + (static_cast<size_t>(s) * (K + 1u) + n) * V;
         const float* drow = a.draft + (static_cast<size_t>(s) * K + n) * V;
-        const double p = exp((static_cast<double>(trow[t]) - __ldcg(&tstat[n].m)) * invT) / __ldcg(&tstat[n].s);
-        const double q = exp((static_cast<double>(drow[t]) - __ldcg(&dstat[n].m)) * invT) / __ldcg(&dstat[n].s);
+        const double p = exp((static_cast<double>(trow[t]) - ld_gpu_f32(&tstat[n].m)) * invT) / ld_gpu_f64(&tstat[n].s);
+        const double q = exp((static_cast<double>(drow[t]) - ld_gpu_f32(&dstat[n].m)) * invT) / ld_gpu_f64(&dstat[n].s);
         const double u = a.u_acc[static_cast<size_t>(s) * K + n];
         if (!(u * q <= p)) break;
     }
@@ -209,44 +212,37 @@ __device__ void decide_sequence(const SpecArgs& a, uint32_t s) {
 }
 
 // Phase 1: per-row (max, sum exp) or (max, argmax); per-sequence decision.
-template <bool kVec, bool kRej>
+template <bool kTma, bool kRej>
 __global__ void __launch_bounds__(kNT) spec_phase1_kernel(SpecArgs a) {
+    extern __shared__ float4 stages[];
+    __shared__ uint64_t full[kStages];
     __shared__ float s_m[kWarps];
     __shared__ uint32_t s_i[kWarps];
     __shared__ uint32_t s_nf[kWarps];
     __shared__ double s_s[kWarps];
-    __shared__ bool s_last;
 
-    const uint32_t chunks = a.chunks;
-    const uint32_t r = blockIdx.x / chunks;
-    const uint32_t chunk = blockIdx.x - r * chunks;
-    uint32_t seq;
-    const float* x = phase1_row(a, r, seq);
-    const uint32_t V = a.V;
-    const uint32_t lo = chunk * a.chunk_elems;
-    const uint32_t hi = min(V, lo + a.chunk_elems);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float invT = kRej ? 1.0f / a.T : 1.0f;
+    auto row_ptr = [&](uint32_t r) {
+        uint32_t seq;
+        return phase1_row(a, r, seq);
+    };
 
-    float m = -INFINITY;   // running max
-    uint32_t bidx = kNoIdx;
-    float sum = 0.0f;      // sum of exp((x - m) / T) over this thread's elements
-    uint32_t absmax = 0;
+    // per-thread running max, lowest argmax id, finite check and (rejection
+    // rule) sum of exp((x - max) / T) over this block's segment of a row
+    float m = -INFINITY;
+    uint32_t bidx = kNoIdx, absmax = 0;
+    float sum = 0.0f;
 
-    for (uint32_t base = lo + 4u * tid; base < hi; base += 4u * kNT * kVPT) {
-        float4 q[kVPT];
-#pragma unroll
-        for (int sl = 0; sl < kVPT; ++sl) q[sl] = ld_quad<kVec>(x, base + 4u * kNT * sl, hi, -INFINITY);
+    auto accum = [&](const Unit& t, float4 (&q)[kVPT]) {
         float tm = -INFINITY;
 #pragma unroll
         for (int sl = 0; sl < kVPT; ++sl) {
-            const uint32_t e = base + 4u * kNT * sl;
-            const bool quad_in = e < hi;
+            const uint32_t e = t.lo + 4u * (tid + kNT * sl);
             const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const bool in = kVec ? quad_in : (e + j < hi);
-                if (in) {
+                if (e + j < t.hi) {
                     absmax = max(absmax, __float_as_uint(f[j]) & 0x7fffffffu);
                     if (f[j] > tm) {
                         tm = f[j];
@@ -255,93 +251,97 @@ __global__ void __launch_bounds__(kNT) spec_phase1_kernel(SpecArgs a) {
                 }
             }
         }
-        if (kRej && tm > -INFINITY) {
+        const float mn = fmaxf(m, tm);
+        if (kRej && mn > -INFINITY && mn < INFINITY) {
             float w[kVPT][4];
 #pragma unroll
             for (int sl = 0; sl < kVPT; ++sl) {
+                const uint32_t e = t.lo + 4u * (tid + kNT * sl);
                 const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) w[sl][j] = expf((f[j] - tm) * invT);  // -inf -> 0
+                for (int j = 0; j < 4; ++j) w[sl][j] = e + j < t.hi ? expf((f[j] - mn) * invT) : 0.0f;
             }
-            const float ts = pairwise32(w);
-            if (tm > m) {
-                sum = sum * expf((m - tm) * invT) + ts;
-            } else {
-                sum = sum + ts * expf((tm - m) * invT);
-            }
+            const float scale = m > -INFINITY ? expf((m - mn) * invT) : 0.0f;
+            sum = sum * scale + pairwise32(w);
         }
-        if (tm > m) m = tm;
-    }
-    uint32_t nf = absmax >= 0x7f800000u ? kNonfiniteBit : 0u;
+        m = mn;
+    };
 
-    // block: max and argmax first, then the sums rescaled to the block max
-    float bm = m;
-    uint32_t bi = bidx;
+    auto flush = [&](const Segment& g) {
+        uint32_t nf = absmax >= 0x7f800000u ? kNonfiniteBit : 0u;
+        float bm = m;
+        uint32_t bi = bidx;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(kFull, bm, o);
-        const uint32_t oi = __shfl_xor_sync(kFull, bi, o);
-        if (beats(ov, oi, bm, bi)) { bm = ov; bi = oi; }
-    }
-    nf = __reduce_or_sync(kFull, nf);
-    if (lane == 0) { s_m[warp] = bm; s_i[warp] = bi; s_nf[warp] = nf; }
-    __syncthreads();
-    bm = s_m[0];
-    bi = s_i[0];
-    nf = s_nf[0];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) {
-        if (beats(s_m[w], s_i[w], bm, bi)) { bm = s_m[w]; bi = s_i[w]; }
-        nf |= s_nf[w];
-    }
-    double bs = 0.0;
-    if (kRej) {
-        double mine = (m > -INFINITY && bm > -INFINITY) ? static_cast<double>(sum) * static_cast<double>(expf((m - bm) * invT)) : 0.0;
-        mine = warp_sum_d(mine);
-        if (lane == 0) s_s[warp] = mine;
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(kFull, bm, o);
+            const uint32_t oi = __shfl_xor_sync(kFull, bi, o);
+            if (beats(ov, oi, bm, bi)) { bm = ov; bi = oi; }
+        }
+        nf = __reduce_or_sync(kFull, nf);
+        if (lane == 0) { s_m[warp] = bm; s_i[warp] = bi; s_nf[warp] = nf; }
         __syncthreads();
+        bm = s_m[0];
+        bi = s_i[0];
+        nf = s_nf[0];
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) bs += s_s[w];
-    }
-
-    RowPart* parts = a.row_parts + static_cast<size_t>(r) * a.cmax;
-    if (tid == 0) {
-        if (chunks == 1) {
-            a.row_stats[r] = RowPart{bm, bi | nf, bs};
-            s_last = true;
-        } else {
-            parts[chunk] = RowPart{bm, bi | nf, bs};
-            s_last = arrive_is_last(&a.row_ctr[r], chunks);
+        for (int w = 1; w < kWarps; ++w) {
+            if (beats(s_m[w], s_i[w], bm, bi)) { bm = s_m[w]; bi = s_i[w]; }
+            nf |= s_nf[w];
         }
-    }
-    __syncthreads();
-    if (!s_last) return;
-
-    if (chunks > 1 && tid == 0) {
-        // merge the row's chunks in chunk order
-        float rm = -INFINITY;
-        uint32_t ri = kNoIdx, rnf = 0;
-        for (uint32_t c = 0; c < chunks; ++c) {
-            const float cm = __ldcg(&parts[c].m);
-            const uint32_t ci = __ldcg(&parts[c].idx);
-            rnf |= ci & kNonfiniteBit;
-            if (beats(cm, ci & ~kNonfiniteBit, rm, ri)) { rm = cm; ri = ci & ~kNonfiniteBit; }
+        // the sums, rescaled to the segment's max, summed in double
+        double bs = 0.0;
+        if (kRej) {
+            double mine = (!nf && m > -INFINITY) ? static_cast<double>(sum) * static_cast<double>(expf((m - bm) * invT))
+                                                 : 0.0;
+            mine = warp_sum_d(mine);
+            if (lane == 0) s_s[warp] = mine;
+            __syncthreads();
+#pragma unroll
+            for (int ww = 0; ww < kWarps; ++ww) bs += s_s[ww];
         }
-        double rs = 0.0;
-        if (kRej && rm > -INFINITY) {
-            const double iT = 1.0 / static_cast<double>(a.T);
-            for (uint32_t c = 0; c < chunks; ++c) {
-                const float cm = __ldcg(&parts[c].m);
-                if (cm > -INFINITY) rs += __ldcg(&parts[c].s) * exp((static_cast<double>(cm) - rm) * iT);
+        m = -INFINITY;
+        bidx = kNoIdx;
+        absmax = 0;
+        sum = 0.0f;
+        if (tid == 0) {
+            bool row_done = true;
+            if (g.count == 1) {
+                a.row_stats[g.row] = RowPart{bm, bi | nf, bs};
+            } else {
+                RowPart* parts = a.row_parts + static_cast<size_t>(g.row) * a.cmax;
+                parts[g.index] = RowPart{bm, bi | nf, bs};
+                row_done = segment_arrive(&a.row_ctr[g.row], g.count);
+                if (row_done) {
+                    // merge the row's segments in segment order
+                    float rm = -INFINITY;
+                    uint32_t ri = kNoIdx, rnf = 0;
+                    for (uint32_t c = 0; c < g.count; ++c) {
+                        const float cm = ld_gpu_f32(&parts[c].m);
+                        const uint32_t ci = ld_gpu_u32(&parts[c].idx);
+                        rnf |= ci & kNonfiniteBit;
+                        if (beats(cm, ci & ~kNonfiniteBit, rm, ri)) { rm = cm; ri = ci & ~kNonfiniteBit; }
+                    }
+                    double rs = 0.0;
+                    if (kRej && !rnf) {
+                        const double iT = 1.0 / static_cast<double>(a.T);
+                        for (uint32_t c = 0; c < g.count; ++c)
+                            rs += ld_gpu_f64(&parts[c].s) * exp((static_cast<double>(ld_gpu_f32(&parts[c].m)) - rm) * iT);
+                    }
+                    a.row_stats[g.row] = RowPart{rm, ri | rnf, rs};
+                }
+            }
+            // the last row of the sequence to finish runs the acceptance chain
+            if (row_done) {
+                uint32_t seq;
+                phase1_row(a, g.row, seq);
+                const uint32_t rows_per_seq = kRej ? 2u * a.K + 1u : a.K + 1u;
+                if (segment_arrive(&a.seq_ctr[seq], rows_per_seq)) decide_sequence<kRej>(a, seq);
             }
         }
-        a.row_stats[r] = RowPart{rm, ri | rnf, rs};
-    }
-    // the last row of the sequence to finish runs the acceptance chain
-    if (tid == 0) {
-        const uint32_t rows_per_seq = kRej ? 2u * a.K + 1u : a.K + 1u;
-        if (arrive_is_last(&a.seq_ctr[seq], rows_per_seq)) decide_sequence<kRej>(a, seq);
-    }
+        __syncthreads();
+    };
+
+    stream_segments<kTma, kNT, kVPT, kStages>(a.cfg, row_ptr, accum, flush, stages, full, a.err);
 }
 
 struct DrawArgs {
@@ -450,11 +450,12 @@ __global__ void __launch_bounds__(kNT) spec_draw_kernel(DrawArgs a) {
     }
     __syncthreads();
     if (!s_last) return;
+    __threadfence();  // order this thread's reads after the arrivals it saw
 
     // last block: locate the chunk, then the element, where u * total falls
     const DrawPart* parts = a.parts + static_cast<size_t>(s) * a.cmax;
     double R = 0.0, P = 0.0;
-    for (uint32_t c = 0; c < chunks; ++c) { R += __ldcg(&parts[c].r); P += __ldcg(&parts[c].p); }
+    for (uint32_t c = 0; c < chunks; ++c) { R += ld_gpu_f64(&parts[c].r); P += ld_gpu_f64(&parts[c].p); }
     const bool use_p = !(R > 0.0);  // residual empty by rounding: draw from p
     const double total = use_p ? P : R;
     const double target = static_cast<double>(a.u_fin[s]) * total;
@@ -462,7 +463,7 @@ __global__ void __launch_bounds__(kNT) spec_draw_kernel(DrawArgs a) {
     double before = 0.0, acc = 0.0;
     uint32_t last_pos_chunk = 0;
     for (uint32_t c = 0; c < chunks; ++c) {
-        const double t = use_p ? __ldcg(&parts[c].p) : __ldcg(&parts[c].r);
+        const double t = use_p ? ld_gpu_f64(&parts[c].p) : ld_gpu_f64(&parts[c].r);
         if (t > 0.0) last_pos_chunk = c;
         if (cstar == chunks && target < acc + t) { cstar = c; before = acc; }
         acc += t;
@@ -470,7 +471,7 @@ __global__ void __launch_bounds__(kNT) spec_draw_kernel(DrawArgs a) {
     if (cstar == chunks) {  // rounding: take the last chunk with mass
         cstar = last_pos_chunk;
         before = 0.0;
-        for (uint32_t c = 0; c < cstar; ++c) before += use_p ? __ldcg(&parts[c].p) : __ldcg(&parts[c].r);
+        for (uint32_t c = 0; c < cstar; ++c) before += use_p ? ld_gpu_f64(&parts[c].p) : ld_gpu_f64(&parts[c].r);
     }
     if (tid == 0) { s_pick = kNoIdx; s_lastpos = -1; }
     __syncthreads();
@@ -576,8 +577,15 @@ extern "C" sel_status spec_accept(const float* d_target, const float* d_draft, c
 
     char* ws = static_cast<char*>(d_ws);
     const uint32_t rows1 = rej ? static_cast<uint32_t>(rows_a) : S * (K + 1u);
-    static const int res1 = resident_blocks(spec_phase1_kernel<true, true>, kNT);
-    const RowPlan plan = plan_rows(rows1, V, sms, kGrain, kMaxChunks, kOverhead, res1);
+    const bool vec = V % 4 == 0 && reinterpret_cast<uintptr_t>(d_target) % 16 == 0 &&
+                     (!rej || K == 0 || reinterpret_cast<uintptr_t>(d_draft) % 16 == 0);
+    constexpr size_t kDyn = stage_bytes<kNT, kVPT, kStages>();
+    static const bool attr_ok = set_dynamic_smem(spec_phase1_kernel<true, true>, kDyn) &&
+                                set_dynamic_smem(spec_phase1_kernel<true, false>, kDyn);
+    static const int res_tma = resident_blocks_dyn(spec_phase1_kernel<true, true>, kNT, kDyn);
+    static const int res_sca = resident_blocks_dyn(spec_phase1_kernel<false, true>, kNT, 0);
+    if (!attr_ok) return SEL_ECUDA;
+    const StreamPlan plan = plan_stream(rows1, V, sms, vec ? res_tma : res_sca, kUnitMin, kUnitMax);
     if (static_cast<uint64_t>(rows1) * plan.chunks > 0x7fffffffull) return SEL_EUNSUPPORTED;
     SpecArgs a{};
     a.target = d_target;
@@ -589,22 +597,20 @@ extern "C" sel_status spec_accept(const float* d_target, const float* d_draft, c
     a.emitted = d_emitted;
     a.S = S; a.K = K; a.V = V;
     a.T = rej ? p->temperature : 1.0f;
-    a.chunks = plan.chunks;
-    a.chunk_elems = plan.chunk_elems;
+    a.cfg = StreamCfg{rows1 * plan.chunks, plan.chunks, plan.chunk_elems, V};
+    a.err = reinterpret_cast<uint32_t*>(ws);
     a.row_ctr = reinterpret_cast<uint32_t*>(ws + l.row_ctr);
     a.seq_ctr = reinterpret_cast<uint32_t*>(ws + l.seq_ctr_a);
     a.row_parts = reinterpret_cast<RowPart*>(ws + l.row_parts);
     a.row_stats = reinterpret_cast<RowPart*>(ws + l.row_stats);
     a.decisions = reinterpret_cast<Decision*>(ws + l.decisions);
     a.cmax = l.cmax_a;
-    const bool vec = V % 4 == 0 && reinterpret_cast<uintptr_t>(d_target) % 16 == 0 &&
-                     (!rej || reinterpret_cast<uintptr_t>(d_draft) % 16 == 0);
-    const dim3 grid1(rows1 * plan.chunks);
+    const dim3 grid1(plan.grid);
     if (rej) {
-        if (vec) spec_phase1_kernel<true, true><<<grid1, kNT, 0, stream>>>(a);
+        if (vec) spec_phase1_kernel<true, true><<<grid1, kNT, kDyn, stream>>>(a);
         else spec_phase1_kernel<false, true><<<grid1, kNT, 0, stream>>>(a);
     } else {
-        if (vec) spec_phase1_kernel<true, false><<<grid1, kNT, 0, stream>>>(a);
+        if (vec) spec_phase1_kernel<true, false><<<grid1, kNT, kDyn, stream>>>(a);
         else spec_phase1_kernel<false, false><<<grid1, kNT, 0, stream>>>(a);
     }
     if (cudaGetLastError() != cudaSuccess) return SEL_ECUDA;

@@ -11,29 +11,31 @@
 // Design (sm_103a). The page's implementation is a ggml graph op (TOP_K +
 // get_rows) whose kernel is not shown; this one is a single launch that
 // reads each row once:
-//  1. Each block streams one chunk of one row in tiles of 8,192 elements
-//     (8 x 128-bit loads per thread, all in flight) and turns each float into
-//     an order-preserving 32-bit key in registers.
+//  1. Persistent blocks stream 32 KB row chunks through the TMA bulk-copy
+//     ring of sel_stream.cuh; each thread holds 32 logits of the chunk in
+//     registers and turns them into order-preserving 32-bit keys on the fly.
 //  2. A cheap exact filter: each warp sorts its 32 lane maxima (shuffle
 //     bitonic sort) and takes the ceil(k/8)-th; the minimum over the 8 warps
-//     is a key that at least k elements of the tile reach, so nothing below
-//     it can be in the top k. Survivors (typically ~1.5 k per tile) go to a
+//     is a key that at least k elements of the chunk reach, so nothing below
+//     it can be in the chunk's top k. Survivors (typically ~1.5 k) go to a
 //     shared-memory buffer as 64-bit candidates (key << 32 | ~id), which
 //     order exactly like (value desc, id asc).
-//  3. The block selects its chunk's top k from the buffer (rank counting for
-//     small buffers, bitonic sort otherwise) and stores them, sorted, in the
-//     workspace. A buffer overflow (adversarial rows such as all-equal
-//     values) falls back to appending 1,024 elements at a time with a
-//     selection in between, which is exact for any input.
-//  4. The last block of the row to arrive merges the per-chunk lists: a
-//     bound taken from the lists' r-th entries (the m-th largest of the
-//     chunks' r-th entries, m * r >= k) discards almost every entry, and the
-//     survivors are selected exactly. Sampling then runs its softmax,
-//     top-p, min-p and inverse-CDF draw on the k candidates in one warp.
-#include <cfloat>
-
-#include "sel_common.cuh"
+//  3. The buffer persists over the consecutive chunks of a row that the
+//     block owns; once it holds k candidates, its k-th key also filters later
+//     chunks (their ids are higher, so an equal key cannot displace it). When
+//     the block leaves the row it selects the segment's top k (rank counting
+//     for small buffers, bitonic sort otherwise) and publishes them, sorted,
+//     in the workspace. A buffer overflow (adversarial chunks such as
+//     all-equal values) falls back to appending 1,024 elements at a time
+//     with a selection in between, which is exact for any input.
+//  4. The block that publishes a row's last segment merges the segment
+//     lists: a bound from the lists' r-th entries (the m-th largest of the
+//     lists' r-th entries is reached by m * r >= k entries) discards almost
+//     every entry, and the survivors are selected exactly. Sampling then
+//     runs its softmax, top-p, min-p and inverse-CDF draw on the k
+//     candidates in one warp.
 #include "sel_plan.h"
+#include "sel_stream.cuh"
 
 namespace sel {
 namespace {
@@ -41,12 +43,11 @@ namespace {
 constexpr int kNT = 256;
 constexpr int kWarps = kNT / 32;
 constexpr int kVPT = 8;
-constexpr uint32_t kTile = 4u * kNT * kVPT;  // 8,192 elements per tile
-constexpr uint32_t kGrain = 4u * kNT;        // chunk sizes are multiples of 1,024
-constexpr uint32_t kMaxChunks = 32;          // merge input <= 32 lists
+constexpr int kStages = 2;
+constexpr uint32_t kUnit = 4u * kNT * kVPT;  // 8,192 elements per chunk
 constexpr uint32_t kCap = 2048;              // candidate buffer (>= SEL_MAX_K + 4 * kNT)
-constexpr uint32_t kOverhead = 2048;         // per-block cost, in elements
 constexpr uint32_t kRankMax = 512;           // rank counting up to this many candidates
+constexpr uint32_t kFastMergeLists = 32;     // one warp lane per chunk list
 
 static_assert(kCap >= SEL_MAX_K + 4 * kNT, "a slot of 1,024 must fit after a selection");
 
@@ -56,10 +57,9 @@ struct TopkShared {
     uint64_t warp_cand[kWarps];
     uint32_t warp_val[kWarps];
     uint32_t count;              // entries appended to buf
-    uint32_t tau_key;            // key of the k-th candidate once buf held k
-    uint32_t flag;
+    uint32_t tau_key;            // key of the k-th candidate after a selection
     uint32_t total;
-    bool last;
+    uint32_t last;
 };
 
 struct SampleArgs {
@@ -71,9 +71,21 @@ struct SampleArgs {
     int order;
 };
 
-__device__ __forceinline__ uint32_t lanemask_lt() {
-    return (1u << (threadIdx.x & 31)) - 1u;
-}
+struct TopkArgs {
+    const float* logits;
+    uint32_t k;
+    float* out_vals;         // [rows][k] (top-k)
+    uint32_t* out_ids;       // [rows][k] (top-k) or [rows] (sampling)
+    uint32_t* counters;      // [rows]
+    uint32_t* chunk_flags;   // [rows][stride]
+    uint64_t* lists;         // [rows][stride][k]
+    uint32_t stride;
+    uint32_t* err;
+    StreamCfg cfg;
+    SampleArgs sa;
+};
+
+__device__ __forceinline__ uint32_t lanemask_lt() { return (1u << (threadIdx.x & 31)) - 1u; }
 
 // Append `cand` for every lane with p set; every lane of the warp must call.
 __device__ __forceinline__ void warp_append(TopkShared& s, bool p, uint64_t cand) {
@@ -156,17 +168,18 @@ __device__ void sample_epilogue(const TopkShared& s, uint32_t n, uint32_t row, b
     const float x0 = key2f(cand_key(s.sorted[0]));
     const float T = sa.temperature;
     const bool temp_last = sa.order == SEL_ORDER_TEMP_LAST;
-    // filter weights wf (T = 1 when temperature comes last) and draw weights wd;
-    // the largest candidate has weight exactly 1.
+    // filter weights wf (T = 1 when temperature comes last) and draw weights
+    // wd, relative to the largest candidate (weight exactly 1)
+    auto wfilter = [&](uint32_t j) {
+        const float d = key2f(cand_key(s.sorted[j])) - x0;
+        return temp_last ? expf(d) : expf(d / T);
+    };
+    auto wdraw = [&](uint32_t j) { return expf((key2f(cand_key(s.sorted[j])) - x0) / T); };
+
     float sum_f = 0.0f;
     for (uint32_t b = 0; b < n; b += 32) {
         const uint32_t j = b + lane;
-        float wf = 0.0f;
-        if (j < n) {
-            const float d = key2f(cand_key(s.sorted[j])) - x0;
-            wf = temp_last ? expf(d) : expf(d / T);
-        }
-        float t = wf;
+        float t = j < n ? wfilter(j) : 0.0f;
 #pragma unroll
         for (int m = 16; m > 0; m >>= 1) t += __shfl_xor_sync(kFull, t, m);
         sum_f += t;
@@ -178,12 +191,7 @@ __device__ void sample_epilogue(const TopkShared& s, uint32_t n, uint32_t row, b
         ns = 0;
         for (uint32_t b = 0; b < n && ns == 0; b += 32) {
             const uint32_t j = b + lane;
-            float p = 0.0f;
-            if (j < n) {
-                const float d = key2f(cand_key(s.sorted[j])) - x0;
-                p = (temp_last ? expf(d) : expf(d / T)) / sum_f;
-            }
-            float incl = p;
+            float incl = j < n ? wfilter(j) / sum_f : 0.0f;
 #pragma unroll
             for (int m = 1; m < 32; m <<= 1) {
                 const float o = __shfl_up_sync(kFull, incl, m);
@@ -201,12 +209,7 @@ __device__ void sample_epilogue(const TopkShared& s, uint32_t n, uint32_t row, b
         uint32_t keep = 1;
         for (uint32_t b = 0; b < ns; b += 32) {
             const uint32_t j = b + lane;
-            bool ok = false;
-            if (j < ns && j > 0) {
-                const float d = key2f(cand_key(s.sorted[j])) - x0;
-                const float wf = temp_last ? expf(d) : expf(d / T);
-                ok = wf >= sa.min_p;
-            }
+            const bool ok = j < ns && j > 0 && wfilter(j) >= sa.min_p;
             const uint32_t m = __ballot_sync(kFull, ok);
             if (m) keep = b + 32 - __clz(m);  // survivors form a prefix
         }
@@ -216,9 +219,7 @@ __device__ void sample_epilogue(const TopkShared& s, uint32_t n, uint32_t row, b
     float sum_d = 0.0f;
     for (uint32_t b = 0; b < ns; b += 32) {
         const uint32_t j = b + lane;
-        float wd = 0.0f;
-        if (j < ns) wd = expf((key2f(cand_key(s.sorted[j])) - x0) / T);
-        float t = wd;
+        float t = j < ns ? wdraw(j) : 0.0f;
 #pragma unroll
         for (int m = 16; m > 0; m >>= 1) t += __shfl_xor_sync(kFull, t, m);
         sum_d += t;
@@ -229,8 +230,7 @@ __device__ void sample_epilogue(const TopkShared& s, uint32_t n, uint32_t row, b
     float cum = 0.0f;
     for (uint32_t b = 0; b < ns && !found; b += 32) {
         const uint32_t j = b + lane;
-        float wd = 0.0f;
-        if (j < ns) wd = expf((key2f(cand_key(s.sorted[j])) - x0) / T);
+        const float wd = j < ns ? wdraw(j) : 0.0f;
         float incl = wd;
 #pragma unroll
         for (int m = 1; m < 32; m <<= 1) {
@@ -247,160 +247,41 @@ __device__ void sample_epilogue(const TopkShared& s, uint32_t n, uint32_t row, b
         }
         cum = __shfl_sync(kFull, incl, 31);
     }
-    if (!found) pick_w = expf((key2f(cand_key(s.sorted[pick])) - x0) / T);
+    if (!found) pick_w = wdraw(pick);
     if (lane == 0) {
         out_ids[row] = cand_id(s.sorted[pick]);
         sa.out_probs[row] = pick_w / sum_d;
     }
 }
 
-template <bool kVec, bool kSample>
-__global__ void __launch_bounds__(kNT, 3) topk_rows_kernel(
-    const float* __restrict__ logits, uint32_t V, uint32_t k, uint32_t chunks,
-    uint32_t chunk_elems, float* __restrict__ out_vals, uint32_t* __restrict__ out_ids,
-    uint32_t* __restrict__ counters, uint32_t* __restrict__ chunk_flags,
-    uint64_t* __restrict__ lists, uint32_t list_stride, SampleArgs sa) {
-    __shared__ TopkShared s;
-
-    const uint32_t row = blockIdx.x / chunks;
-    const uint32_t chunk = blockIdx.x - row * chunks;
-    const float* x = logits + static_cast<size_t>(row) * V;
-    const uint32_t lo = chunk * chunk_elems;
-    const uint32_t hi = min(V, lo + chunk_elems);
+// Merge the sorted chunk lists of one row (L[c * k + j]) into s.sorted[0..k).
+// Block-collective.
+__device__ void merge_row_lists(TopkShared& s, const uint64_t* L, uint32_t chunks, uint32_t k, uint32_t* err) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-    if (tid == 0) { s.count = 0; s.tau_key = 0; }
-    uint32_t kmin = 0xffffffffu, kmax = 0u;  // finite check over real elements
-
-    for (uint32_t tile_lo = lo; tile_lo < hi; tile_lo += kTile) {
-        uint32_t key[kVPT][4];
-        uint32_t tmax = 0;
-        {
-            float4 q[kVPT];
-#pragma unroll
-            for (int sl = 0; sl < kVPT; ++sl) q[sl] = ld_quad<kVec>(x, tile_lo + 4u * (tid + kNT * sl), hi, 0.0f);
-#pragma unroll
-            for (int sl = 0; sl < kVPT; ++sl) {
-                const uint32_t e = tile_lo + 4u * (tid + kNT * sl);
-                const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const bool in = kVec ? (e < hi) : (e + j < hi);
-                    uint32_t kk = f2key(f[j]);
-                    kmin = in ? min(kmin, kk) : kmin;
-                    kk = in ? kk : 0u;
-                    kmax = max(kmax, kk);
-                    tmax = max(tmax, kk);
-                    key[sl][j] = kk;
-                }
-            }
-        }
-        // tile bound: >= k elements of this tile have key >= tau_tile
-        if (k <= 32u * kWarps) {
-            const uint32_t v = warp_sort_desc(tmax);
-            const uint32_t r = (k + kWarps - 1) / kWarps;
-            const uint32_t wv = __shfl_sync(kFull, v, r - 1);
-            if (lane == 0) s.warp_val[warp] = wv;
-        }
-        __syncthreads();
-        uint32_t tau_tile = 0;
-        if (k <= 32u * kWarps) {
-            tau_tile = s.warp_val[0];
-#pragma unroll
-            for (int w = 1; w < kWarps; ++w) tau_tile = min(tau_tile, s.warp_val[w]);
-        }
-        const uint32_t pre = s.count;
-        // later elements have higher ids: an equal key cannot displace the k-th
-        uint32_t thr = max(tau_tile, s.tau_key + 1u);
-        if (__any_sync(kFull, tmax >= thr)) {
-#pragma unroll
-            for (int sl = 0; sl < kVPT; ++sl) {
-                const uint32_t e = tile_lo + 4u * (tid + kNT * sl);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) warp_append(s, key[sl][j] >= thr, make_cand(key[sl][j], e + j));
-            }
-        }
-        __syncthreads();
-        const uint32_t appended = s.count;
-        if (appended > kCap) {
-            // overflow (adversarial rows): redo this tile slot by slot,
-            // selecting in between; the slot is re-read from memory so the
-            // common path keeps its keys in registers only
-            __syncthreads();
-            if (tid == 0) s.count = pre;
-            __syncthreads();
-#pragma unroll 1
-            for (int sl = 0; sl < kVPT; ++sl) {
-                if (s.count + 4u * kNT > kCap) reduce_buffer(s, k);
-                thr = max(tau_tile, s.tau_key + 1u);
-                const uint32_t e = tile_lo + 4u * (tid + kNT * sl);
-                const float4 q = ld_quad<kVec>(x, e, hi, 0.0f);
-                const float f[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const bool in = kVec ? (e < hi) : (e + j < hi);
-                    const uint32_t kk = in ? f2key(f[j]) : 0u;
-                    warp_append(s, kk >= thr, make_cand(kk, e + j));
-                }
-                __syncthreads();
-            }
-        }
-        if (tile_lo + kTile < hi && s.count > k) reduce_buffer(s, k);
-    }
-
-    // the chunk's top k, sorted
-    const uint32_t n = min(s.count, kCap);
-    block_select_sorted(s.buf, n, k, s.sorted);
-    const uint32_t have = n < k ? n : k;
-    const uint32_t nf_local = key_nonfinite(__reduce_min_sync(kFull, kmin), __reduce_max_sync(kFull, kmax)) ? 1u : 0u;
-    if (lane == 0) s.warp_val[warp] = nf_local;
-    __syncthreads();
-    uint32_t nf = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) nf |= s.warp_val[w];
-
-    if (chunks == 1) {
-        if constexpr (kSample) {
-            if (warp == 0) sample_epilogue(s, have, row, nf != 0, sa, out_ids);
-        } else {
-            for (uint32_t j = tid; j < k; j += kNT) {
-                const bool ok = !nf && j < have;
-                out_vals[static_cast<size_t>(row) * k + j] = ok ? key2f(cand_key(s.sorted[j])) : __uint_as_float(0x7fc00000u);
-                out_ids[static_cast<size_t>(row) * k + j] = ok ? cand_id(s.sorted[j]) : SEL_INVALID_ID;
-            }
-        }
-        return;
-    }
-
-    // publish the sorted list (padded with empty candidates) and arrive
-    uint64_t* my_list = lists + (static_cast<size_t>(row) * list_stride + chunk) * k;
-    for (uint32_t j = tid; j < k; j += kNT) my_list[j] = j < have ? s.sorted[j] : 0ull;
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        chunk_flags[static_cast<size_t>(row) * list_stride + chunk] = nf;
-        s.last = arrive_is_last(&counters[row], chunks);
-    }
-    __syncthreads();
-    if (!s.last) return;
-
-    // ---- last block of the row: merge the chunk lists ----
-    const uint64_t* L = lists + static_cast<size_t>(row) * list_stride * k;
-    nf = 0;
-    for (uint32_t c = lane; c < chunks; c += 32) nf |= __ldcg(chunk_flags + static_cast<size_t>(row) * list_stride + c);
-    nf = __reduce_or_sync(kFull, nf);
-
     // bound: for m lists and r = ceil(k / m), the m-th largest of the lists'
     // r-th entries is reached by at least m * r >= k entries
-    {
+    uint64_t b = 0;
+    if (chunks <= kFastMergeLists) {
         const uint32_t m = max(1u, chunks >> warp);
         const uint32_t r = (k + m - 1) / m;
         uint64_t v = 0;
-        if (static_cast<uint32_t>(lane) < chunks) v = __ldcg(reinterpret_cast<const unsigned long long*>(L + static_cast<size_t>(lane) * k + (r - 1)));
+        if (static_cast<uint32_t>(lane) < chunks)
+            v = ld_gpu_u64(L + static_cast<size_t>(lane) * k + (r - 1));
         v = warp_sort_desc(v);
-        const uint64_t b = shfl64(v, static_cast<int>(m - 1));
-        if (lane == 0) s.warp_cand[warp] = b;
+        b = shfl64(v, static_cast<int>(m - 1));
+    } else {
+        // many lists: the largest k-th entry (one list alone reaches it k times)
+        for (uint32_t c = lane; c < chunks; c += 32) {
+            const uint64_t v = ld_gpu_u64(L + static_cast<size_t>(c) * k + (k - 1));
+            b = v > b ? v : b;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const uint64_t w = shfl_xor64(b, o);
+            b = w > b ? w : b;
+        }
     }
+    if (lane == 0) s.warp_cand[warp] = b;
     if (tid == 0) { s.count = 0; s.tau_key = 0; s.total = 0; }
     __syncthreads();
     uint64_t tau_m = s.warp_cand[0];
@@ -410,10 +291,13 @@ __global__ void __launch_bounds__(kNT, 3) topk_rows_kernel(
     // count the survivors first; append in one pass if they fit
     const uint32_t total_entries = chunks * k;
     uint32_t mine = 0;
+    bool disorder = false;
     for (uint32_t i = tid; i < total_entries; i += kNT) {
-        const uint64_t v = __ldcg(reinterpret_cast<const unsigned long long*>(L + i));
+        const uint64_t v = ld_gpu_u64(L + i);
         mine += (v != 0 && v >= tau_m) ? 1u : 0u;
+        if ((i % k) + 1 < k) disorder |= ld_gpu_u64(L + i + 1) > v;
     }
+    if (__any_sync(kFull, disorder) && lane == 0) atomicOr(err, kErrListOrder);
     mine = __reduce_add_sync(kFull, mine);
     if (lane == 0) atomicAdd(&s.total, mine);
     __syncthreads();
@@ -421,10 +305,11 @@ __global__ void __launch_bounds__(kNT, 3) topk_rows_kernel(
         for (uint32_t i0 = 0; i0 < total_entries; i0 += kNT) {
             const uint32_t i = i0 + tid;
             uint64_t v = 0;
-            if (i < total_entries) v = __ldcg(reinterpret_cast<const unsigned long long*>(L + i));
+            if (i < total_entries) v = ld_gpu_u64(L + i);
             warp_append(s, v != 0 && v >= tau_m, v);
         }
         __syncthreads();
+        if (tid == 0 && s.count < k) atomicOr(err, kErrMergeShort);
         block_select_sorted(s.buf, min(s.count, kCap), k, s.sorted);
     } else {
         // list by list, keeping the buffer at its top k in between
@@ -434,7 +319,7 @@ __global__ void __launch_bounds__(kNT, 3) topk_rows_kernel(
             for (uint32_t j0 = 0; j0 < k; j0 += kNT) {
                 const uint32_t j = j0 + tid;
                 uint64_t v = 0;
-                if (j < k) v = __ldcg(reinterpret_cast<const unsigned long long*>(L + static_cast<size_t>(c) * k + j));
+                if (j < k) v = ld_gpu_u64(L + static_cast<size_t>(c) * k + j);
                 warp_append(s, v != 0 && v >= floor_c, v);
             }
             __syncthreads();
@@ -449,62 +334,215 @@ __global__ void __launch_bounds__(kNT, 3) topk_rows_kernel(
         }
         block_select_sorted(s.buf, s.count, k, s.sorted);
     }
+}
 
+template <bool kSample>
+__device__ __forceinline__ void write_row(const TopkShared& s, const TopkArgs& a, uint32_t row, uint32_t have,
+                                          bool nonfinite) {
+    const int tid = threadIdx.x;
     if constexpr (kSample) {
-        if (warp == 0) sample_epilogue(s, k, row, nf != 0, sa, out_ids);
+        if (tid < 32) sample_epilogue(s, have, row, nonfinite, a.sa, a.out_ids);
     } else {
+        const uint32_t k = a.k;
         for (uint32_t j = tid; j < k; j += kNT) {
-            const bool ok = !nf;
-            out_vals[static_cast<size_t>(row) * k + j] = ok ? key2f(cand_key(s.sorted[j])) : __uint_as_float(0x7fc00000u);
-            out_ids[static_cast<size_t>(row) * k + j] = ok ? cand_id(s.sorted[j]) : SEL_INVALID_ID;
+            const bool ok = !nonfinite && j < have;
+            a.out_vals[static_cast<size_t>(row) * k + j] =
+                ok ? key2f(cand_key(s.sorted[j])) : __uint_as_float(0x7fc00000u);
+            a.out_ids[static_cast<size_t>(row) * k + j] = ok ? cand_id(s.sorted[j]) : SEL_INVALID_ID;
         }
     }
 }
 
+template <bool kTma, bool kSample>
+__global__ void __launch_bounds__(kNT, 2) topk_kernel(TopkArgs a) {
+    extern __shared__ float4 stages[];
+    __shared__ uint64_t full[kStages];
+    __shared__ TopkShared s;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t V = a.cfg.V, k = a.k;
+    auto row_ptr = [&](uint32_t r) { return a.logits + static_cast<size_t>(r) * V; };
+
+    // finite check of this thread over the segment (real elements only)
+    uint32_t seg_kmin = 0xffffffffu, seg_kmax = 0;
+    if (tid == 0) { s.count = 0; s.tau_key = 0; }
+    __syncthreads();
+
+    auto accum = [&](const Unit& t, float4 (&q)[kVPT]) {
+        uint32_t kmax = 0;  // the thread's largest key in this chunk
+#pragma unroll
+        for (int sl = 0; sl < kVPT; ++sl) {
+            const uint32_t e = t.lo + 4u * (tid + kNT * sl);
+            const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t kk = f2key(f[j]);
+                const bool in = e + j < t.hi;
+                seg_kmin = in ? min(seg_kmin, kk) : seg_kmin;
+                kmax = in ? max(kmax, kk) : kmax;
+            }
+        }
+        seg_kmax = max(seg_kmax, kmax);
+        // chunk bound: >= k elements of this chunk have key >= tau
+        if (k <= 32u * kWarps) {
+            const uint32_t v = warp_sort_desc(kmax);
+            const uint32_t r = (k + kWarps - 1) / kWarps;
+            const uint32_t wv = __shfl_sync(kFull, v, r - 1);
+            if (lane == 0) s.warp_val[warp] = wv;
+        }
+        __syncthreads();
+        // keep room for a whole chunk of survivors most of the time
+        if (s.count > kCap / 2) reduce_buffer(s, k);
+        uint32_t tau = 0;
+        if (k <= 32u * kWarps) {
+            tau = s.warp_val[0];
+#pragma unroll
+            for (int w = 1; w < kWarps; ++w) tau = min(tau, s.warp_val[w]);
+        }
+        // buffered candidates have lower ids than this chunk, so an equal key
+        // cannot displace the k-th; key 0 marks padding
+        const uint32_t pre = s.count;
+        uint32_t thr = max(tau, s.tau_key + 1u);
+        if (__any_sync(kFull, kmax >= thr)) {
+#pragma unroll
+            for (int sl = 0; sl < kVPT; ++sl) {
+                const uint32_t e = t.lo + 4u * (tid + kNT * sl);
+                const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t kk = e + j < t.hi ? f2key(f[j]) : 0u;
+                    warp_append(s, kk >= thr, make_cand(kk, e + j));
+                }
+            }
+        }
+        __syncthreads();
+        if (s.count > kCap) {
+            // overflow (adversarial chunks): redo the chunk slot by slot
+            // (1,024 elements), selecting in between
+            __syncthreads();
+            if (tid == 0) s.count = pre;
+            __syncthreads();
+#pragma unroll
+            for (int sl = 0; sl < kVPT; ++sl) {
+                if (s.count + 4u * kNT > kCap) reduce_buffer(s, k);
+                thr = max(tau, s.tau_key + 1u);
+                const uint32_t e = t.lo + 4u * (tid + kNT * sl);
+                const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t kk = e + j < t.hi ? f2key(f[j]) : 0u;
+                    warp_append(s, kk >= thr, make_cand(kk, e + j));
+                }
+                __syncthreads();
+            }
+        }
+    };
+
+    auto flush = [&](const Segment& g) {
+        // this segment's top k, sorted
+        const uint32_t n = min(s.count, kCap);
+        block_select_sorted(s.buf, n, k, s.sorted);
+        const uint32_t have = n < k ? n : k;
+        const uint32_t nf_local =
+            key_nonfinite(__reduce_min_sync(kFull, seg_kmin), __reduce_max_sync(kFull, seg_kmax)) ? 1u : 0u;
+        seg_kmin = 0xffffffffu;
+        seg_kmax = 0;
+        if (lane == 0) s.warp_val[warp] = nf_local;
+        __syncthreads();
+        uint32_t nf = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) nf |= s.warp_val[w];
+
+        if (g.count == 1) {
+            write_row<kSample>(s, a, g.row, have, nf != 0);
+            if (tid == 0) atomicAdd(a.err + 1, 1u);  // rows finished (self-check)
+        } else {
+            // publish the sorted list (padded with empty candidates) and arrive
+            uint64_t* my_list = a.lists + (static_cast<size_t>(g.row) * a.stride + g.index) * k;
+            for (uint32_t j = tid; j < k; j += kNT) my_list[j] = j < have ? s.sorted[j] : 0ull;
+            __threadfence();
+            __syncthreads();
+            if (tid == 0) {
+                a.chunk_flags[static_cast<size_t>(g.row) * a.stride + g.index] = nf;
+                s.last = segment_arrive(&a.counters[g.row], g.count) ? 1u : 0u;
+            }
+            __syncthreads();
+            if (s.last) {
+                __threadfence();  // order this thread's reads after the arrivals it saw
+                nf = 0;
+                for (uint32_t c = lane; c < g.count; c += 32)
+                    nf |= ld_gpu_u32(a.chunk_flags + static_cast<size_t>(g.row) * a.stride + c);
+                nf = __reduce_or_sync(kFull, nf);
+                merge_row_lists(s, a.lists + static_cast<size_t>(g.row) * a.stride * k, g.count, k, a.err);
+                write_row<kSample>(s, a, g.row, k, nf != 0);
+                if (tid == 0) atomicAdd(a.err + 1, 1u);  // rows finished (self-check)
+            }
+        }
+        __syncthreads();
+        if (tid == 0) { s.count = 0; s.tau_key = 0; }
+        __syncthreads();
+    };
+
+    stream_segments<kTma, kNT, kVPT, kStages>(a.cfg, row_ptr, accum, flush, stages, full, a.err);
+}
+
 struct TopkLayout {
     size_t counters, flags, lists, total;
-    uint32_t cmax;
+    uint32_t stride;
 };
+
+// One list per chunk of kUnit elements (a whole row when V <= kUnit).
+uint32_t topk_chunks(uint32_t V) { return ceil_div(V, kUnit); }
 
 TopkLayout topk_layout(uint32_t rows, uint32_t V, uint32_t k) {
     TopkLayout l{};
-    l.cmax = max_chunks_bound(V, kGrain, kMaxChunks);
-    if (l.cmax <= 1) return l;  // one block per row: no workspace
-    l.counters = 0;
-    l.flags = ws_counters_bytes(rows);
-    l.lists = l.flags + align_up(static_cast<size_t>(rows) * l.cmax * 4u, 256);
-    l.total = l.lists + static_cast<size_t>(rows) * l.cmax * k * 8u;
+    l.stride = topk_chunks(V);
+    l.counters = kWsHeaderBytes;
+    l.flags = l.counters + ws_counters_bytes(rows);
+    l.lists = l.flags + align_up(static_cast<size_t>(rows) * l.stride * 4u, 256);
+    l.total = l.lists + (l.stride > 1 ? static_cast<size_t>(rows) * l.stride * k * 8u : 0u);
     return l;
 }
 
 template <bool kSample>
-sel_status launch_topk(const float* d_logits, uint32_t rows, uint32_t V, uint32_t k,
-                       float* d_out_vals, uint32_t* d_out_ids, void* d_ws, size_t ws_bytes,
-                       const SampleArgs& sa, cudaStream_t stream) {
+sel_status launch_topk(const float* d_logits, uint32_t rows, uint32_t V, uint32_t k, float* d_out_vals,
+                       uint32_t* d_out_ids, void* d_ws, size_t ws_bytes, const SampleArgs& sa, cudaStream_t stream) {
     const TopkLayout l = topk_layout(rows, V, k);
-    if (l.total > 0) {
-        if (!d_ws) return SEL_EINVAL;
-        if (reinterpret_cast<uintptr_t>(d_ws) % SEL_WS_ALIGN) return SEL_EINVAL;
-        if (ws_bytes < l.total) return SEL_EWORKSPACE;
-    }
+    if (!d_ws) return SEL_EINVAL;
+    if (reinterpret_cast<uintptr_t>(d_ws) % SEL_WS_ALIGN) return SEL_EINVAL;
+    if (ws_bytes < l.total) return SEL_EWORKSPACE;
     const int sms = device_sms();
     if (sms <= 0) return SEL_ECUDA;
-    static const int res = resident_blocks(topk_rows_kernel<true, kSample>, kNT);
-    const RowPlan plan = plan_rows(rows, V, sms, kGrain, kMaxChunks, kOverhead, res, kTile);
+    constexpr size_t kDyn = stage_bytes<kNT, kVPT, kStages>();
+    static const bool attr_ok = set_dynamic_smem(topk_kernel<true, kSample>, kDyn);
+    static const int res_tma = resident_blocks_dyn(topk_kernel<true, kSample>, kNT, kDyn);
+    static const int res_sca = resident_blocks_dyn(topk_kernel<false, kSample>, kNT, 0);
+    if (!attr_ok) return SEL_ECUDA;
+    const bool tma = (reinterpret_cast<uintptr_t>(d_logits) % 16 == 0) && (V % 4 == 0);
+    const uint32_t chunks = topk_chunks(V);
+    const uint32_t ce = chunks == 1 ? static_cast<uint32_t>(align_up(V, 4)) : kUnit;
+    const uint64_t units = static_cast<uint64_t>(rows) * chunks;
+    const uint64_t slots = static_cast<uint64_t>(sms) * (tma ? res_tma : res_sca);
+    if (units > 0x7fffffffull) return SEL_EUNSUPPORTED;
+
     char* ws = static_cast<char*>(d_ws);
-    uint32_t* counters = l.total ? reinterpret_cast<uint32_t*>(ws + l.counters) : nullptr;
-    uint32_t* flags = l.total ? reinterpret_cast<uint32_t*>(ws + l.flags) : nullptr;
-    uint64_t* lists = l.total ? reinterpret_cast<uint64_t*>(ws + l.lists) : nullptr;
-    const bool vec = (reinterpret_cast<uintptr_t>(d_logits) % 16 == 0) && (V % 4 == 0);
-    const dim3 grid(rows * plan.chunks);
-    if (vec)
-        topk_rows_kernel<true, kSample><<<grid, kNT, 0, stream>>>(d_logits, V, k, plan.chunks, plan.chunk_elems,
-                                                                  d_out_vals, d_out_ids, counters, flags, lists,
-                                                                  l.cmax, sa);
+    TopkArgs a{};
+    a.logits = d_logits;
+    a.k = k;
+    a.out_vals = d_out_vals;
+    a.out_ids = d_out_ids;
+    a.counters = reinterpret_cast<uint32_t*>(ws + l.counters);
+    a.chunk_flags = reinterpret_cast<uint32_t*>(ws + l.flags);
+    a.lists = reinterpret_cast<uint64_t*>(ws + l.lists);
+    a.stride = l.stride;
+    a.err = reinterpret_cast<uint32_t*>(ws);
+    a.cfg = StreamCfg{static_cast<uint32_t>(units), chunks, ce, V};
+    a.sa = sa;
+    const dim3 grid(static_cast<uint32_t>(units < slots ? units : slots));
+    if (tma)
+        topk_kernel<true, kSample><<<grid, kNT, kDyn, stream>>>(a);
     else
-        topk_rows_kernel<false, kSample><<<grid, kNT, 0, stream>>>(d_logits, V, k, plan.chunks, plan.chunk_elems,
-                                                                   d_out_vals, d_out_ids, counters, flags, lists,
-                                                                   l.cmax, sa);
+        topk_kernel<false, kSample><<<grid, kNT, 0, stream>>>(a);
     return cudaGetLastError() == cudaSuccess ? SEL_OK : SEL_ECUDA;
 }
 
@@ -516,9 +554,8 @@ size_t topk_ws_bytes(uint32_t rows, uint32_t V, uint32_t k) { return topk_layout
 
 using namespace sel;
 
-extern "C" sel_status sel_topk(const float* d_logits, uint32_t rows, uint32_t V, uint32_t k,
-                               float* d_out_vals, uint32_t* d_out_ids, void* d_ws, size_t ws_bytes,
-                               cudaStream_t stream) {
+extern "C" sel_status sel_topk(const float* d_logits, uint32_t rows, uint32_t V, uint32_t k, float* d_out_vals,
+                               uint32_t* d_out_ids, void* d_ws, size_t ws_bytes, cudaStream_t stream) {
     if (V == 0 || V > SEL_MAX_V || k == 0 || k > V) return SEL_EINVAL;
     if (k > SEL_MAX_K) return SEL_EUNSUPPORTED;
     if (rows == 0) return SEL_OK;
@@ -526,15 +563,13 @@ extern "C" sel_status sel_topk(const float* d_logits, uint32_t rows, uint32_t V,
     if (reinterpret_cast<uintptr_t>(d_logits) % 4 || reinterpret_cast<uintptr_t>(d_out_vals) % 4 ||
         reinterpret_cast<uintptr_t>(d_out_ids) % 4)
         return SEL_EINVAL;
-    if (rows > 0x7fffffffu / kMaxChunks) return SEL_EUNSUPPORTED;
     SampleArgs sa{};
     return launch_topk<false>(d_logits, rows, V, k, d_out_vals, d_out_ids, d_ws, ws_bytes, sa, stream);
 }
 
-extern "C" sel_status sel_sample(const float* d_logits, uint32_t rows, uint32_t V,
-                                 const sel_sample_params* p, const float* d_uniforms,
-                                 uint32_t* d_out_ids, float* d_out_probs, void* d_ws, size_t ws_bytes,
-                                 cudaStream_t stream) {
+extern "C" sel_status sel_sample(const float* d_logits, uint32_t rows, uint32_t V, const sel_sample_params* p,
+                                 const float* d_uniforms, uint32_t* d_out_ids, float* d_out_probs, void* d_ws,
+                                 size_t ws_bytes, cudaStream_t stream) {
     if (!p || V == 0 || V > SEL_MAX_V) return SEL_EINVAL;
     const float T = p->temperature;
     if (!(T >= 0.0f) || !(T < INFINITY)) return SEL_EINVAL;  // rejects NaN too
@@ -551,7 +586,6 @@ extern "C" sel_status sel_sample(const float* d_logits, uint32_t rows, uint32_t 
     if (reinterpret_cast<uintptr_t>(d_logits) % 4 || reinterpret_cast<uintptr_t>(d_uniforms) % 4 ||
         reinterpret_cast<uintptr_t>(d_out_ids) % 4 || reinterpret_cast<uintptr_t>(d_out_probs) % 4)
         return SEL_EINVAL;
-    if (rows > 0x7fffffffu / kMaxChunks) return SEL_EUNSUPPORTED;
     SampleArgs sa{d_uniforms, d_out_probs, T, p->top_p, p->min_p, p->order};
     return launch_topk<true>(d_logits, rows, V, k, nullptr, d_out_ids, d_ws, ws_bytes, sa, stream);
 }

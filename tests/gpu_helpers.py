@@ -2,6 +2,8 @@
 through the C ABI and bring the results back as numpy arrays."""
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
 
@@ -14,10 +16,30 @@ INVALID = 0xFFFFFFFF
 # to this relative error.
 MARGIN = 1e-6
 PROB_RTOL = 1e-5
+# outputs are pre-filled with this, so a row the kernels never wrote shows up
+SENTINEL = -7
+FILL_OUTPUTS = os.environ.get("SEL_TEST_EMPTY_OUTPUTS") is None
+
+
+def _out(shape, dtype):
+    if FILL_OUTPUTS:
+        return torch.full(shape, SENTINEL, dtype=dtype, device=device())
+    return torch.empty(shape, dtype=dtype, device=device())
+
+
+def rows_finished(ws) -> int:
+    """Second header word: rows the top-k/sampling kernel finished."""
+    return int(ws[4:8].cpu().numpy().view(np.uint32)[0])
 
 
 def device():
     return torch.device("cuda:0")
+
+
+def ws_error(ws) -> int:
+    """The workspace's error word (its first 4 bytes): bits the kernels set
+    when a wait timed out or a self-check failed. Must stay 0."""
+    return int(ws[:4].cpu().numpy().view(np.uint32)[0])
 
 
 def to_dev(a: np.ndarray, misalign: bool = False) -> torch.Tensor:
@@ -36,23 +58,28 @@ def to_dev(a: np.ndarray, misalign: bool = False) -> torch.Tensor:
 def argmax(x: np.ndarray, misalign=False, ws=None) -> np.ndarray:
     rows, V = x.shape
     xd = to_dev(x, misalign)
-    out = torch.empty(rows, dtype=torch.int32, device=device())
+    out = torch.full((rows,), SENTINEL, dtype=torch.int32, device=device())
     if ws is None:
         ws = B.workspace(B.SEL_OP_ARGMAX, rows, V, device=device())
     B.sel_argmax(xd, out, ws)
     torch.cuda.synchronize()
+    assert ws_error(ws) == 0, ws_error(ws)
     return B.ids_to_numpy(out)
 
 
 def topk(x: np.ndarray, k: int, misalign=False, ws=None):
     rows, V = x.shape
     xd = to_dev(x, misalign)
-    vals = torch.empty(rows, k, dtype=torch.float32, device=device())
-    ids = torch.empty(rows, k, dtype=torch.int32, device=device())
-    if ws is None:
+    vals = _out((rows, k), torch.float32)
+    ids = _out((rows, k), torch.int32)
+    fresh = ws is None
+    if fresh:
         ws = B.workspace(B.SEL_OP_TOPK, rows, V, k, device=device())
     B.sel_topk(xd, k, vals, ids, ws)
     torch.cuda.synchronize()
+    assert ws_error(ws) == 0, ws_error(ws)
+    if fresh:  # every row finished exactly once
+        assert rows_finished(ws) == rows, (rows_finished(ws), rows)
     return vals.cpu().numpy(), B.ids_to_numpy(ids)
 
 
@@ -61,13 +88,15 @@ def sample(x: np.ndarray, u: np.ndarray, T, top_k, top_p, min_p, temp_last=False
     rows, V = x.shape
     xd = to_dev(x, misalign)
     ud = to_dev(np.asarray(u, dtype=np.float32).reshape(rows))
-    ids = torch.empty(rows, dtype=torch.int32, device=device())
-    probs = torch.empty(rows, dtype=torch.float32, device=device())
+    ids = _out((rows,), torch.int32)
+    probs = _out((rows,), torch.float32)
     ws = B.workspace(B.SEL_OP_SAMPLE, rows, V, top_k, device=device())
     prm = B.SampleParams(T, top_k, top_p, min_p,
                          B.SEL_ORDER_TEMP_LAST if temp_last else B.SEL_ORDER_TEMP_FIRST)
     B.sel_sample(xd, prm, ud, ids, probs, ws)
     torch.cuda.synchronize()
+    assert ws_error(ws) == 0, ws_error(ws)
+    assert rows_finished(ws) == rows, (rows_finished(ws), rows)  # each row exactly once
     return B.ids_to_numpy(ids), probs.cpu().numpy()
 
 
@@ -75,6 +104,7 @@ def assert_sample_matches(got_ids, got_probs, ref, max_mismatch_frac=0.02):
     """ids equal except where the oracle's decision margin is <= MARGIN (and
     such exempt mismatches stay rare); probabilities within PROB_RTOL where
     ids agree."""
+    assert not np.any(got_ids == np.uint32(SENTINEL & 0xFFFFFFFF)), np.nonzero(got_ids == np.uint32(SENTINEL & 0xFFFFFFFF))
     exempt = ref.margin <= MARGIN
     mismatch = got_ids != ref.ids
     bad = mismatch & ~exempt
@@ -96,11 +126,12 @@ def spec(si_target, si_draft, tokens, u_acc, u_fin, T, mode, misalign=False):
     tok = to_dev(np.ascontiguousarray(tokens, dtype=np.uint32).reshape(S, K).view(np.int32))
     ua = None if u_acc is None else to_dev(np.asarray(u_acc, dtype=np.float32).reshape(S, K))
     uf = None if u_fin is None else to_dev(np.asarray(u_fin, dtype=np.float32).reshape(S))
-    acc = torch.empty(S, dtype=torch.int32, device=device())
-    emi = torch.empty(S, K + 1, dtype=torch.int32, device=device())
+    acc = torch.full((S,), SENTINEL, dtype=torch.int32, device=device())
+    emi = torch.full((S, K + 1), SENTINEL, dtype=torch.int32, device=device())
     ws = B.workspace(B.SEL_OP_SPEC, S, V, K, device=device())
     B.spec_accept(t, d, tok, B.SpecParams(T, mode), ua, uf, acc, emi, ws)
     torch.cuda.synchronize()
+    assert ws_error(ws) == 0, ws_error(ws)
     return B.ids_to_numpy(acc), B.ids_to_numpy(emi)
 
 

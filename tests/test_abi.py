@@ -55,7 +55,7 @@ def test_workspace_sizes_are_host_only_and_monotone(lib):
     a = B.sel_workspace_bytes(B.SEL_OP_ARGMAX, 49, 248_320)
     assert a > 0 and a % 8 == 0
     assert B.sel_workspace_bytes(B.SEL_OP_ARGMAX, 98, 248_320) > a
-    assert B.sel_workspace_bytes(B.SEL_OP_ARGMAX, 4, 1000) == 0      # one block per row
+    assert 256 <= B.sel_workspace_bytes(B.SEL_OP_ARGMAX, 4, 1000) <= 4096  # header + counters
     t20 = B.sel_workspace_bytes(B.SEL_OP_TOPK, 49, 248_320, 20)
     t84 = B.sel_workspace_bytes(B.SEL_OP_TOPK, 49, 248_320, 84)
     assert 0 < t20 < t84
