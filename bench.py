@@ -1,0 +1,436 @@
+"""Benchmark of the decode-step token-selection path on GB300.
+
+One step takes a 49 x 248,320 fp32 verify batch (Gumbel-perturbed Zipf(1.1)
+log-probabilities, seed 2) through the whole selection path via the C ABI:
+  sel_argmax, sel_topk (k = 20), sel_sample (T 0.7, top_k 40, top_p 0.9,
+  min_p 0.05, one uniform per row), and spec_accept in both rules over the
+  same 49 rows read as 7 sequences x (6 drafts + 1 bonus) target rows, with
+  draft rows = target + N(0, 0.25) and draft tokens drawn from q.
+value = verify-batch rows taken through that path per second (49 per step
+and rank). Inputs are resident in HBM before the timed region; every launch
+reads a copy of the batch that no launch has touched within the previous
+>= 243 MB of traffic (more than the 129 MB L2), so each read comes from HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+With --impl reference the CPU oracle (the plain, double-precision C
+implementation the tests check against) runs a bounded sample of the same
+step on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+ROWS, V = 49, 248_320
+K_TOPK = 20
+SPEC_S, SPEC_K = 7, 6
+POLICY = dict(temperature=0.7, top_k=40, top_p=0.9, min_p=0.05)
+ROW_BYTES = V * 4
+WORKLOAD = "batched verify selection 49 x 248,320 fp32"
+METRIC = "logits rows/s and achieved HBM GB/s (% of GB300 peak) at V=248k, rows=1-49"
+N_COPIES = 6          # rotating copies of the batch (6 x 48.7 MB)
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def build_inputs():
+    from sampling_row_fp32_gb300 import synth
+    x, _ = synth.workload_verify_batch(ROWS, V)
+    si = synth.spec_inputs(S=SPEC_S, K=SPEC_K, V=V, target=x.reshape(SPEC_S, SPEC_K + 1, V))
+    u = synth.uniforms(4, ROWS)
+    return x, si, u
+
+
+def gpu_arm(args, rank, world, local_rank):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from sampling_row_fp32_gb300 import binding as B
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    x, si, u = build_inputs()
+
+    # resident inputs: rotating copies of the batch and of the draft rows
+    xs = [torch.from_numpy(x).to(dev) for _ in range(N_COPIES)]
+    drafts = [torch.from_numpy(si.draft).to(dev) for _ in range(2)]
+    tok = torch.from_numpy(si.draft_tokens.view(np.int32)).to(dev)
+    ua = torch.from_numpy(si.u_acc).to(dev)
+    uf = torch.from_numpy(si.u_fin).to(dev)
+    ud = torch.from_numpy(u).to(dev)
+    ids = torch.empty(ROWS, dtype=torch.int32, device=dev)
+    tv = torch.empty(ROWS, K_TOPK, dtype=torch.float32, device=dev)
+    ti = torch.empty(ROWS, K_TOPK, dtype=torch.int32, device=dev)
+    sid = torch.empty(ROWS, dtype=torch.int32, device=dev)
+    sp = torch.empty(ROWS, dtype=torch.float32, device=dev)
+    acc = torch.empty(SPEC_S, dtype=torch.int32, device=dev)
+    emi = torch.empty(SPEC_S, SPEC_K + 1, dtype=torch.int32, device=dev)
+    acc2 = torch.empty(SPEC_S, dtype=torch.int32, device=dev)
+    emi2 = torch.empty(SPEC_S, SPEC_K + 1, dtype=torch.int32, device=dev)
+    ws_a = B.workspace(B.SEL_OP_ARGMAX, ROWS, V, device=dev)
+    ws_t = B.workspace(B.SEL_OP_TOPK, ROWS, V, K_TOPK, device=dev)
+    ws_s = B.workspace(B.SEL_OP_SAMPLE, ROWS, V, POLICY["top_k"], device=dev)
+    ws_r = B.workspace(B.SEL_OP_SPEC, SPEC_S, V, SPEC_K, device=dev)
+    ws_g = B.workspace(B.SEL_OP_SPEC, SPEC_S, V, SPEC_K, device=dev)
+    prm = B.SampleParams(POLICY["temperature"], POLICY["top_k"], POLICY["top_p"], POLICY["min_p"],
+                         B.SEL_ORDER_TEMP_FIRST)
+    rej = B.SpecParams(1.0, B.SPEC_MODE_REJECTION)
+    arg = B.SpecParams(1.0, B.SPEC_MODE_ARGMAX)
+    stream = torch.cuda.current_stream()
+    OPS = ["argmax", "topk", "sample", "spec_rejection", "spec_argmax"]
+    # the copy each op of step s reads: consecutive reads walk the N_COPIES
+    # copies in turn, so a copy is read again only after 5 others (243 MB)
+    def copy_for(step, op):
+        return xs[(5 * step + op) % N_COPIES]
+
+    def target_view(t):
+        return t.view(SPEC_S, SPEC_K + 1, V)
+
+    def run_op(step, op):
+        if op == 0:
+            B.sel_argmax(copy_for(step, 0), ids, ws_a, stream)
+        elif op == 1:
+            B.sel_topk(copy_for(step, 1), K_TOPK, tv, ti, ws_t, stream)
+        elif op == 2:
+            B.sel_sample(copy_for(step, 2), prm, ud, sid, sp, ws_s, stream)
+        elif op == 3:
+            B.spec_accept(target_view(copy_for(step, 3)), drafts[step % 2], tok, rej, ua, uf, acc, emi,
+                          ws_r, stream)
+        else:
+            B.spec_accept(target_view(copy_for(step, 4)), None, tok, arg, None, None, acc2, emi2, ws_g,
+                          stream)
+
+    launches_per_step = 6  # spec rejection is two kernels
+    bytes_per_op = [ROWS * ROW_BYTES, ROWS * ROW_BYTES, ROWS * ROW_BYTES,
+                    None, ROWS * ROW_BYTES]
+
+    # warm-up
+    for s in range(args.warmup):
+        for op in range(5):
+            run_op(s, op)
+    torch.cuda.synchronize()
+    # residual re-read of the rejection rule: the rejecting position's target
+    # and draft rows, or the bonus row when all positions accept
+    n_acc = acc.cpu().numpy()
+    resid_rows = int(sum(2 if a < SPEC_K else 1 for a in n_acc))
+    bytes_per_op[3] = (SPEC_S * (2 * SPEC_K + 1) + resid_rows) * ROW_BYTES
+
+    # timed region: events bracket every op on the launching stream
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.25)  # let the sampler start
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        e = evs[s]
+        e[0].record(stream)
+        for op in range(5):
+            run_op(args.warmup + s, op)
+            e[op + 1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    # keep the same load running briefly so the clock sampler sees it even
+    # when the timed region is shorter than its period
+    tail_until = time.time() + 0.6
+    s = args.warmup + args.steps
+    while time.time() < tail_until:
+        for op in range(5):
+            run_op(s, op)
+        s += 1
+        torch.cuda.synchronize()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    per_op_us = [statistics.mean(evs[s][op].elapsed_time(evs[s][op + 1]) for s in range(args.steps)) * 1e3
+                 for op in range(5)]
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # end to end through the same C-ABI calls with host buffers: pinned input
+    # copied to the device, the five calls, results copied back, every step
+    e2e = e2e_leg(args, B, dev, x, si, u, prm, rej, arg, ws_a, ws_t, ws_s, ws_r, ws_g)
+
+    peak, peak_kind = measured_peak()
+    step_s = total_ms / 1e3 / args.steps
+    rows_per_s = ROWS * world / step_s
+    step_bytes = sum(bytes_per_op)
+    dom = int(np.argmax(per_op_us))
+    dom_gbs = bytes_per_op[dom] / (per_op_us[dom] * 1e-6) / 1e9
+    ops = {OPS[i]: {"us": round(per_op_us[i], 3), "bytes": bytes_per_op[i],
+                    "gbs": round(bytes_per_op[i] / (per_op_us[i] * 1e-6) / 1e9, 1),
+                    "frac_of_peak": round(bytes_per_op[i] / (per_op_us[i] * 1e-6) / 1e9 / peak, 4)}
+           for i in range(5)}
+    traffic = load_traffic(OPS[dom])
+    line = {
+        "metric": METRIC,
+        "value": round(rows_per_s, 1),
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded Gumbel-perturbed Zipf(1.1) logits; no dataset)",
+        "config": {"workload": WORKLOAD, "rows": ROWS, "V": V, "topk_k": K_TOPK,
+                   "sample": POLICY, "spec": {"sequences": SPEC_S, "drafts": SPEC_K, "T": 1.0,
+                                              "rules": ["rejection", "argmax"]},
+                   "l2": f"inputs rotate over {N_COPIES} resident copies of the batch; each launch "
+                         "reads a copy untouched for >= 243 MB of traffic (L2 is 129 MB)",
+                   "parallelism": f"replicas x{world} (independent rows)"},
+        "step_gbs": round(step_bytes / step_s / 1e9, 1),
+        "ops": ops,
+        "roofline": {"bound": "hbm", "kernel": OPS[dom], "achieved": round(dom_gbs, 1), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
+                     "traffic": traffic},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    return line
+
+
+def load_traffic(op_name):
+    """dram bytes per launch of the op's kernels from the committed ncu
+    summary, if one exists for the current sources (else null)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        return t.get(op_name)
+    except Exception:
+        return None
+
+
+def e2e_leg(args, B, dev, x, si, u, prm, rej, arg, ws_a, ws_t, ws_s, ws_r, ws_g):
+    import torch
+    hx = torch.from_numpy(x).pin_memory()
+    hd = torch.from_numpy(si.draft).pin_memory()
+    htok = torch.from_numpy(si.draft_tokens.view(np.int32)).pin_memory()
+    hua = torch.from_numpy(si.u_acc).pin_memory()
+    huf = torch.from_numpy(si.u_fin).pin_memory()
+    hu = torch.from_numpy(u).pin_memory()
+    dx = torch.empty(ROWS, V, device=dev)
+    dd = torch.empty_like(hd, device=dev)
+    dtok = torch.empty_like(htok, device=dev)
+    dua = torch.empty_like(hua, device=dev)
+    duf = torch.empty_like(huf, device=dev)
+    du = torch.empty_like(hu, device=dev)
+    outs_d = [torch.empty(ROWS, dtype=torch.int32, device=dev), torch.empty(ROWS, K_TOPK, device=dev),
+              torch.empty(ROWS, K_TOPK, dtype=torch.int32, device=dev),
+              torch.empty(ROWS, dtype=torch.int32, device=dev), torch.empty(ROWS, device=dev),
+              torch.empty(SPEC_S, dtype=torch.int32, device=dev),
+              torch.empty(SPEC_S, SPEC_K + 1, dtype=torch.int32, device=dev),
+              torch.empty(SPEC_S, dtype=torch.int32, device=dev),
+              torch.empty(SPEC_S, SPEC_K + 1, dtype=torch.int32, device=dev)]
+    outs_h = [torch.empty_like(o, device="cpu").pin_memory() for o in outs_d]
+    stream = torch.cuda.current_stream()
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hd, htok, hua, huf, hu))
+    d2h = sum(t.numel() * t.element_size() for t in outs_d)
+
+    def step():
+        for h, d in ((hx, dx), (hd, dd), (htok, dtok), (hua, dua), (huf, duf), (hu, du)):
+            d.copy_(h, non_blocking=True)
+        B.sel_argmax(dx, outs_d[0], ws_a, stream)
+        B.sel_topk(dx, K_TOPK, outs_d[1], outs_d[2], ws_t, stream)
+        B.sel_sample(dx, prm, du, outs_d[3], outs_d[4], ws_s, stream)
+        tv = dx.view(SPEC_S, SPEC_K + 1, V)
+        B.spec_accept(tv, dd, dtok, rej, dua, duf, outs_d[5], outs_d[6], ws_r, stream)
+        B.spec_accept(tv, None, dtok, arg, None, None, outs_d[7], outs_d[8], ws_g, stream)
+        for d, h in zip(outs_d, outs_h):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    n = max(args.steps, 1)
+    a.record(stream)
+    for _ in range(n):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / n
+    return {"value": round(ROWS / (ms / 1e3), 1), "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms, 5)}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle on a bounded sample of the step
+# ---------------------------------------------------------------------------
+
+REF_ROWS = 7  # one spec sequence (6 drafts + bonus) and 7 rows for the other ops
+
+
+def oracle_step(orc, x, si, u):
+    xs = x[:REF_ROWS]
+    orc.argmax(xs)
+    orc.topk(xs, K_TOPK)
+    orc.sample(xs, u[:REF_ROWS], POLICY["temperature"], POLICY["top_k"], POLICY["top_p"], POLICY["min_p"])
+    orc.spec_accept(si.target[:1], si.draft[:1], si.draft_tokens[:1], 1.0, 0, si.u_acc[:1], si.u_fin[:1])
+    orc.spec_accept(si.target[:1], None, si.draft_tokens[:1], 1.0, 1)
+
+
+def cpu_baseline(steps=20):
+    import oracle
+    orc = oracle.default()
+    x, si, u = build_inputs()
+    oracle_step(orc, x, si, u)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle_step(orc, x, si, u)
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": round(REF_ROWS / dt, 3), "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": f"{REF_ROWS} of the {ROWS} rows per step (argmax, top-k, sampling) and one "
+                      f"spec sequence ({SPEC_K} drafts) in both rules; single-threaded C oracle, "
+                      f"{steps} timed steps"}
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    orc = oracle.default()
+    x, si, u = build_inputs()
+    for _ in range(args.warmup):
+        oracle_step(orc, x, si, u)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(orc, x, si, u)
+    dt = time.perf_counter() - t0
+    v = REF_ROWS * args.steps / dt
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": "rows/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded Gumbel-perturbed Zipf(1.1) logits; no dataset)",
+            "config": {"workload": WORKLOAD, "rows": ROWS, "V": V},
+            "cpu_baseline": {"value": round(v, 3), "unit": "rows/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{REF_ROWS} of {ROWS} rows and one spec sequence per step"},
+            "e2e": {"value": round(v, 3), "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+
+    if args.impl == "reference":
+        line = reference_arm(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line = gpu_arm(args, rank, world, local_rank)
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline() if world == 1 else None
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

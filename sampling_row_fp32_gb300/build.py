@@ -50,16 +50,21 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: tuple[str, ...] = ()) -> str:
-    """Compile and link libsel.so unless it is newer than every source."""
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, extra_flags: tuple[str, ...] = (),
+          out: str | None = None) -> str:
+    """Compile and link libsel.so unless it is newer than every source.
+    `out` (with `extra_flags`, e.g. -D tuning overrides) builds a separate
+    copy at that path instead, in its own object directory."""
+    lib = out or LIB
+    if not force and out is None and up_to_date():
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    objdir = BUILD if out is None else os.path.splitext(out)[0] + "_obj"
+    os.makedirs(objdir, exist_ok=True)
     cc = nvcc()
     objs = []
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(objdir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -70,18 +75,18 @@ def build(force: bool = False, verbose: bool = False, extra_flags: tuple[str, ..
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, sources()))
-    fd, tmp = tempfile.mkstemp(suffix=".so", dir=BUILD)
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=objdir)
     os.close(fd)
     try:
         cmd = [cc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
+        os.replace(tmp, lib)
     finally:
         if os.path.exists(tmp):
             os.unlink(tmp)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
