@@ -234,6 +234,29 @@ sel_status spec_accept(const float *d_target, const float *d_draft,
                        uint32_t *d_accepted, uint32_t *d_emitted, void *d_ws,
                        size_t ws_bytes, cudaStream_t stream);
 
+/*
+ * sel_argmax_noalloc -- sel_argmax for callers that cannot allocate device
+ * memory (a runtime that plans all device memory up front, or a plugin
+ * interface that passes a stream but no workspace). The pages have no
+ * counterpart: it is the same per-row argmax as sel_argmax, computed by the
+ * same kernel, with its scratch taken from an array of
+ * SEL_NOALLOC_SCRATCH_BYTES that the library reserves on every GPU it is
+ * loaded on and keeps until the process exits.
+ *
+ *   d_logits, rows, V, d_out_ids  as for sel_argmax
+ * Requests whose workspace would not fit (sel_workspace_bytes(SEL_OP_ARGMAX,
+ * rows, V, 0) > SEL_NOALLOC_SCRATCH_BYTES, e.g. more than 538 rows at
+ * V = 248,320) return SEL_EWORKSPACE. The call allocates and frees nothing;
+ * it zeroes the array's counters with cudaMemsetAsync on `stream` and
+ * launches on `stream`. The first call on a device looks the array's device
+ * address up (cudaGetSymbolAddress), so make that first call before any
+ * stream capture. Every call on a device shares the one array: calls that
+ * may overlap on the GPU (different streams without ordering) race.
+ */
+#define SEL_NOALLOC_SCRATCH_BYTES (1u << 20)
+sel_status sel_argmax_noalloc(const float *d_logits, uint32_t rows, uint32_t V,
+                              uint32_t *d_out_ids, cudaStream_t stream);
+
 /* Static description of a status code. */
 const char *sel_status_string(sel_status status);
 

@@ -26,7 +26,8 @@ SEL_ORDER_TEMP_FIRST, SEL_ORDER_TEMP_LAST = 0, 1
 SPEC_MODE_REJECTION, SPEC_MODE_ARGMAX = 0, 1
 
 EXPORTED = ("sel_workspace_bytes", "sel_workspace_init", "sel_argmax", "sel_topk",
-            "sel_sample", "spec_accept", "sel_status_string")
+            "sel_sample", "spec_accept", "sel_status_string", "sel_argmax_noalloc")
+SEL_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 
 class SelError(RuntimeError):
@@ -81,6 +82,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.spec_accept.argtypes = [_vp, _vp, _vp, _u32, _u32, _u32, ctypes.POINTER(SpecParams),
                                 _vp, _vp, _vp, _vp, _vp, _sz, _vp]
     lib.spec_accept.restype = ctypes.c_int
+    lib.sel_argmax_noalloc.argtypes = [_vp, _u32, _u32, _vp, _vp]
+    lib.sel_argmax_noalloc.restype = ctypes.c_int
     lib.sel_status_string.argtypes = [ctypes.c_int]
     lib.sel_status_string.restype = ctypes.c_char_p
     if path is None:
@@ -149,6 +152,15 @@ def sel_argmax(logits, out_ids, ws=None, stream=None) -> None:
     rows, V = logits.shape
     _check(load().sel_argmax(_ptr(logits), rows, V, _ptr(out_ids), _ptr(ws), _nbytes(ws),
                              _stream(stream)), "sel_argmax")
+
+
+def sel_argmax_noalloc(logits, out_ids, stream=None) -> None:
+    """sel_argmax on the library's reserved scratch (no workspace argument)."""
+    _check_f32(logits, "logits")
+    _check_ids(out_ids, "out_ids")
+    rows, V = logits.shape
+    _check(load().sel_argmax_noalloc(_ptr(logits), rows, V, _ptr(out_ids), _stream(stream)),
+           "sel_argmax_noalloc")
 
 
 def sel_topk(logits, k: int, out_vals, out_ids, ws=None, stream=None) -> None:
