@@ -17,16 +17,30 @@
 // the row; the block that publishes a row's last segment merges that row's
 // partials with one warp and writes the id. (value desc, id asc) is a total
 // order, so the merge order cannot change the result.
+#include <cfloat>
+
 #include "sel_plan.h"
 #include "sel_stream.cuh"
 
 namespace sel {
 namespace {
 
-constexpr int kNT = 256;                        // threads per block
-constexpr int kVPT = 8;                         // float4 per thread per unit
-constexpr int kStages = 4;                      // units in flight per block
-constexpr uint32_t kUnitMax = 4u * kNT * kVPT;  // 8,192 elements (32 KB)
+#ifndef SEL_ARGMAX_NT
+#define SEL_ARGMAX_NT 256
+#endif
+#ifndef SEL_ARGMAX_VPT
+#define SEL_ARGMAX_VPT 4
+#endif
+#ifndef SEL_ARGMAX_STAGES
+#define SEL_ARGMAX_STAGES 4
+#endif
+#ifndef SEL_ARGMAX_MINB
+#define SEL_ARGMAX_MINB 3
+#endif
+constexpr int kNT = SEL_ARGMAX_NT;              // threads per block
+constexpr int kVPT = SEL_ARGMAX_VPT;            // float4 per thread per unit
+constexpr int kStages = SEL_ARGMAX_STAGES;      // units in flight per block
+constexpr uint32_t kUnitMax = 4u * kNT * kVPT;  // elements per unit (16 KB)
 constexpr uint32_t kUnitMin = 1024u;
 constexpr uint32_t kNoIdx = 0x7fffffffu;        // "no element": loses every tie
 constexpr uint32_t kNonfiniteBit = 0x80000000u;
@@ -61,7 +75,7 @@ struct ArgmaxArgs {
 };
 
 template <bool kTma>
-__global__ void __launch_bounds__(kNT) argmax_kernel(ArgmaxArgs a) {
+__global__ void __launch_bounds__(kNT, SEL_ARGMAX_MINB) argmax_kernel(ArgmaxArgs a) {
     extern __shared__ float4 stages[];
     __shared__ uint64_t full[kStages];
     __shared__ float s_v[kNT / 32];
@@ -72,10 +86,15 @@ __global__ void __launch_bounds__(kNT) argmax_kernel(ArgmaxArgs a) {
     const uint32_t V = a.cfg.V;
     auto row_ptr = [&](uint32_t r) { return a.logits + static_cast<size_t>(r) * V; };
 
-    // running (value, id) and finite check of this thread over the segment
-    float best = -INFINITY;  // loses to every finite logit (a row with -inf fails closed)
-    uint32_t bidx = kNoIdx;
-    uint32_t absmax = 0;     // max |bits| over real elements: >= Inf bits means NaN/Inf
+    // Four independent (value, quad start) chains per thread, one per lane of
+    // the float4, so the compare-select chains overlap; the id is quad start
+    // + lane. Padding is -FLT_MAX at an id past every real one, so it never
+    // wins: a real -FLT_MAX ties it and keeps its lower id, and -inf or NaN
+    // fail the row closed anyway. nfacc = sum of x * 0 stays 0 unless some x
+    // is +-Inf or NaN.
+    float best[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    uint32_t bbase[4] = {kNoIdx, kNoIdx, kNoIdx, kNoIdx};
+    float nfacc = 0.0f;
 
     auto accum = [&](const Unit& t, float4 (&q)[kVPT]) {
 #pragma unroll
@@ -84,24 +103,28 @@ __global__ void __launch_bounds__(kNT) argmax_kernel(ArgmaxArgs a) {
             const float f[4] = {q[s].x, q[s].y, q[s].z, q[s].w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                if (e + j < t.hi) {
-                    absmax = max(absmax, __float_as_uint(f[j]) & 0x7fffffffu);
-                    if (f[j] > best) {  // ids rise along the walk: '>' keeps the lowest
-                        best = f[j];
-                        bidx = e + j;
-                    }
+                nfacc = __fmaf_rn(f[j], 0.0f, nfacc);
+                if (f[j] > best[j]) {  // ids rise along each chain: '>' keeps the lowest
+                    best[j] = f[j];
+                    bbase[j] = e;
                 }
             }
         }
     };
 
     auto flush = [&](const Segment& g) {
-        uint32_t nf = absmax >= 0x7f800000u ? kNonfiniteBit : 0u;
-        float v = nf ? -INFINITY : best;
-        uint32_t i = nf ? kNoIdx : bidx;
-        best = -INFINITY;
-        bidx = kNoIdx;
-        absmax = 0;
+        uint32_t nf = (nfacc == 0.0f) ? 0u : kNonfiniteBit;
+        float v = -INFINITY;
+        uint32_t i = kNoIdx;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t id = bbase[j] == kNoIdx ? kNoIdx : bbase[j] + j;
+            if (beats(best[j], id, v, i)) { v = best[j]; i = id; }
+            best[j] = -INFINITY;
+            bbase[j] = kNoIdx;
+        }
+        nfacc = 0.0f;
+        if (nf) { v = -INFINITY; i = kNoIdx; }
         warp_argmax(v, i, nf);
         if (lane == 0) { s_v[warp] = v; s_i[warp] = i; s_nf[warp] = nf; }
         __syncthreads();
@@ -141,7 +164,7 @@ __global__ void __launch_bounds__(kNT) argmax_kernel(ArgmaxArgs a) {
         __syncthreads();
     };
 
-    stream_segments<kTma, kNT, kVPT, kStages>(a.cfg, row_ptr, accum, flush, stages, full, a.err);
+    stream_segments<kTma, kNT, kVPT, kStages>(a.cfg, row_ptr, accum, flush, stages, full, a.err, -FLT_MAX);
 }
 
 struct ArgmaxLayout {

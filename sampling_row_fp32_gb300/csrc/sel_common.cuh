@@ -131,16 +131,18 @@ __device__ __forceinline__ T warp_sort_desc(T v) {
 // Results one block publishes for another (per-chunk partials, candidate
 // lists, flags) are read with strong relaxed loads at GPU scope, after a
 // fence in the reading thread; the publishing threads fence before the
-// arrival counter is bumped.
+// arrival counter is bumped. The loads are volatile asm (kept in order and
+// behind the fence, which is volatile too) without a memory clobber, so
+// their consumers can wait while later loads are already in flight.
 
 __device__ __forceinline__ uint64_t ld_gpu_u64(const void* p) {
     unsigned long long v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p));
     return v;
 }
 __device__ __forceinline__ uint32_t ld_gpu_u32(const void* p) {
     uint32_t v;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p));
     return v;
 }
 __device__ __forceinline__ float ld_gpu_f32(const void* p) { return __uint_as_float(ld_gpu_u32(p)); }

@@ -259,9 +259,9 @@ __global__ void __launch_bounds__(kNT) spec_phase1_kernel(SpecArgs a) {
                 const uint32_t e = t.lo + 4u * (tid + kNT * sl);
                 const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) w[sl][j] = e + j < t.hi ? expf((f[j] - mn) * invT) : 0.0f;
+                for (int j = 0; j < 4; ++j) w[sl][j] = e + j < t.hi ? __expf((f[j] - mn) * invT) : 0.0f;
             }
-            const float scale = m > -INFINITY ? expf((m - mn) * invT) : 0.0f;
+            const float scale = m > -INFINITY ? __expf((m - mn) * invT) : 0.0f;
             sum = sum * scale + pairwise32(w);
         }
         m = mn;
@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(kNT) spec_phase1_kernel(SpecArgs a) {
         // the sums, rescaled to the segment's max, summed in double
         double bs = 0.0;
         if (kRej) {
-            double mine = (!nf && m > -INFINITY) ? static_cast<double>(sum) * static_cast<double>(expf((m - bm) * invT))
+            double mine = (!nf && m > -INFINITY) ? static_cast<double>(sum) * static_cast<double>(__expf((m - bm) * invT))
                                                  : 0.0;
             mine = warp_sum_d(mine);
             if (lane == 0) s_s[warp] = mine;
@@ -369,8 +369,8 @@ __device__ __forceinline__ void quad_weights(const float4& xp, const float4& xq,
     const float fq[4] = {xq.x, xq.y, xq.z, xq.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const float p = expf((fp[j] - pm) * invT) * pinv;
-        const float q = residual ? expf((fq[j] - qm) * invT) * qinv : 0.0f;
+        const float p = __expf((fp[j] - pm) * invT) * pinv;
+        const float q = residual ? __expf((fq[j] - qm) * invT) * qinv : 0.0f;
         pw[j] = p;
         rw[j] = residual ? fmaxf(p - q, 0.0f) : p;
     }
@@ -395,6 +395,9 @@ __global__ void __launch_bounds__(kNT) spec_draw_kernel(DrawArgs a) {
     __shared__ bool s_last;
     __shared__ uint32_t s_pick;
     __shared__ int s_lastpos;
+    __shared__ bool s_use_p;
+    __shared__ uint32_t s_cstar;
+    __shared__ double s_before, s_target;
 
     const uint32_t chunks = a.chunks;
     const uint32_t s = blockIdx.x / chunks;
@@ -452,27 +455,59 @@ __global__ void __launch_bounds__(kNT) spec_draw_kernel(DrawArgs a) {
     if (!s_last) return;
     __threadfence();  // order this thread's reads after the arrivals it saw
 
-    // last block: locate the chunk, then the element, where u * total falls
+    // last block: locate the chunk, then the element, where u * total falls.
+    // Warp 0 walks the chunk sums 32 at a time in chunk order (fixed-order
+    // scans, so the result does not depend on timing).
     const DrawPart* parts = a.parts + static_cast<size_t>(s) * a.cmax;
-    double R = 0.0, P = 0.0;
-    for (uint32_t c = 0; c < chunks; ++c) { R += ld_gpu_f64(&parts[c].r); P += ld_gpu_f64(&parts[c].p); }
-    const bool use_p = !(R > 0.0);  // residual empty by rounding: draw from p
-    const double total = use_p ? P : R;
-    const double target = static_cast<double>(a.u_fin[s]) * total;
-    uint32_t cstar = chunks;
-    double before = 0.0, acc = 0.0;
-    uint32_t last_pos_chunk = 0;
-    for (uint32_t c = 0; c < chunks; ++c) {
-        const double t = use_p ? ld_gpu_f64(&parts[c].p) : ld_gpu_f64(&parts[c].r);
-        if (t > 0.0) last_pos_chunk = c;
-        if (cstar == chunks && target < acc + t) { cstar = c; before = acc; }
-        acc += t;
+    if (warp == 0) {
+        double R = 0.0, P = 0.0;
+        for (uint32_t c0 = 0; c0 < chunks; c0 += 32) {
+            const uint32_t c = c0 + lane;
+            double r = c < chunks ? ld_gpu_f64(&parts[c].r) : 0.0;
+            double p = c < chunks ? ld_gpu_f64(&parts[c].p) : 0.0;
+            r = warp_incl_scan_d(r);
+            p = warp_incl_scan_d(p);
+            R += __shfl_sync(kFull, r, 31);
+            P += __shfl_sync(kFull, p, 31);
+        }
+        const bool use_p = !(R > 0.0);  // residual empty by rounding: draw from p
+        const double total = use_p ? P : R;
+        const double target = static_cast<double>(a.u_fin[s]) * total;
+        uint32_t cstar = chunks, last_pos_chunk = 0;
+        double before = 0.0, acc = 0.0, before_last = 0.0;
+        for (uint32_t c0 = 0; c0 < chunks && cstar == chunks; c0 += 32) {
+            const uint32_t c = c0 + lane;
+            const double t = c < chunks ? (use_p ? ld_gpu_f64(&parts[c].p) : ld_gpu_f64(&parts[c].r)) : 0.0;
+            const double incl = warp_incl_scan_d(t) + acc;
+            const uint32_t pos = __ballot_sync(kFull, c < chunks && t > 0.0);
+            if (pos) {
+                const int l = 31 - __clz(pos);
+                last_pos_chunk = c0 + l;
+                before_last = __shfl_sync(kFull, incl - t, l);
+            }
+            const uint32_t hit = __ballot_sync(kFull, c < chunks && target < incl);
+            if (hit) {
+                const int l = __ffs(hit) - 1;
+                cstar = c0 + l;
+                before = __shfl_sync(kFull, incl - t, l);
+            }
+            acc = __shfl_sync(kFull, incl, 31);
+        }
+        if (cstar == chunks) {  // rounding: take the last chunk with mass
+            cstar = last_pos_chunk;
+            before = before_last;
+        }
+        if (lane == 0) {
+            s_use_p = use_p;
+            s_cstar = cstar;
+            s_before = before;
+            s_target = target;
+        }
     }
-    if (cstar == chunks) {  // rounding: take the last chunk with mass
-        cstar = last_pos_chunk;
-        before = 0.0;
-        for (uint32_t c = 0; c < cstar; ++c) before += use_p ? ld_gpu_f64(&parts[c].p) : ld_gpu_f64(&parts[c].r);
-    }
+    __syncthreads();
+    const bool use_p = s_use_p;
+    const uint32_t cstar = s_cstar;
+    const double before = s_before, target = s_target;
     if (tid == 0) { s_pick = kNoIdx; s_lastpos = -1; }
     __syncthreads();
 

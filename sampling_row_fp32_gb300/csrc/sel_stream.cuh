@@ -127,7 +127,7 @@ constexpr size_t stage_bytes() {
 }
 
 // Stream this block's contiguous units. For each unit, `accum(unit, q)`
-// runs with q[s] holding elements lo + 4 * (tid + kNT * s) + {0..3} (zeros
+// runs with q[s] holding elements lo + 4 * (tid + kNT * s) + {0..3} (`fill`
 // past hi); whenever the row changes, and after the last unit,
 // `flush(segment)` closes this block's segment of the finished row.
 // Block-collective: every thread calls with the same arguments. `stages` is
@@ -135,7 +135,8 @@ constexpr size_t stage_bytes() {
 // workspace error word.
 template <bool kTma, int kNT, int kVPT, int kStages, class RowPtr, class Accum, class Flush>
 __device__ __forceinline__ void stream_segments(const StreamCfg& cfg, RowPtr row_ptr, Accum&& accum,
-                                                Flush&& flush, float4* stages, uint64_t* full, uint32_t* err) {
+                                                Flush&& flush, float4* stages, uint64_t* full, uint32_t* err,
+                                                float fill = 0.0f) {
     const uint32_t tid = threadIdx.x;
     const uint32_t u0 = range_begin(blockIdx.x, cfg.units, gridDim.x);
     const uint32_t u1 = range_begin(blockIdx.x + 1, cfg.units, gridDim.x);
@@ -186,14 +187,14 @@ __device__ __forceinline__ void stream_segments(const StreamCfg& cfg, RowPtr row
 #pragma unroll
             for (int s = 0; s < kVPT; ++s) {
                 const uint32_t k = tid + kNT * s;
-                q[s] = k < n4 ? sp[k] : make_float4(0.f, 0.f, 0.f, 0.f);
+                q[s] = k < n4 ? sp[k] : make_float4(fill, fill, fill, fill);
             }
             __syncthreads();  // the stage is copied out: refill it
             if (tid == 0 && i + kStages < n_my) issue(i + kStages);
         } else {
             const float* x = row_ptr(t.row);
 #pragma unroll
-            for (int s = 0; s < kVPT; ++s) q[s] = ld_quad<false>(x, t.lo + 4u * (tid + kNT * s), t.hi, 0.0f);
+            for (int s = 0; s < kVPT; ++s) q[s] = ld_quad<false>(x, t.lo + 4u * (tid + kNT * s), t.hi, fill);
         }
         accum(t, q);
     }

@@ -34,6 +34,8 @@
 //     every entry, and the survivors are selected exactly. Sampling then
 //     runs its softmax, top-p, min-p and inverse-CDF draw on the k
 //     candidates in one warp.
+#include <cfloat>
+
 #include "sel_plan.h"
 #include "sel_stream.cuh"
 
@@ -149,6 +151,30 @@ __device__ __noinline__ void reduce_buffer(TopkShared& s, uint32_t k) {
         if (kk == k) s.tau_key = cand_key(s.sorted[k - 1]);
     }
     __syncthreads();
+}
+
+// A chunk whose survivors overflow the buffer (adversarial rows such as
+// all-equal values): append it again 1,024 elements at a time, re-read from
+// global memory, selecting the buffer down to k in between. Later slots hold
+// higher ids, so an equal key cannot displace the buffer's k-th candidate.
+// Exact for any input; block-collective; kept out of line.
+template <bool kVec>
+__device__ __noinline__ void overflow_chunk(TopkShared& s, const float* x, uint32_t lo, uint32_t hi, uint32_t k,
+                                            uint32_t tau) {
+    const uint32_t tid = threadIdx.x;
+    for (uint32_t base = lo; base < hi; base += 4u * kNT) {
+        if (s.count + 4u * kNT > kCap) reduce_buffer(s, k);
+        const uint32_t thr = max(max(tau, s.tau_key + 1u), 1u);
+        const uint32_t e = base + 4u * tid;
+        const float4 q = ld_quad<kVec>(x, e, hi, 0.0f);
+        const float f[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t kk = e + j < hi ? f2key(f[j]) : 0u;
+            warp_append(s, kk >= thr, make_cand(kk, e + j));
+        }
+        __syncthreads();
+    }
 }
 
 // Sampling epilogue on the sorted candidates s.sorted[0..n): one warp.
@@ -363,78 +389,75 @@ __global__ void __launch_bounds__(kNT, 2) topk_kernel(TopkArgs a) {
     const uint32_t V = a.cfg.V, k = a.k;
     auto row_ptr = [&](uint32_t r) { return a.logits + static_cast<size_t>(r) * V; };
 
-    // finite check of this thread over the segment (real elements only)
-    uint32_t seg_kmin = 0xffffffffu, seg_kmax = 0;
+    // Nonfinite latch over the segment: nfacc = sum of x * 0 stays 0 unless
+    // some x is +-Inf or NaN. Padding past the row end is -FLT_MAX (finite,
+    // never above a real logit) and is never appended.
+    float nfacc = 0.0f;
     if (tid == 0) { s.count = 0; s.tau_key = 0; }
     __syncthreads();
 
     auto accum = [&](const Unit& t, float4 (&q)[kVPT]) {
-        uint32_t kmax = 0;  // the thread's largest key in this chunk
+        // pass 1: the largest value of each float4 and of the thread
+        float smax[kVPT];
+        float tmax = -INFINITY;
 #pragma unroll
         for (int sl = 0; sl < kVPT; ++sl) {
-            const uint32_t e = t.lo + 4u * (tid + kNT * sl);
-            const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t kk = f2key(f[j]);
-                const bool in = e + j < t.hi;
-                seg_kmin = in ? min(seg_kmin, kk) : seg_kmin;
-                kmax = in ? max(kmax, kk) : kmax;
-            }
+            smax[sl] = fmaxf(fmaxf(q[sl].x, q[sl].y), fmaxf(q[sl].z, q[sl].w));
+            tmax = fmaxf(tmax, smax[sl]);
+            nfacc = __fmaf_rn(q[sl].x, 0.0f, nfacc);
+            nfacc = __fmaf_rn(q[sl].y, 0.0f, nfacc);
+            nfacc = __fmaf_rn(q[sl].z, 0.0f, nfacc);
+            nfacc = __fmaf_rn(q[sl].w, 0.0f, nfacc);
         }
-        seg_kmax = max(seg_kmax, kmax);
-        // chunk bound: >= k elements of this chunk have key >= tau
-        if (k <= 32u * kWarps) {
-            const uint32_t v = warp_sort_desc(kmax);
+        // threshold: once the buffer holds k candidates its k-th key bounds
+        // every later (higher-id) element; before that, the chunk bound
+        // (>= k elements of this chunk have key >= tau) does
+        // the buffer state is read by every thread before anyone appends
+        const uint32_t pre = s.count, tau_key = s.tau_key;
+        const bool have_k = pre >= k && tau_key != 0;
+        const bool bound = !have_k && k <= 32u * kWarps;
+        if (bound) {
+            const uint32_t v = warp_sort_desc(f2key(tmax));
             const uint32_t r = (k + kWarps - 1) / kWarps;
             const uint32_t wv = __shfl_sync(kFull, v, r - 1);
             if (lane == 0) s.warp_val[warp] = wv;
         }
         __syncthreads();
-        // keep room for a whole chunk of survivors most of the time
-        if (s.count > kCap / 2) reduce_buffer(s, k);
         uint32_t tau = 0;
-        if (k <= 32u * kWarps) {
+        if (bound) {
             tau = s.warp_val[0];
 #pragma unroll
             for (int w = 1; w < kWarps; ++w) tau = min(tau, s.warp_val[w]);
         }
-        // buffered candidates have lower ids than this chunk, so an equal key
-        // cannot displace the k-th; key 0 marks padding
-        const uint32_t pre = s.count;
-        uint32_t thr = max(tau, s.tau_key + 1u);
-        if (__any_sync(kFull, kmax >= thr)) {
+        const uint32_t thr = max(max(tau, tau_key + 1u), 1u);
+        // key >= thr  <=>  value >= thr_f (keys below key(-FLT_MAX) are -inf and
+        // NaN patterns: every non-NaN value passes them)
+        const float thr_f = thr <= kKeyMinFinite ? -INFINITY : key2f(thr);
+        // pass 2: only float4s whose max reaches the threshold are examined
+        if (tmax >= thr_f) {
 #pragma unroll
             for (int sl = 0; sl < kVPT; ++sl) {
-                const uint32_t e = t.lo + 4u * (tid + kNT * sl);
-                const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
+                if (smax[sl] >= thr_f) {
+                    const uint32_t e = t.lo + 4u * (tid + kNT * sl);
+                    const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t kk = e + j < t.hi ? f2key(f[j]) : 0u;
-                    warp_append(s, kk >= thr, make_cand(kk, e + j));
+                    for (int j = 0; j < 4; ++j) {
+                        if (f[j] >= thr_f && e + j < t.hi) {
+                            const uint32_t slot = atomicAdd(&s.count, 1u);
+                            if (slot < kCap) s.buf[slot] = make_cand(f2key(f[j]), e + j);
+                        }
+                    }
                 }
             }
         }
         __syncthreads();
         if (s.count > kCap) {
-            // overflow (adversarial chunks): redo the chunk slot by slot
-            // (1,024 elements), selecting in between
             __syncthreads();
             if (tid == 0) s.count = pre;
             __syncthreads();
-#pragma unroll
-            for (int sl = 0; sl < kVPT; ++sl) {
-                if (s.count + 4u * kNT > kCap) reduce_buffer(s, k);
-                thr = max(tau, s.tau_key + 1u);
-                const uint32_t e = t.lo + 4u * (tid + kNT * sl);
-                const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t kk = e + j < t.hi ? f2key(f[j]) : 0u;
-                    warp_append(s, kk >= thr, make_cand(kk, e + j));
-                }
-                __syncthreads();
-            }
+            overflow_chunk<kTma>(s, a.logits + static_cast<size_t>(t.row) * V, t.lo, t.hi, k, tau);
+        } else if (s.count > kCap / 2) {
+            reduce_buffer(s, k);
         }
     };
 
@@ -443,10 +466,8 @@ __global__ void __launch_bounds__(kNT, 2) topk_kernel(TopkArgs a) {
         const uint32_t n = min(s.count, kCap);
         block_select_sorted(s.buf, n, k, s.sorted);
         const uint32_t have = n < k ? n : k;
-        const uint32_t nf_local =
-            key_nonfinite(__reduce_min_sync(kFull, seg_kmin), __reduce_max_sync(kFull, seg_kmax)) ? 1u : 0u;
-        seg_kmin = 0xffffffffu;
-        seg_kmax = 0;
+        const uint32_t nf_local = __any_sync(kFull, nfacc != 0.0f) ? 1u : 0u;
+        nfacc = 0.0f;
         if (lane == 0) s.warp_val[warp] = nf_local;
         __syncthreads();
         uint32_t nf = 0;
@@ -483,7 +504,7 @@ __global__ void __launch_bounds__(kNT, 2) topk_kernel(TopkArgs a) {
         __syncthreads();
     };
 
-    stream_segments<kTma, kNT, kVPT, kStages>(a.cfg, row_ptr, accum, flush, stages, full, a.err);
+    stream_segments<kTma, kNT, kVPT, kStages>(a.cfg, row_ptr, accum, flush, stages, full, a.err, -FLT_MAX);
 }
 
 struct TopkLayout {
