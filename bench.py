@@ -155,7 +155,6 @@ def gpu_arm(args, rank, world, local_rank):
                          B.SEL_ORDER_TEMP_FIRST)
     rej = B.SpecParams(1.0, B.SPEC_MODE_REJECTION)
     arg = B.SpecParams(1.0, B.SPEC_MODE_ARGMAX)
-    stream = torch.cuda.current_stream()
     OPS = ["argmax", "topk", "sample", "spec_rejection", "spec_argmax"]
     # the copy each op of step s reads: consecutive reads walk the N_COPIES
     # copies in turn, so a copy is read again only after 5 others (243 MB)
@@ -165,28 +164,29 @@ def gpu_arm(args, rank, world, local_rank):
     def target_view(t):
         return t.view(SPEC_S, SPEC_K + 1, V)
 
-    def run_op(step, op):
+    def run_op(step, op):  # on the current stream
         if op == 0:
-            B.sel_argmax(copy_for(step, 0), ids, ws_a, stream)
+            B.sel_argmax(copy_for(step, 0), ids, ws_a)
         elif op == 1:
-            B.sel_topk(copy_for(step, 1), K_TOPK, tv, ti, ws_t, stream)
+            B.sel_topk(copy_for(step, 1), K_TOPK, tv, ti, ws_t)
         elif op == 2:
-            B.sel_sample(copy_for(step, 2), prm, ud, sid, sp, ws_s, stream)
+            B.sel_sample(copy_for(step, 2), prm, ud, sid, sp, ws_s)
         elif op == 3:
-            B.spec_accept(target_view(copy_for(step, 3)), drafts[step % 2], tok, rej, ua, uf, acc, emi,
-                          ws_r, stream)
+            B.spec_accept(target_view(copy_for(step, 3)), drafts[step % 2], tok, rej, ua, uf, acc, emi, ws_r)
         else:
-            B.spec_accept(target_view(copy_for(step, 4)), None, tok, arg, None, None, acc2, emi2, ws_g,
-                          stream)
+            B.spec_accept(target_view(copy_for(step, 4)), None, tok, arg, None, None, acc2, emi2, ws_g)
 
     launches_per_step = 6  # spec rejection is two kernels
     bytes_per_op = [ROWS * ROW_BYTES, ROWS * ROW_BYTES, ROWS * ROW_BYTES,
                     None, ROWS * ROW_BYTES]
 
-    # warm-up
-    for s in range(args.warmup):
-        for op in range(5):
-            run_op(s, op)
+    # eager warm-up (also the first launches of every kernel)
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for s in range(max(args.warmup, 1)):
+            for op in range(5):
+                run_op(s, op)
     torch.cuda.synchronize()
     # residual re-read of the rejection rule: the rejecting position's target
     # and draft rows, or the bonus row when all positions accept
@@ -194,8 +194,33 @@ def gpu_arm(args, rank, world, local_rank):
     resid_rows = int(sum(2 if a < SPEC_K else 1 for a in n_acc))
     bytes_per_op[3] = (SPEC_S * (2 * SPEC_K + 1) + resid_rows) * ROW_BYTES
 
-    # timed region: events bracket every op on the launching stream
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    # Each step is replayed from a CUDA graph of its five calls (six kernels),
+    # so the host's launch cost does not gap the GPU. Event-record nodes in
+    # the graph bracket every op on the launching stream; a graph's events
+    # hold the times of its latest replay.
+    n_graphs = min(args.steps, 60)
+    graphs, evs = [], []
+    graph_events = True
+    for gi in range(n_graphs):
+        try:
+            e = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(6)]
+        except TypeError:
+            graph_events, e = False, None
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            if e:
+                e[0].record()
+            for op in range(5):
+                run_op(gi, op)
+                if e:
+                    e[op + 1].record()
+        graphs.append(g)
+        evs.append(e)
+    with torch.cuda.stream(stream):
+        for s in range(args.warmup):
+            graphs[s % n_graphs].replay()
+    torch.cuda.synchronize()
+
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
@@ -205,23 +230,39 @@ def gpu_arm(args, rank, world, local_rank):
     time.sleep(0.25)  # let the sampler start
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for s in range(args.steps):
-        e = evs[s]
-        e[0].record(stream)
-        for op in range(5):
-            run_op(args.warmup + s, op)
-            e[op + 1].record(stream)
-    t_end.record(stream)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for s in range(args.steps):
+            graphs[s % n_graphs].replay()
+        t_end.record(stream)
     torch.cuda.synchronize()
+    if graph_events:
+        # graph g's events hold its latest replay inside the timed region
+        per_op_us = [statistics.mean(evs[gi][op].elapsed_time(evs[gi][op + 1]) for gi in range(n_graphs)) * 1e3
+                     for op in range(5)]
+    else:
+        # this torch cannot put event nodes in a graph: time each op eagerly
+        per_op_us = [0.0] * 5
+        reps = 10
+        for op in range(5):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                for r in range(reps):
+                    run_op(r, op)
+                b.record(stream)
+            torch.cuda.synchronize()
+            per_op_us[op] = a.elapsed_time(b) * 1e3 / reps
     # keep the same load running briefly so the clock sampler sees it even
     # when the timed region is shorter than its period
     tail_until = time.time() + 0.6
-    s = args.warmup + args.steps
+    s = 0
     while time.time() < tail_until:
-        for op in range(5):
-            run_op(s, op)
-        s += 1
+        with torch.cuda.stream(stream):
+            for _ in range(8):
+                graphs[s % n_graphs].replay()
+                s += 1
         torch.cuda.synchronize()
     clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
@@ -274,6 +315,8 @@ def gpu_arm(args, rank, world, local_rank):
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
                      "traffic": traffic},
         "gpu_launches": launches_per_step * args.steps,
+        "timing": "CUDA graph per step; per-op event nodes" if graph_events else
+                  "CUDA graph per step; per-op times from eager launches",
         "clocks": clk,
         "e2e": e2e,
     }

@@ -126,6 +126,76 @@ __device__ __forceinline__ T warp_sort_desc(T v) {
 }
 
 // ---------------------------------------------------------------------------
+// arithmetic helpers
+// ---------------------------------------------------------------------------
+
+// 2^x with the SFU's approximate exp2 (relative error about 2^-22);
+// exp(d / T) = 2^(d * log2(e) / T). Results below 2^-126 flush to 0.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Unevaluated sum hi + lo of two floats (about 44 significant bits),
+// accumulated with Knuth's TwoSum and renormalised with Dekker's Fast2Sum;
+// sums of many small fp32 terms keep ~1e-13 relative error without FP64.
+struct FF {
+    float hi, lo;
+};
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+    const float s = a.hi + b.hi;
+    const float v = s - a.hi;
+    float e = (a.hi - (s - v)) + (b.hi - v);
+    e += a.lo + b.lo;
+    const float h = s + e;
+    return FF{h, e - (h - s)};
+}
+__device__ __forceinline__ FF ff_shfl_xor(FF a, int m) {
+    return FF{__shfl_xor_sync(kFull, a.hi, m), __shfl_xor_sync(kFull, a.lo, m)};
+}
+__device__ __forceinline__ FF ff_shfl_up(FF a, int m) {
+    return FF{__shfl_up_sync(kFull, a.hi, m), __shfl_up_sync(kFull, a.lo, m)};
+}
+__device__ __forceinline__ FF ff_shfl(FF a, int src) {
+    return FF{__shfl_sync(kFull, a.hi, src), __shfl_sync(kFull, a.lo, src)};
+}
+// Warp sum (every lane gets the same value: a fixed butterfly order).
+__device__ __forceinline__ FF ff_warp_sum(FF a) {
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const FF o = ff_shfl_xor(a, m);
+        // combine in lane order so both partners compute the same sum
+        a = ((threadIdx.x & m) == 0) ? ff_add(a, o) : ff_add(o, a);
+    }
+    return a;
+}
+// Inclusive warp scan in lane order.
+__device__ __forceinline__ FF ff_warp_scan(FF a) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const FF o = ff_shfl_up(a, m);
+        if (lane >= m) a = ff_add(o, a);
+    }
+    return a;
+}
+// a * b for a float b (Dekker's product through fmaf, then Fast2Sum).
+__device__ __forceinline__ FF ff_mul_f(FF a, float b) {
+    const float p = a.hi * b;
+    const float e = __fmaf_rn(a.hi, b, -p) + a.lo * b;
+    const float h = p + e;
+    return FF{h, e - (h - p)};
+}
+__device__ __forceinline__ FF ff_from_double(double d) {
+    const float hi = static_cast<float>(d);
+    return FF{hi, static_cast<float>(d - static_cast<double>(hi))};
+}
+// a < b for normalised values (|lo| at most half an ulp of hi).
+__device__ __forceinline__ bool ff_lt(FF a, FF b) { return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo); }
+__device__ __forceinline__ double ff_to_double(FF a) { return static_cast<double>(a.hi) + static_cast<double>(a.lo); }
+
+// ---------------------------------------------------------------------------
 // cross-block hand-off
 // ---------------------------------------------------------------------------
 // Results one block publishes for another (per-chunk partials, candidate

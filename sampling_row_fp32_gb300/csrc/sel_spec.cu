@@ -53,9 +53,10 @@ constexpr uint32_t kNonfiniteBit = 0x80000000u;
 enum : uint32_t { kDrawNone = 0, kDrawResidual = 1, kDrawBonus = 2 };
 
 struct alignas(16) RowPart {
-    float m;       // max of the chunk (row)
+    float m;       // max of the segment (row)
     uint32_t idx;  // lowest id attaining it; bit 31 = nonfinite seen
-    double s;      // sum of exp((x - m) / T)
+    float s_hi;    // sum of exp((x - m) / T) as float-float s_hi + s_lo
+    float s_lo;
 };
 
 struct alignas(16) Decision {
@@ -101,6 +102,7 @@ struct SpecArgs {
     uint32_t* emitted;
     uint32_t S, K, V;
     float T;
+    float log2e_over_T;    // exp(d / T) = 2^(d * log2e_over_T)
     StreamCfg cfg;         // phase-1 units over all rows
     uint32_t* err;
     uint32_t* row_ctr;
@@ -142,135 +144,169 @@ __device__ __forceinline__ double warp_incl_scan_d(double v) {
     return v;
 }
 
-// Pairwise sum of 32 values held in registers.
-__device__ __forceinline__ float pairwise32(float (&w)[kVPT][4]) {
-    float a[kVPT];
-#pragma unroll
-    for (int s = 0; s < kVPT; ++s) a[s] = (w[s][0] + w[s][1]) + (w[s][2] + w[s][3]);
-#pragma unroll
-    for (int h = kVPT / 2; h > 0; h >>= 1)
-#pragma unroll
-        for (int s = 0; s < h; ++s) a[s] += a[s + h];
-    return a[0];
-}
-
-// The acceptance chain of one sequence, run by one thread once every row of
-// the sequence has its statistics.
+// The acceptance chain of one sequence, run by one warp once every row of
+// the sequence has its statistics: lane j tests position j (32 at a time)
+// and the first failing position ends the chain.
 template <bool kRej>
 __device__ void decide_sequence(const SpecArgs& a, uint32_t s) {
+    const uint32_t lane = threadIdx.x & 31u;
     const uint32_t K = a.K, V = a.V;
     const RowPart* tstat = a.row_stats + static_cast<size_t>(s) * (K + 1u);
     const RowPart* dstat = a.row_stats + static_cast<size_t>(a.S) * (K + 1u) + static_cast<size_t>(s) * K;
     const uint32_t* tok = a.tokens + static_cast<size_t>(s) * K;
+    const float* u_acc = a.u_acc + static_cast<size_t>(s) * K;
     uint32_t* em = a.emitted + static_cast<size_t>(s) * (K + 1u);
-    Decision d{0u, kDrawNone, 0u, 0u};
 
-    bool valid = true;
-    for (uint32_t j = 0; j <= K; ++j) valid &= !(ld_gpu_u32(&tstat[j].idx) & kNonfiniteBit);
-    for (uint32_t j = 0; j < K; ++j) valid &= tok[j] < V;
-    if (kRej) {
-        for (uint32_t j = 0; j < K; ++j) {
-            valid &= !(ld_gpu_u32(&dstat[j].idx) & kNonfiniteBit);
-            const float u = a.u_acc[static_cast<size_t>(s) * K + j];
-            valid &= u >= 0.0f && u < 1.0f;
+    bool bad = false;
+    for (uint32_t j = lane; j <= K; j += 32u) bad |= (ld_gpu_u32(&tstat[j].idx) & kNonfiniteBit) != 0u;
+    for (uint32_t j = lane; j < K; j += 32u) {
+        bad |= tok[j] >= V;
+        if (kRej) {
+            bad |= (ld_gpu_u32(&dstat[j].idx) & kNonfiniteBit) != 0u;
+            const float u = u_acc[j];
+            bad |= !(u >= 0.0f && u < 1.0f);
         }
+    }
+    if (kRej && lane == 0) {
         const float uf = a.u_fin[s];
-        valid &= uf >= 0.0f && uf < 1.0f;
+        bad |= !(uf >= 0.0f && uf < 1.0f);
     }
-    if (!valid) {
-        for (uint32_t j = 0; j <= K; ++j) em[j] = SEL_INVALID_ID;
-        a.accepted[s] = SEL_INVALID_ID;
-        a.decisions[s] = d;
+    if (__any_sync(kFull, bad)) {
+        for (uint32_t j = lane; j <= K; j += 32u) em[j] = SEL_INVALID_ID;
+        if (lane == 0) {
+            a.accepted[s] = SEL_INVALID_ID;
+            a.decisions[s] = Decision{0u, kDrawNone, 0u, 0u};
+        }
         return;
     }
-    uint32_t n = 0;
-    if (!kRej) {
-        while (n < K && tok[n] == (ld_gpu_u32(&tstat[n].idx) & ~kNonfiniteBit)) ++n;
-        for (uint32_t j = 0; j < n; ++j) em[j] = tok[j];
-        em[n] = ld_gpu_u32(&tstat[n].idx) & ~kNonfiniteBit;
-        for (uint32_t j = n + 1; j <= K; ++j) em[j] = SEL_INVALID_ID;
+    uint32_t n = K;
+    for (uint32_t j0 = 0; j0 < K; j0 += 32u) {
+        const uint32_t j = j0 + lane;
+        bool fail = false;
+        if (j < K) {
+            const uint32_t t = tok[j];
+            if (!kRej) {
+                fail = t != (ld_gpu_u32(&tstat[j].idx) & ~kNonfiniteBit);
+            } else {
+                // p_j(t) and q_j(t) from the row statistics; accept iff u q <= p
+                const float* trow = a.target + (static_cast<size_t>(s) * (K + 1u) + j) * V;
+                const float* drow = a.draft + (static_cast<size_t>(s) * K + j) * V;
+                const float p = ex2_approx((trow[t] - ld_gpu_f32(&tstat[j].m)) * a.log2e_over_T) /
+                                ld_gpu_f32(&tstat[j].s_hi);
+                const float q = ex2_approx((drow[t] - ld_gpu_f32(&dstat[j].m)) * a.log2e_over_T) /
+                                ld_gpu_f32(&dstat[j].s_hi);
+                fail = !(u_acc[j] * q <= p);
+            }
+        }
+        const uint32_t f = __ballot_sync(kFull, fail);
+        if (f) {
+            n = j0 + static_cast<uint32_t>(__ffs(f) - 1);
+            break;
+        }
+    }
+    for (uint32_t j = lane; j <= K; j += 32u) {
+        uint32_t v = SEL_INVALID_ID;  // in the rejection rule em[n] is the phase-2 draw
+        if (j < n) v = tok[j];
+        else if (!kRej && j == n) v = ld_gpu_u32(&tstat[n].idx) & ~kNonfiniteBit;
+        em[j] = v;
+    }
+    if (lane == 0) {
         a.accepted[s] = n;
-        a.decisions[s] = d;
-        return;
+        a.decisions[s] = Decision{n, kRej ? (n < K ? kDrawResidual : kDrawBonus) : kDrawNone, 0u, 0u};
     }
-    const double invT = 1.0 / static_cast<double>(a.T);
-    for (; n < K; ++n) {
-        const uint32_t t = tok[n];
-        const float* trow = a.target + (static_cast<size_t>(s) * (K + 1u) + n) * V;
-        const float* drow = a.draft + (static_cast<size_t>(s) * K + n) * V;
-        const double p = exp((static_cast<double>(trow[t]) - ld_gpu_f32(&tstat[n].m)) * invT) / ld_gpu_f64(&tstat[n].s);
-        const double q = exp((static_cast<double>(drow[t]) - ld_gpu_f32(&dstat[n].m)) * invT) / ld_gpu_f64(&dstat[n].s);
-        const double u = a.u_acc[static_cast<size_t>(s) * K + n];
-        if (!(u * q <= p)) break;
-    }
-    for (uint32_t j = 0; j < n; ++j) em[j] = tok[j];
-    for (uint32_t j = n; j <= K; ++j) em[j] = SEL_INVALID_ID;  // em[n] is the phase-2 draw
-    a.accepted[s] = n;
-    d.jstar = n;
-    d.kind = n < K ? kDrawResidual : kDrawBonus;
-    a.decisions[s] = d;
 }
 
 // Phase 1: per-row (max, sum exp) or (max, argmax); per-sequence decision.
 template <bool kTma, bool kRej>
-__global__ void __launch_bounds__(kNT) spec_phase1_kernel(SpecArgs a) {
+__global__ void __launch_bounds__(kNT, 2) spec_phase1_kernel(SpecArgs a) {
     extern __shared__ float4 stages[];
     __shared__ uint64_t full[kStages];
     __shared__ float s_m[kWarps];
     __shared__ uint32_t s_i[kWarps];
     __shared__ uint32_t s_nf[kWarps];
-    __shared__ double s_s[kWarps];
+    __shared__ FF s_ff[kWarps];
+    __shared__ uint32_t s_flag;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const float invT = kRej ? 1.0f / a.T : 1.0f;
     auto row_ptr = [&](uint32_t r) {
         uint32_t seq;
         return phase1_row(a, r, seq);
     };
 
-    // per-thread running max, lowest argmax id, finite check and (rejection
-    // rule) sum of exp((x - max) / T) over this block's segment of a row
-    float m = -INFINITY;
-    uint32_t bidx = kNoIdx, absmax = 0;
-    float sum = 0.0f;
+    // Per thread, over this block's segment of a row: four (max, quad start)
+    // chains (the lowest id of the maximum is the quad start + lane), the
+    // nonfinite latch (sum of x * 0 stays 0 unless some x is +-Inf or NaN),
+    // and in the rejection rule four sums of 2^((x - M) * c) = exp((x - M) / T)
+    // relative to the thread's running max M. Padding past the row end is
+    // -FLT_MAX: it never wins and adds exp(-inf) = 0.
+    float best[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    uint32_t bbase[4] = {kNoIdx, kNoIdx, kNoIdx, kNoIdx};
+    float nfacc = 0.0f;
+    float M = -INFINITY;
+    float sum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const float c = a.log2e_over_T;
 
     auto accum = [&](const Unit& t, float4 (&q)[kVPT]) {
-        float tm = -INFINITY;
 #pragma unroll
         for (int sl = 0; sl < kVPT; ++sl) {
             const uint32_t e = t.lo + 4u * (tid + kNT * sl);
             const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                if (e + j < t.hi) {
-                    absmax = max(absmax, __float_as_uint(f[j]) & 0x7fffffffu);
-                    if (f[j] > tm) {
-                        tm = f[j];
-                        if (f[j] > m) bidx = e + j;  // ids rise: '>' keeps the lowest
-                    }
+                nfacc = __fmaf_rn(f[j], 0.0f, nfacc);
+                if (f[j] > best[j]) {  // ids rise along each chain: '>' keeps the lowest
+                    best[j] = f[j];
+                    bbase[j] = e;
                 }
             }
         }
-        const float mn = fmaxf(m, tm);
-        if (kRej && mn > -INFINITY && mn < INFINITY) {
-            float w[kVPT][4];
+        if (kRej) {
+            const float Mn = fmaxf(fmaxf(best[0], best[1]), fmaxf(best[2], best[3]));
+            if (Mn > -INFINITY && Mn < INFINITY) {
+                const float scale = M > -INFINITY ? ex2_approx((M - Mn) * c) : 0.0f;
 #pragma unroll
-            for (int sl = 0; sl < kVPT; ++sl) {
-                const uint32_t e = t.lo + 4u * (tid + kNT * sl);
-                const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
+                for (int j = 0; j < 4; ++j) sum[j] *= scale;
+                const uint32_t n = t.hi - t.lo;
+                if (n == 4u * kNT * kVPT) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) w[sl][j] = e + j < t.hi ? __expf((f[j] - mn) * invT) : 0.0f;
+                    for (int sl = 0; sl < kVPT; ++sl) {
+                        sum[0] += ex2_approx((q[sl].x - Mn) * c);
+                        sum[1] += ex2_approx((q[sl].y - Mn) * c);
+                        sum[2] += ex2_approx((q[sl].z - Mn) * c);
+                        sum[3] += ex2_approx((q[sl].w - Mn) * c);
+                    }
+                } else {
+                    // a short unit: padding must weigh 0 even when every
+                    // real value (and so Mn) is -FLT_MAX
+#pragma unroll
+                    for (int sl = 0; sl < kVPT; ++sl) {
+                        const uint32_t e = 4u * (tid + kNT * sl);
+                        const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            sum[j] += e + j < n ? ex2_approx((f[j] - Mn) * c) : 0.0f;
+                    }
+                }
+                M = Mn;
             }
-            const float scale = m > -INFINITY ? __expf((m - mn) * invT) : 0.0f;
-            sum = sum * scale + pairwise32(w);
         }
-        m = mn;
     };
 
     auto flush = [&](const Segment& g) {
-        uint32_t nf = absmax >= 0x7f800000u ? kNonfiniteBit : 0u;
-        float bm = m;
-        uint32_t bi = bidx;
+        uint32_t nf = nfacc == 0.0f ? 0u : kNonfiniteBit;
+        float bm = -INFINITY;
+        uint32_t bi = kNoIdx;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t id = bbase[j] == kNoIdx ? kNoIdx : bbase[j] + j;
+            if (beats(best[j], id, bm, bi)) { bm = best[j]; bi = id; }
+        }
+        const float thread_m = M;
+        const float thread_s = (sum[0] + sum[1]) + (sum[2] + sum[3]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) { best[j] = -INFINITY; bbase[j] = kNoIdx; sum[j] = 0.0f; }
+        nfacc = 0.0f;
+        M = -INFINITY;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             const float ov = __shfl_xor_sync(kFull, bm, o);
@@ -288,60 +324,75 @@ __global__ void __launch_bounds__(kNT) spec_phase1_kernel(SpecArgs a) {
             if (beats(s_m[w], s_i[w], bm, bi)) { bm = s_m[w]; bi = s_i[w]; }
             nf |= s_nf[w];
         }
-        // the sums, rescaled to the segment's max, summed in double
-        double bs = 0.0;
+        // the sums, rescaled to the segment's max, added as float-float
+        FF tot{0.0f, 0.0f};
         if (kRej) {
-            double mine = (!nf && m > -INFINITY) ? static_cast<double>(sum) * static_cast<double>(__expf((m - bm) * invT))
-                                                 : 0.0;
-            mine = warp_sum_d(mine);
-            if (lane == 0) s_s[warp] = mine;
+            FF mine{(!nf && thread_m > -INFINITY) ? thread_s * ex2_approx((thread_m - bm) * c) : 0.0f, 0.0f};
+            mine = ff_warp_sum(mine);
+            if (lane == 0) s_ff[warp] = mine;
             __syncthreads();
 #pragma unroll
-            for (int ww = 0; ww < kWarps; ++ww) bs += s_s[ww];
+            for (int ww = 0; ww < kWarps; ++ww) tot = ff_add(tot, s_ff[ww]);
         }
-        m = -INFINITY;
-        bidx = kNoIdx;
-        absmax = 0;
-        sum = 0.0f;
+        RowPart* parts = a.row_parts + static_cast<size_t>(g.row) * a.cmax;
         if (tid == 0) {
-            bool row_done = true;
+            const RowPart part{bm, bi | nf, tot.hi, tot.lo};
             if (g.count == 1) {
-                a.row_stats[g.row] = RowPart{bm, bi | nf, bs};
+                a.row_stats[g.row] = part;
+                s_flag = 2u;  // the row is complete
             } else {
-                RowPart* parts = a.row_parts + static_cast<size_t>(g.row) * a.cmax;
-                parts[g.index] = RowPart{bm, bi | nf, bs};
-                row_done = segment_arrive(&a.row_ctr[g.row], g.count);
-                if (row_done) {
-                    // merge the row's segments in segment order
-                    float rm = -INFINITY;
-                    uint32_t ri = kNoIdx, rnf = 0;
-                    for (uint32_t c = 0; c < g.count; ++c) {
-                        const float cm = ld_gpu_f32(&parts[c].m);
-                        const uint32_t ci = ld_gpu_u32(&parts[c].idx);
-                        rnf |= ci & kNonfiniteBit;
-                        if (beats(cm, ci & ~kNonfiniteBit, rm, ri)) { rm = cm; ri = ci & ~kNonfiniteBit; }
-                    }
-                    double rs = 0.0;
-                    if (kRej && !rnf) {
-                        const double iT = 1.0 / static_cast<double>(a.T);
-                        for (uint32_t c = 0; c < g.count; ++c)
-                            rs += ld_gpu_f64(&parts[c].s) * exp((static_cast<double>(ld_gpu_f32(&parts[c].m)) - rm) * iT);
-                    }
-                    a.row_stats[g.row] = RowPart{rm, ri | rnf, rs};
+                parts[g.index] = part;
+                s_flag = segment_arrive(&a.row_ctr[g.row], g.count) ? 1u : 0u;
+            }
+        }
+        __syncthreads();
+        const uint32_t flag = s_flag;
+        if (flag != 0u && warp == 0) {
+            if (flag == 1u) {
+                // this block completed the row: merge its segments in segment order
+                __threadfence();
+                float rm = -INFINITY;
+                uint32_t ri = kNoIdx, rnf = 0u;
+                for (uint32_t cc = lane; cc < g.count; cc += 32u) {
+                    const float cm = ld_gpu_f32(&parts[cc].m);
+                    const uint32_t ci = ld_gpu_u32(&parts[cc].idx);
+                    rnf |= ci & kNonfiniteBit;
+                    if (beats(cm, ci & ~kNonfiniteBit, rm, ri)) { rm = cm; ri = ci & ~kNonfiniteBit; }
                 }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float ov = __shfl_xor_sync(kFull, rm, o);
+                    const uint32_t oi = __shfl_xor_sync(kFull, ri, o);
+                    if (beats(ov, oi, rm, ri)) { rm = ov; ri = oi; }
+                }
+                rnf = __reduce_or_sync(kFull, rnf);
+                FF rs{0.0f, 0.0f};
+                if (kRej && !rnf) {
+                    for (uint32_t cc = lane; cc < g.count; cc += 32u) {
+                        const FF sc{ld_gpu_f32(&parts[cc].s_hi), ld_gpu_f32(&parts[cc].s_lo)};
+                        rs = ff_add(rs, ff_mul_f(sc, ex2_approx((ld_gpu_f32(&parts[cc].m) - rm) * c)));
+                    }
+                    rs = ff_warp_sum(rs);
+                }
+                if (lane == 0) a.row_stats[g.row] = RowPart{rm, ri | rnf, rs.hi, rs.lo};
             }
             // the last row of the sequence to finish runs the acceptance chain
-            if (row_done) {
-                uint32_t seq;
-                phase1_row(a, g.row, seq);
+            uint32_t seq;
+            phase1_row(a, g.row, seq);
+            bool last = false;
+            if (lane == 0) {
                 const uint32_t rows_per_seq = kRej ? 2u * a.K + 1u : a.K + 1u;
-                if (segment_arrive(&a.seq_ctr[seq], rows_per_seq)) decide_sequence<kRej>(a, seq);
+                last = segment_arrive(&a.seq_ctr[seq], rows_per_seq);
+            }
+            if (__shfl_sync(kFull, last, 0)) {
+                __threadfence();
+                decide_sequence<kRej>(a, seq);
             }
         }
         __syncthreads();
     };
 
-    stream_segments<kTma, kNT, kVPT, kStages>(a.cfg, row_ptr, accum, flush, stages, full, a.err);
+    stream_segments<kTma, kNT, kVPT, kStages>(a.cfg, row_ptr, accum, flush, stages, full, a.err, -FLT_MAX);
 }
 
 struct DrawArgs {
@@ -387,13 +438,19 @@ __device__ __forceinline__ void draw_weights(const float* prow, const float* qro
 }
 
 // Phase 2: the inverse-CDF draw from the residual (or from p).
+// Every block sums its chunk; the last block of the sequence finds the chunk
+// where u_fin * total falls (a fixed-order scan of the chunk sums), then scans
+// that chunk in id order with each thread owning kDrawPer consecutive ids.
+constexpr uint32_t kDrawPer = 32;
+constexpr uint32_t kDrawChunkMax = kNT * kDrawPer;  // 8,192
+
 template <bool kVec>
 __global__ void __launch_bounds__(kNT) spec_draw_kernel(DrawArgs a) {
     __shared__ double s_r[kWarps];
     __shared__ double s_p[kWarps];
-    __shared__ double s_scan[kWarps];
+    __shared__ FF s_wtot[kWarps];
     __shared__ bool s_last;
-    __shared__ uint32_t s_pick;
+    __shared__ uint32_t s_cross;
     __shared__ int s_lastpos;
     __shared__ bool s_use_p;
     __shared__ uint32_t s_cstar;
@@ -410,15 +467,15 @@ __global__ void __launch_bounds__(kNT) spec_draw_kernel(DrawArgs a) {
     const float* prow = a.target + static_cast<size_t>(prow_i) * V;
     const RowPart ps = a.row_stats[prow_i];
     const float* qrow = nullptr;
-    RowPart qs{0.0f, 0u, 1.0};
+    RowPart qs{0.0f, 0u, 1.0f, 0.0f};
     if (residual) {
         const uint32_t qrow_i = a.S * (K + 1u) + s * K + d.jstar;
         qrow = a.draft + static_cast<size_t>(s * K + d.jstar) * V;
         qs = a.row_stats[qrow_i];
     }
     const float invT = 1.0f / a.T;
-    const float pinv = static_cast<float>(1.0 / ps.s);
-    const float qinv = static_cast<float>(1.0 / qs.s);
+    const float pinv = 1.0f / ps.s_hi;
+    const float qinv = 1.0f / qs.s_hi;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     const uint32_t lo = chunk * a.chunk_elems;
@@ -502,74 +559,67 @@ __global__ void __launch_bounds__(kNT) spec_draw_kernel(DrawArgs a) {
             s_cstar = cstar;
             s_before = before;
             s_target = target;
+            s_cross = kNoIdx;
+            s_lastpos = -1;
         }
     }
     __syncthreads();
     const bool use_p = s_use_p;
-    const uint32_t cstar = s_cstar;
-    const double before = s_before, target = s_target;
-    if (tid == 0) { s_pick = kNoIdx; s_lastpos = -1; }
-    __syncthreads();
-
-    // scan chunk cstar in id order, kVPT quads (8,192 elements) per step
-    const uint32_t clo = cstar * a.chunk_elems;
+    const uint32_t clo = s_cstar * a.chunk_elems;
     const uint32_t chi = min(V, clo + a.chunk_elems);
-    double running = before;
-    for (uint32_t step = clo; step < chi; step += 4u * kNT * kVPT) {
-        float4 xp[kVPT], xq[kVPT];
+    const FF target = ff_from_double(s_target);
+
+    // thread tid owns ids [e0, e0 + kDrawPer) of chunk cstar
+    const uint32_t e0 = clo + kDrawPer * static_cast<uint32_t>(tid);
+    float w[kDrawPer];
 #pragma unroll
-        for (int sl = 0; sl < kVPT; ++sl) {
-            const uint32_t e = step + 4u * (tid + kNT * sl);
-            xp[sl] = ld_quad<kVec>(prow, e, chi, -INFINITY);
-            xq[sl] = residual ? ld_quad<kVec>(qrow, e, chi, -INFINITY)
-                              : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        }
-#pragma unroll 1
-        for (int sl = 0; sl < kVPT; ++sl) {
-            const uint32_t e = step + 4u * (tid + kNT * sl);
-            float pw[4], rw[4];
-            float4 cp = xp[0], cq = xq[0];
+    for (uint32_t i = 0; i < kDrawPer / 4u; ++i) {
+        const float4 xp = ld_quad<kVec>(prow, e0 + 4u * i, chi, -INFINITY);
+        const float4 xq = residual ? ld_quad<kVec>(qrow, e0 + 4u * i, chi, -INFINITY)
+                                   : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        float pw[4], rw[4];
+        quad_weights(xp, xq, residual, ps.m, pinv, qs.m, qinv, invT, pw, rw);
 #pragma unroll
-            for (int z = 1; z < kVPT; ++z)
-                if (z == sl) { cp = xp[z]; cq = xq[z]; }
-            quad_weights(cp, cq, residual, ps.m, pinv, qs.m, qinv, invT, pw, rw);
-            float w[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) w[j] = (e + j < chi) ? (use_p ? pw[j] : rw[j]) : 0.0f;
-            const double t4 = static_cast<double>((w[0] + w[1]) + (w[2] + w[3]));
-            const double incl = warp_incl_scan_d(t4);
-            if (lane == 31) s_scan[warp] = incl;
-            // the last element with mass, for the rounding fallback
-            int lp = -1;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (w[j] > 0.0f) lp = static_cast<int>(e + j);
-            lp = __reduce_max_sync(kFull, lp);
-            if (lane == 0 && lp >= 0) atomicMax(&s_lastpos, lp);
-            __syncthreads();
-            double woff = 0.0, stotal = 0.0;
-#pragma unroll
-            for (int ww = 0; ww < kWarps; ++ww) {
-                if (ww < warp) woff += s_scan[ww];
-                stotal += s_scan[ww];
-            }
-            if (running + stotal > target) {
-                double c = running + woff + incl - t4;
-                for (int j = 0; j < 4; ++j) {
-                    c += static_cast<double>(w[j]);
-                    if (w[j] > 0.0f && target < c) { atomicMin(&s_pick, e + j); break; }
-                }
-            }
-            __syncthreads();
-            running += stotal;
-            if (s_pick != kNoIdx) break;
-        }
-        if (s_pick != kNoIdx) break;
+        for (int j = 0; j < 4; ++j) w[4u * i + j] = use_p ? pw[j] : rw[j];
     }
-    if (tid == 0) {
-        // no crossing found (rounding): the last element with mass
-        const uint32_t pick = s_pick != kNoIdx ? s_pick : (s_lastpos >= 0 ? static_cast<uint32_t>(s_lastpos) : clo);
+    FF mine{0.0f, 0.0f};
+    int lp = -1;  // this thread's last id with mass
+#pragma unroll
+    for (uint32_t j = 0; j < kDrawPer; ++j) {
+        mine = ff_add(mine, FF{w[j], 0.0f});
+        if (w[j] > 0.0f) lp = static_cast<int>(e0 + j);
+    }
+    // exclusive block scan of the thread sums, in thread (= id) order
+    const FF incl = ff_warp_scan(mine);
+    if (lane == 31) s_wtot[warp] = incl;
+    const int wlp = __reduce_max_sync(kFull, lp);
+    if (lane == 0 && wlp >= 0) atomicMax(&s_lastpos, wlp);
+    __syncthreads();
+    FF start = ff_from_double(s_before);
+    for (int ww = 0; ww < warp; ++ww) start = ff_add(start, s_wtot[ww]);
+    FF excl = ff_shfl_up(incl, 1);
+    if (lane == 0) excl = FF{0.0f, 0.0f};
+    start = ff_add(start, excl);
+    const FF end = ff_add(start, mine);
+    // the first thread whose range ends past the target holds the draw
+    const uint32_t hit = __ballot_sync(kFull, mine.hi > 0.0f && ff_lt(target, end));
+    if (lane == 0 && hit) atomicMin(&s_cross, static_cast<uint32_t>(tid) + static_cast<uint32_t>(__ffs(hit) - 1));
+    __syncthreads();
+    if (static_cast<uint32_t>(tid) == s_cross) {
+        uint32_t pick = kNoIdx;
+        FF cdf = start;
+#pragma unroll
+        for (uint32_t j = 0; j < kDrawPer; ++j) {  // unrolled: w stays in registers
+            cdf = ff_add(cdf, FF{w[j], 0.0f});
+            if (pick == kNoIdx && w[j] > 0.0f && ff_lt(target, cdf)) pick = e0 + j;
+        }
+        if (pick == kNoIdx) pick = static_cast<uint32_t>(lp);  // rounding: its last id with mass
         a.emitted[static_cast<size_t>(s) * (K + 1u) + d.jstar] = pick;
+    }
+    if (tid == 0 && s_cross == kNoIdx) {
+        // no crossing found (rounding): the last id with mass in the chunk
+        a.emitted[static_cast<size_t>(s) * (K + 1u) + d.jstar] =
+            s_lastpos >= 0 ? static_cast<uint32_t>(s_lastpos) : clo;
     }
 }
 
@@ -632,6 +682,7 @@ extern "C" sel_status spec_accept(const float* d_target, const float* d_draft, c
     a.emitted = d_emitted;
     a.S = S; a.K = K; a.V = V;
     a.T = rej ? p->temperature : 1.0f;
+    a.log2e_over_T = static_cast<float>(1.4426950408889634 / static_cast<double>(a.T));
     a.cfg = StreamCfg{rows1 * plan.chunks, plan.chunks, plan.chunk_elems, V};
     a.err = reinterpret_cast<uint32_t*>(ws);
     a.row_ctr = reinterpret_cast<uint32_t*>(ws + l.row_ctr);
@@ -652,7 +703,7 @@ extern "C" sel_status spec_accept(const float* d_target, const float* d_draft, c
     if (!rej) return SEL_OK;
 
     static const int res2 = resident_blocks(spec_draw_kernel<true>, kNT);
-    const RowPlan plan2 = plan_rows(S, V, sms, kGrain, kMaxChunks, kOverhead, res2);
+    const RowPlan plan2 = plan_rows(S, V, sms, kGrain, kMaxChunks, kOverhead, res2, kDrawChunkMax);
     DrawArgs b{};
     b.target = d_target;
     b.draft = d_draft;

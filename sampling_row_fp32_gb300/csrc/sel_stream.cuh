@@ -19,16 +19,16 @@
 //
 // Unaligned rows take the same loop with direct scalar loads.
 //
-// Every wait is bounded: after kWaitPolls failed polls the block records
-// SEL_WS_ERR_TIMEOUT in the workspace error word, waits (bounded again) for
-// its own copies still in flight and returns.
+// Every wait is bounded: after kWaitPolls suspended polls (about two
+// seconds) the block records a timeout bit in the workspace error word,
+// waits (bounded again) for its own copies still in flight and returns.
 #pragma once
 
 #include "sel_common.cuh"
 
 namespace sel {
 
-constexpr uint32_t kWaitPolls = 1u << 22;
+constexpr uint32_t kWaitPolls = 10000;  // x kSuspendNs: about 2 s at most
 constexpr uint32_t kErrTimeout = 1u;       // a bulk-copy wait gave up
 constexpr uint32_t kErrMergeShort = 2u;    // a row merge found fewer than k candidates
 constexpr uint32_t kErrListOrder = 4u;     // a chunk list was not in descending order
@@ -60,14 +60,17 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
+// One bounded wait: the thread sleeps until the phase completes or
+// kSuspendNs elapse (no busy polling).
+constexpr uint32_t kSuspendNs = 200000;  // 0.2 ms
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
         : "memory");
     return ok != 0;
 }

@@ -456,7 +456,8 @@ __global__ void __launch_bounds__(kNT, 2) topk_kernel(TopkArgs a) {
             if (tid == 0) s.count = pre;
             __syncthreads();
             overflow_chunk<kTma>(s, a.logits + static_cast<size_t>(t.row) * V, t.lo, t.hi, k, tau);
-        } else if (s.count > kCap / 2) {
+        } else if (s.count > k) {
+            // keep the buffer at its top k, so its k-th key filters the next chunk
             reduce_buffer(s, k);
         }
     };
