@@ -41,6 +41,7 @@ ROW_BYTES = V * 4
 WORKLOAD = "batched verify selection 49 x 248,320 fp32"
 METRIC = "logits rows/s and achieved HBM GB/s (% of GB300 peak) at V=248k, rows=1-49"
 N_COPIES = 6          # rotating copies of the batch (6 x 48.7 MB)
+OP_REPS = 30          # launches per op in the per-op timed regions
 
 
 def measured_peak():
@@ -195,30 +196,29 @@ def gpu_arm(args, rank, world, local_rank):
     bytes_per_op[3] = (SPEC_S * (2 * SPEC_K + 1) + resid_rows) * ROW_BYTES
 
     # Each step is replayed from a CUDA graph of its five calls (six kernels),
-    # so the host's launch cost does not gap the GPU. Event-record nodes in
-    # the graph bracket every op on the launching stream; a graph's events
-    # hold the times of its latest replay.
+    # so the host's launch cost does not gap the GPU.
     n_graphs = min(args.steps, 60)
-    graphs, evs = [], []
-    graph_events = True
+    graphs = []
     for gi in range(n_graphs):
-        try:
-            e = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(6)]
-        except TypeError:
-            graph_events, e = False, None
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            if e:
-                e[0].record()
             for op in range(5):
                 run_op(gi, op)
-                if e:
-                    e[op + 1].record()
         graphs.append(g)
-        evs.append(e)
+    # per-op timing: one graph of OP_REPS launches of each op (same input
+    # rotation), bracketed by events on the launching stream
+    op_graphs = []
+    for op in range(5):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for r in range(OP_REPS):
+                run_op(r, op)
+        op_graphs.append(g)
     with torch.cuda.stream(stream):
         for s in range(args.warmup):
             graphs[s % n_graphs].replay()
+        for g in op_graphs:
+            g.replay()
     torch.cuda.synchronize()
 
     if world > 1:
@@ -236,24 +236,17 @@ def gpu_arm(args, rank, world, local_rank):
             graphs[s % n_graphs].replay()
         t_end.record(stream)
     torch.cuda.synchronize()
-    if graph_events:
-        # graph g's events hold its latest replay inside the timed region
-        per_op_us = [statistics.mean(evs[gi][op].elapsed_time(evs[gi][op + 1]) for gi in range(n_graphs)) * 1e3
-                     for op in range(5)]
-    else:
-        # this torch cannot put event nodes in a graph: time each op eagerly
-        per_op_us = [0.0] * 5
-        reps = 10
-        for op in range(5):
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                a.record(stream)
-                for r in range(reps):
-                    run_op(r, op)
-                b.record(stream)
-            torch.cuda.synchronize()
-            per_op_us[op] = a.elapsed_time(b) * 1e3 / reps
+    # per-op timed regions, right after the steps (same clocks)
+    per_op_us = []
+    for op in range(5):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            op_graphs[op].replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        per_op_us.append(a.elapsed_time(b) * 1e3 / OP_REPS)
     # keep the same load running briefly so the clock sampler sees it even
     # when the timed region is shorter than its period
     tail_until = time.time() + 0.6
@@ -266,8 +259,6 @@ def gpu_arm(args, rank, world, local_rank):
         torch.cuda.synchronize()
     clk = clocks.stop()
     total_ms = t_start.elapsed_time(t_end)
-    per_op_us = [statistics.mean(evs[s][op].elapsed_time(evs[s][op + 1]) for s in range(args.steps)) * 1e3
-                 for op in range(5)]
     if world > 1:
         import torch
         import torch.distributed as dist
@@ -315,8 +306,8 @@ def gpu_arm(args, rank, world, local_rank):
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
                      "traffic": traffic},
         "gpu_launches": launches_per_step * args.steps,
-        "timing": "CUDA graph per step; per-op event nodes" if graph_events else
-                  "CUDA graph per step; per-op times from eager launches",
+        "timing": f"steps replayed from CUDA graphs; per-op times from {OP_REPS} graph-replayed "
+                  "launches of each op between events on the launching stream",
         "clocks": clk,
         "e2e": e2e,
     }

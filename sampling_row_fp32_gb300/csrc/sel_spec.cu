@@ -28,8 +28,10 @@
 //    sequence finds the chunk where u_fin * total falls and scans it in id
 //    order for the drawn token. Rows are therefore read at most twice, and
 //    only the rejecting position's rows are read again.
-// Sums are pairwise in fp32 over each thread's values and double across
-// threads, blocks and chunks, so the CDF is accurate to ~1e-7 of its total.
+// exp((x - m) / T) is computed as 2^((x - m) * log2(e) / T) with the SFU's
+// exp2 (relative error about 2^-22). Each thread sums its values in fp32;
+// sums across threads, blocks and chunks are float-float (about 44 bits), so
+// the CDF is accurate to ~1e-7 of its total.
 #include <cfloat>
 
 #include "sel_plan.h"
@@ -66,8 +68,8 @@ struct alignas(16) Decision {
 };
 
 struct alignas(16) DrawPart {
-    double r;  // residual mass of the chunk
-    double p;  // target mass of the chunk (fallback)
+    FF r;  // residual mass of the chunk (float-float)
+    FF p;  // target mass of the chunk (fallback)
 };
 
 struct SpecLayout {
@@ -126,22 +128,6 @@ __device__ __forceinline__ const float* phase1_row(const SpecArgs& a, uint32_t r
     }
     seq = (r - nt) / a.K;
     return a.draft + static_cast<size_t>(r - nt) * a.V;
-}
-
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-    for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(kFull, v, m);
-    return v;
-}
-
-__device__ __forceinline__ double warp_incl_scan_d(double v) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
-        const double o = __shfl_up_sync(kFull, v, m);
-        if (lane >= m) v += o;
-    }
-    return v;
 }
 
 // The acceptance chain of one sequence, run by one warp once every row of
@@ -401,9 +387,9 @@ struct DrawArgs {
     const float* u_fin;
     uint32_t* emitted;
     uint32_t S, K, V;
-    float T;
+    float log2e_over_T;
     uint32_t chunks;
-    uint32_t chunk_elems;
+    uint32_t chunk_elems;  // a multiple of 1024, at most kDrawChunkMax
     uint32_t* seq_ctr;
     const RowPart* row_stats;
     const Decision* decisions;
@@ -411,50 +397,41 @@ struct DrawArgs {
     uint32_t cmax;
 };
 
-// Weights of 4 elements of the draw distribution: p, and the residual
-// max(p - q, 0) (or p again for a bonus draw). Padding (-inf) weighs 0.
+// Phase 2: the inverse-CDF draw from the residual (or from p).
+// Every block sums the weights of one chunk of the rows the decision names;
+// the last block of the sequence finds the chunk where u_fin * total falls
+// (a fixed-order scan of the chunk sums), then scans that chunk in id order
+// with each thread owning kDrawPer consecutive ids. All sums are float-float.
+constexpr uint32_t kDrawPer = 64;
+constexpr uint32_t kDrawChunkMax = kNT * kDrawPer;  // 16,384
+
+// Weights of 4 elements of the draw distribution: p = exp((x - m_p) / T) / Z_p
+// and the residual max(p - q, 0) (p again for a bonus draw). Padding (-inf)
+// weighs 0.
 __device__ __forceinline__ void quad_weights(const float4& xp, const float4& xq, bool residual, float pm,
-                                             float pinv, float qm, float qinv, float invT, float (&pw)[4],
+                                             float pinv, float qm, float qinv, float c, float (&pw)[4],
                                              float (&rw)[4]) {
     const float fp[4] = {xp.x, xp.y, xp.z, xp.w};
     const float fq[4] = {xq.x, xq.y, xq.z, xq.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const float p = __expf((fp[j] - pm) * invT) * pinv;
-        const float q = residual ? __expf((fq[j] - qm) * invT) * qinv : 0.0f;
+        const float p = ex2_approx((fp[j] - pm) * c) * pinv;
+        const float q = residual ? ex2_approx((fq[j] - qm) * c) * qinv : 0.0f;
         pw[j] = p;
         rw[j] = residual ? fmaxf(p - q, 0.0f) : p;
     }
 }
 
 template <bool kVec>
-__device__ __forceinline__ void draw_weights(const float* prow, const float* qrow, bool residual, uint32_t e,
-                                             uint32_t hi, float pm, float pinv, float qm, float qinv, float invT,
-                                             float (&pw)[4], float (&rw)[4]) {
-    const float4 xp = ld_quad<kVec>(prow, e, hi, -INFINITY);
-    const float4 xq = residual ? ld_quad<kVec>(qrow, e, hi, -INFINITY)
-                               : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    quad_weights(xp, xq, residual, pm, pinv, qm, qinv, invT, pw, rw);
-}
-
-// Phase 2: the inverse-CDF draw from the residual (or from p).
-// Every block sums its chunk; the last block of the sequence finds the chunk
-// where u_fin * total falls (a fixed-order scan of the chunk sums), then scans
-// that chunk in id order with each thread owning kDrawPer consecutive ids.
-constexpr uint32_t kDrawPer = 32;
-constexpr uint32_t kDrawChunkMax = kNT * kDrawPer;  // 8,192
-
-template <bool kVec>
 __global__ void __launch_bounds__(kNT) spec_draw_kernel(DrawArgs a) {
-    __shared__ double s_r[kWarps];
-    __shared__ double s_p[kWarps];
-    __shared__ FF s_wtot[kWarps];
+    __shared__ FF s_r[kWarps];
+    __shared__ FF s_p[kWarps];
     __shared__ bool s_last;
     __shared__ uint32_t s_cross;
     __shared__ int s_lastpos;
     __shared__ bool s_use_p;
     __shared__ uint32_t s_cstar;
-    __shared__ double s_before, s_target;
+    __shared__ FF s_before, s_target;
 
     const uint32_t chunks = a.chunks;
     const uint32_t s = blockIdx.x / chunks;
@@ -473,82 +450,89 @@ __global__ void __launch_bounds__(kNT) spec_draw_kernel(DrawArgs a) {
         qrow = a.draft + static_cast<size_t>(s * K + d.jstar) * V;
         qs = a.row_stats[qrow_i];
     }
-    const float invT = 1.0f / a.T;
+    const float c = a.log2e_over_T;
     const float pinv = 1.0f / ps.s_hi;
     const float qinv = 1.0f / qs.s_hi;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr float kNegInf = -INFINITY;
+    const float4 none = make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
 
+    // chunk sums: coalesced quads, all loads issued before the arithmetic
     const uint32_t lo = chunk * a.chunk_elems;
     const uint32_t hi = min(V, lo + a.chunk_elems);
+    constexpr int kQ = static_cast<int>(kDrawPer / 4u);
     float rsum = 0.0f, psum = 0.0f;
-    for (uint32_t base = lo + 4u * tid; base < hi; base += 4u * kNT * kVPT) {
-        float4 xp[kVPT], xq[kVPT];
+    {
+        float4 xp[kQ], xq[kQ];
 #pragma unroll
-        for (int sl = 0; sl < kVPT; ++sl) {
-            xp[sl] = ld_quad<kVec>(prow, base + 4u * kNT * sl, hi, -INFINITY);
-            xq[sl] = residual ? ld_quad<kVec>(qrow, base + 4u * kNT * sl, hi, -INFINITY)
-                              : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        for (int i = 0; i < kQ; ++i) {
+            const uint32_t e = lo + 4u * (static_cast<uint32_t>(tid) + kNT * i);
+            xp[i] = ld_quad<kVec>(prow, e, hi, kNegInf);
+            xq[i] = residual ? ld_quad<kVec>(qrow, e, hi, kNegInf) : none;
         }
 #pragma unroll
-        for (int sl = 0; sl < kVPT; ++sl) {
+        for (int i = 0; i < kQ; ++i) {
             float pw[4], rw[4];
-            quad_weights(xp[sl], xq[sl], residual, ps.m, pinv, qs.m, qinv, invT, pw, rw);
+            quad_weights(xp[i], xq[i], residual, ps.m, pinv, qs.m, qinv, c, pw, rw);
             rsum += (rw[0] + rw[1]) + (rw[2] + rw[3]);
             psum += (pw[0] + pw[1]) + (pw[2] + pw[3]);
         }
     }
-    const double wr = warp_sum_d(static_cast<double>(rsum));
-    const double wp = warp_sum_d(static_cast<double>(psum));
+    const FF wr = ff_warp_sum(FF{rsum, 0.0f});
+    const FF wp = ff_warp_sum(FF{psum, 0.0f});
     if (lane == 0) { s_r[warp] = wr; s_p[warp] = wp; }
     __syncthreads();
     if (tid == 0) {
-        double br = 0.0, bp = 0.0;
-        for (int w = 0; w < kWarps; ++w) { br += s_r[w]; bp += s_p[w]; }
-        DrawPart* parts = a.parts + static_cast<size_t>(s) * a.cmax;
-        parts[chunk] = DrawPart{br, bp};
+        FF br{0.0f, 0.0f}, bp{0.0f, 0.0f};
+        for (int w = 0; w < kWarps; ++w) { br = ff_add(br, s_r[w]); bp = ff_add(bp, s_p[w]); }
+        a.parts[static_cast<size_t>(s) * a.cmax + chunk] = DrawPart{br, bp};
         s_last = arrive_is_last(&a.seq_ctr[s], chunks);
     }
     __syncthreads();
     if (!s_last) return;
     __threadfence();  // order this thread's reads after the arrivals it saw
 
-    // last block: locate the chunk, then the element, where u * total falls.
-    // Warp 0 walks the chunk sums 32 at a time in chunk order (fixed-order
-    // scans, so the result does not depend on timing).
+    // last block: warp 0 walks the chunk sums 32 at a time in chunk order
     const DrawPart* parts = a.parts + static_cast<size_t>(s) * a.cmax;
     if (warp == 0) {
-        double R = 0.0, P = 0.0;
+        FF R{0.0f, 0.0f}, P{0.0f, 0.0f};
         for (uint32_t c0 = 0; c0 < chunks; c0 += 32) {
-            const uint32_t c = c0 + lane;
-            double r = c < chunks ? ld_gpu_f64(&parts[c].r) : 0.0;
-            double p = c < chunks ? ld_gpu_f64(&parts[c].p) : 0.0;
-            r = warp_incl_scan_d(r);
-            p = warp_incl_scan_d(p);
-            R += __shfl_sync(kFull, r, 31);
-            P += __shfl_sync(kFull, p, 31);
+            const uint32_t ci = c0 + lane;
+            FF r{0.0f, 0.0f}, p{0.0f, 0.0f};
+            if (ci < chunks) {
+                r = FF{ld_gpu_f32(&parts[ci].r.hi), ld_gpu_f32(&parts[ci].r.lo)};
+                p = FF{ld_gpu_f32(&parts[ci].p.hi), ld_gpu_f32(&parts[ci].p.lo)};
+            }
+            R = ff_add(R, ff_warp_sum(r));
+            P = ff_add(P, ff_warp_sum(p));
         }
-        const bool use_p = !(R > 0.0);  // residual empty by rounding: draw from p
-        const double total = use_p ? P : R;
-        const double target = static_cast<double>(a.u_fin[s]) * total;
+        const bool use_p = !(R.hi > 0.0f);  // residual empty by rounding: draw from p
+        const FF target = ff_mul_f(use_p ? P : R, a.u_fin[s]);
         uint32_t cstar = chunks, last_pos_chunk = 0;
-        double before = 0.0, acc = 0.0, before_last = 0.0;
+        FF before{0.0f, 0.0f}, acc{0.0f, 0.0f}, before_last{0.0f, 0.0f};
         for (uint32_t c0 = 0; c0 < chunks && cstar == chunks; c0 += 32) {
-            const uint32_t c = c0 + lane;
-            const double t = c < chunks ? (use_p ? ld_gpu_f64(&parts[c].p) : ld_gpu_f64(&parts[c].r)) : 0.0;
-            const double incl = warp_incl_scan_d(t) + acc;
-            const uint32_t pos = __ballot_sync(kFull, c < chunks && t > 0.0);
+            const uint32_t ci = c0 + lane;
+            FF t{0.0f, 0.0f};
+            if (ci < chunks) {
+                const FF* src = use_p ? &parts[ci].p : &parts[ci].r;
+                t = FF{ld_gpu_f32(&src->hi), ld_gpu_f32(&src->lo)};
+            }
+            const FF incl = ff_add(acc, ff_warp_scan(t));
+            FF excl = ff_shfl_up(incl, 1);
+            if (lane == 0) excl = acc;
+            const uint32_t pos = __ballot_sync(kFull, ci < chunks && t.hi > 0.0f);
             if (pos) {
                 const int l = 31 - __clz(pos);
                 last_pos_chunk = c0 + l;
-                before_last = __shfl_sync(kFull, incl - t, l);
+                before_last = ff_shfl(excl, l);
             }
-            const uint32_t hit = __ballot_sync(kFull, c < chunks && target < incl);
+            const uint32_t hit = __ballot_sync(kFull, ci < chunks && t.hi > 0.0f && ff_lt(target, incl));
             if (hit) {
                 const int l = __ffs(hit) - 1;
                 cstar = c0 + l;
-                before = __shfl_sync(kFull, incl - t, l);
+                before = ff_shfl(excl, l);
             }
-            acc = __shfl_sync(kFull, incl, 31);
+            acc = ff_shfl(incl, 31);
         }
         if (cstar == chunks) {  // rounding: take the last chunk with mass
             cstar = last_pos_chunk;
@@ -567,20 +551,25 @@ __global__ void __launch_bounds__(kNT) spec_draw_kernel(DrawArgs a) {
     const bool use_p = s_use_p;
     const uint32_t clo = s_cstar * a.chunk_elems;
     const uint32_t chi = min(V, clo + a.chunk_elems);
-    const FF target = ff_from_double(s_target);
+    const FF target = s_target;
 
     // thread tid owns ids [e0, e0 + kDrawPer) of chunk cstar
     const uint32_t e0 = clo + kDrawPer * static_cast<uint32_t>(tid);
     float w[kDrawPer];
+    {
+        float4 xp[kQ], xq[kQ];
 #pragma unroll
-    for (uint32_t i = 0; i < kDrawPer / 4u; ++i) {
-        const float4 xp = ld_quad<kVec>(prow, e0 + 4u * i, chi, -INFINITY);
-        const float4 xq = residual ? ld_quad<kVec>(qrow, e0 + 4u * i, chi, -INFINITY)
-                                   : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        float pw[4], rw[4];
-        quad_weights(xp, xq, residual, ps.m, pinv, qs.m, qinv, invT, pw, rw);
+        for (int i = 0; i < kQ; ++i) {
+            xp[i] = ld_quad<kVec>(prow, e0 + 4u * i, chi, kNegInf);
+            xq[i] = residual ? ld_quad<kVec>(qrow, e0 + 4u * i, chi, kNegInf) : none;
+        }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) w[4u * i + j] = use_p ? pw[j] : rw[j];
+        for (int i = 0; i < kQ; ++i) {
+            float pw[4], rw[4];
+            quad_weights(xp[i], xq[i], residual, ps.m, pinv, qs.m, qinv, c, pw, rw);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) w[4 * i + j] = use_p ? pw[j] : rw[j];
+        }
     }
     FF mine{0.0f, 0.0f};
     int lp = -1;  // this thread's last id with mass
@@ -591,12 +580,12 @@ __global__ void __launch_bounds__(kNT) spec_draw_kernel(DrawArgs a) {
     }
     // exclusive block scan of the thread sums, in thread (= id) order
     const FF incl = ff_warp_scan(mine);
-    if (lane == 31) s_wtot[warp] = incl;
+    if (lane == 31) s_r[warp] = incl;
     const int wlp = __reduce_max_sync(kFull, lp);
     if (lane == 0 && wlp >= 0) atomicMax(&s_lastpos, wlp);
     __syncthreads();
-    FF start = ff_from_double(s_before);
-    for (int ww = 0; ww < warp; ++ww) start = ff_add(start, s_wtot[ww]);
+    FF start = s_before;
+    for (int ww = 0; ww < warp; ++ww) start = ff_add(start, s_r[ww]);
     FF excl = ff_shfl_up(incl, 1);
     if (lane == 0) excl = FF{0.0f, 0.0f};
     start = ff_add(start, excl);
@@ -702,23 +691,30 @@ extern "C" sel_status spec_accept(const float* d_target, const float* d_draft, c
     if (cudaGetLastError() != cudaSuccess) return SEL_ECUDA;
     if (!rej) return SEL_OK;
 
-    static const int res2 = resident_blocks(spec_draw_kernel<true>, kNT);
-    const RowPlan plan2 = plan_rows(S, V, sms, kGrain, kMaxChunks, kOverhead, res2, kDrawChunkMax);
+    // phase 2: one wave of blocks when the sequences allow it (S * chunks
+    // <= SMs), chunks of at most kDrawChunkMax ids, a multiple of 1024
+    uint32_t chunks2 = static_cast<uint32_t>(sms) / S;
+    const uint32_t cmin2 = ceil_div(V, kDrawChunkMax);
+    if (chunks2 < cmin2) chunks2 = cmin2;
+    if (chunks2 > l.cmax_b) chunks2 = l.cmax_b;
+    const uint32_t ce2 = static_cast<uint32_t>(align_up(ceil_div(V, chunks2), kGrain));
+    chunks2 = ceil_div(V, ce2);
+    if (static_cast<uint64_t>(S) * chunks2 > 0x7fffffffull) return SEL_EUNSUPPORTED;
     DrawArgs b{};
     b.target = d_target;
     b.draft = d_draft;
     b.u_fin = d_u_fin;
     b.emitted = d_emitted;
     b.S = S; b.K = K; b.V = V;
-    b.T = p->temperature;
-    b.chunks = plan2.chunks;
-    b.chunk_elems = plan2.chunk_elems;
+    b.log2e_over_T = a.log2e_over_T;
+    b.chunks = chunks2;
+    b.chunk_elems = ce2;
     b.seq_ctr = reinterpret_cast<uint32_t*>(ws + l.seq_ctr_b);
     b.row_stats = a.row_stats;
     b.decisions = a.decisions;
     b.parts = reinterpret_cast<DrawPart*>(ws + l.draw_parts);
     b.cmax = l.cmax_b;
-    const dim3 grid2(S * plan2.chunks);
+    const dim3 grid2(S * chunks2);
     if (vec) spec_draw_kernel<true><<<grid2, kNT, 0, stream>>>(b);
     else spec_draw_kernel<false><<<grid2, kNT, 0, stream>>>(b);
     return cudaGetLastError() == cudaSuccess ? SEL_OK : SEL_ECUDA;

@@ -21,8 +21,10 @@
 //     shared-memory buffer as 64-bit candidates (key << 32 | ~id), which
 //     order exactly like (value desc, id asc).
 //  3. The buffer persists over the consecutive chunks of a row that the
-//     block owns; once it holds k candidates, its k-th key also filters later
-//     chunks (their ids are higher, so an equal key cannot displace it). When
+//     block owns; the first chunk's bound filters them all, and whenever the
+//     buffer passes k + 32 entries it is selected down to its top k, whose
+//     k-th key then filters later chunks (their ids are higher, so an equal
+//     key cannot displace it). When
 //     the block leaves the row it selects the segment's top k (rank counting
 //     for small buffers, bitonic sort otherwise) and publishes them, sorted,
 //     in the workspace. A buffer overflow (adversarial chunks such as
@@ -50,6 +52,7 @@ constexpr uint32_t kUnit = 4u * kNT * kVPT;  // 8,192 elements per chunk
 constexpr uint32_t kCap = 2048;              // candidate buffer (>= SEL_MAX_K + 4 * kNT)
 constexpr uint32_t kRankMax = 512;           // rank counting up to this many candidates
 constexpr uint32_t kFastMergeLists = 32;     // one warp lane per chunk list
+constexpr uint32_t kReduceSlack = 32;        // select the buffer down to k above k + this many
 
 static_assert(kCap >= SEL_MAX_K + 4 * kNT, "a slot of 1,024 must fit after a selection");
 
@@ -379,6 +382,24 @@ __device__ __forceinline__ void write_row(const TopkShared& s, const TopkArgs& a
     }
 }
 
+// Merge the published lists of a row whose segments have all arrived and
+// write its result. Block-collective.
+template <bool kSample>
+__device__ void finish_row(TopkShared& s, const TopkArgs& a, uint32_t row) {
+    const uint32_t k = a.k;
+    __threadfence();  // order this thread's reads after the arrivals it saw
+    const uint32_t count = segment_of(a.cfg, row).count;
+    uint32_t nf = 0;
+    const int lane = threadIdx.x & 31;
+    for (uint32_t c = lane; c < count; c += 32)
+        nf |= ld_gpu_u32(a.chunk_flags + static_cast<size_t>(row) * a.stride + c);
+    nf = __reduce_or_sync(kFull, nf);
+    merge_row_lists(s, a.lists + static_cast<size_t>(row) * a.stride * k, count, k, a.err);
+    write_row<kSample>(s, a, row, k, nf != 0);
+    if (threadIdx.x == 0) atomicAdd(a.err + 1, 1u);  // rows finished (self-check)
+    __syncthreads();
+}
+
 template <bool kTma, bool kSample>
 __global__ void __launch_bounds__(kNT, 2) topk_kernel(TopkArgs a) {
     extern __shared__ float4 stages[];
@@ -393,6 +414,11 @@ __global__ void __launch_bounds__(kNT, 2) topk_kernel(TopkArgs a) {
     // some x is +-Inf or NaN. Padding past the row end is -FLT_MAX (finite,
     // never above a real logit) and is never appended.
     float nfacc = 0.0f;
+    // Block-uniform state of the current segment, kept in registers: the
+    // buffer's entry count after the last sync, the chunk bound of the
+    // segment's first chunk (0 = none yet) and the buffer's k-th key after
+    // its last selection (0 = none).
+    uint32_t cnt = 0, tau = 0, tau_key = 0;
     if (tid == 0) { s.count = 0; s.tau_key = 0; }
     __syncthreads();
 
@@ -409,22 +435,16 @@ __global__ void __launch_bounds__(kNT, 2) topk_kernel(TopkArgs a) {
             nfacc = __fmaf_rn(q[sl].z, 0.0f, nfacc);
             nfacc = __fmaf_rn(q[sl].w, 0.0f, nfacc);
         }
-        // threshold: once the buffer holds k candidates its k-th key bounds
-        // every later (higher-id) element; before that, the chunk bound
-        // (>= k elements of this chunk have key >= tau) does
-        // the buffer state is read by every thread before anyone appends
-        const uint32_t pre = s.count, tau_key = s.tau_key;
-        const bool have_k = pre >= k && tau_key != 0;
-        const bool bound = !have_k && k <= 32u * kWarps;
-        if (bound) {
+        // The segment's first chunk sets the chunk bound: >= k of its
+        // elements have key >= tau, so no element below tau is in the
+        // segment's top k. Once a selection has left k candidates in the
+        // buffer, its k-th key bounds every later (higher-id) element too.
+        if (tau == 0 && tau_key == 0 && k <= 32u * kWarps) {
             const uint32_t v = warp_sort_desc(f2key(tmax));
             const uint32_t r = (k + kWarps - 1) / kWarps;
             const uint32_t wv = __shfl_sync(kFull, v, r - 1);
             if (lane == 0) s.warp_val[warp] = wv;
-        }
-        __syncthreads();
-        uint32_t tau = 0;
-        if (bound) {
+            __syncthreads();
             tau = s.warp_val[0];
 #pragma unroll
             for (int w = 1; w < kWarps; ++w) tau = min(tau, s.warp_val[w]);
@@ -451,20 +471,27 @@ __global__ void __launch_bounds__(kNT, 2) topk_kernel(TopkArgs a) {
             }
         }
         __syncthreads();
-        if (s.count > kCap) {
+        const uint32_t now = s.count;
+        if (now > kCap) {
             __syncthreads();
-            if (tid == 0) s.count = pre;
+            if (tid == 0) s.count = cnt;
             __syncthreads();
             overflow_chunk<kTma>(s, a.logits + static_cast<size_t>(t.row) * V, t.lo, t.hi, k, tau);
-        } else if (s.count > k) {
-            // keep the buffer at its top k, so its k-th key filters the next chunk
+            cnt = s.count;
+            tau_key = s.tau_key;
+        } else if (now > k + kReduceSlack) {
+            // keep the buffer small: its top k, whose k-th key filters later chunks
             reduce_buffer(s, k);
+            cnt = s.count;
+            tau_key = s.tau_key;
+        } else {
+            cnt = now;
         }
     };
 
     auto flush = [&](const Segment& g) {
         // this segment's top k, sorted
-        const uint32_t n = min(s.count, kCap);
+        const uint32_t n = min(cnt, kCap);
         block_select_sorted(s.buf, n, k, s.sorted);
         const uint32_t have = n < k ? n : k;
         const uint32_t nf_local = __any_sync(kFull, nfacc != 0.0f) ? 1u : 0u;
@@ -489,19 +516,15 @@ __global__ void __launch_bounds__(kNT, 2) topk_kernel(TopkArgs a) {
                 s.last = segment_arrive(&a.counters[g.row], g.count) ? 1u : 0u;
             }
             __syncthreads();
-            if (s.last) {
-                __threadfence();  // order this thread's reads after the arrivals it saw
-                nf = 0;
-                for (uint32_t c = lane; c < g.count; c += 32)
-                    nf |= ld_gpu_u32(a.chunk_flags + static_cast<size_t>(g.row) * a.stride + c);
-                nf = __reduce_or_sync(kFull, nf);
-                merge_row_lists(s, a.lists + static_cast<size_t>(g.row) * a.stride * k, g.count, k, a.err);
-                write_row<kSample>(s, a, g.row, k, nf != 0);
-                if (tid == 0) atomicAdd(a.err + 1, 1u);  // rows finished (self-check)
-            }
+            // the block that completed the row merges it now, while its
+            // next chunks are still arriving in the staging ring
+            if (s.last) finish_row<kSample>(s, a, g.row);
         }
         __syncthreads();
         if (tid == 0) { s.count = 0; s.tau_key = 0; }
+        cnt = 0;
+        tau = 0;
+        tau_key = 0;
         __syncthreads();
     };
 
