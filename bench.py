@@ -9,9 +9,11 @@ log-probabilities, seed 2) through the whole selection path via the C ABI:
 value = verify-batch rows taken through that path per second (49 per step
 and rank). Inputs are resident in HBM before the timed region; every launch
 reads a copy of the batch that no launch has touched within the previous
->= 243 MB of traffic (more than the 129 MB L2), so each read comes from HBM.
+>= 487 MB of traffic (more than 3.7 x the 129 MB L2), so each read comes
+from HBM.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+  python bench.py --profile-steps P    # P untimed eager steps (for ncu), then exit
 
 With --impl reference the CPU oracle (the plain, double-precision C
 implementation the tests check against) runs a bounded sample of the same
@@ -40,8 +42,9 @@ POLICY = dict(temperature=0.7, top_k=40, top_p=0.9, min_p=0.05)
 ROW_BYTES = V * 4
 WORKLOAD = "batched verify selection 49 x 248,320 fp32"
 METRIC = "logits rows/s and achieved HBM GB/s (% of GB300 peak) at V=248k, rows=1-49"
-N_COPIES = 6          # rotating copies of the batch (6 x 48.7 MB)
-OP_REPS = 30          # launches per op in the per-op timed regions
+N_COPIES = 11         # rotating copies of the batch: 11 x 48.7 MB = 535 MB >= 4 x L2
+OP_REPS = 110         # launches per op in the per-op timed regions (a multiple of N_COPIES)
+N_GRAPHS = 5 * N_COPIES  # captured step graphs; step s replays graph s % N_GRAPHS
 
 
 def measured_peak():
@@ -158,7 +161,7 @@ def gpu_arm(args, rank, world, local_rank):
     arg = B.SpecParams(1.0, B.SPEC_MODE_ARGMAX)
     OPS = ["argmax", "topk", "sample", "spec_rejection", "spec_argmax"]
     # the copy each op of step s reads: consecutive reads walk the N_COPIES
-    # copies in turn, so a copy is read again only after 5 others (243 MB)
+    # copies in turn, so a copy is read again only after 10 others (487 MB)
     def copy_for(step, op):
         return xs[(5 * step + op) % N_COPIES]
 
@@ -195,9 +198,19 @@ def gpu_arm(args, rank, world, local_rank):
     resid_rows = int(sum(2 if a < SPEC_K else 1 for a in n_acc))
     bytes_per_op[3] = (SPEC_S * (2 * SPEC_K + 1) + resid_rows) * ROW_BYTES
 
+    if args.profile_steps:
+        # untimed eager steps for a profiler, nothing else
+        with torch.cuda.stream(stream):
+            for s in range(args.profile_steps):
+                for op in range(5):
+                    run_op(s, op)
+        torch.cuda.synchronize()
+        return None
+
     # Each step is replayed from a CUDA graph of its five calls (six kernels),
-    # so the host's launch cost does not gap the GPU.
-    n_graphs = min(args.steps, 60)
+    # so the host's launch cost does not gap the GPU. Step s (warm-up steps
+    # first) replays graph s % N_GRAPHS, which keeps the copy rotation.
+    n_graphs = N_GRAPHS
     graphs = []
     for gi in range(n_graphs):
         g = torch.cuda.CUDAGraph()
@@ -232,7 +245,7 @@ def gpu_arm(args, rank, world, local_rank):
     t_end = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         t_start.record(stream)
-        for s in range(args.steps):
+        for s in range(args.warmup, args.warmup + args.steps):
             graphs[s % n_graphs].replay()
         t_end.record(stream)
     torch.cuda.synchronize()
@@ -250,7 +263,7 @@ def gpu_arm(args, rank, world, local_rank):
     # keep the same load running briefly so the clock sampler sees it even
     # when the timed region is shorter than its period
     tail_until = time.time() + 0.6
-    s = 0
+    s = args.warmup + args.steps
     while time.time() < tail_until:
         with torch.cuda.stream(stream):
             for _ in range(8):
@@ -297,8 +310,8 @@ def gpu_arm(args, rank, world, local_rank):
         "config": {"workload": WORKLOAD, "rows": ROWS, "V": V, "topk_k": K_TOPK,
                    "sample": POLICY, "spec": {"sequences": SPEC_S, "drafts": SPEC_K, "T": 1.0,
                                               "rules": ["rejection", "argmax"]},
-                   "l2": f"inputs rotate over {N_COPIES} resident copies of the batch; each launch "
-                         "reads a copy untouched for >= 243 MB of traffic (L2 is 129 MB)",
+                   "l2": f"inputs rotate over {N_COPIES} resident copies of the batch (535 MB); each "
+                         "launch reads a copy untouched for >= 487 MB of traffic (L2 is 129 MB)",
                    "parallelism": f"replicas x{world} (independent rows)"},
         "step_gbs": round(step_bytes / step_s / 1e9, 1),
         "ops": ops,
@@ -314,16 +327,78 @@ def gpu_arm(args, rank, world, local_rank):
     return line
 
 
+OP_KERNELS = {  # ncu kernel-name patterns of each op's launches
+    "argmax": ["argmax_kernel"],
+    "topk": ["topk_kernel<1, 0>", "topk_kernel<0, 0>"],
+    "sample": ["topk_kernel<1, 1>", "topk_kernel<0, 1>"],
+    "spec_rejection": ["spec_phase1_kernel<1, 1>", "spec_phase1_kernel<0, 1>", "spec_draw_kernel"],
+    "spec_argmax": ["spec_phase1_kernel<1, 0>", "spec_phase1_kernel<0, 0>"],
+}
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def sources_fingerprint() -> str:
+    """sha256 over the kernel sources and the public header: counters taken
+    from another fingerprint describe other kernels."""
+    import hashlib
+    h = hashlib.sha256()
+    dirs = [os.path.join(ROOT, "sampling_row_fp32_gb300", "csrc"), os.path.join(ROOT, "include")]
+    for d in dirs:
+        for f in sorted(os.listdir(d)):
+            if f.endswith((".cu", ".cuh", ".h")):
+                h.update(f.encode())
+                with open(os.path.join(d, f), "rb") as fh:
+                    h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def load_traffic(op_name):
-    """dram bytes per launch of the op's kernels from the committed ncu
-    summary, if one exists for the current sources (else null)."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes (read + write) per call of the op, from the committed ncu
+    counters, or None when they were taken on other kernel sources."""
     try:
-        with open(path) as f:
+        with open(TRAFFIC_JSON) as f:
             t = json.load(f)
-        return t.get(op_name)
-    except Exception:
+    except (OSError, ValueError):
         return None
+    if t.get("sources") != sources_fingerprint():
+        return None
+    return t.get("ops", {}).get(op_name)
+
+
+def write_traffic(csv_path):
+    """Turn an ncu CSV of dram__bytes_read.sum / dram__bytes_write.sum per
+    launch (one eager step or more) into profiles/traffic.json: mean bytes
+    per call of each op, stamped with the current sources' fingerprint."""
+    import csv
+    import collections
+    rows = list(csv.reader(open(csv_path)))
+    hdr_i = next(i for i, r in enumerate(rows) if "Kernel Name" in r)
+    hdr = rows[hdr_i]
+    ki, mi, vi, ui, idi = (hdr.index(c) for c in ("Kernel Name", "Metric Name", "Metric Value",
+                                                     "Metric Unit", "ID"))
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+    per_launch = collections.defaultdict(float)
+    names = {}
+    for r in rows[hdr_i + 1:]:
+        if len(r) <= vi or r[mi] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        per_launch[r[idi]] += float(r[vi].replace(",", "")) * scale[r[ui]]
+        names[r[idi]] = r[ki]
+    ops = {}
+    for op, pats in OP_KERNELS.items():
+        by_kernel = collections.defaultdict(list)
+        for lid, b in per_launch.items():
+            for p in pats:
+                if p in names[lid]:
+                    by_kernel[p].append(b)
+        if by_kernel:
+            ops[op] = round(sum(sum(v) / len(v) for v in by_kernel.values()))
+    out = {"sources": sources_fingerprint(), "unit": "bytes per call (dram read + write)",
+           "source_csv": os.path.basename(csv_path), "ops": ops}
+    with open(TRAFFIC_JSON, "w") as f:
+        json.dump(out, f, indent=1)
+        f.write("\n")
+    return out
 
 
 def e2e_leg(args, B, dev, x, si, u, prm, rej, arg, ws_a, ws_t, ws_s, ws_r, ws_g):
@@ -440,7 +515,14 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--profile-steps", type=int, default=0,
+                    help="run this many untimed eager steps (for ncu) and exit")
+    ap.add_argument("--traffic-from", default=None,
+                    help="write profiles/traffic.json from an ncu CSV of dram bytes and exit")
     args = ap.parse_args()
+    if args.traffic_from:
+        print(json.dumps(write_traffic(args.traffic_from)))
+        return
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
@@ -458,6 +540,9 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     line = gpu_arm(args, rank, world, local_rank)
+    if line is None:  # --profile-steps
+        print("profile steps done", flush=True)
+        return
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline() if world == 1 else None
         print(json.dumps(line), flush=True)

@@ -257,6 +257,56 @@ sel_status spec_accept(const float *d_target, const float *d_draft,
 sel_status sel_argmax_noalloc(const float *d_logits, uint32_t rows, uint32_t V,
                               uint32_t *d_out_ids, cudaStream_t stream);
 
+/*
+ * Vocabulary shards -- llama.cpp PR 49, "Problem": under a tensor split each
+ * GPU holds a share of the output head (about 155k and 93k of the 248k
+ * columns there), so each computes the logits of one contiguous id range.
+ * A shard runs sel_topk on its own slice (shard-local ids); the lists of all
+ * shards of a row, gathered into one buffer, merge into the top k of the
+ * whole row, with the same values, ids and order as sel_topk on the
+ * unsharded row (ties: lower global id). Argmax is the case k = 1.
+ *
+ *   d_vals     [rows][G][k] f32: shard g's sel_topk values for each row
+ *   d_ids      [rows][G][k] u32: shard g's sel_topk ids (local to the shard)
+ *   G          number of shards, 1 <= G <= SEL_MAX_SHARDS
+ *   k          entries per shard list, 1 <= k <= SEL_MAX_K
+ *   h_offsets  HOST array of G + 1 increasing ids: shard g covers global
+ *              ids [h_offsets[g], h_offsets[g+1]), at least k of them;
+ *              h_offsets[G] <= SEL_MAX_V. Read during the call only.
+ *   d_out_vals, d_out_ids  [rows][k]: the merged top k, global ids
+ * A row in which any shard reported 0xFFFFFFFF (nonfinite logits), or whose
+ * lists are malformed (an id outside its shard, a nonfinite value, a list
+ * out of order), gets NaN values and 0xFFFFFFFF ids. No workspace: one block
+ * per row, launched on `stream`. The gather itself (all-gather of the lists
+ * between GPUs) is the caller's.
+ */
+#define SEL_MAX_SHARDS 64u
+sel_status sel_merge_shards(const float *d_vals, const uint32_t *d_ids,
+                            uint32_t rows, uint32_t G, uint32_t k,
+                            const uint32_t *h_offsets, float *d_out_vals,
+                            uint32_t *d_out_ids, cudaStream_t stream);
+
+/*
+ * sel_sample_shards -- the sampling stage of sel_sample on gathered shard
+ * lists. With the top-k filter first in the chain (Muser ch. 21, 21.7), the
+ * rest of the chain needs only the top_k candidates (llama.cpp PR 49,
+ * "Change"): the merged lists give exactly the candidates sel_sample finds
+ * in the whole row, so the result (id, probability) is that of sel_sample
+ * on the unsharded row with the same policy and uniforms.
+ *
+ *   d_vals, d_ids, rows, G, k, h_offsets  as for sel_merge_shards; each
+ *              shard list is sel_topk(slice, k) with k = p->top_k (any k
+ *              when p->temperature == 0: greedy takes the top candidate)
+ *   p, d_uniforms, d_out_ids, d_out_probs  as for sel_sample
+ * Per-row errors as for sel_sample (0xFFFFFFFF, probability NaN).
+ */
+sel_status sel_sample_shards(const float *d_vals, const uint32_t *d_ids,
+                             uint32_t rows, uint32_t G, uint32_t k,
+                             const uint32_t *h_offsets,
+                             const sel_sample_params *p,
+                             const float *d_uniforms, uint32_t *d_out_ids,
+                             float *d_out_probs, cudaStream_t stream);
+
 /* Static description of a status code. */
 const char *sel_status_string(sel_status status);
 

@@ -26,8 +26,10 @@ SEL_ORDER_TEMP_FIRST, SEL_ORDER_TEMP_LAST = 0, 1
 SPEC_MODE_REJECTION, SPEC_MODE_ARGMAX = 0, 1
 
 EXPORTED = ("sel_workspace_bytes", "sel_workspace_init", "sel_argmax", "sel_topk",
-            "sel_sample", "spec_accept", "sel_status_string", "sel_argmax_noalloc")
+            "sel_sample", "spec_accept", "sel_status_string", "sel_argmax_noalloc",
+            "sel_merge_shards", "sel_sample_shards")
 SEL_NOALLOC_SCRATCH_BYTES = 1 << 20
+SEL_MAX_SHARDS = 64
 
 
 class SelError(RuntimeError):
@@ -84,6 +86,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.spec_accept.restype = ctypes.c_int
     lib.sel_argmax_noalloc.argtypes = [_vp, _u32, _u32, _vp, _vp]
     lib.sel_argmax_noalloc.restype = ctypes.c_int
+    lib.sel_merge_shards.argtypes = [_vp, _vp, _u32, _u32, _u32, _vp, _vp, _vp, _vp]
+    lib.sel_merge_shards.restype = ctypes.c_int
+    lib.sel_sample_shards.argtypes = [_vp, _vp, _u32, _u32, _u32, _vp, ctypes.POINTER(SampleParams),
+                                      _vp, _vp, _vp, _vp]
+    lib.sel_sample_shards.restype = ctypes.c_int
     lib.sel_status_string.argtypes = [ctypes.c_int]
     lib.sel_status_string.restype = ctypes.c_char_p
     if path is None:
@@ -195,6 +202,42 @@ def spec_accept(target, draft, draft_tokens, params: SpecParams, u_acc, u_fin, a
                               ctypes.byref(params), _ptr(u_acc), _ptr(u_fin), _ptr(accepted),
                               _ptr(emitted), _ptr(ws), _nbytes(ws), _stream(stream)),
            "spec_accept")
+
+
+def _host_offsets(offsets):
+    """Shard offsets (G + 1 ints) as a host uint32 array kept alive by the caller."""
+    arr = (ctypes.c_uint32 * len(offsets))(*[int(o) for o in offsets])
+    return arr
+
+
+def sel_merge_shards(vals, ids, offsets, out_vals, out_ids, stream=None) -> None:
+    """vals/ids [rows, G, k] (shard-local ids), offsets G + 1 host ints."""
+    _check_f32(vals, "vals")
+    _check_f32(out_vals, "out_vals")
+    _check_ids(ids, "ids")
+    _check_ids(out_ids, "out_ids")
+    rows, G, k = vals.shape
+    if len(offsets) != G + 1:
+        raise ValueError("offsets must hold G + 1 entries")
+    off = _host_offsets(offsets)
+    _check(load().sel_merge_shards(_ptr(vals), _ptr(ids), rows, G, k, ctypes.cast(off, _vp),
+                                   _ptr(out_vals), _ptr(out_ids), _stream(stream)), "sel_merge_shards")
+
+
+def sel_sample_shards(vals, ids, offsets, params: SampleParams, uniforms, out_ids, out_probs,
+                      stream=None) -> None:
+    _check_f32(vals, "vals")
+    _check_f32(uniforms, "uniforms")
+    _check_f32(out_probs, "out_probs")
+    _check_ids(ids, "ids")
+    _check_ids(out_ids, "out_ids")
+    rows, G, k = vals.shape
+    if len(offsets) != G + 1:
+        raise ValueError("offsets must hold G + 1 entries")
+    off = _host_offsets(offsets)
+    _check(load().sel_sample_shards(_ptr(vals), _ptr(ids), rows, G, k, ctypes.cast(off, _vp),
+                                    ctypes.byref(params), _ptr(uniforms), _ptr(out_ids),
+                                    _ptr(out_probs), _stream(stream)), "sel_sample_shards")
 
 
 # ---------------------------------------------------------------------------

@@ -400,8 +400,10 @@ struct DrawArgs {
 // Phase 2: the inverse-CDF draw from the residual (or from p).
 // Every block sums the weights of one chunk of the rows the decision names;
 // the last block of the sequence finds the chunk where u_fin * total falls
-// (a fixed-order scan of the chunk sums), then scans that chunk in id order
-// with each thread owning kDrawPer consecutive ids. All sums are float-float.
+// (a fixed-order scan of the chunk sums), then, within that chunk, the
+// 1,024-id stripe, the quad and the id. Sums across threads are float-float.
+// The tail is a few block-wide steps rather than one thread's serial walk:
+// straight-line code run once by one thread is bound by instruction fetch.
 constexpr uint32_t kDrawPer = 64;
 constexpr uint32_t kDrawChunkMax = kNT * kDrawPer;  // 16,384
 
@@ -431,7 +433,9 @@ __global__ void __launch_bounds__(kNT) spec_draw_kernel(DrawArgs a) {
     __shared__ int s_lastpos;
     __shared__ bool s_use_p;
     __shared__ uint32_t s_cstar;
-    __shared__ FF s_before, s_target;
+    __shared__ FF s_before, s_target, s_sbefore;
+    __shared__ float s_stripe[kWarps][kDrawPer / 4];
+    __shared__ int s_istar;
 
     const uint32_t chunks = a.chunks;
     const uint32_t s = blockIdx.x / chunks;
@@ -492,10 +496,11 @@ __global__ void __launch_bounds__(kNT) spec_draw_kernel(DrawArgs a) {
     if (!s_last) return;
     __threadfence();  // order this thread's reads after the arrivals it saw
 
-    // last block: warp 0 walks the chunk sums 32 at a time in chunk order
+    // Last block. Warp 0 walks the chunk sums in chunk order, 32 at a time
+    // (fixed-order scans: the result does not depend on timing).
     const DrawPart* parts = a.parts + static_cast<size_t>(s) * a.cmax;
     if (warp == 0) {
-        FF R{0.0f, 0.0f}, P{0.0f, 0.0f};
+        FF R{0.0f, 0.0f}, P{0.0f, 0.0f}, r0{0.0f, 0.0f}, p0{0.0f, 0.0f};
         for (uint32_t c0 = 0; c0 < chunks; c0 += 32) {
             const uint32_t ci = c0 + lane;
             FF r{0.0f, 0.0f}, p{0.0f, 0.0f};
@@ -503,6 +508,7 @@ __global__ void __launch_bounds__(kNT) spec_draw_kernel(DrawArgs a) {
                 r = FF{ld_gpu_f32(&parts[ci].r.hi), ld_gpu_f32(&parts[ci].r.lo)};
                 p = FF{ld_gpu_f32(&parts[ci].p.hi), ld_gpu_f32(&parts[ci].p.lo)};
             }
+            if (c0 == 0) { r0 = r; p0 = p; }  // the first group is walked from registers
             R = ff_add(R, ff_warp_sum(r));
             P = ff_add(P, ff_warp_sum(p));
         }
@@ -512,10 +518,13 @@ __global__ void __launch_bounds__(kNT) spec_draw_kernel(DrawArgs a) {
         FF before{0.0f, 0.0f}, acc{0.0f, 0.0f}, before_last{0.0f, 0.0f};
         for (uint32_t c0 = 0; c0 < chunks && cstar == chunks; c0 += 32) {
             const uint32_t ci = c0 + lane;
-            FF t{0.0f, 0.0f};
-            if (ci < chunks) {
-                const FF* src = use_p ? &parts[ci].p : &parts[ci].r;
-                t = FF{ld_gpu_f32(&src->hi), ld_gpu_f32(&src->lo)};
+            FF t = use_p ? p0 : r0;
+            if (c0 > 0) {
+                t = FF{0.0f, 0.0f};
+                if (ci < chunks) {
+                    const FF* src = use_p ? &parts[ci].p : &parts[ci].r;
+                    t = FF{ld_gpu_f32(&src->hi), ld_gpu_f32(&src->lo)};
+                }
             }
             const FF incl = ff_add(acc, ff_warp_scan(t));
             FF excl = ff_shfl_up(incl, 1);
@@ -543,69 +552,113 @@ __global__ void __launch_bounds__(kNT) spec_draw_kernel(DrawArgs a) {
             s_cstar = cstar;
             s_before = before;
             s_target = target;
-            s_cross = kNoIdx;
             s_lastpos = -1;
         }
     }
     __syncthreads();
+
+    // The hit chunk, read again (from L2) in the coalesced layout: stripe i
+    // holds ids [clo + 1024 i, clo + 1024 (i + 1)), thread t its quad at
+    // 4 t. Id order is stripe, then thread, then lane: find the stripe from
+    // the stripe totals, the thread by a block scan of that stripe's quad
+    // sums, and the id within the quad.
     const bool use_p = s_use_p;
     const uint32_t clo = s_cstar * a.chunk_elems;
     const uint32_t chi = min(V, clo + a.chunk_elems);
     const FF target = s_target;
-
-    // thread tid owns ids [e0, e0 + kDrawPer) of chunk cstar
-    const uint32_t e0 = clo + kDrawPer * static_cast<uint32_t>(tid);
-    float w[kDrawPer];
-    {
-        float4 xp[kQ], xq[kQ];
+    float4 xp[kQ], xq[kQ];
 #pragma unroll
-        for (int i = 0; i < kQ; ++i) {
-            xp[i] = ld_quad<kVec>(prow, e0 + 4u * i, chi, kNegInf);
-            xq[i] = residual ? ld_quad<kVec>(qrow, e0 + 4u * i, chi, kNegInf) : none;
-        }
-#pragma unroll
-        for (int i = 0; i < kQ; ++i) {
-            float pw[4], rw[4];
-            quad_weights(xp[i], xq[i], residual, ps.m, pinv, qs.m, qinv, c, pw, rw);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) w[4 * i + j] = use_p ? pw[j] : rw[j];
-        }
+    for (int i = 0; i < kQ; ++i) {
+        const uint32_t e = clo + 4u * (static_cast<uint32_t>(tid) + kNT * i);
+        xp[i] = ld_quad<kVec>(prow, e, chi, kNegInf);
+        xq[i] = residual ? ld_quad<kVec>(qrow, e, chi, kNegInf) : none;
     }
-    FF mine{0.0f, 0.0f};
+    float qsum[kQ];
     int lp = -1;  // this thread's last id with mass
 #pragma unroll
-    for (uint32_t j = 0; j < kDrawPer; ++j) {
-        mine = ff_add(mine, FF{w[j], 0.0f});
-        if (w[j] > 0.0f) lp = static_cast<int>(e0 + j);
-    }
-    // exclusive block scan of the thread sums, in thread (= id) order
-    const FF incl = ff_warp_scan(mine);
-    if (lane == 31) s_r[warp] = incl;
-    const int wlp = __reduce_max_sync(kFull, lp);
-    if (lane == 0 && wlp >= 0) atomicMax(&s_lastpos, wlp);
-    __syncthreads();
-    FF start = s_before;
-    for (int ww = 0; ww < warp; ++ww) start = ff_add(start, s_r[ww]);
-    FF excl = ff_shfl_up(incl, 1);
-    if (lane == 0) excl = FF{0.0f, 0.0f};
-    start = ff_add(start, excl);
-    const FF end = ff_add(start, mine);
-    // the first thread whose range ends past the target holds the draw
-    const uint32_t hit = __ballot_sync(kFull, mine.hi > 0.0f && ff_lt(target, end));
-    if (lane == 0 && hit) atomicMin(&s_cross, static_cast<uint32_t>(tid) + static_cast<uint32_t>(__ffs(hit) - 1));
-    __syncthreads();
-    if (static_cast<uint32_t>(tid) == s_cross) {
-        uint32_t pick = kNoIdx;
-        FF cdf = start;
+    for (int i = 0; i < kQ; ++i) {
+        float pw[4], rw[4];
+        quad_weights(xp[i], xq[i], residual, ps.m, pinv, qs.m, qinv, c, pw, rw);
+        const uint32_t e = clo + 4u * (static_cast<uint32_t>(tid) + kNT * i);
+        float w[4];
 #pragma unroll
-        for (uint32_t j = 0; j < kDrawPer; ++j) {  // unrolled: w stays in registers
-            cdf = ff_add(cdf, FF{w[j], 0.0f});
-            if (pick == kNoIdx && w[j] > 0.0f && ff_lt(target, cdf)) pick = e0 + j;
+        for (int j = 0; j < 4; ++j) {
+            w[j] = use_p ? pw[j] : rw[j];
+            if (w[j] > 0.0f) lp = static_cast<int>(e + j);
         }
-        if (pick == kNoIdx) pick = static_cast<uint32_t>(lp);  // rounding: its last id with mass
-        a.emitted[static_cast<size_t>(s) * (K + 1u) + d.jstar] = pick;
+        qsum[i] = (w[0] + w[1]) + (w[2] + w[3]);
     }
-    if (tid == 0 && s_cross == kNoIdx) {
+    {
+        const int wlp = __reduce_max_sync(kFull, lp);
+        if (lane == 0 && wlp >= 0) atomicMax(&s_lastpos, wlp);
+    }
+    // stripe totals: warp sums (fp32) combined across warps in float-float
+#pragma unroll
+    for (int i = 0; i < kQ; ++i) {
+        float v = qsum[i];
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(kFull, v, m);
+        if (lane == 0) s_stripe[warp][i] = v;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        FF t{0.0f, 0.0f};
+        if (lane < kQ)
+            for (int ww = 0; ww < kWarps; ++ww) t = ff_add(t, FF{s_stripe[ww][lane], 0.0f});
+        const FF incl = ff_add(s_before, ff_warp_scan(t));
+        FF excl = ff_shfl_up(incl, 1);
+        if (lane == 0) excl = s_before;
+        const uint32_t valid = (1u << kQ) - 1u;
+        const uint32_t pos = __ballot_sync(kFull, lane < kQ && t.hi > 0.0f) & valid;
+        const uint32_t hit = __ballot_sync(kFull, lane < kQ && t.hi > 0.0f && ff_lt(target, incl)) & valid;
+        // no crossing (rounding): the last stripe with mass
+        const int l = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+        if (lane == 0) {
+            s_istar = l;
+            s_cross = kNoIdx;
+        }
+        if (l >= 0) {
+            const FF b = ff_shfl(excl, l);
+            if (lane == 0) s_sbefore = b;
+        }
+    }
+    __syncthreads();
+    const int istar = s_istar;
+    if (istar >= 0) {
+        // block scan of stripe istar's quad sums in thread order
+        float mine = 0.0f;
+        float4 cp = xp[0], cq = xq[0];
+#pragma unroll
+        for (int i = 0; i < kQ; ++i)
+            if (i == istar) { mine = qsum[i]; cp = xp[i]; cq = xq[i]; }
+        const FF incl = ff_warp_scan(FF{mine, 0.0f});
+        if (lane == 31) s_r[warp] = incl;
+        __syncthreads();
+        FF start = s_sbefore;
+        for (int ww = 0; ww < warp; ++ww) start = ff_add(start, s_r[ww]);
+        FF excl = ff_shfl_up(incl, 1);
+        if (lane == 0) excl = FF{0.0f, 0.0f};
+        start = ff_add(start, excl);
+        const FF end = ff_add(start, FF{mine, 0.0f});
+        const uint32_t hit = __ballot_sync(kFull, mine > 0.0f && ff_lt(target, end));
+        if (lane == 0 && hit) atomicMin(&s_cross, static_cast<uint32_t>(tid) + static_cast<uint32_t>(__ffs(hit) - 1));
+        __syncthreads();
+        if (static_cast<uint32_t>(tid) == s_cross) {
+            float pw[4], rw[4];
+            quad_weights(cp, cq, residual, ps.m, pinv, qs.m, qinv, c, pw, rw);
+            const uint32_t e = clo + 4u * (static_cast<uint32_t>(tid) + kNT * istar);
+            uint32_t pick = kNoIdx, last = kNoIdx;
+            FF cdf = start;
+            for (int j = 0; j < 4; ++j) {
+                const float w = use_p ? pw[j] : rw[j];
+                cdf = ff_add(cdf, FF{w, 0.0f});
+                if (w > 0.0f) last = e + j;
+                if (pick == kNoIdx && w > 0.0f && ff_lt(target, cdf)) pick = e + j;
+            }
+            a.emitted[static_cast<size_t>(s) * (K + 1u) + d.jstar] = pick != kNoIdx ? pick : last;
+        }
+    }
+    if (tid == 0 && (istar < 0 || s_cross == kNoIdx)) {
         // no crossing found (rounding): the last id with mass in the chunk
         a.emitted[static_cast<size_t>(s) * (K + 1u) + d.jstar] =
             s_lastpos >= 0 ? static_cast<uint32_t>(s_lastpos) : clo;

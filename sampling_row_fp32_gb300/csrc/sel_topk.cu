@@ -283,9 +283,11 @@ __device__ void sample_epilogue(const TopkShared& s, uint32_t n, uint32_t row, b
     }
 }
 
-// Merge the sorted chunk lists of one row (L[c * k + j]) into s.sorted[0..k).
-// Block-collective.
-__device__ void merge_row_lists(TopkShared& s, const uint64_t* L, uint32_t chunks, uint32_t k, uint32_t* err) {
+// Merge the sorted lists of one row into s.sorted[0..k). `load(i)` returns
+// entry j of list c for i = c * k + j (0 = empty). Block-collective; `err`
+// receives kErrListOrder / kErrMergeShort.
+template <class Load>
+__device__ void merge_row_lists(TopkShared& s, Load&& load, uint32_t chunks, uint32_t k, uint32_t* err) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // bound: for m lists and r = ceil(k / m), the m-th largest of the lists'
     // r-th entries is reached by at least m * r >= k entries
@@ -295,13 +297,13 @@ __device__ void merge_row_lists(TopkShared& s, const uint64_t* L, uint32_t chunk
         const uint32_t r = (k + m - 1) / m;
         uint64_t v = 0;
         if (static_cast<uint32_t>(lane) < chunks)
-            v = ld_gpu_u64(L + static_cast<size_t>(lane) * k + (r - 1));
+            v = load(lane * k + (r - 1));
         v = warp_sort_desc(v);
         b = shfl64(v, static_cast<int>(m - 1));
     } else {
         // many lists: the largest k-th entry (one list alone reaches it k times)
         for (uint32_t c = lane; c < chunks; c += 32) {
-            const uint64_t v = ld_gpu_u64(L + static_cast<size_t>(c) * k + (k - 1));
+            const uint64_t v = load(c * k + (k - 1));
             b = v > b ? v : b;
         }
 #pragma unroll
@@ -322,9 +324,9 @@ __device__ void merge_row_lists(TopkShared& s, const uint64_t* L, uint32_t chunk
     uint32_t mine = 0;
     bool disorder = false;
     for (uint32_t i = tid; i < total_entries; i += kNT) {
-        const uint64_t v = ld_gpu_u64(L + i);
+        const uint64_t v = load(i);
         mine += (v != 0 && v >= tau_m) ? 1u : 0u;
-        if ((i % k) + 1 < k) disorder |= ld_gpu_u64(L + i + 1) > v;
+        if ((i % k) + 1 < k) disorder |= load(i + 1) > v;
     }
     if (__any_sync(kFull, disorder) && lane == 0) atomicOr(err, kErrListOrder);
     mine = __reduce_add_sync(kFull, mine);
@@ -334,7 +336,7 @@ __device__ void merge_row_lists(TopkShared& s, const uint64_t* L, uint32_t chunk
         for (uint32_t i0 = 0; i0 < total_entries; i0 += kNT) {
             const uint32_t i = i0 + tid;
             uint64_t v = 0;
-            if (i < total_entries) v = ld_gpu_u64(L + i);
+            if (i < total_entries) v = load(i);
             warp_append(s, v != 0 && v >= tau_m, v);
         }
         __syncthreads();
@@ -348,7 +350,7 @@ __device__ void merge_row_lists(TopkShared& s, const uint64_t* L, uint32_t chunk
             for (uint32_t j0 = 0; j0 < k; j0 += kNT) {
                 const uint32_t j = j0 + tid;
                 uint64_t v = 0;
-                if (j < k) v = ld_gpu_u64(L + static_cast<size_t>(c) * k + j);
+                if (j < k) v = load(c * k + j);
                 warp_append(s, v != 0 && v >= floor_c, v);
             }
             __syncthreads();
@@ -394,7 +396,8 @@ __device__ void finish_row(TopkShared& s, const TopkArgs& a, uint32_t row) {
     for (uint32_t c = lane; c < count; c += 32)
         nf |= ld_gpu_u32(a.chunk_flags + static_cast<size_t>(row) * a.stride + c);
     nf = __reduce_or_sync(kFull, nf);
-    merge_row_lists(s, a.lists + static_cast<size_t>(row) * a.stride * k, count, k, a.err);
+    const uint64_t* L = a.lists + static_cast<size_t>(row) * a.stride * k;
+    merge_row_lists(s, [&](uint32_t i) { return ld_gpu_u64(L + i); }, count, k, a.err);
     write_row<kSample>(s, a, row, k, nf != 0);
     if (threadIdx.x == 0) atomicAdd(a.err + 1, 1u);  // rows finished (self-check)
     __syncthreads();
@@ -633,4 +636,112 @@ extern "C" sel_status sel_sample(const float* d_logits, uint32_t rows, uint32_t 
         return SEL_EINVAL;
     SampleArgs sa{d_uniforms, d_out_probs, T, p->top_p, p->min_p, p->order};
     return launch_topk<true>(d_logits, rows, V, k, nullptr, d_out_ids, d_ws, ws_bytes, sa, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Vocabulary shards: merge per-shard top-k lists into the row's top k (and
+// optionally run the sampling candidate stage on the merged list).
+// ---------------------------------------------------------------------------
+
+namespace sel {
+namespace {
+
+struct ShardArgs {
+    const float* vals;    // [rows][G][k], each shard's list sorted like sel_topk's
+    const uint32_t* ids;  // [rows][G][k], shard-local ids
+    uint32_t G;
+    uint32_t off[SEL_MAX_SHARDS + 1];  // shard g covers global ids [off[g], off[g+1])
+};
+
+// One block per row. Entry j of shard g becomes the candidate (key(value),
+// off[g] + id), so the merged order is (value desc, global id asc), the order
+// sel_topk gives the unsharded row. A shard whose row failed (nonfinite
+// logits: id 0xFFFFFFFF) or a malformed list (id outside the shard, a
+// nonfinite value, an unsorted list) makes the row fail closed.
+template <bool kSample>
+__global__ void __launch_bounds__(kNT) merge_shards_kernel(ShardArgs sh, TopkArgs a) {
+    __shared__ TopkShared s;
+    __shared__ uint32_t s_bad;
+    const uint32_t row = blockIdx.x;
+    const uint32_t k = a.k;
+    const size_t base = static_cast<size_t>(row) * sh.G * k;
+    if (threadIdx.x == 0) s_bad = 0u;
+    __syncthreads();
+    auto load = [&](uint32_t i) -> uint64_t {
+        const uint32_t g = i / k;
+        const uint32_t id = sh.ids[base + i];
+        const float x = sh.vals[base + i];
+        if (id >= sh.off[g + 1] - sh.off[g] || !(fabsf(x) <= FLT_MAX)) {
+            atomicOr(&s_bad, 1u);
+            return 0ull;
+        }
+        return make_cand(f2key(x), sh.off[g] + id);
+    };
+    merge_row_lists(s, load, sh.G, k, &s_bad);
+    __syncthreads();
+    write_row<kSample>(s, a, row, k, s_bad != 0u);
+}
+
+sel_status check_shards(const float* d_vals, const uint32_t* d_ids, uint32_t rows, uint32_t G, uint32_t k,
+                        const uint32_t* h_offsets, ShardArgs& sh) {
+    if (G == 0 || G > SEL_MAX_SHARDS || k == 0 || k > SEL_MAX_K || !h_offsets) return SEL_EINVAL;
+    for (uint32_t g = 0; g < G; ++g) {
+        if (h_offsets[g + 1] <= h_offsets[g] || h_offsets[g + 1] - h_offsets[g] < k) return SEL_EINVAL;
+    }
+    if (h_offsets[G] > SEL_MAX_V) return SEL_EINVAL;
+    if (rows > 0x7fffffffu) return SEL_EUNSUPPORTED;
+    if (rows > 0 && (!d_vals || !d_ids)) return SEL_EINVAL;
+    if (reinterpret_cast<uintptr_t>(d_vals) % 4 || reinterpret_cast<uintptr_t>(d_ids) % 4) return SEL_EINVAL;
+    sh.vals = d_vals;
+    sh.ids = d_ids;
+    sh.G = G;
+    for (uint32_t g = 0; g <= G; ++g) sh.off[g] = h_offsets[g];
+    return SEL_OK;
+}
+
+}  // namespace
+}  // namespace sel
+
+extern "C" sel_status sel_merge_shards(const float* d_vals, const uint32_t* d_ids, uint32_t rows, uint32_t G,
+                                       uint32_t k, const uint32_t* h_offsets, float* d_out_vals,
+                                       uint32_t* d_out_ids, cudaStream_t stream) {
+    ShardArgs sh{};
+    const sel_status st = check_shards(d_vals, d_ids, rows, G, k, h_offsets, sh);
+    if (st != SEL_OK) return st;
+    if (rows == 0) return SEL_OK;
+    if (!d_out_vals || !d_out_ids) return SEL_EINVAL;
+    if (reinterpret_cast<uintptr_t>(d_out_vals) % 4 || reinterpret_cast<uintptr_t>(d_out_ids) % 4) return SEL_EINVAL;
+    TopkArgs a{};
+    a.k = k;
+    a.out_vals = d_out_vals;
+    a.out_ids = d_out_ids;
+    merge_shards_kernel<false><<<rows, kNT, 0, stream>>>(sh, a);
+    return cudaGetLastError() == cudaSuccess ? SEL_OK : SEL_ECUDA;
+}
+
+extern "C" sel_status sel_sample_shards(const float* d_vals, const uint32_t* d_ids, uint32_t rows, uint32_t G,
+                                        uint32_t k, const uint32_t* h_offsets, const sel_sample_params* p,
+                                        const float* d_uniforms, uint32_t* d_out_ids, float* d_out_probs,
+                                        cudaStream_t stream) {
+    if (!p) return SEL_EINVAL;
+    const float T = p->temperature;
+    if (!(T >= 0.0f) || !(T < INFINITY)) return SEL_EINVAL;
+    if (!(p->top_p > 0.0f && p->top_p <= 1.0f)) return SEL_EINVAL;
+    if (!(p->min_p >= 0.0f && p->min_p < 1.0f)) return SEL_EINVAL;
+    if (p->order != SEL_ORDER_TEMP_FIRST && p->order != SEL_ORDER_TEMP_LAST) return SEL_EINVAL;
+    if (T > 0.0f && p->top_k != k) return SEL_EINVAL;  // the lists are the policy's top_k candidates
+    ShardArgs sh{};
+    const sel_status st = check_shards(d_vals, d_ids, rows, G, k, h_offsets, sh);
+    if (st != SEL_OK) return st;
+    if (rows == 0) return SEL_OK;
+    if (!d_uniforms || !d_out_ids || !d_out_probs) return SEL_EINVAL;
+    if (reinterpret_cast<uintptr_t>(d_uniforms) % 4 || reinterpret_cast<uintptr_t>(d_out_ids) % 4 ||
+        reinterpret_cast<uintptr_t>(d_out_probs) % 4)
+        return SEL_EINVAL;
+    TopkArgs a{};
+    a.k = k;
+    a.out_ids = d_out_ids;
+    a.sa = SampleArgs{d_uniforms, d_out_probs, T, p->top_p, p->min_p, p->order};
+    merge_shards_kernel<true><<<rows, kNT, 0, stream>>>(sh, a);
+    return cudaGetLastError() == cudaSuccess ? SEL_OK : SEL_ECUDA;
 }

@@ -97,3 +97,39 @@ def test_host_validation_needs_no_gpu(lib):
     prm = B.SampleParams(1.0, 5, 1.0, 0.0, 0)
     assert lib.sel_sample(fake, 1, 10, None, fake, fake, fake, None, 0, None) == B.SEL_EINVAL
     assert lib.sel_sample(fake, 0, 10, ctypes.byref(prm), None, None, None, None, 0, None) == B.SEL_OK
+
+
+def test_shard_merge_validation_needs_no_gpu(lib):
+    from sampling_row_fp32_gb300 import binding as B
+    vp = ctypes.c_void_p
+    fake = vp(0x10000)
+    U = ctypes.c_uint32
+
+    def offs(*o):
+        return ctypes.cast((U * len(o))(*o), vp)
+
+    good = offs(0, 100, 200)
+    m = lib.sel_merge_shards
+    assert m(fake, fake, 0, 2, 5, good, fake, fake, None) == B.SEL_OK                # rows = 0
+    assert m(fake, fake, 1, 0, 5, good, fake, fake, None) == B.SEL_EINVAL            # G = 0
+    assert m(fake, fake, 1, 65, 5, offs(*range(0, 66 * 10, 10)), fake, fake, None) == B.SEL_EINVAL
+    assert m(fake, fake, 1, 2, 0, good, fake, fake, None) == B.SEL_EINVAL            # k = 0
+    assert m(fake, fake, 1, 2, 1025, offs(0, 2000, 4000), fake, fake, None) == B.SEL_EINVAL
+    assert m(fake, fake, 1, 2, 5, offs(0, 3, 200), fake, fake, None) == B.SEL_EINVAL  # shard < k
+    assert m(fake, fake, 1, 2, 5, offs(0, 100, 90), fake, fake, None) == B.SEL_EINVAL  # not increasing
+    assert m(fake, fake, 1, 2, 5, offs(0, 100, 0x80000000), fake, fake, None) == B.SEL_EINVAL
+    assert m(fake, fake, 1, 2, 5, None, fake, fake, None) == B.SEL_EINVAL             # no offsets
+    assert m(None, fake, 1, 2, 5, good, fake, fake, None) == B.SEL_EINVAL
+    assert m(fake, fake, 1, 2, 5, good, None, fake, None) == B.SEL_EINVAL
+    assert m(vp(0x10002), fake, 1, 2, 5, good, fake, fake, None) == B.SEL_EINVAL      # misaligned
+    s = lib.sel_sample_shards
+    p = B.SampleParams(0.7, 5, 0.9, 0.05, 0)
+    assert s(fake, fake, 1, 2, 5, good, None, fake, fake, fake, None) == B.SEL_EINVAL
+    assert s(fake, fake, 1, 2, 5, good, ctypes.byref(B.SampleParams(0.7, 6, 0.9, 0.05, 0)),
+             fake, fake, fake, None) == B.SEL_EINVAL                                   # top_k != k
+    assert s(fake, fake, 1, 2, 5, good, ctypes.byref(B.SampleParams(float("nan"), 5, 0.9, 0.05, 0)),
+             fake, fake, fake, None) == B.SEL_EINVAL
+    assert s(fake, fake, 1, 2, 5, good, ctypes.byref(B.SampleParams(0.7, 5, 1.5, 0.05, 0)),
+             fake, fake, fake, None) == B.SEL_EINVAL
+    assert s(fake, fake, 1, 2, 5, good, ctypes.byref(p), None, fake, fake, None) == B.SEL_EINVAL
+    assert s(fake, fake, 0, 2, 5, good, ctypes.byref(p), None, None, None, None) == B.SEL_OK
