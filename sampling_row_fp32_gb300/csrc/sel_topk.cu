@@ -56,8 +56,8 @@ constexpr uint32_t kReduceSlack = 32;        // select the buffer down to k abov
 
 static_assert(kCap >= SEL_MAX_K + 4 * kNT, "a slot of 1,024 must fit after a selection");
 
-struct TopkShared {
-    uint64_t buf[kCap];          // candidate buffer
+struct alignas(16) TopkShared {
+    uint64_t buf[kCap];          // candidate buffer (16-byte aligned: read as pairs)
     uint64_t sorted[SEL_MAX_K];  // selection output, descending
     uint64_t warp_cand[kWarps];
     uint32_t warp_val[kWarps];
@@ -112,11 +112,24 @@ __device__ __forceinline__ void warp_append(TopkShared& s, bool p, uint64_t cand
 __device__ void block_select_sorted(uint64_t* buf, uint32_t n, uint32_t k, uint64_t* out) {
     const uint32_t tid = threadIdx.x;
     if (n <= kRankMax) {
-        // rank = number of larger candidates; candidates are distinct
+        // rank = number of larger candidates; candidates are distinct. The
+        // scan reads 8 candidates per step with 128-bit loads into four
+        // independent counters, so it is not one load latency per compare.
+        const ulonglong2* b2 = reinterpret_cast<const ulonglong2*>(buf);
         for (uint32_t i = tid; i < n; i += kNT) {
             const uint64_t c = buf[i];
-            uint32_t rank = 0;
-            for (uint32_t j = 0; j < n; ++j) rank += buf[j] > c ? 1u : 0u;
+            uint32_t r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+            uint32_t j = 0;
+#pragma unroll 2
+            for (; j + 8 <= n; j += 8) {
+                const ulonglong2 p0 = b2[j / 2], p1 = b2[j / 2 + 1], p2 = b2[j / 2 + 2], p3 = b2[j / 2 + 3];
+                r0 += (p0.x > c ? 1u : 0u) + (p0.y > c ? 1u : 0u);
+                r1 += (p1.x > c ? 1u : 0u) + (p1.y > c ? 1u : 0u);
+                r2 += (p2.x > c ? 1u : 0u) + (p2.y > c ? 1u : 0u);
+                r3 += (p3.x > c ? 1u : 0u) + (p3.y > c ? 1u : 0u);
+            }
+            for (; j < n; ++j) r0 += buf[j] > c ? 1u : 0u;
+            const uint32_t rank = (r0 + r1) + (r2 + r3);
             if (rank < k) out[rank] = c;
         }
     } else {
@@ -181,7 +194,10 @@ __device__ __noinline__ void overflow_chunk(TopkShared& s, const float* x, uint3
 }
 
 // Sampling epilogue on the sorted candidates s.sorted[0..n): one warp.
-__device__ void sample_epilogue(const TopkShared& s, uint32_t n, uint32_t row, bool nonfinite,
+// The filter weights wf (T = 1 when temperature comes last) and draw weights
+// wd, relative to the largest candidate (weight exactly 1), are computed once
+// per candidate into the (now free) candidate buffer; the scans read them.
+__device__ void sample_epilogue(TopkShared& s, uint32_t n, uint32_t row, bool nonfinite,
                                 const SampleArgs& sa, uint32_t* out_ids) {
     const int lane = threadIdx.x & 31;
     const float u = sa.uniforms[row];
@@ -197,22 +213,24 @@ __device__ void sample_epilogue(const TopkShared& s, uint32_t n, uint32_t row, b
     const float x0 = key2f(cand_key(s.sorted[0]));
     const float T = sa.temperature;
     const bool temp_last = sa.order == SEL_ORDER_TEMP_LAST;
-    // filter weights wf (T = 1 when temperature comes last) and draw weights
-    // wd, relative to the largest candidate (weight exactly 1)
-    auto wfilter = [&](uint32_t j) {
-        const float d = key2f(cand_key(s.sorted[j])) - x0;
-        return temp_last ? expf(d) : expf(d / T);
-    };
-    auto wdraw = [&](uint32_t j) { return expf((key2f(cand_key(s.sorted[j])) - x0) / T); };
-
+    float* wf = reinterpret_cast<float*>(s.buf);  // [SEL_MAX_K]
+    float* wd = wf + SEL_MAX_K;                   // [SEL_MAX_K]
     float sum_f = 0.0f;
     for (uint32_t b = 0; b < n; b += 32) {
         const uint32_t j = b + lane;
-        float t = j < n ? wfilter(j) : 0.0f;
+        float f = 0.0f;
+        if (j < n) {
+            const float d = key2f(cand_key(s.sorted[j])) - x0;
+            const float w_d = expf(d / T);
+            f = temp_last ? expf(d) : w_d;
+            wf[j] = f;
+            wd[j] = w_d;
+        }
 #pragma unroll
-        for (int m = 16; m > 0; m >>= 1) t += __shfl_xor_sync(kFull, t, m);
-        sum_f += t;
+        for (int m = 16; m > 0; m >>= 1) f += __shfl_xor_sync(kFull, f, m);
+        sum_f += f;
     }
+    __syncwarp();
     // top-p: the shortest prefix whose cumulative P reaches top_p
     uint32_t ns = n;
     if (sa.top_p < 1.0f) {
@@ -220,7 +238,7 @@ __device__ void sample_epilogue(const TopkShared& s, uint32_t n, uint32_t row, b
         ns = 0;
         for (uint32_t b = 0; b < n && ns == 0; b += 32) {
             const uint32_t j = b + lane;
-            float incl = j < n ? wfilter(j) / sum_f : 0.0f;
+            float incl = j < n ? wf[j] / sum_f : 0.0f;
 #pragma unroll
             for (int m = 1; m < 32; m <<= 1) {
                 const float o = __shfl_up_sync(kFull, incl, m);
@@ -238,7 +256,7 @@ __device__ void sample_epilogue(const TopkShared& s, uint32_t n, uint32_t row, b
         uint32_t keep = 1;
         for (uint32_t b = 0; b < ns; b += 32) {
             const uint32_t j = b + lane;
-            const bool ok = j < ns && j > 0 && wfilter(j) >= sa.min_p;
+            const bool ok = j < ns && j > 0 && wf[j] >= sa.min_p;
             const uint32_t m = __ballot_sync(kFull, ok);
             if (m) keep = b + 32 - __clz(m);  // survivors form a prefix
         }
@@ -248,7 +266,7 @@ __device__ void sample_epilogue(const TopkShared& s, uint32_t n, uint32_t row, b
     float sum_d = 0.0f;
     for (uint32_t b = 0; b < ns; b += 32) {
         const uint32_t j = b + lane;
-        float t = j < ns ? wdraw(j) : 0.0f;
+        float t = j < ns ? wd[j] : 0.0f;
 #pragma unroll
         for (int m = 16; m > 0; m >>= 1) t += __shfl_xor_sync(kFull, t, m);
         sum_d += t;
@@ -259,8 +277,8 @@ __device__ void sample_epilogue(const TopkShared& s, uint32_t n, uint32_t row, b
     float cum = 0.0f;
     for (uint32_t b = 0; b < ns && !found; b += 32) {
         const uint32_t j = b + lane;
-        const float wd = j < ns ? wdraw(j) : 0.0f;
-        float incl = wd;
+        const float w = j < ns ? wd[j] : 0.0f;
+        float incl = w;
 #pragma unroll
         for (int m = 1; m < 32; m <<= 1) {
             const float o = __shfl_up_sync(kFull, incl, m);
@@ -271,12 +289,12 @@ __device__ void sample_epilogue(const TopkShared& s, uint32_t n, uint32_t row, b
         if (hit) {
             const int l = __ffs(hit) - 1;
             pick = b + l;
-            pick_w = __shfl_sync(kFull, wd, l);
+            pick_w = __shfl_sync(kFull, w, l);
             found = true;
         }
         cum = __shfl_sync(kFull, incl, 31);
     }
-    if (!found) pick_w = wdraw(pick);
+    if (!found) pick_w = wd[pick];
     if (lane == 0) {
         out_ids[row] = cand_id(s.sorted[pick]);
         sa.out_probs[row] = pick_w / sum_d;
@@ -289,6 +307,94 @@ __device__ void sample_epilogue(const TopkShared& s, uint32_t n, uint32_t row, b
 template <class Load>
 __device__ void merge_row_lists(TopkShared& s, Load&& load, uint32_t chunks, uint32_t k, uint32_t* err) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t total = chunks * k;
+    if (total <= kCap) {
+        // Fast path: one coalesced round brings every entry into the buffer;
+        // bound, order check and selection then run in shared memory.
+        constexpr int kPer = static_cast<int>(kCap / kNT);
+        uint64_t v[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const uint32_t e = static_cast<uint32_t>(tid) + kNT * i;
+            v[i] = e < total ? load(e) : 0ull;
+        }
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const uint32_t e = static_cast<uint32_t>(tid) + kNT * i;
+            if (e < total) s.buf[e] = v[i];
+        }
+        if (tid == 0) { s.count = 0; s.tau_key = 0; s.total = 0; }
+        __syncthreads();
+        bool disorder = false;
+        uint32_t nz = 0;
+        for (uint32_t e = tid; e < total; e += kNT) {
+            const uint64_t x = s.buf[e];
+            nz += x != 0 ? 1u : 0u;
+            if ((e % k) + 1 < k) disorder |= s.buf[e + 1] > x;
+        }
+        if (__any_sync(kFull, disorder) && lane == 0) atomicOr(err, kErrListOrder);
+        nz = __reduce_add_sync(kFull, nz);
+        if (lane == 0) atomicAdd(&s.total, nz);
+        __syncthreads();
+        if (tid == 0 && s.total < k) atomicOr(err, kErrMergeShort);
+        if (total <= 64u) {
+            block_select_sorted(s.buf, total, k, s.sorted);  // zeros rank below every entry
+            return;
+        }
+        // bound (as below, from shared memory), survivors into s.sorted,
+        // selection back into the buffer, then copied to s.sorted
+        uint64_t b = 0;
+        if (chunks <= kFastMergeLists) {
+            const uint32_t m = max(1u, chunks >> warp);
+            const uint32_t r = (k + m - 1) / m;
+            uint64_t x = static_cast<uint32_t>(lane) < chunks ? s.buf[lane * k + (r - 1)] : 0ull;
+            x = warp_sort_desc(x);
+            b = shfl64(x, static_cast<int>(m - 1));
+        } else {
+            for (uint32_t c = lane; c < chunks; c += 32) {
+                const uint64_t x = s.buf[c * k + (k - 1)];
+                b = x > b ? x : b;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const uint64_t w = shfl_xor64(b, o);
+                b = w > b ? w : b;
+            }
+        }
+        if (lane == 0) s.warp_cand[warp] = b;
+        __syncthreads();
+        uint64_t tau_m = s.warp_cand[0];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) tau_m = s.warp_cand[w] > tau_m ? s.warp_cand[w] : tau_m;
+        uint32_t surv = 0;
+        for (uint32_t e = tid; e < total; e += kNT) surv += (s.buf[e] != 0 && s.buf[e] >= tau_m) ? 1u : 0u;
+        surv = __reduce_add_sync(kFull, surv);
+        if (lane == 0) s.warp_val[warp] = surv;
+        __syncthreads();
+        uint32_t n_surv = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) n_surv += s.warp_val[w];
+        if (n_surv <= SEL_MAX_K) {
+            for (uint32_t e0 = 0; e0 < total; e0 += kNT) {
+                const uint32_t e = e0 + tid;
+                const uint64_t x = e < total ? s.buf[e] : 0ull;
+                const bool keep = x != 0 && x >= tau_m;
+                const uint32_t m = __ballot_sync(kFull, keep);
+                if (m) {
+                    uint32_t base = 0;
+                    if (lane == __ffs(m) - 1) base = atomicAdd(&s.count, static_cast<uint32_t>(__popc(m)));
+                    base = __shfl_sync(kFull, base, __ffs(m) - 1);
+                    if (keep) s.sorted[base + __popc(m & lanemask_lt())] = x;
+                }
+            }
+            __syncthreads();
+            block_select_sorted(s.sorted, n_surv, k, s.buf);
+            for (uint32_t i = tid; i < k; i += kNT) s.sorted[i] = s.buf[i];
+            __syncthreads();
+            return;
+        }
+        __syncthreads();  // more survivors than fit: the general path below
+    }
     // bound: for m lists and r = ceil(k / m), the m-th largest of the lists'
     // r-th entries is reached by at least m * r >= k entries
     uint64_t b = 0;
@@ -368,7 +474,7 @@ __device__ void merge_row_lists(TopkShared& s, Load&& load, uint32_t chunks, uin
 }
 
 template <bool kSample>
-__device__ __forceinline__ void write_row(const TopkShared& s, const TopkArgs& a, uint32_t row, uint32_t have,
+__device__ __forceinline__ void write_row(TopkShared& s, const TopkArgs& a, uint32_t row, uint32_t have,
                                           bool nonfinite) {
     const int tid = threadIdx.x;
     if constexpr (kSample) {
@@ -393,11 +499,12 @@ __device__ void finish_row(TopkShared& s, const TopkArgs& a, uint32_t row) {
     const uint32_t count = segment_of(a.cfg, row).count;
     uint32_t nf = 0;
     const int lane = threadIdx.x & 31;
+    // the flags' loads are issued before the lists' and consumed after them
     for (uint32_t c = lane; c < count; c += 32)
         nf |= ld_gpu_u32(a.chunk_flags + static_cast<size_t>(row) * a.stride + c);
-    nf = __reduce_or_sync(kFull, nf);
     const uint64_t* L = a.lists + static_cast<size_t>(row) * a.stride * k;
     merge_row_lists(s, [&](uint32_t i) { return ld_gpu_u64(L + i); }, count, k, a.err);
+    nf = __reduce_or_sync(kFull, nf);
     write_row<kSample>(s, a, row, k, nf != 0);
     if (threadIdx.x == 0) atomicAdd(a.err + 1, 1u);  // rows finished (self-check)
     __syncthreads();
