@@ -65,6 +65,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.orc_argmax_row.restype = _u32
     lib.orc_argmax.argtypes = [_f32p, _u32, _u32, _u32p]
     lib.orc_argmax.restype = None
+    lib.orc_argmax_excluding.argtypes = [_f32p, _u32, _u32, _u32p, _u32, _u32p]
+    lib.orc_argmax_excluding.restype = None
     lib.orc_topk.argtypes = [_f32p, _u32, _u32, _u32, _f32p, _u32p]
     lib.orc_topk.restype = None
     lib.orc_sample.argtypes = [_f32p, _u32, _u32, ctypes.c_double, _u32,
@@ -120,6 +122,17 @@ class Oracle:
         rows, V = x.shape
         out = np.empty(rows, dtype=np.uint32)
         self.lib.orc_argmax(_ptr(x, _f32p), rows, V, _ptr(out, _u32p))
+        return out
+
+    def argmax_excluding(self, logits, excluded) -> np.ndarray:
+        """Greedy serving variant: first maximum over the ids not in
+        `excluded` (one set for every row)."""
+        x = _f32(logits)
+        rows, V = x.shape
+        ex = np.ascontiguousarray(np.asarray(excluded, dtype=np.uint32).reshape(-1))
+        out = np.empty(rows, dtype=np.uint32)
+        self.lib.orc_argmax_excluding(_ptr(x, _f32p), rows, V, _ptr(ex, _u32p), ex.size,
+                                      _ptr(out, _u32p))
         return out
 
     def topk(self, logits, k: int) -> tuple[np.ndarray, np.ndarray]:

@@ -212,6 +212,43 @@ void orc_argmax(const float *logits, uint32_t rows, uint32_t V,
         out_ids[r] = orc_argmax_row(logits + (size_t)r * V, V);
 }
 
+/*
+ * [Ch21] 21.4, the greedy serving variant: a request's end-of-generation ids
+ * are masked out inside the reduction only (the logits themselves stay
+ * untouched), and the NaN/Inf latch still covers every logit of the row.
+ * Definition used: the first maximum (strict '>') over the ids that are not
+ * in `excluded`; ids >= V in the set are ignored; duplicates do not matter.
+ * A nonfinite logit anywhere in the row (excluded or not), or a row whose ids
+ * are all excluded, gives 0xFFFFFFFF.
+ */
+uint32_t orc_argmax_excluding_row(const float *x, uint32_t V,
+                                  const uint32_t *excluded, uint32_t n_excluded)
+{
+    if (V == 0 || !row_is_finite(x, V))
+        return ORC_INVALID;
+    uint32_t best = ORC_INVALID;
+    for (uint32_t i = 0; i < V; ++i) {
+        int is_excluded = 0;
+        for (uint32_t e = 0; e < n_excluded; ++e)
+            if (excluded[e] == i)
+                is_excluded = 1;
+        if (is_excluded)
+            continue;
+        if (best == ORC_INVALID || (double)x[i] > (double)x[best])
+            best = i;
+    }
+    return best;
+}
+
+void orc_argmax_excluding(const float *logits, uint32_t rows, uint32_t V,
+                          const uint32_t *excluded, uint32_t n_excluded,
+                          uint32_t *out_ids)
+{
+    for (uint32_t r = 0; r < rows; ++r)
+        out_ids[r] = orc_argmax_excluding_row(logits + (size_t)r * V, V,
+                                              excluded, n_excluded);
+}
+
 /* ----------------------------------------------------------------------- */
 /* top-k                                                                   */
 /* ----------------------------------------------------------------------- */

@@ -122,6 +122,56 @@ def pin_argmax_nonfinite(orc):
             assert int(orc.argmax(x)[0]) == INVALID, (bad, pos)
 
 
+def pin_eog_bruteforce(orc):
+    """Ch 21, 21.4 (greedy serving variant, EOG exclusion): every row over
+    {0, 1, 2} up to length 5 with every excluded subset. The answer is a
+    non-excluded id holding the largest non-excluded value, the lowest such
+    id; with every id excluded there is none (0xFFFFFFFF)."""
+    for V in range(1, 6):
+        rows = np.array(list(itertools.product((0.0, 1.0, 2.0), repeat=V)), dtype=np.float32)
+        for mask in range(1 << V):
+            ex = [i for i in range(V) if mask >> i & 1]
+            got = orc.argmax_excluding(rows, ex)
+            keep = [i for i in range(V) if i not in ex]
+            for r in range(rows.shape[0]):
+                g = int(got[r])
+                if not keep:
+                    assert g == INVALID, (rows[r], ex, g)
+                    continue
+                assert g in keep, (rows[r], ex, g)
+                kv = rows[r][keep]
+                assert rows[r][g] == kv.max(), (rows[r], ex, g)
+                assert all(rows[r][i] < rows[r][g] for i in keep if i < g), (rows[r], ex, g)
+
+
+def pin_eog_reduces_to_argmax(orc):
+    """An empty set, or ids past the row, changes nothing; excluding the
+    argmax gives numpy's first maximum of the row with that id masked (an
+    independent library route); duplicates in the set do not matter."""
+    rng = np.random.default_rng(17)
+    x = rng.integers(0, 6, size=(32, 500)).astype(np.float32)
+    assert np.array_equal(orc.argmax_excluding(x, []), orc.argmax(x))
+    assert np.array_equal(orc.argmax_excluding(x, [500, 777, 0xFFFFFFF0]), orc.argmax(x))
+    for r in range(8):
+        a = int(np.argmax(x[r]))
+        ex = [a, a, 3, 499]
+        masked = x[r].astype(np.float64).copy()
+        masked[[a, 3, 499]] = -np.inf
+        assert int(orc.argmax_excluding(x[r:r + 1], ex)[0]) == int(np.argmax(masked))
+
+
+def pin_eog_nonfinite(orc):
+    """The latch covers excluded ids too: a NaN or Inf anywhere fails the
+    row, and masking never turns a finite row invalid."""
+    x = np.zeros((1, 50), dtype=np.float32)
+    x[0, 7] = 1.0
+    for bad in (np.nan, np.inf, -np.inf):
+        y = x.copy()
+        y[0, 20] = bad
+        assert int(orc.argmax_excluding(y, [20])[0]) == INVALID
+    assert int(orc.argmax_excluding(x, [7])[0]) == 0
+
+
 # ---------------------------------------------------------------------------
 # top-k
 # ---------------------------------------------------------------------------
@@ -397,6 +447,7 @@ def pin_spec_invalid(orc):
 ALL_PINS = [
     pin_argmax_ties, pin_argmax_bruteforce, pin_argmax_numpy,
     pin_argmax_partition, pin_argmax_nonfinite,
+    pin_eog_bruteforce, pin_eog_reduces_to_argmax, pin_eog_nonfinite,
     pin_topk_bruteforce, pin_topk_lexsort, pin_topk_special,
     pin_sample_closed_forms, pin_sample_cdf_grid, pin_sample_support,
     pin_sample_invalid,

@@ -62,6 +62,17 @@ MUTANTS = [
      [("emitted[n] = a;", "emitted[n] = n < K ? tokens[n] : a;")]),
     ("argmax rule used for every temperature",
      [("if (T == 0.0)\n        mode = 1;", "mode = 1;")]),
+    ("EOG set shifted by one id",
+     [("if (excluded[e] == i)", "if (excluded[e] == i + 1)")]),
+    ("EOG ties keep the higher index",
+     [("if (best == ORC_INVALID || (double)x[i] > (double)x[best])",
+       "if (best == ORC_INVALID || (double)x[i] >= (double)x[best])")]),
+    ("EOG latch dropped",
+     [("!row_is_finite(x, V))\n        return ORC_INVALID;\n    uint32_t best = ORC_INVALID;",
+       "0)\n        return ORC_INVALID;\n    uint32_t best = ORC_INVALID;")]),
+    ("EOG all-excluded row answers id 0",
+     [("    return best;\n}\n\nvoid orc_argmax_excluding(",
+       "    return best == ORC_INVALID ? 0 : best;\n}\n\nvoid orc_argmax_excluding(")]),
 ]
 
 
