@@ -258,6 +258,26 @@ sel_status sel_argmax_noalloc(const float *d_logits, uint32_t rows, uint32_t V,
                               uint32_t *d_out_ids, cudaStream_t stream);
 
 /*
+ * sel_argmax_excluding -- Muser ch. 21, 21.4, the greedy serving variant: the
+ * request's end-of-generation ids are masked out inside the reduction only
+ * (the logits are left untouched, for log-probabilities and sessions), while
+ * the NaN/Inf latch still covers every logit. Per row: the lowest id of the
+ * maximum over the ids not in the set.
+ *
+ *   d_excluded  device array of n_excluded ids, one set for every row; ids
+ *               >= V are ignored, duplicates do not matter, any order
+ *   n_excluded  0 <= n_excluded <= SEL_MAX_EXCLUDED (0: plain sel_argmax)
+ *   the rest    as for sel_argmax (same workspace: SEL_OP_ARGMAX)
+ * A row with a nonfinite logit (excluded or not), or whose ids are all
+ * excluded, gets 0xFFFFFFFF.
+ */
+#define SEL_MAX_EXCLUDED 256u
+sel_status sel_argmax_excluding(const float *d_logits, uint32_t rows, uint32_t V,
+                                const uint32_t *d_excluded, uint32_t n_excluded,
+                                uint32_t *d_out_ids, void *d_ws, size_t ws_bytes,
+                                cudaStream_t stream);
+
+/*
  * Vocabulary shards -- llama.cpp PR 49, "Problem": under a tensor split each
  * GPU holds a share of the output head (about 155k and 93k of the 248k
  * columns there), so each computes the logits of one contiguous id range.

@@ -27,9 +27,10 @@ SPEC_MODE_REJECTION, SPEC_MODE_ARGMAX = 0, 1
 
 EXPORTED = ("sel_workspace_bytes", "sel_workspace_init", "sel_argmax", "sel_topk",
             "sel_sample", "spec_accept", "sel_status_string", "sel_argmax_noalloc",
-            "sel_merge_shards", "sel_sample_shards")
+            "sel_merge_shards", "sel_sample_shards", "sel_argmax_excluding")
 SEL_NOALLOC_SCRATCH_BYTES = 1 << 20
 SEL_MAX_SHARDS = 64
+SEL_MAX_EXCLUDED = 256
 
 
 class SelError(RuntimeError):
@@ -86,6 +87,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.spec_accept.restype = ctypes.c_int
     lib.sel_argmax_noalloc.argtypes = [_vp, _u32, _u32, _vp, _vp]
     lib.sel_argmax_noalloc.restype = ctypes.c_int
+    lib.sel_argmax_excluding.argtypes = [_vp, _u32, _u32, _vp, _u32, _vp, _vp, _sz, _vp]
+    lib.sel_argmax_excluding.restype = ctypes.c_int
     lib.sel_merge_shards.argtypes = [_vp, _vp, _u32, _u32, _u32, _vp, _vp, _vp, _vp]
     lib.sel_merge_shards.restype = ctypes.c_int
     lib.sel_sample_shards.argtypes = [_vp, _vp, _u32, _u32, _u32, _vp, ctypes.POINTER(SampleParams),
@@ -159,6 +162,20 @@ def sel_argmax(logits, out_ids, ws=None, stream=None) -> None:
     rows, V = logits.shape
     _check(load().sel_argmax(_ptr(logits), rows, V, _ptr(out_ids), _ptr(ws), _nbytes(ws),
                              _stream(stream)), "sel_argmax")
+
+
+def sel_argmax_excluding(logits, excluded, out_ids, ws=None, stream=None) -> None:
+    """sel_argmax with the ids of `excluded` (a device id tensor, one set for
+    every row) masked out of the reduction."""
+    _check_f32(logits, "logits")
+    _check_ids(out_ids, "out_ids")
+    if excluded is not None and not isinstance(excluded, int):
+        _check_ids(excluded, "excluded")
+    rows, V = logits.shape
+    n = 0 if excluded is None else excluded.numel()
+    _check(load().sel_argmax_excluding(_ptr(logits), rows, V, _ptr(excluded) if n else None, n,
+                                       _ptr(out_ids), _ptr(ws), _nbytes(ws), _stream(stream)),
+           "sel_argmax_excluding")
 
 
 def sel_argmax_noalloc(logits, out_ids, stream=None) -> None:

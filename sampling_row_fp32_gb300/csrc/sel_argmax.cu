@@ -72,15 +72,21 @@ struct ArgmaxArgs {
     uint32_t stride;
     uint32_t* err;
     StreamCfg cfg;
+    const uint32_t* excluded;  // EOG ids masked out of every row (greedy serving variant)
+    uint32_t n_excluded;       // <= SEL_MAX_EXCLUDED
 };
 
-template <bool kTma>
+template <bool kTma, bool kExclude>
 __global__ void __launch_bounds__(kNT, SEL_ARGMAX_MINB) argmax_kernel(ArgmaxArgs a) {
     extern __shared__ float4 stages[];
     __shared__ uint64_t full[kStages];
     __shared__ float s_v[kNT / 32];
     __shared__ uint32_t s_i[kNT / 32];
     __shared__ uint32_t s_nf[kNT / 32];
+    // excluded offsets inside the current unit, in three buffers by unit
+    // number (see accum)
+    __shared__ uint32_t s_ex_count[3];
+    __shared__ uint32_t s_ex_off[kExclude ? 3 : 1][kExclude ? SEL_MAX_EXCLUDED : 1];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t V = a.cfg.V;
@@ -96,14 +102,64 @@ __global__ void __launch_bounds__(kNT, SEL_ARGMAX_MINB) argmax_kernel(ArgmaxArgs
     uint32_t bbase[4] = {kNoIdx, kNoIdx, kNoIdx, kNoIdx};
     float nfacc = 0.0f;
 
+    // EOG exclusion (greedy serving variant): each thread holds one excluded
+    // id (SEL_MAX_EXCLUDED == kNT). Per unit, the ids that fall inside it are
+    // posted as unit offsets; after one barrier every thread masks its own
+    // elements to -inf. The latch has already seen the raw values, so a
+    // nonfinite excluded logit still fails the row. Unit u posts into buffer
+    // u % 3 and thread 0 clears buffer (u + 1) % 3 before u's barrier: that
+    // buffer was last read in unit u - 2, which every thread left before
+    // passing unit u - 1's barrier, and is next filled in unit u + 1, after
+    // unit u's barrier.
+    static_assert(!kExclude || SEL_MAX_EXCLUDED == kNT, "one excluded id per thread");
+    uint32_t my_ex = 0xFFFFFFFFu;
+    uint32_t unit_no = 0;
+    if (kExclude) {
+        if (static_cast<uint32_t>(tid) < a.n_excluded) my_ex = a.excluded[tid];
+        if (tid < 3) s_ex_count[tid] = 0;
+        __syncthreads();
+    }
+
     auto accum = [&](const Unit& t, float4 (&q)[kVPT]) {
+        if (kExclude) {
+#pragma unroll
+            for (int s = 0; s < kVPT; ++s) {
+                nfacc = __fmaf_rn(q[s].x, 0.0f, nfacc);
+                nfacc = __fmaf_rn(q[s].y, 0.0f, nfacc);
+                nfacc = __fmaf_rn(q[s].z, 0.0f, nfacc);
+                nfacc = __fmaf_rn(q[s].w, 0.0f, nfacc);
+            }
+            const uint32_t p = unit_no;
+            unit_no = unit_no == 2u ? 0u : unit_no + 1u;
+            if (tid == 0) s_ex_count[unit_no] = 0;  // next unit's buffer
+            const uint32_t off = my_ex - t.lo;
+            if (my_ex != 0xFFFFFFFFu && off < t.hi - t.lo) s_ex_off[p][atomicAdd(&s_ex_count[p], 1u)] = off;
+            __syncthreads();
+            const uint32_t n = s_ex_count[p];
+            for (uint32_t i = 0; i < n; ++i) {
+                const uint32_t o = s_ex_off[p][i];
+                const uint32_t quad = o >> 2;
+                if (quad % kNT == static_cast<uint32_t>(tid)) {
+                    const uint32_t sl = quad / kNT, j = o & 3u;
+#pragma unroll
+                    for (int s = 0; s < kVPT; ++s) {
+                        if (static_cast<uint32_t>(s) == sl) {
+                            if (j == 0) q[s].x = -INFINITY;
+                            if (j == 1) q[s].y = -INFINITY;
+                            if (j == 2) q[s].z = -INFINITY;
+                            if (j == 3) q[s].w = -INFINITY;
+                        }
+                    }
+                }
+            }
+        }
 #pragma unroll
         for (int s = 0; s < kVPT; ++s) {
             const uint32_t e = t.lo + 4u * (tid + kNT * s);
             const float f[4] = {q[s].x, q[s].y, q[s].z, q[s].w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                nfacc = __fmaf_rn(f[j], 0.0f, nfacc);
+                if (!kExclude) nfacc = __fmaf_rn(f[j], 0.0f, nfacc);
                 if (f[j] > best[j]) {  // ids rise along each chain: '>' keeps the lowest
                     best[j] = f[j];
                     bbase[j] = e;
@@ -159,7 +215,9 @@ __global__ void __launch_bounds__(kNT, SEL_ARGMAX_MINB) argmax_kernel(ArgmaxArgs
                     warp_argmax(v, i, nf);
                 }
             }
-            if (last && lane == 0) a.out_ids[g.row] = nf ? SEL_INVALID_ID : i;
+            // i >= V: no real id won (every id of the row excluded, and the
+            // -FLT_MAX padding past the row end beat the masked -inf values)
+            if (last && lane == 0) a.out_ids[g.row] = (nf || i >= a.cfg.V) ? SEL_INVALID_ID : i;
         }
         __syncthreads();
     };
@@ -189,8 +247,11 @@ size_t argmax_ws_bytes(uint32_t rows, uint32_t V) { return argmax_layout(rows, V
 
 using namespace sel;
 
-extern "C" sel_status sel_argmax(const float* d_logits, uint32_t rows, uint32_t V, uint32_t* d_out_ids, void* d_ws,
-                                 size_t ws_bytes, cudaStream_t stream) {
+namespace sel {
+
+template <bool kExclude>
+sel_status launch_argmax(const float* d_logits, uint32_t rows, uint32_t V, const uint32_t* d_excluded,
+                         uint32_t n_excluded, uint32_t* d_out_ids, void* d_ws, size_t ws_bytes, cudaStream_t stream) {
     if (V == 0 || V > SEL_MAX_V) return SEL_EINVAL;
     if (rows == 0) return SEL_OK;
     if (!d_logits || !d_out_ids) return SEL_EINVAL;
@@ -205,9 +266,9 @@ extern "C" sel_status sel_argmax(const float* d_logits, uint32_t rows, uint32_t 
 
     const bool tma = (reinterpret_cast<uintptr_t>(d_logits) % 16 == 0) && (V % 4 == 0);
     constexpr size_t kDyn = stage_bytes<kNT, kVPT, kStages>();
-    static const bool attr_ok = set_dynamic_smem(argmax_kernel<true>, kDyn);
-    static const int res_tma = resident_blocks_dyn(argmax_kernel<true>, kNT, kDyn);
-    static const int res_sca = resident_blocks_dyn(argmax_kernel<false>, kNT, 0);
+    static const bool attr_ok = set_dynamic_smem(argmax_kernel<true, kExclude>, kDyn);
+    static const int res_tma = resident_blocks_dyn(argmax_kernel<true, kExclude>, kNT, kDyn);
+    static const int res_sca = resident_blocks_dyn(argmax_kernel<false, kExclude>, kNT, 0);
     if (!attr_ok) return SEL_ECUDA;
     const int res = tma ? res_tma : res_sca;
     const StreamPlan sp = plan_stream(rows, V, sms, res, kUnitMin, kUnitMax);
@@ -221,9 +282,28 @@ extern "C" sel_status sel_argmax(const float* d_logits, uint32_t rows, uint32_t 
     a.stride = l.stride;
     a.err = reinterpret_cast<uint32_t*>(ws);
     a.cfg = StreamCfg{rows * sp.chunks, sp.chunks, sp.chunk_elems, V};
+    a.excluded = d_excluded;
+    a.n_excluded = n_excluded;
     if (tma)
-        argmax_kernel<true><<<sp.grid, kNT, kDyn, stream>>>(a);
+        argmax_kernel<true, kExclude><<<sp.grid, kNT, kDyn, stream>>>(a);
     else
-        argmax_kernel<false><<<sp.grid, kNT, 0, stream>>>(a);
+        argmax_kernel<false, kExclude><<<sp.grid, kNT, 0, stream>>>(a);
     return cudaGetLastError() == cudaSuccess ? SEL_OK : SEL_ECUDA;
+}
+
+}  // namespace sel
+
+extern "C" sel_status sel_argmax(const float* d_logits, uint32_t rows, uint32_t V, uint32_t* d_out_ids, void* d_ws,
+                                 size_t ws_bytes, cudaStream_t stream) {
+    return sel::launch_argmax<false>(d_logits, rows, V, nullptr, 0, d_out_ids, d_ws, ws_bytes, stream);
+}
+
+extern "C" sel_status sel_argmax_excluding(const float* d_logits, uint32_t rows, uint32_t V,
+                                           const uint32_t* d_excluded, uint32_t n_excluded, uint32_t* d_out_ids,
+                                           void* d_ws, size_t ws_bytes, cudaStream_t stream) {
+    if (n_excluded > SEL_MAX_EXCLUDED) return SEL_EINVAL;
+    if (n_excluded > 0 && (!d_excluded || reinterpret_cast<uintptr_t>(d_excluded) % 4)) return SEL_EINVAL;
+    if (n_excluded == 0)
+        return sel::launch_argmax<false>(d_logits, rows, V, nullptr, 0, d_out_ids, d_ws, ws_bytes, stream);
+    return sel::launch_argmax<true>(d_logits, rows, V, d_excluded, n_excluded, d_out_ids, d_ws, ws_bytes, stream);
 }

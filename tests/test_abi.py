@@ -133,3 +133,16 @@ def test_shard_merge_validation_needs_no_gpu(lib):
              fake, fake, fake, None) == B.SEL_EINVAL
     assert s(fake, fake, 1, 2, 5, good, ctypes.byref(p), None, fake, fake, None) == B.SEL_EINVAL
     assert s(fake, fake, 0, 2, 5, good, ctypes.byref(p), None, None, None, None) == B.SEL_OK
+
+
+def test_eog_validation_needs_no_gpu(lib):
+    from sampling_row_fp32_gb300 import binding as B
+    vp = ctypes.c_void_p
+    fake = vp(0x10000)
+    f = lib.sel_argmax_excluding
+    assert f(fake, 1, 10, fake, 257, fake, fake, 4096, None) == B.SEL_EINVAL   # too many ids
+    assert f(fake, 1, 10, None, 3, fake, fake, 4096, None) == B.SEL_EINVAL     # no id array
+    assert f(fake, 1, 10, vp(0x10002), 3, fake, fake, 4096, None) == B.SEL_EINVAL
+    assert f(fake, 1, 0, fake, 3, fake, fake, 4096, None) == B.SEL_EINVAL      # V = 0
+    assert f(None, 0, 10, fake, 3, None, None, 0, None) == B.SEL_OK            # rows = 0
+    assert f(fake, 3, 300_000, fake, 3, fake, fake, 16, None) == B.SEL_EWORKSPACE
