@@ -67,6 +67,13 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.orc_argmax.restype = None
     lib.orc_argmax_excluding.argtypes = [_f32p, _u32, _u32, _u32p, _u32, _u32p]
     lib.orc_argmax_excluding.restype = None
+    lib.orc_spec_sampler.argtypes = [_f32p, _u32p, _u32, _u32, _u32, ctypes.c_double, _u32,
+                                     ctypes.c_double, ctypes.c_double, ctypes.c_int, _f32p,
+                                     _u32p, _u32p, _f64p]
+    lib.orc_spec_sampler.restype = ctypes.c_int
+    lib.orc_spec_diagnostics.argtypes = [_f32p, _f32p, _u32, _u32, _u32, ctypes.c_double,
+                                         _f64p, _f64p]
+    lib.orc_spec_diagnostics.restype = None
     lib.orc_topk.argtypes = [_f32p, _u32, _u32, _u32, _f32p, _u32p]
     lib.orc_topk.restype = None
     lib.orc_sample.argtypes = [_f32p, _u32, _u32, ctypes.c_double, _u32,
@@ -134,6 +141,38 @@ class Oracle:
         self.lib.orc_argmax_excluding(_ptr(x, _f32p), rows, V, _ptr(ex, _u32p), ex.size,
                                       _ptr(out, _u32p))
         return out
+
+    def spec_sampler(self, target, draft_tokens, temperature: float, top_k: int, top_p: float,
+                     min_p: float, u, temp_last: bool = False) -> SpecResult:
+        """Sampler-match acceptance: target [S, K+1, V], draft_tokens [S, K],
+        u [S, K+1] (one uniform per verified position). margin_draw holds the
+        smallest sampling margin of the draws each chain used."""
+        t = _f32(target)
+        S, K1, V = t.shape
+        K = K1 - 1
+        tok = np.ascontiguousarray(np.asarray(draft_tokens, dtype=np.uint32).reshape(S, K))
+        uu = _f32(u).reshape(S, K1)
+        acc = np.empty(S, dtype=np.uint32)
+        emi = np.empty((S, K1), dtype=np.uint32)
+        margin = np.empty(S, dtype=np.float64)
+        self.lib.orc_spec_sampler(_ptr(t, _f32p), _ptr(tok, _u32p), S, K, V, float(temperature),
+                                  int(top_k), float(top_p), float(min_p), int(bool(temp_last)),
+                                  _ptr(uu, _f32p), _ptr(acc, _u32p), _ptr(emi, _u32p),
+                                  _ptr(margin, _f64p))
+        return SpecResult(acc, emi, np.full(S, np.inf), margin)
+
+    def spec_diagnostics(self, target, draft, temperature: float):
+        """(sum_min, sum_prod), each [S, K]: sum_x min(p, q) and sum_x p q per
+        verified position."""
+        t = _f32(target)
+        d = _f32(draft)
+        S, K1, V = t.shape
+        K = K1 - 1
+        smin = np.empty((S, K), dtype=np.float64)
+        sprod = np.empty((S, K), dtype=np.float64)
+        self.lib.orc_spec_diagnostics(_ptr(t, _f32p), _ptr(d, _f32p), S, K, V, float(temperature),
+                                      _ptr(smin, _f64p), _ptr(sprod, _f64p))
+        return smin, sprod
 
     def topk(self, logits, k: int) -> tuple[np.ndarray, np.ndarray]:
         x = _f32(logits)

@@ -538,6 +538,113 @@ int orc_spec_accept(const float *target, const float *draft,
     return 0;
 }
 
+/*
+ * [Spec] "Sampler-match (the default at temperature > 0)": position j draws a
+ * fresh token from the target's sampler -- here the sampling chain of
+ * sample_row with the caller's policy and uniform u[j] -- and accepts the
+ * drafted token iff it equals that draw; the first mismatch emits the draw
+ * and ends the chain; when all K drafts match, the draw at position K is the
+ * bonus token. Every emitted token is a fresh draw from the target sampler.
+ * Readings: one uniform per verified position, u[0..K]; the sequence fails
+ * closed (every id 0xFFFFFFFF) on a nonfinite target row, a draft token >= V
+ * or any of its K + 1 uniforms outside [0, 1); T == 0 is the greedy sampler.
+ * *margin = the smallest sampling margin among the draws the chain used.
+ */
+static void spec_sampler_sequence(const float *target, const uint32_t *tokens,
+                                  uint32_t K, uint32_t V, double T,
+                                  uint32_t top_k, double top_p, double min_p,
+                                  int temp_last, const float *u,
+                                  uint32_t *accepted, uint32_t *emitted,
+                                  double *margin)
+{
+    *margin = INFINITY;
+    for (uint32_t j = 0; j <= K; ++j)
+        emitted[j] = ORC_INVALID;
+    *accepted = ORC_INVALID;
+    for (uint32_t j = 0; j <= K; ++j)
+        if (!row_is_finite(target + (size_t)j * V, V) ||
+            !uniform_is_valid(u[j]))
+            return;
+    for (uint32_t j = 0; j < K; ++j)
+        if (tokens[j] >= V)
+            return;
+    uint32_t n = 0, drawn = 0;
+    for (;;) {
+        double prob, m;
+        drawn = sample_row(target + (size_t)n * V, V, T, top_k, top_p, min_p,
+                           temp_last, u[n], &prob, &m);
+        if (m < *margin)
+            *margin = m;
+        if (n == K || tokens[n] != drawn)
+            break;
+        ++n;
+    }
+    for (uint32_t j = 0; j < n; ++j)
+        emitted[j] = tokens[j];
+    emitted[n] = drawn;
+    *accepted = n;
+}
+
+int orc_spec_sampler(const float *target, const uint32_t *draft_tokens,
+                     uint32_t S, uint32_t K, uint32_t V, double temperature,
+                     uint32_t top_k, double top_p, double min_p, int temp_last,
+                     const float *u, uint32_t *accepted, uint32_t *emitted,
+                     double *margin)
+{
+    for (uint32_t s = 0; s < S; ++s) {
+        double m;
+        spec_sampler_sequence(target + (size_t)s * (K + 1) * V,
+                              draft_tokens + (size_t)s * K, K, V, temperature,
+                              top_k, top_p, min_p, temp_last,
+                              u + (size_t)s * (K + 1), &accepted[s],
+                              emitted + (size_t)s * (K + 1), &m);
+        if (margin)
+            margin[s] = m;
+    }
+    return 0;
+}
+
+/*
+ * [Spec] "Verifying the gain before trusting a throughput number": per
+ * verified position, sum_x min(p(x), q(x)) -- the probability that modified
+ * rejection sampling accepts -- and sum_x p(x) q(x) -- the probability that
+ * sampler-match accepts -- with p = softmax(target_j / T) and
+ * q = softmax(draft_j / T), T > 0 (reading: the tempered distributions the
+ * rejection rule here uses, no filters). A position with a nonfinite target
+ * or draft row gives NaN for both.
+ */
+void orc_spec_diagnostics(const float *target, const float *draft, uint32_t S,
+                          uint32_t K, uint32_t V, double T, double *sum_min,
+                          double *sum_prod)
+{
+    double *p = (double *)malloc((size_t)V * sizeof(double));
+    double *q = (double *)malloc((size_t)V * sizeof(double));
+    for (uint32_t s = 0; s < S; ++s) {
+        for (uint32_t j = 0; j < K; ++j) {
+            const float *t = target + ((size_t)s * (K + 1) + j) * V;
+            const float *d = draft + ((size_t)s * K + j) * V;
+            double *om = sum_min + (size_t)s * K + j;
+            double *op = sum_prod + (size_t)s * K + j;
+            if (!row_is_finite(t, V) || !row_is_finite(d, V)) {
+                *om = NAN;
+                *op = NAN;
+                continue;
+            }
+            softmax_row(t, V, T, p);
+            softmax_row(d, V, T, q);
+            double a = 0.0, b = 0.0;
+            for (uint32_t i = 0; i < V; ++i) {
+                a += p[i] < q[i] ? p[i] : q[i];
+                b += p[i] * q[i];
+            }
+            *om = a;
+            *op = b;
+        }
+    }
+    free(q);
+    free(p);
+}
+
 /* Plain softmax of one row in double, exported for tests that need p and q. */
 void orc_softmax_row(const float *x, uint32_t V, double T, double *p)
 {

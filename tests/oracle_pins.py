@@ -444,6 +444,151 @@ def pin_spec_invalid(orc):
     assert r.accepted[2] == INVALID and np.all(r.emitted[2] == INVALID)
 
 
+# ---------------------------------------------------------------------------
+# sampler-match acceptance and the closed-form diagnostics
+# ---------------------------------------------------------------------------
+
+def _pair_rows(p, q):
+    """target [1, 2, V] (positions 0 and the bonus row both p) and draft [1, 1, V]."""
+    lp, lq = _logits_from(p), _logits_from(q)
+    return np.stack([lp, lp])[None], lq[None, None]
+
+
+def pin_diag_closed_forms(orc):
+    """mlxcel rules, "Verifying the gain": hand-computed sum min(p, q) and
+    sum p q (golden spec_diagnostics_closed_forms.json). The rows are fp32
+    logits log(p), so p comes back within ~1e-7."""
+    for c in golden("spec_diagnostics_closed_forms.json")["cases"]:
+        t, d = _pair_rows(c["p"], c["q"])
+        smin, sprod = orc.spec_diagnostics(t, d, 1.0)
+        assert abs(smin[0, 0] - c["sum_min"]) < 1e-6, (c["name"], smin)
+        assert abs(sprod[0, 0] - c["sum_prod"]) < 1e-6, (c["name"], sprod)
+        # the same distributions as logits 2 log p at temperature 2
+        smin2, sprod2 = orc.spec_diagnostics(2 * t, 2 * d, 2.0)
+        assert abs(smin2[0, 0] - c["sum_min"]) < 1e-6 and abs(sprod2[0, 0] - c["sum_prod"]) < 1e-6
+
+
+def pin_diag_inequality(orc):
+    """sum_min >= sum_prod always (min(a, b) >= a b on [0, 1]); both lie in
+    [0, 1]; p = q gives sum_min = 1; temperature scales both rows."""
+    rng = np.random.default_rng(31)
+    t = rng.normal(0, 2, size=(3, 5, 300)).astype(np.float32)
+    d = (t[:, :4] + rng.normal(0, 1, size=(3, 4, 300))).astype(np.float32)
+    for T in (0.5, 1.0, 2.0):
+        smin, sprod = orc.spec_diagnostics(t, d, T)
+        assert np.all(smin >= sprod - 1e-15) and np.all((sprod >= 0) & (smin <= 1 + 1e-12))
+    smin, _ = orc.spec_diagnostics(t, t[:, :4].copy(), 1.0)
+    assert np.allclose(smin, 1.0, atol=1e-12)
+    bad = d.copy()
+    bad[1, 2, 7] = np.nan
+    smin, sprod = orc.spec_diagnostics(t, bad, 1.0)
+    assert np.isnan(smin[1, 2]) and np.isnan(sprod[1, 2]) and not np.isnan(smin[1, 1])
+
+
+def _draw(rng, probs, n):
+    return rng.choice(len(probs), size=n, p=np.asarray(probs) / np.sum(probs))
+
+
+def pin_diag_is_the_rejection_acceptance(orc):
+    """The rejection rule's empirical acceptance at a position, over drafts
+    drawn from q, converges to the oracle's sum_min (5 sigma binomial)."""
+    c = golden("spec_diagnostics_closed_forms.json")["cases"][3]
+    t, d = _pair_rows(c["p"], c["q"])
+    smin, _ = orc.spec_diagnostics(t, d, 1.0)
+    n = 20000
+    rng = np.random.default_rng(32)
+    tok = _draw(rng, c["q"], n).astype(np.uint32).reshape(n, 1)
+    res = orc.spec_accept(np.repeat(t, n, 0), np.repeat(d, n, 0), tok, 1.0, 0,
+                          rng.random((n, 1), dtype=np.float32), rng.random(n, dtype=np.float32))
+    rate = float(np.mean(res.accepted == 1))
+    sd = math.sqrt(smin[0, 0] * (1 - smin[0, 0]) / n)
+    assert abs(rate - smin[0, 0]) < 5 * sd, (rate, smin)
+
+
+def _sampler(orc, t, tok, u, T=1.0, top_k=0):
+    return orc.spec_sampler(t, tok, T, top_k, 1.0, 0.0, u)
+
+
+def pin_sampler_acceptance_law(orc):
+    """mlxcel rules, "Sampler-match": acceptance probability sum_x p(x) q(x)
+    for drafts drawn from q and a fresh draw from p (5 sigma binomial), with
+    sum p q computed here from the two distributions."""
+    for c in golden("spec_diagnostics_closed_forms.json")["cases"][:4:3]:
+        p, q = np.asarray(c["p"]), np.asarray(c["q"])
+        t, _ = _pair_rows(p, q)
+        n = 20000
+        rng = np.random.default_rng(33)
+        tok = _draw(rng, q, n).astype(np.uint32).reshape(n, 1)
+        res = _sampler(orc, np.repeat(t, n, 0), tok, rng.random((n, 2), dtype=np.float32))
+        want = float(np.sum(p * q))
+        rate = float(np.mean(res.accepted == 1))
+        sd = math.sqrt(want * (1 - want) / n)
+        assert abs(rate - want) < 5 * sd + 1e-12, (c["name"], rate, want)
+
+
+def pin_sampler_stream_is_target(orc):
+    """Lossless: the token emitted at the first position is distributed as p
+    whatever q is (chi-square, the recipe of golden chi_square_recipe.json)."""
+    rec = golden("chi_square_recipe.json")
+    V, n = rec["dof"] + 1, rec["samples"]
+    p = np.array([0.30, 0.22, 0.18, 0.12, 0.10, 0.08])
+    q = np.array([0.02, 0.03, 0.05, 0.10, 0.30, 0.50])
+    assert V == p.size
+    t, _ = _pair_rows(p, q)
+    rng = np.random.default_rng(34)
+    tok = _draw(rng, q, n).astype(np.uint32).reshape(n, 1)
+    res = _sampler(orc, np.repeat(t, n, 0), tok, rng.random((n, 2), dtype=np.float32))
+    first = res.emitted[:, 0]
+    counts = np.bincount(first.astype(np.int64), minlength=V)
+    chi2 = float(np.sum((counts - n * p) ** 2 / (n * p)))
+    assert chi2 < rec["critical"], chi2
+    # power: emitting the draft token itself would fail
+    counts_q = np.bincount(tok[:, 0].astype(np.int64), minlength=V)
+    assert float(np.sum((counts_q - n * p) ** 2 / (n * p))) > rec["critical"]
+
+
+def pin_sampler_greedy_and_support(orc):
+    """T = 0: every draw is the row's first maximum (numpy.argmax), so the
+    chain is the first-mismatch rule on argmaxes; with top_k = 2 every emitted
+    draw lies in its row's top two."""
+    rng = np.random.default_rng(35)
+    S, K, V = 40, 4, 9
+    t = rng.integers(0, 4, size=(S, K + 1, V)).astype(np.float32)
+    a = np.argmax(t, axis=2)
+    tok = np.where(rng.random((S, K)) < 0.7, a[:, :K], rng.integers(0, V, size=(S, K))).astype(np.uint32)
+    res = orc.spec_sampler(t, tok, 0.0, 1, 1.0, 0.0, rng.random((S, K + 1), dtype=np.float32))
+    for s in range(S):
+        n = 0
+        while n < K and tok[s, n] == a[s, n]:
+            n += 1
+        assert res.accepted[s] == n
+        assert list(res.emitted[s, :n]) == list(tok[s, :n]) and res.emitted[s, n] == a[s, n]
+        assert np.all(res.emitted[s, n + 1:] == INVALID)
+    t2 = rng.normal(0, 1, size=(S, K + 1, V)).astype(np.float32)
+    res = orc.spec_sampler(t2, tok, 1.0, 2, 1.0, 0.0, rng.random((S, K + 1), dtype=np.float32))
+    for s in range(S):
+        n = int(res.accepted[s])
+        top2 = set(np.argsort(-t2[s, n], kind="stable")[:2])
+        assert int(res.emitted[s, n]) in top2
+
+
+def pin_sampler_invalid(orc):
+    """Fail closed: a bad uniform at any position (used or not), a draft token
+    >= V or a nonfinite target row makes every id of the sequence invalid."""
+    rng = np.random.default_rng(36)
+    S, K, V = 4, 3, 20
+    t = rng.normal(size=(S, K + 1, V)).astype(np.float32)
+    tok = rng.integers(0, V, size=(S, K)).astype(np.uint32)
+    u = rng.random((S, K + 1), dtype=np.float32)
+    u[0, K] = 1.0
+    tok[1, 2] = V
+    t[2, 1, 5] = np.inf
+    res = orc.spec_sampler(t, tok, 1.0, 5, 0.9, 0.0, u)
+    for s in range(3):
+        assert res.accepted[s] == INVALID and np.all(res.emitted[s] == INVALID)
+    assert res.accepted[3] != INVALID
+
+
 ALL_PINS = [
     pin_argmax_ties, pin_argmax_bruteforce, pin_argmax_numpy,
     pin_argmax_partition, pin_argmax_nonfinite,
@@ -454,6 +599,9 @@ ALL_PINS = [
     pin_spec_closed_forms, pin_spec_ceiling_example, pin_spec_acceptance_law,
     pin_spec_stream_is_target, pin_spec_support, pin_spec_regimes,
     pin_spec_greedy, pin_spec_invalid,
+    pin_diag_closed_forms, pin_diag_inequality, pin_diag_is_the_rejection_acceptance,
+    pin_sampler_acceptance_law, pin_sampler_stream_is_target, pin_sampler_greedy_and_support,
+    pin_sampler_invalid,
 ]
 
 

@@ -70,6 +70,19 @@ MUTANTS = [
     ("EOG latch dropped",
      [("!row_is_finite(x, V))\n        return ORC_INVALID;\n    uint32_t best = ORC_INVALID;",
        "0)\n        return ORC_INVALID;\n    uint32_t best = ORC_INVALID;")]),
+    ("sampler-match accepts a mismatch",
+     [("if (n == K || tokens[n] != drawn)", "if (n == K || tokens[n] == drawn)")]),
+    ("sampler-match always samples the first row",
+     [("drawn = sample_row(target + (size_t)n * V, V, T,", "drawn = sample_row(target, V, T,")]),
+    ("sampler-match ignores bad uniforms",
+     [("!uniform_is_valid(u[j]))", "0)")]),
+    ("diagnostics take the max for the min",
+     [("a += p[i] < q[i] ? p[i] : q[i];", "a += p[i] > q[i] ? p[i] : q[i];")]),
+    ("diagnostics square p",
+     [("b += p[i] * q[i];", "b += p[i] * p[i];")]),
+    ("diagnostics ignore the temperature",
+     [("            softmax_row(t, V, T, p);\n            softmax_row(d, V, T, q);",
+       "            softmax_row(t, V, 1.0, p);\n            softmax_row(d, V, 1.0, q);")]),
     ("EOG all-excluded row answers id 0",
      [("    return best;\n}\n\nvoid orc_argmax_excluding(",
        "    return best == ORC_INVALID ? 0 : best;\n}\n\nvoid orc_argmax_excluding(")]),
