@@ -260,6 +260,7 @@ def gpu_arm(args, rank, world, local_rank):
             b.record(stream)
         torch.cuda.synchronize()
         per_op_us.append(a.elapsed_time(b) * 1e3 / OP_REPS)
+    extra = extra_ops(B, dev, xs, drafts, tok, stream)
     # keep the same load running briefly so the clock sampler sees it even
     # when the timed region is shorter than its period
     tail_until = time.time() + 0.6
@@ -323,8 +324,83 @@ def gpu_arm(args, rank, world, local_rank):
                   "launches of each op between events on the launching stream",
         "clocks": clk,
         "e2e": e2e,
+        "extra_ops": extra,
     }
     return line
+
+
+def extra_ops(B, dev, xs, drafts, tok, stream):
+    """The calls beyond the step, on the same batch and copy rotation, each
+    timed over OP_REPS graph-replayed launches: the EOG-excluding argmax (8
+    ids), sampler-match acceptance (7 x 6, the step's policy), the closed-form
+    diagnostics (7 x 6) and a two-shard top-k (k = 20 per shard on each half
+    of the vocabulary, then the merge)."""
+    import torch
+    peak, _ = measured_peak()
+    ids = torch.empty(ROWS, dtype=torch.int32, device=dev)
+    exd = torch.tensor([0, 5, 1000, 4096, 77_777, 151_643, 151_645, 248_000], dtype=torch.int32, device=dev)
+    ws_a = B.workspace(B.SEL_OP_ARGMAX, ROWS, V, device=dev)
+    prm = B.SampleParams(POLICY["temperature"], POLICY["top_k"], POLICY["top_p"], POLICY["min_p"],
+                         B.SEL_ORDER_TEMP_FIRST)
+    ud = torch.rand(SPEC_S, SPEC_K + 1, device=dev)
+    acc = torch.empty(SPEC_S, dtype=torch.int32, device=dev)
+    emi = torch.empty(SPEC_S, SPEC_K + 1, dtype=torch.int32, device=dev)
+    ws_m = B.workspace(B.SEL_OP_SPEC_SAMPLER, ROWS, V, POLICY["top_k"], device=dev)
+    smin = torch.empty(SPEC_S, SPEC_K, device=dev)
+    sprod = torch.empty(SPEC_S, SPEC_K, device=dev)
+    ws_d = B.workspace(B.SEL_OP_SPEC_DIAG, SPEC_S, V, SPEC_K, device=dev)
+    from sampling_row_fp32_gb300 import shards as sh
+    offs = sh.shard_offsets(V, 2, min_size=K_TOPK)
+    halves = [[x[:, offs[g]:offs[g + 1]].contiguous() for g in range(2)] for x in xs]
+    sv = [torch.empty(ROWS, K_TOPK, device=dev) for _ in range(2)]
+    si = [torch.empty(ROWS, K_TOPK, dtype=torch.int32, device=dev) for _ in range(2)]
+    ws_s = [B.workspace(B.SEL_OP_TOPK, ROWS, offs[g + 1] - offs[g], K_TOPK, device=dev) for g in range(2)]
+    gv = torch.empty(ROWS, 2, K_TOPK, device=dev)
+    gi = torch.empty(ROWS, 2, K_TOPK, dtype=torch.int32, device=dev)
+    mv = torch.empty(ROWS, K_TOPK, device=dev)
+    mi = torch.empty(ROWS, K_TOPK, dtype=torch.int32, device=dev)
+
+    def tview(t):
+        return t.view(SPEC_S, SPEC_K + 1, V)
+
+    def sharded(r):
+        for g in range(2):
+            B.sel_topk(halves[r % N_COPIES][g], K_TOPK, sv[g], si[g], ws_s[g])
+            gv[:, g].copy_(sv[g])
+            gi[:, g].copy_(si[g])
+        B.sel_merge_shards(gv, gi, offs, mv, mi)
+
+    calls = {
+        "argmax_excluding_8": (lambda r: B.sel_argmax_excluding(xs[r % N_COPIES], exd, ids, ws_a), ROWS * ROW_BYTES),
+        "spec_sampler_match": (lambda r: B.spec_accept_sampler(tview(xs[r % N_COPIES]), tok, prm, ud, acc, emi, ws_m),
+                               ROWS * ROW_BYTES),
+        "spec_diagnostics": (lambda r: B.spec_diagnostics(tview(xs[r % N_COPIES]), drafts[r % 2], 1.0, smin, sprod,
+                                                          ws_d),
+                             (SPEC_S * (2 * SPEC_K + 1) + 2 * SPEC_S * SPEC_K) * ROW_BYTES),
+        "topk_two_shards": (sharded, ROWS * ROW_BYTES),
+    }
+    out = {}
+    for name, (fn, nbytes) in calls.items():
+        with torch.cuda.stream(stream):
+            for r in range(3):
+                fn(r)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for r in range(OP_REPS):
+                fn(r)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / OP_REPS
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out[name] = {"us": round(us, 3), "bytes": nbytes, "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
+    return out
 
 
 OP_KERNELS = {  # ncu kernel-name patterns of each op's launches

@@ -63,7 +63,8 @@ typedef enum sel_status {
 #define SEL_WS_ALIGN 256u
 
 /* Operation codes for sel_workspace_bytes. */
-enum { SEL_OP_ARGMAX = 0, SEL_OP_TOPK = 1, SEL_OP_SAMPLE = 2, SEL_OP_SPEC = 3 };
+enum { SEL_OP_ARGMAX = 0, SEL_OP_TOPK = 1, SEL_OP_SAMPLE = 2, SEL_OP_SPEC = 3,
+       SEL_OP_SPEC_SAMPLER = 4, SEL_OP_SPEC_DIAG = 5 };
 
 /* Order of temperature and filters in sel_sample. */
 enum {
@@ -87,6 +88,9 @@ enum {
  *   op SEL_OP_TOPK:   rows, V, k
  *   op SEL_OP_SAMPLE: rows, V, k = the policy's top_k
  *   op SEL_OP_SPEC:   rows = S (sequences), V, k = K (draft positions)
+ *   op SEL_OP_SPEC_SAMPLER: rows = S * (K + 1) (target rows), V,
+ *                     k = the policy's top_k
+ *   op SEL_OP_SPEC_DIAG: rows = S, V, k = K
  * The size depends only on these arguments, not on the device. Returns 0
  * when the arguments are invalid (the entry point would refuse them anyway).
  */
@@ -233,6 +237,57 @@ sel_status spec_accept(const float *d_target, const float *d_draft,
                        const float *d_u_acc, const float *d_u_fin,
                        uint32_t *d_accepted, uint32_t *d_emitted, void *d_ws,
                        size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * spec_accept_sampler -- the sampler-match rule of "Speculative-decoding
+ * acceptance rules" (mlxcel), "Sampler-match": each verified position j
+ * draws a fresh token from the target's sampler -- the sel_sample chain with
+ * policy `p` over target row j and the uniform u[s][j] -- and the drafted
+ * token t_j is accepted iff it equals that draw. The first mismatch emits
+ * the draw and ends the chain; if all K drafts match, the draw at position K
+ * is the bonus token. Lossless: every emitted token is a draw from the target
+ * sampler; the acceptance probability is sum_x p(x) q(x).
+ *
+ *   d_target        [S][K+1][V] f32 target logits
+ *   d_draft_tokens  [S][K] u32
+ *   p               the target sampler (as for sel_sample; top_k >= 1 unless
+ *                   temperature == 0, which is greedy)
+ *   d_u             [S][K+1] f32, one uniform per verified position
+ *   d_accepted, d_emitted  as for spec_accept
+ *   d_ws            workspace of sel_workspace_bytes(SEL_OP_SPEC_SAMPLER,
+ *                   S * (K + 1), V, p->top_k)
+ * A sequence with a nonfinite target row, a draft token >= V or any of its
+ * K + 1 uniforms outside [0, 1) gets 0xFFFFFFFF everywhere. Two launches.
+ */
+sel_status spec_accept_sampler(const float *d_target,
+                               const uint32_t *d_draft_tokens, uint32_t S,
+                               uint32_t K, uint32_t V,
+                               const sel_sample_params *p, const float *d_u,
+                               uint32_t *d_accepted, uint32_t *d_emitted,
+                               void *d_ws, size_t ws_bytes,
+                               cudaStream_t stream);
+
+/*
+ * spec_diagnostics -- the closed-form acceptance diagnostics of
+ * "Speculative-decoding acceptance rules" (mlxcel), "Verifying the gain
+ * before trusting a throughput number": per verified position j < K,
+ * sum_x min(p_j(x), q_j(x)) (the acceptance probability of modified rejection
+ * sampling) and sum_x p_j(x) q_j(x) (that of sampler-match), with
+ * p_j = softmax(target_j / T) and q_j = softmax(draft_j / T), T > 0.
+ *
+ *   d_target [S][K+1][V], d_draft [S][K][V] f32 (target row K is read but
+ *            not used)
+ *   d_sum_min, d_sum_prod  [S][K] f32 outputs; NaN for a position whose
+ *            target or draft row holds a NaN or Inf
+ *   d_ws     workspace of sel_workspace_bytes(SEL_OP_SPEC_DIAG, S, V, K)
+ * Reads every row once for its statistics and each position's pair of rows
+ * once more. Two launches.
+ */
+sel_status spec_diagnostics(const float *d_target, const float *d_draft,
+                            uint32_t S, uint32_t K, uint32_t V,
+                            float temperature, float *d_sum_min,
+                            float *d_sum_prod, void *d_ws, size_t ws_bytes,
+                            cudaStream_t stream);
 
 /*
  * sel_argmax_noalloc -- sel_argmax for callers that cannot allocate device

@@ -21,13 +21,14 @@ from . import build as _build
 SEL_OK, SEL_EINVAL, SEL_EWORKSPACE, SEL_ECUDA, SEL_EUNSUPPORTED = range(5)
 SEL_INVALID_ID = 0xFFFFFFFF
 SEL_MAX_K = 1024
-SEL_OP_ARGMAX, SEL_OP_TOPK, SEL_OP_SAMPLE, SEL_OP_SPEC = range(4)
+SEL_OP_ARGMAX, SEL_OP_TOPK, SEL_OP_SAMPLE, SEL_OP_SPEC, SEL_OP_SPEC_SAMPLER, SEL_OP_SPEC_DIAG = range(6)
 SEL_ORDER_TEMP_FIRST, SEL_ORDER_TEMP_LAST = 0, 1
 SPEC_MODE_REJECTION, SPEC_MODE_ARGMAX = 0, 1
 
 EXPORTED = ("sel_workspace_bytes", "sel_workspace_init", "sel_argmax", "sel_topk",
             "sel_sample", "spec_accept", "sel_status_string", "sel_argmax_noalloc",
-            "sel_merge_shards", "sel_sample_shards", "sel_argmax_excluding")
+            "sel_merge_shards", "sel_sample_shards", "sel_argmax_excluding",
+            "spec_accept_sampler", "spec_diagnostics")
 SEL_NOALLOC_SCRATCH_BYTES = 1 << 20
 SEL_MAX_SHARDS = 64
 SEL_MAX_EXCLUDED = 256
@@ -87,6 +88,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.spec_accept.restype = ctypes.c_int
     lib.sel_argmax_noalloc.argtypes = [_vp, _u32, _u32, _vp, _vp]
     lib.sel_argmax_noalloc.restype = ctypes.c_int
+    lib.spec_accept_sampler.argtypes = [_vp, _vp, _u32, _u32, _u32, ctypes.POINTER(SampleParams), _vp,
+                                        _vp, _vp, _vp, _sz, _vp]
+    lib.spec_accept_sampler.restype = ctypes.c_int
+    lib.spec_diagnostics.argtypes = [_vp, _vp, _u32, _u32, _u32, ctypes.c_float, _vp, _vp, _vp, _sz, _vp]
+    lib.spec_diagnostics.restype = ctypes.c_int
     lib.sel_argmax_excluding.argtypes = [_vp, _u32, _u32, _vp, _u32, _vp, _vp, _sz, _vp]
     lib.sel_argmax_excluding.restype = ctypes.c_int
     lib.sel_merge_shards.argtypes = [_vp, _vp, _u32, _u32, _u32, _vp, _vp, _vp, _vp]
@@ -219,6 +225,29 @@ def spec_accept(target, draft, draft_tokens, params: SpecParams, u_acc, u_fin, a
                               ctypes.byref(params), _ptr(u_acc), _ptr(u_fin), _ptr(accepted),
                               _ptr(emitted), _ptr(ws), _nbytes(ws), _stream(stream)),
            "spec_accept")
+
+
+def spec_accept_sampler(target, draft_tokens, params: SampleParams, u, accepted, emitted, ws=None,
+                        stream=None) -> None:
+    """target [S, K+1, V], draft_tokens [S, K], u [S, K+1]."""
+    _check_f32(target, "target")
+    _check_f32(u, "u")
+    _check_ids(draft_tokens, "draft_tokens")
+    S, K1, V = target.shape
+    _check(load().spec_accept_sampler(_ptr(target), _ptr(draft_tokens), S, K1 - 1, V, ctypes.byref(params),
+                                      _ptr(u), _ptr(accepted), _ptr(emitted), _ptr(ws), _nbytes(ws),
+                                      _stream(stream)), "spec_accept_sampler")
+
+
+def spec_diagnostics(target, draft, temperature: float, sum_min, sum_prod, ws=None, stream=None) -> None:
+    """target [S, K+1, V], draft [S, K, V] -> sum_min, sum_prod [S, K]."""
+    _check_f32(target, "target")
+    _check_f32(draft, "draft")
+    _check_f32(sum_min, "sum_min")
+    _check_f32(sum_prod, "sum_prod")
+    S, K1, V = target.shape
+    _check(load().spec_diagnostics(_ptr(target), _ptr(draft), S, K1 - 1, V, float(temperature), _ptr(sum_min),
+                                   _ptr(sum_prod), _ptr(ws), _nbytes(ws), _stream(stream)), "spec_diagnostics")
 
 
 def _host_offsets(offsets):

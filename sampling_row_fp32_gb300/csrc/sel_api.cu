@@ -39,6 +39,10 @@ extern "C" size_t sel_workspace_bytes(int op, uint32_t rows, uint32_t V, uint32_
         }
         case SEL_OP_SPEC:
             return spec_ws_bytes(rows, V, k);
+        case SEL_OP_SPEC_SAMPLER:
+            return spec_sampler_ws_bytes(rows, V, k);
+        case SEL_OP_SPEC_DIAG:
+            return spec_diag_ws_bytes(rows, V, k);
         default:
             return 0;
     }

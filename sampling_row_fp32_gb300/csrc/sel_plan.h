@@ -81,6 +81,8 @@ int device_sms();
 size_t argmax_ws_bytes(uint32_t rows, uint32_t V);
 size_t topk_ws_bytes(uint32_t rows, uint32_t V, uint32_t k);
 size_t spec_ws_bytes(uint32_t S, uint32_t V, uint32_t K);
+size_t spec_diag_ws_bytes(uint32_t S, uint32_t V, uint32_t K);
+size_t spec_sampler_ws_bytes(uint32_t rows_t, uint32_t V, uint32_t top_k);
 
 // Workspace: a 256-byte header (word 0: error flags the kernels raise), a
 // per-row arrival counter array, then the per-op payload.

@@ -113,6 +113,7 @@ struct SpecArgs {
     RowPart* row_stats;    // [rows_a]
     Decision* decisions;   // [S]
     uint32_t cmax;
+    bool decide;           // run the acceptance chain (false: row statistics only)
 };
 
 __device__ __forceinline__ bool beats(float v, uint32_t i, float w, uint32_t j) {
@@ -363,16 +364,18 @@ __global__ void __launch_bounds__(kNT, 2) spec_phase1_kernel(SpecArgs a) {
                 if (lane == 0) a.row_stats[g.row] = RowPart{rm, ri | rnf, rs.hi, rs.lo};
             }
             // the last row of the sequence to finish runs the acceptance chain
-            uint32_t seq;
-            phase1_row(a, g.row, seq);
-            bool last = false;
-            if (lane == 0) {
-                const uint32_t rows_per_seq = kRej ? 2u * a.K + 1u : a.K + 1u;
-                last = segment_arrive(&a.seq_ctr[seq], rows_per_seq);
-            }
-            if (__shfl_sync(kFull, last, 0)) {
-                __threadfence();
-                decide_sequence<kRej>(a, seq);
+            if (a.decide) {
+                uint32_t seq;
+                phase1_row(a, g.row, seq);
+                bool last = false;
+                if (lane == 0) {
+                    const uint32_t rows_per_seq = kRej ? 2u * a.K + 1u : a.K + 1u;
+                    last = segment_arrive(&a.seq_ctr[seq], rows_per_seq);
+                }
+                if (__shfl_sync(kFull, last, 0)) {
+                    __threadfence();
+                    decide_sequence<kRej>(a, seq);
+                }
             }
         }
         __syncthreads();
@@ -665,11 +668,132 @@ __global__ void __launch_bounds__(kNT) spec_draw_kernel(DrawArgs a) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// Closed-form diagnostics (mlxcel rules, "Verifying the gain"): per verified
+// position, sum_x min(p, q) and sum_x p q from the phase-1 row statistics and
+// one more pass over the target and draft rows of the position.
+// ---------------------------------------------------------------------------
+
+struct alignas(16) DiagPart {
+    FF mn;    // sum of min(p, q) over the chunk
+    FF prod;  // sum of p q over the chunk
+};
+
+struct DiagLayout {
+    size_t pos_ctr, parts, total;
+};
+
+DiagLayout diag_layout(uint32_t S, uint32_t V, uint32_t K) {
+    DiagLayout d{};
+    const SpecLayout l = spec_layout(S, V, K);
+    const size_t positions = static_cast<size_t>(S) * K;
+    d.pos_ctr = l.total;
+    d.parts = d.pos_ctr + align_up(positions * 4u, 256);
+    d.total = d.parts + align_up(positions * l.cmax_b * sizeof(DiagPart), 256);
+    return d;
+}
+
+struct DiagArgs {
+    const float* target;
+    const float* draft;
+    uint32_t S, K, V;
+    float log2e_over_T;
+    uint32_t chunks, chunk_elems;  // chunk_elems a multiple of 1024, at most kDrawChunkMax
+    const RowPart* row_stats;
+    uint32_t* pos_ctr;             // [S * K]
+    DiagPart* parts;               // [S * K][cmax]
+    uint32_t cmax;
+    float* sum_min;                // [S][K]
+    float* sum_prod;               // [S][K]
+};
+
+template <bool kVec>
+__global__ void __launch_bounds__(kNT) spec_diag_kernel(DiagArgs a) {
+    __shared__ FF s_m[kWarps];
+    __shared__ FF s_p[kWarps];
+    __shared__ bool s_last;
+    const uint32_t pos = blockIdx.x / a.chunks;
+    const uint32_t chunk = blockIdx.x - pos * a.chunks;
+    const uint32_t s = pos / a.K, j = pos - s * a.K;
+    const uint32_t V = a.V;
+    const uint32_t ti = s * (a.K + 1u) + j;
+    const uint32_t di = a.S * (a.K + 1u) + s * a.K + j;
+    const float* trow = a.target + static_cast<size_t>(ti) * V;
+    const float* drow = a.draft + (static_cast<size_t>(s) * a.K + j) * V;
+    const RowPart ps = a.row_stats[ti];
+    const RowPart qs = a.row_stats[di];
+    const float c = a.log2e_over_T;
+    const float pinv = 1.0f / ps.s_hi, qinv = 1.0f / qs.s_hi;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int kQ = static_cast<int>(kDrawPer / 4u);
+    const uint32_t lo = chunk * a.chunk_elems;
+    const uint32_t hi = min(V, lo + a.chunk_elems);
+    float smin = 0.0f, sprod = 0.0f;
+    {
+        float4 xp[kQ], xq[kQ];
+#pragma unroll
+        for (int i = 0; i < kQ; ++i) {
+            const uint32_t e = lo + 4u * (static_cast<uint32_t>(tid) + kNT * i);
+            xp[i] = ld_quad<kVec>(trow, e, hi, -INFINITY);
+            xq[i] = ld_quad<kVec>(drow, e, hi, -INFINITY);
+        }
+#pragma unroll
+        for (int i = 0; i < kQ; ++i) {
+            const float fp[4] = {xp[i].x, xp[i].y, xp[i].z, xp[i].w};
+            const float fq[4] = {xq[i].x, xq[i].y, xq[i].z, xq[i].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float p = ex2_approx((fp[k] - ps.m) * c) * pinv;
+                const float q = ex2_approx((fq[k] - qs.m) * c) * qinv;
+                smin += fminf(p, q);
+                sprod = __fmaf_rn(p, q, sprod);
+            }
+        }
+    }
+    const FF wm = ff_warp_sum(FF{smin, 0.0f});
+    const FF wp = ff_warp_sum(FF{sprod, 0.0f});
+    if (lane == 0) { s_m[warp] = wm; s_p[warp] = wp; }
+    __syncthreads();
+    if (tid == 0) {
+        FF bm{0.0f, 0.0f}, bp{0.0f, 0.0f};
+        for (int w = 0; w < kWarps; ++w) { bm = ff_add(bm, s_m[w]); bp = ff_add(bp, s_p[w]); }
+        a.parts[static_cast<size_t>(pos) * a.cmax + chunk] = DiagPart{bm, bp};
+        s_last = arrive_is_last(&a.pos_ctr[pos], a.chunks);
+    }
+    __syncthreads();
+    if (!s_last || warp != 0) return;
+    // the last block of the position adds the chunk sums in chunk order
+    __threadfence();
+    const DiagPart* parts = a.parts + static_cast<size_t>(pos) * a.cmax;
+    FF M{0.0f, 0.0f}, P{0.0f, 0.0f};
+    for (uint32_t c0 = 0; c0 < a.chunks; c0 += 32) {
+        const uint32_t ci = c0 + lane;
+        FF m{0.0f, 0.0f}, pr{0.0f, 0.0f};
+        if (ci < a.chunks) {
+            m = FF{ld_gpu_f32(&parts[ci].mn.hi), ld_gpu_f32(&parts[ci].mn.lo)};
+            pr = FF{ld_gpu_f32(&parts[ci].prod.hi), ld_gpu_f32(&parts[ci].prod.lo)};
+        }
+        M = ff_add(M, ff_warp_sum(m));
+        P = ff_add(P, ff_warp_sum(pr));
+    }
+    if (lane == 0) {
+        const bool nf = ((ps.idx | qs.idx) & kNonfiniteBit) != 0u;
+        const float nan = __uint_as_float(0x7fc00000u);
+        a.sum_min[pos] = nf ? nan : M.hi + M.lo;
+        a.sum_prod[pos] = nf ? nan : P.hi + P.lo;
+    }
+}
+
 }  // namespace
 
 size_t spec_ws_bytes(uint32_t S, uint32_t V, uint32_t K) {
     if (S == 0 || V == 0) return 0;
     return spec_layout(S, V, K).total;
+}
+
+size_t spec_diag_ws_bytes(uint32_t S, uint32_t V, uint32_t K) {
+    if (S == 0 || V == 0 || K == 0) return 0;
+    return diag_layout(S, V, K).total;
 }
 
 }  // namespace sel
@@ -733,6 +857,7 @@ extern "C" sel_status spec_accept(const float* d_target, const float* d_draft, c
     a.row_stats = reinterpret_cast<RowPart*>(ws + l.row_stats);
     a.decisions = reinterpret_cast<Decision*>(ws + l.decisions);
     a.cmax = l.cmax_a;
+    a.decide = true;
     const dim3 grid1(plan.grid);
     if (rej) {
         if (vec) spec_phase1_kernel<true, true><<<grid1, kNT, kDyn, stream>>>(a);
@@ -770,5 +895,84 @@ extern "C" sel_status spec_accept(const float* d_target, const float* d_draft, c
     const dim3 grid2(S * chunks2);
     if (vec) spec_draw_kernel<true><<<grid2, kNT, 0, stream>>>(b);
     else spec_draw_kernel<false><<<grid2, kNT, 0, stream>>>(b);
+    return cudaGetLastError() == cudaSuccess ? SEL_OK : SEL_ECUDA;
+}
+
+extern "C" sel_status spec_diagnostics(const float* d_target, const float* d_draft, uint32_t S, uint32_t K,
+                                       uint32_t V, float temperature, float* d_sum_min, float* d_sum_prod,
+                                       void* d_ws, size_t ws_bytes, cudaStream_t stream) {
+    if (V == 0 || V > SEL_MAX_V) return SEL_EINVAL;
+    if (!(temperature > 0.0f) || !(temperature < INFINITY)) return SEL_EINVAL;
+    if (S == 0 || K == 0) return SEL_OK;
+    if (!d_target || !d_draft || !d_sum_min || !d_sum_prod) return SEL_EINVAL;
+    const uintptr_t mis = reinterpret_cast<uintptr_t>(d_target) | reinterpret_cast<uintptr_t>(d_draft) |
+                          reinterpret_cast<uintptr_t>(d_sum_min) | reinterpret_cast<uintptr_t>(d_sum_prod);
+    if (mis % 4) return SEL_EINVAL;
+    const uint64_t rows_a = static_cast<uint64_t>(S) * (2ull * K + 1ull);
+    if (rows_a > 0x7fffffffull || K > 0x3fffffffu) return SEL_EUNSUPPORTED;
+    const SpecLayout l = spec_layout(S, V, K);
+    const DiagLayout dl = diag_layout(S, V, K);
+    if (!d_ws) return SEL_EINVAL;
+    if (reinterpret_cast<uintptr_t>(d_ws) % SEL_WS_ALIGN) return SEL_EINVAL;
+    if (ws_bytes < dl.total) return SEL_EWORKSPACE;
+    const int sms = device_sms();
+    if (sms <= 0) return SEL_ECUDA;
+
+    // phase 1: (max, sum exp) of every target and draft row, no acceptance chain
+    char* ws = static_cast<char*>(d_ws);
+    const uint32_t rows1 = static_cast<uint32_t>(rows_a);
+    const bool vec = V % 4 == 0 && reinterpret_cast<uintptr_t>(d_target) % 16 == 0 &&
+                     reinterpret_cast<uintptr_t>(d_draft) % 16 == 0;
+    constexpr size_t kDyn = stage_bytes<kNT, kVPT, kStages>();
+    static const bool attr_ok = set_dynamic_smem(spec_phase1_kernel<true, true>, kDyn);
+    static const int res_tma = resident_blocks_dyn(spec_phase1_kernel<true, true>, kNT, kDyn);
+    static const int res_sca = resident_blocks_dyn(spec_phase1_kernel<false, true>, kNT, 0);
+    if (!attr_ok) return SEL_ECUDA;
+    const StreamPlan plan = plan_stream(rows1, V, sms, vec ? res_tma : res_sca, kUnitMin, kUnitMax);
+    if (static_cast<uint64_t>(rows1) * plan.chunks > 0x7fffffffull) return SEL_EUNSUPPORTED;
+    SpecArgs a{};
+    a.target = d_target;
+    a.draft = d_draft;
+    a.S = S; a.K = K; a.V = V;
+    a.T = temperature;
+    a.log2e_over_T = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+    a.cfg = StreamCfg{rows1 * plan.chunks, plan.chunks, plan.chunk_elems, V};
+    a.err = reinterpret_cast<uint32_t*>(ws);
+    a.row_ctr = reinterpret_cast<uint32_t*>(ws + l.row_ctr);
+    a.seq_ctr = reinterpret_cast<uint32_t*>(ws + l.seq_ctr_a);
+    a.row_parts = reinterpret_cast<RowPart*>(ws + l.row_parts);
+    a.row_stats = reinterpret_cast<RowPart*>(ws + l.row_stats);
+    a.decisions = reinterpret_cast<Decision*>(ws + l.decisions);
+    a.cmax = l.cmax_a;
+    a.decide = false;
+    if (vec) spec_phase1_kernel<true, true><<<plan.grid, kNT, kDyn, stream>>>(a);
+    else spec_phase1_kernel<false, true><<<plan.grid, kNT, 0, stream>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return SEL_ECUDA;
+
+    // the paired pass: chunks of at most kDrawChunkMax ids, about two blocks per SM
+    const uint64_t positions = static_cast<uint64_t>(S) * K;
+    uint32_t chunks = static_cast<uint32_t>((2ull * sms + positions - 1) / positions);
+    const uint32_t cmin = ceil_div(V, kDrawChunkMax);
+    if (chunks < cmin) chunks = cmin;
+    if (chunks > l.cmax_b) chunks = l.cmax_b;
+    const uint32_t ce = static_cast<uint32_t>(align_up(ceil_div(V, chunks), kGrain));
+    chunks = ceil_div(V, ce);
+    if (positions * chunks > 0x7fffffffull) return SEL_EUNSUPPORTED;
+    DiagArgs d{};
+    d.target = d_target;
+    d.draft = d_draft;
+    d.S = S; d.K = K; d.V = V;
+    d.log2e_over_T = a.log2e_over_T;
+    d.chunks = chunks;
+    d.chunk_elems = ce;
+    d.row_stats = a.row_stats;
+    d.pos_ctr = reinterpret_cast<uint32_t*>(ws + dl.pos_ctr);
+    d.parts = reinterpret_cast<DiagPart*>(ws + dl.parts);
+    d.cmax = l.cmax_b;
+    d.sum_min = d_sum_min;
+    d.sum_prod = d_sum_prod;
+    const dim3 grid2(static_cast<uint32_t>(positions * chunks));
+    if (vec) spec_diag_kernel<true><<<grid2, kNT, 0, stream>>>(d);
+    else spec_diag_kernel<false><<<grid2, kNT, 0, stream>>>(d);
     return cudaGetLastError() == cudaSuccess ? SEL_OK : SEL_ECUDA;
 }

@@ -852,3 +852,107 @@ extern "C" sel_status sel_sample_shards(const float* d_vals, const uint32_t* d_i
     merge_shards_kernel<true><<<rows, kNT, 0, stream>>>(sh, a);
     return cudaGetLastError() == cudaSuccess ? SEL_OK : SEL_ECUDA;
 }
+
+// ---------------------------------------------------------------------------
+// Sampler-match acceptance (mlxcel rules, "Sampler-match"): every verified
+// position draws from the target sampler (the sampling chain above, one
+// launch over all S * (K + 1) target rows); a warp per sequence then accepts
+// drafts while they equal the draws.
+// ---------------------------------------------------------------------------
+
+namespace sel {
+namespace {
+
+struct SamplerLayout {
+    size_t draws, probs, total;
+};
+
+SamplerLayout sampler_layout(uint32_t rows_t, uint32_t V, uint32_t k) {
+    SamplerLayout l{};
+    l.draws = align_up(topk_layout(rows_t, V, k).total, 256);
+    l.probs = l.draws + align_up(static_cast<size_t>(rows_t) * 4u, 256);
+    l.total = l.probs + align_up(static_cast<size_t>(rows_t) * 4u, 256);
+    return l;
+}
+
+__global__ void __launch_bounds__(kNT) sampler_decide_kernel(const uint32_t* draws, const uint32_t* tokens,
+                                                             uint32_t S, uint32_t K, uint32_t V,
+                                                             uint32_t* accepted, uint32_t* emitted) {
+    const uint32_t s = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (s >= S) return;  // whole warps
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t* d = draws + static_cast<size_t>(s) * (K + 1u);
+    const uint32_t* t = tokens + static_cast<size_t>(s) * K;
+    uint32_t* em = emitted + static_cast<size_t>(s) * (K + 1u);
+    // a failed draw (nonfinite row or bad uniform) or a draft token >= V
+    // fails the whole sequence closed
+    bool bad = false;
+    for (uint32_t j = lane; j <= K; j += 32u) bad |= d[j] == SEL_INVALID_ID;
+    for (uint32_t j = lane; j < K; j += 32u) bad |= t[j] >= V;
+    if (__any_sync(kFull, bad)) {
+        for (uint32_t j = lane; j <= K; j += 32u) em[j] = SEL_INVALID_ID;
+        if (lane == 0) accepted[s] = SEL_INVALID_ID;
+        return;
+    }
+    uint32_t n = K;
+    for (uint32_t j0 = 0; j0 < K; j0 += 32u) {
+        const uint32_t j = j0 + lane;
+        const uint32_t f = __ballot_sync(kFull, j < K && t[j] != d[j]);
+        if (f) {
+            n = j0 + static_cast<uint32_t>(__ffs(f) - 1);
+            break;
+        }
+    }
+    for (uint32_t j = lane; j <= K; j += 32u) em[j] = j < n ? t[j] : (j == n ? d[n] : SEL_INVALID_ID);
+    if (lane == 0) accepted[s] = n;
+}
+
+}  // namespace
+
+size_t spec_sampler_ws_bytes(uint32_t rows_t, uint32_t V, uint32_t top_k) {
+    uint32_t k = top_k == 0 ? 1u : top_k;
+    if (k > V) k = V;
+    if (rows_t == 0 || k > SEL_MAX_K) return 0;
+    return sampler_layout(rows_t, V, k).total;
+}
+
+}  // namespace sel
+
+extern "C" sel_status spec_accept_sampler(const float* d_target, const uint32_t* d_draft_tokens, uint32_t S,
+                                          uint32_t K, uint32_t V, const sel_sample_params* p, const float* d_u,
+                                          uint32_t* d_accepted, uint32_t* d_emitted, void* d_ws, size_t ws_bytes,
+                                          cudaStream_t stream) {
+    if (!p || V == 0 || V > SEL_MAX_V) return SEL_EINVAL;
+    const float T = p->temperature;
+    if (!(T >= 0.0f) || !(T < INFINITY)) return SEL_EINVAL;
+    if (!(p->top_p > 0.0f && p->top_p <= 1.0f)) return SEL_EINVAL;
+    if (!(p->min_p >= 0.0f && p->min_p < 1.0f)) return SEL_EINVAL;
+    if (p->order != SEL_ORDER_TEMP_FIRST && p->order != SEL_ORDER_TEMP_LAST) return SEL_EINVAL;
+    uint32_t k = p->top_k;
+    if (T == 0.0f) k = 1;
+    if (k == 0) return SEL_EUNSUPPORTED;
+    if (k > V) k = V;
+    if (k > SEL_MAX_K) return SEL_EUNSUPPORTED;
+    if (S == 0) return SEL_OK;
+    if (!d_target || !d_u || !d_accepted || !d_emitted || (K > 0 && !d_draft_tokens)) return SEL_EINVAL;
+    const uintptr_t mis = reinterpret_cast<uintptr_t>(d_target) | reinterpret_cast<uintptr_t>(d_u) |
+                          reinterpret_cast<uintptr_t>(d_accepted) | reinterpret_cast<uintptr_t>(d_emitted) |
+                          reinterpret_cast<uintptr_t>(d_draft_tokens);
+    if (mis % 4) return SEL_EINVAL;
+    const uint64_t rows_t = static_cast<uint64_t>(S) * (static_cast<uint64_t>(K) + 1u);
+    if (rows_t > 0x7fffffffull) return SEL_EUNSUPPORTED;
+    const SamplerLayout l = sampler_layout(static_cast<uint32_t>(rows_t), V, k);
+    if (!d_ws) return SEL_EINVAL;
+    if (reinterpret_cast<uintptr_t>(d_ws) % SEL_WS_ALIGN) return SEL_EINVAL;
+    if (ws_bytes < l.total) return SEL_EWORKSPACE;
+    char* ws = static_cast<char*>(d_ws);
+    uint32_t* draws = reinterpret_cast<uint32_t*>(ws + l.draws);
+    float* probs = reinterpret_cast<float*>(ws + l.probs);
+    SampleArgs sa{d_u, probs, T, p->top_p, p->min_p, p->order};
+    const sel_status st = launch_topk<true>(d_target, static_cast<uint32_t>(rows_t), V, k, nullptr, draws, d_ws,
+                                           l.draws, sa, stream);
+    if (st != SEL_OK) return st;
+    const dim3 grid((S + kWarps - 1) / kWarps);
+    sampler_decide_kernel<<<grid, kNT, 0, stream>>>(draws, d_draft_tokens, S, K, V, d_accepted, d_emitted);
+    return cudaGetLastError() == cudaSuccess ? SEL_OK : SEL_ECUDA;
+}

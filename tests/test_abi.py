@@ -146,3 +146,24 @@ def test_eog_validation_needs_no_gpu(lib):
     assert f(fake, 1, 0, fake, 3, fake, fake, 4096, None) == B.SEL_EINVAL      # V = 0
     assert f(None, 0, 10, fake, 3, None, None, 0, None) == B.SEL_OK            # rows = 0
     assert f(fake, 3, 300_000, fake, 3, fake, fake, 16, None) == B.SEL_EWORKSPACE
+
+
+def test_spec_rules_validation_needs_no_gpu(lib):
+    from sampling_row_fp32_gb300 import binding as B
+    vp = ctypes.c_void_p
+    fake = vp(0x10000)
+    p = B.SampleParams(1.0, 10, 0.9, 0.0, 0)
+    f = lib.spec_accept_sampler
+    assert f(fake, fake, 0, 3, 100, ctypes.byref(p), fake, fake, fake, fake, 4096, None) == B.SEL_OK  # S = 0
+    assert f(fake, fake, 2, 3, 100, None, fake, fake, fake, fake, 4096, None) == B.SEL_EINVAL
+    assert f(fake, fake, 2, 3, 100, ctypes.byref(B.SampleParams(1.0, 0, 0.9, 0.0, 0)), fake, fake, fake,
+             fake, 4096, None) == B.SEL_EUNSUPPORTED                                          # top_k = 0
+    assert f(fake, fake, 2, 3, 100, ctypes.byref(p), None, fake, fake, fake, 4096, None) == B.SEL_EINVAL
+    assert f(fake, fake, 2, 3, 300_000, ctypes.byref(p), fake, fake, fake, fake, 16, None) == B.SEL_EWORKSPACE
+    g = lib.spec_diagnostics
+    assert g(fake, fake, 2, 3, 100, ctypes.c_float(0.0), fake, fake, fake, 4096, None) == B.SEL_EINVAL  # T = 0
+    assert g(fake, fake, 2, 0, 100, ctypes.c_float(1.0), fake, fake, fake, 4096, None) == B.SEL_OK      # K = 0
+    assert g(fake, None, 2, 3, 100, ctypes.c_float(1.0), fake, fake, fake, 4096, None) == B.SEL_EINVAL
+    assert g(fake, fake, 2, 3, 300_000, ctypes.c_float(1.0), fake, fake, fake, 16, None) == B.SEL_EWORKSPACE
+    assert B.sel_workspace_bytes(B.SEL_OP_SPEC_DIAG, 8, 151_936, 8) > B.sel_workspace_bytes(B.SEL_OP_SPEC, 8, 151_936, 8)
+    assert B.sel_workspace_bytes(B.SEL_OP_SPEC_SAMPLER, 72, 151_936, 40) > B.sel_workspace_bytes(B.SEL_OP_SAMPLE, 72, 151_936, 40)
