@@ -67,6 +67,10 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.orc_argmax.restype = None
     lib.orc_argmax_excluding.argtypes = [_f32p, _u32, _u32, _u32p, _u32, _u32p]
     lib.orc_argmax_excluding.restype = None
+    lib.orc_sample_ex.argtypes = [_f32p, _u32, _u32, ctypes.c_double, _u32, ctypes.c_double,
+                                  ctypes.c_double, ctypes.c_int, ctypes.c_double, ctypes.c_double,
+                                  _f32p, _u32p, _f64p, _f64p]
+    lib.orc_sample_ex.restype = ctypes.c_int
     lib.orc_spec_sampler.argtypes = [_f32p, _u32p, _u32, _u32, _u32, ctypes.c_double, _u32,
                                      ctypes.c_double, ctypes.c_double, ctypes.c_int, _f32p,
                                      _u32p, _u32p, _f64p]
@@ -184,18 +188,19 @@ class Oracle:
         return vals, ids
 
     def sample(self, logits, uniforms, temperature: float, top_k: int,
-               top_p: float, min_p: float, temp_last: bool = False) -> SampleResult:
+               top_p: float, min_p: float, temp_last: bool = False,
+               top_n_sigma: float = 0.0, typical_p: float = 1.0) -> SampleResult:
         x = _f32(logits)
         rows, V = x.shape
         u = _f32(uniforms).reshape(rows)
         ids = np.empty(rows, dtype=np.uint32)
         probs = np.empty(rows, dtype=np.float64)
         margin = np.empty(rows, dtype=np.float64)
-        self.lib.orc_sample(_ptr(x, _f32p), rows, V, float(temperature),
-                            int(top_k), float(top_p), float(min_p),
-                            int(bool(temp_last)), _ptr(u, _f32p),
-                            _ptr(ids, _u32p), _ptr(probs, _f64p),
-                            _ptr(margin, _f64p))
+        self.lib.orc_sample_ex(_ptr(x, _f32p), rows, V, float(temperature),
+                               int(top_k), float(top_p), float(min_p),
+                               int(bool(temp_last)), float(top_n_sigma), float(typical_p),
+                               _ptr(u, _f32p), _ptr(ids, _u32p), _ptr(probs, _f64p),
+                               _ptr(margin, _f64p))
         return SampleResult(ids, probs, margin)
 
     def spec_accept(self, target, draft, draft_tokens, temperature: float,

@@ -291,22 +291,32 @@ void orc_topk(const float *logits, uint32_t rows, uint32_t V, uint32_t k,
 /* ----------------------------------------------------------------------- */
 
 /*
- * One row of filtered sampling. Steps, in order:
+ * One row of filtered sampling. Steps, in order (the chain of [Ch21] 21.7:
+ * top_n_sigma, top-k, typical_p, top-p; then min-p):
  *  1. z_i = x_i / T                     (T == 0: greedy, prob 1)
- *  2. candidates C: the top_k ids of z by the top-k definition above
- *     (top_k == 0: all V ids), in (z desc, id asc) order
+ *  2. top_n_sigma > 0: only ids with x_i >= max(x) - top_n_sigma * sigma
+ *     remain, sigma the population standard deviation of the row's logits
+ *     (a mask against the max; it does not depend on T)
+ *     candidates C: the top_k of the remaining ids by the top-k definition
+ *     above (top_k == 0: all of them), in (z desc, id asc) order
  *  3. w_i = exp(z_i - z_max), P_i = w_i / sum_C w       (softmax over C)
+ *  3b. 0 < typical_p < 1 (locally typical sampling): H = -sum_C P ln P,
+ *     score_i = |-ln P_i - H|; in (score asc, then C's order) keep the
+ *     shortest prefix with cumulative P >= typical_p (at least one); the
+ *     kept ids stay in C's order and P is renormalised over them
  *  4. top_p < 1: keep the shortest prefix of C with cumulative P >= top_p
  *  5. min_p > 0: keep survivors with P_i >= min_p * P_max
  *  6. Q_i = w_i / sum_survivors w ; draw by inverse CDF in the same order
  * temp_last != 0: steps 3-5 use T = 1 probabilities (filter on the
  * untempered distribution) and step 6 uses the tempered weights.
  * *margin = distance of the nearest decision to its threshold: |u - C_i|,
- * |cum_i - top_p| and |P_i / P_max - min_p|.
+ * |cum_i - top_p|, |P_i / P_max - min_p|, |cum - typical_p| and the score gap
+ * at the typical cut, and |x - (max - n sigma)| / max(|max - n sigma|, 1).
  */
 static uint32_t sample_row(const float *x, uint32_t V, double T,
                            uint32_t top_k, double top_p, double min_p,
-                           int temp_last, float u_f, double *prob,
+                           int temp_last, double top_n_sigma,
+                           double typical_p, float u_f, double *prob,
                            double *margin)
 {
     *margin = INFINITY;
@@ -327,6 +337,36 @@ static uint32_t sample_row(const float *x, uint32_t V, double T,
     uint32_t *order = sorted_ids_desc(z, V);
     uint32_t nc = (top_k == 0 || top_k > V) ? V : top_k;
 
+    /* 2. top-n-sigma: the ids at or above max - n sigma are a prefix of the
+     *    order (z = x / T orders like x) */
+    if (top_n_sigma > 0.0) {
+        double mean = 0.0;
+        for (uint32_t i = 0; i < V; ++i)
+            mean += (double)x[i];
+        mean /= (double)V;
+        double var = 0.0;
+        for (uint32_t i = 0; i < V; ++i)
+            var += ((double)x[i] - mean) * ((double)x[i] - mean);
+        double sigma = sqrt(var / (double)V);
+        double thr = (double)x[order[0]] - top_n_sigma * sigma;
+        double scale = fabs(thr) > 1.0 ? fabs(thr) : 1.0;
+        uint32_t m = 0;
+        while (m < V && (double)x[order[m]] >= thr)
+            ++m;
+        if (m > 0) {
+            double d = fabs((double)x[order[m - 1]] - thr) / scale;
+            if (d < *margin)
+                *margin = d;
+        }
+        if (m < V) {
+            double d = fabs((double)x[order[m]] - thr) / scale;
+            if (d < *margin)
+                *margin = d;
+        }
+        if (m < nc)
+            nc = m;
+    }
+
     /* 3. softmax over the candidates (filter distribution and draw weights) */
     double Tf = temp_last ? 1.0 : T;
     double *wf = (double *)malloc((size_t)nc * sizeof(double)); /* filter */
@@ -337,6 +377,62 @@ static uint32_t sample_row(const float *x, uint32_t V, double T,
         wf[j] = exp((double)x[order[j]] / Tf - zmax_f);
         wd[j] = exp(z[order[j]] - zmax_d);
         Sf += wf[j];
+    }
+
+    /* 3b. locally typical: keep the most typical ids up to typical_p mass */
+    if (typical_p > 0.0 && typical_p < 1.0 && nc > 1) {
+        double H = 0.0;
+        for (uint32_t j = 0; j < nc; ++j) {
+            double P = wf[j] / Sf;
+            if (P > 0.0)
+                H -= P * log(P);
+        }
+        double *score = (double *)malloc((size_t)nc * sizeof(double));
+        for (uint32_t j = 0; j < nc; ++j) {
+            double P = wf[j] / Sf;
+            score[j] = P > 0.0 ? fabs(-log(P) - H) : INFINITY;
+        }
+        /* (score asc, position asc): a stable sort of the positions by -score */
+        double *neg = (double *)malloc((size_t)nc * sizeof(double));
+        for (uint32_t j = 0; j < nc; ++j)
+            neg[j] = -score[j];
+        uint32_t *tord = sorted_ids_desc(neg, nc);
+        char *keep = (char *)calloc(nc, 1);
+        double cum = 0.0;
+        for (uint32_t t = 0; t < nc; ++t) {
+            uint32_t j = tord[t];
+            keep[j] = 1;
+            cum += wf[j] / Sf;
+            double d = fabs(cum - typical_p);
+            if (d < *margin)
+                *margin = d;
+            if (cum >= typical_p) {
+                if (t + 1 < nc) {
+                    double g = fabs(score[tord[t + 1]] - score[j]);
+                    double sc = score[j] > 1.0 ? score[j] : 1.0;
+                    if (g / sc < *margin)
+                        *margin = g / sc;
+                }
+                break;
+            }
+        }
+        uint32_t n2 = 0;
+        double S2 = 0.0;
+        for (uint32_t j = 0; j < nc; ++j) {
+            if (!keep[j])
+                continue;
+            order[n2] = order[j];
+            wf[n2] = wf[j];
+            wd[n2] = wd[j];
+            S2 += wf[n2];
+            ++n2;
+        }
+        nc = n2;
+        Sf = S2;
+        free(keep);
+        free(tord);
+        free(neg);
+        free(score);
     }
 
     /* 4. top-p: shortest prefix with cumulative mass >= top_p */
@@ -388,20 +484,31 @@ static uint32_t sample_row(const float *x, uint32_t V, double T,
     return id;
 }
 
+int orc_sample_ex(const float *logits, uint32_t rows, uint32_t V,
+                  double temperature, uint32_t top_k, double top_p,
+                  double min_p, int temp_last, double top_n_sigma,
+                  double typical_p, const float *uniforms, uint32_t *out_ids,
+                  double *out_probs, double *out_margin)
+{
+    for (uint32_t r = 0; r < rows; ++r) {
+        double m;
+        out_ids[r] = sample_row(logits + (size_t)r * V, V, temperature,
+                                top_k, top_p, min_p, temp_last, top_n_sigma,
+                                typical_p, uniforms[r], &out_probs[r], &m);
+        if (out_margin)
+            out_margin[r] = m;
+    }
+    return 0;
+}
+
 int orc_sample(const float *logits, uint32_t rows, uint32_t V,
                double temperature, uint32_t top_k, double top_p,
                double min_p, int temp_last, const float *uniforms,
                uint32_t *out_ids, double *out_probs, double *out_margin)
 {
-    for (uint32_t r = 0; r < rows; ++r) {
-        double m;
-        out_ids[r] = sample_row(logits + (size_t)r * V, V, temperature,
-                                top_k, top_p, min_p, temp_last, uniforms[r],
-                                &out_probs[r], &m);
-        if (out_margin)
-            out_margin[r] = m;
-    }
-    return 0;
+    return orc_sample_ex(logits, rows, V, temperature, top_k, top_p, min_p,
+                         temp_last, 0.0, 1.0, uniforms, out_ids, out_probs,
+                         out_margin);
 }
 
 /* ----------------------------------------------------------------------- */
@@ -572,7 +679,7 @@ static void spec_sampler_sequence(const float *target, const uint32_t *tokens,
     for (;;) {
         double prob, m;
         drawn = sample_row(target + (size_t)n * V, V, T, top_k, top_p, min_p,
-                           temp_last, u[n], &prob, &m);
+                           temp_last, 0.0, 1.0, u[n], &prob, &m);
         if (m < *margin)
             *margin = m;
         if (n == K || tokens[n] != drawn)

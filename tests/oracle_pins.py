@@ -444,6 +444,48 @@ def pin_spec_invalid(orc):
     assert r.accepted[2] == INVALID and np.all(r.emitted[2] == INVALID)
 
 
+def pin_filters_closed_forms(orc):
+    """Ch 21, 21.7 (top_n_sigma, typical_p in the chain): survivors and draw
+    probabilities from golden sample_filters_closed_forms.json. A grid of u
+    over [0, 1) must map onto exactly the kept ids with frequencies Q, and
+    each draw reports its Q."""
+    n = 20000
+    u = ((np.arange(n) + 0.5) / n).astype(np.float32)
+    for c in golden("sample_filters_closed_forms.json")["cases"]:
+        x = np.tile(np.asarray(c["logits"], dtype=np.float32), (n, 1))
+        r = orc.sample(x, u, 1.0, 0, c["top_p"], 0.0, top_n_sigma=c["top_n_sigma"], typical_p=c["typical_p"])
+        kept, Q = c["kept"], np.asarray(c["Q"])
+        assert set(np.unique(r.ids).tolist()) <= set(kept), (c["name"], np.unique(r.ids))
+        freq = np.array([np.mean(r.ids == i) for i in kept])
+        assert np.allclose(freq, Q, atol=2e-4), (c["name"], freq, Q)
+        for i, q in zip(kept, Q):
+            got = r.probs[r.ids == i]
+            assert got.size and np.allclose(got, q, rtol=1e-9), (c["name"], i)
+
+
+def pin_filters_reduce(orc):
+    """top_n_sigma <= 0 and typical_p >= 1 change nothing; the sigma mask is
+    the same at every temperature (it compares logits against the max) and
+    keeps the ids numpy's population std (an independent library routine)
+    puts at or above max - n sigma."""
+    rng = np.random.default_rng(41)
+    x = rng.normal(0, 2, size=(24, 400)).astype(np.float32)
+    u = rng.random(24, dtype=np.float32)
+    base = orc.sample(x, u, 0.8, 50, 0.9, 0.02)
+    for a, b in ((0.0, 1.0), (-1.0, 1.0), (0.0, 1.5)):
+        r = orc.sample(x, u, 0.8, 50, 0.9, 0.02, top_n_sigma=a, typical_p=b)
+        assert np.array_equal(r.ids, base.ids) and np.allclose(r.probs, base.probs, rtol=1e-12)
+    n = 1.5
+    xd = x.astype(np.float64)
+    thr = xd.max(axis=1) - n * xd.std(axis=1)
+    uu = ((np.arange(400) + 0.5) / 400).astype(np.float32)
+    for T in (0.5, 2.0):
+        for rr in range(4):
+            r = orc.sample(np.tile(x[rr], (400, 1)), uu, T, 0, 1.0, 0.0, top_n_sigma=n)
+            assert np.all(x[rr][r.ids] >= thr[rr]), (T, rr)
+            assert np.any(x[rr][r.ids] == x[rr].max())
+
+
 # ---------------------------------------------------------------------------
 # sampler-match acceptance and the closed-form diagnostics
 # ---------------------------------------------------------------------------
@@ -595,7 +637,7 @@ ALL_PINS = [
     pin_eog_bruteforce, pin_eog_reduces_to_argmax, pin_eog_nonfinite,
     pin_topk_bruteforce, pin_topk_lexsort, pin_topk_special,
     pin_sample_closed_forms, pin_sample_cdf_grid, pin_sample_support,
-    pin_sample_invalid,
+    pin_sample_invalid, pin_filters_closed_forms, pin_filters_reduce,
     pin_spec_closed_forms, pin_spec_ceiling_example, pin_spec_acceptance_law,
     pin_spec_stream_is_target, pin_spec_support, pin_spec_regimes,
     pin_spec_greedy, pin_spec_invalid,

@@ -83,6 +83,16 @@ MUTANTS = [
     ("diagnostics ignore the temperature",
      [("            softmax_row(t, V, T, p);\n            softmax_row(d, V, T, q);",
        "            softmax_row(t, V, 1.0, p);\n            softmax_row(d, V, 1.0, q);")]),
+    ("top-n-sigma uses the variance",
+     [("double sigma = sqrt(var / (double)V);", "double sigma = var / (double)V;")]),
+    ("top-n-sigma measured from the mean",
+     [("double thr = (double)x[order[0]] - top_n_sigma * sigma;", "double thr = mean - top_n_sigma * sigma;")]),
+    ("typical order reversed",
+     [("neg[j] = -score[j];", "neg[j] = score[j];")]),
+    ("typical keeps past the crossing",
+     [("if (cum >= typical_p) {", "if (cum > typical_p + 0.2) {")]),
+    ("typical set not renormalised",
+     [("        Sf = S2;\n", "        Sf = Sf;\n")]),
     ("EOG all-excluded row answers id 0",
      [("    return best;\n}\n\nvoid orc_argmax_excluding(",
        "    return best == ORC_INVALID ? 0 : best;\n}\n\nvoid orc_argmax_excluding(")]),
