@@ -180,7 +180,9 @@ def gpu_arm(args, rank, world, local_rank):
         else:
             B.spec_accept(target_view(copy_for(step, 4)), None, tok, arg, None, None, acc2, emi2, ws_g)
 
-    launches_per_step = 6  # spec rejection is two kernels
+    # argmax, top-k, sample and the argmax rule: a main launch and a finishing
+    # launch each; the rejection rule: phase 1, its finishing launch, the draw
+    launches_per_step = 11
     bytes_per_op = [ROWS * ROW_BYTES, ROWS * ROW_BYTES, ROWS * ROW_BYTES,
                     None, ROWS * ROW_BYTES]
 

@@ -300,9 +300,9 @@ sel_status spec_diagnostics(const float *d_target, const float *d_draft,
  *
  *   d_logits, rows, V, d_out_ids  as for sel_argmax
  * Requests whose workspace would not fit (sel_workspace_bytes(SEL_OP_ARGMAX,
- * rows, V, 0) > SEL_NOALLOC_SCRATCH_BYTES, e.g. more than 538 rows at
- * V = 248,320) return SEL_EWORKSPACE. The call allocates and frees nothing;
- * it zeroes the array's counters with cudaMemsetAsync on `stream` and
+ * rows, V, 0) > SEL_NOALLOC_SCRATCH_BYTES: more than 131,040 rows, at any
+ * V) return SEL_EWORKSPACE. The call allocates and frees nothing;
+ * it zeroes the part of the array it uses with cudaMemsetAsync on `stream` and
  * launches on `stream`. The first call on a device looks the array's device
  * address up (cudaGetSymbolAddress), so make that first call before any
  * stream capture. Every call on a device shares the one array: calls that

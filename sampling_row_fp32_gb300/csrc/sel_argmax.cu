@@ -9,46 +9,40 @@
 // Design (sm_103a). The page's Metal version is a two-dispatch tree: one
 // 1,024-thread threadgroup per 1,024-element chunk writes a partial, an
 // explicit barrier orders the hazard, and a second dispatch reduces the
-// partials. Here one launch does both. Persistent blocks stream contiguous
-// runs of 32 KB row chunks through a TMA bulk-copy ring (sel_stream.cuh) and
-// keep a running (value, index) per thread across the chunks of a row; when
-// a block leaves a row it merges across the warp with shuffles and across
-// warps through shared memory and publishes one partial for its segment of
-// the row; the block that publishes a row's last segment merges that row's
-// partials with one warp and writes the id. (value desc, id asc) is a total
-// order, so the merge order cannot change the result.
+// partials. Here one block per row chunk of up to 16 KB loads its chunk with
+// 128-bit loads straight into registers (all in flight at once), keeps four
+// independent (value, index) chains per thread, and merges across the warp
+// with shuffles and across warps through shared memory (sel_units.cuh). The
+// cross-block combine needs no barrier and no partials: (value desc, id asc)
+// is a total order that one 64-bit key carries -- the order-preserving key of
+// the value above the complement of the id -- so each block folds its winner
+// into the row's slot with one atomic max, which no block waits for. A
+// one-block finishing launch (programmatic dependent launch, so it is
+// resident before the main launch ends) turns each slot into the id and
+// clears it for the next call. A nonfinite logit sets the slot to the
+// all-ones key, which outranks every value and reads as "fail closed".
 #include <cfloat>
 
 #include "sel_plan.h"
-#include "sel_stream.cuh"
+#include "sel_units.cuh"
 
 namespace sel {
 namespace {
 
-#ifndef SEL_ARGMAX_NT
-#define SEL_ARGMAX_NT 256
-#endif
-#ifndef SEL_ARGMAX_VPT
-#define SEL_ARGMAX_VPT 4
-#endif
-#ifndef SEL_ARGMAX_STAGES
-#define SEL_ARGMAX_STAGES 4
-#endif
-#ifndef SEL_ARGMAX_MINB
-#define SEL_ARGMAX_MINB 3
-#endif
-constexpr int kNT = SEL_ARGMAX_NT;              // threads per block
-constexpr int kVPT = SEL_ARGMAX_VPT;            // float4 per thread per unit
-constexpr int kStages = SEL_ARGMAX_STAGES;      // units in flight per block
+constexpr int kNT = 256;                        // threads per block
+constexpr int kVPT = 4;                         // float4 per thread
+constexpr uint32_t kGrain = 4u * kNT;           // unit sizes are multiples of this
 constexpr uint32_t kUnitMax = 4u * kNT * kVPT;  // elements per unit (16 KB)
-constexpr uint32_t kUnitMin = 1024u;
 constexpr uint32_t kNoIdx = 0x7fffffffu;        // "no element": loses every tie
 constexpr uint32_t kNonfiniteBit = 0x80000000u;
 
-struct alignas(8) ArgPair {
-    float v;
-    uint32_t i;  // id; bit 31 = a nonfinite logit was seen
-};
+constexpr unsigned long long kSlotNonfinite = ~0ull;  // the row saw +-Inf or NaN
+
+// (value desc, id asc) as one integer: a larger key is a larger value, or the
+// same value at a lower id. 0 means "no candidate" (below every real key).
+__device__ __forceinline__ unsigned long long arg_key(float v, uint32_t i) {
+    return (static_cast<unsigned long long>(f2key(v)) << 32) | static_cast<uint32_t>(~i);
+}
 
 __device__ __forceinline__ bool beats(float v, uint32_t i, float w, uint32_t j) {
     return v > w || (v == w && i < j);
@@ -66,176 +60,139 @@ __device__ __forceinline__ void warp_argmax(float& v, uint32_t& i, uint32_t& nf)
 
 struct ArgmaxArgs {
     const float* logits;
-    uint32_t* out_ids;
-    uint32_t* counters;  // [rows]
-    ArgPair* partials;   // [rows][stride]
-    uint32_t stride;
-    uint32_t* err;
-    StreamCfg cfg;
+    unsigned long long* slots;  // [rows]: the row's best key so far (0 between calls)
+    uint32_t V, chunks, chunk_elems;
     const uint32_t* excluded;  // EOG ids masked out of every row (greedy serving variant)
     uint32_t n_excluded;       // <= SEL_MAX_EXCLUDED
 };
 
-template <bool kTma, bool kExclude>
-__global__ void __launch_bounds__(kNT, SEL_ARGMAX_MINB) argmax_kernel(ArgmaxArgs a) {
-    extern __shared__ float4 stages[];
-    __shared__ uint64_t full[kStages];
+template <bool kVec, bool kExclude>
+__global__ void __launch_bounds__(kNT) argmax_kernel(ArgmaxArgs a) {
     __shared__ float s_v[kNT / 32];
     __shared__ uint32_t s_i[kNT / 32];
     __shared__ uint32_t s_nf[kNT / 32];
-    // excluded offsets inside the current unit, in three buffers by unit
-    // number (see accum)
-    __shared__ uint32_t s_ex_count[3];
-    __shared__ uint32_t s_ex_off[kExclude ? 3 : 1][kExclude ? SEL_MAX_EXCLUDED : 1];
+    __shared__ uint32_t s_ex_count;
+    __shared__ uint32_t s_ex_off[kExclude ? SEL_MAX_EXCLUDED : 1];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint32_t V = a.cfg.V;
-    auto row_ptr = [&](uint32_t r) { return a.logits + static_cast<size_t>(r) * V; };
-
-    // Four independent (value, quad start) chains per thread, one per lane of
-    // the float4, so the compare-select chains overlap; the id is quad start
-    // + lane. Padding is -FLT_MAX at an id past every real one, so it never
-    // wins: a real -FLT_MAX ties it and keeps its lower id, and -inf or NaN
-    // fail the row closed anyway. nfacc = sum of x * 0 stays 0 unless some x
-    // is +-Inf or NaN.
-    float best[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-    uint32_t bbase[4] = {kNoIdx, kNoIdx, kNoIdx, kNoIdx};
-    float nfacc = 0.0f;
-
-    // EOG exclusion (greedy serving variant): each thread holds one excluded
-    // id (SEL_MAX_EXCLUDED == kNT). Per unit, the ids that fall inside it are
-    // posted as unit offsets; after one barrier every thread masks its own
-    // elements to -inf. The latch has already seen the raw values, so a
-    // nonfinite excluded logit still fails the row. Unit u posts into buffer
-    // u % 3 and thread 0 clears buffer (u + 1) % 3 before u's barrier: that
-    // buffer was last read in unit u - 2, which every thread left before
-    // passing unit u - 1's barrier, and is next filled in unit u + 1, after
-    // unit u's barrier.
-    static_assert(!kExclude || SEL_MAX_EXCLUDED == kNT, "one excluded id per thread");
+    const uint32_t V = a.V;
+    pdl_wait();
+    const BlockUnit t = block_unit(a.chunks, a.chunk_elems, V);
+    // Padding is -FLT_MAX at an id past every real one, so it never wins: a
+    // real -FLT_MAX ties it and keeps its lower id, and -inf or NaN fail the
+    // row closed anyway.
+    float4 q[kVPT];
+    load_unit<kNT, kVPT, kVec>(a.logits + static_cast<size_t>(t.row) * V, t.lo, t.hi, -FLT_MAX, q);
     uint32_t my_ex = 0xFFFFFFFFu;
-    uint32_t unit_no = 0;
     if (kExclude) {
+        if (tid == 0) s_ex_count = 0;
         if (static_cast<uint32_t>(tid) < a.n_excluded) my_ex = a.excluded[tid];
-        if (tid < 3) s_ex_count[tid] = 0;
+    }
+    pdl_trigger();
+
+    // nonfinite latch: sum of x * 0 stays 0 unless some x is +-Inf or NaN
+    float2 nfacc = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int s = 0; s < kVPT; ++s) latch_nonfinite(nfacc, q[s]);
+
+    if (kExclude) {
+        // EOG exclusion (greedy serving variant): each thread holds one
+        // excluded id (SEL_MAX_EXCLUDED == kNT); the ids inside this unit are
+        // posted as offsets, and after one barrier the thread owning each
+        // masks it to -inf. The latch has already seen the raw values, so a
+        // nonfinite excluded logit still fails the row.
+        static_assert(!kExclude || SEL_MAX_EXCLUDED == kNT, "one excluded id per thread");
         __syncthreads();
+        const uint32_t off = my_ex - t.lo;
+        if (my_ex != 0xFFFFFFFFu && off < t.hi - t.lo) s_ex_off[atomicAdd(&s_ex_count, 1u)] = off;
+        __syncthreads();
+        const uint32_t n = s_ex_count;
+        for (uint32_t i = 0; i < n; ++i) {
+            const uint32_t o = s_ex_off[i];
+            const uint32_t quad = o >> 2;
+            if (quad % kNT == static_cast<uint32_t>(tid)) {
+                const uint32_t sl = quad / kNT, j = o & 3u;
+#pragma unroll
+                for (int s = 0; s < kVPT; ++s) {
+                    if (static_cast<uint32_t>(s) == sl) {
+                        if (j == 0) q[s].x = -INFINITY;
+                        if (j == 1) q[s].y = -INFINITY;
+                        if (j == 2) q[s].z = -INFINITY;
+                        if (j == 3) q[s].w = -INFINITY;
+                    }
+                }
+            }
+        }
     }
 
-    auto accum = [&](const Unit& t, float4 (&q)[kVPT]) {
-        if (kExclude) {
+    // Four independent (value, quad start) chains, one per lane of the
+    // float4, so the compare-select chains overlap; ids rise along each
+    // chain, so '>' keeps the lowest. The id is quad start + lane.
+    float best[4] = {q[0].x, q[0].y, q[0].z, q[0].w};
+    uint32_t bbase[4];
+    {
+        const uint32_t e0 = t.lo + 4u * tid;
 #pragma unroll
-            for (int s = 0; s < kVPT; ++s) {
-                nfacc = __fmaf_rn(q[s].x, 0.0f, nfacc);
-                nfacc = __fmaf_rn(q[s].y, 0.0f, nfacc);
-                nfacc = __fmaf_rn(q[s].z, 0.0f, nfacc);
-                nfacc = __fmaf_rn(q[s].w, 0.0f, nfacc);
-            }
-            const uint32_t p = unit_no;
-            unit_no = unit_no == 2u ? 0u : unit_no + 1u;
-            if (tid == 0) s_ex_count[unit_no] = 0;  // next unit's buffer
-            const uint32_t off = my_ex - t.lo;
-            if (my_ex != 0xFFFFFFFFu && off < t.hi - t.lo) s_ex_off[p][atomicAdd(&s_ex_count[p], 1u)] = off;
-            __syncthreads();
-            const uint32_t n = s_ex_count[p];
-            for (uint32_t i = 0; i < n; ++i) {
-                const uint32_t o = s_ex_off[p][i];
-                const uint32_t quad = o >> 2;
-                if (quad % kNT == static_cast<uint32_t>(tid)) {
-                    const uint32_t sl = quad / kNT, j = o & 3u;
+        for (int j = 0; j < 4; ++j) bbase[j] = e0;
+    }
 #pragma unroll
-                    for (int s = 0; s < kVPT; ++s) {
-                        if (static_cast<uint32_t>(s) == sl) {
-                            if (j == 0) q[s].x = -INFINITY;
-                            if (j == 1) q[s].y = -INFINITY;
-                            if (j == 2) q[s].z = -INFINITY;
-                            if (j == 3) q[s].w = -INFINITY;
-                        }
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int s = 0; s < kVPT; ++s) {
-            const uint32_t e = t.lo + 4u * (tid + kNT * s);
-            const float f[4] = {q[s].x, q[s].y, q[s].z, q[s].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (!kExclude) nfacc = __fmaf_rn(f[j], 0.0f, nfacc);
-                if (f[j] > best[j]) {  // ids rise along each chain: '>' keeps the lowest
-                    best[j] = f[j];
-                    bbase[j] = e;
-                }
-            }
-        }
-    };
-
-    auto flush = [&](const Segment& g) {
-        uint32_t nf = (nfacc == 0.0f) ? 0u : kNonfiniteBit;
-        float v = -INFINITY;
-        uint32_t i = kNoIdx;
+    for (int s = 1; s < kVPT; ++s) {
+        const uint32_t e = t.lo + 4u * (tid + kNT * s);
+        const float f[4] = {q[s].x, q[s].y, q[s].z, q[s].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const uint32_t id = bbase[j] == kNoIdx ? kNoIdx : bbase[j] + j;
-            if (beats(best[j], id, v, i)) { v = best[j]; i = id; }
-            best[j] = -INFINITY;
-            bbase[j] = kNoIdx;
-        }
-        nfacc = 0.0f;
-        if (nf) { v = -INFINITY; i = kNoIdx; }
-        warp_argmax(v, i, nf);
-        if (lane == 0) { s_v[warp] = v; s_i[warp] = i; s_nf[warp] = nf; }
-        __syncthreads();
-        if (warp == 0) {
-            v = lane < kNT / 32 ? s_v[lane] : -INFINITY;
-            i = lane < kNT / 32 ? s_i[lane] : kNoIdx;
-            nf = lane < kNT / 32 ? s_nf[lane] : 0u;
-            warp_argmax(v, i, nf);
-            bool last = true;
-            if (g.count > 1) {
-                uint32_t flag = 0;
-                if (lane == 0) {
-                    a.partials[static_cast<size_t>(g.row) * a.stride + g.index] = ArgPair{v, i | nf};
-                    flag = segment_arrive(&a.counters[g.row], g.count) ? 1u : 0u;
-                }
-                last = __shfl_sync(kFull, flag, 0) != 0;
-                if (last) {
-                    // merge the row's segments (any order gives the same answer)
-                    __threadfence();
-                    v = -INFINITY;
-                    i = kNoIdx;
-                    nf = 0;
-                    const ArgPair* part = a.partials + static_cast<size_t>(g.row) * a.stride;
-                    for (uint32_t c = lane; c < g.count; c += 32) {
-                        const uint64_t raw = ld_gpu_u64(part + c);
-                        const float pv = __uint_as_float(static_cast<uint32_t>(raw));
-                        const uint32_t hi = static_cast<uint32_t>(raw >> 32);
-                        const uint32_t pi = hi & ~kNonfiniteBit;
-                        nf |= hi & kNonfiniteBit;
-                        if (beats(pv, pi, v, i)) { v = pv; i = pi; }
-                    }
-                    warp_argmax(v, i, nf);
-                }
+            if (f[j] > best[j]) {
+                best[j] = f[j];
+                bbase[j] = e;
             }
-            // i >= V: no real id won (every id of the row excluded, and the
-            // -FLT_MAX padding past the row end beat the masked -inf values)
-            if (last && lane == 0) a.out_ids[g.row] = (nf || i >= a.cfg.V) ? SEL_INVALID_ID : i;
         }
-        __syncthreads();
-    };
+    }
+    uint32_t nf = (nfacc.x + nfacc.y == 0.0f) ? 0u : kNonfiniteBit;
+    float v = -INFINITY;
+    uint32_t i = kNoIdx;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t id = bbase[j] + j;
+        // ids at or past hi are padding, whatever their value
+        if (id < t.hi && beats(best[j], id, v, i)) { v = best[j]; i = id; }
+    }
+    // -inf never wins: a real -inf fails the row closed, and an excluded id
+    // is no candidate (a row whose ids are all excluded has no answer)
+    if (nf || !(v > -INFINITY)) { v = -INFINITY; i = kNoIdx; }
+    warp_argmax(v, i, nf);
+    if (lane == 0) { s_v[warp] = v; s_i[warp] = i; s_nf[warp] = nf; }
+    __syncthreads();
+    if (warp != 0) return;
+    v = lane < kNT / 32 ? s_v[lane] : -INFINITY;
+    i = lane < kNT / 32 ? s_i[lane] : kNoIdx;
+    nf = lane < kNT / 32 ? s_nf[lane] : 0u;
+    warp_argmax(v, i, nf);
+    if (lane == 0 && (nf || i != kNoIdx))
+        atomicMax(&a.slots[t.row], nf ? kSlotNonfinite : arg_key(v, i));
+}
 
-    stream_segments<kTma, kNT, kVPT, kStages>(a.cfg, row_ptr, accum, flush, stages, full, a.err, -FLT_MAX);
+// Turn each row's slot into its id and clear the slot for the next call.
+__global__ void __launch_bounds__(kNT) argmax_finish_kernel(unsigned long long* slots, uint32_t* out_ids,
+                                                            uint32_t rows) {
+    pdl_wait();
+    pdl_trigger();
+    const uint32_t r = blockIdx.x * kNT + threadIdx.x;
+    if (r >= rows) return;
+    const unsigned long long key = slots[r];
+    slots[r] = 0ull;
+    // 0: every id excluded; all ones: a nonfinite logit
+    out_ids[r] = (key == 0ull || key == kSlotNonfinite) ? SEL_INVALID_ID : ~static_cast<uint32_t>(key);
 }
 
 struct ArgmaxLayout {
-    size_t counters, partials, total;
-    uint32_t stride;
+    size_t slots, total;
 };
 
 ArgmaxLayout argmax_layout(uint32_t rows, uint32_t V) {
+    (void)V;
     ArgmaxLayout l{};
-    l.stride = ceil_div(V, kUnitMin);  // most chunks any plan uses
-    l.counters = kWsHeaderBytes;
-    l.partials = l.counters + ws_counters_bytes(rows);
-    l.total = l.partials + static_cast<size_t>(rows) * l.stride * sizeof(ArgPair);
+    l.slots = kWsHeaderBytes;
+    l.total = l.slots + align_up(static_cast<size_t>(rows) * 8u, 256);
     return l;
 }
 
@@ -264,31 +221,28 @@ sel_status launch_argmax(const float* d_logits, uint32_t rows, uint32_t V, const
     const int sms = device_sms();
     if (sms <= 0) return SEL_ECUDA;
 
-    const bool tma = (reinterpret_cast<uintptr_t>(d_logits) % 16 == 0) && (V % 4 == 0);
-    constexpr size_t kDyn = stage_bytes<kNT, kVPT, kStages>();
-    static const bool attr_ok = set_dynamic_smem(argmax_kernel<true, kExclude>, kDyn);
-    static const int res_tma = resident_blocks_dyn(argmax_kernel<true, kExclude>, kNT, kDyn);
-    static const int res_sca = resident_blocks_dyn(argmax_kernel<false, kExclude>, kNT, 0);
-    if (!attr_ok) return SEL_ECUDA;
-    const int res = tma ? res_tma : res_sca;
-    const StreamPlan sp = plan_stream(rows, V, sms, res, kUnitMin, kUnitMax);
+    const bool vec = (reinterpret_cast<uintptr_t>(d_logits) % 16 == 0) && (V % 4 == 0);
+    // units as large as possible while giving every SM two blocks or more
+    const uint32_t ce = plan_unit(rows, V, kGrain, kUnitMax, 2ull * static_cast<uint64_t>(sms));
+    const uint32_t chunks = ceil_div(V, ce);
+    const uint64_t blocks = static_cast<uint64_t>(rows) * chunks;
+    if (blocks > 0x7fffffffull) return SEL_EUNSUPPORTED;
 
     char* ws = static_cast<char*>(d_ws);
     ArgmaxArgs a{};
     a.logits = d_logits;
-    a.out_ids = d_out_ids;
-    a.counters = reinterpret_cast<uint32_t*>(ws + l.counters);
-    a.partials = reinterpret_cast<ArgPair*>(ws + l.partials);
-    a.stride = l.stride;
-    a.err = reinterpret_cast<uint32_t*>(ws);
-    a.cfg = StreamCfg{rows * sp.chunks, sp.chunks, sp.chunk_elems, V};
+    a.slots = reinterpret_cast<unsigned long long*>(ws + l.slots);
+    a.V = V;
+    a.chunks = chunks;
+    a.chunk_elems = ce;
     a.excluded = d_excluded;
     a.n_excluded = n_excluded;
-    if (tma)
-        argmax_kernel<true, kExclude><<<sp.grid, kNT, kDyn, stream>>>(a);
-    else
-        argmax_kernel<false, kExclude><<<sp.grid, kNT, 0, stream>>>(a);
-    return cudaGetLastError() == cudaSuccess ? SEL_OK : SEL_ECUDA;
+    const dim3 grid(static_cast<uint32_t>(blocks));
+    cudaError_t e = vec ? launch_pdl(argmax_kernel<true, kExclude>, grid, dim3(kNT), 0, stream, a)
+                        : launch_pdl(argmax_kernel<false, kExclude>, grid, dim3(kNT), 0, stream, a);
+    if (e != cudaSuccess) return SEL_ECUDA;
+    e = launch_pdl(argmax_finish_kernel, dim3(ceil_div(rows, kNT)), dim3(kNT), 0, stream, a.slots, d_out_ids, rows);
+    return e == cudaSuccess ? SEL_OK : SEL_ECUDA;
 }
 
 }  // namespace sel

@@ -9,9 +9,9 @@
 // passes the logits and the output ids.
 //
 // The array is shared by every call on a device and keeps what the last call
-// left there. Each call clears the part that must start at zero (the error
-// word and the per-row arrival counters) with cudaMemsetAsync on its stream,
-// then runs the regular argmax kernel on the array. Calls that overlap on
+// left there. Each call clears the part it uses (the error word and the
+// per-row slots, which must start at zero) with cudaMemsetAsync on its
+// stream, then runs the regular argmax kernels on the array. Calls that overlap on
 // the GPU (on different streams without ordering) race on the array.
 #include <atomic>
 
@@ -57,8 +57,7 @@ extern "C" sel_status sel_argmax_noalloc(const float* d_logits, uint32_t rows, u
     void* ws = nullptr;
     const sel_status st = scratch_address(&ws);
     if (st != SEL_OK) return st;
-    // the error word and the arrival counters must start at zero
-    const size_t zero = sel::kWsHeaderBytes + sel::ws_counters_bytes(rows);
-    if (cudaMemsetAsync(ws, 0, zero, stream) != cudaSuccess) return SEL_ECUDA;
+    // the error word and the per-row slots must start at zero
+    if (cudaMemsetAsync(ws, 0, need, stream) != cudaSuccess) return SEL_ECUDA;
     return sel_argmax(d_logits, rows, V, d_out_ids, ws, kNoAllocScratchBytes, stream);
 }

@@ -17,11 +17,12 @@
 // rows ("two extra full-vocabulary passes and an extra host sync per
 // verified position" is the mlxcel cost note). Here:
 //  Phase 1 (one launch over every target and draft row of every sequence):
-//    blocks stream row chunks once, reducing each to (max, sum of
-//    exp((x - max) / T)) -- in the argmax rule, to (max, lowest argmax id).
-//    The last block of a row merges the row's chunks in chunk order; the
-//    last row of a sequence to finish runs the acceptance chain for that
-//    sequence on the gathered logits x[t_j] and records the decision.
+//    one block per row chunk (sel_units.cuh) reduces its chunk to (max, sum
+//    of exp((x - max) / T)) -- in the argmax rule, to (max, lowest argmax
+//    id) -- and stores it (no block waits on another). A finishing launch
+//    with one block per sequence (programmatic dependent launch) merges each
+//    row's chunks in chunk order, then runs the sequence's acceptance chain
+//    on the gathered logits x[t_j] and records the decision.
 //  Phase 2 (rejection rule only): blocks stream the one or two rows the
 //    decision names (target and draft row j*, or target row K), summing the
 //    residual (and p, for the fallback) per chunk; the last block of the
@@ -35,7 +36,7 @@
 #include <cfloat>
 
 #include "sel_plan.h"
-#include "sel_stream.cuh"
+#include "sel_units.cuh"
 
 namespace sel {
 namespace {
@@ -43,12 +44,9 @@ namespace {
 constexpr int kNT = 256;
 constexpr int kWarps = kNT / 32;
 constexpr int kVPT = 8;
-constexpr int kStages = 3;
+constexpr uint32_t kGrain = 4u * kNT;           // unit sizes are multiples of this
 constexpr uint32_t kUnitMax = 4u * kNT * kVPT;  // 8,192 elements per unit
-constexpr uint32_t kUnitMin = 1024u;
-constexpr uint32_t kGrain = 4u * kNT;
-constexpr uint32_t kMaxChunks = 4096;
-constexpr uint32_t kOverhead = 1024;
+constexpr uint32_t kUnitMin = kGrain;
 constexpr uint32_t kNoIdx = 0x7fffffffu;
 constexpr uint32_t kNonfiniteBit = 0x80000000u;
 
@@ -105,7 +103,7 @@ struct SpecArgs {
     uint32_t S, K, V;
     float T;
     float log2e_over_T;    // exp(d / T) = 2^(d * log2e_over_T)
-    StreamCfg cfg;         // phase-1 units over all rows
+    uint32_t chunks, chunk_elems;  // phase-1 units: chunks per row, elements per chunk
     uint32_t* err;
     uint32_t* row_ctr;
     uint32_t* seq_ctr;
@@ -131,11 +129,22 @@ __device__ __forceinline__ const float* phase1_row(const SpecArgs& a, uint32_t r
     return a.draft + static_cast<size_t>(r - nt) * a.V;
 }
 
+// Values of the first kPre positions of a sequence that the acceptance
+// chain reads, loaded while the rows are merged.
+constexpr uint32_t kPre = 64;
+struct ChainPre {
+    uint32_t tok[kPre];
+    float u[kPre];
+    float xt[kPre];  // target_j[t_j]
+    float xd[kPre];  // draft_j[t_j]
+};
+
 // The acceptance chain of one sequence, run by one warp once every row of
 // the sequence has its statistics: lane j tests position j (32 at a time)
-// and the first failing position ends the chain.
+// and the first failing position ends the chain. Positions below kPre read
+// their token, uniform and logits from `pre`.
 template <bool kRej>
-__device__ void decide_sequence(const SpecArgs& a, uint32_t s) {
+__device__ void decide_sequence(const SpecArgs& a, uint32_t s, const ChainPre& pre) {
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t K = a.K, V = a.V;
     const RowPart* tstat = a.row_stats + static_cast<size_t>(s) * (K + 1u);
@@ -143,14 +152,15 @@ __device__ void decide_sequence(const SpecArgs& a, uint32_t s) {
     const uint32_t* tok = a.tokens + static_cast<size_t>(s) * K;
     const float* u_acc = a.u_acc + static_cast<size_t>(s) * K;
     uint32_t* em = a.emitted + static_cast<size_t>(s) * (K + 1u);
+    auto token = [&](uint32_t j) { return j < kPre ? pre.tok[j] : tok[j]; };
 
     bool bad = false;
-    for (uint32_t j = lane; j <= K; j += 32u) bad |= (ld_gpu_u32(&tstat[j].idx) & kNonfiniteBit) != 0u;
+    for (uint32_t j = lane; j <= K; j += 32u) bad |= (tstat[j].idx & kNonfiniteBit) != 0u;
     for (uint32_t j = lane; j < K; j += 32u) {
-        bad |= tok[j] >= V;
+        bad |= token(j) >= V;
         if (kRej) {
-            bad |= (ld_gpu_u32(&dstat[j].idx) & kNonfiniteBit) != 0u;
-            const float u = u_acc[j];
+            bad |= (dstat[j].idx & kNonfiniteBit) != 0u;
+            const float u = j < kPre ? pre.u[j] : u_acc[j];
             bad |= !(u >= 0.0f && u < 1.0f);
         }
     }
@@ -171,18 +181,24 @@ __device__ void decide_sequence(const SpecArgs& a, uint32_t s) {
         const uint32_t j = j0 + lane;
         bool fail = false;
         if (j < K) {
-            const uint32_t t = tok[j];
+            const uint32_t t = token(j);
             if (!kRej) {
-                fail = t != (ld_gpu_u32(&tstat[j].idx) & ~kNonfiniteBit);
+                fail = t != (tstat[j].idx & ~kNonfiniteBit);
             } else {
                 // p_j(t) and q_j(t) from the row statistics; accept iff u q <= p
-                const float* trow = a.target + (static_cast<size_t>(s) * (K + 1u) + j) * V;
-                const float* drow = a.draft + (static_cast<size_t>(s) * K + j) * V;
-                const float p = ex2_approx((trow[t] - ld_gpu_f32(&tstat[j].m)) * a.log2e_over_T) /
-                                ld_gpu_f32(&tstat[j].s_hi);
-                const float q = ex2_approx((drow[t] - ld_gpu_f32(&dstat[j].m)) * a.log2e_over_T) /
-                                ld_gpu_f32(&dstat[j].s_hi);
-                fail = !(u_acc[j] * q <= p);
+                float xt, xd, u;
+                if (j < kPre) {
+                    xt = pre.xt[j];
+                    xd = pre.xd[j];
+                    u = pre.u[j];
+                } else {
+                    xt = a.target[(static_cast<size_t>(s) * (K + 1u) + j) * V + t];
+                    xd = a.draft[(static_cast<size_t>(s) * K + j) * V + t];
+                    u = u_acc[j];
+                }
+                const float p = ex2_approx((xt - tstat[j].m) * a.log2e_over_T) / tstat[j].s_hi;
+                const float q = ex2_approx((xd - dstat[j].m) * a.log2e_over_T) / dstat[j].s_hi;
+                fail = !(u * q <= p);
             }
         }
         const uint32_t f = __ballot_sync(kFull, fail);
@@ -193,8 +209,8 @@ __device__ void decide_sequence(const SpecArgs& a, uint32_t s) {
     }
     for (uint32_t j = lane; j <= K; j += 32u) {
         uint32_t v = SEL_INVALID_ID;  // in the rejection rule em[n] is the phase-2 draw
-        if (j < n) v = tok[j];
-        else if (!kRej && j == n) v = ld_gpu_u32(&tstat[n].idx) & ~kNonfiniteBit;
+        if (j < n) v = token(j);
+        else if (!kRej && j == n) v = tstat[n].idx & ~kNonfiniteBit;
         em[j] = v;
     }
     if (lane == 0) {
@@ -203,185 +219,213 @@ __device__ void decide_sequence(const SpecArgs& a, uint32_t s) {
     }
 }
 
+// Two fp32 lanes at once (packed f32x2 arithmetic, round to nearest).
+__device__ __forceinline__ unsigned long long pk(float x, float y) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+__device__ __forceinline__ float2 unpk(unsigned long long r) {
+    float2 v;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+    return v;
+}
+// ((x - m) * c) for two lanes: the difference first, so a value at the
+// maximum gets exactly 2^0 = 1
+__device__ __forceinline__ float2 scaled_diff2(float x, float y, unsigned long long neg_m, unsigned long long c2) {
+    unsigned long long d = pk(x, y);
+    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(d) : "l"(neg_m));
+    asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(d) : "l"(c2));
+    return unpk(d);
+}
+__device__ __forceinline__ void acc2(unsigned long long& acc, float x, float y) {
+    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(acc) : "l"(pk(x, y)));
+}
+
 // Phase 1: per-row (max, sum exp) or (max, argmax); per-sequence decision.
-template <bool kTma, bool kRej>
-__global__ void __launch_bounds__(kNT, 2) spec_phase1_kernel(SpecArgs a) {
-    extern __shared__ float4 stages[];
-    __shared__ uint64_t full[kStages];
+// One block per row chunk.
+template <bool kVec, bool kRej>
+__global__ void __launch_bounds__(kNT) spec_phase1_kernel(SpecArgs a) {
     __shared__ float s_m[kWarps];
     __shared__ uint32_t s_i[kWarps];
     __shared__ uint32_t s_nf[kWarps];
     __shared__ FF s_ff[kWarps];
-    __shared__ uint32_t s_flag;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    auto row_ptr = [&](uint32_t r) {
-        uint32_t seq;
-        return phase1_row(a, r, seq);
-    };
+    pdl_wait();
+    const BlockUnit t = block_unit(a.chunks, a.chunk_elems, a.V);
+    uint32_t seq;
+    const float* row = phase1_row(a, t.row, seq);
+    // Padding past the row end is -inf: it never wins the argmax and weighs
+    // exp(-inf) = 0; the latch skips it.
+    float4 q[kVPT];
+    load_unit<kNT, kVPT, kVec>(row, t.lo, t.hi, -INFINITY, q);
+    pdl_trigger();
 
-    // Per thread, over this block's segment of a row: four (max, quad start)
-    // chains (the lowest id of the maximum is the quad start + lane), the
-    // nonfinite latch (sum of x * 0 stays 0 unless some x is +-Inf or NaN),
-    // and in the rejection rule four sums of 2^((x - M) * c) = exp((x - M) / T)
-    // relative to the thread's running max M. Padding past the row end is
-    // -FLT_MAX: it never wins and adds exp(-inf) = 0.
-    float best[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-    uint32_t bbase[4] = {kNoIdx, kNoIdx, kNoIdx, kNoIdx};
-    float nfacc = 0.0f;
-    float M = -INFINITY;
-    float sum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    // nonfinite latch over the real quads (sum of x * 0 stays 0 unless some
+    // x is +-Inf or NaN; a partial quad's padding lanes are -inf too, so the
+    // scalar path latches by element)
+    float2 nfacc = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int sl = 0; sl < kVPT; ++sl) {
+        const uint32_t e = t.lo + 4u * (tid + kNT * sl);
+        if (e + 3u < t.hi) {
+            latch_nonfinite(nfacc, q[sl]);
+        } else if (e < t.hi) {
+            const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (e + j < t.hi) nfacc.x = __fmaf_rn(f[j], 0.0f, nfacc.x);
+        }
+    }
+    uint32_t nf = nfacc.x + nfacc.y == 0.0f ? 0u : kNonfiniteBit;
+
+    float bm = -INFINITY;
+    uint32_t bi = kNoIdx;
+    float thread_s = 0.0f;
     const float c = a.log2e_over_T;
-
-    auto accum = [&](const Unit& t, float4 (&q)[kVPT]) {
+    if (kRej) {
+        // the thread's max, then sum of 2^((x - M) c) = exp((x - M) / T),
+        // two lanes at a time; padding weighs 2^-inf = 0
+        float m = quad_max(q[0]);
+#pragma unroll
+        for (int sl = 1; sl < kVPT; ++sl) m = max3f(m, fmaxf(q[sl].x, q[sl].y), fmaxf(q[sl].z, q[sl].w));
+        bm = m;
+        const float nm = m > -INFINITY ? -m : 0.0f;  // a padding-only thread sums zeros
+        const unsigned long long neg_m = pk(nm, nm), c2 = pk(c, c);
+        unsigned long long acc0 = 0ull, acc1 = 0ull;
+#pragma unroll
+        for (int sl = 0; sl < kVPT; ++sl) {
+            const float2 xy = scaled_diff2(q[sl].x, q[sl].y, neg_m, c2);
+            const float2 zw = scaled_diff2(q[sl].z, q[sl].w, neg_m, c2);
+            acc2(acc0, ex2_approx(xy.x), ex2_approx(xy.y));
+            acc2(acc1, ex2_approx(zw.x), ex2_approx(zw.y));
+        }
+        const float2 s0 = unpk(acc0), s1 = unpk(acc1);
+        thread_s = (s0.x + s0.y) + (s1.x + s1.y);
+    } else {
+        // four independent (max, quad start) chains, one per lane of the
+        // float4; ids rise along each chain, so '>' keeps the lowest
+        float best[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        uint32_t bbase[4] = {kNoIdx, kNoIdx, kNoIdx, kNoIdx};
 #pragma unroll
         for (int sl = 0; sl < kVPT; ++sl) {
             const uint32_t e = t.lo + 4u * (tid + kNT * sl);
             const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                nfacc = __fmaf_rn(f[j], 0.0f, nfacc);
-                if (f[j] > best[j]) {  // ids rise along each chain: '>' keeps the lowest
+                if (f[j] > best[j]) {
                     best[j] = f[j];
                     bbase[j] = e;
                 }
             }
         }
-        if (kRej) {
-            const float Mn = fmaxf(fmaxf(best[0], best[1]), fmaxf(best[2], best[3]));
-            if (Mn > -INFINITY && Mn < INFINITY) {
-                const float scale = M > -INFINITY ? ex2_approx((M - Mn) * c) : 0.0f;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) sum[j] *= scale;
-                const uint32_t n = t.hi - t.lo;
-                if (n == 4u * kNT * kVPT) {
-#pragma unroll
-                    for (int sl = 0; sl < kVPT; ++sl) {
-                        sum[0] += ex2_approx((q[sl].x - Mn) * c);
-                        sum[1] += ex2_approx((q[sl].y - Mn) * c);
-                        sum[2] += ex2_approx((q[sl].z - Mn) * c);
-                        sum[3] += ex2_approx((q[sl].w - Mn) * c);
-                    }
-                } else {
-                    // a short unit: padding must weigh 0 even when every
-                    // real value (and so Mn) is -FLT_MAX
-#pragma unroll
-                    for (int sl = 0; sl < kVPT; ++sl) {
-                        const uint32_t e = 4u * (tid + kNT * sl);
-                        const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            sum[j] += e + j < n ? ex2_approx((f[j] - Mn) * c) : 0.0f;
-                    }
-                }
-                M = Mn;
-            }
-        }
-    };
-
-    auto flush = [&](const Segment& g) {
-        uint32_t nf = nfacc == 0.0f ? 0u : kNonfiniteBit;
-        float bm = -INFINITY;
-        uint32_t bi = kNoIdx;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const uint32_t id = bbase[j] == kNoIdx ? kNoIdx : bbase[j] + j;
             if (beats(best[j], id, bm, bi)) { bm = best[j]; bi = id; }
         }
-        const float thread_m = M;
-        const float thread_s = (sum[0] + sum[1]) + (sum[2] + sum[3]);
+    }
+    const float thread_m = bm;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) { best[j] = -INFINITY; bbase[j] = kNoIdx; sum[j] = 0.0f; }
-        nfacc = 0.0f;
-        M = -INFINITY;
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(kFull, bm, o);
+        const uint32_t oi = __shfl_xor_sync(kFull, bi, o);
+        if (beats(ov, oi, bm, bi)) { bm = ov; bi = oi; }
+    }
+    nf = __reduce_or_sync(kFull, nf);
+    if (lane == 0) { s_m[warp] = bm; s_i[warp] = bi; s_nf[warp] = nf; }
+    __syncthreads();
+    bm = s_m[0];
+    bi = s_i[0];
+    nf = s_nf[0];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(kFull, bm, o);
-            const uint32_t oi = __shfl_xor_sync(kFull, bi, o);
-            if (beats(ov, oi, bm, bi)) { bm = ov; bi = oi; }
-        }
-        nf = __reduce_or_sync(kFull, nf);
-        if (lane == 0) { s_m[warp] = bm; s_i[warp] = bi; s_nf[warp] = nf; }
+    for (int w = 1; w < kWarps; ++w) {
+        if (beats(s_m[w], s_i[w], bm, bi)) { bm = s_m[w]; bi = s_i[w]; }
+        nf |= s_nf[w];
+    }
+    // the sums, rescaled to the chunk's max, added as float-float
+    FF tot{0.0f, 0.0f};
+    if (kRej) {
+        FF mine{(!nf && thread_m > -INFINITY) ? thread_s * ex2_approx((thread_m - bm) * c) : 0.0f, 0.0f};
+        mine = ff_warp_sum(mine);
+        if (lane == 0) s_ff[warp] = mine;
         __syncthreads();
-        bm = s_m[0];
-        bi = s_i[0];
-        nf = s_nf[0];
 #pragma unroll
-        for (int w = 1; w < kWarps; ++w) {
-            if (beats(s_m[w], s_i[w], bm, bi)) { bm = s_m[w]; bi = s_i[w]; }
-            nf |= s_nf[w];
-        }
-        // the sums, rescaled to the segment's max, added as float-float
-        FF tot{0.0f, 0.0f};
-        if (kRej) {
-            FF mine{(!nf && thread_m > -INFINITY) ? thread_s * ex2_approx((thread_m - bm) * c) : 0.0f, 0.0f};
-            mine = ff_warp_sum(mine);
-            if (lane == 0) s_ff[warp] = mine;
-            __syncthreads();
-#pragma unroll
-            for (int ww = 0; ww < kWarps; ++ww) tot = ff_add(tot, s_ff[ww]);
-        }
-        RowPart* parts = a.row_parts + static_cast<size_t>(g.row) * a.cmax;
-        if (tid == 0) {
-            const RowPart part{bm, bi | nf, tot.hi, tot.lo};
-            if (g.count == 1) {
-                a.row_stats[g.row] = part;
-                s_flag = 2u;  // the row is complete
-            } else {
-                parts[g.index] = part;
-                s_flag = segment_arrive(&a.row_ctr[g.row], g.count) ? 1u : 0u;
-            }
-        }
-        __syncthreads();
-        const uint32_t flag = s_flag;
-        if (flag != 0u && warp == 0) {
-            if (flag == 1u) {
-                // this block completed the row: merge its segments in segment order
-                __threadfence();
-                float rm = -INFINITY;
-                uint32_t ri = kNoIdx, rnf = 0u;
-                for (uint32_t cc = lane; cc < g.count; cc += 32u) {
-                    const float cm = ld_gpu_f32(&parts[cc].m);
-                    const uint32_t ci = ld_gpu_u32(&parts[cc].idx);
-                    rnf |= ci & kNonfiniteBit;
-                    if (beats(cm, ci & ~kNonfiniteBit, rm, ri)) { rm = cm; ri = ci & ~kNonfiniteBit; }
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const float ov = __shfl_xor_sync(kFull, rm, o);
-                    const uint32_t oi = __shfl_xor_sync(kFull, ri, o);
-                    if (beats(ov, oi, rm, ri)) { rm = ov; ri = oi; }
-                }
-                rnf = __reduce_or_sync(kFull, rnf);
-                FF rs{0.0f, 0.0f};
-                if (kRej && !rnf) {
-                    for (uint32_t cc = lane; cc < g.count; cc += 32u) {
-                        const FF sc{ld_gpu_f32(&parts[cc].s_hi), ld_gpu_f32(&parts[cc].s_lo)};
-                        rs = ff_add(rs, ff_mul_f(sc, ex2_approx((ld_gpu_f32(&parts[cc].m) - rm) * c)));
-                    }
-                    rs = ff_warp_sum(rs);
-                }
-                if (lane == 0) a.row_stats[g.row] = RowPart{rm, ri | rnf, rs.hi, rs.lo};
-            }
-            // the last row of the sequence to finish runs the acceptance chain
-            if (a.decide) {
-                uint32_t seq;
-                phase1_row(a, g.row, seq);
-                bool last = false;
-                if (lane == 0) {
-                    const uint32_t rows_per_seq = kRej ? 2u * a.K + 1u : a.K + 1u;
-                    last = segment_arrive(&a.seq_ctr[seq], rows_per_seq);
-                }
-                if (__shfl_sync(kFull, last, 0)) {
-                    __threadfence();
-                    decide_sequence<kRej>(a, seq);
-                }
-            }
-        }
-        __syncthreads();
-    };
+        for (int ww = 0; ww < kWarps; ++ww) tot = ff_add(tot, s_ff[ww]);
+    }
+    if (tid == 0) a.row_parts[static_cast<size_t>(t.row) * a.cmax + t.chunk] = RowPart{bm, bi | nf, tot.hi, tot.lo};
+}
 
-    stream_segments<kTma, kNT, kVPT, kStages>(a.cfg, row_ptr, accum, flush, stages, full, a.err, -FLT_MAX);
+// Merge row r's chunk statistics in chunk order (one warp) into row_stats.
+template <bool kRej>
+__device__ void merge_row(const SpecArgs& a, uint32_t r) {
+    const uint32_t lane = threadIdx.x & 31u;
+    const RowPart* parts = a.row_parts + static_cast<size_t>(r) * a.cmax;
+    const float c = a.log2e_over_T;
+    float rm = -INFINITY;
+    uint32_t ri = kNoIdx, rnf = 0u;
+    for (uint32_t cc = lane; cc < a.chunks; cc += 32u) {
+        const float cm = parts[cc].m;
+        const uint32_t ci = parts[cc].idx;
+        rnf |= ci & kNonfiniteBit;
+        if (beats(cm, ci & ~kNonfiniteBit, rm, ri)) { rm = cm; ri = ci & ~kNonfiniteBit; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(kFull, rm, o);
+        const uint32_t oi = __shfl_xor_sync(kFull, ri, o);
+        if (beats(ov, oi, rm, ri)) { rm = ov; ri = oi; }
+    }
+    rnf = __reduce_or_sync(kFull, rnf);
+    FF rs{0.0f, 0.0f};
+    if (kRej && !rnf) {
+        // chunk sums in chunk order: 32 at a time, each group a fixed butterfly
+        for (uint32_t c0 = 0; c0 < a.chunks; c0 += 32u) {
+            const uint32_t cc = c0 + lane;
+            FF sc{0.0f, 0.0f};
+            if (cc < a.chunks) {
+                const float cm = parts[cc].m;
+                // a chunk of padding only (max -inf) adds nothing
+                if (cm > -INFINITY) sc = ff_mul_f(FF{parts[cc].s_hi, parts[cc].s_lo}, ex2_approx((cm - rm) * c));
+            }
+            rs = ff_add(rs, ff_warp_sum(sc));
+        }
+    }
+    if (lane == 0) a.row_stats[r] = RowPart{rm, ri | rnf, rs.hi, rs.lo};
+}
+
+// Finishing launch of phase 1: block s merges the rows of sequence s and,
+// when deciding, runs its acceptance chain.
+template <bool kRej>
+__global__ void __launch_bounds__(kNT) spec_rows_kernel(SpecArgs a) {
+    __shared__ ChainPre pre;
+    pdl_wait();
+    pdl_trigger();
+    const uint32_t s = blockIdx.x, K = a.K;
+    const uint32_t tid = threadIdx.x, warp = tid >> 5;
+    if (a.decide) {
+        // the chain's inputs, loaded while the rows are merged
+        const uint32_t* tok = a.tokens + static_cast<size_t>(s) * K;
+        for (uint32_t j = tid; j < K && j < kPre; j += kNT) {
+            const uint32_t t = tok[j];
+            pre.tok[j] = t;
+            if (kRej) {
+                pre.u[j] = a.u_acc[static_cast<size_t>(s) * K + j];
+                const bool ok = t < a.V;
+                pre.xt[j] = ok ? a.target[(static_cast<size_t>(s) * (K + 1u) + j) * a.V + t] : 0.0f;
+                pre.xd[j] = ok ? a.draft[(static_cast<size_t>(s) * K + j) * a.V + t] : 0.0f;
+            }
+        }
+    }
+    const uint32_t rows_t = K + 1u, rows_d = kRej ? K : 0u;
+    for (uint32_t i = warp; i < rows_t + rows_d; i += kWarps) {
+        const uint32_t r = i < rows_t ? s * rows_t + i : a.S * rows_t + s * K + (i - rows_t);
+        merge_row<kRej>(a, r);
+    }
+    if (!a.decide) return;
+    __syncthreads();  // row statistics and prefetched inputs of this block
+    if (warp == 0) decide_sequence<kRej>(a, s, pre);
 }
 
 struct DrawArgs {
@@ -440,6 +484,7 @@ __global__ void __launch_bounds__(kNT) spec_draw_kernel(DrawArgs a) {
     __shared__ float s_stripe[kWarps][kDrawPer / 4];
     __shared__ int s_istar;
 
+    pdl_wait();
     const uint32_t chunks = a.chunks;
     const uint32_t s = blockIdx.x / chunks;
     const uint32_t chunk = blockIdx.x - s * chunks;
@@ -712,6 +757,7 @@ __global__ void __launch_bounds__(kNT) spec_diag_kernel(DiagArgs a) {
     __shared__ FF s_m[kWarps];
     __shared__ FF s_p[kWarps];
     __shared__ bool s_last;
+    pdl_wait();
     const uint32_t pos = blockIdx.x / a.chunks;
     const uint32_t chunk = blockIdx.x - pos * a.chunks;
     const uint32_t s = pos / a.K, j = pos - s * a.K;
@@ -830,14 +876,9 @@ extern "C" sel_status spec_accept(const float* d_target, const float* d_draft, c
     const uint32_t rows1 = rej ? static_cast<uint32_t>(rows_a) : S * (K + 1u);
     const bool vec = V % 4 == 0 && reinterpret_cast<uintptr_t>(d_target) % 16 == 0 &&
                      (!rej || K == 0 || reinterpret_cast<uintptr_t>(d_draft) % 16 == 0);
-    constexpr size_t kDyn = stage_bytes<kNT, kVPT, kStages>();
-    static const bool attr_ok = set_dynamic_smem(spec_phase1_kernel<true, true>, kDyn) &&
-                                set_dynamic_smem(spec_phase1_kernel<true, false>, kDyn);
-    static const int res_tma = resident_blocks_dyn(spec_phase1_kernel<true, true>, kNT, kDyn);
-    static const int res_sca = resident_blocks_dyn(spec_phase1_kernel<false, true>, kNT, 0);
-    if (!attr_ok) return SEL_ECUDA;
-    const StreamPlan plan = plan_stream(rows1, V, sms, vec ? res_tma : res_sca, kUnitMin, kUnitMax);
-    if (static_cast<uint64_t>(rows1) * plan.chunks > 0x7fffffffull) return SEL_EUNSUPPORTED;
+    const uint32_t ce1 = plan_unit(rows1, V, kGrain, kUnitMax, 2ull * static_cast<uint64_t>(sms));
+    const uint32_t chunks1 = ceil_div(V, ce1);
+    if (static_cast<uint64_t>(rows1) * chunks1 > 0x7fffffffull) return SEL_EUNSUPPORTED;
     SpecArgs a{};
     a.target = d_target;
     a.draft = d_draft;
@@ -849,7 +890,8 @@ extern "C" sel_status spec_accept(const float* d_target, const float* d_draft, c
     a.S = S; a.K = K; a.V = V;
     a.T = rej ? p->temperature : 1.0f;
     a.log2e_over_T = static_cast<float>(1.4426950408889634 / static_cast<double>(a.T));
-    a.cfg = StreamCfg{rows1 * plan.chunks, plan.chunks, plan.chunk_elems, V};
+    a.chunks = chunks1;
+    a.chunk_elems = ce1;
     a.err = reinterpret_cast<uint32_t*>(ws);
     a.row_ctr = reinterpret_cast<uint32_t*>(ws + l.row_ctr);
     a.seq_ctr = reinterpret_cast<uint32_t*>(ws + l.seq_ctr_a);
@@ -858,15 +900,16 @@ extern "C" sel_status spec_accept(const float* d_target, const float* d_draft, c
     a.decisions = reinterpret_cast<Decision*>(ws + l.decisions);
     a.cmax = l.cmax_a;
     a.decide = true;
-    const dim3 grid1(plan.grid);
-    if (rej) {
-        if (vec) spec_phase1_kernel<true, true><<<grid1, kNT, kDyn, stream>>>(a);
-        else spec_phase1_kernel<false, true><<<grid1, kNT, 0, stream>>>(a);
-    } else {
-        if (vec) spec_phase1_kernel<true, false><<<grid1, kNT, kDyn, stream>>>(a);
-        else spec_phase1_kernel<false, false><<<grid1, kNT, 0, stream>>>(a);
-    }
-    if (cudaGetLastError() != cudaSuccess) return SEL_ECUDA;
+    const dim3 grid1(rows1 * chunks1);
+    cudaError_t e1;
+    if (rej) e1 = vec ? launch_pdl(spec_phase1_kernel<true, true>, grid1, dim3(kNT), 0, stream, a)
+                      : launch_pdl(spec_phase1_kernel<false, true>, grid1, dim3(kNT), 0, stream, a);
+    else e1 = vec ? launch_pdl(spec_phase1_kernel<true, false>, grid1, dim3(kNT), 0, stream, a)
+                  : launch_pdl(spec_phase1_kernel<false, false>, grid1, dim3(kNT), 0, stream, a);
+    if (e1 != cudaSuccess) return SEL_ECUDA;
+    e1 = rej ? launch_pdl(spec_rows_kernel<true>, dim3(S), dim3(kNT), 0, stream, a)
+             : launch_pdl(spec_rows_kernel<false>, dim3(S), dim3(kNT), 0, stream, a);
+    if (e1 != cudaSuccess) return SEL_ECUDA;
     if (!rej) return SEL_OK;
 
     // phase 2: one wave of blocks when the sequences allow it (S * chunks
@@ -893,9 +936,9 @@ extern "C" sel_status spec_accept(const float* d_target, const float* d_draft, c
     b.parts = reinterpret_cast<DrawPart*>(ws + l.draw_parts);
     b.cmax = l.cmax_b;
     const dim3 grid2(S * chunks2);
-    if (vec) spec_draw_kernel<true><<<grid2, kNT, 0, stream>>>(b);
-    else spec_draw_kernel<false><<<grid2, kNT, 0, stream>>>(b);
-    return cudaGetLastError() == cudaSuccess ? SEL_OK : SEL_ECUDA;
+    const cudaError_t e2 = vec ? launch_pdl(spec_draw_kernel<true>, grid2, dim3(kNT), 0, stream, b)
+                               : launch_pdl(spec_draw_kernel<false>, grid2, dim3(kNT), 0, stream, b);
+    return e2 == cudaSuccess ? SEL_OK : SEL_ECUDA;
 }
 
 extern "C" sel_status spec_diagnostics(const float* d_target, const float* d_draft, uint32_t S, uint32_t K,
@@ -923,20 +966,17 @@ extern "C" sel_status spec_diagnostics(const float* d_target, const float* d_dra
     const uint32_t rows1 = static_cast<uint32_t>(rows_a);
     const bool vec = V % 4 == 0 && reinterpret_cast<uintptr_t>(d_target) % 16 == 0 &&
                      reinterpret_cast<uintptr_t>(d_draft) % 16 == 0;
-    constexpr size_t kDyn = stage_bytes<kNT, kVPT, kStages>();
-    static const bool attr_ok = set_dynamic_smem(spec_phase1_kernel<true, true>, kDyn);
-    static const int res_tma = resident_blocks_dyn(spec_phase1_kernel<true, true>, kNT, kDyn);
-    static const int res_sca = resident_blocks_dyn(spec_phase1_kernel<false, true>, kNT, 0);
-    if (!attr_ok) return SEL_ECUDA;
-    const StreamPlan plan = plan_stream(rows1, V, sms, vec ? res_tma : res_sca, kUnitMin, kUnitMax);
-    if (static_cast<uint64_t>(rows1) * plan.chunks > 0x7fffffffull) return SEL_EUNSUPPORTED;
+    const uint32_t ce1 = plan_unit(rows1, V, kGrain, kUnitMax, 2ull * static_cast<uint64_t>(sms));
+    const uint32_t chunks1 = ceil_div(V, ce1);
+    if (static_cast<uint64_t>(rows1) * chunks1 > 0x7fffffffull) return SEL_EUNSUPPORTED;
     SpecArgs a{};
     a.target = d_target;
     a.draft = d_draft;
     a.S = S; a.K = K; a.V = V;
     a.T = temperature;
     a.log2e_over_T = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
-    a.cfg = StreamCfg{rows1 * plan.chunks, plan.chunks, plan.chunk_elems, V};
+    a.chunks = chunks1;
+    a.chunk_elems = ce1;
     a.err = reinterpret_cast<uint32_t*>(ws);
     a.row_ctr = reinterpret_cast<uint32_t*>(ws + l.row_ctr);
     a.seq_ctr = reinterpret_cast<uint32_t*>(ws + l.seq_ctr_a);
@@ -945,9 +985,10 @@ extern "C" sel_status spec_diagnostics(const float* d_target, const float* d_dra
     a.decisions = reinterpret_cast<Decision*>(ws + l.decisions);
     a.cmax = l.cmax_a;
     a.decide = false;
-    if (vec) spec_phase1_kernel<true, true><<<plan.grid, kNT, kDyn, stream>>>(a);
-    else spec_phase1_kernel<false, true><<<plan.grid, kNT, 0, stream>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return SEL_ECUDA;
+    const cudaError_t e1 = vec ? launch_pdl(spec_phase1_kernel<true, true>, dim3(rows1 * chunks1), dim3(kNT), 0, stream, a)
+                               : launch_pdl(spec_phase1_kernel<false, true>, dim3(rows1 * chunks1), dim3(kNT), 0, stream, a);
+    if (e1 != cudaSuccess) return SEL_ECUDA;
+    if (launch_pdl(spec_rows_kernel<true>, dim3(S), dim3(kNT), 0, stream, a) != cudaSuccess) return SEL_ECUDA;
 
     // the paired pass: chunks of at most kDrawChunkMax ids, about two blocks per SM
     const uint64_t positions = static_cast<uint64_t>(S) * K;
@@ -972,7 +1013,7 @@ extern "C" sel_status spec_diagnostics(const float* d_target, const float* d_dra
     d.sum_min = d_sum_min;
     d.sum_prod = d_sum_prod;
     const dim3 grid2(static_cast<uint32_t>(positions * chunks));
-    if (vec) spec_diag_kernel<true><<<grid2, kNT, 0, stream>>>(d);
-    else spec_diag_kernel<false><<<grid2, kNT, 0, stream>>>(d);
-    return cudaGetLastError() == cudaSuccess ? SEL_OK : SEL_ECUDA;
+    const cudaError_t e2 = vec ? launch_pdl(spec_diag_kernel<true>, grid2, dim3(kNT), 0, stream, d)
+                               : launch_pdl(spec_diag_kernel<false>, grid2, dim3(kNT), 0, stream, d);
+    return e2 == cudaSuccess ? SEL_OK : SEL_ECUDA;
 }

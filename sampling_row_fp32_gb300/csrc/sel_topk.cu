@@ -11,35 +11,34 @@
 // Design (sm_103a). The page's implementation is a ggml graph op (TOP_K +
 // get_rows) whose kernel is not shown; this one is a single launch that
 // reads each row once:
-//  1. Persistent blocks stream 32 KB row chunks through the TMA bulk-copy
-//     ring of sel_stream.cuh; each thread holds 32 logits of the chunk in
-//     registers and turns them into order-preserving 32-bit keys on the fly.
-//  2. A cheap exact filter: each warp sorts its 32 lane maxima (shuffle
-//     bitonic sort) and takes the ceil(k/8)-th; the minimum over the 8 warps
-//     is a key that at least k elements of the chunk reach, so nothing below
-//     it can be in the chunk's top k. Survivors (typically ~1.5 k) go to a
-//     shared-memory buffer as 64-bit candidates (key << 32 | ~id), which
-//     order exactly like (value desc, id asc).
-//  3. The buffer persists over the consecutive chunks of a row that the
-//     block owns; the first chunk's bound filters them all, and whenever the
-//     buffer passes k + 32 entries it is selected down to its top k, whose
-//     k-th key then filters later chunks (their ids are higher, so an equal
-//     key cannot displace it). When
-//     the block leaves the row it selects the segment's top k (rank counting
-//     for small buffers, bitonic sort otherwise) and publishes them, sorted,
-//     in the workspace. A buffer overflow (adversarial chunks such as
-//     all-equal values) falls back to appending 1,024 elements at a time
-//     with a selection in between, which is exact for any input.
-//  4. The block that publishes a row's last segment merges the segment
+//  1. One block per row chunk of up to 8,192 logits (sel_units.cuh): each
+//     thread loads its 32 logits with 128-bit loads straight into registers
+//     and keeps the largest of each float4 and of the thread.
+//  2. A cheap exact bound: with r = ceil(k / 8), each warp takes the r-th
+//     largest of its 32 lane maxima (r - 1 knock-out rounds of a warp max, or
+//     a shuffle bitonic sort for large r), and the minimum over the 8 warps
+//     is a value that at least 8 r >= k logits of the chunk reach, so nothing
+//     below it is in the chunk's top k. Only float4s whose maximum reaches
+//     the bound are looked at again; the survivors (typically k to 2 k) go to
+//     shared memory as 64-bit candidates (key << 32 | ~id), which order
+//     exactly like (value desc, id asc), and are selected exactly (rank
+//     counting, or a bitonic sort for large buffers). A chunk with more
+//     survivors than the buffer holds (ties, or k beyond the bound's reach)
+//     takes an exact radix select of its k-th key instead, ties going to the
+//     lowest ids.
+//  3. Each block stores its sorted list in the workspace with plain stores
+//     (no fence, no arrival counter: no block waits on another). A finishing
+//     launch with one block per row (programmatic dependent launch, so its
+//     blocks are resident before the main launch ends) merges the row's
 //     lists: a bound from the lists' r-th entries (the m-th largest of the
 //     lists' r-th entries is reached by m * r >= k entries) discards almost
 //     every entry, and the survivors are selected exactly. Sampling then
-//     runs its softmax, top-p, min-p and inverse-CDF draw on the k
-//     candidates in one warp.
+//     runs its softmax, top-p, min-p and inverse-CDF draw on the k candidates
+//     in one warp.
 #include <cfloat>
 
 #include "sel_plan.h"
-#include "sel_stream.cuh"
+#include "sel_units.cuh"
 
 namespace sel {
 namespace {
@@ -47,24 +46,26 @@ namespace {
 constexpr int kNT = 256;
 constexpr int kWarps = kNT / 32;
 constexpr int kVPT = 8;
-constexpr int kStages = 2;
-constexpr uint32_t kUnit = 4u * kNT * kVPT;  // 8,192 elements per chunk
-constexpr uint32_t kCap = 2048;              // candidate buffer (>= SEL_MAX_K + 4 * kNT)
+constexpr uint32_t kGrain = 4u * kNT;        // unit sizes are multiples of this
+constexpr uint32_t kUnitMax = 4u * kNT * kVPT;  // 8,192 elements per unit
+constexpr uint32_t kCap = 2048;              // merge buffer
+constexpr uint32_t kBlockCap = SEL_MAX_K;    // a chunk's survivors before the radix path
 constexpr uint32_t kRankMax = 512;           // rank counting up to this many candidates
 constexpr uint32_t kFastMergeLists = 32;     // one warp lane per chunk list
-constexpr uint32_t kReduceSlack = 32;        // select the buffer down to k above k + this many
 
-static_assert(kCap >= SEL_MAX_K + 4 * kNT, "a slot of 1,024 must fit after a selection");
+static_assert(kBlockCap <= kCap && SEL_MAX_K <= kCap, "selection buffers");
 
 struct alignas(16) TopkShared {
     uint64_t buf[kCap];          // candidate buffer (16-byte aligned: read as pairs)
     uint64_t sorted[SEL_MAX_K];  // selection output, descending
+    uint32_t hist[256];          // radix select
     uint64_t warp_cand[kWarps];
     uint32_t warp_val[kWarps];
+    uint32_t warp_nf[kWarps];
     uint32_t count;              // entries appended to buf
-    uint32_t tau_key;            // key of the k-th candidate after a selection
     uint32_t total;
     uint32_t last;
+    uint32_t digit, want;        // radix select
 };
 
 struct SampleArgs {
@@ -86,7 +87,7 @@ struct TopkArgs {
     uint64_t* lists;         // [rows][stride][k]
     uint32_t stride;
     uint32_t* err;
-    StreamCfg cfg;
+    uint32_t V, chunks, chunk_elems;
     SampleArgs sa;
 };
 
@@ -107,8 +108,9 @@ __device__ __forceinline__ void warp_append(TopkShared& s, bool p, uint64_t cand
     }
 }
 
-// The min(n, k) largest of buf[0..n) (distinct, non-zero) into out[], in
-// descending order. All threads call; buf may be reordered. Ends synced.
+// The min(n, k) largest of buf[0..n) (distinct, non-zero, n <= kCap) into
+// out[], in descending order. All threads call; buf may be reordered. Ends
+// synced.
 __device__ void block_select_sorted(uint64_t* buf, uint32_t n, uint32_t k, uint64_t* out) {
     const uint32_t tid = threadIdx.x;
     if (n <= kRankMax) {
@@ -155,40 +157,108 @@ __device__ void block_select_sorted(uint64_t* buf, uint32_t n, uint32_t k, uint6
     __syncthreads();
 }
 
-// Shrink the buffer to its top min(count, k); record the k-th key.
-__device__ __noinline__ void reduce_buffer(TopkShared& s, uint32_t k) {
-    const uint32_t n = min(s.count, kCap);
-    block_select_sorted(s.buf, n, k, s.sorted);
-    const uint32_t kk = n < k ? n : k;
-    for (uint32_t i = threadIdx.x; i < kk; i += kNT) s.buf[i] = s.sorted[i];
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        s.count = kk;
-        if (kk == k) s.tau_key = cand_key(s.sorted[k - 1]);
-    }
-    __syncthreads();
-}
-
-// A chunk whose survivors overflow the buffer (adversarial rows such as
-// all-equal values): append it again 1,024 elements at a time, re-read from
-// global memory, selecting the buffer down to k in between. Later slots hold
-// higher ids, so an equal key cannot displace the buffer's k-th candidate.
-// Exact for any input; block-collective; kept out of line.
+// A chunk whose survivors overflow the buffer (ties, or k beyond the
+// bound's reach): find its k-th largest key kappa exactly, one 8-bit digit
+// at a time from the top (a shared histogram per digit), then append every
+// element above kappa and, of those equal to kappa, the lowest ids until k
+// are taken. Ids rise with (slot, thread, lane), the order the tie pass
+// walks. The chunk is read again (from L2). Leaves exactly k entries in
+// s.buf (the chunk has more than k). Block-collective; kept out of line
+// (rare).
 template <bool kVec>
-__device__ __noinline__ void overflow_chunk(TopkShared& s, const float* x, uint32_t lo, uint32_t hi, uint32_t k,
-                                            uint32_t tau) {
-    const uint32_t tid = threadIdx.x;
-    for (uint32_t base = lo; base < hi; base += 4u * kNT) {
-        if (s.count + 4u * kNT > kCap) reduce_buffer(s, k);
-        const uint32_t thr = max(max(tau, s.tau_key + 1u), 1u);
-        const uint32_t e = base + 4u * tid;
-        const float4 q = ld_quad<kVec>(x, e, hi, 0.0f);
-        const float f[4] = {q.x, q.y, q.z, q.w};
+__device__ __noinline__ void radix_select_chunk(TopkShared& s, const float* row, uint32_t lo, uint32_t hi,
+                                                uint32_t k) {
+    const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
+    float4 q[kVPT];
+    load_unit<kNT, kVPT, kVec>(row, lo, hi, -FLT_MAX, q);
+    uint32_t prefix = 0, mask = 0, want = k;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        for (uint32_t i = tid; i < 256u; i += kNT) s.hist[i] = 0;
+        __syncthreads();
+#pragma unroll
+        for (int sl = 0; sl < kVPT; ++sl) {
+            const uint32_t e = lo + 4u * (tid + kNT * sl);
+            const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t key = f2key(f[j]);
+                if (e + j < hi && (key & mask) == prefix) atomicAdd(&s.hist[(key >> shift) & 255u], 1u);
+            }
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // lane l holds digits 255 - 8 l .. 248 - 8 l; suffix sums from the top
+            uint32_t c[8], sum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) { c[i] = s.hist[255u - 8u * lane - i]; sum += c[i]; }
+            uint32_t incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t v = __shfl_up_sync(kFull, incl, o);
+                if (lane >= static_cast<uint32_t>(o)) incl += v;
+            }
+            const uint32_t above_lane = incl - sum;  // counts of the digits above this lane's
+            // the lane whose range holds the want-th largest
+            const bool mine = above_lane < want && want <= incl;
+            if (mine) {
+                uint32_t above = above_lane;
+                for (int i = 0; i < 8; ++i) {
+                    if (above + c[i] >= want) {
+                        s.digit = 255u - 8u * lane - i;
+                        s.want = want - above;
+                        break;
+                    }
+                    above += c[i];
+                }
+            }
+        }
+        __syncthreads();
+        prefix |= s.digit << shift;
+        mask |= 255u << shift;
+        want = s.want;
+        __syncthreads();
+    }
+    // prefix = kappa; take every key above it, then `want` of the ties
+    if (tid == 0) s.count = 0;
+    __syncthreads();
+    uint32_t base = 0;
+#pragma unroll
+    for (int sl = 0; sl < kVPT; ++sl) {
+        const uint32_t e = lo + 4u * (tid + kNT * sl);
+        const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
+        uint32_t ties = 0;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const uint32_t kk = e + j < hi ? f2key(f[j]) : 0u;
-            warp_append(s, kk >= thr, make_cand(kk, e + j));
+            const uint32_t key = f2key(f[j]);
+            if (e + j < hi && key > prefix) s.buf[atomicAdd(&s.count, 1u)] = make_cand(key, e + j);
+            ties += (e + j < hi && key == prefix) ? 1u : 0u;
         }
+        // exclusive block scan of the tie counts in thread order
+        uint32_t incl = ties;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(kFull, incl, o);
+            if (lane >= static_cast<uint32_t>(o)) incl += v;
+        }
+        if (lane == 31) s.warp_val[warp] = incl;
+        __syncthreads();
+        uint32_t before = base, total = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const uint32_t v = s.warp_val[w];
+            if (w < static_cast<int>(warp)) before += v;
+            total += v;
+        }
+        uint32_t rank = before + incl - ties;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t key = f2key(f[j]);
+            if (e + j < hi && key == prefix) {
+                if (rank < want) s.buf[atomicAdd(&s.count, 1u)] = make_cand(key, e + j);
+                ++rank;
+            }
+        }
+        base += total;
         __syncthreads();
     }
 }
@@ -323,7 +393,7 @@ __device__ void merge_row_lists(TopkShared& s, Load&& load, uint32_t chunks, uin
             const uint32_t e = static_cast<uint32_t>(tid) + kNT * i;
             if (e < total) s.buf[e] = v[i];
         }
-        if (tid == 0) { s.count = 0; s.tau_key = 0; s.total = 0; }
+        if (tid == 0) { s.count = 0; s.total = 0; }
         __syncthreads();
         bool disorder = false;
         uint32_t nz = 0;
@@ -419,7 +489,7 @@ __device__ void merge_row_lists(TopkShared& s, Load&& load, uint32_t chunks, uin
         }
     }
     if (lane == 0) s.warp_cand[warp] = b;
-    if (tid == 0) { s.count = 0; s.tau_key = 0; s.total = 0; }
+    if (tid == 0) { s.count = 0; s.total = 0; }
     __syncthreads();
     uint64_t tau_m = s.warp_cand[0];
 #pragma unroll
@@ -490,155 +560,132 @@ __device__ __forceinline__ void write_row(TopkShared& s, const TopkArgs& a, uint
     }
 }
 
-// Merge the published lists of a row whose segments have all arrived and
-// write its result. Block-collective.
-template <bool kSample>
-__device__ void finish_row(TopkShared& s, const TopkArgs& a, uint32_t row) {
-    const uint32_t k = a.k;
-    __threadfence();  // order this thread's reads after the arrivals it saw
-    const uint32_t count = segment_of(a.cfg, row).count;
-    uint32_t nf = 0;
-    const int lane = threadIdx.x & 31;
-    // the flags' loads are issued before the lists' and consumed after them
-    for (uint32_t c = lane; c < count; c += 32)
-        nf |= ld_gpu_u32(a.chunk_flags + static_cast<size_t>(row) * a.stride + c);
-    const uint64_t* L = a.lists + static_cast<size_t>(row) * a.stride * k;
-    merge_row_lists(s, [&](uint32_t i) { return ld_gpu_u64(L + i); }, count, k, a.err);
-    nf = __reduce_or_sync(kFull, nf);
-    write_row<kSample>(s, a, row, k, nf != 0);
-    if (threadIdx.x == 0) atomicAdd(a.err + 1, 1u);  // rows finished (self-check)
-    __syncthreads();
-}
-
-template <bool kTma, bool kSample>
-__global__ void __launch_bounds__(kNT, 2) topk_kernel(TopkArgs a) {
-    extern __shared__ float4 stages[];
-    __shared__ uint64_t full[kStages];
+// The main launch: one block per row chunk; each stores the chunk's top k,
+// sorted (padded with empty candidates), and its nonfinite flag.
+template <bool kVec>
+__global__ void __launch_bounds__(kNT, 3) topk_kernel(TopkArgs a) {
     __shared__ TopkShared s;
-
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint32_t V = a.cfg.V, k = a.k;
-    auto row_ptr = [&](uint32_t r) { return a.logits + static_cast<size_t>(r) * V; };
+    const uint32_t V = a.V, k = a.k;
+    pdl_wait();
+    const BlockUnit t = block_unit(a.chunks, a.chunk_elems, V);
+    // Padding past the row end is -FLT_MAX: finite (the latch ignores it),
+    // never above a real logit, and never appended (e < hi is checked).
+    float4 q[kVPT];
+    load_unit<kNT, kVPT, kVec>(a.logits + static_cast<size_t>(t.row) * V, t.lo, t.hi, -FLT_MAX, q);
+    pdl_trigger();
+    if (tid == 0) s.count = 0;
 
-    // Nonfinite latch over the segment: nfacc = sum of x * 0 stays 0 unless
-    // some x is +-Inf or NaN. Padding past the row end is -FLT_MAX (finite,
-    // never above a real logit) and is never appended.
-    float nfacc = 0.0f;
-    // Block-uniform state of the current segment, kept in registers: the
-    // buffer's entry count after the last sync, the chunk bound of the
-    // segment's first chunk (0 = none yet) and the buffer's k-th key after
-    // its last selection (0 = none).
-    uint32_t cnt = 0, tau = 0, tau_key = 0;
-    if (tid == 0) { s.count = 0; s.tau_key = 0; }
+    // the largest value of each float4 and of the thread; the nonfinite
+    // latch (sum of x * 0 stays 0 unless some x is +-Inf or NaN)
+    float2 nfacc = make_float2(0.0f, 0.0f);
+    float smax[kVPT];
+#pragma unroll
+    for (int sl = 0; sl < kVPT; ++sl) {
+        latch_nonfinite(nfacc, q[sl]);
+        smax[sl] = quad_max(q[sl]);
+    }
+    float tmax = smax[0];
+#pragma unroll
+    for (int sl = 1; sl + 1 < kVPT; sl += 2) tmax = max3f(tmax, smax[sl], smax[sl + 1]);
+    if ((kVPT & 1) == 0) tmax = fmaxf(tmax, smax[kVPT - 1]);
+
+    // The chunk bound: >= k elements of the chunk have key >= tau, so no
+    // element below tau is in the chunk's top k (0: no bound).
+    uint32_t wv = 0;
+    if (k <= 32u * kWarps) {
+        const uint32_t r = (k + kWarps - 1) / kWarps;
+        uint32_t key = f2key(tmax);
+        if (r <= 8) {
+            for (uint32_t i = 1; i < r; ++i) {  // knock out the r - 1 largest
+                const uint32_t m = __reduce_max_sync(kFull, key);
+                const uint32_t b = __ballot_sync(kFull, key == m);
+                if (lane == __ffs(b) - 1) key = 0;
+            }
+            wv = __reduce_max_sync(kFull, key);
+        } else {
+            wv = __shfl_sync(kFull, warp_sort_desc(key), static_cast<int>(r - 1));
+        }
+    }
+    const uint32_t wnf = __any_sync(kFull, nfacc.x + nfacc.y != 0.0f) ? 1u : 0u;
+    if (lane == 0) { s.warp_val[warp] = wv; s.warp_nf[warp] = wnf; }
     __syncthreads();
-
-    auto accum = [&](const Unit& t, float4 (&q)[kVPT]) {
-        // pass 1: the largest value of each float4 and of the thread
-        float smax[kVPT];
-        float tmax = -INFINITY;
+    uint32_t tau = s.warp_val[0], nf = s.warp_nf[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) { tau = min(tau, s.warp_val[w]); nf |= s.warp_nf[w]; }
+    // key >= tau  <=>  value >= thr (keys below key(-FLT_MAX) are -inf and
+    // NaN patterns: every non-NaN value passes them)
+    const float thr = tau <= kKeyMinFinite ? -INFINITY : key2f(tau);
+    // survivors: counted per thread, one shared atomic per warp for the
+    // warp's slots, then written in thread order
+    uint32_t mine = 0;
+    if (tmax >= thr) {
 #pragma unroll
         for (int sl = 0; sl < kVPT; ++sl) {
-            smax[sl] = fmaxf(fmaxf(q[sl].x, q[sl].y), fmaxf(q[sl].z, q[sl].w));
-            tmax = fmaxf(tmax, smax[sl]);
-            nfacc = __fmaf_rn(q[sl].x, 0.0f, nfacc);
-            nfacc = __fmaf_rn(q[sl].y, 0.0f, nfacc);
-            nfacc = __fmaf_rn(q[sl].z, 0.0f, nfacc);
-            nfacc = __fmaf_rn(q[sl].w, 0.0f, nfacc);
-        }
-        // The segment's first chunk sets the chunk bound: >= k of its
-        // elements have key >= tau, so no element below tau is in the
-        // segment's top k. Once a selection has left k candidates in the
-        // buffer, its k-th key bounds every later (higher-id) element too.
-        if (tau == 0 && tau_key == 0 && k <= 32u * kWarps) {
-            const uint32_t v = warp_sort_desc(f2key(tmax));
-            const uint32_t r = (k + kWarps - 1) / kWarps;
-            const uint32_t wv = __shfl_sync(kFull, v, r - 1);
-            if (lane == 0) s.warp_val[warp] = wv;
-            __syncthreads();
-            tau = s.warp_val[0];
+            if (smax[sl] >= thr) {
+                const uint32_t e = t.lo + 4u * (tid + kNT * sl);
+                const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
 #pragma unroll
-            for (int w = 1; w < kWarps; ++w) tau = min(tau, s.warp_val[w]);
+                for (int j = 0; j < 4; ++j) mine += (f[j] >= thr && e + j < t.hi) ? 1u : 0u;
+            }
         }
-        const uint32_t thr = max(max(tau, tau_key + 1u), 1u);
-        // key >= thr  <=>  value >= thr_f (keys below key(-FLT_MAX) are -inf and
-        // NaN patterns: every non-NaN value passes them)
-        const float thr_f = thr <= kKeyMinFinite ? -INFINITY : key2f(thr);
-        // pass 2: only float4s whose max reaches the threshold are examined
-        if (tmax >= thr_f) {
+    }
+    if (__any_sync(kFull, mine != 0u)) {
+        uint32_t incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += v;
+        }
+        uint32_t base = 0;
+        if (lane == 31) base = atomicAdd(&s.count, incl);
+        base = __shfl_sync(kFull, base, 31) + incl - mine;
+        if (mine) {
 #pragma unroll
             for (int sl = 0; sl < kVPT; ++sl) {
-                if (smax[sl] >= thr_f) {
+                if (smax[sl] >= thr) {
                     const uint32_t e = t.lo + 4u * (tid + kNT * sl);
                     const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        if (f[j] >= thr_f && e + j < t.hi) {
-                            const uint32_t slot = atomicAdd(&s.count, 1u);
-                            if (slot < kCap) s.buf[slot] = make_cand(f2key(f[j]), e + j);
+                        if (f[j] >= thr && e + j < t.hi) {
+                            if (base < kBlockCap) s.buf[base] = make_cand(f2key(f[j]), e + j);
+                            ++base;
                         }
                     }
                 }
             }
         }
-        __syncthreads();
-        const uint32_t now = s.count;
-        if (now > kCap) {
-            __syncthreads();
-            if (tid == 0) s.count = cnt;
-            __syncthreads();
-            overflow_chunk<kTma>(s, a.logits + static_cast<size_t>(t.row) * V, t.lo, t.hi, k, tau);
-            cnt = s.count;
-            tau_key = s.tau_key;
-        } else if (now > k + kReduceSlack) {
-            // keep the buffer small: its top k, whose k-th key filters later chunks
-            reduce_buffer(s, k);
-            cnt = s.count;
-            tau_key = s.tau_key;
-        } else {
-            cnt = now;
-        }
-    };
+    }
+    __syncthreads();
+    uint32_t n = s.count;
+    if (n > kBlockCap) {
+        radix_select_chunk<kVec>(s, a.logits + static_cast<size_t>(t.row) * V, t.lo, t.hi, k);
+        n = s.count;
+    }
+    block_select_sorted(s.buf, n, k, s.sorted);
+    const uint32_t have = n < k ? n : k;
+    uint64_t* my_list = a.lists + (static_cast<size_t>(t.row) * a.stride + t.chunk) * k;
+    for (uint32_t j = tid; j < k; j += kNT) my_list[j] = j < have ? s.sorted[j] : 0ull;
+    if (tid == 0) a.chunk_flags[static_cast<size_t>(t.row) * a.stride + t.chunk] = nf;
+}
 
-    auto flush = [&](const Segment& g) {
-        // this segment's top k, sorted
-        const uint32_t n = min(cnt, kCap);
-        block_select_sorted(s.buf, n, k, s.sorted);
-        const uint32_t have = n < k ? n : k;
-        const uint32_t nf_local = __any_sync(kFull, nfacc != 0.0f) ? 1u : 0u;
-        nfacc = 0.0f;
-        if (lane == 0) s.warp_val[warp] = nf_local;
-        __syncthreads();
-        uint32_t nf = 0;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) nf |= s.warp_val[w];
-
-        if (g.count == 1) {
-            write_row<kSample>(s, a, g.row, have, nf != 0);
-            if (tid == 0) atomicAdd(a.err + 1, 1u);  // rows finished (self-check)
-        } else {
-            // publish the sorted list (padded with empty candidates) and arrive
-            uint64_t* my_list = a.lists + (static_cast<size_t>(g.row) * a.stride + g.index) * k;
-            for (uint32_t j = tid; j < k; j += kNT) my_list[j] = j < have ? s.sorted[j] : 0ull;
-            __threadfence();
-            __syncthreads();
-            if (tid == 0) {
-                a.chunk_flags[static_cast<size_t>(g.row) * a.stride + g.index] = nf;
-                s.last = segment_arrive(&a.counters[g.row], g.count) ? 1u : 0u;
-            }
-            __syncthreads();
-            // the block that completed the row merges it now, while its
-            // next chunks are still arriving in the staging ring
-            if (s.last) finish_row<kSample>(s, a, g.row);
-        }
-        __syncthreads();
-        if (tid == 0) { s.count = 0; s.tau_key = 0; }
-        cnt = 0;
-        tau = 0;
-        tau_key = 0;
-        __syncthreads();
-    };
-
-    stream_segments<kTma, kNT, kVPT, kStages>(a.cfg, row_ptr, accum, flush, stages, full, a.err, -FLT_MAX);
+// The finishing launch: block r merges row r's lists and writes its result.
+template <bool kSample>
+__global__ void __launch_bounds__(kNT) topk_finish_kernel(TopkArgs a) {
+    __shared__ TopkShared s;
+    pdl_wait();
+    pdl_trigger();
+    const uint32_t row = blockIdx.x, k = a.k, count = a.chunks;
+    uint32_t nf = 0;
+    const int lane = threadIdx.x & 31;
+    // the flags' loads are issued before the lists' and consumed after them
+    for (uint32_t c = lane; c < count; c += 32) nf |= a.chunk_flags[static_cast<size_t>(row) * a.stride + c];
+    const uint64_t* L = a.lists + static_cast<size_t>(row) * a.stride * k;
+    merge_row_lists(s, [&](uint32_t i) { return L[i]; }, count, k, a.err);
+    nf = __reduce_or_sync(kFull, nf);
+    write_row<kSample>(s, a, row, k, nf != 0);
+    if (threadIdx.x == 0) atomicAdd(a.err + 1, 1u);  // rows finished (self-check)
 }
 
 struct TopkLayout {
@@ -646,16 +693,16 @@ struct TopkLayout {
     uint32_t stride;
 };
 
-// One list per chunk of kUnit elements (a whole row when V <= kUnit).
-uint32_t topk_chunks(uint32_t V) { return ceil_div(V, kUnit); }
+// At most one list per 1,024 elements (the smallest unit a plan uses).
+uint32_t topk_max_chunks(uint32_t V) { return ceil_div(V, kGrain); }
 
 TopkLayout topk_layout(uint32_t rows, uint32_t V, uint32_t k) {
     TopkLayout l{};
-    l.stride = topk_chunks(V);
+    l.stride = topk_max_chunks(V);
     l.counters = kWsHeaderBytes;
     l.flags = l.counters + ws_counters_bytes(rows);
     l.lists = l.flags + align_up(static_cast<size_t>(rows) * l.stride * 4u, 256);
-    l.total = l.lists + (l.stride > 1 ? static_cast<size_t>(rows) * l.stride * k * 8u : 0u);
+    l.total = l.lists + static_cast<size_t>(rows) * l.stride * k * 8u;
     return l;
 }
 
@@ -668,17 +715,13 @@ sel_status launch_topk(const float* d_logits, uint32_t rows, uint32_t V, uint32_
     if (ws_bytes < l.total) return SEL_EWORKSPACE;
     const int sms = device_sms();
     if (sms <= 0) return SEL_ECUDA;
-    constexpr size_t kDyn = stage_bytes<kNT, kVPT, kStages>();
-    static const bool attr_ok = set_dynamic_smem(topk_kernel<true, kSample>, kDyn);
-    static const int res_tma = resident_blocks_dyn(topk_kernel<true, kSample>, kNT, kDyn);
-    static const int res_sca = resident_blocks_dyn(topk_kernel<false, kSample>, kNT, 0);
-    if (!attr_ok) return SEL_ECUDA;
-    const bool tma = (reinterpret_cast<uintptr_t>(d_logits) % 16 == 0) && (V % 4 == 0);
-    const uint32_t chunks = topk_chunks(V);
-    const uint32_t ce = chunks == 1 ? static_cast<uint32_t>(align_up(V, 4)) : kUnit;
-    const uint64_t units = static_cast<uint64_t>(rows) * chunks;
-    const uint64_t slots = static_cast<uint64_t>(sms) * (tma ? res_tma : res_sca);
-    if (units > 0x7fffffffull) return SEL_EUNSUPPORTED;
+    const bool vec = (reinterpret_cast<uintptr_t>(d_logits) % 16 == 0) && (V % 4 == 0);
+    // units as large as possible while giving every SM a block (fewer,
+    // larger units mean fewer lists to merge)
+    const uint32_t ce = plan_unit(rows, V, kGrain, kUnitMax, static_cast<uint64_t>(sms));
+    const uint32_t chunks = ceil_div(V, ce);
+    const uint64_t blocks = static_cast<uint64_t>(rows) * chunks;
+    if (blocks > 0x7fffffffull) return SEL_EUNSUPPORTED;
 
     char* ws = static_cast<char*>(d_ws);
     TopkArgs a{};
@@ -691,14 +734,16 @@ sel_status launch_topk(const float* d_logits, uint32_t rows, uint32_t V, uint32_
     a.lists = reinterpret_cast<uint64_t*>(ws + l.lists);
     a.stride = l.stride;
     a.err = reinterpret_cast<uint32_t*>(ws);
-    a.cfg = StreamCfg{static_cast<uint32_t>(units), chunks, ce, V};
+    a.V = V;
+    a.chunks = chunks;
+    a.chunk_elems = ce;
     a.sa = sa;
-    const dim3 grid(static_cast<uint32_t>(units < slots ? units : slots));
-    if (tma)
-        topk_kernel<true, kSample><<<grid, kNT, kDyn, stream>>>(a);
-    else
-        topk_kernel<false, kSample><<<grid, kNT, 0, stream>>>(a);
-    return cudaGetLastError() == cudaSuccess ? SEL_OK : SEL_ECUDA;
+    const dim3 grid(static_cast<uint32_t>(blocks));
+    cudaError_t e = vec ? launch_pdl(topk_kernel<true>, grid, dim3(kNT), 0, stream, a)
+                        : launch_pdl(topk_kernel<false>, grid, dim3(kNT), 0, stream, a);
+    if (e != cudaSuccess) return SEL_ECUDA;
+    e = launch_pdl(topk_finish_kernel<kSample>, dim3(rows), dim3(kNT), 0, stream, a);
+    return e == cudaSuccess ? SEL_OK : SEL_ECUDA;
 }
 
 }  // namespace
@@ -769,6 +814,7 @@ template <bool kSample>
 __global__ void __launch_bounds__(kNT) merge_shards_kernel(ShardArgs sh, TopkArgs a) {
     __shared__ TopkShared s;
     __shared__ uint32_t s_bad;
+    pdl_wait();
     const uint32_t row = blockIdx.x;
     const uint32_t k = a.k;
     const size_t base = static_cast<size_t>(row) * sh.G * k;
@@ -822,8 +868,9 @@ extern "C" sel_status sel_merge_shards(const float* d_vals, const uint32_t* d_id
     a.k = k;
     a.out_vals = d_out_vals;
     a.out_ids = d_out_ids;
-    merge_shards_kernel<false><<<rows, kNT, 0, stream>>>(sh, a);
-    return cudaGetLastError() == cudaSuccess ? SEL_OK : SEL_ECUDA;
+    return launch_pdl(merge_shards_kernel<false>, dim3(rows), dim3(kNT), 0, stream, sh, a) == cudaSuccess
+               ? SEL_OK
+               : SEL_ECUDA;
 }
 
 extern "C" sel_status sel_sample_shards(const float* d_vals, const uint32_t* d_ids, uint32_t rows, uint32_t G,
@@ -849,8 +896,9 @@ extern "C" sel_status sel_sample_shards(const float* d_vals, const uint32_t* d_i
     a.k = k;
     a.out_ids = d_out_ids;
     a.sa = SampleArgs{d_uniforms, d_out_probs, T, p->top_p, p->min_p, p->order};
-    merge_shards_kernel<true><<<rows, kNT, 0, stream>>>(sh, a);
-    return cudaGetLastError() == cudaSuccess ? SEL_OK : SEL_ECUDA;
+    return launch_pdl(merge_shards_kernel<true>, dim3(rows), dim3(kNT), 0, stream, sh, a) == cudaSuccess
+               ? SEL_OK
+               : SEL_ECUDA;
 }
 
 // ---------------------------------------------------------------------------
@@ -878,6 +926,7 @@ SamplerLayout sampler_layout(uint32_t rows_t, uint32_t V, uint32_t k) {
 __global__ void __launch_bounds__(kNT) sampler_decide_kernel(const uint32_t* draws, const uint32_t* tokens,
                                                              uint32_t S, uint32_t K, uint32_t V,
                                                              uint32_t* accepted, uint32_t* emitted) {
+    pdl_wait();
     const uint32_t s = blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (s >= S) return;  // whole warps
     const uint32_t lane = threadIdx.x & 31u;
@@ -953,6 +1002,8 @@ extern "C" sel_status spec_accept_sampler(const float* d_target, const uint32_t*
                                            l.draws, sa, stream);
     if (st != SEL_OK) return st;
     const dim3 grid((S + kWarps - 1) / kWarps);
-    sampler_decide_kernel<<<grid, kNT, 0, stream>>>(draws, d_draft_tokens, S, K, V, d_accepted, d_emitted);
-    return cudaGetLastError() == cudaSuccess ? SEL_OK : SEL_ECUDA;
+    return launch_pdl(sampler_decide_kernel, grid, dim3(kNT), 0, stream, static_cast<const uint32_t*>(draws),
+                      d_draft_tokens, S, K, V, d_accepted, d_emitted) == cudaSuccess
+               ? SEL_OK
+               : SEL_ECUDA;
 }

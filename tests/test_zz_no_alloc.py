@@ -55,10 +55,11 @@ def test_matches_sel_argmax_on_two_calls_in_a_row(lib):
 
 
 def test_rejects_requests_beyond_the_reserved_scratch(lib):
-    rows, V = 2000, 248_320
+    rows, V = 200_000, 248_320
     need = B.sel_workspace_bytes(B.SEL_OP_ARGMAX, rows, V)
     assert need > B.SEL_NOALLOC_SCRATCH_BYTES
     fake = ctypes.c_void_p(0x10000)   # never dereferenced: the size check comes first
     assert lib.sel_argmax_noalloc(fake, rows, V, fake, None) == B.SEL_EWORKSPACE
-    assert B.sel_workspace_bytes(B.SEL_OP_ARGMAX, 538, V) <= B.SEL_NOALLOC_SCRATCH_BYTES
-    assert B.sel_workspace_bytes(B.SEL_OP_ARGMAX, 539, V) > B.SEL_NOALLOC_SCRATCH_BYTES
+    # 8 bytes per row after a 256-byte header, in 256-byte steps
+    assert B.sel_workspace_bytes(B.SEL_OP_ARGMAX, 131_040, V) <= B.SEL_NOALLOC_SCRATCH_BYTES
+    assert B.sel_workspace_bytes(B.SEL_OP_ARGMAX, 131_041, V) > B.SEL_NOALLOC_SCRATCH_BYTES
