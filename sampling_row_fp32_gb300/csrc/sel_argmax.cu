@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kNT) argmax_kernel(ArgmaxArgs a) {
     nf = lane < kNT / 32 ? s_nf[lane] : 0u;
     warp_argmax(v, i, nf);
     if (lane == 0 && (nf || i != kNoIdx))
-        atomicMax(&a.slots[t.row], nf ? kSlotNonfinite : arg_key(v, i));
+        red_max_u64(&a.slots[t.row], nf ? kSlotNonfinite : arg_key(v, i));
 }
 
 // Turn each row's slot into its id and clear the slot for the next call.

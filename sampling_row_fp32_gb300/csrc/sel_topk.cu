@@ -48,12 +48,43 @@ constexpr int kWarps = kNT / 32;
 constexpr int kVPT = 8;
 constexpr uint32_t kGrain = 4u * kNT;        // unit sizes are multiples of this
 constexpr uint32_t kUnitMax = 4u * kNT * kVPT;  // 8,192 elements per unit
-constexpr uint32_t kCap = 2048;              // merge buffer
+constexpr uint32_t kCap = 2048;              // shard-merge buffer
 constexpr uint32_t kBlockCap = SEL_MAX_K;    // a chunk's survivors before the radix path
+constexpr uint32_t kFinishBuf = 4096;        // row-merge buffer
+constexpr uint32_t kRound = kFinishBuf - SEL_MAX_K;  // list entries filtered per round
+constexpr int kRoundPer = static_cast<int>(kRound / kNT);
 constexpr uint32_t kRankMax = 512;           // rank counting up to this many candidates
 constexpr uint32_t kFastMergeLists = 32;     // one warp lane per chunk list
 
 static_assert(kBlockCap <= kCap && SEL_MAX_K <= kCap, "selection buffers");
+static_assert(kRound % kNT == 0, "whole rounds");
+
+// Entries of a chunk list: the chunk's survivors above its bound, unsorted
+// and zero-padded, or (when they would not fit) its top k.
+__host__ __device__ constexpr uint32_t list_len(uint32_t k) {
+    return k > 32u * kWarps ? k : (k + 32u > 96u ? k + 32u : 96u);
+}
+constexpr uint32_t kPool = kWarps;  // pool entries per chunk: its warp maxima
+
+// Shared memory of the main launch.
+struct alignas(16) ChunkShared {
+    uint64_t buf[kBlockCap];     // survivors
+    uint64_t sorted[SEL_MAX_K];  // selection output, descending
+    uint32_t hist[256];          // radix select
+    alignas(16) uint32_t warp_val[kWarps];
+    alignas(16) uint32_t warp_max[kWarps];
+    alignas(16) uint32_t warp_nf[kWarps];
+    uint32_t count;
+    uint32_t digit, want;        // radix select
+};
+
+// Shared memory of the finishing launch.
+struct alignas(16) FinishShared {
+    uint64_t buf[kFinishBuf];    // survivors of the row's lists
+    uint64_t sorted[SEL_MAX_K];  // the row's top k, descending
+    uint32_t bound[kWarps];
+    uint32_t count;
+};
 
 struct alignas(16) TopkShared {
     uint64_t buf[kCap];          // candidate buffer (16-byte aligned: read as pairs)
@@ -82,10 +113,11 @@ struct TopkArgs {
     uint32_t k;
     float* out_vals;         // [rows][k] (top-k)
     uint32_t* out_ids;       // [rows][k] (top-k) or [rows] (sampling)
-    uint32_t* counters;      // [rows]
+    uint32_t* row_tau;       // [rows]: the largest chunk bound (key), 0 between calls
+    uint32_t* pools;         // [rows][stride][kPool]: each chunk's warp maxima (keys), descending
     uint32_t* chunk_flags;   // [rows][stride]
-    uint64_t* lists;         // [rows][stride][k]
-    uint32_t stride;
+    uint64_t* lists;         // [rows][stride][list_len(k)]
+    uint32_t stride, list_len;
     uint32_t* err;
     uint32_t V, chunks, chunk_elems;
     SampleArgs sa;
@@ -165,8 +197,8 @@ __device__ void block_select_sorted(uint64_t* buf, uint32_t n, uint32_t k, uint6
 // walks. The chunk is read again (from L2). Leaves exactly k entries in
 // s.buf (the chunk has more than k). Block-collective; kept out of line
 // (rare).
-template <bool kVec>
-__device__ __noinline__ void radix_select_chunk(TopkShared& s, const float* row, uint32_t lo, uint32_t hi,
+template <bool kVec, class Sh>
+__device__ __noinline__ void radix_select_chunk(Sh& s, const float* row, uint32_t lo, uint32_t hi,
                                                 uint32_t k) {
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
     float4 q[kVPT];
@@ -263,12 +295,12 @@ __device__ __noinline__ void radix_select_chunk(TopkShared& s, const float* row,
     }
 }
 
-// Sampling epilogue on the sorted candidates s.sorted[0..n): one warp.
+// Sampling epilogue on the sorted candidates sorted[0..n): one warp.
 // The filter weights wf (T = 1 when temperature comes last) and draw weights
 // wd, relative to the largest candidate (weight exactly 1), are computed once
-// per candidate into the (now free) candidate buffer; the scans read them.
-__device__ void sample_epilogue(TopkShared& s, uint32_t n, uint32_t row, bool nonfinite,
-                                const SampleArgs& sa, uint32_t* out_ids) {
+// per candidate into `scratch` (2 * SEL_MAX_K floats); the scans read them.
+__device__ void sample_epilogue(const uint64_t* sorted, float* scratch, uint32_t n, uint32_t row,
+                                bool nonfinite, const SampleArgs& sa, uint32_t* out_ids) {
     const int lane = threadIdx.x & 31;
     const float u = sa.uniforms[row];
     const bool valid = !nonfinite && u >= 0.0f && u < 1.0f;
@@ -277,20 +309,20 @@ __device__ void sample_epilogue(TopkShared& s, uint32_t n, uint32_t row, bool no
         return;
     }
     if (sa.temperature == 0.0f || n == 1) {  // greedy, or a single candidate
-        if (lane == 0) { out_ids[row] = cand_id(s.sorted[0]); sa.out_probs[row] = 1.0f; }
+        if (lane == 0) { out_ids[row] = cand_id(sorted[0]); sa.out_probs[row] = 1.0f; }
         return;
     }
-    const float x0 = key2f(cand_key(s.sorted[0]));
+    const float x0 = key2f(cand_key(sorted[0]));
     const float T = sa.temperature;
     const bool temp_last = sa.order == SEL_ORDER_TEMP_LAST;
-    float* wf = reinterpret_cast<float*>(s.buf);  // [SEL_MAX_K]
+    float* wf = scratch;                          // [SEL_MAX_K]
     float* wd = wf + SEL_MAX_K;                   // [SEL_MAX_K]
     float sum_f = 0.0f;
     for (uint32_t b = 0; b < n; b += 32) {
         const uint32_t j = b + lane;
         float f = 0.0f;
         if (j < n) {
-            const float d = key2f(cand_key(s.sorted[j])) - x0;
+            const float d = key2f(cand_key(sorted[j])) - x0;
             const float w_d = expf(d / T);
             f = temp_last ? expf(d) : w_d;
             wf[j] = f;
@@ -366,7 +398,7 @@ __device__ void sample_epilogue(TopkShared& s, uint32_t n, uint32_t row, bool no
     }
     if (!found) pick_w = wd[pick];
     if (lane == 0) {
-        out_ids[row] = cand_id(s.sorted[pick]);
+        out_ids[row] = cand_id(sorted[pick]);
         sa.out_probs[row] = pick_w / sum_d;
     }
 }
@@ -544,27 +576,27 @@ __device__ void merge_row_lists(TopkShared& s, Load&& load, uint32_t chunks, uin
 }
 
 template <bool kSample>
-__device__ __forceinline__ void write_row(TopkShared& s, const TopkArgs& a, uint32_t row, uint32_t have,
-                                          bool nonfinite) {
+__device__ __forceinline__ void write_row(const uint64_t* sorted, float* scratch, const TopkArgs& a, uint32_t row,
+                                          uint32_t have, bool nonfinite) {
     const int tid = threadIdx.x;
     if constexpr (kSample) {
-        if (tid < 32) sample_epilogue(s, have, row, nonfinite, a.sa, a.out_ids);
+        if (tid < 32) sample_epilogue(sorted, scratch, have, row, nonfinite, a.sa, a.out_ids);
     } else {
         const uint32_t k = a.k;
         for (uint32_t j = tid; j < k; j += kNT) {
             const bool ok = !nonfinite && j < have;
             a.out_vals[static_cast<size_t>(row) * k + j] =
-                ok ? key2f(cand_key(s.sorted[j])) : __uint_as_float(0x7fc00000u);
-            a.out_ids[static_cast<size_t>(row) * k + j] = ok ? cand_id(s.sorted[j]) : SEL_INVALID_ID;
+                ok ? key2f(cand_key(sorted[j])) : __uint_as_float(0x7fc00000u);
+            a.out_ids[static_cast<size_t>(row) * k + j] = ok ? cand_id(sorted[j]) : SEL_INVALID_ID;
         }
     }
 }
 
-// The main launch: one block per row chunk; each stores the chunk's top k,
-// sorted (padded with empty candidates), and its nonfinite flag.
+// The main launch: one block per row chunk. Each stores its chunk list and
+// nonfinite flag, and folds its bound into the row's slot (atomic max).
 template <bool kVec>
-__global__ void __launch_bounds__(kNT, 3) topk_kernel(TopkArgs a) {
-    __shared__ TopkShared s;
+__global__ void __launch_bounds__(kNT, 4) topk_kernel(TopkArgs a) {
+    __shared__ ChunkShared s;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t V = a.V, k = a.k;
     pdl_wait();
@@ -572,125 +604,258 @@ __global__ void __launch_bounds__(kNT, 3) topk_kernel(TopkArgs a) {
     // Padding past the row end is -FLT_MAX: finite (the latch ignores it),
     // never above a real logit, and never appended (e < hi is checked).
     float4 q[kVPT];
-    load_unit<kNT, kVPT, kVec>(a.logits + static_cast<size_t>(t.row) * V, t.lo, t.hi, -FLT_MAX, q);
+    const float* rowp = a.logits + static_cast<size_t>(t.row) * V;
+    if (kVec && t.hi - t.lo == kUnitMax) {
+        // a chunk of the largest size, whole: all kVPT quads of every thread
+        // are in it
+#pragma unroll
+        for (int sl = 0; sl < kVPT; ++sl) q[sl] = ld_stream4(rowp + t.lo + 4u * (tid + kNT * sl));
+    } else {
+        load_unit<kNT, kVPT, kVec>(rowp, t.lo, t.hi, -FLT_MAX, q);
+    }
     pdl_trigger();
     if (tid == 0) s.count = 0;
 
-    // the largest value of each float4 and of the thread; the nonfinite
-    // latch (sum of x * 0 stays 0 unless some x is +-Inf or NaN)
-    float2 nfacc = make_float2(0.0f, 0.0f);
-    float smax[kVPT];
+    // the thread's largest value; the nonfinite latch (sum of x * 0 stays 0
+    // unless some x is +-Inf or NaN)
+    unsigned long long nfacc = 0ull;
+    float tmax = -INFINITY;
 #pragma unroll
     for (int sl = 0; sl < kVPT; ++sl) {
-        latch_nonfinite(nfacc, q[sl]);
-        smax[sl] = quad_max(q[sl]);
+        latch_nonfinite2(nfacc, q[sl]);
+        tmax = max3f(tmax, fmaxf(q[sl].x, q[sl].y), fmaxf(q[sl].z, q[sl].w));
     }
-    float tmax = smax[0];
-#pragma unroll
-    for (int sl = 1; sl + 1 < kVPT; sl += 2) tmax = max3f(tmax, smax[sl], smax[sl + 1]);
-    if ((kVPT & 1) == 0) tmax = fmaxf(tmax, smax[kVPT - 1]);
 
     // The chunk bound: >= k elements of the chunk have key >= tau, so no
     // element below tau is in the chunk's top k (0: no bound).
-    uint32_t wv = 0;
-    if (k <= 32u * kWarps) {
-        const uint32_t r = (k + kWarps - 1) / kWarps;
+    // Each warp's largest lane maximum joins the row's pool of distinct
+    // elements (the finishing launch bounds the row's k-th key with it).
+    uint32_t wv = 0, wmax;
+    {
         uint32_t key = f2key(tmax);
-        if (r <= 8) {
-            for (uint32_t i = 1; i < r; ++i) {  // knock out the r - 1 largest
-                const uint32_t m = __reduce_max_sync(kFull, key);
-                const uint32_t b = __ballot_sync(kFull, key == m);
-                if (lane == __ffs(b) - 1) key = 0;
+        wmax = __reduce_max_sync(kFull, key);
+        if (k <= 32u * kWarps) {
+            const uint32_t r = (k + kWarps - 1) / kWarps;
+            if (r <= 8) {
+                uint32_t m = wmax;
+                for (uint32_t i = 1; i < r; ++i) {  // knock out the r - 1 largest
+                    const uint32_t b = __ballot_sync(kFull, key == m);
+                    if (lane == __ffs(b) - 1) key = 0;
+                    m = __reduce_max_sync(kFull, key);
+                }
+                wv = m;
+            } else {
+                wv = __shfl_sync(kFull, warp_sort_desc(key), static_cast<int>(r - 1));
             }
-            wv = __reduce_max_sync(kFull, key);
-        } else {
-            wv = __shfl_sync(kFull, warp_sort_desc(key), static_cast<int>(r - 1));
         }
     }
-    const uint32_t wnf = __any_sync(kFull, nfacc.x + nfacc.y != 0.0f) ? 1u : 0u;
-    if (lane == 0) { s.warp_val[warp] = wv; s.warp_nf[warp] = wnf; }
+    const uint32_t wnf = __any_sync(kFull, !latch_clear(nfacc)) ? 1u : 0u;
+    if (lane == 0) { s.warp_val[warp] = wv; s.warp_max[warp] = wmax; s.warp_nf[warp] = wnf; }
     __syncthreads();
-    uint32_t tau = s.warp_val[0], nf = s.warp_nf[0];
+    // this chunk's pool entries (the finishing launch sorts them)
+    if (tid < static_cast<int>(kPool))
+        a.pools[(static_cast<size_t>(t.row) * a.stride + t.chunk) * kPool + tid] = s.warp_max[tid];
+    uint32_t tau = 0xFFFFFFFFu, nf = 0;
 #pragma unroll
-    for (int w = 1; w < kWarps; ++w) { tau = min(tau, s.warp_val[w]); nf |= s.warp_nf[w]; }
-    // key >= tau  <=>  value >= thr (keys below key(-FLT_MAX) are -inf and
-    // NaN patterns: every non-NaN value passes them)
-    const float thr = tau <= kKeyMinFinite ? -INFINITY : key2f(tau);
-    // survivors: counted per thread, one shared atomic per warp for the
-    // warp's slots, then written in thread order
-    uint32_t mine = 0;
-    if (tmax >= thr) {
+    for (int w = 0; w < kWarps; w += 4) {
+        const uint4 tv = *reinterpret_cast<const uint4*>(&s.warp_val[w]);
+        const uint4 nv = *reinterpret_cast<const uint4*>(&s.warp_nf[w]);
+        tau = min(min(tau, min(tv.x, tv.y)), min(tv.z, tv.w));
+        nf |= (nv.x | nv.y) | (nv.z | nv.w);
+    }
+    const uint32_t n_real = t.hi - t.lo;
+    if (tau != 0u) {
+        // key >= tau  <=>  value >= thr (keys at or below key(-FLT_MAX) are
+        // -inf and NaN patterns: every non-NaN value passes them). Per slot, a
+        // ballot finds the quads whose maximum reaches thr; lanes 0-3 test the
+        // four elements of each such quad and append the survivors.
+        const float thr = tau <= kKeyMinFinite ? -INFINITY : key2f(tau);
+        // survivors: each thread marks its own in a bit mask (bit 4 s + j;
+        // only quads whose maximum reaches thr are looked at), one shared
+        // atomic per warp reserves the warp's slots, and each thread writes
+        // its survivors in order
+        uint32_t marks = 0;
 #pragma unroll
         for (int sl = 0; sl < kVPT; ++sl) {
-            if (smax[sl] >= thr) {
+            if (quad_max(q[sl]) >= thr) {
                 const uint32_t e = t.lo + 4u * (tid + kNT * sl);
-                const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) mine += (f[j] >= thr && e + j < t.hi) ? 1u : 0u;
+                uint32_t m4 = (q[sl].x >= thr ? 1u : 0u) | (q[sl].y >= thr ? 2u : 0u) | (q[sl].z >= thr ? 4u : 0u) |
+                              (q[sl].w >= thr ? 8u : 0u);
+                if (e + 4u > t.hi) m4 &= (e < t.hi) ? (1u << (t.hi - e)) - 1u : 0u;  // the row's ragged end
+                marks |= m4 << (4 * sl);
             }
         }
-    }
-    if (__any_sync(kFull, mine != 0u)) {
+        const uint32_t mine = __popc(marks);
         uint32_t incl = mine;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const uint32_t v = __shfl_up_sync(kFull, incl, o);
             if (lane >= o) incl += v;
         }
-        uint32_t base = 0;
-        if (lane == 31) base = atomicAdd(&s.count, incl);
-        base = __shfl_sync(kFull, base, 31) + incl - mine;
-        if (mine) {
+        uint32_t slot = 0;
+        if (lane == 31 && incl) slot = atomicAdd(&s.count, incl);
+        slot = __shfl_sync(kFull, slot, 31) + incl - mine;
 #pragma unroll
-            for (int sl = 0; sl < kVPT; ++sl) {
-                if (smax[sl] >= thr) {
-                    const uint32_t e = t.lo + 4u * (tid + kNT * sl);
-                    const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        if (f[j] >= thr && e + j < t.hi) {
-                            if (base < kBlockCap) s.buf[base] = make_cand(f2key(f[j]), e + j);
-                            ++base;
-                        }
-                    }
-                }
+        for (int sl = 0; sl < kVPT; ++sl) {
+            uint32_t m4 = (marks >> (4 * sl)) & 15u;
+            const uint32_t e = t.lo + 4u * (tid + kNT * sl);
+            while (m4) {
+                const int j = __ffs(m4) - 1;
+                m4 &= m4 - 1u;
+                const float f = j == 0 ? q[sl].x : (j == 1 ? q[sl].y : (j == 2 ? q[sl].z : q[sl].w));
+                if (slot < kBlockCap) s.buf[slot] = make_cand(f2key(f), e + j);
+                ++slot;
             }
         }
+    } else if (n_real <= kBlockCap) {
+        // no bound (k beyond its reach, or too few elements): the whole chunk
+#pragma unroll
+        for (int sl = 0; sl < kVPT; ++sl) {
+            const uint32_t e = t.lo + 4u * (tid + kNT * sl);
+            const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (e + j < t.hi) s.buf[e + j - t.lo] = make_cand(f2key(f[j]), e + j);
+        }
+        if (tid == 0) s.count = n_real;
+    } else if (tid == 0) {
+        s.count = n_real;  // more than the buffer: the radix path below
     }
     __syncthreads();
     uint32_t n = s.count;
-    if (n > kBlockCap) {
-        radix_select_chunk<kVec>(s, a.logits + static_cast<size_t>(t.row) * V, t.lo, t.hi, k);
-        n = s.count;
+    const uint32_t L = a.list_len;
+    uint64_t* my_list = a.lists + (static_cast<size_t>(t.row) * a.stride + t.chunk) * L;
+    const uint64_t* src_list = s.buf;
+    if (n > L) {
+        // too many to store: the chunk's top k (exactly; ties to lower ids)
+        if (n > kBlockCap) {
+            radix_select_chunk<kVec>(s, a.logits + static_cast<size_t>(t.row) * V, t.lo, t.hi, k);
+            n = s.count;
+        }
+        block_select_sorted(s.buf, n, k, s.sorted);
+        n = k;
+        src_list = s.sorted;
+        tau = cand_key(s.sorted[k - 1]);
     }
-    block_select_sorted(s.buf, n, k, s.sorted);
-    const uint32_t have = n < k ? n : k;
-    uint64_t* my_list = a.lists + (static_cast<size_t>(t.row) * a.stride + t.chunk) * k;
-    for (uint32_t j = tid; j < k; j += kNT) my_list[j] = j < have ? s.sorted[j] : 0ull;
-    if (tid == 0) a.chunk_flags[static_cast<size_t>(t.row) * a.stride + t.chunk] = nf;
+    for (uint32_t j = tid; j < L; j += kNT) my_list[j] = j < n ? src_list[j] : 0ull;
+    if (tid == 0) {
+        a.chunk_flags[static_cast<size_t>(t.row) * a.stride + t.chunk] = nf;
+        if (tau != 0u) red_max_u32(&a.row_tau[t.row], tau);
+    }
 }
 
-// The finishing launch: block r merges row r's lists and writes its result.
+// Sort 8 values descending in registers (odd-even merge network).
+__device__ __forceinline__ void sort_desc8(uint32_t (&e)[8]) {
+    auto cs = [&](int i, int j) {
+        const uint32_t a = e[i], b = e[j];
+        e[i] = max(a, b);
+        e[j] = min(a, b);
+    };
+    cs(0, 1); cs(2, 3); cs(4, 5); cs(6, 7);
+    cs(0, 2); cs(1, 3); cs(4, 6); cs(5, 7);
+    cs(1, 2); cs(5, 6);
+    cs(0, 4); cs(1, 5); cs(2, 6); cs(3, 7);
+    cs(2, 4); cs(3, 5);
+    cs(1, 2); cs(3, 4); cs(5, 6);
+}
+
+// The finishing launch: block r keeps the entries of row r's lists whose key
+// reaches a bound B on the row's k-th key, selects the top k exactly and
+// writes the result. B is the largest of: every chunk's own bound (each
+// chunk holds k elements at or above it), and, for r = 1, 2, 4, 8, the
+// ceil(k / r)-th largest of the chunks' r-th pool entries (that many chunks
+// hold r distinct elements at or above it). Every list holds all of its
+// chunk's entries at or above the chunk's bound, or the chunk's top k, so
+// the row's top k all survive. Lists are filtered kRound entries at a time,
+// with a selection down to k between rounds when more follow.
 template <bool kSample>
 __global__ void __launch_bounds__(kNT) topk_finish_kernel(TopkArgs a) {
-    __shared__ TopkShared s;
+    __shared__ FinishShared s;
     pdl_wait();
     pdl_trigger();
-    const uint32_t row = blockIdx.x, k = a.k, count = a.chunks;
+    const uint32_t row = blockIdx.x, k = a.k, chunks = a.chunks;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t total = chunks * a.list_len;
+    const uint64_t* lists = a.lists + static_cast<size_t>(row) * a.stride * a.list_len;
+    // every load of the first round is issued before any result is used
+    uint64_t v[kRoundPer];
+#pragma unroll
+    for (int i = 0; i < kRoundPer; ++i) {
+        const uint32_t e = static_cast<uint32_t>(tid) + kNT * i;
+        v[i] = e < total ? lists[e] : 0ull;
+    }
     uint32_t nf = 0;
-    const int lane = threadIdx.x & 31;
-    // the flags' loads are issued before the lists' and consumed after them
-    for (uint32_t c = lane; c < count; c += 32) nf |= a.chunk_flags[static_cast<size_t>(row) * a.stride + c];
-    const uint64_t* L = a.lists + static_cast<size_t>(row) * a.stride * k;
-    merge_row_lists(s, [&](uint32_t i) { return L[i]; }, count, k, a.err);
+    for (uint32_t c = lane; c < chunks; c += 32) nf |= a.chunk_flags[static_cast<size_t>(row) * a.stride + c];
+    const uint32_t tau_row = a.row_tau[row];
+    uint32_t pb = 0;  // this warp's pool bound (warps 0-3: r = 1, 2, 4, 8)
+    const uint32_t pr = 1u << warp, pm = (k + pr - 1) / pr;
+    if (warp < 4 && pm <= chunks && pm <= 32u) {
+        // lane l: the largest r-th pool entry among chunks l, l + 32, ...;
+        // the pm-th largest of these is reached by pm chunks' r distinct
+        // elements
+        const uint32_t* pool = a.pools + static_cast<size_t>(row) * a.stride * kPool;
+        uint32_t v = 0;
+        for (uint32_t c = lane; c < chunks; c += 32) {
+            const uint4 lo4 = *reinterpret_cast<const uint4*>(pool + c * kPool);
+            const uint4 hi4 = *reinterpret_cast<const uint4*>(pool + c * kPool + 4);
+            uint32_t e[kPool] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
+            sort_desc8(e);
+            v = max(v, e[pr - 1]);
+        }
+        pb = __shfl_sync(kFull, warp_sort_desc(v), static_cast<int>(pm - 1));
+    }
+    if (lane == 0) s.bound[warp] = pb;
+    if (tid == 0) s.count = 0;
+    __syncthreads();
+    if (tid == 0) a.row_tau[row] = 0u;  // for the next call
+    uint32_t B = tau_row;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) B = max(B, s.bound[w]);
+    uint64_t floor_c = static_cast<uint64_t>(B) << 32;
+    for (uint32_t base = 0; base < total; base += kRound) {
+        if (base > 0) {
+#pragma unroll
+            for (int i = 0; i < kRoundPer; ++i) {
+                const uint32_t e = base + static_cast<uint32_t>(tid) + kNT * i;
+                v[i] = e < total ? lists[e] : 0ull;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kRoundPer; ++i) {
+            const bool p = v[i] != 0ull && v[i] >= floor_c;
+            const uint32_t m = __ballot_sync(kFull, p);
+            if (m) {
+                const int leader = __ffs(m) - 1;
+                uint32_t b = 0;
+                if (lane == leader) b = atomicAdd(&s.count, static_cast<uint32_t>(__popc(m)));
+                b = __shfl_sync(kFull, b, leader);
+                if (p) s.buf[b + __popc(m & lanemask_lt())] = v[i];
+            }
+        }
+        __syncthreads();
+        if (base + kRound < total && s.count > k) {
+            // keep the buffer's top k; its k-th key bounds later rounds
+            block_select_sorted(s.buf, s.count, k, s.sorted);
+            for (uint32_t i = tid; i < k; i += kNT) s.buf[i] = s.sorted[i];
+            floor_c = s.sorted[k - 1] > floor_c ? s.sorted[k - 1] : floor_c;
+            __syncthreads();
+            if (tid == 0) s.count = k;
+            __syncthreads();
+        }
+    }
+    const uint32_t n = s.count;
     nf = __reduce_or_sync(kFull, nf);
-    write_row<kSample>(s, a, row, k, nf != 0);
-    if (threadIdx.x == 0) atomicAdd(a.err + 1, 1u);  // rows finished (self-check)
+    // a row with an infinite logit can bound above its finite ones; it fails
+    // closed anyway
+    if (tid == 0 && n < k && nf == 0) atomicOr(a.err, kErrMergeShort);
+    block_select_sorted(s.buf, n, k, s.sorted);
+    write_row<kSample>(s.sorted, reinterpret_cast<float*>(s.buf), a, row, n < k ? n : k, nf != 0);
+    if (tid == 0) atomicAdd(a.err + 1, 1u);  // rows finished (self-check)
 }
 
 struct TopkLayout {
-    size_t counters, flags, lists, total;
-    uint32_t stride;
+    size_t row_tau, pools, flags, lists, total;
+    uint32_t stride, list_len;
 };
 
 // At most one list per 1,024 elements (the smallest unit a plan uses).
@@ -699,10 +864,12 @@ uint32_t topk_max_chunks(uint32_t V) { return ceil_div(V, kGrain); }
 TopkLayout topk_layout(uint32_t rows, uint32_t V, uint32_t k) {
     TopkLayout l{};
     l.stride = topk_max_chunks(V);
-    l.counters = kWsHeaderBytes;
-    l.flags = l.counters + ws_counters_bytes(rows);
+    l.list_len = list_len(k);
+    l.row_tau = kWsHeaderBytes;
+    l.pools = l.row_tau + ws_counters_bytes(rows);
+    l.flags = l.pools + align_up(static_cast<size_t>(rows) * l.stride * kPool * 4u, 256);
     l.lists = l.flags + align_up(static_cast<size_t>(rows) * l.stride * 4u, 256);
-    l.total = l.lists + static_cast<size_t>(rows) * l.stride * k * 8u;
+    l.total = l.lists + static_cast<size_t>(rows) * l.stride * l.list_len * 8u;
     return l;
 }
 
@@ -729,10 +896,12 @@ sel_status launch_topk(const float* d_logits, uint32_t rows, uint32_t V, uint32_
     a.k = k;
     a.out_vals = d_out_vals;
     a.out_ids = d_out_ids;
-    a.counters = reinterpret_cast<uint32_t*>(ws + l.counters);
+    a.row_tau = reinterpret_cast<uint32_t*>(ws + l.row_tau);
+    a.pools = reinterpret_cast<uint32_t*>(ws + l.pools);
     a.chunk_flags = reinterpret_cast<uint32_t*>(ws + l.flags);
     a.lists = reinterpret_cast<uint64_t*>(ws + l.lists);
     a.stride = l.stride;
+    a.list_len = l.list_len;
     a.err = reinterpret_cast<uint32_t*>(ws);
     a.V = V;
     a.chunks = chunks;
@@ -832,7 +1001,7 @@ __global__ void __launch_bounds__(kNT) merge_shards_kernel(ShardArgs sh, TopkArg
     };
     merge_row_lists(s, load, sh.G, k, &s_bad);
     __syncthreads();
-    write_row<kSample>(s, a, row, k, s_bad != 0u);
+    write_row<kSample>(s.sorted, reinterpret_cast<float*>(s.buf), a, row, k, s_bad != 0u);
 }
 
 sel_status check_shards(const float* d_vals, const uint32_t* d_ids, uint32_t rows, uint32_t G, uint32_t k,

@@ -77,6 +77,21 @@ __device__ __forceinline__ void latch_nonfinite(float2& acc, const float4& q) {
     asm("mov.b64 {%0, %1}, %2;" : "=f"(acc.x), "=f"(acc.y) : "l"(a));
 }
 
+// The same latch with the accumulator kept packed across calls.
+__device__ __forceinline__ void latch_nonfinite2(unsigned long long& acc, const float4& q) {
+    unsigned long long xy, zw;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(xy) : "f"(q.x), "f"(q.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(zw) : "f"(q.z), "f"(q.w));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(xy), "l"(0ull));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(zw), "l"(0ull));
+}
+// True when the packed latch saw only finite values.
+__device__ __forceinline__ bool latch_clear(unsigned long long acc) {
+    float x, y;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(acc));
+    return x + y == 0.0f;
+}
+
 // max(a, b, c) in one instruction (NaN operands are ignored, like fmaxf).
 __device__ __forceinline__ float max3f(float a, float b, float c) {
     float r;
@@ -84,6 +99,14 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
     return r;
 }
 __device__ __forceinline__ float quad_max(const float4& q) { return max3f(q.x, q.y, fmaxf(q.z, q.w)); }
+
+// Fire-and-forget atomic maxima (no value returned, nothing waits).
+__device__ __forceinline__ void red_max_u32(uint32_t* p, uint32_t v) {
+    asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_max_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 
 // Arrival of one block at its row (one thread): release this block's
 // results, take a ticket, and report whether it was the row's last (the
