@@ -593,27 +593,53 @@ __device__ __forceinline__ void write_row(const uint64_t* sorted, float* scratch
 }
 
 // The main launch: one block per row chunk. Each stores its chunk list and
-// nonfinite flag, and folds its bound into the row's slot (atomic max).
+// nonfinite flag, and folds its bound into the row's slot (atomic max). The
+// chunk is staged in shared memory (one bulk copy for aligned rows), so a
+// survivor's value is read back by its offset.
 template <bool kVec>
 __global__ void __launch_bounds__(kNT, 4) topk_kernel(TopkArgs a) {
+    extern __shared__ float4 stage[];  // the chunk: kUnitMax floats
     __shared__ ChunkShared s;
+    __shared__ uint64_t bar;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t V = a.V, k = a.k;
+    if (kVec) {
+        if (tid == 0) mbar_init(&bar, 1);
+        __syncthreads();  // the barrier is initialised before anyone polls it
+    }
     pdl_wait();
     const BlockUnit t = block_unit(a.chunks, a.chunk_elems, V);
-    // Padding past the row end is -FLT_MAX: finite (the latch ignores it),
-    // never above a real logit, and never appended (e < hi is checked).
-    float4 q[kVPT];
+    const uint32_t n_real = t.hi - t.lo;
     const float* rowp = a.logits + static_cast<size_t>(t.row) * V;
-    if (kVec && t.hi - t.lo == kUnitMax) {
-        // a chunk of the largest size, whole: all kVPT quads of every thread
-        // are in it
+    const float* sf = reinterpret_cast<const float*>(stage);
+    float4 q[kVPT];
+    if (kVec) {
+        // 16-byte aligned row, V % 4 == 0: the chunk is whole quads
+        if (tid == 0) bulk_load(stage, rowp + t.lo, n_real * 4u, &bar);
+        pdl_trigger();
+        const bool ok = mbar_wait(&bar, 0);
+        if (__syncthreads_or(!ok)) {
+            // the copy engine stopped answering: record it, wait (bounded)
+            // for the copy still in flight, and leave
+            if (tid == 0) {
+                atomicOr(a.err, kErrTimeout);
+                mbar_wait(&bar, 0);
+            }
+            return;
+        }
+        // Padding past the row end is -FLT_MAX: finite (the latch ignores
+        // it), never above a real logit, and never a survivor (e < hi).
 #pragma unroll
-        for (int sl = 0; sl < kVPT; ++sl) q[sl] = ld_stream4(rowp + t.lo + 4u * (tid + kNT * sl));
+        for (int sl = 0; sl < kVPT; ++sl) {
+            const uint32_t o = 4u * (tid + kNT * sl);
+            q[sl] = o < n_real ? stage[o / 4u] : make_float4(-FLT_MAX, -FLT_MAX, -FLT_MAX, -FLT_MAX);
+        }
     } else {
-        load_unit<kNT, kVPT, kVec>(rowp, t.lo, t.hi, -FLT_MAX, q);
+        load_unit<kNT, kVPT, false>(rowp, t.lo, t.hi, -FLT_MAX, q);
+        pdl_trigger();
+#pragma unroll
+        for (int sl = 0; sl < kVPT; ++sl) stage[tid + kNT * sl] = q[sl];
     }
-    pdl_trigger();
     if (tid == 0) s.count = 0;
 
     // the thread's largest value; the nonfinite latch (sum of x * 0 stays 0
@@ -663,26 +689,28 @@ __global__ void __launch_bounds__(kNT, 4) topk_kernel(TopkArgs a) {
         tau = min(min(tau, min(tv.x, tv.y)), min(tv.z, tv.w));
         nf |= (nv.x | nv.y) | (nv.z | nv.w);
     }
-    const uint32_t n_real = t.hi - t.lo;
     if (tau != 0u) {
         // key >= tau  <=>  value >= thr (keys at or below key(-FLT_MAX) are
-        // -inf and NaN patterns: every non-NaN value passes them). Per slot, a
-        // ballot finds the quads whose maximum reaches thr; lanes 0-3 test the
-        // four elements of each such quad and append the survivors.
+        // -inf and NaN patterns: every non-NaN value passes them)
         const float thr = tau <= kKeyMinFinite ? -INFINITY : key2f(tau);
-        // survivors: each thread marks its own in a bit mask (bit 4 s + j;
-        // only quads whose maximum reaches thr are looked at), one shared
-        // atomic per warp reserves the warp's slots, and each thread writes
-        // its survivors in order
+        // survivors: each thread marks its own in a bit mask (bit 4 s + j),
+        // one shared atomic per warp reserves the warp's slots, and each
+        // thread writes its survivors, reading their values back from the
+        // staged chunk
         uint32_t marks = 0;
 #pragma unroll
         for (int sl = 0; sl < kVPT; ++sl) {
-            if (quad_max(q[sl]) >= thr) {
-                const uint32_t e = t.lo + 4u * (tid + kNT * sl);
-                uint32_t m4 = (q[sl].x >= thr ? 1u : 0u) | (q[sl].y >= thr ? 2u : 0u) | (q[sl].z >= thr ? 4u : 0u) |
-                              (q[sl].w >= thr ? 8u : 0u);
-                if (e + 4u > t.hi) m4 &= (e < t.hi) ? (1u << (t.hi - e)) - 1u : 0u;  // the row's ragged end
-                marks |= m4 << (4 * sl);
+            const uint32_t m4 = (q[sl].x >= thr ? 1u : 0u) | (q[sl].y >= thr ? 2u : 0u) |
+                                (q[sl].z >= thr ? 4u : 0u) | (q[sl].w >= thr ? 8u : 0u);
+            marks |= m4 << (4 * sl);
+        }
+        if (n_real != kUnitMax) {
+            // the row's ragged end: offsets at or past n_real are padding
+#pragma unroll
+            for (int sl = 0; sl < kVPT; ++sl) {
+                const uint32_t o = 4u * (tid + kNT * sl);
+                const uint32_t keep = o >= n_real ? 0u : (n_real - o >= 4u ? 15u : (1u << (n_real - o)) - 1u);
+                marks &= ~((15u & ~keep) << (4 * sl));
             }
         }
         const uint32_t mine = __popc(marks);
@@ -695,17 +723,12 @@ __global__ void __launch_bounds__(kNT, 4) topk_kernel(TopkArgs a) {
         uint32_t slot = 0;
         if (lane == 31 && incl) slot = atomicAdd(&s.count, incl);
         slot = __shfl_sync(kFull, slot, 31) + incl - mine;
-#pragma unroll
-        for (int sl = 0; sl < kVPT; ++sl) {
-            uint32_t m4 = (marks >> (4 * sl)) & 15u;
-            const uint32_t e = t.lo + 4u * (tid + kNT * sl);
-            while (m4) {
-                const int j = __ffs(m4) - 1;
-                m4 &= m4 - 1u;
-                const float f = j == 0 ? q[sl].x : (j == 1 ? q[sl].y : (j == 2 ? q[sl].z : q[sl].w));
-                if (slot < kBlockCap) s.buf[slot] = make_cand(f2key(f), e + j);
-                ++slot;
-            }
+        while (marks) {
+            const uint32_t b = static_cast<uint32_t>(__ffs(marks) - 1);
+            marks &= marks - 1u;
+            const uint32_t o = 4u * (tid + kNT * (b >> 2)) + (b & 3u);
+            if (slot < kBlockCap) s.buf[slot] = make_cand(f2key(sf[o]), t.lo + o);
+            ++slot;
         }
     } else if (n_real <= kBlockCap) {
         // no bound (k beyond its reach, or too few elements): the whole chunk
@@ -908,8 +931,12 @@ sel_status launch_topk(const float* d_logits, uint32_t rows, uint32_t V, uint32_
     a.chunk_elems = ce;
     a.sa = sa;
     const dim3 grid(static_cast<uint32_t>(blocks));
-    cudaError_t e = vec ? launch_pdl(topk_kernel<true>, grid, dim3(kNT), 0, stream, a)
-                        : launch_pdl(topk_kernel<false>, grid, dim3(kNT), 0, stream, a);
+    constexpr size_t kStage = static_cast<size_t>(kUnitMax) * 4u;
+    static const bool attr_ok =
+        set_dynamic_smem(topk_kernel<true>, kStage) && set_dynamic_smem(topk_kernel<false>, kStage);
+    if (!attr_ok) return SEL_ECUDA;
+    cudaError_t e = vec ? launch_pdl(topk_kernel<true>, grid, dim3(kNT), kStage, stream, a)
+                        : launch_pdl(topk_kernel<false>, grid, dim3(kNT), kStage, stream, a);
     if (e != cudaSuccess) return SEL_ECUDA;
     e = launch_pdl(topk_finish_kernel<kSample>, dim3(rows), dim3(kNT), 0, stream, a);
     return e == cudaSuccess ? SEL_OK : SEL_ECUDA;
