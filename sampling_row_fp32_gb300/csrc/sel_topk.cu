@@ -57,7 +57,9 @@ constexpr uint32_t kRankMax = 512;           // rank counting up to this many ca
 constexpr uint32_t kFastMergeLists = 32;     // one warp lane per chunk list
 
 static_assert(kBlockCap <= kCap && SEL_MAX_K <= kCap, "selection buffers");
+static_assert(4u * SEL_MAX_K * sizeof(float) <= kCap * sizeof(uint64_t), "sampling scratch fits the merge buffer");
 static_assert(kRound % kNT == 0, "whole rounds");
+static_assert(256u * 4u + SEL_MAX_K * 8u <= kUnitMax * 4u, "rare-path buffers fit the stage");
 
 // Entries of a chunk list: the chunk's survivors above its bound, unsorted
 // and zero-padded, or (when they would not fit) its top k.
@@ -66,11 +68,11 @@ __host__ __device__ constexpr uint32_t list_len(uint32_t k) {
 }
 constexpr uint32_t kPool = kWarps;  // pool entries per chunk: its warp maxima
 
-// Shared memory of the main launch.
+// Shared memory of the main launch (the selection output and the radix
+// histogram of the rare paths live in the chunk's stage once it is no longer
+// read).
 struct alignas(16) ChunkShared {
     uint64_t buf[kBlockCap];     // survivors
-    uint64_t sorted[SEL_MAX_K];  // selection output, descending
-    uint32_t hist[256];          // radix select
     alignas(16) uint32_t warp_val[kWarps];
     alignas(16) uint32_t warp_max[kWarps];
     alignas(16) uint32_t warp_nf[kWarps];
@@ -198,14 +200,14 @@ __device__ void block_select_sorted(uint64_t* buf, uint32_t n, uint32_t k, uint6
 // s.buf (the chunk has more than k). Block-collective; kept out of line
 // (rare).
 template <bool kVec, class Sh>
-__device__ __noinline__ void radix_select_chunk(Sh& s, const float* row, uint32_t lo, uint32_t hi,
+__device__ __noinline__ void radix_select_chunk(Sh& s, uint32_t* hist, const float* row, uint32_t lo, uint32_t hi,
                                                 uint32_t k) {
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
     float4 q[kVPT];
     load_unit<kNT, kVPT, kVec>(row, lo, hi, -FLT_MAX, q);
     uint32_t prefix = 0, mask = 0, want = k;
     for (int shift = 24; shift >= 0; shift -= 8) {
-        for (uint32_t i = tid; i < 256u; i += kNT) s.hist[i] = 0;
+        for (uint32_t i = tid; i < 256u; i += kNT) hist[i] = 0;
         __syncthreads();
 #pragma unroll
         for (int sl = 0; sl < kVPT; ++sl) {
@@ -214,7 +216,7 @@ __device__ __noinline__ void radix_select_chunk(Sh& s, const float* row, uint32_
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const uint32_t key = f2key(f[j]);
-                if (e + j < hi && (key & mask) == prefix) atomicAdd(&s.hist[(key >> shift) & 255u], 1u);
+                if (e + j < hi && (key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
             }
         }
         __syncthreads();
@@ -222,7 +224,7 @@ __device__ __noinline__ void radix_select_chunk(Sh& s, const float* row, uint32_
             // lane l holds digits 255 - 8 l .. 248 - 8 l; suffix sums from the top
             uint32_t c[8], sum = 0;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) { c[i] = s.hist[255u - 8u * lane - i]; sum += c[i]; }
+            for (int i = 0; i < 8; ++i) { c[i] = hist[255u - 8u * lane - i]; sum += c[i]; }
             uint32_t incl = sum;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -296,60 +298,66 @@ __device__ __noinline__ void radix_select_chunk(Sh& s, const float* row, uint32_
 }
 
 // Sampling epilogue on the sorted candidates sorted[0..n): one warp.
-// The filter weights wf (T = 1 when temperature comes last) and draw weights
-// wd, relative to the largest candidate (weight exactly 1), are computed once
-// per candidate into `scratch` (2 * SEL_MAX_K floats); the scans read them.
-__device__ void sample_epilogue(const uint64_t* sorted, float* scratch, uint32_t n, uint32_t row,
-                                bool nonfinite, const SampleArgs& sa, uint32_t* out_ids) {
+// One pass computes, per candidate j, the filter weight wf_j (T = 1 when
+// temperature comes last) and draw weight wd_j relative to the largest
+// candidate (weight exactly 1), and their inclusive prefix sums pf, pd (kept
+// in `scratch`, 4 * SEL_MAX_K floats). Then: top-p keeps the shortest prefix
+// with pf >= top_p * pf_total; min-p keeps wf_j >= min_p (wf is
+// non-increasing, so the survivors stay a prefix); the draw takes the first j
+// of the prefix with u * pd_end < pd_j.
+// `live` false: compute but write nothing (see warm_finish).
+__device__ void sample_epilogue(const uint64_t* sorted, float* scratch, uint32_t n, uint32_t row, float u,
+                                bool nonfinite, const SampleArgs& sa, uint32_t* out_ids, bool live = true) {
     const int lane = threadIdx.x & 31;
-    const float u = sa.uniforms[row];
     const bool valid = !nonfinite && u >= 0.0f && u < 1.0f;
     if (!valid) {
-        if (lane == 0) { out_ids[row] = SEL_INVALID_ID; sa.out_probs[row] = __uint_as_float(0x7fc00000u); }
+        if (live && lane == 0) { out_ids[row] = SEL_INVALID_ID; sa.out_probs[row] = __uint_as_float(0x7fc00000u); }
         return;
     }
     if (sa.temperature == 0.0f || n == 1) {  // greedy, or a single candidate
-        if (lane == 0) { out_ids[row] = cand_id(sorted[0]); sa.out_probs[row] = 1.0f; }
+        if (live && lane == 0) { out_ids[row] = cand_id(sorted[0]); sa.out_probs[row] = 1.0f; }
         return;
     }
     const float x0 = key2f(cand_key(sorted[0]));
     const float T = sa.temperature;
     const bool temp_last = sa.order == SEL_ORDER_TEMP_LAST;
-    float* wf = scratch;                          // [SEL_MAX_K]
-    float* wd = wf + SEL_MAX_K;                   // [SEL_MAX_K]
-    float sum_f = 0.0f;
+    float* wf = scratch;                 // [SEL_MAX_K]
+    float* wd = wf + SEL_MAX_K;          // [SEL_MAX_K]
+    float* pf = wd + SEL_MAX_K;          // [SEL_MAX_K]
+    float* pd = pf + SEL_MAX_K;          // [SEL_MAX_K]
+    float cf = 0.0f, cd = 0.0f;          // carries into the next group of 32
     for (uint32_t b = 0; b < n; b += 32) {
         const uint32_t j = b + lane;
-        float f = 0.0f;
+        float f = 0.0f, w = 0.0f;
         if (j < n) {
             const float d = key2f(cand_key(sorted[j])) - x0;
-            const float w_d = expf(d / T);
-            f = temp_last ? expf(d) : w_d;
+            w = expf(d / T);
+            f = temp_last ? expf(d) : w;
             wf[j] = f;
-            wd[j] = w_d;
+            wd[j] = w;
         }
 #pragma unroll
-        for (int m = 16; m > 0; m >>= 1) f += __shfl_xor_sync(kFull, f, m);
-        sum_f += f;
+        for (int m = 1; m < 32; m <<= 1) {
+            const float of = __shfl_up_sync(kFull, f, m);
+            const float od = __shfl_up_sync(kFull, w, m);
+            if (lane >= m) { f += of; w += od; }
+        }
+        f += cf;
+        w += cd;
+        if (j < n) { pf[j] = f; pd[j] = w; }
+        cf = __shfl_sync(kFull, f, 31);
+        cd = __shfl_sync(kFull, w, 31);
     }
     __syncwarp();
     // top-p: the shortest prefix whose cumulative P reaches top_p
     uint32_t ns = n;
     if (sa.top_p < 1.0f) {
-        float cum = 0.0f;
+        const float need = sa.top_p * pf[n - 1];
         ns = 0;
         for (uint32_t b = 0; b < n && ns == 0; b += 32) {
             const uint32_t j = b + lane;
-            float incl = j < n ? wf[j] / sum_f : 0.0f;
-#pragma unroll
-            for (int m = 1; m < 32; m <<= 1) {
-                const float o = __shfl_up_sync(kFull, incl, m);
-                if (lane >= m) incl += o;
-            }
-            incl += cum;
-            const uint32_t hit = __ballot_sync(kFull, j < n && incl >= sa.top_p);
+            const uint32_t hit = __ballot_sync(kFull, j < n && pf[j] >= need);
             if (hit) ns = b + __ffs(hit);
-            cum = __shfl_sync(kFull, incl, 31);
         }
         if (ns == 0) ns = n;  // rounding kept the total below top_p
     }
@@ -358,48 +366,27 @@ __device__ void sample_epilogue(const uint64_t* sorted, float* scratch, uint32_t
         uint32_t keep = 1;
         for (uint32_t b = 0; b < ns; b += 32) {
             const uint32_t j = b + lane;
-            const bool ok = j < ns && j > 0 && wf[j] >= sa.min_p;
-            const uint32_t m = __ballot_sync(kFull, ok);
+            const uint32_t m = __ballot_sync(kFull, j < ns && j > 0 && wf[j] >= sa.min_p);
             if (m) keep = b + 32 - __clz(m);  // survivors form a prefix
         }
         ns = keep;
     }
-    // renormalise the draw weights over the survivors and invert the CDF
-    float sum_d = 0.0f;
+    // the draw over the survivors, renormalised by their total
+    const float total = pd[ns - 1];
+    const float target = u * total;
+    uint32_t pick = ns - 1;  // rounding: no crossing, the last survivor
     for (uint32_t b = 0; b < ns; b += 32) {
         const uint32_t j = b + lane;
-        float t = j < ns ? wd[j] : 0.0f;
-#pragma unroll
-        for (int m = 16; m > 0; m >>= 1) t += __shfl_xor_sync(kFull, t, m);
-        sum_d += t;
-    }
-    uint32_t pick = ns - 1;
-    float pick_w = 0.0f;
-    bool found = false;
-    float cum = 0.0f;
-    for (uint32_t b = 0; b < ns && !found; b += 32) {
-        const uint32_t j = b + lane;
-        const float w = j < ns ? wd[j] : 0.0f;
-        float incl = w;
-#pragma unroll
-        for (int m = 1; m < 32; m <<= 1) {
-            const float o = __shfl_up_sync(kFull, incl, m);
-            if (lane >= m) incl += o;
-        }
-        incl += cum;
-        const uint32_t hit = __ballot_sync(kFull, j < ns && u < incl / sum_d);
+        const uint32_t hit = __ballot_sync(kFull, j < ns && target < pd[j]);
         if (hit) {
-            const int l = __ffs(hit) - 1;
-            pick = b + l;
-            pick_w = __shfl_sync(kFull, w, l);
-            found = true;
+            pick = b + __ffs(hit) - 1;
+            break;
         }
-        cum = __shfl_sync(kFull, incl, 31);
     }
-    if (!found) pick_w = wd[pick];
-    if (lane == 0) {
+    const float prob = wd[pick] / total;
+    if (live && lane == 0) {
         out_ids[row] = cand_id(sorted[pick]);
-        sa.out_probs[row] = pick_w / sum_d;
+        sa.out_probs[row] = prob;
     }
 }
 
@@ -580,7 +567,7 @@ __device__ __forceinline__ void write_row(const uint64_t* sorted, float* scratch
                                           uint32_t have, bool nonfinite) {
     const int tid = threadIdx.x;
     if constexpr (kSample) {
-        if (tid < 32) sample_epilogue(sorted, scratch, have, row, nonfinite, a.sa, a.out_ids);
+        if (tid < 32) sample_epilogue(sorted, scratch, have, row, a.sa.uniforms[row], nonfinite, a.sa, a.out_ids);
     } else {
         const uint32_t k = a.k;
         for (uint32_t j = tid; j < k; j += kNT) {
@@ -597,7 +584,7 @@ __device__ __forceinline__ void write_row(const uint64_t* sorted, float* scratch
 // chunk is staged in shared memory (one bulk copy for aligned rows), so a
 // survivor's value is read back by its offset.
 template <bool kVec>
-__global__ void __launch_bounds__(kNT, 4) topk_kernel(TopkArgs a) {
+__global__ void __launch_bounds__(kNT, 5) topk_kernel(TopkArgs a) {
     extern __shared__ float4 stage[];  // the chunk: kUnitMax floats
     __shared__ ChunkShared s;
     __shared__ uint64_t bar;
@@ -612,7 +599,6 @@ __global__ void __launch_bounds__(kNT, 4) topk_kernel(TopkArgs a) {
     const uint32_t n_real = t.hi - t.lo;
     const float* rowp = a.logits + static_cast<size_t>(t.row) * V;
     const float* sf = reinterpret_cast<const float*>(stage);
-    float4 q[kVPT];
     if (kVec) {
         // 16-byte aligned row, V % 4 == 0: the chunk is whole quads
         if (tid == 0) bulk_load(stage, rowp + t.lo, n_real * 4u, &bar);
@@ -627,14 +613,8 @@ __global__ void __launch_bounds__(kNT, 4) topk_kernel(TopkArgs a) {
             }
             return;
         }
-        // Padding past the row end is -FLT_MAX: finite (the latch ignores
-        // it), never above a real logit, and never a survivor (e < hi).
-#pragma unroll
-        for (int sl = 0; sl < kVPT; ++sl) {
-            const uint32_t o = 4u * (tid + kNT * sl);
-            q[sl] = o < n_real ? stage[o / 4u] : make_float4(-FLT_MAX, -FLT_MAX, -FLT_MAX, -FLT_MAX);
-        }
     } else {
+        float4 q[kVPT];
         load_unit<kNT, kVPT, false>(rowp, t.lo, t.hi, -FLT_MAX, q);
         pdl_trigger();
 #pragma unroll
@@ -642,14 +622,23 @@ __global__ void __launch_bounds__(kNT, 4) topk_kernel(TopkArgs a) {
     }
     if (tid == 0) s.count = 0;
 
-    // the thread's largest value; the nonfinite latch (sum of x * 0 stays 0
-    // unless some x is +-Inf or NaN)
+    // The thread's largest value and the nonfinite latch (sum of x * 0 stays
+    // 0 unless some x is +-Inf or NaN), one quad at a time from the stage.
+    // Offsets at or past n_real (the row's ragged end, aligned rows only)
+    // hold no data: they are skipped.
     unsigned long long nfacc = 0ull;
     float tmax = -INFINITY;
+    float qmax[kVPT];  // each quad's largest value
+    const bool whole = !kVec || n_real == kUnitMax;
 #pragma unroll
     for (int sl = 0; sl < kVPT; ++sl) {
-        latch_nonfinite2(nfacc, q[sl]);
-        tmax = max3f(tmax, fmaxf(q[sl].x, q[sl].y), fmaxf(q[sl].z, q[sl].w));
+        qmax[sl] = -INFINITY;
+        if (whole || 4u * (tid + kNT * sl) < n_real) {
+            const float4 q = stage[tid + kNT * sl];
+            latch_nonfinite2(nfacc, q);
+            qmax[sl] = quad_max(q);
+            tmax = fmaxf(tmax, qmax[sl]);
+        }
     }
 
     // The chunk bound: >= k elements of the chunk have key >= tau, so no
@@ -697,21 +686,21 @@ __global__ void __launch_bounds__(kNT, 4) topk_kernel(TopkArgs a) {
         // one shared atomic per warp reserves the warp's slots, and each
         // thread writes its survivors, reading their values back from the
         // staged chunk
+        // only the quads whose maximum reaches thr are read again
+        uint32_t hits = 0;
+#pragma unroll
+        for (int sl = 0; sl < kVPT; ++sl) hits |= (qmax[sl] >= thr ? 1u : 0u) << sl;
         uint32_t marks = 0;
-#pragma unroll
-        for (int sl = 0; sl < kVPT; ++sl) {
-            const uint32_t m4 = (q[sl].x >= thr ? 1u : 0u) | (q[sl].y >= thr ? 2u : 0u) |
-                                (q[sl].z >= thr ? 4u : 0u) | (q[sl].w >= thr ? 8u : 0u);
-            marks |= m4 << (4 * sl);
-        }
-        if (n_real != kUnitMax) {
-            // the row's ragged end: offsets at or past n_real are padding
-#pragma unroll
-            for (int sl = 0; sl < kVPT; ++sl) {
-                const uint32_t o = 4u * (tid + kNT * sl);
-                const uint32_t keep = o >= n_real ? 0u : (n_real - o >= 4u ? 15u : (1u << (n_real - o)) - 1u);
-                marks &= ~((15u & ~keep) << (4 * sl));
-            }
+        while (hits) {
+            const uint32_t sl = static_cast<uint32_t>(__ffs(hits) - 1);
+            hits &= hits - 1u;
+            const uint32_t o = 4u * (tid + kNT * sl);
+            const float4 q = stage[o / 4u];
+            uint32_t m4 = (q.x >= thr ? 1u : 0u) | (q.y >= thr ? 2u : 0u) | (q.z >= thr ? 4u : 0u) |
+                          (q.w >= thr ? 8u : 0u);
+            // the row's ragged end (scalar rows: the padding is -FLT_MAX)
+            if (o + 4u > n_real) m4 &= o < n_real ? (1u << (n_real - o)) - 1u : 0u;
+            marks |= m4 << (4u * sl);
         }
         const uint32_t mine = __popc(marks);
         uint32_t incl = mine;
@@ -732,14 +721,7 @@ __global__ void __launch_bounds__(kNT, 4) topk_kernel(TopkArgs a) {
         }
     } else if (n_real <= kBlockCap) {
         // no bound (k beyond its reach, or too few elements): the whole chunk
-#pragma unroll
-        for (int sl = 0; sl < kVPT; ++sl) {
-            const uint32_t e = t.lo + 4u * (tid + kNT * sl);
-            const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (e + j < t.hi) s.buf[e + j - t.lo] = make_cand(f2key(f[j]), e + j);
-        }
+        for (uint32_t o = tid; o < n_real; o += kNT) s.buf[o] = make_cand(f2key(sf[o]), t.lo + o);
         if (tid == 0) s.count = n_real;
     } else if (tid == 0) {
         s.count = n_real;  // more than the buffer: the radix path below
@@ -750,21 +732,39 @@ __global__ void __launch_bounds__(kNT, 4) topk_kernel(TopkArgs a) {
     uint64_t* my_list = a.lists + (static_cast<size_t>(t.row) * a.stride + t.chunk) * L;
     const uint64_t* src_list = s.buf;
     if (n > L) {
-        // too many to store: the chunk's top k (exactly; ties to lower ids)
+        // too many to store: the chunk's top k (exactly; ties to lower ids);
+        // the stage is free now (its survivors are in s.buf)
+        uint32_t* hist = reinterpret_cast<uint32_t*>(stage);
+        uint64_t* sorted = reinterpret_cast<uint64_t*>(stage) + 256;
         if (n > kBlockCap) {
-            radix_select_chunk<kVec>(s, a.logits + static_cast<size_t>(t.row) * V, t.lo, t.hi, k);
+            radix_select_chunk<kVec>(s, hist, a.logits + static_cast<size_t>(t.row) * V, t.lo, t.hi, k);
             n = s.count;
         }
-        block_select_sorted(s.buf, n, k, s.sorted);
+        block_select_sorted(s.buf, n, k, sorted);
         n = k;
-        src_list = s.sorted;
-        tau = cand_key(s.sorted[k - 1]);
+        src_list = sorted;
+        tau = cand_key(sorted[k - 1]);
     }
     for (uint32_t j = tid; j < L; j += kNT) my_list[j] = j < n ? src_list[j] : 0ull;
     if (tid == 0) {
         a.chunk_flags[static_cast<size_t>(t.row) * a.stride + t.chunk] = nf;
         if (tau != 0u) red_max_u32(&a.row_tau[t.row], tau);
     }
+}
+
+// The m-th largest (1 <= m <= 32) of the warp's 32 values: each lane counts
+// the lanes that rank above it (larger, or equal at a lower lane) with 32
+// independent shuffles; the lane of rank m - 1 holds the answer.
+__device__ __forceinline__ uint32_t warp_kth_largest(uint32_t v, uint32_t m) {
+    const uint32_t lane = threadIdx.x & 31u;
+    uint32_t rank = 0;
+#pragma unroll
+    for (uint32_t i = 0; i < 32u; ++i) {
+        const uint32_t o = __shfl_sync(kFull, v, static_cast<int>(i));
+        rank += (o > v || (o == v && i < lane)) ? 1u : 0u;
+    }
+    const uint32_t hit = __ballot_sync(kFull, rank == m - 1u);
+    return __shfl_sync(kFull, v, __ffs(hit) - 1);
 }
 
 // Sort 8 values descending in registers (odd-even merge network).
@@ -791,9 +791,26 @@ __device__ __forceinline__ void sort_desc8(uint32_t (&e)[8]) {
 // chunk's entries at or above the chunk's bound, or the chunk's top k, so
 // the row's top k all survive. Lists are filtered kRound entries at a time,
 // with a selection down to k between rounds when more follow.
+// Run the selection and sampling code once on synthetic candidates in
+// shared memory, writing nothing: the finishing blocks start (programmatic
+// dependent launch) while the main launch still runs, and this brings their
+// instructions into the SM's caches before the real data can arrive. Touches
+// no global memory.
+template <bool kSample>
+__device__ void warm_finish(FinishShared& s, const TopkArgs& a) {
+    const uint32_t k = a.k, n = k + 16u;
+    for (uint32_t i = threadIdx.x; i < n; i += kNT) s.buf[i] = make_cand(f2key(-0.25f * static_cast<float>(i)), i);
+    __syncthreads();
+    block_select_sorted(s.buf, n, k, s.sorted);
+    if (kSample && threadIdx.x < 32)
+        sample_epilogue(s.sorted, reinterpret_cast<float*>(s.buf), k, 0, 0.5f, false, a.sa, nullptr, false);
+    __syncthreads();
+}
+
 template <bool kSample>
 __global__ void __launch_bounds__(kNT) topk_finish_kernel(TopkArgs a) {
     __shared__ FinishShared s;
+    warm_finish<kSample>(s, a);
     pdl_wait();
     pdl_trigger();
     const uint32_t row = blockIdx.x, k = a.k, chunks = a.chunks;
@@ -825,7 +842,7 @@ __global__ void __launch_bounds__(kNT) topk_finish_kernel(TopkArgs a) {
             sort_desc8(e);
             v = max(v, e[pr - 1]);
         }
-        pb = __shfl_sync(kFull, warp_sort_desc(v), static_cast<int>(pm - 1));
+        pb = warp_kth_largest(v, pm);
     }
     if (lane == 0) s.bound[warp] = pb;
     if (tid == 0) s.count = 0;
@@ -843,17 +860,23 @@ __global__ void __launch_bounds__(kNT) topk_finish_kernel(TopkArgs a) {
                 v[i] = e < total ? lists[e] : 0ull;
             }
         }
+        // survivors: counted per thread, one shared atomic per warp
+        uint32_t mine = 0;
 #pragma unroll
-        for (int i = 0; i < kRoundPer; ++i) {
-            const bool p = v[i] != 0ull && v[i] >= floor_c;
-            const uint32_t m = __ballot_sync(kFull, p);
-            if (m) {
-                const int leader = __ffs(m) - 1;
-                uint32_t b = 0;
-                if (lane == leader) b = atomicAdd(&s.count, static_cast<uint32_t>(__popc(m)));
-                b = __shfl_sync(kFull, b, leader);
-                if (p) s.buf[b + __popc(m & lanemask_lt())] = v[i];
-            }
+        for (int i = 0; i < kRoundPer; ++i) mine += (v[i] != 0ull && v[i] >= floor_c) ? 1u : 0u;
+        uint32_t incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += t;
+        }
+        uint32_t slot = 0;
+        if (lane == 31 && incl) slot = atomicAdd(&s.count, incl);
+        slot = __shfl_sync(kFull, slot, 31) + incl - mine;
+        if (mine) {
+#pragma unroll
+            for (int i = 0; i < kRoundPer; ++i)
+                if (v[i] != 0ull && v[i] >= floor_c) s.buf[slot++] = v[i];
         }
         __syncthreads();
         if (base + kRound < total && s.count > k) {
