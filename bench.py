@@ -181,8 +181,9 @@ def gpu_arm(args, rank, world, local_rank):
             B.spec_accept(target_view(copy_for(step, 4)), None, tok, arg, None, None, acc2, emi2, ws_g)
 
     # argmax, top-k, sample and the argmax rule: a main launch and a finishing
-    # launch each; the rejection rule: phase 1, its finishing launch, the draw
-    launches_per_step = 11
+    # launch each; the rejection rule: phase 1, its finishing launch, and the
+    # draw's sum and find launches
+    launches_per_step = 12
     bytes_per_op = [ROWS * ROW_BYTES, ROWS * ROW_BYTES, ROWS * ROW_BYTES,
                     None, ROWS * ROW_BYTES]
 

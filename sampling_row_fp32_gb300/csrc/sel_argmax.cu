@@ -125,37 +125,40 @@ __global__ void __launch_bounds__(kNT) argmax_kernel(ArgmaxArgs a) {
         }
     }
 
-    // Four independent (value, quad start) chains, one per lane of the
-    // float4, so the compare-select chains overlap; ids rise along each
-    // chain, so '>' keeps the lowest. The id is quad start + lane.
-    float best[4] = {q[0].x, q[0].y, q[0].z, q[0].w};
-    uint32_t bbase[4];
-    {
-        const uint32_t e0 = t.lo + 4u * tid;
+    // The thread's max, then the first quad holding it: ids rise with the
+    // slot and the lane, so that is the lowest id of the max. Quads at or
+    // past hi are padding and never count; in the last, partial quad of an
+    // unaligned row the lanes past hi are skipped.
+    float qm[kVPT];
+    float v = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) bbase[j] = e0;
-    }
-#pragma unroll
-    for (int s = 1; s < kVPT; ++s) {
+    for (int s = 0; s < kVPT; ++s) {
         const uint32_t e = t.lo + 4u * (tid + kNT * s);
-        const float f[4] = {q[s].x, q[s].y, q[s].z, q[s].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if (f[j] > best[j]) {
-                best[j] = f[j];
-                bbase[j] = e;
+        qm[s] = -INFINITY;
+        if (e < t.hi) {
+            float4 r = q[s];
+            if (!kVec && e + 4u > t.hi) {
+                if (e + 1u >= t.hi) r.y = -INFINITY;
+                if (e + 2u >= t.hi) r.z = -INFINITY;
+                if (e + 3u >= t.hi) r.w = -INFINITY;
+                q[s] = r;
             }
+            qm[s] = quad_max(r);
         }
+        v = fmaxf(v, qm[s]);
+    }
+    uint32_t i = kNoIdx;
+    if (v > -INFINITY) {
+        int hit = kVPT - 1;
+#pragma unroll
+        for (int s = kVPT - 2; s >= 0; --s) hit = qm[s] == v ? s : hit;
+        float4 qq = q[0];
+#pragma unroll
+        for (int s = 1; s < kVPT; ++s) qq = s == hit ? q[s] : qq;
+        const uint32_t j = qq.x == v ? 0u : (qq.y == v ? 1u : (qq.z == v ? 2u : 3u));
+        i = t.lo + 4u * (tid + kNT * static_cast<uint32_t>(hit)) + j;
     }
     uint32_t nf = (nfacc.x + nfacc.y == 0.0f) ? 0u : kNonfiniteBit;
-    float v = -INFINITY;
-    uint32_t i = kNoIdx;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t id = bbase[j] + j;
-        // ids at or past hi are padding, whatever their value
-        if (id < t.hi && beats(best[j], id, v, i)) { v = best[j]; i = id; }
-    }
     // -inf never wins: a real -inf fails the row closed, and an excluded id
     // is no candidate (a row whose ids are all excluded has no answer)
     if (nf || !(v > -INFINITY)) { v = -INFINITY; i = kNoIdx; }

@@ -219,29 +219,6 @@ __device__ void decide_sequence(const SpecArgs& a, uint32_t s, const ChainPre& p
     }
 }
 
-// Two fp32 lanes at once (packed f32x2 arithmetic, round to nearest).
-__device__ __forceinline__ unsigned long long pk(float x, float y) {
-    unsigned long long r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
-    return r;
-}
-__device__ __forceinline__ float2 unpk(unsigned long long r) {
-    float2 v;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
-    return v;
-}
-// ((x - m) * c) for two lanes: the difference first, so a value at the
-// maximum gets exactly 2^0 = 1
-__device__ __forceinline__ float2 scaled_diff2(float x, float y, unsigned long long neg_m, unsigned long long c2) {
-    unsigned long long d = pk(x, y);
-    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(d) : "l"(neg_m));
-    asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(d) : "l"(c2));
-    return unpk(d);
-}
-__device__ __forceinline__ void acc2(unsigned long long& acc, float x, float y) {
-    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(acc) : "l"(pk(x, y)));
-}
-
 // Phase 1: per-row (max, sum exp) or (max, argmax); per-sequence decision.
 // One block per row chunk.
 template <bool kVec, bool kRej>
@@ -285,53 +262,78 @@ __global__ void __launch_bounds__(kNT) spec_phase1_kernel(SpecArgs a) {
     float thread_s = 0.0f;
     const float c = a.log2e_over_T;
     if (kRej) {
-        // the thread's max, then sum of 2^((x - M) c) = exp((x - M) / T),
-        // two lanes at a time; padding weighs 2^-inf = 0
+        // The thread's max M, then sum of 2^((x - M) c) = exp((x - M) / T).
+        // With M c = h + l (h = the float nearest M c, l its rounding error,
+        // exact through fmaf), 2^(x c - M c) = 2^(fmaf(x, c, -h)) * 2^(-l):
+        // one fused multiply-add per logit, and the common factor 2^(-l) once
+        // per thread. A logit equal to M gets 2^(l) * 2^(-l) = 1 up to the
+        // exp2 approximation. That needs |l| small: it is at most half an ulp
+        // of h, so below 2^23 it is at most 0.5; a thread whose |M c| is
+        // larger (masked logits such as -1e30) takes the difference first.
+        // Padding (-inf) weighs 2^-inf = 0.
         float m = quad_max(q[0]);
 #pragma unroll
         for (int sl = 1; sl < kVPT; ++sl) m = max3f(m, fmaxf(q[sl].x, q[sl].y), fmaxf(q[sl].z, q[sl].w));
         bm = m;
-        const float nm = m > -INFINITY ? -m : 0.0f;  // a padding-only thread sums zeros
-        const unsigned long long neg_m = pk(nm, nm), c2 = pk(c, c);
-        unsigned long long acc0 = 0ull, acc1 = 0ull;
+        if (m > -INFINITY) {  // a padding-only thread sums nothing
+            const float h = m * c;
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (fabsf(h) < 8388608.0f) {
+                const float l = __fmaf_rn(m, c, -h);
 #pragma unroll
-        for (int sl = 0; sl < kVPT; ++sl) {
-            const float2 xy = scaled_diff2(q[sl].x, q[sl].y, neg_m, c2);
-            const float2 zw = scaled_diff2(q[sl].z, q[sl].w, neg_m, c2);
-            acc2(acc0, ex2_approx(xy.x), ex2_approx(xy.y));
-            acc2(acc1, ex2_approx(zw.x), ex2_approx(zw.y));
-        }
-        const float2 s0 = unpk(acc0), s1 = unpk(acc1);
-        thread_s = (s0.x + s0.y) + (s1.x + s1.y);
-    } else {
-        // four independent (max, quad start) chains, one per lane of the
-        // float4; ids rise along each chain, so '>' keeps the lowest
-        float best[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        uint32_t bbase[4] = {kNoIdx, kNoIdx, kNoIdx, kNoIdx};
-#pragma unroll
-        for (int sl = 0; sl < kVPT; ++sl) {
-            const uint32_t e = t.lo + 4u * (tid + kNT * sl);
-            const float f[4] = {q[sl].x, q[sl].y, q[sl].z, q[sl].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (f[j] > best[j]) {
-                    best[j] = f[j];
-                    bbase[j] = e;
+                for (int sl = 0; sl < kVPT; ++sl) {
+                    acc[0] += ex2_approx(__fmaf_rn(q[sl].x, c, -h));
+                    acc[1] += ex2_approx(__fmaf_rn(q[sl].y, c, -h));
+                    acc[2] += ex2_approx(__fmaf_rn(q[sl].z, c, -h));
+                    acc[3] += ex2_approx(__fmaf_rn(q[sl].w, c, -h));
                 }
+                thread_s = ((acc[0] + acc[1]) + (acc[2] + acc[3])) * ex2_approx(-l);
+            } else {
+#pragma unroll
+                for (int sl = 0; sl < kVPT; ++sl) {
+                    acc[0] += ex2_approx((q[sl].x - m) * c);
+                    acc[1] += ex2_approx((q[sl].y - m) * c);
+                    acc[2] += ex2_approx((q[sl].z - m) * c);
+                    acc[3] += ex2_approx((q[sl].w - m) * c);
+                }
+                thread_s = (acc[0] + acc[1]) + (acc[2] + acc[3]);
             }
         }
+    } else {
+        // the thread's max, then the first quad holding it (ids rise with
+        // the slot and the lane, so that is the lowest id of the max);
+        // padding (-inf) never wins
+        float qm[kVPT];
+        float m = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t id = bbase[j] == kNoIdx ? kNoIdx : bbase[j] + j;
-            if (beats(best[j], id, bm, bi)) { bm = best[j]; bi = id; }
+        for (int sl = 0; sl < kVPT; ++sl) {
+            qm[sl] = quad_max(q[sl]);
+            m = fmaxf(m, qm[sl]);
+        }
+        if (m > -INFINITY) {
+            int hit = kVPT - 1;
+#pragma unroll
+            for (int sl = kVPT - 2; sl >= 0; --sl) hit = qm[sl] == m ? sl : hit;
+            float4 qq = q[0];
+#pragma unroll
+            for (int sl = 1; sl < kVPT; ++sl) qq = sl == hit ? q[sl] : qq;
+            const uint32_t j = qq.x == m ? 0u : (qq.y == m ? 1u : (qq.z == m ? 2u : 3u));
+            bm = m;
+            bi = t.lo + 4u * (tid + kNT * static_cast<uint32_t>(hit)) + j;
         }
     }
     const float thread_m = bm;
+    if (kRej) {
+        // the chunk's max (no ids in this rule)
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(kFull, bm, o);
-        const uint32_t oi = __shfl_xor_sync(kFull, bi, o);
-        if (beats(ov, oi, bm, bi)) { bm = ov; bi = oi; }
+        for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, o));
+    } else {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(kFull, bm, o);
+            const uint32_t oi = __shfl_xor_sync(kFull, bi, o);
+            if (beats(ov, oi, bm, bi)) { bm = ov; bi = oi; }
+        }
     }
     nf = __reduce_or_sync(kFull, nf);
     if (lane == 0) { s_m[warp] = bm; s_i[warp] = bi; s_nf[warp] = nf; }
@@ -344,15 +346,17 @@ __global__ void __launch_bounds__(kNT) spec_phase1_kernel(SpecArgs a) {
         if (beats(s_m[w], s_i[w], bm, bi)) { bm = s_m[w]; bi = s_i[w]; }
         nf |= s_nf[w];
     }
-    // the sums, rescaled to the chunk's max, added as float-float
+    // the sums, rescaled to the chunk's max: fp32 within a warp (each thread's
+    // sum is already an fp32 sum of its 32 terms), float-float across warps
     FF tot{0.0f, 0.0f};
     if (kRej) {
-        FF mine{(!nf && thread_m > -INFINITY) ? thread_s * ex2_approx((thread_m - bm) * c) : 0.0f, 0.0f};
-        mine = ff_warp_sum(mine);
-        if (lane == 0) s_ff[warp] = mine;
-        __syncthreads();
+        float mine = (!nf && thread_m > -INFINITY) ? thread_s * ex2_approx((thread_m - bm) * c) : 0.0f;
 #pragma unroll
-        for (int ww = 0; ww < kWarps; ++ww) tot = ff_add(tot, s_ff[ww]);
+        for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(kFull, mine, o);
+        if (lane == 0) s_ff[warp] = FF{mine, 0.0f};
+        __syncthreads();
+        if (tid == 0)
+            for (int ww = 0; ww < kWarps; ++ww) tot = ff_add(tot, s_ff[ww]);
     }
     if (tid == 0) a.row_parts[static_cast<size_t>(t.row) * a.cmax + t.chunk] = RowPart{bm, bi | nf, tot.hi, tot.lo};
 }
@@ -437,23 +441,22 @@ struct DrawArgs {
     float log2e_over_T;
     uint32_t chunks;
     uint32_t chunk_elems;  // a multiple of 1024, at most kDrawChunkMax
-    uint32_t* seq_ctr;
     const RowPart* row_stats;
     const Decision* decisions;
     DrawPart* parts;  // [S][cmax]
     uint32_t cmax;
 };
 
-// Phase 2: the inverse-CDF draw from the residual (or from p).
-// Every block sums the weights of one chunk of the rows the decision names;
-// the last block of the sequence finds the chunk where u_fin * total falls
-// (a fixed-order scan of the chunk sums), then, within that chunk, the
-// 1,024-id stripe, the quad and the id. Sums across threads are float-float.
-// The tail is a few block-wide steps rather than one thread's serial walk:
-// straight-line code run once by one thread is bound by instruction fetch.
-constexpr uint32_t kDrawPer = 64;
-constexpr uint32_t kDrawChunkMax = kNT * kDrawPer;  // 16,384
-
+// Phase 2: the inverse-CDF draw from the residual (or from p), in two
+// launches. 2a: every block sums the weights of one chunk of the rows the
+// decision names. 2b: one block per sequence finds the chunk where
+// u_fin * total falls (a fixed-order scan of the chunk sums), then, within
+// that chunk, the 1,024-id stripe, the quad and the id. Sums across threads
+// are float-float. The search is a few block-wide steps rather than one
+// thread's serial walk: straight-line code run once by one thread is bound
+// by instruction fetch.
+constexpr uint32_t kDrawPer = 16;                   // ids per thread and chunk
+constexpr uint32_t kDrawChunkMax = kNT * kDrawPer;  // 4,096
 // Weights of 4 elements of the draw distribution: p = exp((x - m_p) / T) / Z_p
 // and the residual max(p - q, 0) (p again for a bonus draw). Padding (-inf)
 // weighs 0.
@@ -472,19 +475,12 @@ __device__ __forceinline__ void quad_weights(const float4& xp, const float4& xq,
 }
 
 template <bool kVec>
-__global__ void __launch_bounds__(kNT) spec_draw_kernel(DrawArgs a) {
+__global__ void __launch_bounds__(kNT) spec_draw_sum_kernel(DrawArgs a) {
     __shared__ FF s_r[kWarps];
     __shared__ FF s_p[kWarps];
-    __shared__ bool s_last;
-    __shared__ uint32_t s_cross;
-    __shared__ int s_lastpos;
-    __shared__ bool s_use_p;
-    __shared__ uint32_t s_cstar;
-    __shared__ FF s_before, s_target, s_sbefore;
-    __shared__ float s_stripe[kWarps][kDrawPer / 4];
-    __shared__ int s_istar;
 
     pdl_wait();
+    pdl_trigger();
     const uint32_t chunks = a.chunks;
     const uint32_t s = blockIdx.x / chunks;
     const uint32_t chunk = blockIdx.x - s * chunks;
@@ -538,13 +534,50 @@ __global__ void __launch_bounds__(kNT) spec_draw_kernel(DrawArgs a) {
         FF br{0.0f, 0.0f}, bp{0.0f, 0.0f};
         for (int w = 0; w < kWarps; ++w) { br = ff_add(br, s_r[w]); bp = ff_add(bp, s_p[w]); }
         a.parts[static_cast<size_t>(s) * a.cmax + chunk] = DrawPart{br, bp};
-        s_last = arrive_is_last(&a.seq_ctr[s], chunks);
     }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();  // order this thread's reads after the arrivals it saw
+}
 
-    // Last block. Warp 0 walks the chunk sums in chunk order, 32 at a time
+// Phase 2b: block s finds the chunk where u_fin * total falls (a fixed-order
+// scan of the chunk sums), then, within that chunk, the 1,024-id stripe, the
+// quad and the id.
+template <bool kVec>
+__global__ void __launch_bounds__(kNT) spec_draw_find_kernel(DrawArgs a) {
+    __shared__ FF s_r[kWarps];
+    __shared__ uint32_t s_cross;
+    __shared__ int s_lastpos;
+    __shared__ bool s_use_p;
+    __shared__ uint32_t s_cstar;
+    __shared__ FF s_before, s_target, s_sbefore;
+    __shared__ float s_stripe[kWarps][kDrawPer / 4];
+    __shared__ int s_istar;
+
+    pdl_wait();
+    pdl_trigger();
+    const uint32_t chunks = a.chunks;
+    const uint32_t s = blockIdx.x;
+    const Decision d = a.decisions[s];
+    if (d.kind == kDrawNone) return;  // invalid sequence, or no draw
+    const bool residual = d.kind == kDrawResidual;
+    const uint32_t K = a.K, V = a.V;
+    const uint32_t prow_i = static_cast<uint32_t>(s) * (K + 1u) + d.jstar;
+    const float* prow = a.target + static_cast<size_t>(prow_i) * V;
+    const RowPart ps = a.row_stats[prow_i];
+    const float* qrow = nullptr;
+    RowPart qs{0.0f, 0u, 1.0f, 0.0f};
+    if (residual) {
+        const uint32_t qrow_i = a.S * (K + 1u) + s * K + d.jstar;
+        qrow = a.draft + static_cast<size_t>(s * K + d.jstar) * V;
+        qs = a.row_stats[qrow_i];
+    }
+    const float c = a.log2e_over_T;
+    const float pinv = 1.0f / ps.s_hi;
+    const float qinv = 1.0f / qs.s_hi;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr float kNegInf = -INFINITY;
+    const float4 none = make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
+    constexpr int kQ = static_cast<int>(kDrawPer / 4u);
+
+    // Warp 0 walks the chunk sums in chunk order, 32 at a time
     // (fixed-order scans: the result does not depend on timing).
     const DrawPart* parts = a.parts + static_cast<size_t>(s) * a.cmax;
     if (warp == 0) {
@@ -912,14 +945,9 @@ extern "C" sel_status spec_accept(const float* d_target, const float* d_draft, c
     if (e1 != cudaSuccess) return SEL_ECUDA;
     if (!rej) return SEL_OK;
 
-    // phase 2: one wave of blocks when the sequences allow it (S * chunks
-    // <= SMs), chunks of at most kDrawChunkMax ids, a multiple of 1024
-    uint32_t chunks2 = static_cast<uint32_t>(sms) / S;
-    const uint32_t cmin2 = ceil_div(V, kDrawChunkMax);
-    if (chunks2 < cmin2) chunks2 = cmin2;
-    if (chunks2 > l.cmax_b) chunks2 = l.cmax_b;
-    const uint32_t ce2 = static_cast<uint32_t>(align_up(ceil_div(V, chunks2), kGrain));
-    chunks2 = ceil_div(V, ce2);
+    // phase 2: chunks of kDrawChunkMax ids
+    const uint32_t ce2 = kDrawChunkMax;
+    const uint32_t chunks2 = ceil_div(V, ce2);
     if (static_cast<uint64_t>(S) * chunks2 > 0x7fffffffull) return SEL_EUNSUPPORTED;
     DrawArgs b{};
     b.target = d_target;
@@ -930,14 +958,16 @@ extern "C" sel_status spec_accept(const float* d_target, const float* d_draft, c
     b.log2e_over_T = a.log2e_over_T;
     b.chunks = chunks2;
     b.chunk_elems = ce2;
-    b.seq_ctr = reinterpret_cast<uint32_t*>(ws + l.seq_ctr_b);
     b.row_stats = a.row_stats;
     b.decisions = a.decisions;
     b.parts = reinterpret_cast<DrawPart*>(ws + l.draw_parts);
     b.cmax = l.cmax_b;
     const dim3 grid2(S * chunks2);
-    const cudaError_t e2 = vec ? launch_pdl(spec_draw_kernel<true>, grid2, dim3(kNT), 0, stream, b)
-                               : launch_pdl(spec_draw_kernel<false>, grid2, dim3(kNT), 0, stream, b);
+    cudaError_t e2 = vec ? launch_pdl(spec_draw_sum_kernel<true>, grid2, dim3(kNT), 0, stream, b)
+                         : launch_pdl(spec_draw_sum_kernel<false>, grid2, dim3(kNT), 0, stream, b);
+    if (e2 != cudaSuccess) return SEL_ECUDA;
+    e2 = vec ? launch_pdl(spec_draw_find_kernel<true>, dim3(S), dim3(kNT), 0, stream, b)
+             : launch_pdl(spec_draw_find_kernel<false>, dim3(S), dim3(kNT), 0, stream, b);
     return e2 == cudaSuccess ? SEL_OK : SEL_ECUDA;
 }
 
