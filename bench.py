@@ -335,7 +335,8 @@ def gpu_arm(args, rank, world, local_rank):
 def extra_ops(B, dev, xs, drafts, tok, stream):
     """The calls beyond the step, on the same batch and copy rotation, each
     timed over OP_REPS graph-replayed launches: the EOG-excluding argmax (8
-    ids), sampler-match acceptance (7 x 6, the step's policy), the closed-form
+    ids), sampling with the step's policy plus top-n-sigma 1.0 and typical_p
+    0.8, sampler-match acceptance (7 x 6, the step's policy), the closed-form
     diagnostics (7 x 6) and a two-shard top-k (k = 20 per shard on each half
     of the vocabulary, then the merge)."""
     import torch
@@ -373,8 +374,16 @@ def extra_ops(B, dev, xs, drafts, tok, stream):
             gi[:, g].copy_(si[g])
         B.sel_merge_shards(gv, gi, offs, mv, mi)
 
+    prm_f = B.SampleParams(POLICY["temperature"], POLICY["top_k"], POLICY["top_p"], POLICY["min_p"],
+                           B.SEL_ORDER_TEMP_FIRST, 1.0, 0.8)
+    sid = torch.empty(ROWS, dtype=torch.int32, device=dev)
+    spr = torch.empty(ROWS, dtype=torch.float32, device=dev)
+    uu = torch.rand(ROWS, device=dev)
+    ws_f = B.workspace(B.SEL_OP_SAMPLE, ROWS, V, POLICY["top_k"], device=dev)
     calls = {
         "argmax_excluding_8": (lambda r: B.sel_argmax_excluding(xs[r % N_COPIES], exd, ids, ws_a), ROWS * ROW_BYTES),
+        "sample_nsigma1_typical08": (lambda r: B.sel_sample(xs[r % N_COPIES], prm_f, uu, sid, spr, ws_f),
+                                     ROWS * ROW_BYTES),
         "spec_sampler_match": (lambda r: B.spec_accept_sampler(tview(xs[r % N_COPIES]), tok, prm, ud, acc, emi, ws_m),
                                ROWS * ROW_BYTES),
         "spec_diagnostics": (lambda r: B.spec_diagnostics(tview(xs[r % N_COPIES]), drafts[r % 2], 1.0, smin, sprod,

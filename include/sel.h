@@ -151,6 +151,19 @@ sel_status sel_topk(const float *d_logits, uint32_t rows, uint32_t V,
  *   top_p        (0, 1]; 1 disables it
  *   min_p        [0, 1); 0 disables it
  *   order        SEL_ORDER_TEMP_FIRST or SEL_ORDER_TEMP_LAST
+ *   top_n_sigma  >= 0, finite; 0 disables it. Keeps only ids whose logit is
+ *                at least max - top_n_sigma * sigma, sigma the population
+ *                standard deviation of the row's V logits (a mask against the
+ *                maximum, independent of T), before top-k (Muser book 21.7,
+ *                the sampler chain: top-n-sigma, then top-k)
+ *   typical_p    [0, 1]; 0 and 1 disable it. Locally typical sampling on the
+ *                candidates (after top-k, before top-p; Muser book 21.7):
+ *                with H the entropy of P over the candidates, keep the ids
+ *                of smallest |-ln P - H| (ties: the more probable one) until
+ *                their P reaches typical_p; they keep their order and P is
+ *                renormalised over them
+ * The last two fields were appended; a zero-initialised struct leaves both
+ * filters off.
  */
 typedef struct sel_sample_params {
     float temperature;
@@ -158,14 +171,17 @@ typedef struct sel_sample_params {
     float top_p;
     float min_p;
     int32_t order;
+    float top_n_sigma;
+    float typical_p;
 } sel_sample_params;
 
 /*
  * sel_sample -- per row, one token drawn by inverse CDF from the filtered,
  * temperature-scaled softmax, with a caller-supplied uniform.
  *
- * Steps (TEMP_FIRST): z = x / T; the top_k candidates of z (the sel_topk
- * definition); P = softmax over the candidates; top-p keeps the shortest
+ * Steps (TEMP_FIRST): z = x / T; the top-n-sigma mask (if on); the top_k
+ * candidates of z (the sel_topk definition); P = softmax over the
+ * candidates; the locally typical window (if on); top-p keeps the shortest
  * prefix, in (P desc, id asc) order, whose cumulative P reaches top_p (the
  * crossing token included); min-p keeps candidates with P >= min_p * P_max;
  * Q = P renormalised over the survivors; the draw is the first survivor, in

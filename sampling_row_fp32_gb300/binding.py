@@ -41,10 +41,11 @@ class SelError(RuntimeError):
 
 
 class SampleParams(ctypes.Structure):
-    """struct sel_sample_params"""
+    """struct sel_sample_params (top_n_sigma and typical_p default to off)"""
     _fields_ = [("temperature", ctypes.c_float), ("top_k", ctypes.c_uint32),
                 ("top_p", ctypes.c_float), ("min_p", ctypes.c_float),
-                ("order", ctypes.c_int32)]
+                ("order", ctypes.c_int32), ("top_n_sigma", ctypes.c_float),
+                ("typical_p", ctypes.c_float)]
 
 
 class SpecParams(ctypes.Structure):

@@ -76,6 +76,7 @@ struct alignas(16) ChunkShared {
     alignas(16) uint32_t warp_val[kWarps];
     alignas(16) uint32_t warp_max[kWarps];
     alignas(16) uint32_t warp_nf[kWarps];
+    float warp_m1[kWarps], warp_m2[kWarps];  // moments (top-n-sigma)
     uint32_t count;
     uint32_t digit, want;        // radix select
 };
@@ -108,6 +109,8 @@ struct SampleArgs {
     float top_p;
     float min_p;
     int order;
+    float top_n_sigma;      // 0: off
+    float typical_p;        // on when 0 < typical_p < 1
 };
 
 struct TopkArgs {
@@ -118,6 +121,8 @@ struct TopkArgs {
     uint32_t* row_tau;       // [rows]: the largest chunk bound (key), 0 between calls
     uint32_t* pools;         // [rows][stride][kPool]: each chunk's warp maxima (keys), descending
     uint32_t* chunk_flags;   // [rows][stride]
+    float* moments;          // [rows][stride][4]: sum (x - x_0), sum (x - x_0)^2 as float-float
+    uint32_t want_moments;   // the row's standard deviation is needed (top-n-sigma)
     uint64_t* lists;         // [rows][stride][list_len(k)]
     uint32_t stride, list_len;
     uint32_t* err;
@@ -297,76 +302,159 @@ __device__ __noinline__ void radix_select_chunk(Sh& s, uint32_t* hist, const flo
     }
 }
 
-// Sampling epilogue on the sorted candidates sorted[0..n): one warp.
-// One pass computes, per candidate j, the filter weight wf_j (T = 1 when
-// temperature comes last) and draw weight wd_j relative to the largest
-// candidate (weight exactly 1), and their inclusive prefix sums pf, pd (kept
-// in `scratch`, 4 * SEL_MAX_K floats). Then: top-p keeps the shortest prefix
-// with pf >= top_p * pf_total; min-p keeps wf_j >= min_p (wf is
-// non-increasing, so the survivors stay a prefix); the draw takes the first j
-// of the prefix with u * pd_end < pd_j.
+// Sampling epilogue on the sorted candidates sorted[0..n): one warp, in
+// the order of the sampler chain.
+//  - top-n-sigma (nsig_thr > -inf): the candidates whose logit reaches the
+//    threshold, a prefix [0, nc).
+//  - One pass computes, per candidate j, the filter weight wf_j = exp(g_j)
+//    with g_j = (x_j - x_0) / Tf (Tf = 1 when temperature comes last), the
+//    draw weight wd_j relative to the largest candidate (weight exactly 1),
+//    and their inclusive prefix sums pf, pd (in `scratch`, 4 * SEL_MAX_K
+//    floats).
+//  - Locally typical (0 < typical_p < 1): with P_j = wf_j / S and
+//    H = -sum P ln P, -ln P_j - H = gbar - g_j, gbar = sum_j P_j g_j. g falls
+//    along the candidates, so the score |gbar - g_j| falls then rises, and
+//    the ids in (score asc, position asc) order grow a window outward from the
+//    first j with g_j <= gbar, the left (more probable) side winning ties, up
+//    to the first size whose mass reaches typical_p * S. The prefix sums are
+//    taken again over the window [lo, hi).
+//  - top-p keeps the shortest prefix of the window with pf >= top_p * its
+//    total; min-p keeps wf_j >= min_p * wf_lo (wf falls, so the survivors
+//    stay a prefix); the draw takes the first j with u * pd_end < pd_j.
 // `live` false: compute but write nothing (see warm_finish).
 __device__ void sample_epilogue(const uint64_t* sorted, float* scratch, uint32_t n, uint32_t row, float u,
-                                bool nonfinite, const SampleArgs& sa, uint32_t* out_ids, bool live = true) {
+                                bool nonfinite, const SampleArgs& sa, double nsig_thr, uint32_t* out_ids,
+                                bool live = true) {
     const int lane = threadIdx.x & 31;
     const bool valid = !nonfinite && u >= 0.0f && u < 1.0f;
     if (!valid) {
         if (live && lane == 0) { out_ids[row] = SEL_INVALID_ID; sa.out_probs[row] = __uint_as_float(0x7fc00000u); }
         return;
     }
-    if (sa.temperature == 0.0f || n == 1) {  // greedy, or a single candidate
+    // top-n-sigma: candidate 0 (the row's maximum) always reaches the threshold
+    uint32_t nc = n;
+    if (nsig_thr > -INFINITY) {
+        for (uint32_t b = 0; b < n; b += 32) {
+            const uint32_t j = b + lane;
+            const uint32_t miss =
+                __ballot_sync(kFull, j < n && static_cast<double>(key2f(cand_key(sorted[j]))) < nsig_thr);
+            if (miss) {
+                nc = b + __ffs(miss) - 1;
+                break;
+            }
+        }
+        if (nc == 0) nc = 1;
+    }
+    if (sa.temperature == 0.0f || nc == 1) {  // greedy, or a single candidate
         if (live && lane == 0) { out_ids[row] = cand_id(sorted[0]); sa.out_probs[row] = 1.0f; }
         return;
     }
     const float x0 = key2f(cand_key(sorted[0]));
     const float T = sa.temperature;
     const bool temp_last = sa.order == SEL_ORDER_TEMP_LAST;
+    const float Tf = temp_last ? 1.0f : T;
     float* wf = scratch;                 // [SEL_MAX_K]
     float* wd = wf + SEL_MAX_K;          // [SEL_MAX_K]
     float* pf = wd + SEL_MAX_K;          // [SEL_MAX_K]
     float* pd = pf + SEL_MAX_K;          // [SEL_MAX_K]
-    float cf = 0.0f, cd = 0.0f;          // carries into the next group of 32
-    for (uint32_t b = 0; b < n; b += 32) {
-        const uint32_t j = b + lane;
-        float f = 0.0f, w = 0.0f;
-        if (j < n) {
-            const float d = key2f(cand_key(sorted[j])) - x0;
-            w = expf(d / T);
-            f = temp_last ? expf(d) : w;
-            wf[j] = f;
-            wd[j] = w;
+    // weights, and inclusive prefix sums from `lo` (both scans in one pass)
+    auto scan = [&](uint32_t lo, uint32_t hi, bool weights) {
+        float cf = 0.0f, cd = 0.0f;  // carries into the next group of 32
+        for (uint32_t b = lo; b < hi; b += 32) {
+            const uint32_t j = b + lane;
+            float f = 0.0f, w = 0.0f;
+            if (j < hi) {
+                if (weights) {
+                    const float d = key2f(cand_key(sorted[j])) - x0;
+                    w = expf(d / T);
+                    f = temp_last ? expf(d) : w;
+                    wf[j] = f;
+                    wd[j] = w;
+                } else {
+                    f = wf[j];
+                    w = wd[j];
+                }
+            }
+#pragma unroll
+            for (int m = 1; m < 32; m <<= 1) {
+                const float of = __shfl_up_sync(kFull, f, m);
+                const float od = __shfl_up_sync(kFull, w, m);
+                if (lane >= m) { f += of; w += od; }
+            }
+            f += cf;
+            w += cd;
+            if (j < hi) { pf[j] = f; pd[j] = w; }
+            cf = __shfl_sync(kFull, f, 31);
+            cd = __shfl_sync(kFull, w, 31);
+        }
+        __syncwarp();
+    };
+    scan(0, nc, true);
+    uint32_t lo = 0, hi = nc;
+    if (sa.typical_p > 0.0f && sa.typical_p < 1.0f) {
+        const float S = pf[nc - 1];
+        float acc = 0.0f;
+        for (uint32_t b = 0; b < nc; b += 32) {
+            const uint32_t j = b + lane;
+            if (j < nc) acc += wf[j] * ((key2f(cand_key(sorted[j])) - x0) / Tf);
         }
 #pragma unroll
-        for (int m = 1; m < 32; m <<= 1) {
-            const float of = __shfl_up_sync(kFull, f, m);
-            const float od = __shfl_up_sync(kFull, w, m);
-            if (lane >= m) { f += of; w += od; }
-        }
-        f += cf;
-        w += cd;
-        if (j < n) { pf[j] = f; pd[j] = w; }
-        cf = __shfl_sync(kFull, f, 31);
-        cd = __shfl_sync(kFull, w, 31);
-    }
-    __syncwarp();
-    // top-p: the shortest prefix whose cumulative P reaches top_p
-    uint32_t ns = n;
-    if (sa.top_p < 1.0f) {
-        const float need = sa.top_p * pf[n - 1];
-        ns = 0;
-        for (uint32_t b = 0; b < n && ns == 0; b += 32) {
+        for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(kFull, acc, m);
+        const float gbar = acc / S;
+        uint32_t c = nc;
+        for (uint32_t b = 0; b < nc; b += 32) {
             const uint32_t j = b + lane;
-            const uint32_t hit = __ballot_sync(kFull, j < n && pf[j] >= need);
+            const uint32_t hit =
+                __ballot_sync(kFull, j < nc && (key2f(cand_key(sorted[j])) - x0) / Tf <= gbar);
+            if (hit) {
+                c = b + __ffs(hit) - 1;
+                break;
+            }
+        }
+        if (lane == 0) {
+            const float need = sa.typical_p * S;
+            int L = static_cast<int>(c) - 1;
+            uint32_t R = c;
+            float cum = 0.0f;
+            for (;;) {
+                bool take_left;
+                if (L < 0) take_left = false;
+                else if (R >= nc) take_left = true;
+                else {
+                    const float sl = (key2f(cand_key(sorted[L])) - x0) / Tf - gbar;
+                    const float sr = gbar - (key2f(cand_key(sorted[R])) - x0) / Tf;
+                    take_left = sl <= sr;
+                }
+                if (take_left) cum += wf[L--];
+                else cum += wf[R++];
+                if (cum >= need || (L < 0 && R >= nc)) break;
+            }
+            lo = static_cast<uint32_t>(L + 1);
+            hi = R;
+        }
+        lo = __shfl_sync(kFull, lo, 0);
+        hi = __shfl_sync(kFull, hi, 0);
+        scan(lo, hi, false);
+    }
+    // top-p: the shortest prefix of the window whose cumulative P reaches top_p
+    uint32_t ns = hi;
+    if (sa.top_p < 1.0f) {
+        const float need = sa.top_p * pf[hi - 1];
+        ns = 0;
+        for (uint32_t b = lo; b < hi && ns == 0; b += 32) {
+            const uint32_t j = b + lane;
+            const uint32_t hit = __ballot_sync(kFull, j < hi && pf[j] >= need);
             if (hit) ns = b + __ffs(hit);
         }
-        if (ns == 0) ns = n;  // rounding kept the total below top_p
+        if (ns == 0) ns = hi;  // rounding kept the total below top_p
     }
-    // min-p: keep P_j >= min_p * P_max, i.e. wf_j >= min_p (wf_0 = 1)
+    // min-p: keep P_j >= min_p * P_max, i.e. wf_j >= min_p * wf_lo
     if (sa.min_p > 0.0f) {
-        uint32_t keep = 1;
-        for (uint32_t b = 0; b < ns; b += 32) {
+        const float floor_w = sa.min_p * wf[lo];
+        uint32_t keep = lo + 1;
+        for (uint32_t b = lo; b < ns; b += 32) {
             const uint32_t j = b + lane;
-            const uint32_t m = __ballot_sync(kFull, j < ns && j > 0 && wf[j] >= sa.min_p);
+            const uint32_t m = __ballot_sync(kFull, j < ns && j > lo && wf[j] >= floor_w);
             if (m) keep = b + 32 - __clz(m);  // survivors form a prefix
         }
         ns = keep;
@@ -375,7 +463,7 @@ __device__ void sample_epilogue(const uint64_t* sorted, float* scratch, uint32_t
     const float total = pd[ns - 1];
     const float target = u * total;
     uint32_t pick = ns - 1;  // rounding: no crossing, the last survivor
-    for (uint32_t b = 0; b < ns; b += 32) {
+    for (uint32_t b = lo; b < ns; b += 32) {
         const uint32_t j = b + lane;
         const uint32_t hit = __ballot_sync(kFull, j < ns && target < pd[j]);
         if (hit) {
@@ -564,10 +652,11 @@ __device__ void merge_row_lists(TopkShared& s, Load&& load, uint32_t chunks, uin
 
 template <bool kSample>
 __device__ __forceinline__ void write_row(const uint64_t* sorted, float* scratch, const TopkArgs& a, uint32_t row,
-                                          uint32_t have, bool nonfinite) {
+                                          uint32_t have, bool nonfinite, double nsig_thr = -INFINITY) {
     const int tid = threadIdx.x;
     if constexpr (kSample) {
-        if (tid < 32) sample_epilogue(sorted, scratch, have, row, a.sa.uniforms[row], nonfinite, a.sa, a.out_ids);
+        if (tid < 32)
+            sample_epilogue(sorted, scratch, have, row, a.sa.uniforms[row], nonfinite, a.sa, nsig_thr, a.out_ids);
     } else {
         const uint32_t k = a.k;
         for (uint32_t j = tid; j < k; j += kNT) {
@@ -630,14 +719,31 @@ __global__ void __launch_bounds__(kNT, 5) topk_kernel(TopkArgs a) {
     float tmax = -INFINITY;
     float qmax[kVPT];  // each quad's largest value
     const bool whole = !kVec || n_real == kUnitMax;
+    // top-n-sigma: sums of d = x - x_0 and d^2 over the chunk's logits (x_0 the
+    // row's first logit, a shift against cancellation), two chains each
+    const bool moments = a.want_moments != 0u;
+    const float x_0 = moments ? rowp[0] : 0.0f;
+    float m1[2] = {0.0f, 0.0f}, m2[2] = {0.0f, 0.0f};
 #pragma unroll
     for (int sl = 0; sl < kVPT; ++sl) {
         qmax[sl] = -INFINITY;
-        if (whole || 4u * (tid + kNT * sl) < n_real) {
+        const uint32_t o = 4u * (tid + kNT * sl);
+        if (whole || o < n_real) {
             const float4 q = stage[tid + kNT * sl];
             latch_nonfinite2(nfacc, q);
             qmax[sl] = quad_max(q);
             tmax = fmaxf(tmax, qmax[sl]);
+            if (moments && o < n_real) {
+                const float f[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (o + j < n_real) {
+                        const float d = f[j] - x_0;
+                        m1[j & 1] += d;
+                        m2[j & 1] = __fmaf_rn(d, d, m2[j & 1]);
+                    }
+                }
+            }
         }
     }
 
@@ -665,8 +771,26 @@ __global__ void __launch_bounds__(kNT, 5) topk_kernel(TopkArgs a) {
         }
     }
     const uint32_t wnf = __any_sync(kFull, !latch_clear(nfacc)) ? 1u : 0u;
+    if (moments) {
+        float a1 = m1[0] + m1[1], a2 = m2[0] + m2[1];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            a1 += __shfl_xor_sync(kFull, a1, o);
+            a2 += __shfl_xor_sync(kFull, a2, o);
+        }
+        if (lane == 0) { s.warp_m1[warp] = a1; s.warp_m2[warp] = a2; }
+    }
     if (lane == 0) { s.warp_val[warp] = wv; s.warp_max[warp] = wmax; s.warp_nf[warp] = wnf; }
     __syncthreads();
+    if (moments && tid == 0) {
+        FF t1{0.0f, 0.0f}, t2{0.0f, 0.0f};
+        for (int w = 0; w < kWarps; ++w) {
+            t1 = ff_add(t1, FF{s.warp_m1[w], 0.0f});
+            t2 = ff_add(t2, FF{s.warp_m2[w], 0.0f});
+        }
+        reinterpret_cast<float4*>(a.moments)[static_cast<size_t>(t.row) * a.stride + t.chunk] =
+            make_float4(t1.hi, t1.lo, t2.hi, t2.lo);
+    }
     // this chunk's pool entries (the finishing launch sorts them)
     if (tid < static_cast<int>(kPool))
         a.pools[(static_cast<size_t>(t.row) * a.stride + t.chunk) * kPool + tid] = s.warp_max[tid];
@@ -803,7 +927,8 @@ __device__ void warm_finish(FinishShared& s, const TopkArgs& a) {
     __syncthreads();
     block_select_sorted(s.buf, n, k, s.sorted);
     if (kSample && threadIdx.x < 32)
-        sample_epilogue(s.sorted, reinterpret_cast<float*>(s.buf), k, 0, 0.5f, false, a.sa, nullptr, false);
+        sample_epilogue(s.sorted, reinterpret_cast<float*>(s.buf), k, 0, 0.5f, false, a.sa, -INFINITY, nullptr,
+                        false);
     __syncthreads();
 }
 
@@ -827,6 +952,22 @@ __global__ void __launch_bounds__(kNT) topk_finish_kernel(TopkArgs a) {
     uint32_t nf = 0;
     for (uint32_t c = lane; c < chunks; c += 32) nf |= a.chunk_flags[static_cast<size_t>(row) * a.stride + c];
     const uint32_t tau_row = a.row_tau[row];
+    // top-n-sigma: the row's moments, summed in double (lane-strided, then
+    // across the warp)
+    double mo1 = 0.0, mo2 = 0.0;
+    if (kSample && a.want_moments) {
+        const float4* mo = reinterpret_cast<const float4*>(a.moments) + static_cast<size_t>(row) * a.stride;
+        for (uint32_t c = lane; c < chunks; c += 32) {
+            const float4 m = mo[c];
+            mo1 += static_cast<double>(m.x) + static_cast<double>(m.y);
+            mo2 += static_cast<double>(m.z) + static_cast<double>(m.w);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            mo1 += __shfl_xor_sync(kFull, mo1, o);
+            mo2 += __shfl_xor_sync(kFull, mo2, o);
+        }
+    }
     uint32_t pb = 0;  // this warp's pool bound (warps 0-3: r = 1, 2, 4, 8)
     const uint32_t pr = 1u << warp, pm = (k + pr - 1) / pr;
     if (warp < 4 && pm <= chunks && pm <= 32u) {
@@ -895,12 +1036,22 @@ __global__ void __launch_bounds__(kNT) topk_finish_kernel(TopkArgs a) {
     // closed anyway
     if (tid == 0 && n < k && nf == 0) atomicOr(a.err, kErrMergeShort);
     block_select_sorted(s.buf, n, k, s.sorted);
-    write_row<kSample>(s.sorted, reinterpret_cast<float*>(s.buf), a, row, n < k ? n : k, nf != 0);
+    double nsig_thr = -INFINITY;
+    if (kSample && a.want_moments && n > 0) {
+        // mean and population variance from the shifted sums; the threshold
+        // is taken against the row's maximum, the top candidate
+        const double Vd = static_cast<double>(a.V);
+        const double mean_d = mo1 / Vd;
+        const double var = fmax(mo2 / Vd - mean_d * mean_d, 0.0);
+        nsig_thr = static_cast<double>(key2f(cand_key(s.sorted[0]))) -
+                   static_cast<double>(a.sa.top_n_sigma) * sqrt(var);
+    }
+    write_row<kSample>(s.sorted, reinterpret_cast<float*>(s.buf), a, row, n < k ? n : k, nf != 0, nsig_thr);
     if (tid == 0) atomicAdd(a.err + 1, 1u);  // rows finished (self-check)
 }
 
 struct TopkLayout {
-    size_t row_tau, pools, flags, lists, total;
+    size_t row_tau, pools, flags, moments, lists, total;
     uint32_t stride, list_len;
 };
 
@@ -914,9 +1065,35 @@ TopkLayout topk_layout(uint32_t rows, uint32_t V, uint32_t k) {
     l.row_tau = kWsHeaderBytes;
     l.pools = l.row_tau + ws_counters_bytes(rows);
     l.flags = l.pools + align_up(static_cast<size_t>(rows) * l.stride * kPool * 4u, 256);
-    l.lists = l.flags + align_up(static_cast<size_t>(rows) * l.stride * 4u, 256);
+    l.moments = l.flags + align_up(static_cast<size_t>(rows) * l.stride * 4u, 256);
+    l.lists = l.moments + align_up(static_cast<size_t>(rows) * l.stride * 16u, 256);
     l.total = l.lists + static_cast<size_t>(rows) * l.stride * l.list_len * 8u;
     return l;
+}
+
+// A sampling policy the entry points accept (NaN fails every test).
+bool policy_valid(const sel_sample_params& p) {
+    const float T = p.temperature;
+    if (!(T >= 0.0f) || !(T < INFINITY)) return false;
+    if (!(p.top_p > 0.0f && p.top_p <= 1.0f)) return false;
+    if (!(p.min_p >= 0.0f && p.min_p < 1.0f)) return false;
+    if (p.order != SEL_ORDER_TEMP_FIRST && p.order != SEL_ORDER_TEMP_LAST) return false;
+    if (!(p.top_n_sigma >= 0.0f) || !(p.top_n_sigma < INFINITY)) return false;
+    if (!(p.typical_p >= 0.0f && p.typical_p <= 1.0f)) return false;
+    return true;
+}
+
+SampleArgs sample_args(const sel_sample_params& p, const float* uniforms, float* probs) {
+    SampleArgs sa{};
+    sa.uniforms = uniforms;
+    sa.out_probs = probs;
+    sa.temperature = p.temperature;
+    sa.top_p = p.top_p;
+    sa.min_p = p.min_p;
+    sa.order = p.order;
+    sa.top_n_sigma = p.top_n_sigma;
+    sa.typical_p = p.typical_p;
+    return sa;
 }
 
 template <bool kSample>
@@ -945,6 +1122,8 @@ sel_status launch_topk(const float* d_logits, uint32_t rows, uint32_t V, uint32_
     a.row_tau = reinterpret_cast<uint32_t*>(ws + l.row_tau);
     a.pools = reinterpret_cast<uint32_t*>(ws + l.pools);
     a.chunk_flags = reinterpret_cast<uint32_t*>(ws + l.flags);
+    a.moments = reinterpret_cast<float*>(ws + l.moments);
+    a.want_moments = (kSample && sa.top_n_sigma > 0.0f) ? 1u : 0u;
     a.lists = reinterpret_cast<uint64_t*>(ws + l.lists);
     a.stride = l.stride;
     a.list_len = l.list_len;
@@ -991,10 +1170,7 @@ extern "C" sel_status sel_sample(const float* d_logits, uint32_t rows, uint32_t 
                                  size_t ws_bytes, cudaStream_t stream) {
     if (!p || V == 0 || V > SEL_MAX_V) return SEL_EINVAL;
     const float T = p->temperature;
-    if (!(T >= 0.0f) || !(T < INFINITY)) return SEL_EINVAL;  // rejects NaN too
-    if (!(p->top_p > 0.0f && p->top_p <= 1.0f)) return SEL_EINVAL;
-    if (!(p->min_p >= 0.0f && p->min_p < 1.0f)) return SEL_EINVAL;
-    if (p->order != SEL_ORDER_TEMP_FIRST && p->order != SEL_ORDER_TEMP_LAST) return SEL_EINVAL;
+    if (!policy_valid(*p)) return SEL_EINVAL;
     uint32_t k = p->top_k;
     if (T == 0.0f) k = 1;  // greedy: the top-1 candidate is the argmax
     if (k == 0) return SEL_EUNSUPPORTED;
@@ -1005,7 +1181,7 @@ extern "C" sel_status sel_sample(const float* d_logits, uint32_t rows, uint32_t 
     if (reinterpret_cast<uintptr_t>(d_logits) % 4 || reinterpret_cast<uintptr_t>(d_uniforms) % 4 ||
         reinterpret_cast<uintptr_t>(d_out_ids) % 4 || reinterpret_cast<uintptr_t>(d_out_probs) % 4)
         return SEL_EINVAL;
-    SampleArgs sa{d_uniforms, d_out_probs, T, p->top_p, p->min_p, p->order};
+    const SampleArgs sa = sample_args(*p, d_uniforms, d_out_probs);
     return launch_topk<true>(d_logits, rows, V, k, nullptr, d_out_ids, d_ws, ws_bytes, sa, stream);
 }
 
@@ -1098,11 +1274,11 @@ extern "C" sel_status sel_sample_shards(const float* d_vals, const uint32_t* d_i
                                         cudaStream_t stream) {
     if (!p) return SEL_EINVAL;
     const float T = p->temperature;
-    if (!(T >= 0.0f) || !(T < INFINITY)) return SEL_EINVAL;
-    if (!(p->top_p > 0.0f && p->top_p <= 1.0f)) return SEL_EINVAL;
-    if (!(p->min_p >= 0.0f && p->min_p < 1.0f)) return SEL_EINVAL;
-    if (p->order != SEL_ORDER_TEMP_FIRST && p->order != SEL_ORDER_TEMP_LAST) return SEL_EINVAL;
+    if (!policy_valid(*p)) return SEL_EINVAL;
     if (T > 0.0f && p->top_k != k) return SEL_EINVAL;  // the lists are the policy's top_k candidates
+    // top-n-sigma needs the whole row's standard deviation, which the
+    // per-shard candidate lists do not carry
+    if (T > 0.0f && p->top_n_sigma > 0.0f) return SEL_EUNSUPPORTED;
     ShardArgs sh{};
     const sel_status st = check_shards(d_vals, d_ids, rows, G, k, h_offsets, sh);
     if (st != SEL_OK) return st;
@@ -1114,7 +1290,7 @@ extern "C" sel_status sel_sample_shards(const float* d_vals, const uint32_t* d_i
     TopkArgs a{};
     a.k = k;
     a.out_ids = d_out_ids;
-    a.sa = SampleArgs{d_uniforms, d_out_probs, T, p->top_p, p->min_p, p->order};
+    a.sa = sample_args(*p, d_uniforms, d_out_probs);
     return launch_pdl(merge_shards_kernel<true>, dim3(rows), dim3(kNT), 0, stream, sh, a) == cudaSuccess
                ? SEL_OK
                : SEL_ECUDA;
@@ -1192,10 +1368,7 @@ extern "C" sel_status spec_accept_sampler(const float* d_target, const uint32_t*
                                           cudaStream_t stream) {
     if (!p || V == 0 || V > SEL_MAX_V) return SEL_EINVAL;
     const float T = p->temperature;
-    if (!(T >= 0.0f) || !(T < INFINITY)) return SEL_EINVAL;
-    if (!(p->top_p > 0.0f && p->top_p <= 1.0f)) return SEL_EINVAL;
-    if (!(p->min_p >= 0.0f && p->min_p < 1.0f)) return SEL_EINVAL;
-    if (p->order != SEL_ORDER_TEMP_FIRST && p->order != SEL_ORDER_TEMP_LAST) return SEL_EINVAL;
+    if (!policy_valid(*p)) return SEL_EINVAL;
     uint32_t k = p->top_k;
     if (T == 0.0f) k = 1;
     if (k == 0) return SEL_EUNSUPPORTED;
@@ -1216,7 +1389,7 @@ extern "C" sel_status spec_accept_sampler(const float* d_target, const uint32_t*
     char* ws = static_cast<char*>(d_ws);
     uint32_t* draws = reinterpret_cast<uint32_t*>(ws + l.draws);
     float* probs = reinterpret_cast<float*>(ws + l.probs);
-    SampleArgs sa{d_u, probs, T, p->top_p, p->min_p, p->order};
+    const SampleArgs sa = sample_args(*p, d_u, probs);
     const sel_status st = launch_topk<true>(d_target, static_cast<uint32_t>(rows_t), V, k, nullptr, draws, d_ws,
                                            l.draws, sa, stream);
     if (st != SEL_OK) return st;

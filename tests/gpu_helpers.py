@@ -84,7 +84,7 @@ def topk(x: np.ndarray, k: int, misalign=False, ws=None):
 
 
 def sample(x: np.ndarray, u: np.ndarray, T, top_k, top_p, min_p, temp_last=False,
-           misalign=False):
+           misalign=False, top_n_sigma=0.0, typical_p=0.0):
     rows, V = x.shape
     xd = to_dev(x, misalign)
     ud = to_dev(np.asarray(u, dtype=np.float32).reshape(rows))
@@ -92,7 +92,8 @@ def sample(x: np.ndarray, u: np.ndarray, T, top_k, top_p, min_p, temp_last=False
     probs = _out((rows,), torch.float32)
     ws = B.workspace(B.SEL_OP_SAMPLE, rows, V, top_k, device=device())
     prm = B.SampleParams(T, top_k, top_p, min_p,
-                         B.SEL_ORDER_TEMP_LAST if temp_last else B.SEL_ORDER_TEMP_FIRST)
+                         B.SEL_ORDER_TEMP_LAST if temp_last else B.SEL_ORDER_TEMP_FIRST,
+                         top_n_sigma, typical_p)
     B.sel_sample(xd, prm, ud, ids, probs, ws)
     torch.cuda.synchronize()
     assert ws_error(ws) == 0, ws_error(ws)

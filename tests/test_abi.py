@@ -83,9 +83,16 @@ def test_host_validation_needs_no_gpu(lib):
     assert lib.sel_topk(fake, 1, 10, 0, fake, fake, None, 0, None) == B.SEL_EINVAL   # k = 0
     assert lib.sel_topk(fake, 1, 5000, 1025, fake, fake, None, 0, None) == B.SEL_EUNSUPPORTED
 
-    def sample(T, k, p, m, order=0):
-        prm = B.SampleParams(T, k, p, m, order)
+    def sample(T, k, p, m, order=0, nsig=0.0, typ=0.0):
+        prm = B.SampleParams(T, k, p, m, order, nsig, typ)
         return lib.sel_sample(fake, 1, 10, ctypes.byref(prm), fake, fake, fake, None, 0, None)
+    # top-n-sigma: finite and >= 0; typical_p in [0, 1] (0 and 1 are off)
+    assert sample(1.0, 5, 1.0, 0.0, nsig=-0.5) == B.SEL_EINVAL
+    assert sample(1.0, 5, 1.0, 0.0, nsig=float("nan")) == B.SEL_EINVAL
+    assert sample(1.0, 5, 1.0, 0.0, nsig=float("inf")) == B.SEL_EINVAL
+    assert sample(1.0, 5, 1.0, 0.0, typ=-0.1) == B.SEL_EINVAL
+    assert sample(1.0, 5, 1.0, 0.0, typ=1.5) == B.SEL_EINVAL
+    assert sample(1.0, 5, 1.0, 0.0, typ=float("nan")) == B.SEL_EINVAL
     assert sample(float("nan"), 5, 1.0, 0.0) == B.SEL_EINVAL
     assert sample(-1.0, 5, 1.0, 0.0) == B.SEL_EINVAL
     assert sample(1.0, 5, 0.0, 0.0) == B.SEL_EINVAL
@@ -132,6 +139,9 @@ def test_shard_merge_validation_needs_no_gpu(lib):
     assert s(fake, fake, 1, 2, 5, good, ctypes.byref(B.SampleParams(0.7, 5, 1.5, 0.05, 0)),
              fake, fake, fake, None) == B.SEL_EINVAL
     assert s(fake, fake, 1, 2, 5, good, ctypes.byref(p), None, fake, fake, None) == B.SEL_EINVAL
+    # top-n-sigma needs the whole row's standard deviation: not from shard lists
+    assert s(fake, fake, 1, 2, 5, good, ctypes.byref(B.SampleParams(0.7, 5, 0.9, 0.05, 0, 1.0, 0.0)),
+             fake, fake, fake, None) == B.SEL_EUNSUPPORTED
     assert s(fake, fake, 0, 2, 5, good, ctypes.byref(p), None, None, None, None) == B.SEL_OK
 
 
