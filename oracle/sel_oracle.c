@@ -151,6 +151,12 @@ static void softmax_row(const float *x, uint32_t V, double T, double *p)
  * rounding leaves none, the last i with w_i > 0. *margin receives
  * min_i |u - C_i| over every boundary except the final one (which is 1).
  */
+static int cmp_u64(const void *a, const void *b)
+{
+    uint64_t x = *(const uint64_t *)a, y = *(const uint64_t *)b;
+    return x < y ? -1 : (x > y ? 1 : 0);
+}
+
 static uint32_t inverse_cdf(const double *w, uint32_t n, double u,
                             double *margin)
 {
@@ -307,6 +313,7 @@ void orc_topk(const float *logits, uint32_t rows, uint32_t V, uint32_t k,
  *  4. top_p < 1: keep the shortest prefix of C with cumulative P >= top_p
  *  5. min_p > 0: keep survivors with P_i >= min_p * P_max
  *  6. Q_i = w_i / sum_survivors w ; draw by inverse CDF in the same order
+ *     (full-row sampling, top_k == 0: in ascending id among the survivors)
  * temp_last != 0: steps 3-5 use T = 1 probabilities (filter on the
  * untempered distribution) and step 6 uses the tempered weights.
  * *margin = distance of the nearest decision to its threshold: |u - C_i|,
@@ -466,16 +473,37 @@ static uint32_t sample_row(const float *x, uint32_t V, double T,
         ns = keep;
     }
 
-    /* 6. renormalise over the survivors and draw */
+    /* 6. renormalise over the survivors and draw: in the survivors' order,
+     *    or, for full-row sampling (top_k == 0), in ascending id. The pages
+     *    fix no CDF order; the distribution is the same either way, and
+     *    ascending id needs no sort of V (the residual and bonus draws of
+     *    speculative acceptance take the same reading). */
     double Sd = 0.0;
     for (uint32_t j = 0; j < ns; ++j)
         Sd += wd[j];
     double m_draw;
-    uint32_t pick = inverse_cdf(wd, ns, u, &m_draw);
+    uint32_t id;
+    if (top_k == 0) {
+        /* survivors by ascending id: (id << 32 | position), sorted */
+        uint64_t *by_id = (uint64_t *)malloc((size_t)ns * sizeof(uint64_t));
+        for (uint32_t j = 0; j < ns; ++j)
+            by_id[j] = ((uint64_t)order[j] << 32) | j;
+        qsort(by_id, ns, sizeof(uint64_t), cmp_u64);
+        double *wa = (double *)malloc((size_t)ns * sizeof(double));
+        for (uint32_t i = 0; i < ns; ++i)
+            wa[i] = wd[(uint32_t)by_id[i]];
+        uint32_t pick = inverse_cdf(wa, ns, u, &m_draw);
+        id = (uint32_t)(by_id[pick] >> 32);
+        *prob = wa[pick] / Sd;
+        free(wa);
+        free(by_id);
+    } else {
+        uint32_t pick = inverse_cdf(wd, ns, u, &m_draw);
+        id = order[pick];
+        *prob = wd[pick] / Sd;
+    }
     if (m_draw < *margin)
         *margin = m_draw;
-    uint32_t id = order[pick];
-    *prob = wd[pick] / Sd;
 
     free(wd);
     free(wf);

@@ -245,19 +245,21 @@ def pin_sample_closed_forms(orc):
 
 def pin_sample_cdf_grid(orc):
     """Sweep u over a 10^5-point grid on a row with hand-chosen probabilities:
-    the share of grid points mapped to each id equals its probability."""
+    the share of grid points mapped to each id equals its probability, and
+    the map is monotone in u along the draw order: (P desc, id asc) for the
+    top-k candidates (top_k = V here), ascending id for full-row sampling
+    (top_k = 0)."""
     P = np.array([0.05, 0.4, 0.15, 0.1, 0.3])  # order by P: ids 1, 4, 2, 3, 0
     x = np.tile(_logits_from(P), (100_000, 1))
     u = ((np.arange(100_000) + 0.5) / 100_000).astype(np.float32)
-    r = orc.sample(x, u, 1.0, 0, 1.0, 0.0)
-    share = np.bincount(r.ids.astype(np.int64), minlength=5) / 100_000
-    assert np.allclose(share, P, atol=2e-5), share
-    # the map is monotone in u along the (P desc, id asc) order
-    rank_of = {1: 0, 4: 1, 2: 2, 3: 3, 0: 4}
-    ranks = np.array([rank_of[int(i)] for i in r.ids])
-    assert np.all(np.diff(ranks) >= 0)
-    # each drawn id's reported probability is its own
-    assert np.allclose(r.probs, P[r.ids.astype(np.int64)], rtol=1e-6)
+    for top_k, rank_of in ((5, {1: 0, 4: 1, 2: 2, 3: 3, 0: 4}), (0, {i: i for i in range(5)})):
+        r = orc.sample(x, u, 1.0, top_k, 1.0, 0.0)
+        share = np.bincount(r.ids.astype(np.int64), minlength=5) / 100_000
+        assert np.allclose(share, P, atol=2e-5), (top_k, share)
+        ranks = np.array([rank_of[int(i)] for i in r.ids])
+        assert np.all(np.diff(ranks) >= 0), top_k
+        # each drawn id's reported probability is its own
+        assert np.allclose(r.probs, P[r.ids.astype(np.int64)], rtol=1e-6)
 
 
 def pin_sample_support(orc):

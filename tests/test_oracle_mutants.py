@@ -38,7 +38,11 @@ MUTANTS = [
     ("min-p compares absolute probability",
      [("double ratio = (wf[j] / Sf) / pmax;", "double ratio = (wf[j] / Sf);")]),
     ("probability not renormalised after filtering",
-     [("*prob = wd[pick] / Sd;", "*prob = wd[pick] / Sf;")]),
+     [("        id = order[pick];\n        *prob = wd[pick] / Sd;", "        id = order[pick];\n        *prob = wd[pick] / Sf;")]),
+    ("full-row draw in the candidates' order instead of ascending id",
+     [("    if (top_k == 0) {\n        /* survivors by ascending id", "    if (0) {\n        /* survivors by ascending id")]),
+    ("full-row draw maps u to the neighbouring id",
+     [("        id = (uint32_t)(by_id[pick] >> 32);", "        id = (uint32_t)(by_id[pick + 1 < ns ? pick + 1 : pick] >> 32);")]),
     ("inverse CDF picks the next index",
      [("if (pick == ORC_INVALID && u < C)\n            pick = i;",
        "if (pick == ORC_INVALID && u < C)\n            pick = i + 1 < n ? i + 1 : i;")]),
