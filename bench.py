@@ -336,7 +336,8 @@ def extra_ops(B, dev, xs, drafts, tok, stream):
     """The calls beyond the step, on the same batch and copy rotation, each
     timed over OP_REPS graph-replayed launches: the EOG-excluding argmax (8
     ids), sampling with the step's policy plus top-n-sigma 1.0 and typical_p
-    0.8, sampler-match acceptance (7 x 6, the step's policy), the closed-form
+    0.8, full-row sampling (top_k = 0, the step's T, top_p and min_p),
+    sampler-match acceptance (7 x 6, the step's policy), the closed-form
     diagnostics (7 x 6) and a two-shard top-k (k = 20 per shard on each half
     of the vocabulary, then the merge)."""
     import torch
@@ -380,8 +381,13 @@ def extra_ops(B, dev, xs, drafts, tok, stream):
     spr = torch.empty(ROWS, dtype=torch.float32, device=dev)
     uu = torch.rand(ROWS, device=dev)
     ws_f = B.workspace(B.SEL_OP_SAMPLE, ROWS, V, POLICY["top_k"], device=dev)
+    prm_full = B.SampleParams(POLICY["temperature"], 0, POLICY["top_p"], POLICY["min_p"], B.SEL_ORDER_TEMP_FIRST)
+    ws_full = B.workspace(B.SEL_OP_SAMPLE, ROWS, V, 0, device=dev)
     calls = {
         "argmax_excluding_8": (lambda r: B.sel_argmax_excluding(xs[r % N_COPIES], exd, ids, ws_a), ROWS * ROW_BYTES),
+        # full-row sampling reads every row twice (candidates and sums, then the draw)
+        "sample_full_row": (lambda r: B.sel_sample(xs[r % N_COPIES], prm_full, uu, sid, spr, ws_full),
+                            2 * ROWS * ROW_BYTES),
         "sample_nsigma1_typical08": (lambda r: B.sel_sample(xs[r % N_COPIES], prm_f, uu, sid, spr, ws_f),
                                      ROWS * ROW_BYTES),
         "spec_sampler_match": (lambda r: B.spec_accept_sampler(tview(xs[r % N_COPIES]), tok, prm, ud, acc, emi, ws_m),

@@ -32,7 +32,7 @@ extern "C" size_t sel_workspace_bytes(int op, uint32_t rows, uint32_t V, uint32_
             if (k == 0 || k > V || k > SEL_MAX_K) return 0;
             return topk_ws_bytes(rows, V, k);
         case SEL_OP_SAMPLE: {
-            uint32_t kk = k == 0 ? 1u : k;  // greedy policies select one candidate
+            uint32_t kk = k == 0 ? kFullRowCandidates : k;  // full-row sampling (greedy needs 1)
             if (kk > V) kk = V;
             if (kk > SEL_MAX_K) return 0;
             return topk_ws_bytes(rows, V, kk);

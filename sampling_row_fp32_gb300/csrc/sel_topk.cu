@@ -53,6 +53,9 @@ constexpr uint32_t kBlockCap = SEL_MAX_K;    // a chunk's survivors before the r
 constexpr uint32_t kFinishBuf = 4096;        // row-merge buffer
 constexpr uint32_t kRound = kFinishBuf - SEL_MAX_K;  // list entries filtered per round
 constexpr int kRoundPer = static_cast<int>(kRound / kNT);
+constexpr uint32_t kFullCand = kFullRowCandidates;  // candidates of full-row sampling (top_k = 0)
+constexpr uint32_t kDrawIds = 4096;          // ids per chunk of the full-row draw
+constexpr int kDrawQ = static_cast<int>(kDrawIds / (4u * kNT));  // quads per thread and draw chunk
 constexpr uint32_t kRankMax = 512;           // rank counting up to this many candidates
 constexpr uint32_t kFastMergeLists = 32;     // one warp lane per chunk list
 
@@ -77,6 +80,7 @@ struct alignas(16) ChunkShared {
     alignas(16) uint32_t warp_max[kWarps];
     alignas(16) uint32_t warp_nf[kWarps];
     float warp_m1[kWarps], warp_m2[kWarps];  // moments (top-n-sigma)
+    float warp_fs[kWarps], warp_fq[kWarps];  // exponent sums (full-row sampling)
     uint32_t count;
     uint32_t digit, want;        // radix select
 };
@@ -102,6 +106,17 @@ struct alignas(16) TopkShared {
     uint32_t digit, want;        // radix select
 };
 
+// Full-row sampling: the survivors of a row are the ids whose candidate
+// key c = (key(x) << 32 | ~id) lies in [key_lo, key_hi]; they are drawn in
+// ascending id with weights exp((x - M) / T).
+struct alignas(16) FullRow {
+    unsigned long long key_lo, key_hi;
+    float M;         // the row's maximum logit
+    float u;         // the row's uniform
+    uint32_t valid;  // 0: the row fails closed
+    uint32_t pad;
+};
+
 struct SampleArgs {
     const float* uniforms;  // [rows]
     float* out_probs;       // [rows]
@@ -123,6 +138,13 @@ struct TopkArgs {
     uint32_t* chunk_flags;   // [rows][stride]
     float* moments;          // [rows][stride][4]: sum (x - x_0), sum (x - x_0)^2 as float-float
     uint32_t want_moments;   // the row's standard deviation is needed (top-n-sigma)
+    uint32_t full_row;       // full-row sampling (top_k = 0): chunk exponent sums and a survivor range
+    float4* full_parts;      // [rows][stride]: chunk max m, sum 2^((x - m) c) as float-float, sum w (x - m) c
+    FullRow* full_rows;      // [rows]
+    FF* draw_sums;           // [rows][draw_chunks]
+    uint32_t draw_chunks;
+    float full_cf;           // log2(e) / T of the filters (T = 1 when temperature comes last)
+    float draw_c;            // log2(e) / T of the draw
     uint64_t* lists;         // [rows][stride][list_len(k)]
     uint32_t stride, list_len;
     uint32_t* err;
@@ -791,6 +813,57 @@ __global__ void __launch_bounds__(kNT, 5) topk_kernel(TopkArgs a) {
         reinterpret_cast<float4*>(a.moments)[static_cast<size_t>(t.row) * a.stride + t.chunk] =
             make_float4(t1.hi, t1.lo, t2.hi, t2.lo);
     }
+    if (a.full_row) {
+        // Full-row sampling: the chunk's max m and, over its logits, the sums
+        // of w = 2^((x - m) c) and of w (x - m) c (c = log2(e) / T), each
+        // thread first relative to its own max (its real logits only)
+        uint32_t mk = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) mk = max(mk, s.warp_max[w]);
+        const float mb = key2f(mk);
+        const float c = a.full_cf;
+        float fs = 0.0f, fq = 0.0f;
+        if (tmax > -INFINITY && tmax < INFINITY && mb < INFINITY) {
+            float ts = 0.0f, tq = 0.0f;
+#pragma unroll
+            for (int sl = 0; sl < kVPT; ++sl) {
+                const uint32_t o = 4u * (tid + kNT * sl);
+                if (o < n_real) {
+                    const float4 q = stage[tid + kNT * sl];
+                    const float f[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (o + j < n_real) {
+                            const float arg = (f[j] - tmax) * c;
+                            const float w = ex2_approx(arg);
+                            ts += w;
+                            tq = __fmaf_rn(w, arg, tq);
+                        }
+                    }
+                }
+            }
+            const float shift = (tmax - mb) * c;
+            const float scale = ex2_approx(shift);
+            fs = ts * scale;
+            fq = (tq + ts * shift) * scale;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            fs += __shfl_xor_sync(kFull, fs, o);
+            fq += __shfl_xor_sync(kFull, fq, o);
+        }
+        if (lane == 0) { s.warp_fs[warp] = fs; s.warp_fq[warp] = fq; }
+        __syncthreads();
+        if (tid == 0) {
+            FF S{0.0f, 0.0f};
+            float Q = 0.0f;
+            for (int w = 0; w < kWarps; ++w) {
+                S = ff_add(S, FF{s.warp_fs[w], 0.0f});
+                Q += s.warp_fq[w];
+            }
+            a.full_parts[static_cast<size_t>(t.row) * a.stride + t.chunk] = make_float4(mb, S.hi, S.lo, Q);
+        }
+    }
     // this chunk's pool entries (the finishing launch sorts them)
     if (tid < static_cast<int>(kPool))
         a.pools[(static_cast<size_t>(t.row) * a.stride + t.chunk) * kPool + tid] = s.warp_max[tid];
@@ -915,6 +988,404 @@ __device__ __forceinline__ void sort_desc8(uint32_t (&e)[8]) {
 // chunk's entries at or above the chunk's bound, or the chunk's top k, so
 // the row's top k all survive. Lists are filtered kRound entries at a time,
 // with a selection down to k between rounds when more follow.
+// Full-row sampling (top_k = 0): the sampler chain on the row's kFullCand
+// most probable candidates, with probabilities normalised over the whole row
+// (Z, and the mean log-weight gbar, from the main launch's chunk sums).
+// Decides the survivor set as a range of candidate keys: a prefix or window
+// of the sorted candidates where a top-p or typical cut applies, or every id
+// at or above a value threshold (min-p, top-n-sigma) otherwise. A cut that
+// would need candidates past the kFullCand most probable ones is not
+// decided: the row fails closed and kErrBeyond is raised. One warp.
+__device__ void full_row_plan(const uint64_t* sorted, float* scratch, uint32_t n, uint32_t row, bool nonfinite,
+                              const TopkArgs& a, double Z, double gbar_all, double sigma) {
+    const int lane = threadIdx.x & 31;
+    const SampleArgs& sa = a.sa;
+    FullRow out{};
+    out.u = sa.uniforms[row];
+    out.M = n > 0 ? key2f(cand_key(sorted[0])) : 0.0f;
+    bool resolved = !nonfinite && out.u >= 0.0f && out.u < 1.0f && n > 0 && Z > 0.0;
+    bool beyond_err = false;
+    if (resolved) {
+        const float M = out.M;
+        const bool temp_last = sa.order == SEL_ORDER_TEMP_LAST;
+        const float Tf = temp_last ? 1.0f : sa.temperature;
+        auto xv = [&](uint32_t j) { return key2f(cand_key(sorted[j])); };
+        auto gv = [&](uint32_t j) { return (xv(j) - M) / Tf; };
+        bool beyond = a.V > n;  // the ids past the candidates may survive
+        // top-n-sigma: the candidates at or above the threshold, a prefix
+        uint32_t nc = n;
+        double thr_ns = -INFINITY;
+        if (sa.top_n_sigma > 0.0f) {
+            thr_ns = static_cast<double>(M) - static_cast<double>(sa.top_n_sigma) * sigma;
+            for (uint32_t b = 0; b < n; b += 32) {
+                const uint32_t j = b + lane;
+                const uint32_t miss = __ballot_sync(kFull, j < n && static_cast<double>(xv(j)) < thr_ns);
+                if (miss) {
+                    nc = b + __ffs(miss) - 1;
+                    beyond = false;
+                    break;
+                }
+            }
+            if (nc == 0) nc = 1;
+        }
+        float* wf = scratch;  // [kFullCand]
+        for (uint32_t j = lane; j < nc; j += 32) wf[j] = expf(gv(j));
+        __syncwarp();
+        // mass and mean log-weight of the candidate set C
+        double ZC = Z, gC = gbar_all;
+        bool known = true;
+        if (sa.top_n_sigma > 0.0f) {
+            if (beyond) {
+                known = false;  // C runs past the candidates
+            } else {
+                double z = 0.0, q = 0.0;
+                for (uint32_t j = lane; j < nc; j += 32) {
+                    z += wf[j];
+                    q += static_cast<double>(wf[j]) * gv(j);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    z += __shfl_xor_sync(kFull, z, o);
+                    q += __shfl_xor_sync(kFull, q, o);
+                }
+                ZC = z;
+                gC = q / z;
+            }
+        }
+        const bool typical = sa.typical_p > 0.0f && sa.typical_p < 1.0f;
+        const bool topp = sa.top_p < 1.0f;
+        if ((typical || topp) && !known) resolved = false;
+        uint32_t lo = 0, hi = nc;
+        double ZW = ZC;
+        if (resolved && typical && (nc > 1 || beyond)) {
+            // the window grows from the first candidate with g <= gbar, the
+            // more probable side winning ties
+            uint32_t c = nc;
+            for (uint32_t b = 0; b < nc; b += 32) {
+                const uint32_t j = b + lane;
+                const uint32_t hit = __ballot_sync(kFull, j < nc && static_cast<double>(gv(j)) <= gC);
+                if (hit) {
+                    c = b + __ffs(hit) - 1;
+                    break;
+                }
+            }
+            uint32_t ok = 1, wlo = 0, whi = 0;
+            double cum = 0.0;
+            if (lane == 0) {
+                if (c == nc && beyond) {
+                    ok = 0;  // the window's centre lies past the candidates
+                } else {
+                    const double need = static_cast<double>(sa.typical_p) * ZC;
+                    int L = static_cast<int>(c) - 1;
+                    uint32_t R = c;
+                    for (;;) {
+                        bool take_left;
+                        if (L < 0) take_left = false;
+                        else if (R >= nc) take_left = !beyond;
+                        else take_left = gv(L) - gC <= gC - gv(R);
+                        if (!take_left && R >= nc) {  // the next one lies past the candidates
+                            ok = 0;
+                            break;
+                        }
+                        if (take_left) cum += wf[L--];
+                        else cum += wf[R++];
+                        if (cum >= need || (L < 0 && R >= nc && !beyond)) break;
+                    }
+                    wlo = static_cast<uint32_t>(L + 1);
+                    whi = R;
+                }
+            }
+            ok = __shfl_sync(kFull, ok, 0);
+            if (!ok) {
+                resolved = false;
+            } else {
+                lo = __shfl_sync(kFull, wlo, 0);
+                hi = __shfl_sync(kFull, whi, 0);
+                ZW = __shfl_sync(kFull, cum, 0);
+                beyond = false;
+            }
+        }
+        uint32_t end = hi;
+        if (resolved && topp) {
+            // the shortest prefix of the window whose mass reaches top_p
+            const double need = static_cast<double>(sa.top_p) * ZW;
+            double carry = 0.0;
+            uint32_t found = 0;
+            for (uint32_t b = lo; b < hi && !found; b += 32) {
+                const uint32_t j = b + lane;
+                double v = j < hi ? static_cast<double>(wf[j]) : 0.0;
+#pragma unroll
+                for (int m = 1; m < 32; m <<= 1) {
+                    const double o = __shfl_up_sync(kFull, v, m);
+                    if (lane >= m) v += o;
+                }
+                v += carry;
+                const uint32_t hit = __ballot_sync(kFull, j < hi && v >= need);
+                if (hit) found = b + __ffs(hit);
+                carry = __shfl_sync(kFull, v, 31);
+            }
+            if (found) {
+                end = found;
+                beyond = false;
+            } else if (beyond) {
+                resolved = false;  // the nucleus runs past the candidates
+            } else {
+                end = hi;  // rounding kept the total below top_p
+            }
+        }
+        double thr_mp = -INFINITY;
+        if (resolved && sa.min_p > 0.0f) {
+            // P_j >= min_p * P_max: wf_j >= min_p * wf_lo
+            thr_mp = static_cast<double>(M) + static_cast<double>(Tf) * log(static_cast<double>(sa.min_p));
+            if (beyond && static_cast<double>(xv(n - 1)) < thr_mp) beyond = false;
+            if (!beyond) {
+                const float floor_w = sa.min_p * wf[lo];
+                uint32_t keep = lo + 1;
+                for (uint32_t b = lo; b < end; b += 32) {
+                    const uint32_t j = b + lane;
+                    const uint32_t m = __ballot_sync(kFull, j < end && j > lo && wf[j] >= floor_w);
+                    if (m) keep = b + 32 - __clz(m);
+                }
+                end = keep;
+            }
+        }
+        if (resolved) {
+            if (!beyond) {
+                out.key_hi = sorted[lo];
+                out.key_lo = sorted[end - 1];
+            } else {
+                // every id at or above the value threshold
+                const double thr = fmax(thr_ns, thr_mp);
+                out.key_hi = ~0ull;
+                out.key_lo = 1ull;
+                if (thr > -INFINITY) {
+                    float f = static_cast<float>(thr);
+                    if (static_cast<double>(f) < thr) f = nextafterf(f, INFINITY);
+                    out.key_lo = static_cast<unsigned long long>(f2key(f)) << 32;
+                }
+            }
+        } else {
+            beyond_err = !nonfinite && out.u >= 0.0f && out.u < 1.0f;
+        }
+    }
+    out.valid = resolved ? 1u : 0u;
+    if (lane == 0) {
+        a.full_rows[row] = out;
+        if (beyond_err) atomicOr(a.err, kErrBeyond);
+    }
+}
+
+// Full-row draw, 1: block (row, chunk) sums the survivors' weights
+// 2^((x - M) c) (c = log2(e) / T) over its kDrawIds ids.
+template <bool kVec>
+__global__ void __launch_bounds__(kNT) full_draw_sum_kernel(TopkArgs a) {
+    __shared__ FF s_w[kWarps];
+    pdl_wait();
+    pdl_trigger();
+    const uint32_t row = blockIdx.x / a.draw_chunks;
+    const uint32_t chunk = blockIdx.x - row * a.draw_chunks;
+    const FullRow fr = a.full_rows[row];
+    if (!fr.valid) return;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t V = a.V, lo = chunk * kDrawIds, hi = min(V, lo + kDrawIds);
+    const float* x = a.logits + static_cast<size_t>(row) * V;
+    float4 q[kDrawQ];
+#pragma unroll
+    for (int i = 0; i < kDrawQ; ++i) q[i] = ld_quad<kVec>(x, lo + 4u * (tid + kNT * i), hi, -INFINITY);
+    float sum = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kDrawQ; ++i) {
+        const uint32_t e = lo + 4u * (tid + kNT * i);
+        const float f[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint64_t cd = make_cand(f2key(f[j]), e + j);
+            if (e + j < hi && cd >= fr.key_lo && cd <= fr.key_hi) sum += ex2_approx((f[j] - fr.M) * a.draw_c);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+    if (lane == 0) s_w[warp] = FF{sum, 0.0f};
+    __syncthreads();
+    if (tid == 0) {
+        FF t{0.0f, 0.0f};
+        for (int w = 0; w < kWarps; ++w) t = ff_add(t, s_w[w]);
+        a.draw_sums[static_cast<size_t>(row) * a.draw_chunks + chunk] = t;
+    }
+}
+
+// Full-row draw, 2: block r finds the chunk where u * total falls (a
+// fixed-order scan of the chunk sums), then, within it, the 1,024-id stripe,
+// the quad and the id, walking ids in ascending order; writes the id and its
+// probability weight / total.
+template <bool kVec>
+__global__ void __launch_bounds__(kNT) full_draw_find_kernel(TopkArgs a) {
+    __shared__ FF s_r[kWarps];
+    __shared__ uint32_t s_cross;
+    __shared__ int s_lastpos;
+    __shared__ uint32_t s_cstar;
+    __shared__ FF s_before, s_target, s_sbefore, s_total;
+    __shared__ float s_stripe[kWarps][kDrawQ];
+    __shared__ int s_istar;
+    pdl_wait();
+    pdl_trigger();
+    const uint32_t row = blockIdx.x;
+    const FullRow fr = a.full_rows[row];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (!fr.valid) {
+        if (tid == 0) { a.out_ids[row] = SEL_INVALID_ID; a.sa.out_probs[row] = __uint_as_float(0x7fc00000u); }
+        return;
+    }
+    const uint32_t V = a.V, chunks = a.draw_chunks;
+    const FF* sums = a.draw_sums + static_cast<size_t>(row) * chunks;
+    if (warp == 0) {
+        FF W{0.0f, 0.0f};
+        for (uint32_t c0 = 0; c0 < chunks; c0 += 32) {
+            const uint32_t ci = c0 + lane;
+            W = ff_add(W, ff_warp_sum(ci < chunks ? sums[ci] : FF{0.0f, 0.0f}));
+        }
+        const FF target = ff_mul_f(W, fr.u);
+        uint32_t cstar = chunks, last_pos_chunk = 0;
+        FF before{0.0f, 0.0f}, acc{0.0f, 0.0f}, before_last{0.0f, 0.0f};
+        for (uint32_t c0 = 0; c0 < chunks && cstar == chunks; c0 += 32) {
+            const uint32_t ci = c0 + lane;
+            const FF t = ci < chunks ? sums[ci] : FF{0.0f, 0.0f};
+            const FF incl = ff_add(acc, ff_warp_scan(t));
+            FF excl = ff_shfl_up(incl, 1);
+            if (lane == 0) excl = acc;
+            const uint32_t pos = __ballot_sync(kFull, ci < chunks && t.hi > 0.0f);
+            if (pos) {
+                const int l = 31 - __clz(pos);
+                last_pos_chunk = c0 + l;
+                before_last = ff_shfl(excl, l);
+            }
+            const uint32_t hit = __ballot_sync(kFull, ci < chunks && t.hi > 0.0f && ff_lt(target, incl));
+            if (hit) {
+                const int l = __ffs(hit) - 1;
+                cstar = c0 + l;
+                before = ff_shfl(excl, l);
+            }
+            acc = ff_shfl(incl, 31);
+        }
+        if (cstar == chunks) {  // rounding: the last chunk with mass
+            cstar = last_pos_chunk;
+            before = before_last;
+        }
+        if (lane == 0) {
+            s_cstar = cstar;
+            s_before = before;
+            s_target = target;
+            s_total = W;
+            s_lastpos = -1;
+        }
+    }
+    __syncthreads();
+    // the hit chunk again (from L2): stripe i holds ids [clo + 1024 i,
+    // clo + 1024 (i + 1)), thread t its quad at 4 t; id order is stripe,
+    // thread, lane
+    const uint32_t clo = s_cstar * kDrawIds;
+    const uint32_t chi = min(V, clo + kDrawIds);
+    const FF target = s_target;
+    const float* x = a.logits + static_cast<size_t>(row) * V;
+    float4 q[kDrawQ];
+#pragma unroll
+    for (int i = 0; i < kDrawQ; ++i) q[i] = ld_quad<kVec>(x, clo + 4u * (tid + kNT * i), chi, -INFINITY);
+    auto weight = [&](float f, uint32_t id) {
+        const uint64_t cd = make_cand(f2key(f), id);
+        return (id < chi && cd >= fr.key_lo && cd <= fr.key_hi) ? ex2_approx((f - fr.M) * a.draw_c) : 0.0f;
+    };
+    float qsum[kDrawQ];
+    int lp = -1;
+#pragma unroll
+    for (int i = 0; i < kDrawQ; ++i) {
+        const uint32_t e = clo + 4u * (tid + kNT * i);
+        const float f[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+        float w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            w[j] = weight(f[j], e + j);
+            if (w[j] > 0.0f) lp = static_cast<int>(e + j);
+        }
+        qsum[i] = (w[0] + w[1]) + (w[2] + w[3]);
+    }
+    {
+        const int wlp = __reduce_max_sync(kFull, lp);
+        if (lane == 0 && wlp >= 0) atomicMax(&s_lastpos, wlp);
+    }
+#pragma unroll
+    for (int i = 0; i < kDrawQ; ++i) {
+        float v = qsum[i];
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(kFull, v, m);
+        if (lane == 0) s_stripe[warp][i] = v;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        FF t{0.0f, 0.0f};
+        if (lane < kDrawQ)
+            for (int ww = 0; ww < kWarps; ++ww) t = ff_add(t, FF{s_stripe[ww][lane], 0.0f});
+        const FF incl = ff_add(s_before, ff_warp_scan(t));
+        FF excl = ff_shfl_up(incl, 1);
+        if (lane == 0) excl = s_before;
+        const uint32_t valid = (1u << kDrawQ) - 1u;
+        const uint32_t pos = __ballot_sync(kFull, lane < kDrawQ && t.hi > 0.0f) & valid;
+        const uint32_t hit = __ballot_sync(kFull, lane < kDrawQ && t.hi > 0.0f && ff_lt(target, incl)) & valid;
+        const int l = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+        if (lane == 0) {
+            s_istar = l;
+            s_cross = 0xFFFFFFFFu;
+        }
+        if (l >= 0) {
+            const FF b = ff_shfl(excl, l);
+            if (lane == 0) s_sbefore = b;
+        }
+    }
+    __syncthreads();
+    const int istar = s_istar;
+    const float total = s_total.hi + s_total.lo;
+    if (istar >= 0) {
+        float mine = 0.0f;
+        float4 cp = q[0];
+#pragma unroll
+        for (int i = 0; i < kDrawQ; ++i)
+            if (i == istar) { mine = qsum[i]; cp = q[i]; }
+        const FF incl = ff_warp_scan(FF{mine, 0.0f});
+        if (lane == 31) s_r[warp] = incl;
+        __syncthreads();
+        FF start = s_sbefore;
+        for (int ww = 0; ww < warp; ++ww) start = ff_add(start, s_r[ww]);
+        FF excl = ff_shfl_up(incl, 1);
+        if (lane == 0) excl = FF{0.0f, 0.0f};
+        start = ff_add(start, excl);
+        const FF fin = ff_add(start, FF{mine, 0.0f});
+        const uint32_t hit = __ballot_sync(kFull, mine > 0.0f && ff_lt(target, fin));
+        if (lane == 0 && hit) atomicMin(&s_cross, static_cast<uint32_t>(tid) + static_cast<uint32_t>(__ffs(hit) - 1));
+        __syncthreads();
+        if (static_cast<uint32_t>(tid) == s_cross) {
+            const uint32_t e = clo + 4u * (static_cast<uint32_t>(tid) + kNT * istar);
+            const float f[4] = {cp.x, cp.y, cp.z, cp.w};
+            uint32_t pick = 0xFFFFFFFFu, last = 0xFFFFFFFFu;
+            float pw = 0.0f, lw = 0.0f;
+            FF cdf = start;
+            for (int j = 0; j < 4; ++j) {
+                const float w = weight(f[j], e + j);
+                cdf = ff_add(cdf, FF{w, 0.0f});
+                if (w > 0.0f) { last = e + j; lw = w; }
+                if (pick == 0xFFFFFFFFu && w > 0.0f && ff_lt(target, cdf)) { pick = e + j; pw = w; }
+            }
+            if (pick == 0xFFFFFFFFu) { pick = last; pw = lw; }
+            a.out_ids[row] = pick;
+            a.sa.out_probs[row] = pw / total;
+        }
+    }
+    if (tid == 0 && (istar < 0 || s_cross == 0xFFFFFFFFu)) {
+        // no crossing found (rounding): the last id with mass in the chunk
+        const uint32_t id = s_lastpos >= 0 ? static_cast<uint32_t>(s_lastpos) : clo;
+        a.out_ids[row] = id;
+        a.sa.out_probs[row] = weight(x[id], id) / total;
+    }
+}
+
 // Run the selection and sampling code once on synthetic candidates in
 // shared memory, writing nothing: the finishing blocks start (programmatic
 // dependent launch) while the main launch still runs, and this brings their
@@ -1046,12 +1517,46 @@ __global__ void __launch_bounds__(kNT) topk_finish_kernel(TopkArgs a) {
         nsig_thr = static_cast<double>(key2f(cand_key(s.sorted[0]))) -
                    static_cast<double>(a.sa.top_n_sigma) * sqrt(var);
     }
-    write_row<kSample>(s.sorted, reinterpret_cast<float*>(s.buf), a, row, n < k ? n : k, nf != 0, nsig_thr);
+    if (kSample && a.full_row) {
+        // the row's exponent sum Z and mean log-weight over all V, from the
+        // chunk sums (in double; every warp computes them)
+        const float4* fp = a.full_parts + static_cast<size_t>(row) * a.stride;
+        float M = -INFINITY;
+        for (uint32_t c = lane; c < chunks; c += 32) M = fmaxf(M, fp[c].x);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+        const double c2 = static_cast<double>(a.full_cf);
+        double z = 0.0, q = 0.0;
+        for (uint32_t c = lane; c < chunks; c += 32) {
+            const float4 pc = fp[c];
+            const double sh = (static_cast<double>(pc.x) - M) * c2;  // log2 of the rescale
+            const double f = exp2(sh);
+            const double sc = static_cast<double>(pc.y) + static_cast<double>(pc.z);
+            z += f * sc;
+            q += f * (static_cast<double>(pc.w) + sc * sh);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            z += __shfl_xor_sync(kFull, z, o);
+            q += __shfl_xor_sync(kFull, q, o);
+        }
+        const double gbar = z > 0.0 ? q / z * 0.6931471805599453 : 0.0;  // natural units
+        double sigma = 0.0;
+        if (a.want_moments) {
+            const double Vd = static_cast<double>(a.V);
+            const double mean_d = mo1 / Vd;
+            sigma = sqrt(fmax(mo2 / Vd - mean_d * mean_d, 0.0));
+        }
+        if (tid < 32)
+            full_row_plan(s.sorted, reinterpret_cast<float*>(s.buf), n < k ? n : k, row, nf != 0, a, z, gbar, sigma);
+    } else {
+        write_row<kSample>(s.sorted, reinterpret_cast<float*>(s.buf), a, row, n < k ? n : k, nf != 0, nsig_thr);
+    }
     if (tid == 0) atomicAdd(a.err + 1, 1u);  // rows finished (self-check)
 }
 
 struct TopkLayout {
-    size_t row_tau, pools, flags, moments, lists, total;
+    size_t row_tau, pools, flags, moments, full_parts, full_rows, draw_sums, lists, total;
     uint32_t stride, list_len;
 };
 
@@ -1066,7 +1571,10 @@ TopkLayout topk_layout(uint32_t rows, uint32_t V, uint32_t k) {
     l.pools = l.row_tau + ws_counters_bytes(rows);
     l.flags = l.pools + align_up(static_cast<size_t>(rows) * l.stride * kPool * 4u, 256);
     l.moments = l.flags + align_up(static_cast<size_t>(rows) * l.stride * 4u, 256);
-    l.lists = l.moments + align_up(static_cast<size_t>(rows) * l.stride * 16u, 256);
+    l.full_parts = l.moments + align_up(static_cast<size_t>(rows) * l.stride * 16u, 256);
+    l.full_rows = l.full_parts + align_up(static_cast<size_t>(rows) * l.stride * 16u, 256);
+    l.draw_sums = l.full_rows + align_up(static_cast<size_t>(rows) * sizeof(FullRow), 256);
+    l.lists = l.draw_sums + align_up(static_cast<size_t>(rows) * ceil_div(V, kDrawIds) * sizeof(FF), 256);
     l.total = l.lists + static_cast<size_t>(rows) * l.stride * l.list_len * 8u;
     return l;
 }
@@ -1098,7 +1606,8 @@ SampleArgs sample_args(const sel_sample_params& p, const float* uniforms, float*
 
 template <bool kSample>
 sel_status launch_topk(const float* d_logits, uint32_t rows, uint32_t V, uint32_t k, float* d_out_vals,
-                       uint32_t* d_out_ids, void* d_ws, size_t ws_bytes, const SampleArgs& sa, cudaStream_t stream) {
+                       uint32_t* d_out_ids, void* d_ws, size_t ws_bytes, const SampleArgs& sa, cudaStream_t stream,
+                       bool full_row = false) {
     const TopkLayout l = topk_layout(rows, V, k);
     if (!d_ws) return SEL_EINVAL;
     if (reinterpret_cast<uintptr_t>(d_ws) % SEL_WS_ALIGN) return SEL_EINVAL;
@@ -1124,6 +1633,16 @@ sel_status launch_topk(const float* d_logits, uint32_t rows, uint32_t V, uint32_
     a.chunk_flags = reinterpret_cast<uint32_t*>(ws + l.flags);
     a.moments = reinterpret_cast<float*>(ws + l.moments);
     a.want_moments = (kSample && sa.top_n_sigma > 0.0f) ? 1u : 0u;
+    a.full_row = (kSample && full_row) ? 1u : 0u;
+    a.full_parts = reinterpret_cast<float4*>(ws + l.full_parts);
+    a.full_rows = reinterpret_cast<FullRow*>(ws + l.full_rows);
+    a.draw_sums = reinterpret_cast<FF*>(ws + l.draw_sums);
+    a.draw_chunks = ceil_div(V, kDrawIds);
+    if (kSample && sa.temperature > 0.0f) {
+        const double Tf = sa.order == SEL_ORDER_TEMP_LAST ? 1.0 : static_cast<double>(sa.temperature);
+        a.full_cf = static_cast<float>(1.4426950408889634 / Tf);
+        a.draw_c = static_cast<float>(1.4426950408889634 / static_cast<double>(sa.temperature));
+    }
     a.lists = reinterpret_cast<uint64_t*>(ws + l.lists);
     a.stride = l.stride;
     a.list_len = l.list_len;
@@ -1141,6 +1660,17 @@ sel_status launch_topk(const float* d_logits, uint32_t rows, uint32_t V, uint32_
                         : launch_pdl(topk_kernel<false>, grid, dim3(kNT), kStage, stream, a);
     if (e != cudaSuccess) return SEL_ECUDA;
     e = launch_pdl(topk_finish_kernel<kSample>, dim3(rows), dim3(kNT), 0, stream, a);
+    if (e != cudaSuccess) return SEL_ECUDA;
+    if (kSample && full_row) {
+        // the draw over the survivors, in ascending id
+        const uint64_t dblocks = static_cast<uint64_t>(rows) * a.draw_chunks;
+        if (dblocks > 0x7fffffffull) return SEL_EUNSUPPORTED;
+        e = vec ? launch_pdl(full_draw_sum_kernel<true>, dim3(static_cast<uint32_t>(dblocks)), dim3(kNT), 0, stream, a)
+                : launch_pdl(full_draw_sum_kernel<false>, dim3(static_cast<uint32_t>(dblocks)), dim3(kNT), 0, stream, a);
+        if (e != cudaSuccess) return SEL_ECUDA;
+        e = vec ? launch_pdl(full_draw_find_kernel<true>, dim3(rows), dim3(kNT), 0, stream, a)
+                : launch_pdl(full_draw_find_kernel<false>, dim3(rows), dim3(kNT), 0, stream, a);
+    }
     return e == cudaSuccess ? SEL_OK : SEL_ECUDA;
 }
 
@@ -1173,7 +1703,8 @@ extern "C" sel_status sel_sample(const float* d_logits, uint32_t rows, uint32_t 
     if (!policy_valid(*p)) return SEL_EINVAL;
     uint32_t k = p->top_k;
     if (T == 0.0f) k = 1;  // greedy: the top-1 candidate is the argmax
-    if (k == 0) return SEL_EUNSUPPORTED;
+    const bool full_row = k == 0;  // full-row sampling: the most probable kFullCand as candidates
+    if (full_row) k = kFullCand;
     if (k > V) k = V;
     if (k > SEL_MAX_K) return SEL_EUNSUPPORTED;
     if (rows == 0) return SEL_OK;
@@ -1182,7 +1713,7 @@ extern "C" sel_status sel_sample(const float* d_logits, uint32_t rows, uint32_t 
         reinterpret_cast<uintptr_t>(d_out_ids) % 4 || reinterpret_cast<uintptr_t>(d_out_probs) % 4)
         return SEL_EINVAL;
     const SampleArgs sa = sample_args(*p, d_uniforms, d_out_probs);
-    return launch_topk<true>(d_logits, rows, V, k, nullptr, d_out_ids, d_ws, ws_bytes, sa, stream);
+    return launch_topk<true>(d_logits, rows, V, k, nullptr, d_out_ids, d_ws, ws_bytes, sa, stream, full_row);
 }
 
 // ---------------------------------------------------------------------------

@@ -30,9 +30,10 @@
 
 namespace sel {
 
-constexpr uint32_t kErrTimeout = 1u;       // reserved (no kernel waits on another)
+constexpr uint32_t kErrTimeout = 1u;       // a bulk-copy wait gave up
 constexpr uint32_t kErrMergeShort = 2u;    // a row merge found fewer than k candidates
 constexpr uint32_t kErrListOrder = 4u;     // a chunk list was not in descending order
+constexpr uint32_t kErrBeyond = 8u;        // a full-row filter cut lay past the candidates
 
 // Wait until the previous grid in the stream has completed and its memory
 // is visible (a no-op without a programmatic dependency).

@@ -1,0 +1,140 @@
+"""Full-row sampling (sel_sample with top_k = 0) on the GPU against the CPU
+oracle. The filters act on softmax(x / T) over the whole vocabulary (the
+sampler chain of the Muser book, "Ch 21 -- Sampling, argmax, and grammar",
+21.1 and 21.7, without top-k); the draw walks the survivors in ascending id.
+
+Temperature alone, min-p and top-n-sigma are decided on every row. A top-p
+or locally typical cut is decided from the row's 256 most probable tokens;
+a row whose cut lies past them fails closed (0xFFFFFFFF, NaN) and raises
+error bit 8 -- checked here against the oracle's own nucleus sizes."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import gpu_helpers as G
+from sampling_row_fp32_gb300 import binding as B
+from sampling_row_fp32_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+CAND = 256
+ERR_BEYOND = 8
+
+
+@pytest.fixture(scope="module")
+def orc():
+    import __graft_entry__
+    __graft_entry__.build()
+    return oracle.default()
+
+
+def run(x, u, T, top_p, min_p, nsig=0.0, typ=0.0, temp_last=False, misalign=False):
+    rows, V = x.shape
+    xd = G.to_dev(x, misalign)
+    ud = G.to_dev(np.asarray(u, dtype=np.float32).reshape(rows))
+    ids = torch.full((rows,), G.SENTINEL, dtype=torch.int32, device=G.device())
+    probs = torch.full((rows,), -7.0, dtype=torch.float32, device=G.device())
+    ws = B.workspace(B.SEL_OP_SAMPLE, rows, V, 0, device=G.device())
+    prm = B.SampleParams(T, 0, top_p, min_p, B.SEL_ORDER_TEMP_LAST if temp_last else B.SEL_ORDER_TEMP_FIRST,
+                         nsig, typ)
+    B.sel_sample(xd, prm, ud, ids, probs, ws)
+    torch.cuda.synchronize()
+    return B.ids_to_numpy(ids), probs.cpu().numpy(), G.ws_error(ws)
+
+
+def nucleus_sizes(x, T, top_p):
+    """Tokens in each row's top-p nucleus (double precision)."""
+    z = x.astype(np.float64) / T
+    z -= z.max(axis=1, keepdims=True)
+    w = np.exp(z)
+    w /= w.sum(axis=1, keepdims=True)
+    c = np.cumsum(-np.sort(-w, axis=1), axis=1)
+    return (c < top_p).sum(axis=1) + 1
+
+
+def check(orc, x, u, T, top_p, min_p, nsig=0.0, typ=0.0, temp_last=False, misalign=False, decided=None):
+    gi, gp, err = run(x, u, T, top_p, min_p, nsig, typ, temp_last, misalign)
+    ref = orc.sample(x, u, T, 0, top_p, min_p, temp_last, top_n_sigma=nsig, typical_p=typ if typ > 0 else 1.0)
+    failed = (gi == G.INVALID) & (ref.ids != G.INVALID)
+    if decided is not None:
+        assert np.array_equal(~failed, decided), (np.nonzero(failed != ~decided)[0][:10])
+    assert bool(err & ERR_BEYOND) == bool(failed.any()), (err, failed.sum())
+    assert err & ~ERR_BEYOND == 0, err
+    assert np.all(np.isnan(gp[failed]))
+    keep = ~failed
+    G.assert_sample_matches(gi[keep], gp[keep], type(ref)(ref.ids[keep], ref.probs[keep], ref.margin[keep]))
+    return gi, gp, ref, failed
+
+
+@pytest.mark.parametrize("T", [0.5, 1.0, 1.7])
+@pytest.mark.parametrize("misalign", [False, True])
+def test_temperature_alone(orc, T, misalign):
+    """No filter: every row decided, the draw over all V in ascending id."""
+    x = synth.normal_rows(61, 40, 30_001, 2.0)
+    u = synth.uniforms(62, 40)
+    check(orc, x, u, T, 1.0, 0.0, misalign=misalign, decided=np.ones(40, bool))
+
+
+@pytest.mark.parametrize("min_p", [0.001, 0.05, 0.3])
+def test_min_p(orc, min_p):
+    x = synth.normal_rows(63, 40, 60_001, 3.0)
+    u = synth.uniforms(64, 40)
+    check(orc, x, u, 0.8, 1.0, min_p, decided=np.ones(40, bool))
+
+
+@pytest.mark.parametrize("nsig", [0.5, 1.0, 3.0])
+def test_top_n_sigma(orc, nsig):
+    x = synth.normal_rows(65, 32, 50_003, 2.5)
+    u = synth.uniforms(66, 32)
+    check(orc, x, u, 1.0, 1.0, 0.0, nsig=nsig, decided=np.ones(32, bool))
+
+
+def test_top_p_on_verify_batch(orc):
+    """49 x 248,320 Zipf/Gumbel rows at T 0.7, top_p 0.9: a row is decided
+    exactly when its nucleus fits the 256 candidates."""
+    x, _ = synth.workload_verify_batch()
+    u = synth.uniforms(67, 49)
+    decided = nucleus_sizes(x, 0.7, 0.9) <= CAND
+    assert decided.mean() > 0.8
+    check(orc, x, u, 0.7, 0.9, 0.0, decided=decided)
+
+
+@pytest.mark.parametrize("T,top_p", [(0.5, 0.9), (1.0, 0.5), (1.0, 0.95)])
+def test_top_p_decided_iff_nucleus_fits(orc, T, top_p):
+    x = synth.normal_rows(68, 40, 30_001, 4.0)
+    u = synth.uniforms(69, 40)
+    decided = nucleus_sizes(x, T, top_p) <= CAND
+    check(orc, x, u, T, top_p, 0.0, decided=decided)
+
+
+def test_whole_chain_on_short_rows(orc):
+    """V <= 256: the candidates hold the whole row, so every filter of the
+    chain is decided, in both temperature orders."""
+    x = synth.normal_rows(70, 30, 200, 2.0)
+    u = synth.uniforms(71, 30)
+    for last in (False, True):
+        check(orc, x, u, 0.8, 0.9, 0.02, nsig=2.0, typ=0.7, temp_last=last, decided=np.ones(30, bool))
+
+
+def test_typical_and_top_p_together(orc):
+    x = synth.normal_rows(72, 30, 20_000, 3.0)
+    u = synth.uniforms(73, 30)
+    check(orc, x, u, 0.6, 0.9, 0.0, nsig=1.0, typ=0.8)
+
+
+def test_invalid_rows(orc):
+    x = synth.normal_rows(74, 5, 9_000, 1.0)
+    x[3, 10] = np.nan
+    u = np.array([0.5, 1.0, -0.1, 0.5, 0.25], dtype=np.float32)
+    gi, gp, _, _ = check(orc, x, u, 1.0, 1.0, 0.0, decided=np.ones(5, bool))
+    assert np.all(gi[1:4] == G.INVALID) and gi[0] != G.INVALID and gi[4] != G.INVALID
+
+
+def test_draw_walks_ascending_ids(orc):
+    """Many uniforms against one row: the drawn id rises with u."""
+    row = synth.normal_rows(75, 1, 5_000, 1.5)
+    n = 2000
+    x = np.tile(row, (n, 1))
+    u = ((np.arange(n) + 0.5) / n).astype(np.float32)
+    gi, _, _, _ = check(orc, x, u, 1.0, 1.0, 0.0, decided=np.ones(n, bool))
+    assert np.all(np.diff(gi.astype(np.int64)) >= 0)
