@@ -26,7 +26,7 @@ size_t spec_diag_ws_bytes(uint32_t S, uint32_t V, uint32_t K);
 size_t spec_sampler_ws_bytes(uint32_t rows_t, uint32_t V, uint32_t top_k);
 
 // Candidates of full-row sampling (sel_sample with top_k = 0).
-constexpr uint32_t kFullRowCandidates = 256;
+constexpr uint32_t kFullRowCandidates = 64;
 
 // Workspace: a 256-byte header (word 0: error flags the kernels raise), a
 // per-row arrival counter array, then the per-op payload.

@@ -324,6 +324,70 @@ __device__ __noinline__ void radix_select_chunk(Sh& s, uint32_t* hist, const flo
     }
 }
 
+// Locally typical cut over candidates [0, nc) (one warp): score_j =
+// |g_j - gbar|; each lane ranks its candidates in (score asc, position asc)
+// order by counting, the weights are laid out in that order (byr) and
+// scanned, and the kept ids are those of rank <= the first rank whose
+// cumulative weight reaches `need`. g falls along the candidates, so the
+// kept positions form a window [lo, hi) around where g crosses gbar (up to
+// exact ties of the score, which the tolerance exempts). Returns the score
+// of the last kept id.
+__device__ float typical_window(const float* wf, const float* g, float* byr, uint32_t nc, float gbar, float need,
+                                uint32_t& lo, uint32_t& hi) {
+    const int lane = threadIdx.x & 31;
+    for (uint32_t j = lane; j < nc; j += 32) {
+        const float sj = fabsf(g[j] - gbar);
+        uint32_t r = 0;
+        for (uint32_t i = 0; i < nc; ++i) {
+            const float si = fabsf(g[i] - gbar);
+            r += (si < sj || (si == sj && i < j)) ? 1u : 0u;
+        }
+        byr[r] = wf[j];
+    }
+    __syncwarp();
+    uint32_t t = nc - 1;  // rounding kept the total below need: everything
+    float carry = 0.0f;
+    for (uint32_t b = 0; b < nc; b += 32) {
+        const uint32_t r = b + lane;
+        float v = r < nc ? byr[r] : 0.0f;
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+            const float o = __shfl_up_sync(kFull, v, m);
+            if (lane >= m) v += o;
+        }
+        v += carry;
+        const uint32_t hit = __ballot_sync(kFull, r < nc && v >= need);
+        if (hit) {
+            t = b + __ffs(hit) - 1;
+            break;
+        }
+        carry = __shfl_sync(kFull, v, 31);
+    }
+    __syncwarp();
+    // the kept positions: ranks <= t
+    uint32_t mn = nc, mx = 0;
+    float smax = 0.0f;
+    for (uint32_t j = lane; j < nc; j += 32) {
+        const float sj = fabsf(g[j] - gbar);
+        uint32_t r = 0;
+        for (uint32_t i = 0; i < nc; ++i) {
+            const float si = fabsf(g[i] - gbar);
+            r += (si < sj || (si == sj && i < j)) ? 1u : 0u;
+        }
+        if (r <= t) {
+            mn = min(mn, j);
+            mx = max(mx, j + 1u);
+            smax = fmaxf(smax, sj);
+        }
+    }
+    lo = __reduce_min_sync(kFull, mn);
+    hi = __reduce_max_sync(kFull, mx);
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) smax = fmaxf(smax, __shfl_xor_sync(kFull, smax, m));
+    __syncwarp();
+    return smax;
+}
+
 // Sampling epilogue on the sorted candidates sorted[0..n): one warp, in
 // the order of the sampler chain.
 //  - top-n-sigma (nsig_thr > -inf): the candidates whose logit reaches the
@@ -334,12 +398,11 @@ __device__ __noinline__ void radix_select_chunk(Sh& s, uint32_t* hist, const flo
 //    and their inclusive prefix sums pf, pd (in `scratch`, 4 * SEL_MAX_K
 //    floats).
 //  - Locally typical (0 < typical_p < 1): with P_j = wf_j / S and
-//    H = -sum P ln P, -ln P_j - H = gbar - g_j, gbar = sum_j P_j g_j. g falls
-//    along the candidates, so the score |gbar - g_j| falls then rises, and
-//    the ids in (score asc, position asc) order grow a window outward from the
-//    first j with g_j <= gbar, the left (more probable) side winning ties, up
-//    to the first size whose mass reaches typical_p * S. The prefix sums are
-//    taken again over the window [lo, hi).
+//    H = -sum P ln P, -ln P_j - H = gbar - g_j, gbar = sum_j P_j g_j, so the
+//    score is |g_j - gbar|; the ids of smallest score, in (score asc,
+//    position asc) order, are kept until their mass reaches typical_p * S
+//    (typical_window). g falls along the candidates, so they form a window
+//    [lo, hi); the prefix sums are taken again over it.
 //  - top-p keeps the shortest prefix of the window with pf >= top_p * its
 //    total; min-p keeps wf_j >= min_p * wf_lo (wf falls, so the survivors
 //    stay a prefix); the draw takes the first j with u * pd_end < pd_j.
@@ -415,47 +478,19 @@ __device__ void sample_epilogue(const uint64_t* sorted, float* scratch, uint32_t
     uint32_t lo = 0, hi = nc;
     if (sa.typical_p > 0.0f && sa.typical_p < 1.0f) {
         const float S = pf[nc - 1];
+        float* g = pd;    // scratch until the window's prefix sums are taken
+        float* byr = pf;  // the same
         float acc = 0.0f;
-        for (uint32_t b = 0; b < nc; b += 32) {
-            const uint32_t j = b + lane;
-            if (j < nc) acc += wf[j] * ((key2f(cand_key(sorted[j])) - x0) / Tf);
+        for (uint32_t j = lane; j < nc; j += 32) {
+            const float gj = (key2f(cand_key(sorted[j])) - x0) / Tf;
+            g[j] = gj;
+            acc += wf[j] * gj;
         }
 #pragma unroll
         for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(kFull, acc, m);
+        __syncwarp();
         const float gbar = acc / S;
-        uint32_t c = nc;
-        for (uint32_t b = 0; b < nc; b += 32) {
-            const uint32_t j = b + lane;
-            const uint32_t hit =
-                __ballot_sync(kFull, j < nc && (key2f(cand_key(sorted[j])) - x0) / Tf <= gbar);
-            if (hit) {
-                c = b + __ffs(hit) - 1;
-                break;
-            }
-        }
-        if (lane == 0) {
-            const float need = sa.typical_p * S;
-            int L = static_cast<int>(c) - 1;
-            uint32_t R = c;
-            float cum = 0.0f;
-            for (;;) {
-                bool take_left;
-                if (L < 0) take_left = false;
-                else if (R >= nc) take_left = true;
-                else {
-                    const float sl = (key2f(cand_key(sorted[L])) - x0) / Tf - gbar;
-                    const float sr = gbar - (key2f(cand_key(sorted[R])) - x0) / Tf;
-                    take_left = sl <= sr;
-                }
-                if (take_left) cum += wf[L--];
-                else cum += wf[R++];
-                if (cum >= need || (L < 0 && R >= nc)) break;
-            }
-            lo = static_cast<uint32_t>(L + 1);
-            hi = R;
-        }
-        lo = __shfl_sync(kFull, lo, 0);
-        hi = __shfl_sync(kFull, hi, 0);
+        typical_window(wf, g, byr, nc, gbar, sa.typical_p * S, lo, hi);
         scan(lo, hi, false);
     }
     // top-p: the shortest prefix of the window whose cumulative P reaches top_p
@@ -825,19 +860,36 @@ __global__ void __launch_bounds__(kNT, 5) topk_kernel(TopkArgs a) {
         float fs = 0.0f, fq = 0.0f;
         if (tmax > -INFINITY && tmax < INFINITY && mb < INFINITY) {
             float ts = 0.0f, tq = 0.0f;
+            const bool want_q = a.sa.typical_p > 0.0f && a.sa.typical_p < 1.0f;
+            if (kVec && n_real == kUnitMax) {
+                // a whole chunk: no ragged end to skip
 #pragma unroll
-            for (int sl = 0; sl < kVPT; ++sl) {
-                const uint32_t o = 4u * (tid + kNT * sl);
-                if (o < n_real) {
+                for (int sl = 0; sl < kVPT; ++sl) {
                     const float4 q = stage[tid + kNT * sl];
                     const float f[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        if (o + j < n_real) {
-                            const float arg = (f[j] - tmax) * c;
-                            const float w = ex2_approx(arg);
-                            ts += w;
-                            tq = __fmaf_rn(w, arg, tq);
+                        const float arg = (f[j] - tmax) * c;
+                        const float w = ex2_approx(arg);
+                        ts += w;
+                        if (want_q) tq = __fmaf_rn(w, arg, tq);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int sl = 0; sl < kVPT; ++sl) {
+                    const uint32_t o = 4u * (tid + kNT * sl);
+                    if (o < n_real) {
+                        const float4 q = stage[tid + kNT * sl];
+                        const float f[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            if (o + j < n_real) {
+                                const float arg = (f[j] - tmax) * c;
+                                const float w = ex2_approx(arg);
+                                ts += w;
+                                if (want_q) tq = __fmaf_rn(w, arg, tq);
+                            }
                         }
                     }
                 }
@@ -1058,50 +1110,28 @@ __device__ void full_row_plan(const uint64_t* sorted, float* scratch, uint32_t n
         uint32_t lo = 0, hi = nc;
         double ZW = ZC;
         if (resolved && typical && (nc > 1 || beyond)) {
-            // the window grows from the first candidate with g <= gbar, the
-            // more probable side winning ties
-            uint32_t c = nc;
-            for (uint32_t b = 0; b < nc; b += 32) {
-                const uint32_t j = b + lane;
-                const uint32_t hit = __ballot_sync(kFull, j < nc && static_cast<double>(gv(j)) <= gC);
-                if (hit) {
-                    c = b + __ffs(hit) - 1;
-                    break;
-                }
-            }
-            uint32_t ok = 1, wlo = 0, whi = 0;
-            double cum = 0.0;
-            if (lane == 0) {
-                if (c == nc && beyond) {
-                    ok = 0;  // the window's centre lies past the candidates
-                } else {
-                    const double need = static_cast<double>(sa.typical_p) * ZC;
-                    int L = static_cast<int>(c) - 1;
-                    uint32_t R = c;
-                    for (;;) {
-                        bool take_left;
-                        if (L < 0) take_left = false;
-                        else if (R >= nc) take_left = !beyond;
-                        else take_left = gv(L) - gC <= gC - gv(R);
-                        if (!take_left && R >= nc) {  // the next one lies past the candidates
-                            ok = 0;
-                            break;
-                        }
-                        if (take_left) cum += wf[L--];
-                        else cum += wf[R++];
-                        if (cum >= need || (L < 0 && R >= nc && !beyond)) break;
-                    }
-                    wlo = static_cast<uint32_t>(L + 1);
-                    whi = R;
-                }
-            }
-            ok = __shfl_sync(kFull, ok, 0);
-            if (!ok) {
-                resolved = false;
+            // the candidates' window; exact when every id past the
+            // candidates scores above (or ties, later in position) the last
+            // kept one: their g is at most g_{nc-1}, so their score is at
+            // least gC - g_{nc-1}
+            float* g = scratch + kFullCand;
+            float* byr = g + kFullCand;
+            for (uint32_t j = lane; j < nc; j += 32) g[j] = gv(j);
+            __syncwarp();
+            const float need = static_cast<float>(static_cast<double>(sa.typical_p) * ZC);
+            uint32_t wlo = 0, whi = 0;
+            const float s_last = typical_window(wf, g, byr, nc, static_cast<float>(gC), need, wlo, whi);
+            double mass = 0.0;
+            for (uint32_t j = wlo + lane; j < whi; j += 32) mass += wf[j];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mass += __shfl_xor_sync(kFull, mass, o);
+            const double beyond_min = fmax(gC - static_cast<double>(gv(nc - 1)), 0.0);
+            if (beyond && !(mass >= static_cast<double>(need) && beyond_min >= static_cast<double>(s_last))) {
+                resolved = false;  // the window may run past the candidates
             } else {
-                lo = __shfl_sync(kFull, wlo, 0);
-                hi = __shfl_sync(kFull, whi, 0);
-                ZW = __shfl_sync(kFull, cum, 0);
+                lo = wlo;
+                hi = whi;
+                ZW = mass;
                 beyond = false;
             }
         }
@@ -1175,6 +1205,27 @@ __device__ void full_row_plan(const uint64_t* sorted, float* scratch, uint32_t n
     }
 }
 
+// The survivor test of a FullRow by value, with the ids only at the two
+// boundary values: c = (key(x) << 32 | ~id) in [key_lo, key_hi].
+struct Members {
+    float vlo, vhi;
+    uint32_t idlo, idhi;
+    bool has_lo, has_hi;
+    __device__ explicit Members(const FullRow& fr) {
+        has_lo = (fr.key_lo >> 32) >= kKeyMinFinite;
+        has_hi = fr.key_hi != ~0ull;
+        vlo = has_lo ? key2f(static_cast<uint32_t>(fr.key_lo >> 32)) : -INFINITY;
+        vhi = has_hi ? key2f(static_cast<uint32_t>(fr.key_hi >> 32)) : INFINITY;
+        idlo = cand_id(fr.key_lo);
+        idhi = cand_id(fr.key_hi);
+    }
+    __device__ __forceinline__ bool operator()(float x, uint32_t id) const {
+        const bool above = !has_lo || x > vlo || (x == vlo && id <= idlo);
+        const bool below = !has_hi || x < vhi || (x == vhi && id >= idhi);
+        return above && below;
+    }
+};
+
 // Full-row draw, 1: block (row, chunk) sums the survivors' weights
 // 2^((x - M) c) (c = log2(e) / T) over its kDrawIds ids.
 template <bool kVec>
@@ -1188,6 +1239,19 @@ __global__ void __launch_bounds__(kNT) full_draw_sum_kernel(TopkArgs a) {
     if (!fr.valid) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t V = a.V, lo = chunk * kDrawIds, hi = min(V, lo + kDrawIds);
+    const Members member(fr);
+    // a chunk whose logits all lie below the survivors (the main launch's
+    // chunk maxima tell) holds none: it is not read
+    if (member.has_lo) {
+        const uint32_t c0 = lo / a.chunk_elems, c1 = (hi - 1u) / a.chunk_elems;
+        float mx = -INFINITY;
+        for (uint32_t cc = c0; cc <= c1; ++cc)
+            mx = fmaxf(mx, a.full_parts[static_cast<size_t>(row) * a.stride + cc].x);
+        if (mx < member.vlo) {
+            if (tid == 0) a.draw_sums[static_cast<size_t>(row) * a.draw_chunks + chunk] = FF{0.0f, 0.0f};
+            return;
+        }
+    }
     const float* x = a.logits + static_cast<size_t>(row) * V;
     float4 q[kDrawQ];
 #pragma unroll
@@ -1198,10 +1262,8 @@ __global__ void __launch_bounds__(kNT) full_draw_sum_kernel(TopkArgs a) {
         const uint32_t e = lo + 4u * (tid + kNT * i);
         const float f[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint64_t cd = make_cand(f2key(f[j]), e + j);
-            if (e + j < hi && cd >= fr.key_lo && cd <= fr.key_hi) sum += ex2_approx((f[j] - fr.M) * a.draw_c);
-        }
+        for (int j = 0; j < 4; ++j)
+            if (e + j < hi && member(f[j], e + j)) sum += ex2_approx((f[j] - fr.M) * a.draw_c);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
@@ -1290,9 +1352,9 @@ __global__ void __launch_bounds__(kNT) full_draw_find_kernel(TopkArgs a) {
     float4 q[kDrawQ];
 #pragma unroll
     for (int i = 0; i < kDrawQ; ++i) q[i] = ld_quad<kVec>(x, clo + 4u * (tid + kNT * i), chi, -INFINITY);
+    const Members member(fr);
     auto weight = [&](float f, uint32_t id) {
-        const uint64_t cd = make_cand(f2key(f), id);
-        return (id < chi && cd >= fr.key_lo && cd <= fr.key_hi) ? ex2_approx((f - fr.M) * a.draw_c) : 0.0f;
+        return (id < chi && member(f, id)) ? ex2_approx((f - fr.M) * a.draw_c) : 0.0f;
     };
     float qsum[kDrawQ];
     int lp = -1;
@@ -1530,7 +1592,7 @@ __global__ void __launch_bounds__(kNT) topk_finish_kernel(TopkArgs a) {
         for (uint32_t c = lane; c < chunks; c += 32) {
             const float4 pc = fp[c];
             const double sh = (static_cast<double>(pc.x) - M) * c2;  // log2 of the rescale
-            const double f = exp2(sh);
+            const double f = ex2_approx(static_cast<float>(sh));
             const double sc = static_cast<double>(pc.y) + static_cast<double>(pc.z);
             z += f * sc;
             q += f * (static_cast<double>(pc.w) + sc * sh);

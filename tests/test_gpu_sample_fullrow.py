@@ -4,7 +4,7 @@ sampler chain of the Muser book, "Ch 21 -- Sampling, argmax, and grammar",
 21.1 and 21.7, without top-k); the draw walks the survivors in ascending id.
 
 Temperature alone, min-p and top-n-sigma are decided on every row. A top-p
-or locally typical cut is decided from the row's 256 most probable tokens;
+or locally typical cut is decided from the row's 64 most probable tokens;
 a row whose cut lies past them fails closed (0xFFFFFFFF, NaN) and raises
 error bit 8 -- checked here against the oracle's own nucleus sizes."""
 import numpy as np
@@ -17,7 +17,7 @@ from sampling_row_fp32_gb300 import binding as B
 from sampling_row_fp32_gb300 import synth
 
 pytestmark = pytest.mark.gpu
-CAND = 256
+CAND = 64
 ERR_BEYOND = 8
 
 
@@ -91,11 +91,11 @@ def test_top_n_sigma(orc, nsig):
 
 def test_top_p_on_verify_batch(orc):
     """49 x 248,320 Zipf/Gumbel rows at T 0.7, top_p 0.9: a row is decided
-    exactly when its nucleus fits the 256 candidates."""
+    exactly when its nucleus fits the 64 candidates."""
     x, _ = synth.workload_verify_batch()
     u = synth.uniforms(67, 49)
     decided = nucleus_sizes(x, 0.7, 0.9) <= CAND
-    assert decided.mean() > 0.8
+    assert decided.mean() > 0.6
     check(orc, x, u, 0.7, 0.9, 0.0, decided=decided)
 
 
@@ -108,9 +108,9 @@ def test_top_p_decided_iff_nucleus_fits(orc, T, top_p):
 
 
 def test_whole_chain_on_short_rows(orc):
-    """V <= 256: the candidates hold the whole row, so every filter of the
+    """V <= 64: the candidates hold the whole row, so every filter of the
     chain is decided, in both temperature orders."""
-    x = synth.normal_rows(70, 30, 200, 2.0)
+    x = synth.normal_rows(70, 30, 60, 2.0)
     u = synth.uniforms(71, 30)
     for last in (False, True):
         check(orc, x, u, 0.8, 0.9, 0.02, nsig=2.0, typ=0.7, temp_last=last, decided=np.ones(30, bool))
