@@ -729,7 +729,7 @@ __device__ __forceinline__ void write_row(const uint64_t* sorted, float* scratch
 // nonfinite flag, and folds its bound into the row's slot (atomic max). The
 // chunk is staged in shared memory (one bulk copy for aligned rows), so a
 // survivor's value is read back by its offset.
-template <bool kVec>
+template <bool kVec, bool kExtra>
 __global__ void __launch_bounds__(kNT, 5) topk_kernel(TopkArgs a) {
     extern __shared__ float4 stage[];  // the chunk: kUnitMax floats
     __shared__ ChunkShared s;
@@ -778,7 +778,7 @@ __global__ void __launch_bounds__(kNT, 5) topk_kernel(TopkArgs a) {
     const bool whole = !kVec || n_real == kUnitMax;
     // top-n-sigma: sums of d = x - x_0 and d^2 over the chunk's logits (x_0 the
     // row's first logit, a shift against cancellation), two chains each
-    const bool moments = a.want_moments != 0u;
+    const bool moments = kExtra && a.want_moments != 0u;
     const float x_0 = moments ? rowp[0] : 0.0f;
     float m1[2] = {0.0f, 0.0f}, m2[2] = {0.0f, 0.0f};
 #pragma unroll
@@ -848,7 +848,7 @@ __global__ void __launch_bounds__(kNT, 5) topk_kernel(TopkArgs a) {
         reinterpret_cast<float4*>(a.moments)[static_cast<size_t>(t.row) * a.stride + t.chunk] =
             make_float4(t1.hi, t1.lo, t2.hi, t2.lo);
     }
-    if (a.full_row) {
+    if (kExtra && a.full_row) {
         // Full-row sampling: the chunk's max m and, over its logits, the sums
         // of w = 2^((x - m) c) and of w (x - m) c (c = log2(e) / T), each
         // thread first relative to its own max (its real logits only)
@@ -1465,7 +1465,7 @@ __device__ void warm_finish(FinishShared& s, const TopkArgs& a) {
     __syncthreads();
 }
 
-template <bool kSample>
+template <bool kSample, bool kFull>
 __global__ void __launch_bounds__(kNT) topk_finish_kernel(TopkArgs a) {
     __shared__ FinishShared s;
     warm_finish<kSample>(s, a);
@@ -1579,7 +1579,7 @@ __global__ void __launch_bounds__(kNT) topk_finish_kernel(TopkArgs a) {
         nsig_thr = static_cast<double>(key2f(cand_key(s.sorted[0]))) -
                    static_cast<double>(a.sa.top_n_sigma) * sqrt(var);
     }
-    if (kSample && a.full_row) {
+    if constexpr (kSample && kFull) {
         // the row's exponent sum Z and mean log-weight over all V, from the
         // chunk sums (in double; every warp computes them)
         const float4* fp = a.full_parts + static_cast<size_t>(row) * a.stride;
@@ -1716,12 +1716,22 @@ sel_status launch_topk(const float* d_logits, uint32_t rows, uint32_t V, uint32_
     const dim3 grid(static_cast<uint32_t>(blocks));
     constexpr size_t kStage = static_cast<size_t>(kUnitMax) * 4u;
     static const bool attr_ok =
-        set_dynamic_smem(topk_kernel<true>, kStage) && set_dynamic_smem(topk_kernel<false>, kStage);
+        set_dynamic_smem(topk_kernel<true, false>, kStage) && set_dynamic_smem(topk_kernel<false, false>, kStage) &&
+        set_dynamic_smem(topk_kernel<true, true>, kStage) && set_dynamic_smem(topk_kernel<false, true>, kStage);
     if (!attr_ok) return SEL_ECUDA;
-    cudaError_t e = vec ? launch_pdl(topk_kernel<true>, grid, dim3(kNT), kStage, stream, a)
-                        : launch_pdl(topk_kernel<false>, grid, dim3(kNT), kStage, stream, a);
+    // the chunk moments and full-row sums live in their own instances, out
+    // of the plain path
+    const bool extra = a.want_moments || a.full_row;
+    cudaError_t e;
+    if (extra)
+        e = vec ? launch_pdl(topk_kernel<true, true>, grid, dim3(kNT), kStage, stream, a)
+                : launch_pdl(topk_kernel<false, true>, grid, dim3(kNT), kStage, stream, a);
+    else
+        e = vec ? launch_pdl(topk_kernel<true, false>, grid, dim3(kNT), kStage, stream, a)
+                : launch_pdl(topk_kernel<false, false>, grid, dim3(kNT), kStage, stream, a);
     if (e != cudaSuccess) return SEL_ECUDA;
-    e = launch_pdl(topk_finish_kernel<kSample>, dim3(rows), dim3(kNT), 0, stream, a);
+    e = a.full_row ? launch_pdl(topk_finish_kernel<kSample, true>, dim3(rows), dim3(kNT), 0, stream, a)
+                   : launch_pdl(topk_finish_kernel<kSample, false>, dim3(rows), dim3(kNT), 0, stream, a);
     if (e != cudaSuccess) return SEL_ECUDA;
     if (kSample && full_row) {
         // the draw over the survivors, in ascending id
