@@ -421,13 +421,16 @@ def extra_ops(B, dev, xs, drafts, tok, stream):
     return out
 
 
-OP_KERNELS = {  # ncu kernel-name patterns of each op's launches
-    "argmax": ["argmax_kernel"],
-    "topk": ["topk_kernel<1, 0>", "topk_kernel<0, 0>"],
-    "sample": ["topk_kernel<1, 1>", "topk_kernel<0, 1>"],
-    "spec_rejection": ["spec_phase1_kernel<1, 1>", "spec_phase1_kernel<0, 1>", "spec_draw_kernel"],
-    "spec_argmax": ["spec_phase1_kernel<1, 0>", "spec_phase1_kernel<0, 0>"],
-}
+# The launches of one eager step, in order, with the op each belongs to and
+# a piece of its kernel name (ncu prints "...<1, 0>" for template flags).
+STEP_LAUNCHES = [
+    ("argmax", "argmax_kernel"), ("argmax", "argmax_finish_kernel"),
+    ("topk", "topk_kernel"), ("topk", "topk_finish_kernel<0"),
+    ("sample", "topk_kernel"), ("sample", "topk_finish_kernel<1"),
+    ("spec_rejection", "spec_phase1_kernel"), ("spec_rejection", "spec_rows_kernel<1"),
+    ("spec_rejection", "spec_draw_sum_kernel"), ("spec_rejection", "spec_draw_find_kernel"),
+    ("spec_argmax", "spec_phase1_kernel"), ("spec_argmax", "spec_rows_kernel<0"),
+]
 TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -461,8 +464,9 @@ def load_traffic(op_name):
 
 def write_traffic(csv_path):
     """Turn an ncu CSV of dram__bytes_read.sum / dram__bytes_write.sum per
-    launch (one eager step or more) into profiles/traffic.json: mean bytes
-    per call of each op, stamped with the current sources' fingerprint."""
+    launch (whole eager steps, from the first launch of a step) into
+    profiles/traffic.json: mean bytes per call of each op, stamped with the
+    current sources' fingerprint."""
     import csv
     import collections
     rows = list(csv.reader(open(csv_path)))
@@ -478,15 +482,21 @@ def write_traffic(csv_path):
             continue
         per_launch[r[idi]] += float(r[vi].replace(",", "")) * scale[r[ui]]
         names[r[idi]] = r[ki]
-    ops = {}
-    for op, pats in OP_KERNELS.items():
-        by_kernel = collections.defaultdict(list)
-        for lid, b in per_launch.items():
-            for p in pats:
-                if p in names[lid]:
-                    by_kernel[p].append(b)
-        if by_kernel:
-            ops[op] = round(sum(sum(v) / len(v) for v in by_kernel.values()))
+    # whole steps of STEP_LAUNCHES, in launch order; each launch's name must
+    # match its slot
+    ids = sorted(per_launch, key=int)
+    n = len(STEP_LAUNCHES)
+    steps = len(ids) // n
+    if steps == 0:
+        raise SystemExit(f"{csv_path}: fewer than {n} launches")
+    sums = collections.defaultdict(float)
+    for st in range(steps):
+        for j, (op, pat) in enumerate(STEP_LAUNCHES):
+            lid = ids[st * n + j]
+            if pat not in names[lid]:
+                raise SystemExit(f"launch {lid} is {names[lid]!r}, expected {pat!r}: not aligned to a step")
+            sums[op] += per_launch[lid]
+    ops = {op: round(v / steps) for op, v in sums.items()}
     out = {"sources": sources_fingerprint(), "unit": "bytes per call (dram read + write)",
            "source_csv": os.path.basename(csv_path), "ops": ops}
     with open(TRAFFIC_JSON, "w") as f:

@@ -12,10 +12,12 @@
 // persistent grid with static unit ranges lost 3 to 5 us to its slowest
 // blocks.
 //
-// Each block publishes one partial result for its unit in the caller's
-// workspace and takes a ticket on its row's arrival counter; the block that
-// takes the row's last ticket merges the partials in chunk order and resets
-// the counter for the next call.
+// Each block publishes its unit's partial result in the caller's workspace,
+// either as a 64-bit key folded in with a relaxed atomic maximum (red.max)
+// or as a per-chunk record at its own slot. A small finishing launch that
+// follows in the same stream reads them, in chunk order where the order
+// matters, and clears what it used for the next call: no fence, ticket or
+// last-arrival block is needed.
 //
 // Launches use programmatic dependent launch: a kernel waits for its
 // predecessor in the stream (griddepcontrol.wait) before it touches global
@@ -107,20 +109,6 @@ __device__ __forceinline__ void red_max_u32(uint32_t* p, uint32_t v) {
 }
 __device__ __forceinline__ void red_max_u64(unsigned long long* p, unsigned long long v) {
     asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-// Arrival of one block at its row (one thread): release this block's
-// results, take a ticket, and report whether it was the row's last (the
-// caller then merges; the counter is reset for the next call).
-__device__ __forceinline__ bool segment_arrive(uint32_t* counter, uint32_t segments) {
-    __threadfence();
-    const uint32_t t = atomicAdd(counter, 1u);
-    const bool last = t == segments - 1;
-    if (last) {
-        *counter = 0u;
-        __threadfence();
-    }
-    return last;
 }
 
 // ---------------------------------------------------------------------------
