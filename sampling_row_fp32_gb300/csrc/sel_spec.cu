@@ -19,14 +19,17 @@
 //  Phase 1 (one launch over every target and draft row of every sequence):
 //    one block per row chunk (sel_units.cuh) reduces its chunk to (max, sum
 //    of exp((x - max) / T)) -- in the argmax rule, to (max, lowest argmax
-//    id) -- and stores it (no block waits on another). A finishing launch
-//    with one block per sequence (programmatic dependent launch) merges each
-//    row's chunks in chunk order, then runs the sequence's acceptance chain
-//    on the gathered logits x[t_j] and records the decision.
-//  Phase 2 (rejection rule only): blocks stream the one or two rows the
+//    id) -- and stores it (no block waits on another). In the rejection
+//    rule the block holding a row's draft token also stores that logit.
+//  Decision: a launch that follows by programmatic dependent launch merges
+//    each row's chunks in chunk order and runs the sequence's acceptance
+//    chain. In the rejection rule with K <= 64 this is fused into phase 2a:
+//    every block of a sequence stages the sequence's chunk statistics in
+//    shared memory and reaches the same decision.
+//  Phase 2 (rejection rule only): 2a blocks stream the one or two rows the
 //    decision names (target and draft row j*, or target row K), summing the
-//    residual (and p, for the fallback) per chunk; the last block of the
-//    sequence finds the chunk where u_fin * total falls and scans it in id
+//    residual (and p, for the fallback) per chunk; 2b, one block per
+//    sequence, finds the chunk where u_fin * total falls and scans it in id
 //    order for the drawn token. Rows are therefore read at most twice, and
 //    only the rejecting position's rows are read again.
 // exp((x - m) / T) is computed as 2^((x - m) * log2(e) / T) with the SFU's
@@ -59,9 +62,13 @@ struct alignas(16) RowPart {
     float s_lo;
 };
 
-struct alignas(16) Decision {
+// A sequence's decision and what its draw needs: the position whose rows it
+// reads and their statistics (max and 1 / sum of exp).
+struct alignas(16) DrawPlan {
     uint32_t jstar;  // rejecting position (K = all accepted)
     uint32_t kind;   // kDraw*
+    float pm, pinv;  // target row j*: max, 1 / sum exp((x - max) / T)
+    float qm, qinv;  // draft row j* (residual draws only)
     uint32_t pad0, pad1;
 };
 
@@ -71,7 +78,7 @@ struct alignas(16) DrawPart {
 };
 
 struct SpecLayout {
-    size_t row_ctr, seq_ctr_a, seq_ctr_b, row_parts, row_stats, decisions, draw_parts, total;
+    size_t row_ctr, seq_ctr_a, seq_ctr_b, row_parts, row_stats, tok_logit, plans, draw_parts, total;
     uint32_t rows_a, cmax_a, cmax_b;
 };
 
@@ -86,7 +93,8 @@ SpecLayout spec_layout(uint32_t S, uint32_t V, uint32_t K) {
     l.seq_ctr_b = o; o += align_up(static_cast<size_t>(S) * 4u, 256);
     l.row_parts = o; o += align_up(static_cast<size_t>(l.rows_a) * l.cmax_a * sizeof(RowPart), 256);
     l.row_stats = o; o += align_up(static_cast<size_t>(l.rows_a) * sizeof(RowPart), 256);
-    l.decisions = o; o += align_up(static_cast<size_t>(S) * sizeof(Decision), 256);
+    l.tok_logit = o; o += align_up(static_cast<size_t>(l.rows_a) * 4u, 256);
+    l.plans = o;     o += align_up(static_cast<size_t>(S) * sizeof(DrawPlan), 256);
     l.draw_parts = o; o += align_up(static_cast<size_t>(S) * l.cmax_b * sizeof(DrawPart), 256);
     l.total = o;
     return l;
@@ -109,7 +117,8 @@ struct SpecArgs {
     uint32_t* seq_ctr;
     RowPart* row_parts;    // [rows_a][cmax_a]
     RowPart* row_stats;    // [rows_a]
-    Decision* decisions;   // [S]
+    float* tok_logit;      // [rows_a]: the row's logit at its draft token (phase 1, rejection rule)
+    DrawPlan* plans;       // [S]
     uint32_t cmax;
     bool decide;           // run the acceptance chain (false: row statistics only)
 };
@@ -137,18 +146,40 @@ struct ChainPre {
     float u[kPre];
     float xt[kPre];  // target_j[t_j]
     float xd[kPre];  // draft_j[t_j]
+    float uf;        // u_fin (rejection rule)
 };
 
-// The acceptance chain of one sequence, run by one warp once every row of
-// the sequence has its statistics: lane j tests position j (32 at a time)
-// and the first failing position ends the chain. Positions below kPre read
-// their token, uniform and logits from `pre`.
+// Load the chain inputs of sequence s for positions below kPre (block-wide).
+// The logits at the draft tokens come from phase 1's tok_logit.
 template <bool kRej>
-__device__ void decide_sequence(const SpecArgs& a, uint32_t s, const ChainPre& pre) {
+__device__ __forceinline__ void load_chain_pre(const SpecArgs& a, uint32_t s, ChainPre& pre) {
+    const uint32_t K = a.K;
+    const uint32_t nt = a.S * (K + 1u);
+    if (kRej && threadIdx.x == 0) pre.uf = a.u_fin[s];
+    for (uint32_t j = threadIdx.x; j < K && j < kPre; j += blockDim.x) {
+        pre.tok[j] = a.tokens[static_cast<size_t>(s) * K + j];
+        if (kRej) {
+            pre.u[j] = a.u_acc[static_cast<size_t>(s) * K + j];
+            pre.xt[j] = a.tok_logit[s * (K + 1u) + j];
+            pre.xd[j] = a.tok_logit[nt + s * K + j];
+        }
+    }
+}
+
+// The acceptance chain of one sequence, run by one warp once every row of
+// the sequence has its statistics (tstat: target rows 0..K, dstat: draft
+// rows 0..K-1): lane j tests position j (32 at a time) and the first failing
+// position ends the chain. Positions below kPre read their token, uniform
+// and logits from `pre`. Returns, in every lane, the number of accepted
+// positions n (K: all), or kNoIdx for an invalid sequence. With `write` the
+// emitted tokens and the accepted count are stored (the rejection rule's
+// em[n] is left to the draw).
+template <bool kRej>
+__device__ uint32_t decide_sequence(const SpecArgs& a, uint32_t s, const ChainPre& pre, const RowPart* tstat,
+                                    const RowPart* dstat, bool write) {
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t K = a.K, V = a.V;
-    const RowPart* tstat = a.row_stats + static_cast<size_t>(s) * (K + 1u);
-    const RowPart* dstat = a.row_stats + static_cast<size_t>(a.S) * (K + 1u) + static_cast<size_t>(s) * K;
+    const uint32_t nt = a.S * (K + 1u);
     const uint32_t* tok = a.tokens + static_cast<size_t>(s) * K;
     const float* u_acc = a.u_acc + static_cast<size_t>(s) * K;
     uint32_t* em = a.emitted + static_cast<size_t>(s) * (K + 1u);
@@ -165,16 +196,15 @@ __device__ void decide_sequence(const SpecArgs& a, uint32_t s, const ChainPre& p
         }
     }
     if (kRej && lane == 0) {
-        const float uf = a.u_fin[s];
+        const float uf = pre.uf;
         bad |= !(uf >= 0.0f && uf < 1.0f);
     }
     if (__any_sync(kFull, bad)) {
-        for (uint32_t j = lane; j <= K; j += 32u) em[j] = SEL_INVALID_ID;
-        if (lane == 0) {
-            a.accepted[s] = SEL_INVALID_ID;
-            a.decisions[s] = Decision{0u, kDrawNone, 0u, 0u};
+        if (write) {
+            for (uint32_t j = lane; j <= K; j += 32u) em[j] = SEL_INVALID_ID;
+            if (lane == 0) a.accepted[s] = SEL_INVALID_ID;
         }
-        return;
+        return kNoIdx;
     }
     uint32_t n = K;
     for (uint32_t j0 = 0; j0 < K; j0 += 32u) {
@@ -192,8 +222,8 @@ __device__ void decide_sequence(const SpecArgs& a, uint32_t s, const ChainPre& p
                     xd = pre.xd[j];
                     u = pre.u[j];
                 } else {
-                    xt = a.target[(static_cast<size_t>(s) * (K + 1u) + j) * V + t];
-                    xd = a.draft[(static_cast<size_t>(s) * K + j) * V + t];
+                    xt = a.tok_logit[s * (K + 1u) + j];
+                    xd = a.tok_logit[nt + s * K + j];
                     u = u_acc[j];
                 }
                 const float p = ex2_approx((xt - tstat[j].m) * a.log2e_over_T) / tstat[j].s_hi;
@@ -207,16 +237,32 @@ __device__ void decide_sequence(const SpecArgs& a, uint32_t s, const ChainPre& p
             break;
         }
     }
-    for (uint32_t j = lane; j <= K; j += 32u) {
-        uint32_t v = SEL_INVALID_ID;  // in the rejection rule em[n] is the phase-2 draw
-        if (j < n) v = token(j);
-        else if (!kRej && j == n) v = tstat[n].idx & ~kNonfiniteBit;
-        em[j] = v;
+    if (write) {
+        for (uint32_t j = lane; j <= K; j += 32u) {
+            uint32_t v = SEL_INVALID_ID;  // in the rejection rule em[n] is the phase-2 draw
+            if (j < n) v = token(j);
+            else if (!kRej && j == n) v = tstat[n].idx & ~kNonfiniteBit;
+            em[j] = v;
+        }
+        if (lane == 0) a.accepted[s] = n;
     }
-    if (lane == 0) {
-        a.accepted[s] = n;
-        a.decisions[s] = Decision{n, kRej ? (n < K ? kDrawResidual : kDrawBonus) : kDrawNone, 0u, 0u};
+    return n;
+}
+
+// The draw plan of a decision (n from decide_sequence).
+__device__ __forceinline__ DrawPlan make_plan(uint32_t n, uint32_t K, const RowPart* tstat, const RowPart* dstat) {
+    DrawPlan d{};
+    if (n == kNoIdx) {
+        d.kind = kDrawNone;
+        return d;
     }
+    d.jstar = n;
+    d.kind = n < K ? kDrawResidual : kDrawBonus;
+    d.pm = tstat[n].m;
+    d.pinv = 1.0f / tstat[n].s_hi;
+    d.qm = n < K ? dstat[n].m : 0.0f;
+    d.qinv = n < K ? 1.0f / dstat[n].s_hi : 1.0f;
+    return d;
 }
 
 // Phase 1: per-row (max, sum exp) or (max, argmax); per-sequence decision.
@@ -238,6 +284,15 @@ __global__ void __launch_bounds__(kNT) spec_phase1_kernel(SpecArgs a) {
     float4 q[kVPT];
     load_unit<kNT, kVPT, kVec>(row, t.lo, t.hi, -INFINITY, q);
     pdl_trigger();
+    // Rejection rule: the row's draft token (target rows 0..K-1 and every
+    // draft row have one); the thread whose quads hold it stores the logit
+    // there for the acceptance chain.
+    uint32_t tok_t = 0xFFFFFFFFu;
+    if (kRej && a.decide) {
+        const uint32_t nt = a.S * (a.K + 1u);
+        const uint32_t j = t.row < nt ? t.row - seq * (a.K + 1u) : (t.row - nt) - seq * a.K;
+        if (j < a.K) tok_t = a.tokens[static_cast<size_t>(seq) * a.K + j];
+    }
 
     // nonfinite latch over the real quads (sum of x * 0 stays 0 unless some
     // x is +-Inf or NaN; a partial quad's padding lanes are -inf too, so the
@@ -297,6 +352,18 @@ __global__ void __launch_bounds__(kNT) spec_phase1_kernel(SpecArgs a) {
                     acc[3] += ex2_approx((q[sl].w - m) * c);
                 }
                 thread_s = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+            }
+        }
+        if (tok_t >= t.lo && tok_t < t.hi) {
+            const uint32_t o = tok_t - t.lo;
+            const uint32_t qi = o >> 2;
+            if (qi % kNT == static_cast<uint32_t>(tid)) {
+                const uint32_t hold = qi / kNT;
+                float4 qq = q[0];
+#pragma unroll
+                for (int sl = 1; sl < kVPT; ++sl) qq = static_cast<uint32_t>(sl) == hold ? q[sl] : qq;
+                const uint32_t c4 = o & 3u;
+                a.tok_logit[t.row] = c4 == 0u ? qq.x : (c4 == 1u ? qq.y : (c4 == 2u ? qq.z : qq.w));
             }
         }
     } else {
@@ -361,15 +428,16 @@ __global__ void __launch_bounds__(kNT) spec_phase1_kernel(SpecArgs a) {
     if (tid == 0) a.row_parts[static_cast<size_t>(t.row) * a.cmax + t.chunk] = RowPart{bm, bi | nf, tot.hi, tot.lo};
 }
 
-// Merge row r's chunk statistics in chunk order (one warp) into row_stats.
+// Merge the C chunk statistics of one row in chunk order (one warp; every
+// lane gets the result): the max, the lowest id attaining it, the nonfinite
+// bit, and (rejection rule) the float-float sum of the chunk sums rescaled to
+// the row's max.
 template <bool kRej>
-__device__ void merge_row(const SpecArgs& a, uint32_t r) {
+__device__ RowPart merge_parts(const RowPart* parts, uint32_t C, float c) {
     const uint32_t lane = threadIdx.x & 31u;
-    const RowPart* parts = a.row_parts + static_cast<size_t>(r) * a.cmax;
-    const float c = a.log2e_over_T;
     float rm = -INFINITY;
     uint32_t ri = kNoIdx, rnf = 0u;
-    for (uint32_t cc = lane; cc < a.chunks; cc += 32u) {
+    for (uint32_t cc = lane; cc < C; cc += 32u) {
         const float cm = parts[cc].m;
         const uint32_t ci = parts[cc].idx;
         rnf |= ci & kNonfiniteBit;
@@ -385,10 +453,10 @@ __device__ void merge_row(const SpecArgs& a, uint32_t r) {
     FF rs{0.0f, 0.0f};
     if (kRej && !rnf) {
         // chunk sums in chunk order: 32 at a time, each group a fixed butterfly
-        for (uint32_t c0 = 0; c0 < a.chunks; c0 += 32u) {
+        for (uint32_t c0 = 0; c0 < C; c0 += 32u) {
             const uint32_t cc = c0 + lane;
             FF sc{0.0f, 0.0f};
-            if (cc < a.chunks) {
+            if (cc < C) {
                 const float cm = parts[cc].m;
                 // a chunk of padding only (max -inf) adds nothing
                 if (cm > -INFINITY) sc = ff_mul_f(FF{parts[cc].s_hi, parts[cc].s_lo}, ex2_approx((cm - rm) * c));
@@ -396,11 +464,75 @@ __device__ void merge_row(const SpecArgs& a, uint32_t r) {
             rs = ff_add(rs, ff_warp_sum(sc));
         }
     }
-    if (lane == 0) a.row_stats[r] = RowPart{rm, ri | rnf, rs.hi, rs.lo};
+    return RowPart{rm, ri | rnf, rs.hi, rs.lo};
 }
 
-// Finishing launch of phase 1: block s merges the rows of sequence s and,
-// when deciding, runs its acceptance chain.
+// FF sum over a half-warp (every lane of the half gets the same value: a
+// fixed butterfly order).
+__device__ __forceinline__ FF ff_half_sum(FF a) {
+#pragma unroll
+    for (int m = 1; m < 16; m <<= 1) {
+        const FF o = ff_shfl_xor(a, m);
+        a = ((threadIdx.x & m) == 0) ? ff_add(a, o) : ff_add(o, a);
+    }
+    return a;
+}
+
+// Merge the staged chunk statistics of gn rows (st: row i's C chunks at
+// st + i * C) into out[0..gn), block-wide: a half-warp per row, lane l
+// folding chunks l, l + 16, ... in order, then a butterfly over the half.
+// The result depends on the data only, not on timing.
+template <bool kRej>
+__device__ void merge_staged(const RowPart* st, uint32_t gn, uint32_t C, float c, RowPart* out) {
+    const uint32_t tid = threadIdx.x, h = tid >> 4, hl = tid & 15u;
+    constexpr uint32_t kHalves = kNT / 16;
+    for (uint32_t i0 = 0; i0 < gn; i0 += kHalves) {
+        const uint32_t i = i0 + h;
+        const bool live = i < gn;
+        const RowPart* parts = st + static_cast<size_t>(live ? i : 0u) * C;
+        float rm = -INFINITY;
+        uint32_t ri = kNoIdx, rnf = 0u;
+        if (live) {
+            for (uint32_t cc = hl; cc < C; cc += 16u) {
+                const float cm = parts[cc].m;
+                const uint32_t ci = parts[cc].idx;
+                rnf |= ci & kNonfiniteBit;
+                if (beats(cm, ci & ~kNonfiniteBit, rm, ri)) { rm = cm; ri = ci & ~kNonfiniteBit; }
+            }
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(kFull, rm, o);
+            const uint32_t oi = __shfl_xor_sync(kFull, ri, o);
+            rnf |= __shfl_xor_sync(kFull, rnf, o);
+            if (beats(ov, oi, rm, ri)) { rm = ov; ri = oi; }
+        }
+        FF rs{0.0f, 0.0f};
+        if (kRej) {
+            if (live && !rnf) {
+                for (uint32_t cc = hl; cc < C; cc += 16u) {
+                    const float cm = parts[cc].m;
+                    // a chunk of padding only (max -inf) adds nothing
+                    if (cm > -INFINITY)
+                        rs = ff_add(rs, ff_mul_f(FF{parts[cc].s_hi, parts[cc].s_lo}, ex2_approx((cm - rm) * c)));
+                }
+            }
+            rs = ff_half_sum(rs);
+        }
+        if (live && hl == 0) out[i] = RowPart{rm, ri | rnf, rs.hi, rs.lo};
+    }
+}
+
+// Row r of sequence s's rows in chain order: target rows 0..K, then draft
+// rows 0..K-1.
+__device__ __forceinline__ uint32_t seq_row(const SpecArgs& a, uint32_t s, uint32_t i) {
+    const uint32_t rows_t = a.K + 1u;
+    return i < rows_t ? s * rows_t + i : a.S * rows_t + s * a.K + (i - rows_t);
+}
+
+// Finishing launch of phase 1: block s merges the rows of sequence s into
+// row_stats and, when deciding, runs its acceptance chain and records the
+// draw plan.
 template <bool kRej>
 __global__ void __launch_bounds__(kNT) spec_rows_kernel(SpecArgs a) {
     __shared__ ChainPre pre;
@@ -408,28 +540,21 @@ __global__ void __launch_bounds__(kNT) spec_rows_kernel(SpecArgs a) {
     pdl_trigger();
     const uint32_t s = blockIdx.x, K = a.K;
     const uint32_t tid = threadIdx.x, warp = tid >> 5;
-    if (a.decide) {
-        // the chain's inputs, loaded while the rows are merged
-        const uint32_t* tok = a.tokens + static_cast<size_t>(s) * K;
-        for (uint32_t j = tid; j < K && j < kPre; j += kNT) {
-            const uint32_t t = tok[j];
-            pre.tok[j] = t;
-            if (kRej) {
-                pre.u[j] = a.u_acc[static_cast<size_t>(s) * K + j];
-                const bool ok = t < a.V;
-                pre.xt[j] = ok ? a.target[(static_cast<size_t>(s) * (K + 1u) + j) * a.V + t] : 0.0f;
-                pre.xd[j] = ok ? a.draft[(static_cast<size_t>(s) * K + j) * a.V + t] : 0.0f;
-            }
-        }
-    }
+    if (a.decide) load_chain_pre<kRej>(a, s, pre);  // loaded while the rows are merged
     const uint32_t rows_t = K + 1u, rows_d = kRej ? K : 0u;
     for (uint32_t i = warp; i < rows_t + rows_d; i += kWarps) {
-        const uint32_t r = i < rows_t ? s * rows_t + i : a.S * rows_t + s * K + (i - rows_t);
-        merge_row<kRej>(a, r);
+        const uint32_t r = seq_row(a, s, i);
+        const RowPart m = merge_parts<kRej>(a.row_parts + static_cast<size_t>(r) * a.cmax, a.chunks, a.log2e_over_T);
+        if ((tid & 31u) == 0) a.row_stats[r] = m;
     }
     if (!a.decide) return;
     __syncthreads();  // row statistics and prefetched inputs of this block
-    if (warp == 0) decide_sequence<kRej>(a, s, pre);
+    if (warp == 0) {
+        const RowPart* tstat = a.row_stats + static_cast<size_t>(s) * rows_t;
+        const RowPart* dstat = a.row_stats + static_cast<size_t>(a.S) * rows_t + static_cast<size_t>(s) * K;
+        const uint32_t n = decide_sequence<kRej>(a, s, pre, tstat, dstat, true);
+        if (kRej && tid == 0) a.plans[s] = make_plan(n, K, tstat, dstat);
+    }
 }
 
 struct DrawArgs {
@@ -440,21 +565,17 @@ struct DrawArgs {
     uint32_t S, K, V;
     float log2e_over_T;
     uint32_t chunks;
-    uint32_t chunk_elems;  // a multiple of 1024, at most kDrawChunkMax
-    const RowPart* row_stats;
-    const Decision* decisions;
+    uint32_t chunk_elems;  // kDrawChunkMax
+    const DrawPlan* plans;
     DrawPart* parts;  // [S][cmax]
     uint32_t cmax;
 };
 
 // Phase 2: the inverse-CDF draw from the residual (or from p), in two
-// launches. 2a: every block sums the weights of one chunk of the rows the
-// decision names. 2b: one block per sequence finds the chunk where
-// u_fin * total falls (a fixed-order scan of the chunk sums), then, within
-// that chunk, the 1,024-id stripe, the quad and the id. Sums across threads
-// are float-float. The search is a few block-wide steps rather than one
-// thread's serial walk: straight-line code run once by one thread is bound
-// by instruction fetch.
+// steps. 2a: every block sums the weights of one chunk of the rows the plan
+// names. 2b: one block per sequence finds the chunk where u_fin * total falls
+// (a fixed-order block scan of the chunk sums), then scans that chunk in id
+// order. Sums across threads are float-float.
 constexpr uint32_t kDrawPer = 16;                   // ids per thread and chunk
 constexpr uint32_t kDrawChunkMax = kNT * kDrawPer;  // 4,096
 // Weights of 4 elements of the draw distribution: p = exp((x - m_p) / T) / Z_p
@@ -474,40 +595,29 @@ __device__ __forceinline__ void quad_weights(const float4& xp, const float4& xq,
     }
 }
 
-template <bool kVec>
-__global__ void __launch_bounds__(kNT) spec_draw_sum_kernel(DrawArgs a) {
-    __shared__ FF s_r[kWarps];
-    __shared__ FF s_p[kWarps];
+// The target and draft rows a plan names (the draft row only for a residual).
+__device__ __forceinline__ const float* plan_prow(const DrawArgs& b, uint32_t s, const DrawPlan& d) {
+    return b.target + (static_cast<size_t>(s) * (b.K + 1u) + d.jstar) * b.V;
+}
+__device__ __forceinline__ const float* plan_qrow(const DrawArgs& b, uint32_t s, const DrawPlan& d) {
+    return b.draft + (static_cast<size_t>(s) * b.K + d.jstar) * b.V;
+}
 
-    pdl_wait();
-    pdl_trigger();
-    const uint32_t chunks = a.chunks;
-    const uint32_t s = blockIdx.x / chunks;
-    const uint32_t chunk = blockIdx.x - s * chunks;
-    const Decision d = a.decisions[s];
-    if (d.kind == kDrawNone) return;  // invalid sequence, or no draw
+// 2a for one chunk (block-wide): the residual and target masses of ids
+// [chunk * chunk_elems, ...) of the plan's rows, stored to parts[s][chunk].
+// Coalesced quads, all loads issued before the arithmetic.
+template <bool kVec>
+__device__ __forceinline__ void draw_chunk_sum(const DrawArgs& b, uint32_t s, uint32_t chunk, const DrawPlan& d,
+                                               FF* s_r, FF* s_p) {
     const bool residual = d.kind == kDrawResidual;
-    const uint32_t K = a.K, V = a.V;
-    const uint32_t prow_i = static_cast<uint32_t>(s) * (K + 1u) + d.jstar;
-    const float* prow = a.target + static_cast<size_t>(prow_i) * V;
-    const RowPart ps = a.row_stats[prow_i];
-    const float* qrow = nullptr;
-    RowPart qs{0.0f, 0u, 1.0f, 0.0f};
-    if (residual) {
-        const uint32_t qrow_i = a.S * (K + 1u) + s * K + d.jstar;
-        qrow = a.draft + static_cast<size_t>(s * K + d.jstar) * V;
-        qs = a.row_stats[qrow_i];
-    }
-    const float c = a.log2e_over_T;
-    const float pinv = 1.0f / ps.s_hi;
-    const float qinv = 1.0f / qs.s_hi;
+    const float* prow = plan_prow(b, s, d);
+    const float* qrow = residual ? plan_qrow(b, s, d) : nullptr;
+    const float c = b.log2e_over_T;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr float kNegInf = -INFINITY;
     const float4 none = make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
-
-    // chunk sums: coalesced quads, all loads issued before the arithmetic
-    const uint32_t lo = chunk * a.chunk_elems;
-    const uint32_t hi = min(V, lo + a.chunk_elems);
+    const uint32_t lo = chunk * b.chunk_elems;
+    const uint32_t hi = min(b.V, lo + b.chunk_elems);
     constexpr int kQ = static_cast<int>(kDrawPer / 4u);
     float rsum = 0.0f, psum = 0.0f;
     {
@@ -521,7 +631,7 @@ __global__ void __launch_bounds__(kNT) spec_draw_sum_kernel(DrawArgs a) {
 #pragma unroll
         for (int i = 0; i < kQ; ++i) {
             float pw[4], rw[4];
-            quad_weights(xp[i], xq[i], residual, ps.m, pinv, qs.m, qinv, c, pw, rw);
+            quad_weights(xp[i], xq[i], residual, d.pm, d.pinv, d.qm, d.qinv, c, pw, rw);
             rsum += (rw[0] + rw[1]) + (rw[2] + rw[3]);
             psum += (pw[0] + pw[1]) + (pw[2] + pw[3]);
         }
@@ -533,216 +643,276 @@ __global__ void __launch_bounds__(kNT) spec_draw_sum_kernel(DrawArgs a) {
     if (tid == 0) {
         FF br{0.0f, 0.0f}, bp{0.0f, 0.0f};
         for (int w = 0; w < kWarps; ++w) { br = ff_add(br, s_r[w]); bp = ff_add(bp, s_p[w]); }
-        a.parts[static_cast<size_t>(s) * a.cmax + chunk] = DrawPart{br, bp};
+        b.parts[static_cast<size_t>(s) * b.cmax + chunk] = DrawPart{br, bp};
     }
 }
 
-// Phase 2b: block s finds the chunk where u_fin * total falls (a fixed-order
-// scan of the chunk sums), then, within that chunk, the 1,024-id stripe, the
-// quad and the id.
 template <bool kVec>
-__global__ void __launch_bounds__(kNT) spec_draw_find_kernel(DrawArgs a) {
+__global__ void __launch_bounds__(kNT) spec_draw_sum_kernel(DrawArgs b) {
     __shared__ FF s_r[kWarps];
-    __shared__ uint32_t s_cross;
-    __shared__ int s_lastpos;
-    __shared__ bool s_use_p;
-    __shared__ uint32_t s_cstar;
-    __shared__ FF s_before, s_target, s_sbefore;
-    __shared__ float s_stripe[kWarps][kDrawPer / 4];
-    __shared__ int s_istar;
-
+    __shared__ FF s_p[kWarps];
     pdl_wait();
     pdl_trigger();
-    const uint32_t chunks = a.chunks;
-    const uint32_t s = blockIdx.x;
-    const Decision d = a.decisions[s];
-    if (d.kind == kDrawNone) return;  // invalid sequence, or no draw
-    const bool residual = d.kind == kDrawResidual;
-    const uint32_t K = a.K, V = a.V;
-    const uint32_t prow_i = static_cast<uint32_t>(s) * (K + 1u) + d.jstar;
-    const float* prow = a.target + static_cast<size_t>(prow_i) * V;
-    const RowPart ps = a.row_stats[prow_i];
-    const float* qrow = nullptr;
-    RowPart qs{0.0f, 0u, 1.0f, 0.0f};
-    if (residual) {
-        const uint32_t qrow_i = a.S * (K + 1u) + s * K + d.jstar;
-        qrow = a.draft + static_cast<size_t>(s * K + d.jstar) * V;
-        qs = a.row_stats[qrow_i];
-    }
-    const float c = a.log2e_over_T;
-    const float pinv = 1.0f / ps.s_hi;
-    const float qinv = 1.0f / qs.s_hi;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    constexpr float kNegInf = -INFINITY;
-    const float4 none = make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
-    constexpr int kQ = static_cast<int>(kDrawPer / 4u);
+    const uint32_t s = blockIdx.x / b.chunks;
+    const uint32_t chunk = blockIdx.x - s * b.chunks;
+    const DrawPlan d = b.plans[s];
+    if (d.kind == kDrawNone) return;  // invalid sequence
+    draw_chunk_sum<kVec>(b, s, chunk, d, s_r, s_p);
+}
 
-    // Warp 0 walks the chunk sums in chunk order, 32 at a time
-    // (fixed-order scans: the result does not depend on timing).
-    const DrawPart* parts = a.parts + static_cast<size_t>(s) * a.cmax;
-    if (warp == 0) {
-        FF R{0.0f, 0.0f}, P{0.0f, 0.0f}, r0{0.0f, 0.0f}, p0{0.0f, 0.0f};
-        for (uint32_t c0 = 0; c0 < chunks; c0 += 32) {
-            const uint32_t ci = c0 + lane;
-            FF r{0.0f, 0.0f}, p{0.0f, 0.0f};
-            if (ci < chunks) {
-                r = FF{ld_gpu_f32(&parts[ci].r.hi), ld_gpu_f32(&parts[ci].r.lo)};
-                p = FF{ld_gpu_f32(&parts[ci].p.hi), ld_gpu_f32(&parts[ci].p.lo)};
-            }
-            if (c0 == 0) { r0 = r; p0 = p; }  // the first group is walked from registers
-            R = ff_add(R, ff_warp_sum(r));
-            P = ff_add(P, ff_warp_sum(p));
-        }
-        const bool use_p = !(R.hi > 0.0f);  // residual empty by rounding: draw from p
-        const FF target = ff_mul_f(use_p ? P : R, a.u_fin[s]);
-        uint32_t cstar = chunks, last_pos_chunk = 0;
-        FF before{0.0f, 0.0f}, acc{0.0f, 0.0f}, before_last{0.0f, 0.0f};
-        for (uint32_t c0 = 0; c0 < chunks && cstar == chunks; c0 += 32) {
-            const uint32_t ci = c0 + lane;
-            FF t = use_p ? p0 : r0;
-            if (c0 > 0) {
-                t = FF{0.0f, 0.0f};
-                if (ci < chunks) {
-                    const FF* src = use_p ? &parts[ci].p : &parts[ci].r;
-                    t = FF{ld_gpu_f32(&src->hi), ld_gpu_f32(&src->lo)};
+// Rejection rule with K <= kPre and at most kStage chunk statistics per row:
+// the row merge, the acceptance chain and 2a in one launch. Block (s, chunk)
+// stages sequence s's chunk statistics in shared memory, merges its rows and
+// runs its chain (every block of the sequence reaches the same decision from
+// the same data; chunk 0's block stores it), then sums its chunk of the rows
+// the decision names. This saves a launch and two round trips through L2 on
+// the path from phase 1 to the draw.
+constexpr uint32_t kStage = 1024;               // chunk statistics staged at once (16 KB)
+constexpr uint32_t kChainRows = 2u * kPre + 1u;  // rows of a sequence with K <= kPre
+
+struct DecideShared {
+    RowPart st[kStage];
+    RowPart rs[kChainRows];
+    ChainPre pre;
+    FF s_r[kWarps], s_p[kWarps];
+    DrawPlan plan;
+};
+
+template <bool kVec>
+__global__ void __launch_bounds__(kNT) spec_decide_draw_kernel(SpecArgs a, DrawArgs b) {
+    __shared__ DecideShared sh;
+    const uint32_t s = blockIdx.x / b.chunks;
+    const uint32_t chunk = blockIdx.x - s * b.chunks;
+    const uint32_t K = a.K, C = a.chunks;
+    const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
+    const uint32_t rows_t = K + 1u, nrows = 2u * K + 1u;
+    const uint32_t per = kStage / C;  // rows staged at once (C <= kStage)
+    pdl_wait();
+    pdl_trigger();
+    load_chain_pre<true>(a, s, sh.pre);
+    for (uint32_t g0 = 0; g0 < nrows; g0 += per) {
+        const uint32_t gn = min(per, nrows - g0);
+        const uint32_t n = gn * C;
+        for (uint32_t e0 = 0; e0 < n; e0 += 4u * kNT) {
+            RowPart v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t e = e0 + tid + kNT * i;
+                if (e < n) {
+                    const uint32_t ri = e / C;
+                    v[i] = a.row_parts[static_cast<size_t>(seq_row(a, s, g0 + ri)) * a.cmax + (e - ri * C)];
                 }
             }
-            const FF incl = ff_add(acc, ff_warp_scan(t));
-            FF excl = ff_shfl_up(incl, 1);
-            if (lane == 0) excl = acc;
-            const uint32_t pos = __ballot_sync(kFull, ci < chunks && t.hi > 0.0f);
-            if (pos) {
-                const int l = 31 - __clz(pos);
-                last_pos_chunk = c0 + l;
-                before_last = ff_shfl(excl, l);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t e = e0 + tid + kNT * i;
+                if (e < n) sh.st[e] = v[i];
             }
-            const uint32_t hit = __ballot_sync(kFull, ci < chunks && t.hi > 0.0f && ff_lt(target, incl));
-            if (hit) {
-                const int l = __ffs(hit) - 1;
-                cstar = c0 + l;
-                before = ff_shfl(excl, l);
-            }
-            acc = ff_shfl(incl, 31);
         }
-        if (cstar == chunks) {  // rounding: take the last chunk with mass
-            cstar = last_pos_chunk;
-            before = before_last;
-        }
+        __syncthreads();
+        merge_staged<true>(sh.st, gn, C, a.log2e_over_T, sh.rs + g0);
+        __syncthreads();
+    }
+    if (warp == 0) {
+        const uint32_t n = decide_sequence<true>(a, s, sh.pre, sh.rs, sh.rs + rows_t, chunk == 0);
         if (lane == 0) {
-            s_use_p = use_p;
-            s_cstar = cstar;
-            s_before = before;
-            s_target = target;
-            s_lastpos = -1;
+            const DrawPlan d = make_plan(n, K, sh.rs, sh.rs + rows_t);
+            sh.plan = d;
+            if (chunk == 0) a.plans[s] = d;
         }
     }
     __syncthreads();
+    const DrawPlan d = sh.plan;
+    if (d.kind == kDrawNone) return;  // invalid sequence
+    draw_chunk_sum<kVec>(b, s, chunk, d, sh.s_r, sh.s_p);
+}
 
-    // The hit chunk, read again (from L2) in the coalesced layout: stripe i
-    // holds ids [clo + 1024 i, clo + 1024 (i + 1)), thread t its quad at
-    // 4 t. Id order is stripe, then thread, then lane: find the stripe from
-    // the stripe totals, the thread by a block scan of that stripe's quad
-    // sums, and the id within the quad.
-    const bool use_p = s_use_p;
-    const uint32_t clo = s_cstar * a.chunk_elems;
-    const uint32_t chi = min(V, clo + a.chunk_elems);
-    const FF target = s_target;
+// Block-wide scan in thread order of two FF values at once (the two chains
+// interleave): inclusive and exclusive prefixes of this thread, and the
+// block totals in every thread. s_a, s_b: kWarps entries of shared memory
+// each; the call starts and ends with the block in step.
+__device__ __forceinline__ void block_scan2(FF a, FF b, FF& ia, FF& ea, FF& ib, FF& eb, FF& ta, FF& tb, FF* s_a,
+                                            FF* s_b) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    FF wa = a, wb = b;
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const FF oa = ff_shfl_up(wa, m), ob = ff_shfl_up(wb, m);
+        if (lane >= m) {
+            wa = ff_add(oa, wa);
+            wb = ff_add(ob, wb);
+        }
+    }
+    FF xa = ff_shfl_up(wa, 1), xb = ff_shfl_up(wb, 1);
+    if (lane == 31) { s_a[warp] = wa; s_b[warp] = wb; }
+    __syncthreads();
+    FF pa{0.0f, 0.0f}, pb{0.0f, 0.0f};
+    ta = FF{0.0f, 0.0f};
+    tb = FF{0.0f, 0.0f};
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        if (w == warp) { pa = ta; pb = tb; }
+        ta = ff_add(ta, s_a[w]);
+        tb = ff_add(tb, s_b[w]);
+    }
+    ia = ff_add(pa, wa);
+    ib = ff_add(pb, wb);
+    ea = lane == 0 ? pa : ff_add(pa, xa);
+    eb = lane == 0 ? pb : ff_add(pb, xb);
+    __syncthreads();
+}
+
+// 2b: block s finds the chunk where u_fin * total falls, then the id within
+// it. The chunk sums are scanned in chunk order, kNT at a time (one per
+// thread); within the hit chunk, thread t holds the kDrawPer consecutive ids
+// from clo + kDrawPer * t, so a block scan of the thread sums in thread
+// order is a scan in id order, and the thread where the target falls finds
+// the id among its own.
+template <bool kVec>
+__global__ void __launch_bounds__(kNT) spec_draw_find_kernel(DrawArgs a) {
+    __shared__ FF s_a[kWarps], s_b[kWarps];
+    __shared__ uint32_t s_cstar, s_cross;
+    __shared__ int s_clast, s_lastid;
+    __shared__ FF s_before, s_before_last;
+
+    const uint32_t chunks = a.chunks;
+    const uint32_t s = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const DrawPart* parts = a.parts + static_cast<size_t>(s) * a.cmax;
+    const DrawPart zero{FF{0.0f, 0.0f}, FF{0.0f, 0.0f}};
+    pdl_wait();
+    pdl_trigger();
+    // the plan, the first kNT chunk sums and u_fin, loaded together
+    const DrawPlan d = a.plans[s];
+    const DrawPart first = static_cast<uint32_t>(tid) < chunks ? parts[tid] : zero;
+    const float uf = a.u_fin[s];
+    if (d.kind == kDrawNone) return;  // invalid sequence
+    const bool residual = d.kind == kDrawResidual;
+    if (tid == 0) {
+        s_cstar = kNoIdx;
+        s_cross = kNoIdx;
+        s_clast = -1;
+        s_lastid = -1;
+    }
+    FF ir, er, ip, ep, R, P;
+    const bool one_group = chunks <= static_cast<uint32_t>(kNT);
+    if (one_group) {
+        block_scan2(first.r, first.p, ir, er, ip, ep, R, P, s_a, s_b);
+    } else {
+        // the totals first, in a fixed order (warps, then groups)
+        R = FF{0.0f, 0.0f};
+        P = FF{0.0f, 0.0f};
+        for (uint32_t g0 = 0; g0 < chunks; g0 += kNT) {
+            const uint32_t ci = g0 + tid;
+            const DrawPart v = g0 == 0 ? first : (ci < chunks ? parts[ci] : zero);
+            FF tr, tp;
+            block_scan2(v.r, v.p, ir, er, ip, ep, tr, tp, s_a, s_b);
+            R = ff_add(R, tr);
+            P = ff_add(P, tp);
+        }
+    }
+    const bool use_p = !(R.hi > 0.0f);  // residual empty by rounding: draw from p
+    const FF target = ff_mul_f(use_p ? P : R, uf);
+
+    // the first chunk with mass whose inclusive prefix passes the target
+    // (else, by rounding, the last chunk with mass)
+    FF base{0.0f, 0.0f};
+    for (uint32_t g0 = 0; g0 < chunks; g0 += kNT) {
+        const uint32_t ci = g0 + tid;
+        FF w, incl, start;
+        if (one_group) {
+            w = use_p ? first.p : first.r;
+            incl = use_p ? ip : ir;
+            start = use_p ? ep : er;
+        } else {
+            const DrawPart v = g0 == 0 ? first : (ci < chunks ? parts[ci] : zero);
+            w = use_p ? v.p : v.r;
+            FF i2, e2, t2, tw;
+            block_scan2(w, FF{0.0f, 0.0f}, incl, start, i2, e2, tw, t2, s_a, s_b);
+            incl = ff_add(base, incl);
+            start = ff_add(base, start);
+            base = ff_add(base, tw);
+        }
+        const bool mass = ci < chunks && w.hi > 0.0f;
+        const uint32_t hit = __ballot_sync(kFull, mass && ff_lt(target, incl));
+        if (lane == 0 && hit) atomicMin(&s_cstar, g0 + static_cast<uint32_t>(warp * 32 + __ffs(hit) - 1));
+        const uint32_t has = __ballot_sync(kFull, mass);
+        if (lane == 0 && has) atomicMax(&s_clast, static_cast<int>(g0 + warp * 32 + 31 - __clz(has)));
+        __syncthreads();
+        if (ci == s_cstar) s_before = start;
+        if (static_cast<int>(ci) == s_clast) s_before_last = start;
+        __syncthreads();
+        if (s_cstar != kNoIdx) break;
+    }
+    uint32_t cstar = s_cstar;
+    FF before = s_before;
+    if (cstar == kNoIdx) {
+        cstar = s_clast >= 0 ? static_cast<uint32_t>(s_clast) : 0u;
+        before = s_clast >= 0 ? s_before_last : FF{0.0f, 0.0f};
+    }
+
+    // the hit chunk, read again: thread t's ids [e0, e0 + kDrawPer)
+    const float* prow = plan_prow(a, s, d);
+    const float* qrow = residual ? plan_qrow(a, s, d) : nullptr;
+    const float c = a.log2e_over_T;
+    const uint32_t clo = cstar * a.chunk_elems;
+    const uint32_t chi = min(a.V, clo + a.chunk_elems);
+    const uint32_t e0 = clo + kDrawPer * static_cast<uint32_t>(tid);
+    constexpr int kQ = static_cast<int>(kDrawPer / 4u);
+    constexpr float kNegInf = -INFINITY;
+    const float4 none = make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
     float4 xp[kQ], xq[kQ];
 #pragma unroll
     for (int i = 0; i < kQ; ++i) {
-        const uint32_t e = clo + 4u * (static_cast<uint32_t>(tid) + kNT * i);
-        xp[i] = ld_quad<kVec>(prow, e, chi, kNegInf);
-        xq[i] = residual ? ld_quad<kVec>(qrow, e, chi, kNegInf) : none;
+        xp[i] = ld_quad<kVec>(prow, e0 + 4u * i, chi, kNegInf);
+        xq[i] = residual ? ld_quad<kVec>(qrow, e0 + 4u * i, chi, kNegInf) : none;
     }
-    float qsum[kQ];
+    // weights and their running sums within the thread (a log-depth scan,
+    // so every partial sum carries at most 4 roundings)
+    float w[kDrawPer], cs[kDrawPer];
     int lp = -1;  // this thread's last id with mass
 #pragma unroll
     for (int i = 0; i < kQ; ++i) {
         float pw[4], rw[4];
-        quad_weights(xp[i], xq[i], residual, ps.m, pinv, qs.m, qinv, c, pw, rw);
-        const uint32_t e = clo + 4u * (static_cast<uint32_t>(tid) + kNT * i);
-        float w[4];
+        quad_weights(xp[i], xq[i], residual, d.pm, d.pinv, d.qm, d.qinv, c, pw, rw);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            w[j] = use_p ? pw[j] : rw[j];
-            if (w[j] > 0.0f) lp = static_cast<int>(e + j);
+            const float wj = use_p ? pw[j] : rw[j];
+            w[4 * i + j] = wj;
+            cs[4 * i + j] = wj;
+            if (wj > 0.0f) lp = static_cast<int>(e0 + 4u * i + j);
         }
-        qsum[i] = (w[0] + w[1]) + (w[2] + w[3]);
     }
-    {
-        const int wlp = __reduce_max_sync(kFull, lp);
-        if (lane == 0 && wlp >= 0) atomicMax(&s_lastpos, wlp);
-    }
-    // stripe totals: warp sums (fp32) combined across warps in float-float
 #pragma unroll
-    for (int i = 0; i < kQ; ++i) {
-        float v = qsum[i];
+    for (int o = 1; o < static_cast<int>(kDrawPer); o <<= 1) {
 #pragma unroll
-        for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(kFull, v, m);
-        if (lane == 0) s_stripe[warp][i] = v;
+        for (int j = static_cast<int>(kDrawPer) - 1; j >= o; --j) cs[j] += cs[j - o];
     }
+    const float tsum = cs[kDrawPer - 1];
+    const int wlp = __reduce_max_sync(kFull, lp);
+    if (lane == 0 && wlp >= 0) atomicMax(&s_lastid, wlp);
+    FF incl, start, i2, e2, t1, t2;
+    block_scan2(FF{tsum, 0.0f}, FF{0.0f, 0.0f}, incl, start, i2, e2, t1, t2, s_a, s_b);
+    incl = ff_add(before, incl);
+    start = ff_add(before, start);
+    const uint32_t hit = __ballot_sync(kFull, tsum > 0.0f && ff_lt(target, incl));
+    if (lane == 0 && hit) atomicMin(&s_cross, static_cast<uint32_t>(warp * 32 + __ffs(hit) - 1));
     __syncthreads();
-    if (warp == 0) {
-        FF t{0.0f, 0.0f};
-        if (lane < kQ)
-            for (int ww = 0; ww < kWarps; ++ww) t = ff_add(t, FF{s_stripe[ww][lane], 0.0f});
-        const FF incl = ff_add(s_before, ff_warp_scan(t));
-        FF excl = ff_shfl_up(incl, 1);
-        if (lane == 0) excl = s_before;
-        const uint32_t valid = (1u << kQ) - 1u;
-        const uint32_t pos = __ballot_sync(kFull, lane < kQ && t.hi > 0.0f) & valid;
-        const uint32_t hit = __ballot_sync(kFull, lane < kQ && t.hi > 0.0f && ff_lt(target, incl)) & valid;
-        // no crossing (rounding): the last stripe with mass
-        const int l = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
-        if (lane == 0) {
-            s_istar = l;
-            s_cross = kNoIdx;
-        }
-        if (l >= 0) {
-            const FF b = ff_shfl(excl, l);
-            if (lane == 0) s_sbefore = b;
-        }
-    }
-    __syncthreads();
-    const int istar = s_istar;
-    if (istar >= 0) {
-        // block scan of stripe istar's quad sums in thread order
-        float mine = 0.0f;
-        float4 cp = xp[0], cq = xq[0];
+    uint32_t* out = a.emitted + static_cast<size_t>(s) * (a.K + 1u) + d.jstar;
+    if (static_cast<uint32_t>(tid) == s_cross) {
+        // the target's offset into this thread's mass
+        const float off = ff_add(target, FF{-start.hi, -start.lo}).hi;
+        uint32_t pick = kNoIdx, last = kNoIdx;
 #pragma unroll
-        for (int i = 0; i < kQ; ++i)
-            if (i == istar) { mine = qsum[i]; cp = xp[i]; cq = xq[i]; }
-        const FF incl = ff_warp_scan(FF{mine, 0.0f});
-        if (lane == 31) s_r[warp] = incl;
-        __syncthreads();
-        FF start = s_sbefore;
-        for (int ww = 0; ww < warp; ++ww) start = ff_add(start, s_r[ww]);
-        FF excl = ff_shfl_up(incl, 1);
-        if (lane == 0) excl = FF{0.0f, 0.0f};
-        start = ff_add(start, excl);
-        const FF end = ff_add(start, FF{mine, 0.0f});
-        const uint32_t hit = __ballot_sync(kFull, mine > 0.0f && ff_lt(target, end));
-        if (lane == 0 && hit) atomicMin(&s_cross, static_cast<uint32_t>(tid) + static_cast<uint32_t>(__ffs(hit) - 1));
-        __syncthreads();
-        if (static_cast<uint32_t>(tid) == s_cross) {
-            float pw[4], rw[4];
-            quad_weights(cp, cq, residual, ps.m, pinv, qs.m, qinv, c, pw, rw);
-            const uint32_t e = clo + 4u * (static_cast<uint32_t>(tid) + kNT * istar);
-            uint32_t pick = kNoIdx, last = kNoIdx;
-            FF cdf = start;
-            for (int j = 0; j < 4; ++j) {
-                const float w = use_p ? pw[j] : rw[j];
-                cdf = ff_add(cdf, FF{w, 0.0f});
-                if (w > 0.0f) last = e + j;
-                if (pick == kNoIdx && w > 0.0f && ff_lt(target, cdf)) pick = e + j;
-            }
-            a.emitted[static_cast<size_t>(s) * (K + 1u) + d.jstar] = pick != kNoIdx ? pick : last;
+        for (int j = 0; j < static_cast<int>(kDrawPer); ++j) {
+            if (w[j] > 0.0f) last = e0 + j;
+            if (pick == kNoIdx && w[j] > 0.0f && off < cs[j]) pick = e0 + j;
         }
+        *out = pick != kNoIdx ? pick : last;
     }
-    if (tid == 0 && (istar < 0 || s_cross == kNoIdx)) {
-        // no crossing found (rounding): the last id with mass in the chunk
-        a.emitted[static_cast<size_t>(s) * (K + 1u) + d.jstar] =
-            s_lastpos >= 0 ? static_cast<uint32_t>(s_lastpos) : clo;
+    if (tid == 0 && s_cross == kNoIdx) {
+        // no crossing (rounding): the last id with mass in the chunk
+        *out = s_lastid >= 0 ? static_cast<uint32_t>(s_lastid) : clo;
     }
 }
 
@@ -930,7 +1100,8 @@ extern "C" sel_status spec_accept(const float* d_target, const float* d_draft, c
     a.seq_ctr = reinterpret_cast<uint32_t*>(ws + l.seq_ctr_a);
     a.row_parts = reinterpret_cast<RowPart*>(ws + l.row_parts);
     a.row_stats = reinterpret_cast<RowPart*>(ws + l.row_stats);
-    a.decisions = reinterpret_cast<Decision*>(ws + l.decisions);
+    a.tok_logit = reinterpret_cast<float*>(ws + l.tok_logit);
+    a.plans = reinterpret_cast<DrawPlan*>(ws + l.plans);
     a.cmax = l.cmax_a;
     a.decide = true;
     const dim3 grid1(rows1 * chunks1);
@@ -940,10 +1111,10 @@ extern "C" sel_status spec_accept(const float* d_target, const float* d_draft, c
     else e1 = vec ? launch_pdl(spec_phase1_kernel<true, false>, grid1, dim3(kNT), 0, stream, a)
                   : launch_pdl(spec_phase1_kernel<false, false>, grid1, dim3(kNT), 0, stream, a);
     if (e1 != cudaSuccess) return SEL_ECUDA;
-    e1 = rej ? launch_pdl(spec_rows_kernel<true>, dim3(S), dim3(kNT), 0, stream, a)
-             : launch_pdl(spec_rows_kernel<false>, dim3(S), dim3(kNT), 0, stream, a);
-    if (e1 != cudaSuccess) return SEL_ECUDA;
-    if (!rej) return SEL_OK;
+    if (!rej) {
+        e1 = launch_pdl(spec_rows_kernel<false>, dim3(S), dim3(kNT), 0, stream, a);
+        return e1 == cudaSuccess ? SEL_OK : SEL_ECUDA;
+    }
 
     // phase 2: chunks of kDrawChunkMax ids
     const uint32_t ce2 = kDrawChunkMax;
@@ -958,13 +1129,21 @@ extern "C" sel_status spec_accept(const float* d_target, const float* d_draft, c
     b.log2e_over_T = a.log2e_over_T;
     b.chunks = chunks2;
     b.chunk_elems = ce2;
-    b.row_stats = a.row_stats;
-    b.decisions = a.decisions;
+    b.plans = a.plans;
     b.parts = reinterpret_cast<DrawPart*>(ws + l.draw_parts);
     b.cmax = l.cmax_b;
     const dim3 grid2(S * chunks2);
-    cudaError_t e2 = vec ? launch_pdl(spec_draw_sum_kernel<true>, grid2, dim3(kNT), 0, stream, b)
-                         : launch_pdl(spec_draw_sum_kernel<false>, grid2, dim3(kNT), 0, stream, b);
+    cudaError_t e2;
+    if (K <= kPre && chunks1 <= kStage) {
+        // merge, chain and chunk sums in one launch
+        e2 = vec ? launch_pdl(spec_decide_draw_kernel<true>, grid2, dim3(kNT), 0, stream, a, b)
+                 : launch_pdl(spec_decide_draw_kernel<false>, grid2, dim3(kNT), 0, stream, a, b);
+    } else {
+        e2 = launch_pdl(spec_rows_kernel<true>, dim3(S), dim3(kNT), 0, stream, a);
+        if (e2 != cudaSuccess) return SEL_ECUDA;
+        e2 = vec ? launch_pdl(spec_draw_sum_kernel<true>, grid2, dim3(kNT), 0, stream, b)
+                 : launch_pdl(spec_draw_sum_kernel<false>, grid2, dim3(kNT), 0, stream, b);
+    }
     if (e2 != cudaSuccess) return SEL_ECUDA;
     e2 = vec ? launch_pdl(spec_draw_find_kernel<true>, dim3(S), dim3(kNT), 0, stream, b)
              : launch_pdl(spec_draw_find_kernel<false>, dim3(S), dim3(kNT), 0, stream, b);
@@ -1012,7 +1191,8 @@ extern "C" sel_status spec_diagnostics(const float* d_target, const float* d_dra
     a.seq_ctr = reinterpret_cast<uint32_t*>(ws + l.seq_ctr_a);
     a.row_parts = reinterpret_cast<RowPart*>(ws + l.row_parts);
     a.row_stats = reinterpret_cast<RowPart*>(ws + l.row_stats);
-    a.decisions = reinterpret_cast<Decision*>(ws + l.decisions);
+    a.tok_logit = reinterpret_cast<float*>(ws + l.tok_logit);
+    a.plans = reinterpret_cast<DrawPlan*>(ws + l.plans);
     a.cmax = l.cmax_a;
     a.decide = false;
     const cudaError_t e1 = vec ? launch_pdl(spec_phase1_kernel<true, true>, dim3(rows1 * chunks1), dim3(kNT), 0, stream, a)

@@ -55,6 +55,23 @@ def test_bench_workload(orc):
     run_both(orc, si, ARG)
 
 
+@pytest.mark.parametrize("S,K,V,equal_upto", [(2, 70, 3000, 66), (3, 66, 1000, 66), (1, 1, 8_400_001, 0)])
+def test_separate_decision_launch(orc, S, K, V, equal_upto):
+    """Shapes past the fused decision launch's limits (more than 64 drafts,
+    or more than 1,024 phase-1 chunks per row) take the separate merge
+    launch. Drafts equal to the target up to position 66 are accepted
+    whatever u is, so those chains pass position 64 and read their logits
+    past the prefetched ones; the residual or bonus draw then reads rows
+    past position 64."""
+    si = synth.spec_inputs(S=S, K=K, V=V, seed_target=K + 1, seed_draft=V, seed_u=S + 11, sigma_noise=0.7)
+    if equal_upto:
+        si.draft[:, :equal_upto] = si.target[:, :equal_upto]
+    acc, _, _ = run_both(orc, si, REJ)
+    if equal_upto:
+        assert np.all(acc >= equal_upto)
+    run_both(orc, si, ARG)
+
+
 def test_temperature_zero_is_the_argmax_rule(orc):
     si = synth.spec_inputs(S=6, K=4, V=9000, temperature=1.0, sigma_noise=0.1)
     a0, e0 = G.spec(si.target, si.draft, si.draft_tokens, si.u_acc, si.u_fin, 0.0, REJ)
