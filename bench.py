@@ -45,6 +45,7 @@ METRIC = "logits rows/s and achieved HBM GB/s (% of GB300 peak) at V=248k, rows=
 N_COPIES = 11         # rotating copies of the batch: 11 x 48.7 MB = 535 MB >= 4 x L2
 OP_REPS = 110         # launches per op in the per-op timed regions (a multiple of N_COPIES)
 N_GRAPHS = 5 * N_COPIES  # captured step graphs; step s replays graph s % N_GRAPHS
+STEPS_PER_GRAPH = 5      # steps captured together for the timed loop
 
 
 def measured_peak():
@@ -221,6 +222,29 @@ def gpu_arm(args, rank, world, local_rank):
             for op in range(5):
                 run_op(gi, op)
         graphs.append(g)
+    # The timed loop replays runs of STEPS_PER_GRAPH consecutive steps from
+    # one graph (steps s0 .. s0 + 4 for s0 a multiple of 5), so a graph
+    # launch's own latency is paid once per run; steps outside a whole run
+    # replay their single-step graph.
+    multi = []
+    for gi in range(n_graphs // STEPS_PER_GRAPH):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for s in range(gi * STEPS_PER_GRAPH, (gi + 1) * STEPS_PER_GRAPH):
+                for op in range(5):
+                    run_op(s, op)
+        multi.append(g)
+
+    def replay_steps(first, count):
+        s, end = first, first + count
+        while s < end:
+            if s % STEPS_PER_GRAPH == 0 and s + STEPS_PER_GRAPH <= end:
+                multi[(s % n_graphs) // STEPS_PER_GRAPH].replay()
+                s += STEPS_PER_GRAPH
+            else:
+                graphs[s % n_graphs].replay()
+                s += 1
+
     # per-op timing: one graph of OP_REPS launches of each op (same input
     # rotation), bracketed by events on the launching stream
     op_graphs = []
@@ -233,6 +257,8 @@ def gpu_arm(args, rank, world, local_rank):
     with torch.cuda.stream(stream):
         for s in range(args.warmup):
             graphs[s % n_graphs].replay()
+        for g in multi:
+            g.replay()
         for g in op_graphs:
             g.replay()
     torch.cuda.synchronize()
@@ -248,8 +274,7 @@ def gpu_arm(args, rank, world, local_rank):
     t_end = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         t_start.record(stream)
-        for s in range(args.warmup, args.warmup + args.steps):
-            graphs[s % n_graphs].replay()
+        replay_steps(args.warmup, args.steps)
         t_end.record(stream)
     torch.cuda.synchronize()
     # per-op timed regions, right after the steps (same clocks)
@@ -323,8 +348,8 @@ def gpu_arm(args, rank, world, local_rank):
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
                      "traffic": traffic},
         "gpu_launches": launches_per_step * args.steps,
-        "timing": f"steps replayed from CUDA graphs; per-op times from {OP_REPS} graph-replayed "
-                  "launches of each op between events on the launching stream",
+        "timing": f"steps replayed from CUDA graphs of {STEPS_PER_GRAPH} consecutive steps; per-op times "
+                  f"from {OP_REPS} graph-replayed launches of each op between events on the launching stream",
         "clocks": clk,
         "e2e": e2e,
         "extra_ops": extra,

@@ -493,29 +493,27 @@ __device__ void sample_epilogue(const uint64_t* sorted, float* scratch, uint32_t
         typical_window(wf, g, byr, nc, gbar, sa.typical_p * S, lo, hi);
         scan(lo, hi, false);
     }
-    // top-p: the shortest prefix of the window whose cumulative P reaches top_p
-    uint32_t ns = hi;
-    if (sa.top_p < 1.0f) {
-        const float need = sa.top_p * pf[hi - 1];
-        ns = 0;
-        for (uint32_t b = lo; b < hi && ns == 0; b += 32) {
+    // top-p: the shortest prefix of the window whose cumulative P reaches
+    // top_p; min-p: keep P_j >= min_p * P_max, i.e. wf_j >= min_p * wf_lo.
+    // wf falls along the window, so the min-p survivors are a prefix too, and
+    // min-p applied after top-p keeps the shorter of the two prefixes: both
+    // are found in one pass.
+    const bool use_p = sa.top_p < 1.0f, use_m = sa.min_p > 0.0f;
+    const float need = use_p ? sa.top_p * pf[hi - 1] : 0.0f;
+    const float floor_w = sa.min_p * wf[lo];
+    uint32_t ns_p = 0, keep = lo + 1;
+    if (use_p || use_m) {
+        for (uint32_t b = lo; b < hi; b += 32) {
             const uint32_t j = b + lane;
-            const uint32_t hit = __ballot_sync(kFull, j < hi && pf[j] >= need);
-            if (hit) ns = b + __ffs(hit);
+            const bool in = j < hi;
+            const uint32_t hit = __ballot_sync(kFull, use_p && in && pf[j] >= need);
+            if (ns_p == 0 && hit) ns_p = b + __ffs(hit);
+            const uint32_t m = __ballot_sync(kFull, use_m && in && j > lo && wf[j] >= floor_w);
+            if (m) keep = b + 32 - __clz(m);
         }
-        if (ns == 0) ns = hi;  // rounding kept the total below top_p
     }
-    // min-p: keep P_j >= min_p * P_max, i.e. wf_j >= min_p * wf_lo
-    if (sa.min_p > 0.0f) {
-        const float floor_w = sa.min_p * wf[lo];
-        uint32_t keep = lo + 1;
-        for (uint32_t b = lo; b < ns; b += 32) {
-            const uint32_t j = b + lane;
-            const uint32_t m = __ballot_sync(kFull, j < ns && j > lo && wf[j] >= floor_w);
-            if (m) keep = b + 32 - __clz(m);  // survivors form a prefix
-        }
-        ns = keep;
-    }
+    uint32_t ns = (use_p && ns_p != 0) ? ns_p : hi;  // no crossing: rounding kept the total below top_p
+    if (use_m) ns = min(ns, keep);
     // the draw over the survivors, renormalised by their total
     const float total = pd[ns - 1];
     const float target = u * total;
@@ -707,13 +705,13 @@ __device__ void merge_row_lists(TopkShared& s, Load&& load, uint32_t chunks, uin
     }
 }
 
+// u: the row's uniform (sampling), loaded by the caller ahead of time.
 template <bool kSample>
 __device__ __forceinline__ void write_row(const uint64_t* sorted, float* scratch, const TopkArgs& a, uint32_t row,
-                                          uint32_t have, bool nonfinite, double nsig_thr = -INFINITY) {
+                                          uint32_t have, bool nonfinite, float u, double nsig_thr = -INFINITY) {
     const int tid = threadIdx.x;
     if constexpr (kSample) {
-        if (tid < 32)
-            sample_epilogue(sorted, scratch, have, row, a.sa.uniforms[row], nonfinite, a.sa, nsig_thr, a.out_ids);
+        if (tid < 32) sample_epilogue(sorted, scratch, have, row, u, nonfinite, a.sa, nsig_thr, a.out_ids);
     } else {
         const uint32_t k = a.k;
         for (uint32_t j = tid; j < k; j += kNT) {
@@ -1049,11 +1047,11 @@ __device__ __forceinline__ void sort_desc8(uint32_t (&e)[8]) {
 // would need candidates past the kFullCand most probable ones is not
 // decided: the row fails closed and kErrBeyond is raised. One warp.
 __device__ void full_row_plan(const uint64_t* sorted, float* scratch, uint32_t n, uint32_t row, bool nonfinite,
-                              const TopkArgs& a, double Z, double gbar_all, double sigma) {
+                              const TopkArgs& a, double Z, double gbar_all, double sigma, float u) {
     const int lane = threadIdx.x & 31;
     const SampleArgs& sa = a.sa;
     FullRow out{};
-    out.u = sa.uniforms[row];
+    out.u = u;
     out.M = n > 0 ? key2f(cand_key(sorted[0])) : 0.0f;
     bool resolved = !nonfinite && out.u >= 0.0f && out.u < 1.0f && n > 0 && Z > 0.0;
     bool beyond_err = false;
@@ -1485,6 +1483,7 @@ __global__ void __launch_bounds__(kNT) topk_finish_kernel(TopkArgs a) {
     uint32_t nf = 0;
     for (uint32_t c = lane; c < chunks; c += 32) nf |= a.chunk_flags[static_cast<size_t>(row) * a.stride + c];
     const uint32_t tau_row = a.row_tau[row];
+    const float u_row = kSample ? a.sa.uniforms[row] : 0.0f;  // needed only at the end: loaded now
     // top-n-sigma: the row's moments, summed in double (lane-strided, then
     // across the warp)
     double mo1 = 0.0, mo2 = 0.0;
@@ -1610,9 +1609,11 @@ __global__ void __launch_bounds__(kNT) topk_finish_kernel(TopkArgs a) {
             sigma = sqrt(fmax(mo2 / Vd - mean_d * mean_d, 0.0));
         }
         if (tid < 32)
-            full_row_plan(s.sorted, reinterpret_cast<float*>(s.buf), n < k ? n : k, row, nf != 0, a, z, gbar, sigma);
+            full_row_plan(s.sorted, reinterpret_cast<float*>(s.buf), n < k ? n : k, row, nf != 0, a, z, gbar, sigma,
+                          u_row);
     } else {
-        write_row<kSample>(s.sorted, reinterpret_cast<float*>(s.buf), a, row, n < k ? n : k, nf != 0, nsig_thr);
+        write_row<kSample>(s.sorted, reinterpret_cast<float*>(s.buf), a, row, n < k ? n : k, nf != 0, u_row,
+                           nsig_thr);
     }
     if (tid == 0) atomicAdd(a.err + 1, 1u);  // rows finished (self-check)
 }
@@ -1816,6 +1817,7 @@ __global__ void __launch_bounds__(kNT) merge_shards_kernel(ShardArgs sh, TopkArg
     const uint32_t row = blockIdx.x;
     const uint32_t k = a.k;
     const size_t base = static_cast<size_t>(row) * sh.G * k;
+    const float u_row = kSample ? a.sa.uniforms[row] : 0.0f;
     if (threadIdx.x == 0) s_bad = 0u;
     __syncthreads();
     auto load = [&](uint32_t i) -> uint64_t {
@@ -1830,7 +1832,7 @@ __global__ void __launch_bounds__(kNT) merge_shards_kernel(ShardArgs sh, TopkArg
     };
     merge_row_lists(s, load, sh.G, k, &s_bad);
     __syncthreads();
-    write_row<kSample>(s.sorted, reinterpret_cast<float*>(s.buf), a, row, k, s_bad != 0u);
+    write_row<kSample>(s.sorted, reinterpret_cast<float*>(s.buf), a, row, k, s_bad != 0u, u_row);
 }
 
 sel_status check_shards(const float* d_vals, const uint32_t* d_ids, uint32_t rows, uint32_t G, uint32_t k,
