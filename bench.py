@@ -182,9 +182,9 @@ def gpu_arm(args, rank, world, local_rank):
             B.spec_accept(target_view(copy_for(step, 4)), None, tok, arg, None, None, acc2, emi2, ws_g)
 
     # argmax, top-k, sample and the argmax rule: a main launch and a finishing
-    # launch each; the rejection rule: phase 1, its finishing launch, and the
-    # draw's sum and find launches
-    launches_per_step = 12
+    # launch each; the rejection rule: phase 1, the decision with the draw's
+    # chunk sums, and the draw's find launch
+    launches_per_step = len(STEP_LAUNCHES)
     bytes_per_op = [ROWS * ROW_BYTES, ROWS * ROW_BYTES, ROWS * ROW_BYTES,
                     None, ROWS * ROW_BYTES]
 
@@ -211,7 +211,7 @@ def gpu_arm(args, rank, world, local_rank):
         torch.cuda.synchronize()
         return None
 
-    # Each step is replayed from a CUDA graph of its five calls (six kernels),
+    # Each step is replayed from a CUDA graph of its five calls (11 launches),
     # so the host's launch cost does not gap the GPU. Step s (warm-up steps
     # first) replays graph s % N_GRAPHS, which keeps the copy rotation.
     n_graphs = N_GRAPHS
@@ -452,8 +452,8 @@ STEP_LAUNCHES = [
     ("argmax", "argmax_kernel"), ("argmax", "argmax_finish_kernel"),
     ("topk", "topk_kernel"), ("topk", "topk_finish_kernel<0"),
     ("sample", "topk_kernel"), ("sample", "topk_finish_kernel<1"),
-    ("spec_rejection", "spec_phase1_kernel"), ("spec_rejection", "spec_rows_kernel<1"),
-    ("spec_rejection", "spec_draw_sum_kernel"), ("spec_rejection", "spec_draw_find_kernel"),
+    ("spec_rejection", "spec_phase1_kernel"), ("spec_rejection", "spec_decide_draw_kernel"),
+    ("spec_rejection", "spec_draw_find_kernel"),
     ("spec_argmax", "spec_phase1_kernel"), ("spec_argmax", "spec_rows_kernel<0"),
 ]
 TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
