@@ -438,6 +438,64 @@ __device__ void sample_epilogue(const uint64_t* sorted, float* scratch, uint32_t
     const float T = sa.temperature;
     const bool temp_last = sa.order == SEL_ORDER_TEMP_LAST;
     const float Tf = temp_last ? 1.0f : T;
+    const bool use_typ = sa.typical_p > 0.0f && sa.typical_p < 1.0f;
+    if (nc <= 64u && !use_typ) {
+        // At most 64 candidates and no typical cut: the same steps with the
+        // weights and prefix sums in registers (lane l holds candidates l and
+        // l + 32; the same scans, so the same sums as the path below).
+        const uint32_t j0 = lane, j1 = lane + 32u;
+        float f0 = 0.0f, w0 = 0.0f, f1 = 0.0f, w1 = 0.0f;
+        if (j0 < nc) {
+            const float d = key2f(cand_key(sorted[j0])) - x0;
+            w0 = expf(d / T);
+            f0 = temp_last ? expf(d) : w0;
+        }
+        if (j1 < nc) {
+            const float d = key2f(cand_key(sorted[j1])) - x0;
+            w1 = expf(d / T);
+            f1 = temp_last ? expf(d) : w1;
+        }
+        float pf0 = f0, pd0 = w0, pf1 = f1, pd1 = w1;
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+            const float a0 = __shfl_up_sync(kFull, pf0, m), b0 = __shfl_up_sync(kFull, pd0, m);
+            const float a1 = __shfl_up_sync(kFull, pf1, m), b1 = __shfl_up_sync(kFull, pd1, m);
+            if (lane >= m) {
+                pf0 += a0;
+                pd0 += b0;
+                pf1 += a1;
+                pd1 += b1;
+            }
+        }
+        pf1 += __shfl_sync(kFull, pf0, 31);
+        pd1 += __shfl_sync(kFull, pd0, 31);
+        // top-p and min-p prefixes (as below), then the draw
+        const bool use_p = sa.top_p < 1.0f, use_m = sa.min_p > 0.0f;
+        const uint32_t last = nc - 1u;
+        const float S = __shfl_sync(kFull, last < 32u ? pf0 : pf1, static_cast<int>(last & 31u));
+        const float need = sa.top_p * S;
+        const uint32_t hp0 = __ballot_sync(kFull, use_p && j0 < nc && pf0 >= need);
+        const uint32_t hp1 = __ballot_sync(kFull, use_p && j1 < nc && pf1 >= need);
+        const uint32_t ns_p = hp0 ? static_cast<uint32_t>(__ffs(hp0)) : (hp1 ? 32u + __ffs(hp1) : 0u);
+        const float floor_w = sa.min_p * __shfl_sync(kFull, f0, 0);
+        const uint32_t m0 = __ballot_sync(kFull, use_m && j0 < nc && j0 > 0u && f0 >= floor_w);
+        const uint32_t m1 = __ballot_sync(kFull, use_m && j1 < nc && f1 >= floor_w);
+        const uint32_t keep = m1 ? 64u - __clz(m1) : (m0 ? 32u - __clz(m0) : 1u);
+        uint32_t ns = (use_p && ns_p != 0u) ? ns_p : nc;  // no crossing: rounding kept the total below top_p
+        if (use_m) ns = min(ns, keep);
+        const uint32_t e = ns - 1u;
+        const float total = __shfl_sync(kFull, e < 32u ? pd0 : pd1, static_cast<int>(e & 31u));
+        const float target = u * total;
+        const uint32_t h0 = __ballot_sync(kFull, j0 < ns && target < pd0);
+        const uint32_t h1 = __ballot_sync(kFull, j1 < ns && target < pd1);
+        const uint32_t pick = h0 ? static_cast<uint32_t>(__ffs(h0) - 1) : (h1 ? 31u + __ffs(h1) : e);
+        const float wp = __shfl_sync(kFull, pick < 32u ? w0 : w1, static_cast<int>(pick & 31u));
+        if (live && lane == 0) {
+            out_ids[row] = cand_id(sorted[pick]);
+            sa.out_probs[row] = wp / total;
+        }
+        return;
+    }
     float* wf = scratch;                 // [SEL_MAX_K]
     float* wd = wf + SEL_MAX_K;          // [SEL_MAX_K]
     float* pf = wd + SEL_MAX_K;          // [SEL_MAX_K]
@@ -476,7 +534,7 @@ __device__ void sample_epilogue(const uint64_t* sorted, float* scratch, uint32_t
     };
     scan(0, nc, true);
     uint32_t lo = 0, hi = nc;
-    if (sa.typical_p > 0.0f && sa.typical_p < 1.0f) {
+    if (use_typ) {
         const float S = pf[nc - 1];
         float* g = pd;    // scratch until the window's prefix sums are taken
         float* byr = pf;  // the same
