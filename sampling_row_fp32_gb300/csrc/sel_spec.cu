@@ -18,12 +18,14 @@
 // verified position" is the mlxcel cost note). Here:
 //  Phase 1 (one launch over every target and draft row of every sequence):
 //    one block per row chunk (sel_units.cuh) reduces its chunk to (max, sum
-//    of exp((x - max) / T)) -- in the argmax rule, to (max, lowest argmax
-//    id) -- and stores it (no block waits on another). In the rejection
-//    rule the block holding a row's draft token also stores that logit.
-//  Decision: a launch that follows by programmatic dependent launch merges
-//    each row's chunks in chunk order and runs the sequence's acceptance
-//    chain. In the rejection rule with K <= 64 this is fused into phase 2a:
+//    of exp((x - max) / T)) and stores it; in the argmax rule it folds
+//    (max, lowest argmax id) into the row's slot with one 64-bit atomic
+//    maximum (no block waits on another). In the rejection rule the block
+//    holding a row's draft token also stores that logit.
+//  Decision: a launch that follows by programmatic dependent launch reads
+//    the slots (argmax rule) or merges each row's chunks in chunk order, and
+//    runs the sequence's acceptance chain. In the rejection rule with
+//    K <= 64 this is fused into phase 2a:
 //    every block of a sequence stages the sequence's chunk statistics in
 //    shared memory and reaches the same decision.
 //  Phase 2 (rejection rule only): 2a blocks stream the one or two rows the
@@ -78,7 +80,7 @@ struct alignas(16) DrawPart {
 };
 
 struct SpecLayout {
-    size_t row_ctr, seq_ctr_a, seq_ctr_b, row_parts, row_stats, tok_logit, plans, draw_parts, total;
+    size_t row_ctr, seq_ctr_a, seq_ctr_b, row_parts, row_stats, slots, tok_logit, plans, draw_parts, total;
     uint32_t rows_a, cmax_a, cmax_b;
 };
 
@@ -93,6 +95,7 @@ SpecLayout spec_layout(uint32_t S, uint32_t V, uint32_t K) {
     l.seq_ctr_b = o; o += align_up(static_cast<size_t>(S) * 4u, 256);
     l.row_parts = o; o += align_up(static_cast<size_t>(l.rows_a) * l.cmax_a * sizeof(RowPart), 256);
     l.row_stats = o; o += align_up(static_cast<size_t>(l.rows_a) * sizeof(RowPart), 256);
+    l.slots = o;     o += align_up(static_cast<size_t>(l.rows_a) * 8u, 256);
     l.tok_logit = o; o += align_up(static_cast<size_t>(l.rows_a) * 4u, 256);
     l.plans = o;     o += align_up(static_cast<size_t>(S) * sizeof(DrawPlan), 256);
     l.draw_parts = o; o += align_up(static_cast<size_t>(S) * l.cmax_b * sizeof(DrawPart), 256);
@@ -117,6 +120,7 @@ struct SpecArgs {
     uint32_t* seq_ctr;
     RowPart* row_parts;    // [rows_a][cmax_a]
     RowPart* row_stats;    // [rows_a]
+    unsigned long long* slots;  // [rows_a] argmax rule: the row's (max, lowest id) key, 0 between calls
     float* tok_logit;      // [rows_a]: the row's logit at its draft token (phase 1, rejection rule)
     DrawPlan* plans;       // [S]
     uint32_t cmax;
@@ -425,7 +429,17 @@ __global__ void __launch_bounds__(kNT) spec_phase1_kernel(SpecArgs a) {
         if (tid == 0)
             for (int ww = 0; ww < kWarps; ++ww) tot = ff_add(tot, s_ff[ww]);
     }
-    if (tid == 0) a.row_parts[static_cast<size_t>(t.row) * a.cmax + t.chunk] = RowPart{bm, bi | nf, tot.hi, tot.lo};
+    if (tid == 0) {
+        if (kRej) {
+            a.row_parts[static_cast<size_t>(t.row) * a.cmax + t.chunk] = RowPart{bm, bi | nf, tot.hi, tot.lo};
+        } else {
+            // argmax rule: fold (max, lowest id) into the row's slot; a larger
+            // key is a larger value, then a lower id; nonfinite: all ones
+            const unsigned long long key =
+                nf ? ~0ull : (static_cast<unsigned long long>(f2key(bm)) << 32) | static_cast<uint32_t>(~bi);
+            red_max_u64(&a.slots[t.row], key);
+        }
+    }
 }
 
 // Merge the C chunk statistics of one row in chunk order (one warp; every
@@ -536,24 +550,43 @@ __device__ __forceinline__ uint32_t seq_row(const SpecArgs& a, uint32_t s, uint3
 template <bool kRej>
 __global__ void __launch_bounds__(kNT) spec_rows_kernel(SpecArgs a) {
     __shared__ ChainPre pre;
+    __shared__ RowPart rs[kPre + 1];  // argmax rule with K <= kPre: the target rows
     pdl_wait();
     pdl_trigger();
     const uint32_t s = blockIdx.x, K = a.K;
     const uint32_t tid = threadIdx.x, warp = tid >> 5;
     if (a.decide) load_chain_pre<kRej>(a, s, pre);  // loaded while the rows are merged
     const uint32_t rows_t = K + 1u, rows_d = kRej ? K : 0u;
-    for (uint32_t i = warp; i < rows_t + rows_d; i += kWarps) {
-        const uint32_t r = seq_row(a, s, i);
-        const RowPart m = merge_parts<kRej>(a.row_parts + static_cast<size_t>(r) * a.cmax, a.chunks, a.log2e_over_T);
-        if ((tid & 31u) == 0) a.row_stats[r] = m;
-    }
-    if (!a.decide) return;
-    __syncthreads();  // row statistics and prefetched inputs of this block
-    if (warp == 0) {
-        const RowPart* tstat = a.row_stats + static_cast<size_t>(s) * rows_t;
-        const RowPart* dstat = a.row_stats + static_cast<size_t>(a.S) * rows_t + static_cast<size_t>(s) * K;
-        const uint32_t n = decide_sequence<kRej>(a, s, pre, tstat, dstat, true);
-        if (kRej && tid == 0) a.plans[s] = make_plan(n, K, tstat, dstat);
+    if constexpr (!kRej) {
+        // argmax rule (always deciding): each target row's key is in its
+        // slot, folded by phase 1's atomic maxima; read it and clear it
+        const bool small = K <= kPre;
+        for (uint32_t i = tid; i < rows_t; i += kNT) {
+            const uint32_t r = s * rows_t + i;
+            const unsigned long long key = a.slots[r];
+            a.slots[r] = 0ull;  // for the next call
+            const RowPart m{0.0f, key == ~0ull ? kNonfiniteBit : ~static_cast<uint32_t>(key), 0.0f, 0.0f};
+            if (small) rs[i] = m;
+            else a.row_stats[r] = m;
+        }
+        __syncthreads();
+        if (warp == 0)
+            decide_sequence<false>(a, s, pre, small ? rs : a.row_stats + static_cast<size_t>(s) * rows_t, nullptr,
+                                   true);
+    } else {
+        for (uint32_t i = warp; i < rows_t + rows_d; i += kWarps) {
+            const uint32_t r = seq_row(a, s, i);
+            const RowPart m = merge_parts<kRej>(a.row_parts + static_cast<size_t>(r) * a.cmax, a.chunks, a.log2e_over_T);
+            if ((tid & 31u) == 0) a.row_stats[r] = m;
+        }
+        if (!a.decide) return;
+        __syncthreads();  // row statistics and prefetched inputs of this block
+        if (warp == 0) {
+            const RowPart* tstat = a.row_stats + static_cast<size_t>(s) * rows_t;
+            const RowPart* dstat = a.row_stats + static_cast<size_t>(a.S) * rows_t + static_cast<size_t>(s) * K;
+            const uint32_t n = decide_sequence<kRej>(a, s, pre, tstat, dstat, true);
+            if (tid == 0) a.plans[s] = make_plan(n, K, tstat, dstat);
+        }
     }
 }
 
@@ -1100,6 +1133,7 @@ extern "C" sel_status spec_accept(const float* d_target, const float* d_draft, c
     a.seq_ctr = reinterpret_cast<uint32_t*>(ws + l.seq_ctr_a);
     a.row_parts = reinterpret_cast<RowPart*>(ws + l.row_parts);
     a.row_stats = reinterpret_cast<RowPart*>(ws + l.row_stats);
+    a.slots = reinterpret_cast<unsigned long long*>(ws + l.slots);
     a.tok_logit = reinterpret_cast<float*>(ws + l.tok_logit);
     a.plans = reinterpret_cast<DrawPlan*>(ws + l.plans);
     a.cmax = l.cmax_a;
