@@ -289,10 +289,10 @@ __global__ void __launch_bounds__(kNT) spec_phase1_kernel(SpecArgs a) {
     load_unit<kNT, kVPT, kVec>(row, t.lo, t.hi, -INFINITY, q);
     pdl_trigger();
     // Rejection rule: the row's draft token (target rows 0..K-1 and every
-    // draft row have one); the thread whose quads hold it stores the logit
-    // there for the acceptance chain.
+    // draft row have one); the block whose chunk holds it stores the logit
+    // there for the acceptance chain (thread 0, at its end)
     uint32_t tok_t = 0xFFFFFFFFu;
-    if (kRej && a.decide) {
+    if (kRej && a.decide && tid == 0) {
         const uint32_t nt = a.S * (a.K + 1u);
         const uint32_t j = t.row < nt ? t.row - seq * (a.K + 1u) : (t.row - nt) - seq * a.K;
         if (j < a.K) tok_t = a.tokens[static_cast<size_t>(seq) * a.K + j];
@@ -358,18 +358,6 @@ __global__ void __launch_bounds__(kNT) spec_phase1_kernel(SpecArgs a) {
                 thread_s = (acc[0] + acc[1]) + (acc[2] + acc[3]);
             }
         }
-        if (tok_t >= t.lo && tok_t < t.hi) {
-            const uint32_t o = tok_t - t.lo;
-            const uint32_t qi = o >> 2;
-            if (qi % kNT == static_cast<uint32_t>(tid)) {
-                const uint32_t hold = qi / kNT;
-                float4 qq = q[0];
-#pragma unroll
-                for (int sl = 1; sl < kVPT; ++sl) qq = static_cast<uint32_t>(sl) == hold ? q[sl] : qq;
-                const uint32_t c4 = o & 3u;
-                a.tok_logit[t.row] = c4 == 0u ? qq.x : (c4 == 1u ? qq.y : (c4 == 2u ? qq.z : qq.w));
-            }
-        }
     } else {
         // the thread's max, then the first quad holding it (ids rise with
         // the slot and the lane, so that is the lowest id of the max);
@@ -432,6 +420,7 @@ __global__ void __launch_bounds__(kNT) spec_phase1_kernel(SpecArgs a) {
     if (tid == 0) {
         if (kRej) {
             a.row_parts[static_cast<size_t>(t.row) * a.cmax + t.chunk] = RowPart{bm, bi | nf, tot.hi, tot.lo};
+            if (tok_t >= t.lo && tok_t < t.hi) a.tok_logit[t.row] = row[tok_t];
         } else {
             // argmax rule: fold (max, lowest id) into the row's slot; a larger
             // key is a larger value, then a lower id; nonfinite: all ones
