@@ -406,14 +406,12 @@ __device__ float typical_window(const float* wf, const float* g, float* byr, uin
 //  - top-p keeps the shortest prefix of the window with pf >= top_p * its
 //    total; min-p keeps wf_j >= min_p * wf_lo (wf falls, so the survivors
 //    stay a prefix); the draw takes the first j with u * pd_end < pd_j.
-// `live` false: compute but write nothing (see warm_finish).
 __device__ void sample_epilogue(const uint64_t* sorted, float* scratch, uint32_t n, uint32_t row, float u,
-                                bool nonfinite, const SampleArgs& sa, double nsig_thr, uint32_t* out_ids,
-                                bool live = true) {
+                                bool nonfinite, const SampleArgs& sa, double nsig_thr, uint32_t* out_ids) {
     const int lane = threadIdx.x & 31;
     const bool valid = !nonfinite && u >= 0.0f && u < 1.0f;
     if (!valid) {
-        if (live && lane == 0) { out_ids[row] = SEL_INVALID_ID; sa.out_probs[row] = __uint_as_float(0x7fc00000u); }
+        if (lane == 0) { out_ids[row] = SEL_INVALID_ID; sa.out_probs[row] = __uint_as_float(0x7fc00000u); }
         return;
     }
     // top-n-sigma: candidate 0 (the row's maximum) always reaches the threshold
@@ -431,7 +429,7 @@ __device__ void sample_epilogue(const uint64_t* sorted, float* scratch, uint32_t
         if (nc == 0) nc = 1;
     }
     if (sa.temperature == 0.0f || nc == 1) {  // greedy, or a single candidate
-        if (live && lane == 0) { out_ids[row] = cand_id(sorted[0]); sa.out_probs[row] = 1.0f; }
+        if (lane == 0) { out_ids[row] = cand_id(sorted[0]); sa.out_probs[row] = 1.0f; }
         return;
     }
     const float x0 = key2f(cand_key(sorted[0]));
@@ -490,7 +488,7 @@ __device__ void sample_epilogue(const uint64_t* sorted, float* scratch, uint32_t
         const uint32_t h1 = __ballot_sync(kFull, j1 < ns && target < pd1);
         const uint32_t pick = h0 ? static_cast<uint32_t>(__ffs(h0) - 1) : (h1 ? 31u + __ffs(h1) : e);
         const float wp = __shfl_sync(kFull, pick < 32u ? w0 : w1, static_cast<int>(pick & 31u));
-        if (live && lane == 0) {
+        if (lane == 0) {
             out_ids[row] = cand_id(sorted[pick]);
             sa.out_probs[row] = wp / total;
         }
@@ -585,7 +583,7 @@ __device__ void sample_epilogue(const uint64_t* sorted, float* scratch, uint32_t
         }
     }
     const float prob = wd[pick] / total;
-    if (live && lane == 0) {
+    if (lane == 0) {
         out_ids[row] = cand_id(sorted[pick]);
         sa.out_probs[row] = prob;
     }
@@ -1504,27 +1502,9 @@ __global__ void __launch_bounds__(kNT) full_draw_find_kernel(TopkArgs a) {
     }
 }
 
-// Run the selection and sampling code once on synthetic candidates in
-// shared memory, writing nothing: the finishing blocks start (programmatic
-// dependent launch) while the main launch still runs, and this brings their
-// instructions into the SM's caches before the real data can arrive. Touches
-// no global memory.
-template <bool kSample>
-__device__ void warm_finish(FinishShared& s, const TopkArgs& a) {
-    const uint32_t k = a.k, n = k + 16u;
-    for (uint32_t i = threadIdx.x; i < n; i += kNT) s.buf[i] = make_cand(f2key(-0.25f * static_cast<float>(i)), i);
-    __syncthreads();
-    block_select_sorted(s.buf, n, k, s.sorted);
-    if (kSample && threadIdx.x < 32)
-        sample_epilogue(s.sorted, reinterpret_cast<float*>(s.buf), k, 0, 0.5f, false, a.sa, -INFINITY, nullptr,
-                        false);
-    __syncthreads();
-}
-
 template <bool kSample, bool kFull>
 __global__ void __launch_bounds__(kNT) topk_finish_kernel(TopkArgs a) {
     __shared__ FinishShared s;
-    warm_finish<kSample>(s, a);
     pdl_wait();
     pdl_trigger();
     const uint32_t row = blockIdx.x, k = a.k, chunks = a.chunks;
