@@ -9,32 +9,36 @@
 // request that a chain with top-k first needs only the k candidates.
 //
 // Design (sm_103a). The page's implementation is a ggml graph op (TOP_K +
-// get_rows) whose kernel is not shown; this one is a single launch that
-// reads each row once:
-//  1. One block per row chunk of up to 8,192 logits (sel_units.cuh): each
-//     thread loads its 32 logits with 128-bit loads straight into registers
-//     and keeps the largest of each float4 and of the thread.
+// get_rows) whose kernel is not shown; this one reads each row once, in a
+// main launch and a finishing launch:
+//  1. One block per row chunk of up to 8,192 logits (sel_units.cuh). An
+//     aligned row's chunk lands in shared memory with one TMA bulk copy (a
+//     bounded mbarrier wait); other rows go through 128-bit or scalar loads
+//     into registers and then the same buffer. Each thread keeps the largest
+//     of each of its float4s and of its 32 logits.
 //  2. A cheap exact bound: with r = ceil(k / 8), each warp takes the r-th
 //     largest of its 32 lane maxima (r - 1 knock-out rounds of a warp max, or
 //     a shuffle bitonic sort for large r), and the minimum over the 8 warps
 //     is a value that at least 8 r >= k logits of the chunk reach, so nothing
 //     below it is in the chunk's top k. Only float4s whose maximum reaches
-//     the bound are looked at again; the survivors (typically k to 2 k) go to
-//     shared memory as 64-bit candidates (key << 32 | ~id), which order
-//     exactly like (value desc, id asc), and are selected exactly (rank
-//     counting, or a bitonic sort for large buffers). A chunk with more
-//     survivors than the buffer holds (ties, or k beyond the bound's reach)
+//     the bound are looked at again; the survivors (typically k to 3 k) are
+//     stored, unsorted, as the chunk's list of 64-bit candidates (key << 32 |
+//     ~id, which order exactly like (value desc, id asc)). A chunk with more
+//     survivors than its list holds (ties, or k beyond the bound's reach)
 //     takes an exact radix select of its k-th key instead, ties going to the
 //     lowest ids.
-//  3. Each block stores its sorted list in the workspace with plain stores
-//     (no fence, no arrival counter: no block waits on another). A finishing
-//     launch with one block per row (programmatic dependent launch, so its
-//     blocks are resident before the main launch ends) merges the row's
-//     lists: a bound from the lists' r-th entries (the m-th largest of the
-//     lists' r-th entries is reached by m * r >= k entries) discards almost
-//     every entry, and the survivors are selected exactly. Sampling then
-//     runs its softmax, top-p, min-p and inverse-CDF draw on the k candidates
-//     in one warp.
+//  3. Each block also stores its 8 warp maxima (the row's pool) and its
+//     nonfinite flag, and folds its bound into the row's slot with one atomic
+//     max: plain stores, no fence, no arrival counter, no block waits on
+//     another. The finishing launch (one block per row, programmatic
+//     dependent launch) bounds the row's k-th key by the larger of the slot
+//     and the pool bounds (the m-th largest of the chunks' r-th largest pool
+//     entries is reached by m r >= k distinct logits), keeps the list entries
+//     at or above it (typically a few dozen of the row's ~1,500), and selects
+//     the top k exactly by rank counting. Sampling then runs its filters and
+//     inverse-CDF draw on the k candidates in one warp (registers only for up
+//     to 64 candidates). Full-row sampling (top_k = 0) adds a second read of
+//     the row for the draw (see full_row_plan).
 #include <cfloat>
 
 #include "sel_plan.h"

@@ -17,7 +17,9 @@
 // or as a per-chunk record at its own slot. A small finishing launch that
 // follows in the same stream reads them, in chunk order where the order
 // matters, and clears what it used for the next call: no fence, ticket or
-// last-arrival block is needed.
+// last-arrival block is needed. (The diagnostics' paired pass is the one
+// launch that still ends each position with a last-arrival block,
+// arrive_is_last in sel_common.cuh.)
 //
 // Launches use programmatic dependent launch: a kernel waits for its
 // predecessor in the stream (griddepcontrol.wait) before it touches global
