@@ -54,6 +54,11 @@ constexpr uint32_t kGrain = 4u * kNT;        // unit sizes are multiples of this
 constexpr uint32_t kUnitMax = 4u * kNT * kVPT;  // 8,192 elements per unit
 constexpr uint32_t kCap = 2048;              // shard-merge buffer
 constexpr uint32_t kBlockCap = SEL_MAX_K;    // a chunk's survivors before the radix path
+// k up to kSmallK (without the moments or full-row sums) takes a main launch
+// with a smaller survivor buffer, so that six blocks (32 KB stage each) fit
+// an SM instead of five
+constexpr uint32_t kSmallK = 128;
+constexpr uint32_t kBlockCapSmall = 512;
 constexpr uint32_t kFinishBuf = 4096;        // row-merge buffer
 constexpr uint32_t kRound = kFinishBuf - SEL_MAX_K;  // list entries filtered per round
 constexpr int kRoundPer = static_cast<int>(kRound / kNT);
@@ -78,8 +83,9 @@ constexpr uint32_t kPool = kWarps;  // pool entries per chunk: its warp maxima
 // Shared memory of the main launch (the selection output and the radix
 // histogram of the rare paths live in the chunk's stage once it is no longer
 // read).
+template <uint32_t kCapB>
 struct alignas(16) ChunkShared {
-    uint64_t buf[kBlockCap];     // survivors
+    uint64_t buf[kCapB];         // survivors
     alignas(16) uint32_t warp_val[kWarps];
     alignas(16) uint32_t warp_max[kWarps];
     alignas(16) uint32_t warp_nf[kWarps];
@@ -787,10 +793,11 @@ __device__ __forceinline__ void write_row(const uint64_t* sorted, float* scratch
 // nonfinite flag, and folds its bound into the row's slot (atomic max). The
 // chunk is staged in shared memory (one bulk copy for aligned rows), so a
 // survivor's value is read back by its offset.
-template <bool kVec, bool kExtra>
-__global__ void __launch_bounds__(kNT, 5) topk_kernel(TopkArgs a) {
+template <bool kVec, bool kExtra, bool kSmall>
+__global__ void __launch_bounds__(kNT, kSmall ? 6 : 5) topk_kernel(TopkArgs a) {
+    constexpr uint32_t kCapB = kSmall ? kBlockCapSmall : kBlockCap;
     extern __shared__ float4 stage[];  // the chunk: kUnitMax floats
-    __shared__ ChunkShared s;
+    __shared__ ChunkShared<kCapB> s;
     __shared__ uint64_t bar;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t V = a.V, k = a.k;
@@ -1023,10 +1030,10 @@ __global__ void __launch_bounds__(kNT, 5) topk_kernel(TopkArgs a) {
             const uint32_t b = static_cast<uint32_t>(__ffs(marks) - 1);
             marks &= marks - 1u;
             const uint32_t o = 4u * (tid + kNT * (b >> 2)) + (b & 3u);
-            if (slot < kBlockCap) s.buf[slot] = make_cand(f2key(sf[o]), t.lo + o);
+            if (slot < kCapB) s.buf[slot] = make_cand(f2key(sf[o]), t.lo + o);
             ++slot;
         }
-    } else if (n_real <= kBlockCap) {
+    } else if (n_real <= kCapB) {
         // no bound (k beyond its reach, or too few elements): the whole chunk
         for (uint32_t o = tid; o < n_real; o += kNT) s.buf[o] = make_cand(f2key(sf[o]), t.lo + o);
         if (tid == 0) s.count = n_real;
@@ -1043,7 +1050,7 @@ __global__ void __launch_bounds__(kNT, 5) topk_kernel(TopkArgs a) {
         // the stage is free now (its survivors are in s.buf)
         uint32_t* hist = reinterpret_cast<uint32_t*>(stage);
         uint64_t* sorted = reinterpret_cast<uint64_t*>(stage) + 256;
-        if (n > kBlockCap) {
+        if (n > kCapB) {
             radix_select_chunk<kVec>(s, hist, a.logits + static_cast<size_t>(t.row) * V, t.lo, t.hi, k);
             n = s.count;
         }
@@ -1759,19 +1766,31 @@ sel_status launch_topk(const float* d_logits, uint32_t rows, uint32_t V, uint32_
     const dim3 grid(static_cast<uint32_t>(blocks));
     constexpr size_t kStage = static_cast<size_t>(kUnitMax) * 4u;
     static const bool attr_ok =
-        set_dynamic_smem(topk_kernel<true, false>, kStage) && set_dynamic_smem(topk_kernel<false, false>, kStage) &&
-        set_dynamic_smem(topk_kernel<true, true>, kStage) && set_dynamic_smem(topk_kernel<false, true>, kStage);
+        set_dynamic_smem(topk_kernel<true, false, false>, kStage) &&
+        set_dynamic_smem(topk_kernel<false, false, false>, kStage) &&
+        set_dynamic_smem(topk_kernel<true, true, false>, kStage) &&
+        set_dynamic_smem(topk_kernel<false, true, false>, kStage) &&
+        set_dynamic_smem(topk_kernel<true, false, true>, kStage) &&
+        set_dynamic_smem(topk_kernel<false, false, true>, kStage);
     if (!attr_ok) return SEL_ECUDA;
     // the chunk moments and full-row sums live in their own instances, out
     // of the plain path
     const bool extra = a.want_moments || a.full_row;
+    // the plain path with k <= kSmallK runs six blocks per SM (the moments
+    // and full-row sums need the registers of five)
+    const bool small = k <= kSmallK && !extra;
     cudaError_t e;
-    if (extra)
-        e = vec ? launch_pdl(topk_kernel<true, true>, grid, dim3(kNT), kStage, stream, a)
-                : launch_pdl(topk_kernel<false, true>, grid, dim3(kNT), kStage, stream, a);
-    else
-        e = vec ? launch_pdl(topk_kernel<true, false>, grid, dim3(kNT), kStage, stream, a)
-                : launch_pdl(topk_kernel<false, false>, grid, dim3(kNT), kStage, stream, a);
+    if (small) {
+        e = vec ? launch_pdl(topk_kernel<true, false, true>, grid, dim3(kNT), kStage, stream, a)
+                : launch_pdl(topk_kernel<false, false, true>, grid, dim3(kNT), kStage, stream, a);
+    } else {
+        if (extra)
+            e = vec ? launch_pdl(topk_kernel<true, true, false>, grid, dim3(kNT), kStage, stream, a)
+                    : launch_pdl(topk_kernel<false, true, false>, grid, dim3(kNT), kStage, stream, a);
+        else
+            e = vec ? launch_pdl(topk_kernel<true, false, false>, grid, dim3(kNT), kStage, stream, a)
+                    : launch_pdl(topk_kernel<false, false, false>, grid, dim3(kNT), kStage, stream, a);
+    }
     if (e != cudaSuccess) return SEL_ECUDA;
     e = a.full_row ? launch_pdl(topk_finish_kernel<kSample, true>, dim3(rows), dim3(kNT), 0, stream, a)
                    : launch_pdl(topk_finish_kernel<kSample, false>, dim3(rows), dim3(kNT), 0, stream, a);
