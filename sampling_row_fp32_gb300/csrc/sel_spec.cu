@@ -272,7 +272,7 @@ __device__ __forceinline__ DrawPlan make_plan(uint32_t n, uint32_t K, const RowP
 // Phase 1: per-row (max, sum exp) or (max, argmax); per-sequence decision.
 // One block per row chunk.
 template <bool kVec, bool kRej>
-__global__ void __launch_bounds__(kNT) spec_phase1_kernel(SpecArgs a) {
+__global__ void __launch_bounds__(kNT, 6) spec_phase1_kernel(SpecArgs a) {
     __shared__ float s_m[kWarps];
     __shared__ uint32_t s_i[kWarps];
     __shared__ uint32_t s_nf[kWarps];
