@@ -28,7 +28,8 @@ def check(orc, x, k, misalign=False):
 @pytest.mark.parametrize("rows,V,k", [
     (1, 1, 1), (2, 5, 3), (3, 16, 16), (2, 1000, 20), (4, 1025, 84), (3, 8192, 84),
     (3, 8193, 20), (5, 20_000, 40), (2, 65_537, 256), (2, 65_537, 257), (2, 100_000, 1024),
-    (3, 202_048, 84), (2, 248_320, 1), (4, 300_000, 20), (70, 5000, 7)])
+    (3, 202_048, 84), (2, 248_320, 1), (4, 300_000, 20), (70, 5000, 7),
+    (3, 248_320, 128), (3, 248_320, 129)])
 @pytest.mark.parametrize("misalign", [False, True])
 def test_random_rows(orc, rows, V, k, misalign):
     x = synth.normal_rows(rows + V + k, rows, V, 2.0)
@@ -44,7 +45,8 @@ def test_many_ties(orc, V, k):
     check(orc, x, k)
 
 
-@pytest.mark.parametrize("V,k", [(100, 7), (20_000, 84), (248_320, 20), (248_320, 1024)])
+@pytest.mark.parametrize("V,k", [(100, 7), (20_000, 84), (248_320, 20), (248_320, 128), (248_320, 129),
+                                 (248_320, 1024)])
 def test_adversarial_rows(orc, V, k):
     """All-equal, ascending and descending rows overflow the candidate
     buffer or defeat the filters; the fallback paths stay exact."""
