@@ -978,7 +978,7 @@ struct DiagArgs {
 };
 
 template <bool kVec>
-__global__ void __launch_bounds__(kNT) spec_diag_kernel(DiagArgs a) {
+__global__ void __launch_bounds__(kNT, 6) spec_diag_kernel(DiagArgs a) {
     __shared__ FF s_m[kWarps];
     __shared__ FF s_p[kWarps];
     __shared__ bool s_last;

@@ -1294,7 +1294,7 @@ struct Members {
 // Full-row draw, 1: block (row, chunk) sums the survivors' weights
 // 2^((x - M) c) (c = log2(e) / T) over its kDrawIds ids.
 template <bool kVec>
-__global__ void __launch_bounds__(kNT) full_draw_sum_kernel(TopkArgs a) {
+__global__ void __launch_bounds__(kNT, 8) full_draw_sum_kernel(TopkArgs a) {
     __shared__ FF s_w[kWarps];
     pdl_wait();
     pdl_trigger();
