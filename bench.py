@@ -336,12 +336,10 @@ def gpu_arm(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic (seeded Gumbel-perturbed Zipf(1.1) logits; no dataset)",
-        "config": {"workload": WORKLOAD, "rows": ROWS, "V": V, "topk_k": K_TOPK,
-                   "sample": POLICY, "spec": {"sequences": SPEC_S, "drafts": SPEC_K, "T": 1.0,
-                                              "rules": ["rejection", "argmax"]},
-                   "l2": f"inputs rotate over {N_COPIES} resident copies of the batch (535 MB); each "
-                         "launch reads a copy untouched for >= 487 MB of traffic (L2 is 129 MB)",
-                   "parallelism": f"replicas x{world} (independent rows)"},
+        "config": dict(workload_config(),
+                       l2=f"inputs rotate over {N_COPIES} resident copies of the batch (535 MB); each "
+                          "launch reads a copy untouched for >= 487 MB of traffic (L2 is 129 MB)",
+                       parallelism=f"replicas x{world} (independent rows)"),
         "step_gbs": round(step_bytes / step_s / 1e9, 1),
         "ops": ops,
         "roofline": {"bound": "hbm", "kernel": OPS[dom], "achieved": round(dom_gbs, 1), "peak": peak,
@@ -667,6 +665,12 @@ def cpu_baseline(steps=20, par_steps=3):
                                         f"{steps} steps"}}
 
 
+def workload_config():
+    """The workload both arms run (the GPU arm adds how its inputs are laid out)."""
+    return {"workload": WORKLOAD, "rows": ROWS, "V": V, "topk_k": K_TOPK, "sample": POLICY,
+            "spec": {"sequences": SPEC_S, "drafts": SPEC_K, "T": 1.0, "rules": ["rejection", "argmax"]}}
+
+
 def reference_arm(args, rank, world):
     if rank != 0:
         return None
@@ -684,7 +688,7 @@ def reference_arm(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded Gumbel-perturbed Zipf(1.1) logits; no dataset)",
-            "config": {"workload": WORKLOAD, "rows": ROWS, "V": V},
+            "config": workload_config(),
             "cpu_baseline": {"value": round(v, 3), "unit": "rows/s", "cores": 1, "kind": "oracle",
                              "sample": f"{REF_ROWS} of {ROWS} rows and one spec sequence per step"},
             "e2e": {"value": round(v, 3), "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
