@@ -266,8 +266,9 @@ sel_status spec_accept(const float *d_target, const float *d_draft,
  *
  *   d_target        [S][K+1][V] f32 target logits
  *   d_draft_tokens  [S][K] u32
- *   p               the target sampler (as for sel_sample; top_k >= 1 unless
- *                   temperature == 0, which is greedy)
+ *   p               the target sampler, as for sel_sample (temperature == 0
+ *                   is greedy; top_k == 0 samples the whole row, and a draw
+ *                   that fails closed there fails its sequence closed)
  *   d_u             [S][K+1] f32, one uniform per verified position
  *   d_accepted, d_emitted  as for spec_accept
  *   d_ws            workspace of sel_workspace_bytes(SEL_OP_SPEC_SAMPLER,

@@ -2020,7 +2020,7 @@ __global__ void __launch_bounds__(kNT) sampler_decide_kernel(const uint32_t* dra
 }  // namespace
 
 size_t spec_sampler_ws_bytes(uint32_t rows_t, uint32_t V, uint32_t top_k) {
-    uint32_t k = top_k == 0 ? 1u : top_k;
+    uint32_t k = top_k == 0 ? kFullRowCandidates : top_k;  // top_k = 0: full-row sampling
     if (k > V) k = V;
     if (rows_t == 0 || k > SEL_MAX_K) return 0;
     return sampler_layout(rows_t, V, k).total;
@@ -2037,7 +2037,8 @@ extern "C" sel_status spec_accept_sampler(const float* d_target, const uint32_t*
     if (!policy_valid(*p)) return SEL_EINVAL;
     uint32_t k = p->top_k;
     if (T == 0.0f) k = 1;
-    if (k == 0) return SEL_EUNSUPPORTED;
+    const bool full_row = k == 0;  // the whole row, as sel_sample with top_k = 0
+    if (full_row) k = kFullCand;
     if (k > V) k = V;
     if (k > SEL_MAX_K) return SEL_EUNSUPPORTED;
     if (S == 0) return SEL_OK;
@@ -2057,7 +2058,7 @@ extern "C" sel_status spec_accept_sampler(const float* d_target, const uint32_t*
     float* probs = reinterpret_cast<float*>(ws + l.probs);
     const SampleArgs sa = sample_args(*p, d_u, probs);
     const sel_status st = launch_topk<true>(d_target, static_cast<uint32_t>(rows_t), V, k, nullptr, draws, d_ws,
-                                           l.draws, sa, stream);
+                                           l.draws, sa, stream, full_row);
     if (st != SEL_OK) return st;
     const dim3 grid((S + kWarps - 1) / kWarps);
     return launch_pdl(sampler_decide_kernel, grid, dim3(kNT), 0, stream, static_cast<const uint32_t*>(draws),

@@ -168,7 +168,9 @@ def test_spec_rules_validation_needs_no_gpu(lib):
     assert f(fake, fake, 0, 3, 100, ctypes.byref(p), fake, fake, fake, fake, 4096, None) == B.SEL_OK  # S = 0
     assert f(fake, fake, 2, 3, 100, None, fake, fake, fake, fake, 4096, None) == B.SEL_EINVAL
     assert f(fake, fake, 2, 3, 100, ctypes.byref(B.SampleParams(1.0, 0, 0.9, 0.0, 0)), fake, fake, fake,
-             fake, 4096, None) == B.SEL_EUNSUPPORTED                                          # top_k = 0
+             fake, 16, None) == B.SEL_EWORKSPACE                                              # top_k = 0: full row
+    assert (B.sel_workspace_bytes(B.SEL_OP_SPEC_SAMPLER, 8, 151_936, 0)
+            == B.sel_workspace_bytes(B.SEL_OP_SPEC_SAMPLER, 8, 151_936, 64))
     assert f(fake, fake, 2, 3, 100, ctypes.byref(p), None, fake, fake, fake, 4096, None) == B.SEL_EINVAL
     assert f(fake, fake, 2, 3, 300_000, ctypes.byref(p), fake, fake, fake, fake, 16, None) == B.SEL_EWORKSPACE
     g = lib.spec_diagnostics

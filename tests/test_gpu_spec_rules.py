@@ -70,6 +70,26 @@ def test_sampler_match_on_the_spec_workload(orc, T, top_k, top_p, min_p, temp_la
             assert emi[s, n] == a[s, n] and all(tok[s, :n] == a[s, :n])
 
 
+@pytest.mark.parametrize("T,top_p,min_p,temp_last", [(1.0, 1.0, 0.0, False), (0.8, 1.0, 0.05, False),
+                                                     (1.0, 0.9, 0.0, False), (1.2, 0.95, 0.02, True)])
+@pytest.mark.parametrize("misalign", [False, True])
+def test_sampler_match_full_row(orc, T, top_p, min_p, temp_last, misalign):
+    """top_k = 0: each position draws from its whole target row (sel_sample's
+    full-row sampling). The rows are peaked enough (the spec workload's
+    logits times 6: every nucleus of these policies holds at most 32 ids)
+    that every top-p cut lies within the 64 candidates the draw is decided
+    on, so no row fails closed."""
+    si = synth.workload_spec()
+    tgt = (si.target * 6.0).astype(np.float32)
+    tok = drafts_near_target(tgt, 76)
+    S, K1, _ = tgt.shape
+    u = synth.uniforms(77, S * K1).reshape(S, K1)
+    acc, emi = sampler(tgt, tok, u, T, 0, top_p, min_p, temp_last, misalign)
+    ref = orc.spec_sampler(tgt, tok, T, 0, top_p, min_p, u, temp_last)
+    assert np.all(acc != INVALID)
+    assert_spec_matches(acc, emi, ref, max_mismatch_frac=0.13)
+
+
 @pytest.mark.parametrize("S,K,V,misalign", [(1, 0, 1000, False), (5, 1, 4097, True), (33, 3, 2048, False)])
 def test_sampler_match_shapes(orc, S, K, V, misalign):
     rng = np.random.default_rng(72 + K)
