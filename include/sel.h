@@ -146,8 +146,9 @@ sel_status sel_topk(const float *d_logits, uint32_t rows, uint32_t V,
 /*
  * Sampling policy.
  *   temperature  >= 0; 0 means greedy (the argmax, probability 1)
- *   top_k        1 <= top_k <= SEL_MAX_K (top_k > V means V); 0 (no
- *                truncation) returns SEL_EUNSUPPORTED unless temperature == 0
+ *   top_k        1 <= top_k <= SEL_MAX_K (top_k > V means V); 0 means no
+ *                truncation: full-row sampling, the chain over all V ids
+ *                (see sel_sample)
  *   top_p        (0, 1]; 1 disables it
  *   min_p        [0, 1); 0 disables it
  *   order        SEL_ORDER_TEMP_FIRST or SEL_ORDER_TEMP_LAST
@@ -188,6 +189,14 @@ typedef struct sel_sample_params {
  * the same order, whose cumulative Q exceeds u (the last survivor if
  * rounding leaves none). TEMP_LAST computes the filters with T = 1 and Q with
  * the tempered weights.
+ * Full-row sampling (top_k == 0, temperature > 0): the same chain with every
+ * id of the row as a candidate; the draw walks the survivors in ascending
+ * token id instead (the same distribution, without sorting the row). The
+ * row is read twice. The filters are decided from the row's 64 most probable
+ * ids against sums over the whole row; a top-p or typical cut that needs ids
+ * beyond those 64 is not decided: that row fails closed (SEL_INVALID_ID,
+ * probability NaN) and bit 3 (8) is set in the workspace's first 32-bit
+ * word.
  * Sources: Muser book 21.1 (temperature-scaled softmax, then a draw
  * restricted to top-k / top-p candidates) and 21.7 (top-k truncation before
  * the top-p cutoff); llama.cpp pull 49, "Change" (a chain with top-k first
@@ -322,8 +331,11 @@ sel_status spec_diagnostics(const float *d_target, const float *d_draft,
  * it zeroes the part of the array it uses with cudaMemsetAsync on `stream` and
  * launches on `stream`. The first call on a device looks the array's device
  * address up (cudaGetSymbolAddress), so make that first call before any
- * stream capture. Every call on a device shares the one array: calls that
- * may overlap on the GPU (different streams without ordering) race.
+ * stream capture. Later calls look it up again unless their stream is being
+ * captured, so a cudaDeviceReset or another context made current between
+ * calls is followed. Every call on a device shares the one array: calls that
+ * may overlap on the GPU (different streams without ordering) race; order
+ * them (one stream, or an event between streams).
  */
 #define SEL_NOALLOC_SCRATCH_BYTES (1u << 20)
 sel_status sel_argmax_noalloc(const float *d_logits, uint32_t rows, uint32_t V,

@@ -27,16 +27,24 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch per device (null until looked up). In
-// host code the array's name is only a host-side stand-in, so the first call
-// on a device looks the address up with cudaGetSymbolAddress while that
-// device is current, and later calls reuse it.
+// Device address of g_noalloc_scratch per device, from the last lookup on
+// that device (null until the first). In host code the array's name is only
+// a host-side stand-in, so the address is looked up with
+// cudaGetSymbolAddress while the device is current. The lookup is repeated
+// on every call whose stream is not being captured: a cudaDeviceReset, or a
+// different context made current since the last call, gives the array a new
+// address, and a stale one would send the kernels to memory this context
+// does not own. A call on a capturing stream reuses the last address found
+// on its device, looking it up only when there is none yet.
 std::atomic<void*> g_scratch_addr[kMaxDevices];
 
-sel_status scratch_address(void** out) {
+sel_status scratch_address(cudaStream_t stream, void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SEL_ECUDA;
-    void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return SEL_ECUDA;
+    void* p = nullptr;
+    if (cap != cudaStreamCaptureStatusNone) p = g_scratch_addr[dev].load(std::memory_order_acquire);
     if (!p) {
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return SEL_ECUDA;
         g_scratch_addr[dev].store(p, std::memory_order_release);
@@ -55,7 +63,7 @@ extern "C" sel_status sel_argmax_noalloc(const float* d_logits, uint32_t rows, u
     const size_t need = sel_workspace_bytes(SEL_OP_ARGMAX, rows, V, 0);
     if (need == 0 || need > kNoAllocScratchBytes) return SEL_EWORKSPACE;  // beyond the reserved size
     void* ws = nullptr;
-    const sel_status st = scratch_address(&ws);
+    const sel_status st = scratch_address(stream, &ws);
     if (st != SEL_OK) return st;
     // the error word and the per-row slots must start at zero
     if (cudaMemsetAsync(ws, 0, need, stream) != cudaSuccess) return SEL_ECUDA;

@@ -101,17 +101,17 @@ def sample(x: np.ndarray, u: np.ndarray, T, top_k, top_p, min_p, temp_last=False
     return B.ids_to_numpy(ids), probs.cpu().numpy()
 
 
-def assert_sample_matches(got_ids, got_probs, ref, max_mismatch_frac=0.02):
-    """ids equal except where the oracle's decision margin is <= MARGIN (and
-    such exempt mismatches stay rare); probabilities within PROB_RTOL where
-    ids agree."""
+def assert_sample_matches(got_ids, got_probs, ref, max_mismatch=0):
+    """ids equal except where the oracle's decision margin is <= MARGIN, and
+    at most `max_mismatch` such exempt rows may differ (an absolute count);
+    probabilities within PROB_RTOL where ids agree."""
     assert not np.any(got_ids == np.uint32(SENTINEL & 0xFFFFFFFF)), np.nonzero(got_ids == np.uint32(SENTINEL & 0xFFFFFFFF))
     exempt = ref.margin <= MARGIN
     mismatch = got_ids != ref.ids
     bad = mismatch & ~exempt
     assert not bad.any(), (np.nonzero(bad)[0][:10], got_ids[bad][:10], ref.ids[bad][:10],
                            ref.margin[bad][:10])
-    assert mismatch.mean() <= max_mismatch_frac, mismatch.mean()
+    assert int(mismatch.sum()) <= max_mismatch, (int(mismatch.sum()), int(exempt.sum()), mismatch.size)
     same = (got_ids == ref.ids) & (ref.ids != INVALID)
     np.testing.assert_allclose(got_probs[same], ref.probs[same], rtol=PROB_RTOL)
     inval = ref.ids == INVALID
@@ -136,16 +136,17 @@ def spec(si_target, si_draft, tokens, u_acc, u_fin, T, mode, misalign=False):
     return B.ids_to_numpy(acc), B.ids_to_numpy(emi)
 
 
-def assert_spec_matches(acc, emi, ref, max_mismatch_frac=0.05):
+def assert_spec_matches(acc, emi, ref, max_mismatch=0):
     """accepted counts and emitted tokens equal the oracle's, except for
     sequences whose accept test (|u q - p| <= 1e-6 max(p, q)) or final draw
-    (|u - C_i| <= 1e-6) sits on a threshold; such exempt mismatches stay
-    rare. (At V ~ 150k the CDF steps are ~1e-5 apart, so a sizeable share of
-    draws is exempt; the GPU's CDF error is far below 1e-6, so exempt draws
-    still match almost always.)"""
+    (|u - C_i| <= 1e-6) sits on a threshold; at most `max_mismatch` such
+    exempt sequences may differ (an absolute count). (At V ~ 150k the CDF
+    steps are ~1e-5 apart, so a sizeable share of draws is exempt; the GPU's
+    CDF error is far below 1e-6, so exempt draws still match almost
+    always.)"""
     exempt = (ref.margin_accept <= MARGIN) | (ref.margin_draw <= MARGIN)
     mismatch = (acc != ref.accepted) | (emi != ref.emitted).any(axis=1)
     bad = mismatch & ~exempt
     assert not bad.any(), (np.nonzero(bad)[0][:5], acc[bad][:5], ref.accepted[bad][:5],
                            emi[bad][:5], ref.emitted[bad][:5])
-    assert mismatch.mean() <= max_mismatch_frac, mismatch.mean()
+    assert int(mismatch.sum()) <= max_mismatch, (int(mismatch.sum()), int(exempt.sum()), mismatch.size)

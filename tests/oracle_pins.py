@@ -282,6 +282,50 @@ def pin_sample_invalid(orc):
     assert np.all(r.ids == INVALID) and np.all(np.isnan(r.probs))
 
 
+def pin_sample_margins(orc):
+    """The decision margins of filtered sampling, hand-derived
+    (golden margins_closed_forms.json): distance of u to the nearest CDF step
+    (neither 0 nor the final step counts), of each top-p prefix to top_p, of
+    each min-p ratio to min_p, of the typical cut (with its score gap) and of
+    the ids around the top-n-sigma threshold. These margins decide which GPU
+    rows are exempt from bit-exact comparison."""
+    g = golden("margins_closed_forms.json")
+    for case in g["sample"]:
+        x = _logits_from(case)[None]
+        r = orc.sample(x, [case["u"]], case["T"], case["top_k"], case["top_p"], case["min_p"],
+                       False, case.get("top_n_sigma", 0.0), case.get("typical_p", 1.0))
+        assert int(r.ids[0]) == case["id"], (case["name"], r.ids[0])
+        assert abs(r.probs[0] - case["prob"]) <= 1e-6, (case["name"], r.probs[0])
+        assert abs(r.margin[0] - case["margin"]) <= 1e-6, (case["name"], r.margin[0], case["margin"])
+
+
+def pin_spec_margins(orc):
+    """The rejection test's margin |u q - p| / max(p, q) and the residual and
+    bonus draws' CDF margins in ascending id, hand-derived (golden
+    margins_closed_forms.json)."""
+    g = golden("margins_closed_forms.json")
+    rows = {k: _logits_from(v) for k, v in g["spec_rows"].items()}
+    for case in g["spec"]:
+        target = np.stack([rows[n] for n in case["target"]])[None]
+        draft = np.stack([rows[n] for n in case["draft"]])[None]
+        tok = np.asarray(case["tokens"], dtype=np.uint32)[None]
+        r = orc.spec_accept(target, draft, tok, 1.0, 0, np.asarray(case["u_acc"], np.float32)[None],
+                            np.asarray([case["u_fin"]], np.float32))
+        assert int(r.accepted[0]) == case["accepted"], (case["name"], r.accepted[0])
+        assert [int(e) for e in r.emitted[0]] == case["emitted"], (case["name"], r.emitted[0])
+        assert abs(r.margin_accept[0] - case["margin_accept"]) <= 1e-6, (case["name"], r.margin_accept[0])
+        assert abs(r.margin_draw[0] - case["margin_draw"]) <= 1e-6, (case["name"], r.margin_draw[0])
+    rows = {k: _logits_from(v) for k, v in g["sampler_rows"].items()}
+    for case in g["sampler"]:
+        target = np.stack([rows[n] for n in case["target"]])[None]
+        tok = np.asarray(case["tokens"], dtype=np.uint32)[None]
+        u = np.asarray(case["u"], dtype=np.float32)[None]
+        r = orc.spec_sampler(target, tok, case["T"], case["top_k"], 1.0, 0.0, u)
+        assert int(r.accepted[0]) == case["accepted"], (case["name"], r.accepted[0])
+        assert [int(e) for e in r.emitted[0]] == case["emitted"], (case["name"], r.emitted[0])
+        assert abs(r.margin_draw[0] - case["margin"]) <= 1e-6, (case["name"], r.margin_draw[0])
+
+
 # ---------------------------------------------------------------------------
 # speculative acceptance
 # ---------------------------------------------------------------------------
@@ -639,10 +683,10 @@ ALL_PINS = [
     pin_eog_bruteforce, pin_eog_reduces_to_argmax, pin_eog_nonfinite,
     pin_topk_bruteforce, pin_topk_lexsort, pin_topk_special,
     pin_sample_closed_forms, pin_sample_cdf_grid, pin_sample_support,
-    pin_sample_invalid, pin_filters_closed_forms, pin_filters_reduce,
+    pin_sample_invalid, pin_sample_margins, pin_filters_closed_forms, pin_filters_reduce,
     pin_spec_closed_forms, pin_spec_ceiling_example, pin_spec_acceptance_law,
     pin_spec_stream_is_target, pin_spec_support, pin_spec_regimes,
-    pin_spec_greedy, pin_spec_invalid,
+    pin_spec_greedy, pin_spec_invalid, pin_spec_margins,
     pin_diag_closed_forms, pin_diag_inequality, pin_diag_is_the_rejection_acceptance,
     pin_sampler_acceptance_law, pin_sampler_stream_is_target, pin_sampler_greedy_and_support,
     pin_sampler_invalid,

@@ -18,10 +18,10 @@ def orc():
     return oracle.default()
 
 
-def check(orc, x, u, T, k, p, m, temp_last=False, misalign=False, max_mismatch_frac=0.02):
+def check(orc, x, u, T, k, p, m, temp_last=False, misalign=False, max_mismatch=0):
     gi, gp = G.sample(x, u, T, k, p, m, temp_last, misalign)
     ref = orc.sample(x, u, T, k, p, m, temp_last)
-    G.assert_sample_matches(gi, gp, ref, max_mismatch_frac)
+    G.assert_sample_matches(gi, gp, ref, max_mismatch)
     return gi, gp, ref
 
 

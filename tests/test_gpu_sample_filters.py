@@ -21,10 +21,10 @@ def orc():
     return oracle.default()
 
 
-def check(orc, x, u, T, k, p, m, nsig=0.0, typ=0.0, temp_last=False, misalign=False, max_mismatch_frac=0.02):
+def check(orc, x, u, T, k, p, m, nsig=0.0, typ=0.0, temp_last=False, misalign=False, max_mismatch=0):
     gi, gp = G.sample(x, u, T, k, p, m, temp_last, misalign, nsig, typ)
     ref = orc.sample(x, u, T, k, p, m, temp_last, top_n_sigma=nsig, typical_p=typ if typ > 0 else 1.0)
-    G.assert_sample_matches(gi, gp, ref, max_mismatch_frac)
+    G.assert_sample_matches(gi, gp, ref, max_mismatch)
     return gi, gp, ref
 
 

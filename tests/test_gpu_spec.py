@@ -22,12 +22,12 @@ def orc():
     return oracle.default()
 
 
-def run_both(orc, si, mode, misalign=False, max_mismatch_frac=0.05):
+def run_both(orc, si, mode, misalign=False, max_mismatch=0):
     acc, emi = G.spec(si.target, si.draft, si.draft_tokens, si.u_acc, si.u_fin,
                       si.temperature, mode, misalign)
     ref = orc.spec_accept(si.target, si.draft, si.draft_tokens, si.temperature, mode,
                           si.u_acc, si.u_fin)
-    G.assert_spec_matches(acc, emi, ref, max_mismatch_frac)
+    G.assert_spec_matches(acc, emi, ref, max_mismatch)
     return acc, emi, ref
 
 

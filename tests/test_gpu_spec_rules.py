@@ -62,7 +62,7 @@ def test_sampler_match_on_the_spec_workload(orc, T, top_k, top_p, min_p, temp_la
     u = synth.uniforms(71, S * K1).reshape(S, K1)
     acc, emi = sampler(tgt, tok, u, T, top_k, top_p, min_p, temp_last)
     ref = orc.spec_sampler(tgt, tok, T, top_k, top_p, min_p, u, temp_last)
-    assert_spec_matches(acc, emi, ref, max_mismatch_frac=0.13)
+    assert_spec_matches(acc, emi, ref)
     if T == 0.0:  # greedy sampler = the argmax rule
         a = np.argmax(tgt, axis=2)
         for s in range(S):
@@ -87,7 +87,7 @@ def test_sampler_match_full_row(orc, T, top_p, min_p, temp_last, misalign):
     acc, emi = sampler(tgt, tok, u, T, 0, top_p, min_p, temp_last, misalign)
     ref = orc.spec_sampler(tgt, tok, T, 0, top_p, min_p, u, temp_last)
     assert np.all(acc != INVALID)
-    assert_spec_matches(acc, emi, ref, max_mismatch_frac=0.13)
+    assert_spec_matches(acc, emi, ref)
 
 
 @pytest.mark.parametrize("S,K,V,misalign", [(1, 0, 1000, False), (5, 1, 4097, True), (33, 3, 2048, False)])
@@ -98,7 +98,7 @@ def test_sampler_match_shapes(orc, S, K, V, misalign):
     u = rng.random((S, K + 1), dtype=np.float32)
     acc, emi = sampler(tgt, tok, u, 1.0, 16, 0.95, 0.0, misalign=misalign)
     ref = orc.spec_sampler(tgt, tok, 1.0, 16, 0.95, 0.0, u)
-    assert_spec_matches(acc, emi, ref, max_mismatch_frac=0.1)
+    assert_spec_matches(acc, emi, ref)
 
 
 def test_sampler_match_fails_closed(orc):
@@ -115,7 +115,7 @@ def test_sampler_match_fails_closed(orc):
     for s in range(4):
         assert acc[s] == INVALID and np.all(emi[s] == INVALID)
     ref = orc.spec_sampler(tgt, tok, 1.0, 10, 1.0, 0.0, u)
-    assert_spec_matches(acc, emi, ref, max_mismatch_frac=0.34)
+    assert_spec_matches(acc, emi, ref)
 
 
 @pytest.mark.parametrize("T", [0.5, 1.0, 2.0])

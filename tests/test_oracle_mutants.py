@@ -97,6 +97,28 @@ MUTANTS = [
      [("if (cum >= typical_p) {", "if (cum > typical_p + 0.2) {")]),
     ("typical set not renormalised",
      [("        Sf = S2;\n", "        Sf = Sf;\n")]),
+    ("CDF margin measured to the previous step",
+     [("double d = fabs(u - c / W);", "double d = fabs(u - (c - w[i]) / W);")]),
+    ("CDF margin counts the final step",
+     [("if (last_pos != ORC_INVALID && i >= last_pos)", "if (last_pos != ORC_INVALID && i > last_pos)")]),
+    ("CDF margin counts steps without mass",
+     [("if (w[i] > 0.0) {", "if (1) {")]),
+    ("accept margin not scaled by max(p, q)",
+     [("double d = fabs(lhs - pt) / scale;", "double d = fabs(lhs - pt);")]),
+    ("accept margin scaled by p alone",
+     [("double d = fabs(lhs - pt) / scale;", "double d = fabs(lhs - pt) / pt;")]),
+    ("top-p margin taken before the prefix's own mass",
+     [("            cum += wf[j] / Sf;\n            double d = fabs(cum - top_p);",
+       "            double d = fabs(cum - top_p);\n            cum += wf[j] / Sf;")]),
+    ("min-p margin on the absolute probability",
+     [("double d = fabs(ratio - min_p);", "double d = fabs(wf[j] / Sf - min_p);")]),
+    ("top-n-sigma margin not relative to the threshold",
+     [("double scale = fabs(thr) > 1.0 ? fabs(thr) : 1.0;", "double scale = 1.0;")]),
+    ("typical margin ignores the score gap at the cut",
+     [("if (g / sc < *margin)", "if (0)")]),
+    ("sampler-match margin keeps only the last draw",
+     [("        if (m < *margin)\n            *margin = m;\n        if (n == K || tokens[n] != drawn)",
+       "        *margin = m;\n        if (n == K || tokens[n] != drawn)")]),
     ("EOG all-excluded row answers id 0",
      [("    return best;\n}\n\nvoid orc_argmax_excluding(",
        "    return best == ORC_INVALID ? 0 : best;\n}\n\nvoid orc_argmax_excluding(")]),

@@ -63,3 +63,41 @@ def test_rejects_requests_beyond_the_reserved_scratch(lib):
     # 8 bytes per row after a 256-byte header, in 256-byte steps
     assert B.sel_workspace_bytes(B.SEL_OP_ARGMAX, 131_040, V) <= B.SEL_NOALLOC_SCRATCH_BYTES
     assert B.sel_workspace_bytes(B.SEL_OP_ARGMAX, 131_041, V) > B.SEL_NOALLOC_SCRATCH_BYTES
+
+
+def test_largest_request_that_fits(lib):
+    """131,040 rows need the whole reserved scratch (8 bytes a row after the
+    header): the largest call the entry point accepts, on short rows."""
+    rows, V = 131_040, 8
+    assert B.sel_workspace_bytes(B.SEL_OP_ARGMAX, rows, V) <= B.SEL_NOALLOC_SCRATCH_BYTES
+    x = torch.from_numpy(synth.normal_rows(33, rows, V, 3.0)).cuda()
+    x[7, [2, 5]] = x[7].max() + 1                  # a tie inside one row
+    want = regular_argmax(x)
+    for _ in range(2):
+        got = noalloc_argmax(x)
+        torch.cuda.synchronize()
+        assert torch.equal(got, want)
+    assert int(got[7]) == 2
+
+
+def test_calls_on_two_streams_ordered_by_an_event(lib):
+    """The calls share one scratch array, so calls on different streams must
+    be ordered: here the second stream waits on an event recorded after the
+    first call. Both results equal sel_argmax's."""
+    a = torch.from_numpy(synth.normal_rows(34, 49, 248_320, 3.0)).cuda()
+    b = torch.from_numpy(synth.normal_rows(35, 64, 202_048, 3.0)).cuda()
+    want_a, want_b = regular_argmax(a), regular_argmax(b)
+    out_a = torch.full((49,), -7, dtype=torch.int32, device="cuda")
+    out_b = torch.full((64,), -7, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()  # inputs and pre-filled outputs are ready for both streams
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    done = torch.cuda.Event()
+    with torch.cuda.stream(s1):
+        B.sel_argmax_noalloc(a, out_a, stream=s1)
+        done.record(s1)
+    s2.wait_event(done)
+    with torch.cuda.stream(s2):
+        B.sel_argmax_noalloc(b, out_b, stream=s2)
+    torch.cuda.synchronize()
+    assert torch.equal(out_a, want_a)
+    assert torch.equal(out_b, want_b)
