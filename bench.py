@@ -48,6 +48,14 @@ N_GRAPHS = 5 * N_COPIES  # captured step graphs; step s replays graph s % N_GRAP
 STEPS_PER_GRAPH = 5      # steps captured together for the timed loop
 
 
+NOMINAL_HBM_GBS = 8000.0  # the ~8 TB/s HBM3e figure the target is stated against
+
+
+def fracs(gbs: float, peak: float) -> dict:
+    """Fractions of the measured copy peak and of the nominal HBM figure."""
+    return {"frac_of_peak": round(gbs / peak, 4), "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4)}
+
+
 def measured_peak():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -318,9 +326,9 @@ def gpu_arm(args, rank, world, local_rank):
     step_bytes = sum(bytes_per_op)
     dom = int(np.argmax(per_op_us))
     dom_gbs = bytes_per_op[dom] / (per_op_us[dom] * 1e-6) / 1e9
-    ops = {OPS[i]: {"us": round(per_op_us[i], 3), "bytes": bytes_per_op[i],
-                    "gbs": round(bytes_per_op[i] / (per_op_us[i] * 1e-6) / 1e9, 1),
-                    "frac_of_peak": round(bytes_per_op[i] / (per_op_us[i] * 1e-6) / 1e9 / peak, 4)}
+    ops = {OPS[i]: dict({"us": round(per_op_us[i], 3), "bytes": bytes_per_op[i],
+                         "gbs": round(bytes_per_op[i] / (per_op_us[i] * 1e-6) / 1e9, 1)},
+                        **fracs(bytes_per_op[i] / (per_op_us[i] * 1e-6) / 1e9, peak))
            for i in range(5)}
     traffic = load_traffic(OPS[dom])
     line = {
@@ -344,6 +352,7 @@ def gpu_arm(args, rank, world, local_rank):
         "ops": ops,
         "roofline": {"bound": "hbm", "kernel": OPS[dom], "achieved": round(dom_gbs, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
+                     "frac_of_nominal": round(dom_gbs / NOMINAL_HBM_GBS, 4), "nominal_gbs": NOMINAL_HBM_GBS,
                      "traffic": traffic},
         "gpu_launches": launches_per_step * args.steps,
         "timing": f"steps replayed from CUDA graphs of {STEPS_PER_GRAPH} consecutive steps; per-op times "
@@ -351,6 +360,7 @@ def gpu_arm(args, rank, world, local_rank):
         "clocks": clk,
         "e2e": e2e,
         "extra_ops": extra,
+        "configs": named_configs(B, dev, stream),
     }
     return line
 
@@ -405,6 +415,8 @@ def extra_ops(B, dev, xs, drafts, tok, stream):
     uu = torch.rand(ROWS, device=dev)
     ws_f = B.workspace(B.SEL_OP_SAMPLE, ROWS, V, POLICY["top_k"], device=dev)
     prm_full = B.SampleParams(POLICY["temperature"], 0, POLICY["top_p"], POLICY["min_p"], B.SEL_ORDER_TEMP_FIRST)
+    prm_last = B.SampleParams(POLICY["temperature"], POLICY["top_k"], POLICY["top_p"], POLICY["min_p"],
+                              B.SEL_ORDER_TEMP_LAST)
     ws_full = B.workspace(B.SEL_OP_SAMPLE, ROWS, V, 0, device=dev)
     calls = {
         "argmax_excluding_8": (lambda r: B.sel_argmax_excluding(xs[r % N_COPIES], exd, ids, ws_a), ROWS * ROW_BYTES),
@@ -413,6 +425,10 @@ def extra_ops(B, dev, xs, drafts, tok, stream):
                             2 * ROWS * ROW_BYTES),
         "sample_nsigma1_typical08": (lambda r: B.sel_sample(xs[r % N_COPIES], prm_f, uu, sid, spr, ws_f),
                                      ROWS * ROW_BYTES),
+        # the step's policy with the filters on the untempered distribution
+        # and the temperature in the draw only
+        "sample_temp_last": (lambda r: B.sel_sample(xs[r % N_COPIES], prm_last, uu, sid, spr, ws_f),
+                             ROWS * ROW_BYTES),
         "spec_sampler_match": (lambda r: B.spec_accept_sampler(tview(xs[r % N_COPIES]), tok, prm, ud, acc, emi, ws_m),
                                ROWS * ROW_BYTES),
         "spec_diagnostics": (lambda r: B.spec_diagnostics(tview(xs[r % N_COPIES]), drafts[r % 2], 1.0, smin, sprod,
@@ -440,7 +456,112 @@ def extra_ops(B, dev, xs, drafts, tok, stream):
         torch.cuda.synchronize()
         us = a.elapsed_time(b) * 1e3 / OP_REPS
         gbs = nbytes / (us * 1e-6) / 1e9
-        out[name] = {"us": round(us, 3), "bytes": nbytes, "gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
+        out[name] = dict({"us": round(us, 3), "bytes": nbytes, "gbs": round(gbs, 1)}, **fracs(gbs, peak))
+    return out
+
+
+def named_configs(B, dev, stream):
+    """The other named workloads, each timed like the step's ops: graph-replayed
+    calls between events, every call reading a copy of its input that at
+    least ~480 MB of other reads have passed since (L2 is 129 MB). The one-row
+    argmax and the three-row top-k move under 3 MB a call: they are bound by
+    launch latency, so their HBM fractions are reported but mean little."""
+    import torch
+    from sampling_row_fp32_gb300 import synth
+    peak, _ = measured_peak()
+    out = {}
+
+    def timed(fn, n_copies, reps):
+        with torch.cuda.stream(stream):
+            for r in range(3):
+                fn(r % n_copies)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for r in range(reps):
+                fn(r % n_copies)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / reps
+
+    def record(name, what, us, rows, nbytes, note=None):
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out[name] = dict({"workload": what, "us": round(us, 3), "rows_per_s": round(rows / (us * 1e-6), 1),
+                          "bytes": nbytes, "gbs": round(gbs, 1)}, **fracs(gbs, peak))
+        if note:
+            out[name]["note"] = note
+
+    def copies(a: np.ndarray, n: int):
+        t = torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        big = torch.empty((n,) + tuple(t.shape), dtype=t.dtype, device=dev)
+        big.copy_(t.unsqueeze(0).expand_as(big))
+        return big
+
+    latency = "latency-bound: under 3 MB a call, so the HBM fraction is not the figure of merit"
+    # greedy argmax, 1 x 202,048, three planted maxima
+    x1, _ = synth.workload_argmax_planted()
+    n1 = 640
+    c1 = copies(x1, n1)
+    ids1 = torch.empty(1, dtype=torch.int32, device=dev)
+    ws1 = B.workspace(B.SEL_OP_ARGMAX, 1, x1.shape[1], device=dev)
+    us = timed(lambda r: B.sel_argmax(c1[r], ids1, ws1), n1, n1)
+    record("argmax_1x202048", "greedy argmax, 1 x 202,048 fp32, 3 planted maxima", us, 1, x1.nbytes, latency)
+    del c1
+    # exact top-k, k = 84, 3 x 248,320 with a peaked head
+    x2, k2 = synth.workload_topk_peaked()
+    n2 = 180
+    c2 = copies(x2, n2)
+    tv2 = torch.empty(3, k2, device=dev)
+    ti2 = torch.empty(3, k2, dtype=torch.int32, device=dev)
+    ws2 = B.workspace(B.SEL_OP_TOPK, 3, x2.shape[1], k2, device=dev)
+    us = timed(lambda r: B.sel_topk(c2[r], k2, tv2, ti2, ws2), n2, n2)
+    record("topk84_3x248320", "exact top-k k = 84, 3 x 248,320 fp32, peaked head", us, 3, x2.nbytes, latency)
+    del c2
+    # filtered sampling, 64 x 202,048, T 0.7, top_k 40, top_p 0.9, min_p 0.05
+    x4, u4, pol = synth.workload_sample()
+    n4 = 11
+    c4 = copies(x4, n4)
+    ud4 = torch.from_numpy(u4).to(dev)
+    sid4 = torch.empty(64, dtype=torch.int32, device=dev)
+    sp4 = torch.empty(64, device=dev)
+    prm4 = B.SampleParams(pol.temperature, pol.top_k, pol.top_p, pol.min_p, B.SEL_ORDER_TEMP_FIRST)
+    ws4 = B.workspace(B.SEL_OP_SAMPLE, 64, x4.shape[1], pol.top_k, device=dev)
+    us = timed(lambda r: B.sel_sample(c4[r], prm4, ud4, sid4, sp4, ws4), n4, 10 * n4)
+    record("sample_64x202048", "sampling 64 x 202,048 fp32, T 0.7, top_k 40, top_p 0.9, min_p 0.05",
+           us, 64, x4.nbytes)
+    del c4
+    # speculative acceptance, 8 sequences x 8 drafts, V = 151,936, both rules
+    si = synth.workload_spec()
+    S5, K5 = si.draft_tokens.shape
+    V5 = si.target.shape[2]
+    n5 = 7
+    ct = copies(si.target, n5)
+    cd = copies(si.draft, n5)
+    tok5 = torch.from_numpy(si.draft_tokens.view(np.int32)).to(dev)
+    ua5 = torch.from_numpy(si.u_acc).to(dev)
+    uf5 = torch.from_numpy(si.u_fin).to(dev)
+    acc5 = torch.empty(S5, dtype=torch.int32, device=dev)
+    emi5 = torch.empty(S5, K5 + 1, dtype=torch.int32, device=dev)
+    ws5 = B.workspace(B.SEL_OP_SPEC, S5, V5, K5, device=dev)
+    rej = B.SpecParams(si.temperature, B.SPEC_MODE_REJECTION)
+    arg = B.SpecParams(si.temperature, B.SPEC_MODE_ARGMAX)
+    row5 = V5 * 4
+    us = timed(lambda r: B.spec_accept(ct[r], cd[r], tok5, rej, ua5, uf5, acc5, emi5, ws5), n5, 10 * n5)
+    n_acc = B.ids_to_numpy(acc5)
+    resid = int(sum(2 if a < K5 else 1 for a in n_acc))
+    record("spec_rejection_8x8", "speculative acceptance, rejection rule, 8 x 8 drafts, V = 151,936",
+           us, S5, (S5 * (2 * K5 + 1) + resid) * row5)
+    us = timed(lambda r: B.spec_accept(ct[r], None, tok5, arg, None, None, acc5, emi5, ws5), n5, 10 * n5)
+    record("spec_argmax_8x8", "speculative acceptance, argmax rule, 8 x 8 drafts, V = 151,936",
+           us, S5, S5 * (K5 + 1) * row5)
+    del ct, cd
+    torch.cuda.synchronize()
     return out
 
 
