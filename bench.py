@@ -365,6 +365,20 @@ def gpu_arm(args, rank, world, local_rank):
     return line
 
 
+def full_row_search_rows() -> int:
+    """Rows of the verify batch whose top-p nucleus (at the step's T and
+    top_p, over the whole row) holds more than the 64 candidates, so that the
+    cut search decides them (computed in double on the host)."""
+    from sampling_row_fp32_gb300 import synth
+    x, _ = synth.workload_verify_batch(ROWS, V)
+    z = x.astype(np.float64) / POLICY["temperature"]
+    z -= z.max(axis=1, keepdims=True)
+    w = np.exp(z)
+    w /= w.sum(axis=1, keepdims=True)
+    c = np.cumsum(-np.sort(-w, axis=1), axis=1)
+    return int((((c < POLICY["top_p"]).sum(axis=1) + 1) > 64).sum())
+
+
 def extra_ops(B, dev, xs, drafts, tok, stream):
     """The calls beyond the step, on the same batch and copy rotation, each
     timed over OP_REPS graph-replayed launches: the EOG-excluding argmax (8
@@ -420,9 +434,11 @@ def extra_ops(B, dev, xs, drafts, tok, stream):
     ws_full = B.workspace(B.SEL_OP_SAMPLE, ROWS, V, 0, device=dev)
     calls = {
         "argmax_excluding_8": (lambda r: B.sel_argmax_excluding(xs[r % N_COPIES], exd, ids, ws_a), ROWS * ROW_BYTES),
-        # full-row sampling reads every row twice (candidates and sums, then the draw)
+        # full-row sampling reads every row twice (candidates and sums, then
+        # the draw); a row whose nucleus runs past the 64 candidates is read
+        # four more times by the cut search (from L2, mostly): counted too
         "sample_full_row": (lambda r: B.sel_sample(xs[r % N_COPIES], prm_full, uu, sid, spr, ws_full),
-                            2 * ROWS * ROW_BYTES),
+                            (2 * ROWS + 4 * full_row_search_rows()) * ROW_BYTES),
         "sample_nsigma1_typical08": (lambda r: B.sel_sample(xs[r % N_COPIES], prm_f, uu, sid, spr, ws_f),
                                      ROWS * ROW_BYTES),
         # the step's policy with the filters on the untempered distribution
@@ -457,6 +473,11 @@ def extra_ops(B, dev, xs, drafts, tok, stream):
         us = a.elapsed_time(b) * 1e3 / OP_REPS
         gbs = nbytes / (us * 1e-6) / 1e9
         out[name] = dict({"us": round(us, 3), "bytes": nbytes, "gbs": round(gbs, 1)}, **fracs(gbs, peak))
+    out["sample_full_row"]["cut_search_rows"] = full_row_search_rows()
+    with torch.cuda.stream(stream):
+        B.sel_sample(xs[0], prm_full, uu, sid, spr, ws_full)
+    torch.cuda.synchronize()
+    out["sample_full_row"]["failed_rows"] = int((B.ids_to_numpy(sid) == 0xFFFFFFFF).sum())
     return out
 
 

@@ -41,6 +41,8 @@
 //     the row for the draw (see full_row_plan).
 #include <cfloat>
 
+#include <cooperative_groups.h>
+
 #include "sel_plan.h"
 #include "sel_units.cuh"
 
@@ -123,8 +125,11 @@ struct alignas(16) FullRow {
     unsigned long long key_lo, key_hi;
     float M;         // the row's maximum logit
     float u;         // the row's uniform
-    uint32_t valid;  // 0: the row fails closed
+    uint32_t valid;  // 0: the row fails closed; 1: decided; 2: top-p cut to be found over the row
     uint32_t pad;
+    float c_floor;   // (valid 2) the candidates C are the ids with x >= c_floor (top-n-sigma; -inf: all)
+    float mp_floor;  // (valid 2) min-p keeps x >= mp_floor (-inf: off)
+    uint32_t pad2, pad3;
 };
 
 struct SampleArgs {
@@ -154,6 +159,7 @@ struct TopkArgs {
     FF* draw_sums;           // [rows][draw_chunks]
     uint32_t draw_chunks;
     float full_cf;           // log2(e) / T of the filters (T = 1 when temperature comes last)
+    float cut_scale;         // 2^S: a filter weight (at most 1) as an integer mass (full-row cut search)
     float draw_c;            // log2(e) / T of the draw
     uint64_t* lists;         // [rows][stride][list_len(k)]
     uint32_t stride, list_len;
@@ -1122,6 +1128,7 @@ __device__ void full_row_plan(const uint64_t* sorted, float* scratch, uint32_t n
     out.M = n > 0 ? key2f(cand_key(sorted[0])) : 0.0f;
     bool resolved = !nonfinite && out.u >= 0.0f && out.u < 1.0f && n > 0 && Z > 0.0;
     bool beyond_err = false;
+    bool search = false;  // a top-p cut left to the cut search
     if (resolved) {
         const float M = out.M;
         const bool temp_last = sa.order == SEL_ORDER_TEMP_LAST;
@@ -1171,7 +1178,10 @@ __device__ void full_row_plan(const uint64_t* sorted, float* scratch, uint32_t n
         }
         const bool typical = sa.typical_p > 0.0f && sa.typical_p < 1.0f;
         const bool topp = sa.top_p < 1.0f;
-        if ((typical || topp) && !known) resolved = false;
+        // a top-p cut past the candidates is found over the whole row by the
+        // cut search (full_cut_kernel); a typical window past them is not
+        if (!known && typical) resolved = false;
+        else if (!known && topp) search = true;
         uint32_t lo = 0, hi = nc;
         double ZW = ZC;
         if (resolved && typical && (nc > 1 || beyond)) {
@@ -1201,7 +1211,7 @@ __device__ void full_row_plan(const uint64_t* sorted, float* scratch, uint32_t n
             }
         }
         uint32_t end = hi;
-        if (resolved && topp) {
+        if (resolved && !search && topp) {
             // the shortest prefix of the window whose mass reaches top_p
             const double need = static_cast<double>(sa.top_p) * ZW;
             double carry = 0.0;
@@ -1223,7 +1233,7 @@ __device__ void full_row_plan(const uint64_t* sorted, float* scratch, uint32_t n
                 end = found;
                 beyond = false;
             } else if (beyond) {
-                resolved = false;  // the nucleus runs past the candidates
+                search = true;  // the nucleus runs past the candidates
             } else {
                 end = hi;  // rounding kept the total below top_p
             }
@@ -1232,8 +1242,8 @@ __device__ void full_row_plan(const uint64_t* sorted, float* scratch, uint32_t n
         if (resolved && sa.min_p > 0.0f) {
             // P_j >= min_p * P_max: wf_j >= min_p * wf_lo
             thr_mp = static_cast<double>(M) + static_cast<double>(Tf) * log(static_cast<double>(sa.min_p));
-            if (beyond && static_cast<double>(xv(n - 1)) < thr_mp) beyond = false;
-            if (!beyond) {
+            if (!search && beyond && static_cast<double>(xv(n - 1)) < thr_mp) beyond = false;
+            if (!search && !beyond) {
                 const float floor_w = sa.min_p * wf[lo];
                 uint32_t keep = lo + 1;
                 for (uint32_t b = lo; b < end; b += 32) {
@@ -1244,7 +1254,19 @@ __device__ void full_row_plan(const uint64_t* sorted, float* scratch, uint32_t n
                 end = keep;
             }
         }
-        if (resolved) {
+        // a value threshold as the smallest float at or above it
+        auto floor_f = [](double thr) {
+            if (!(thr > -INFINITY)) return -INFINITY;
+            float f = static_cast<float>(thr);
+            if (static_cast<double>(f) < thr) f = nextafterf(f, INFINITY);
+            return f;
+        };
+        if (resolved && search) {
+            out.key_hi = ~0ull;
+            out.key_lo = 1ull;
+            out.c_floor = floor_f(thr_ns);
+            out.mp_floor = floor_f(thr_mp);
+        } else if (resolved) {
             if (!beyond) {
                 out.key_hi = sorted[lo];
                 out.key_lo = sorted[end - 1];
@@ -1263,7 +1285,7 @@ __device__ void full_row_plan(const uint64_t* sorted, float* scratch, uint32_t n
             beyond_err = !nonfinite && out.u >= 0.0f && out.u < 1.0f;
         }
     }
-    out.valid = resolved ? 1u : 0u;
+    out.valid = resolved ? (search ? 2u : 1u) : 0u;
     if (lane == 0) {
         a.full_rows[row] = out;
         if (beyond_err) atomicOr(a.err, kErrBeyond);
@@ -1301,7 +1323,7 @@ __global__ void __launch_bounds__(kNT, 8) full_draw_sum_kernel(TopkArgs a) {
     const uint32_t row = blockIdx.x / a.draw_chunks;
     const uint32_t chunk = blockIdx.x - row * a.draw_chunks;
     const FullRow fr = a.full_rows[row];
-    if (!fr.valid) return;
+    if (fr.valid != 1u) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t V = a.V, lo = chunk * kDrawIds, hi = min(V, lo + kDrawIds);
     const Members member(fr);
@@ -1359,7 +1381,7 @@ __global__ void __launch_bounds__(kNT) full_draw_find_kernel(TopkArgs a) {
     const uint32_t row = blockIdx.x;
     const FullRow fr = a.full_rows[row];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (!fr.valid) {
+    if (fr.valid != 1u) {
         if (tid == 0) { a.out_ids[row] = SEL_INVALID_ID; a.sa.out_probs[row] = __uint_as_float(0x7fc00000u); }
         return;
     }
@@ -1511,6 +1533,316 @@ __global__ void __launch_bounds__(kNT) full_draw_find_kernel(TopkArgs a) {
         a.out_ids[row] = id;
         a.sa.out_probs[row] = weight(x[id], id) / total;
     }
+}
+
+// Full-row sampling, the cut search. A top-p cut that lies past the row's
+// kFullCand most probable ids (a flat row: a large nucleus) is found over
+// the whole row instead of failing the row closed. The survivors are the
+// shortest prefix of the candidates C, in (value desc, id asc) order, whose
+// filter mass exp((x - M) / Tf) reaches top_p of C's mass (C: every id, or
+// the ids at or above the top-n-sigma floor). The cut is a candidate key
+// c* = key(x) << 32 | ~id, found by a radix select over the 32-bit value key
+// weighted by mass: four passes, one 8-bit digit each from the top, each
+// passing over the row (from L2 after the first) with a histogram of the
+// mass under the digits found so far. Masses are integers, w * 2^S rounded
+// (S = cut_scale's exponent, so that V * 2^S < 2^63): integer sums do not
+// depend on their order, which keeps the cut independent of scheduling.
+// Equal values at the cut weigh the same, so the number of them that the
+// prefix takes follows from the masses; when it takes only some of them,
+// one more pass finds the last of those in id order (ties go to lower ids,
+// as everywhere). min-p then keeps x >= mp_floor.
+//
+// One thread-block cluster of kCutCL blocks per row (rows whose plan is
+// already decided return at once): block b of the cluster takes a
+// contiguous segment of the row; each warp keeps its own histogram in
+// shared memory (lanes that share a digit add their masses first), the
+// block sums its warps', and block 0 of the cluster reads all the blocks'
+// histograms through distributed shared memory, picks the digit and leaves
+// the decision in its shared memory for the others. Cluster barriers order
+// the steps; no block waits on a flag.
+constexpr uint32_t kCutCL = 8;     // blocks per row (one cluster)
+constexpr int kCutNT = 512;
+constexpr int kCutWarps = kCutNT / 32;
+// A block's segment of the row is staged in shared memory once when it fits
+// (V up to about 390k); longer rows are read from global memory each pass.
+constexpr uint32_t kCutStageMax = 190u * 1024u;
+
+struct CutDecision {
+    unsigned long long above;  // mass of C above the prefix range (keys greater than the prefix's)
+    unsigned long long hd;     // mass of the chosen digit's bucket
+    double need;               // top_p times C's mass
+    uint32_t digit;
+    uint32_t ok;               // 0: no crossing was found (the row fails closed)
+};
+
+struct alignas(16) CutShared {
+    unsigned long long wh[kCutWarps][256];  // per-warp mass histograms
+    unsigned long long bh[256];             // the block's histogram
+    CutDecision dec;                        // block 0's decision of the pass
+    uint32_t warp_cnt[kCutWarps];
+    uint32_t tie_cnt;                       // ids at the cut value in this block's segment
+    uint32_t found_id;
+    int found;
+};
+
+__device__ __forceinline__ unsigned long long shfl_down_u64(unsigned long long v, int o) {
+    const uint32_t lo = __shfl_down_sync(kFull, static_cast<uint32_t>(v), o);
+    const uint32_t hi = __shfl_down_sync(kFull, static_cast<uint32_t>(v >> 32), o);
+    return (static_cast<unsigned long long>(hi) << 32) | lo;
+}
+
+template <bool kVec, bool kStaged>
+__global__ void __launch_bounds__(kCutNT, 1) full_cut_kernel(TopkArgs a) {
+    __shared__ CutShared sh;
+    extern __shared__ float4 seg4[];  // kStaged: the block's segment, quad by quad
+    namespace cg = cooperative_groups;
+    cg::cluster_group cl = cg::this_cluster();
+    pdl_wait();
+    pdl_trigger();
+    const uint32_t row = blockIdx.x / kCutCL;
+    const FullRow fr = a.full_rows[row];
+    if (fr.valid != 2u) return;  // every block of the cluster reads the same plan
+    const uint32_t rank = cl.block_rank();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t V = a.V;
+    const float* x = a.logits + static_cast<size_t>(row) * V;
+    const uint32_t seg = ((V + kCutCL - 1u) / kCutCL + 3u) & ~3u;
+    const uint32_t lo = min(V, rank * seg), hi = min(V, lo + seg);
+    const uint32_t key_floor = fr.c_floor > -INFINITY ? f2key(fr.c_floor) : 0u;
+    const float M = fr.M, cf = a.full_cf, scale = a.cut_scale;
+    const float top_p = a.sa.top_p;
+    auto mass = [&](float v) { return __float2ull_rn(ex2_approx((v - M) * cf) * scale); };
+    if (kStaged) {
+        // every load is issued before the stores that wait for it
+#pragma unroll 8
+        for (uint32_t e = lo + 4u * static_cast<uint32_t>(tid); e < hi; e += 4u * kCutNT)
+            seg4[(e - lo) >> 2] = ld_quad<kVec>(x, e, hi, -INFINITY);
+        __syncthreads();
+    }
+    // quad e .. e + 3 of the segment (-inf at or past hi)
+    auto quad = [&](uint32_t e) {
+        if (kStaged) {
+            const float4 q = seg4[(e - lo) >> 2];
+            if (kVec || e + 4u <= hi) return q;
+            return make_float4(q.x, e + 1u < hi ? q.y : -INFINITY, e + 2u < hi ? q.z : -INFINITY, -INFINITY);
+        }
+        return ld_quad<kVec>(x, e, hi, -INFINITY);
+    };
+
+    uint32_t prefix = 0, pmask = 0;
+    unsigned long long above = 0, hd = 0;
+    double need = 0.0;
+    uint32_t ok = 1;
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        for (int i = lane; i < 256; i += 32) sh.wh[warp][i] = 0ull;
+        __syncwarp();
+        // every thread runs the same number of iterations: the warp-wide
+        // votes below need all 32 lanes
+        // Lanes with the same digit add their masses (split in two 22-bit
+        // halves so the 32-bit sums cannot overflow), then one lane of each
+        // digit adds them to the warp's histogram. A thread first merges its
+        // four elements when they share a digit (the usual case), so a warp
+        // mostly needs one round per quad; it needs none when no element of
+        // the warp's quads lies under the prefix (most of passes 2-4).
+        auto add_round = [&](uint32_t d, unsigned long long w) {
+            const uint32_t live = __ballot_sync(kFull, d < 256u);
+            if (!live) return;
+            const int first = __ffs(live) - 1;
+            const uint32_t d0 = __shfl_sync(kFull, d, first);
+            uint32_t peers = kFull;
+            int leader = first;
+            if (!__all_sync(kFull, d == d0 || d == 256u)) {
+                peers = __match_any_sync(kFull, d);
+                leader = __ffs(peers) - 1;
+            }
+            const uint32_t whi = __reduce_add_sync(peers, static_cast<uint32_t>(w >> 22));
+            const uint32_t wlo = __reduce_add_sync(peers, static_cast<uint32_t>(w & 0x3FFFFFull));
+            if (d < 256u && lane == leader) sh.wh[warp][d] += (static_cast<unsigned long long>(whi) << 22) + wlo;
+        };
+        // every thread runs the same number of iterations: the warp-wide
+        // votes need all 32 lanes
+        for (uint32_t base = lo; base < hi; base += 4u * kCutNT) {
+            const uint32_t e = base + 4u * static_cast<uint32_t>(tid);
+            const float4 q = e < hi ? quad(e) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            const float f[4] = {q.x, q.y, q.z, q.w};
+            uint32_t d[4];
+            unsigned long long w[4];
+            uint32_t dq = 256u;
+            bool same = true;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t key = f2key(f[j]);
+                d[j] = 256u;
+                w[j] = 0ull;
+                if (e + j < hi && key >= key_floor && (key & pmask) == prefix) {
+                    w[j] = mass(f[j]);
+                    if (w[j] != 0ull) d[j] = (key >> shift) & 255u;
+                }
+                if (d[j] < 256u) {
+                    same &= dq == 256u || dq == d[j];
+                    dq = d[j];
+                }
+            }
+            if (!__any_sync(kFull, dq < 256u)) continue;
+            if (__all_sync(kFull, same)) {
+                add_round(dq, (w[0] + w[1]) + (w[2] + w[3]));
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) add_round(d[j], w[j]);
+            }
+        }
+        __syncthreads();
+        if (tid < 256) {
+            unsigned long long sum = 0ull;
+#pragma unroll
+            for (int w = 0; w < kCutWarps; ++w) sum += sh.wh[w][tid];
+            sh.bh[tid] = sum;
+        }
+        cl.sync();  // every block's histogram is complete
+        if (rank == 0 && warp == 0) {
+            // the cluster's histogram; lane l holds buckets 8 l .. 8 l + 7
+            unsigned long long h[8] = {0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull};
+            for (uint32_t b = 0; b < kCutCL; ++b) {
+                const unsigned long long* rb = cl.map_shared_rank(sh.bh, b);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) h[i] += rb[8 * lane + i];
+            }
+            unsigned long long T = 0ull;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) T += h[i];
+            // U: mass of buckets 8 l and up (suffix over the lanes)
+            unsigned long long U = T;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long v = shfl_down_u64(U, o);
+                if (lane + o < 32) U += v;
+            }
+            if (pass == 0) need = static_cast<double>(top_p) * static_cast<double>(shfl64(U, 0));  // C's mass
+            // the lane whose buckets hold the crossing: the cumulative mass
+            // from the top reaches need within them
+            const unsigned long long above_l = above + (U - T);
+            const bool cross = static_cast<double>(above + U) >= need && static_cast<double>(above_l) < need;
+            const uint32_t who = __ballot_sync(kFull, cross);
+            if (who == 0u) {
+                if (lane == 0) sh.dec = CutDecision{above, 0ull, need, 0u, 0u};
+            } else if (lane == __ffs(who) - 1) {
+                unsigned long long acc = above_l, hs = 0ull;
+                int ds = 0;
+                for (int i = 7; i >= 0; --i) {
+                    if (static_cast<double>(acc + h[i]) >= need) {
+                        ds = i;
+                        hs = h[i];
+                        break;
+                    }
+                    acc += h[i];
+                }
+                sh.dec = CutDecision{acc, hs, need, 8u * static_cast<uint32_t>(lane) + static_cast<uint32_t>(ds), 1u};
+            }
+        }
+        cl.sync();  // block 0's decision is ready
+        const CutDecision dec = *cl.map_shared_rank(&sh.dec, 0u);
+        prefix |= dec.digit << shift;
+        pmask |= 255u << shift;
+        above = dec.above;
+        hd = dec.hd;
+        need = dec.need;
+        ok &= dec.ok;
+    }
+    // The cut value's key is `prefix`; each id there weighs w1, and the
+    // prefix of C takes t of its nt ids (the lowest).
+    const unsigned long long w1 = mass(key2f(prefix));
+    const uint32_t nt = (ok && w1 != 0ull) ? static_cast<uint32_t>(hd / w1) : 0u;
+    uint32_t t = 0;
+    if (nt != 0u) {
+        const double tn = ceil((need - static_cast<double>(above)) / static_cast<double>(w1));
+        t = tn < 1.0 ? 1u : (tn >= static_cast<double>(nt) ? nt : static_cast<uint32_t>(tn));
+    }
+    const unsigned long long mp =
+        fr.mp_floor > -INFINITY ? static_cast<unsigned long long>(f2key(fr.mp_floor)) << 32 : 0ull;
+    auto write_plan = [&](bool good, unsigned long long cstar) {
+        FullRow out = fr;
+        out.key_hi = ~0ull;
+        out.key_lo = cstar > mp ? cstar : mp;
+        out.valid = good ? 1u : 0u;
+        a.full_rows[row] = out;
+        if (!good) atomicOr(a.err, kErrBeyond);
+    };
+    if (nt == 0u || t >= nt) {
+        // every id at the cut value is kept (or no cut was found)
+        if (rank == 0 && tid == 0) write_plan(nt != 0u, static_cast<unsigned long long>(prefix) << 32);
+        cl.sync();  // no block leaves while block 0's shared memory may still be read
+        return;
+    }
+    // Only the t lowest ids at the cut value are kept: count them per block,
+    // then the block holding the t-th finds it in id order.
+    uint32_t mine = 0;
+    for (uint32_t base = lo; base < hi; base += 4u * kCutNT) {
+        const uint32_t e = base + 4u * static_cast<uint32_t>(tid);
+        const float4 q = e < hi ? quad(e) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        const float f[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mine += (e + j < hi && f2key(f[j]) == prefix) ? 1u : 0u;
+    }
+    mine = __reduce_add_sync(kFull, mine);
+    if (lane == 0) sh.warp_cnt[warp] = mine;
+    __syncthreads();
+    if (tid == 0) {
+        uint32_t c = 0;
+        for (int w = 0; w < kCutWarps; ++w) c += sh.warp_cnt[w];
+        sh.tie_cnt = c;
+        sh.found = 0;
+    }
+    cl.sync();
+    uint32_t before = 0, bstar = kCutCL, tb = 0;
+    for (uint32_t b = 0; b < kCutCL; ++b) {
+        const uint32_t c = *cl.map_shared_rank(&sh.tie_cnt, b);
+        if (bstar == kCutCL && before + c >= t) {
+            bstar = b;
+            tb = t - before;
+        }
+        before += c;
+    }
+    if (rank == bstar) {
+        for (uint32_t tile = lo; tile < hi; tile += 4u * kCutNT) {
+            const uint32_t e = tile + 4u * static_cast<uint32_t>(tid);
+            const float4 q = e < hi ? quad(e) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            const float f[4] = {q.x, q.y, q.z, q.w};
+            uint32_t flags = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) flags |= (e + j < hi && f2key(f[j]) == prefix) ? (1u << j) : 0u;
+            const uint32_t cnt = __popc(flags);
+            uint32_t incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t v = __shfl_up_sync(kFull, incl, o);
+                if (lane >= o) incl += v;
+            }
+            if (lane == 31) sh.warp_cnt[warp] = incl;
+            __syncthreads();
+            uint32_t woff = 0, total = 0;
+            for (int w = 0; w < kCutWarps; ++w) {
+                const uint32_t c = sh.warp_cnt[w];
+                if (w < warp) woff += c;
+                total += c;
+            }
+            const uint32_t excl = woff + incl - cnt;
+            if (cnt != 0u && excl < tb && tb <= excl + cnt) {
+                uint32_t m = flags;
+                for (uint32_t r = tb - excl; r > 1u; --r) m &= m - 1u;
+                sh.found_id = e + static_cast<uint32_t>(__ffs(m) - 1);
+                sh.found = 1;
+            }
+            __syncthreads();
+            if (sh.found) break;
+            tb -= total;
+            __syncthreads();  // the counts are read before the next tile's
+        }
+        if (tid == 0)
+            write_plan(sh.found != 0,
+                       (static_cast<unsigned long long>(prefix) << 32) | static_cast<uint32_t>(~sh.found_id));
+    }
+    cl.sync();  // no block leaves while its shared memory may still be read
 }
 
 template <bool kSample, bool kFull>
@@ -1750,6 +2082,13 @@ sel_status launch_topk(const float* d_logits, uint32_t rows, uint32_t V, uint32_
     a.full_rows = reinterpret_cast<FullRow*>(ws + l.full_rows);
     a.draw_sums = reinterpret_cast<FF*>(ws + l.draw_sums);
     a.draw_chunks = ceil_div(V, kDrawIds);
+    {
+        // integer masses: V * 2^S stays below 2^62, and S <= 44 keeps a
+        // warp's 32 half-masses (22 bits each) within 32-bit sums
+        int lg = 0;
+        while ((1ull << lg) < V) ++lg;
+        a.cut_scale = ldexpf(1.0f, min(44, 62 - lg));
+    }
     if (kSample && sa.temperature > 0.0f) {
         const double Tf = sa.order == SEL_ORDER_TEMP_LAST ? 1.0 : static_cast<double>(sa.temperature);
         a.full_cf = static_cast<float>(1.4426950408889634 / Tf);
@@ -1796,6 +2135,22 @@ sel_status launch_topk(const float* d_logits, uint32_t rows, uint32_t V, uint32_
                    : launch_pdl(topk_finish_kernel<kSample, false>, dim3(rows), dim3(kNT), 0, stream, a);
     if (e != cudaSuccess) return SEL_ECUDA;
     if (kSample && full_row) {
+        // the cut search for rows whose top-p cut lies past the candidates
+        // (one thread-block cluster per row; decided rows return at once)
+        if (static_cast<uint64_t>(rows) * kCutCL > 0x7fffffffull) return SEL_EUNSUPPORTED;
+        const size_t seg_bytes = static_cast<size_t>(((V + kCutCL - 1u) / kCutCL + 3u) & ~3u) * 4u;
+        const bool staged = seg_bytes <= kCutStageMax;
+        static const bool cut_attr_ok = set_dynamic_smem(full_cut_kernel<true, true>, kCutStageMax) &&
+                                        set_dynamic_smem(full_cut_kernel<false, true>, kCutStageMax);
+        if (!cut_attr_ok) return SEL_ECUDA;
+        const dim3 cg(rows * kCutCL), cb(kCutNT);
+        if (staged)
+            e = vec ? launch_pdl_cluster(full_cut_kernel<true, true>, cg, cb, kCutCL, seg_bytes, stream, a)
+                    : launch_pdl_cluster(full_cut_kernel<false, true>, cg, cb, kCutCL, seg_bytes, stream, a);
+        else
+            e = vec ? launch_pdl_cluster(full_cut_kernel<true, false>, cg, cb, kCutCL, 0, stream, a)
+                    : launch_pdl_cluster(full_cut_kernel<false, false>, cg, cb, kCutCL, 0, stream, a);
+        if (e != cudaSuccess) return SEL_ECUDA;
         // the draw over the survivors, in ascending id
         const uint64_t dblocks = static_cast<uint64_t>(rows) * a.draw_chunks;
         if (dblocks > 0x7fffffffull) return SEL_EUNSUPPORTED;

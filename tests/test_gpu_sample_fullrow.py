@@ -3,10 +3,13 @@ oracle. The filters act on softmax(x / T) over the whole vocabulary (the
 sampler chain of the Muser book, "Ch 21 -- Sampling, argmax, and grammar",
 21.1 and 21.7, without top-k); the draw walks the survivors in ascending id.
 
-Temperature alone, min-p and top-n-sigma are decided on every row. A top-p
-or locally typical cut is decided from the row's 64 most probable tokens;
-a row whose cut lies past them fails closed (0xFFFFFFFF, NaN) and raises
-error bit 8 -- checked here against the oracle's own nucleus sizes."""
+Temperature alone, min-p, top-n-sigma and top-p are decided on every row:
+a top-p cut inside the row's 64 most probable tokens is decided from them,
+one past them by the cut search over the whole row (a radix select on the
+value key weighted by probability mass, exact ties going to the lower ids).
+A locally typical cut is decided from the 64 candidates only; a row whose
+typical window runs past them fails closed (0xFFFFFFFF, NaN) and raises
+error bit 8."""
 import numpy as np
 import pytest
 import torch
@@ -90,21 +93,54 @@ def test_top_n_sigma(orc, nsig):
 
 
 def test_top_p_on_verify_batch(orc):
-    """49 x 248,320 Zipf/Gumbel rows at T 0.7, top_p 0.9: a row is decided
-    exactly when its nucleus fits the 64 candidates."""
+    """49 x 248,320 Zipf/Gumbel rows at T 0.7, top_p 0.9: the rows whose
+    nucleus fits the 64 candidates and the rows whose nucleus does not (the
+    cut search) are all decided."""
     x, _ = synth.workload_verify_batch()
     u = synth.uniforms(67, 49)
-    decided = nucleus_sizes(x, 0.7, 0.9) <= CAND
-    assert decided.mean() > 0.6
-    check(orc, x, u, 0.7, 0.9, 0.0, decided=decided)
+    sizes = nucleus_sizes(x, 0.7, 0.9)
+    assert (sizes > CAND).any() and (sizes <= CAND).mean() > 0.6
+    check(orc, x, u, 0.7, 0.9, 0.0, decided=np.ones(49, bool))
 
 
-@pytest.mark.parametrize("T,top_p", [(0.5, 0.9), (1.0, 0.5), (1.0, 0.95)])
-def test_top_p_decided_iff_nucleus_fits(orc, T, top_p):
-    x = synth.normal_rows(68, 40, 30_001, 4.0)
+@pytest.mark.parametrize("T,top_p", [(0.5, 0.9), (1.0, 0.5), (1.0, 0.95), (2.0, 0.3)])
+@pytest.mark.parametrize("misalign", [False, True])
+def test_top_p_past_the_candidates(orc, T, top_p, misalign):
+    """Flat rows (N(0, 1.5^2)): every nucleus holds hundreds to thousands
+    of tokens, so the cut search decides it; every row matches the oracle."""
+    x = synth.normal_rows(68, 40, 30_001, 1.5)
     u = synth.uniforms(69, 40)
-    decided = nucleus_sizes(x, T, top_p) <= CAND
-    check(orc, x, u, T, top_p, 0.0, decided=decided)
+    assert (nucleus_sizes(x, T, top_p) > CAND).mean() > 0.5
+    check(orc, x, u, T, top_p, 0.0, misalign=misalign, decided=np.ones(40, bool))
+
+
+@pytest.mark.parametrize("nsig,min_p,temp_last", [(2.0, 0.0, False), (0.0, 0.01, False), (1.5, 0.02, True),
+                                                  (0.0, 0.0, True)])
+def test_top_p_search_with_the_other_filters(orc, nsig, min_p, temp_last):
+    """The cut search under top-n-sigma (the candidates are the ids above
+    max - n sigma), followed by min-p, and in the temperature-last order."""
+    x = synth.normal_rows(76, 24, 50_000, 3.0)
+    u = synth.uniforms(77, 24)
+    check(orc, x, u, 1.3, 0.8, min_p, nsig=nsig, temp_last=temp_last, decided=np.ones(24, bool))
+
+
+@pytest.mark.parametrize("top_p", [0.3, 0.5, 0.77])
+def test_top_p_cut_inside_a_run_of_equal_logits(orc, top_p):
+    """Integer-valued rows: thousands of ids share each value, so the cut
+    falls inside a run of equal logits and takes its lowest ids only (the
+    tie order of the chain)."""
+    rng = np.random.default_rng(int(top_p * 100))
+    x = rng.integers(0, 6, size=(12, 20_000)).astype(np.float32)
+    u = synth.uniforms(78, 12)
+    check(orc, x, u, 1.0, top_p, 0.0, decided=np.ones(12, bool))
+
+
+def test_top_p_search_on_a_large_row(orc):
+    """One flat row of 2,000,003 logits (a ragged tail, eight segments of a
+    cluster that are not all equal)."""
+    x = synth.normal_rows(79, 2, 2_000_003, 5.0)
+    u = synth.uniforms(80, 2)
+    check(orc, x, u, 1.0, 0.9, 0.0, decided=np.ones(2, bool))
 
 
 def test_whole_chain_on_short_rows(orc):
