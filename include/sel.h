@@ -64,7 +64,7 @@ typedef enum sel_status {
 
 /* Operation codes for sel_workspace_bytes. */
 enum { SEL_OP_ARGMAX = 0, SEL_OP_TOPK = 1, SEL_OP_SAMPLE = 2, SEL_OP_SPEC = 3,
-       SEL_OP_SPEC_SAMPLER = 4, SEL_OP_SPEC_DIAG = 5 };
+       SEL_OP_SPEC_SAMPLER = 4, SEL_OP_SPEC_DIAG = 5, SEL_OP_SHARD_DRAW = 6 };
 
 /* Order of temperature and filters in sel_sample. */
 enum {
@@ -91,6 +91,7 @@ enum {
  *   op SEL_OP_SPEC_SAMPLER: rows = S * (K + 1) (target rows), V,
  *                     k = the policy's top_k
  *   op SEL_OP_SPEC_DIAG: rows = S, V, k = K
+ *   op SEL_OP_SHARD_DRAW: rows, V = the shard's slice width (k ignored)
  * The size depends only on these arguments, not on the device. Returns 0
  * when the arguments are invalid (the entry point would refuse them anyway).
  */
@@ -393,25 +394,147 @@ sel_status sel_merge_shards(const float *d_vals, const uint32_t *d_ids,
                             uint32_t *d_out_ids, cudaStream_t stream);
 
 /*
- * sel_sample_shards -- the sampling stage of sel_sample on gathered shard
- * lists. With the top-k filter first in the chain (Muser ch. 21, 21.7), the
- * rest of the chain needs only the top_k candidates (llama.cpp PR 49,
- * "Change"): the merged lists give exactly the candidates sel_sample finds
- * in the whole row, so the result (id, probability) is that of sel_sample
- * on the unsharded row with the same policy and uniforms.
+ * Per-shard row statistics: what a shard's slice adds to the whole row's
+ * softmax normaliser, mean log-weight and standard deviation, so that the
+ * filters that look at the whole row (top-n-sigma, and sampling with
+ * top_k == 0) can run on vocabulary shards. Written by sel_topk_stats, one
+ * record per row of the slice; the caller all-gathers them with the lists.
+ * With Tf the filter temperature (the policy's temperature, or 1 in the
+ * temperature-last order, or 1 for a greedy policy) and m the slice's
+ * largest logit:
+ */
+typedef struct sel_row_stats {
+    float max;      /* m: the slice's largest logit */
+    uint32_t flags; /* bit 0: the slice holds a NaN or +-Inf logit (the
+                       other fields are then meaningless) */
+    float x0;       /* shift of s1 and s2: the slice's first logit */
+    uint32_t n;     /* logits in the slice */
+    double s1;      /* sum over the slice of (x - x0) */
+    double s2;      /* sum over the slice of (x - x0)^2 */
+    double z;       /* sum of exp((x - m) / Tf) */
+    double h;       /* sum of exp((x - m) / Tf) * (x - m) / Tf; 0 unless the
+                       policy's typical_p filter is on */
+} sel_row_stats;    /* 48 bytes */
+
+/*
+ * sel_topk_stats -- sel_topk on a shard's slice plus that slice's
+ * sel_row_stats, from one read of the slice.
  *
- *   d_vals, d_ids, rows, G, k, h_offsets  as for sel_merge_shards; each
- *              shard list is sel_topk(slice, k) with k = p->top_k (any k
- *              when p->temperature == 0: greedy takes the top candidate)
- *   p, d_uniforms, d_out_ids, d_out_probs  as for sel_sample
- * Per-row errors as for sel_sample (0xFFFFFFFF, probability NaN).
+ *   d_logits, rows, V, k, d_out_vals, d_out_ids  as for sel_topk (V is the
+ *              slice's width; ids local to the slice)
+ *   p          the sampling policy (host pointer, read during the call):
+ *              fixes Tf and whether h is summed
+ *   d_stats    [rows] sel_row_stats, device
+ *   d_ws       workspace of sel_workspace_bytes(SEL_OP_TOPK, rows, V, k)
+ * A row with a nonfinite logit gets SEL_INVALID_ID ids (as sel_topk) and
+ * flags bit 0.
+ */
+sel_status sel_topk_stats(const float *d_logits, uint32_t rows, uint32_t V,
+                          uint32_t k, const sel_sample_params *p,
+                          float *d_out_vals, uint32_t *d_out_ids,
+                          sel_row_stats *d_stats, void *d_ws, size_t ws_bytes,
+                          cudaStream_t stream);
+
+/*
+ * The survivor set and draw of one row of full-row sampling on shards:
+ * written by sel_sample_shards, read by sel_shard_draw_mass and
+ * sel_shard_draw. Opaque; every rank holds the same copy when it ran
+ * sel_sample_shards on the same gathered inputs.
+ */
+typedef struct sel_shard_plan {
+    uint32_t opaque[12];
+} sel_shard_plan;   /* 48 bytes */
+
+/*
+ * sel_sample_shards -- the sampling chain of sel_sample over a row split
+ * into vocabulary shards, from the shards' gathered lists and statistics.
+ *
+ * With top_k > 0 the top-k filter comes first in the chain (Muser ch. 21,
+ * 21.7), so the rest of the chain needs only the top_k candidates (llama.cpp
+ * PR 49, "Change"): the merged lists give exactly the candidates sel_sample
+ * finds in the whole row, and the call writes (id, probability) directly.
+ * Top-n-sigma needs the whole row's standard deviation as well, merged here
+ * from the shards' (n, x0, s1, s2): pass d_stats.
+ *
+ * With top_k == 0 (full-row sampling) the call decides each row's survivor
+ * set from the merged 64 most probable candidates and the merged
+ * normaliser (sum of z rescaled to the row's maximum), as sel_sample does,
+ * and writes it to d_plan; the draw over the survivors, in ascending global
+ * id, then runs on the shards: sel_shard_draw_mass on every shard,
+ * an all-gather of the masses, sel_shard_draw on every shard, and an
+ * all-reduce of the shards' outputs (minimum of the ids, sum of the
+ * probabilities). A row whose top-p cut lies past the 64 candidates (the
+ * unsharded call finds it by a search over the row) and a row whose
+ * typical window runs past them fail closed in this form, with error bit 8
+ * raised by sel_shard_draw.
+ *
+ *   d_vals, d_ids  [rows][G][k], as for sel_merge_shards; each shard list is
+ *              sel_topk (or sel_topk_stats) of the slice with k = p->top_k,
+ *              or with k = min(64, smallest slice) when p->top_k == 0 (any
+ *              k when p->temperature == 0: greedy takes the top candidate)
+ *   d_stats    [rows][G] sel_row_stats from sel_topk_stats on each slice with
+ *              the same policy, or NULL when top_k > 0 and top-n-sigma is off
+ *   rows, G, k, h_offsets  as for sel_merge_shards
+ *   p, d_uniforms  as for sel_sample
+ *   d_out_ids, d_out_probs  [rows], as for sel_sample (top_k > 0 or greedy);
+ *              unused (may be NULL) when top_k == 0
+ *   d_plan     [rows] sel_shard_plan (top_k == 0; may be NULL otherwise)
+ * Per-row errors as for sel_sample (0xFFFFFFFF, probability NaN): a shard
+ * whose list or statistics report a nonfinite logit, a malformed list, or
+ * statistics whose n differs from the shard's width fail the row closed.
+ * Returns SEL_EINVAL when d_stats is NULL but top-n-sigma is on or
+ * top_k == 0, or d_plan is NULL with top_k == 0.
  */
 sel_status sel_sample_shards(const float *d_vals, const uint32_t *d_ids,
-                             uint32_t rows, uint32_t G, uint32_t k,
-                             const uint32_t *h_offsets,
+                             const sel_row_stats *d_stats, uint32_t rows,
+                             uint32_t G, uint32_t k, const uint32_t *h_offsets,
                              const sel_sample_params *p,
                              const float *d_uniforms, uint32_t *d_out_ids,
-                             float *d_out_probs, cudaStream_t stream);
+                             float *d_out_probs, sel_shard_plan *d_plan,
+                             cudaStream_t stream);
+
+/*
+ * sel_shard_draw_mass -- step 1 of the full-row draw on shards: each
+ * shard's mass of the row's survivors, sum of exp((x - max) / T) over the
+ * survivors in its slice (the row's maximum and T from the plan). Also
+ * leaves per-chunk sums in d_ws for sel_shard_draw.
+ *
+ *   d_logits   [rows][V] f32: this shard's slice (V its width)
+ *   offset     the slice's first global id (h_offsets[g])
+ *   d_plan     [rows] from sel_sample_shards
+ *   d_mass     [rows] f64, device: this shard's survivor mass (0 for a row
+ *              that fails closed)
+ *   d_ws       workspace of sel_workspace_bytes(SEL_OP_SHARD_DRAW, rows, V,
+ *              0), kept untouched until the matching sel_shard_draw
+ */
+sel_status sel_shard_draw_mass(const float *d_logits, uint32_t rows, uint32_t V,
+                               uint32_t offset, const sel_shard_plan *d_plan,
+                               double *d_mass, void *d_ws, size_t ws_bytes,
+                               cudaStream_t stream);
+
+/*
+ * sel_shard_draw -- step 2: with every shard's mass gathered, the draw
+ * u * total falls in one shard (shards in id order, a fixed-order scan);
+ * that shard walks its survivors in ascending id and writes the global id
+ * and its probability (weight / total). Every other shard writes
+ * SEL_OTHER_SHARD and probability 0, so an all-reduce (minimum of the ids,
+ * sum of the probabilities) over the shards gives the row's result on
+ * every rank. A row that fails closed gets SEL_INVALID_ID and NaN on every
+ * shard.
+ *
+ *   d_logits, rows, V, offset, d_plan  as for sel_shard_draw_mass
+ *   g, G       this shard's index and the number of shards
+ *   d_masses   [rows][G] f64: every shard's d_mass, gathered in shard order
+ *   d_out_ids, d_out_probs  [rows]
+ *   d_ws       the workspace of this shard's sel_shard_draw_mass call; its
+ *              first word collects error bit 8 (a cut past the candidates)
+ */
+#define SEL_OTHER_SHARD 0xFFFFFFFEu
+sel_status sel_shard_draw(const float *d_logits, uint32_t rows, uint32_t V,
+                          uint32_t offset, uint32_t g, uint32_t G,
+                          const sel_shard_plan *d_plan, const double *d_masses,
+                          uint32_t *d_out_ids, float *d_out_probs, void *d_ws,
+                          size_t ws_bytes, cudaStream_t stream);
 
 /* Static description of a status code. */
 const char *sel_status_string(sel_status status);

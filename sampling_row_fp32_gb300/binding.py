@@ -21,17 +21,23 @@ from . import build as _build
 SEL_OK, SEL_EINVAL, SEL_EWORKSPACE, SEL_ECUDA, SEL_EUNSUPPORTED = range(5)
 SEL_INVALID_ID = 0xFFFFFFFF
 SEL_MAX_K = 1024
-SEL_OP_ARGMAX, SEL_OP_TOPK, SEL_OP_SAMPLE, SEL_OP_SPEC, SEL_OP_SPEC_SAMPLER, SEL_OP_SPEC_DIAG = range(6)
+(SEL_OP_ARGMAX, SEL_OP_TOPK, SEL_OP_SAMPLE, SEL_OP_SPEC, SEL_OP_SPEC_SAMPLER, SEL_OP_SPEC_DIAG,
+ SEL_OP_SHARD_DRAW) = range(7)
 SEL_ORDER_TEMP_FIRST, SEL_ORDER_TEMP_LAST = 0, 1
 SPEC_MODE_REJECTION, SPEC_MODE_ARGMAX = 0, 1
 
 EXPORTED = ("sel_workspace_bytes", "sel_workspace_init", "sel_argmax", "sel_topk",
             "sel_sample", "spec_accept", "sel_status_string", "sel_argmax_noalloc",
             "sel_merge_shards", "sel_sample_shards", "sel_argmax_excluding",
-            "spec_accept_sampler", "spec_diagnostics")
+            "spec_accept_sampler", "spec_diagnostics", "sel_topk_stats", "sel_shard_draw_mass",
+            "sel_shard_draw")
 SEL_NOALLOC_SCRATCH_BYTES = 1 << 20
 SEL_MAX_SHARDS = 64
 SEL_MAX_EXCLUDED = 256
+SEL_OTHER_SHARD = 0xFFFFFFFE
+ROW_STATS_BYTES = 48   # struct sel_row_stats
+SHARD_PLAN_BYTES = 48  # struct sel_shard_plan
+FULL_ROW_CANDIDATES = 64
 
 
 class SelError(RuntimeError):
@@ -98,8 +104,15 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.sel_argmax_excluding.restype = ctypes.c_int
     lib.sel_merge_shards.argtypes = [_vp, _vp, _u32, _u32, _u32, _vp, _vp, _vp, _vp]
     lib.sel_merge_shards.restype = ctypes.c_int
-    lib.sel_sample_shards.argtypes = [_vp, _vp, _u32, _u32, _u32, _vp, ctypes.POINTER(SampleParams),
-                                      _vp, _vp, _vp, _vp]
+    lib.sel_sample_shards.argtypes = [_vp, _vp, _vp, _u32, _u32, _u32, _vp, ctypes.POINTER(SampleParams),
+                                      _vp, _vp, _vp, _vp, _vp]
+    lib.sel_topk_stats.argtypes = [_vp, _u32, _u32, _u32, ctypes.POINTER(SampleParams), _vp, _vp, _vp, _vp,
+                                   _sz, _vp]
+    lib.sel_topk_stats.restype = ctypes.c_int
+    lib.sel_shard_draw_mass.argtypes = [_vp, _u32, _u32, _u32, _vp, _vp, _vp, _sz, _vp]
+    lib.sel_shard_draw_mass.restype = ctypes.c_int
+    lib.sel_shard_draw.argtypes = [_vp, _u32, _u32, _u32, _u32, _u32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+    lib.sel_shard_draw.restype = ctypes.c_int
     lib.sel_sample_shards.restype = ctypes.c_int
     lib.sel_status_string.argtypes = [ctypes.c_int]
     lib.sel_status_string.restype = ctypes.c_char_p
@@ -271,8 +284,10 @@ def sel_merge_shards(vals, ids, offsets, out_vals, out_ids, stream=None) -> None
                                    _ptr(out_vals), _ptr(out_ids), _stream(stream)), "sel_merge_shards")
 
 
-def sel_sample_shards(vals, ids, offsets, params: SampleParams, uniforms, out_ids, out_probs,
-                      stream=None) -> None:
+def sel_sample_shards(vals, ids, offsets, params: SampleParams, uniforms, out_ids=None, out_probs=None,
+                      stats=None, plan=None, stream=None) -> None:
+    """vals/ids [rows, G, k] gathered lists; stats [rows, G, 48] uint8 gathered
+    sel_row_stats (top-n-sigma, top_k = 0); plan [rows, 48] uint8 (top_k = 0)."""
     _check_f32(vals, "vals")
     _check_f32(uniforms, "uniforms")
     _check_f32(out_probs, "out_probs")
@@ -281,10 +296,51 @@ def sel_sample_shards(vals, ids, offsets, params: SampleParams, uniforms, out_id
     rows, G, k = vals.shape
     if len(offsets) != G + 1:
         raise ValueError("offsets must hold G + 1 entries")
+    if stats is not None and tuple(stats.shape) != (rows, G, ROW_STATS_BYTES):
+        raise ValueError("stats must be [rows, G, 48] bytes")
+    if plan is not None and tuple(plan.shape) != (rows, SHARD_PLAN_BYTES):
+        raise ValueError("plan must be [rows, 48] bytes")
     off = _host_offsets(offsets)
-    _check(load().sel_sample_shards(_ptr(vals), _ptr(ids), rows, G, k, ctypes.cast(off, _vp),
+    _check(load().sel_sample_shards(_ptr(vals), _ptr(ids), _ptr(stats), rows, G, k, ctypes.cast(off, _vp),
                                     ctypes.byref(params), _ptr(uniforms), _ptr(out_ids),
-                                    _ptr(out_probs), _stream(stream)), "sel_sample_shards")
+                                    _ptr(out_probs), _ptr(plan), _stream(stream)), "sel_sample_shards")
+
+
+def sel_topk_stats(logits, k: int, params: SampleParams, out_vals, out_ids, stats, ws=None, stream=None) -> None:
+    """logits [rows, V] (a shard's slice) -> top k [rows, k] and stats [rows, 48] uint8."""
+    _check_f32(logits, "logits")
+    _check_f32(out_vals, "out_vals")
+    _check_ids(out_ids, "out_ids")
+    rows, V = logits.shape
+    if tuple(stats.shape) != (rows, ROW_STATS_BYTES):
+        raise ValueError("stats must be [rows, 48] bytes")
+    _check(load().sel_topk_stats(_ptr(logits), rows, V, k, ctypes.byref(params), _ptr(out_vals), _ptr(out_ids),
+                                 _ptr(stats), _ptr(ws), _nbytes(ws), _stream(stream)), "sel_topk_stats")
+
+
+def sel_shard_draw_mass(logits, offset: int, plan, mass, ws=None, stream=None) -> None:
+    """logits [rows, V] (a shard's slice), plan [rows, 48] -> mass [rows] float64."""
+    _check_f32(logits, "logits")
+    if mass.dtype != torch.float64:
+        raise ValueError("mass must be float64")
+    rows, V = logits.shape
+    _check(load().sel_shard_draw_mass(_ptr(logits), rows, V, int(offset), _ptr(plan), _ptr(mass), _ptr(ws),
+                                      _nbytes(ws), _stream(stream)), "sel_shard_draw_mass")
+
+
+def sel_shard_draw(logits, offset: int, g: int, G: int, plan, masses, out_ids, out_probs, ws=None,
+                   stream=None) -> None:
+    """logits [rows, V] (shard g's slice), masses [rows, G] float64 -> out_ids,
+    out_probs [rows] (SEL_OTHER_SHARD / 0 where the draw is another shard's)."""
+    _check_f32(logits, "logits")
+    _check_f32(out_probs, "out_probs")
+    _check_ids(out_ids, "out_ids")
+    if masses.dtype != torch.float64:
+        raise ValueError("masses must be float64")
+    rows, V = logits.shape
+    _check(load().sel_shard_draw(_ptr(logits), rows, V, int(offset), int(g), int(G), _ptr(plan), _ptr(masses),
+                                 _ptr(out_ids), _ptr(out_probs), _ptr(ws), _nbytes(ws), _stream(stream)),
+           "sel_shard_draw")
 
 
 # ---------------------------------------------------------------------------

@@ -119,18 +119,23 @@ struct alignas(16) TopkShared {
 };
 
 // Full-row sampling: the survivors of a row are the ids whose candidate
-// key c = (key(x) << 32 | ~id) lies in [key_lo, key_hi]; they are drawn in
-// ascending id with weights exp((x - M) / T).
+// key c = (key(x) << 32 | ~id) lies in [key_lo, key_hi] (global ids on
+// shards); they are drawn in ascending id with weights exp((x - M) / T).
+// On vocabulary shards this record is the row's plan that every shard
+// receives (48 bytes, the size of sel_shard_plan).
 struct alignas(16) FullRow {
     unsigned long long key_lo, key_hi;
     float M;         // the row's maximum logit
     float u;         // the row's uniform
     uint32_t valid;  // 0: the row fails closed; 1: decided; 2: top-p cut to be found over the row
-    uint32_t pad;
+    uint32_t flags;  // kPlanBeyond: failed closed because a cut lay past the candidates
     float c_floor;   // (valid 2) the candidates C are the ids with x >= c_floor (top-n-sigma; -inf: all)
     float mp_floor;  // (valid 2) min-p keeps x >= mp_floor (-inf: off)
-    uint32_t pad2, pad3;
+    float draw_c;    // log2(e) / T of the draw
+    uint32_t pad;
 };
+static_assert(sizeof(FullRow) == sizeof(sel_shard_plan), "a shard plan is a FullRow");
+constexpr uint32_t kPlanBeyond = 1u;
 
 struct SampleArgs {
     const float* uniforms;  // [rows]
@@ -153,6 +158,10 @@ struct TopkArgs {
     uint32_t* chunk_flags;   // [rows][stride]
     float* moments;          // [rows][stride][4]: sum (x - x_0), sum (x - x_0)^2 as float-float
     uint32_t want_moments;   // the row's standard deviation is needed (top-n-sigma)
+    sel_row_stats* stats_out;  // [rows]: the slice's statistics (sel_topk_stats), else null
+    const double* shard_masses;  // [rows][shard_G]: every shard's survivor mass (shard draw), else null
+    uint32_t shard_g, shard_G;   // this shard and the number of shards (shard draw)
+    uint32_t id_base;            // global id of the slice's first logit (0 unsharded)
     uint32_t full_row;       // full-row sampling (top_k = 0): chunk exponent sums and a survivor range
     float4* full_parts;      // [rows][stride]: chunk max m, sum 2^((x - m) c) as float-float, sum w (x - m) c
     FullRow* full_rows;      // [rows]
@@ -940,7 +949,7 @@ __global__ void __launch_bounds__(kNT, kSmall ? 6 : 5) topk_kernel(TopkArgs a) {
                     const float f[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const float arg = (f[j] - tmax) * c;
+                        const float arg = fmaxf((f[j] - tmax) * c, -256.0f);  // w is 0 below
                         const float w = ex2_approx(arg);
                         ts += w;
                         if (want_q) tq = __fmaf_rn(w, arg, tq);
@@ -956,7 +965,7 @@ __global__ void __launch_bounds__(kNT, kSmall ? 6 : 5) topk_kernel(TopkArgs a) {
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             if (o + j < n_real) {
-                                const float arg = (f[j] - tmax) * c;
+                                const float arg = fmaxf((f[j] - tmax) * c, -256.0f);  // w is 0 below
                                 const float w = ex2_approx(arg);
                                 ts += w;
                                 if (want_q) tq = __fmaf_rn(w, arg, tq);
@@ -967,8 +976,12 @@ __global__ void __launch_bounds__(kNT, kSmall ? 6 : 5) topk_kernel(TopkArgs a) {
             }
             const float shift = (tmax - mb) * c;
             const float scale = ex2_approx(shift);
-            fs = ts * scale;
-            fq = (tq + ts * shift) * scale;
+            // a thread whose own logits are all past the chunk's end (fill
+            // values: shift -inf) or far below the chunk maximum adds nothing
+            if (scale > 0.0f) {
+                fs = ts * scale;
+                fq = (tq + ts * shift) * scale;
+            }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -1261,6 +1274,12 @@ __device__ void full_row_plan(const uint64_t* sorted, float* scratch, uint32_t n
             if (static_cast<double>(f) < thr) f = nextafterf(f, INFINITY);
             return f;
         };
+        if (resolved && search && a.shard_G != 0u) {
+            // on shards the cut search is not run: the row fails closed
+            resolved = false;
+            search = false;
+            beyond_err = true;
+        }
         if (resolved && search) {
             out.key_hi = ~0ull;
             out.key_lo = 1ull;
@@ -1286,9 +1305,11 @@ __device__ void full_row_plan(const uint64_t* sorted, float* scratch, uint32_t n
         }
     }
     out.valid = resolved ? (search ? 2u : 1u) : 0u;
+    out.flags = beyond_err ? kPlanBeyond : 0u;
+    out.draw_c = a.draw_c;
     if (lane == 0) {
         a.full_rows[row] = out;
-        if (beyond_err) atomicOr(a.err, kErrBeyond);
+        if (beyond_err && a.err) atomicOr(a.err, kErrBeyond);
     }
 }
 
@@ -1314,7 +1335,8 @@ struct Members {
 };
 
 // Full-row draw, 1: block (row, chunk) sums the survivors' weights
-// 2^((x - M) c) (c = log2(e) / T) over its kDrawIds ids.
+// 2^((x - M) c) (c = log2(e) / T) over its kDrawIds ids. On a shard the
+// slice's ids are offset by id_base in the survivor test.
 template <bool kVec>
 __global__ void __launch_bounds__(kNT, 8) full_draw_sum_kernel(TopkArgs a) {
     __shared__ FF s_w[kWarps];
@@ -1326,10 +1348,11 @@ __global__ void __launch_bounds__(kNT, 8) full_draw_sum_kernel(TopkArgs a) {
     if (fr.valid != 1u) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t V = a.V, lo = chunk * kDrawIds, hi = min(V, lo + kDrawIds);
+    const uint32_t ib = a.id_base;
     const Members member(fr);
     // a chunk whose logits all lie below the survivors (the main launch's
-    // chunk maxima tell) holds none: it is not read
-    if (member.has_lo) {
+    // chunk maxima tell, when this call follows it) holds none: it is not read
+    if (member.has_lo && a.full_parts) {
         const uint32_t c0 = lo / a.chunk_elems, c1 = (hi - 1u) / a.chunk_elems;
         float mx = -INFINITY;
         for (uint32_t cc = c0; cc <= c1; ++cc)
@@ -1350,7 +1373,7 @@ __global__ void __launch_bounds__(kNT, 8) full_draw_sum_kernel(TopkArgs a) {
         const float f[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            if (e + j < hi && member(f[j], e + j)) sum += ex2_approx((f[j] - fr.M) * a.draw_c);
+            if (e + j < hi && member(f[j], e + j + ib)) sum += ex2_approx((f[j] - fr.M) * fr.draw_c);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
@@ -1363,10 +1386,32 @@ __global__ void __launch_bounds__(kNT, 8) full_draw_sum_kernel(TopkArgs a) {
     }
 }
 
+// Shard draw, the mass: one warp per row sums the row's chunk sums in chunk
+// order (0 for a row that fails closed).
+__global__ void __launch_bounds__(32) shard_mass_kernel(TopkArgs a, double* mass) {
+    pdl_wait();
+    pdl_trigger();
+    const uint32_t row = blockIdx.x;
+    const int lane = threadIdx.x;
+    if (a.full_rows[row].valid != 1u) {
+        if (lane == 0) mass[row] = 0.0;
+        return;
+    }
+    const FF* sums = a.draw_sums + static_cast<size_t>(row) * a.draw_chunks;
+    FF W{0.0f, 0.0f};
+    for (uint32_t c0 = 0; c0 < a.draw_chunks; c0 += 32) {
+        const uint32_t ci = c0 + lane;
+        W = ff_add(W, ff_warp_sum(ci < a.draw_chunks ? sums[ci] : FF{0.0f, 0.0f}));
+    }
+    if (lane == 0) mass[row] = static_cast<double>(W.hi) + static_cast<double>(W.lo);
+}
+
 // Full-row draw, 2: block r finds the chunk where u * total falls (a
 // fixed-order scan of the chunk sums), then, within it, the 1,024-id stripe,
 // the quad and the id, walking ids in ascending order; writes the id and its
-// probability weight / total.
+// probability weight / total. On a shard the total and the mass before this
+// slice come from every shard's mass (shards in id order); a shard that
+// the draw does not fall in writes SEL_OTHER_SHARD and probability 0.
 template <bool kVec>
 __global__ void __launch_bounds__(kNT) full_draw_find_kernel(TopkArgs a) {
     __shared__ FF s_r[kWarps];
@@ -1376,27 +1421,66 @@ __global__ void __launch_bounds__(kNT) full_draw_find_kernel(TopkArgs a) {
     __shared__ FF s_before, s_target, s_sbefore, s_total;
     __shared__ float s_stripe[kWarps][kDrawQ];
     __shared__ int s_istar;
+    __shared__ uint32_t s_other;
     pdl_wait();
     pdl_trigger();
     const uint32_t row = blockIdx.x;
     const FullRow fr = a.full_rows[row];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t ib = a.id_base;
     if (fr.valid != 1u) {
-        if (tid == 0) { a.out_ids[row] = SEL_INVALID_ID; a.sa.out_probs[row] = __uint_as_float(0x7fc00000u); }
+        if (tid == 0) {
+            a.out_ids[row] = SEL_INVALID_ID;
+            a.sa.out_probs[row] = __uint_as_float(0x7fc00000u);
+            if (a.shard_masses && (fr.valid == 2u || (fr.flags & kPlanBeyond))) atomicOr(a.err, kErrBeyond);
+        }
         return;
     }
     const uint32_t V = a.V, chunks = a.draw_chunks;
     const FF* sums = a.draw_sums + static_cast<size_t>(row) * chunks;
     if (warp == 0) {
-        FF W{0.0f, 0.0f};
-        for (uint32_t c0 = 0; c0 < chunks; c0 += 32) {
-            const uint32_t ci = c0 + lane;
-            W = ff_add(W, ff_warp_sum(ci < chunks ? sums[ci] : FF{0.0f, 0.0f}));
+        FF W{0.0f, 0.0f}, target, acc{0.0f, 0.0f};
+        bool other = false, fail = false;
+        if (a.shard_masses) {
+            // the shard the draw falls in: the first with mass whose
+            // inclusive prefix exceeds u * total (else the last with mass)
+            const double* ms = a.shard_masses + static_cast<size_t>(row) * a.shard_G;
+            double tot = 0.0;
+            for (uint32_t g = 0; g < a.shard_G; ++g) tot += ms[g];
+            const double tg = static_cast<double>(fr.u) * tot;
+            double run = 0.0, before_g = 0.0, before_last = 0.0;
+            uint32_t gstar = a.shard_G, glast = a.shard_G;
+            for (uint32_t g = 0; g < a.shard_G; ++g) {
+                const double m = ms[g];
+                if (m > 0.0) {
+                    glast = g;
+                    before_last = run;
+                    if (gstar == a.shard_G && tg < run + m) {
+                        gstar = g;
+                        before_g = run;
+                    }
+                }
+                run += m;
+            }
+            if (gstar == a.shard_G) {
+                gstar = glast;
+                before_g = before_last;
+            }
+            other = gstar != a.shard_g;
+            fail = !(tot > 0.0);
+            W = ff_from_double(tot);
+            target = ff_from_double(tg);
+            acc = ff_from_double(before_g);
+        } else {
+            for (uint32_t c0 = 0; c0 < chunks; c0 += 32) {
+                const uint32_t ci = c0 + lane;
+                W = ff_add(W, ff_warp_sum(ci < chunks ? sums[ci] : FF{0.0f, 0.0f}));
+            }
+            target = ff_mul_f(W, fr.u);
         }
-        const FF target = ff_mul_f(W, fr.u);
         uint32_t cstar = chunks, last_pos_chunk = 0;
-        FF before{0.0f, 0.0f}, acc{0.0f, 0.0f}, before_last{0.0f, 0.0f};
-        for (uint32_t c0 = 0; c0 < chunks && cstar == chunks; c0 += 32) {
+        FF before = acc, before_last = acc;
+        for (uint32_t c0 = 0; c0 < chunks && cstar == chunks && !other && !fail; c0 += 32) {
             const uint32_t ci = c0 + lane;
             const FF t = ci < chunks ? sums[ci] : FF{0.0f, 0.0f};
             const FF incl = ff_add(acc, ff_warp_scan(t));
@@ -1426,9 +1510,17 @@ __global__ void __launch_bounds__(kNT) full_draw_find_kernel(TopkArgs a) {
             s_target = target;
             s_total = W;
             s_lastpos = -1;
+            s_other = fail ? 2u : (other ? 1u : 0u);
         }
     }
     __syncthreads();
+    if (s_other) {
+        if (tid == 0) {
+            a.out_ids[row] = s_other == 1u ? SEL_OTHER_SHARD : SEL_INVALID_ID;
+            a.sa.out_probs[row] = s_other == 1u ? 0.0f : __uint_as_float(0x7fc00000u);
+        }
+        return;
+    }
     // the hit chunk again (from L2): stripe i holds ids [clo + 1024 i,
     // clo + 1024 (i + 1)), thread t its quad at 4 t; id order is stripe,
     // thread, lane
@@ -1441,7 +1533,7 @@ __global__ void __launch_bounds__(kNT) full_draw_find_kernel(TopkArgs a) {
     for (int i = 0; i < kDrawQ; ++i) q[i] = ld_quad<kVec>(x, clo + 4u * (tid + kNT * i), chi, -INFINITY);
     const Members member(fr);
     auto weight = [&](float f, uint32_t id) {
-        return (id < chi && member(f, id)) ? ex2_approx((f - fr.M) * a.draw_c) : 0.0f;
+        return (id < chi && member(f, id + ib)) ? ex2_approx((f - fr.M) * fr.draw_c) : 0.0f;
     };
     float qsum[kDrawQ];
     int lp = -1;
@@ -1523,14 +1615,14 @@ __global__ void __launch_bounds__(kNT) full_draw_find_kernel(TopkArgs a) {
                 if (pick == 0xFFFFFFFFu && w > 0.0f && ff_lt(target, cdf)) { pick = e + j; pw = w; }
             }
             if (pick == 0xFFFFFFFFu) { pick = last; pw = lw; }
-            a.out_ids[row] = pick;
+            a.out_ids[row] = pick + ib;
             a.sa.out_probs[row] = pw / total;
         }
     }
     if (tid == 0 && (istar < 0 || s_cross == 0xFFFFFFFFu)) {
         // no crossing found (rounding): the last id with mass in the chunk
         const uint32_t id = s_lastpos >= 0 ? static_cast<uint32_t>(s_lastpos) : clo;
-        a.out_ids[row] = id;
+        a.out_ids[row] = id + ib;
         a.sa.out_probs[row] = weight(x[id], id) / total;
     }
 }
@@ -1845,7 +1937,7 @@ __global__ void __launch_bounds__(kCutNT, 1) full_cut_kernel(TopkArgs a) {
     cl.sync();  // no block leaves while its shared memory may still be read
 }
 
-template <bool kSample, bool kFull>
+template <bool kSample, bool kRowPlan>
 __global__ void __launch_bounds__(kNT) topk_finish_kernel(TopkArgs a) {
     __shared__ FinishShared s;
     pdl_wait();
@@ -1865,10 +1957,10 @@ __global__ void __launch_bounds__(kNT) topk_finish_kernel(TopkArgs a) {
     for (uint32_t c = lane; c < chunks; c += 32) nf |= a.chunk_flags[static_cast<size_t>(row) * a.stride + c];
     const uint32_t tau_row = a.row_tau[row];
     const float u_row = kSample ? a.sa.uniforms[row] : 0.0f;  // needed only at the end: loaded now
-    // top-n-sigma: the row's moments, summed in double (lane-strided, then
-    // across the warp)
+    // top-n-sigma (and a shard's statistics): the row's moments, summed in
+    // double (lane-strided, then across the warp)
     double mo1 = 0.0, mo2 = 0.0;
-    if (kSample && a.want_moments) {
+    if ((kSample || kRowPlan) && a.want_moments) {
         const float4* mo = reinterpret_cast<const float4*>(a.moments) + static_cast<size_t>(row) * a.stride;
         for (uint32_t c = lane; c < chunks; c += 32) {
             const float4 m = mo[c];
@@ -1959,7 +2051,7 @@ __global__ void __launch_bounds__(kNT) topk_finish_kernel(TopkArgs a) {
         nsig_thr = static_cast<double>(key2f(cand_key(s.sorted[0]))) -
                    static_cast<double>(a.sa.top_n_sigma) * sqrt(var);
     }
-    if constexpr (kSample && kFull) {
+    if constexpr (kSample && kRowPlan) {
         // the row's exponent sum Z and mean log-weight over all V, from the
         // chunk sums (in double; every warp computes them)
         const float4* fp = a.full_parts + static_cast<size_t>(row) * a.stride;
@@ -1992,6 +2084,45 @@ __global__ void __launch_bounds__(kNT) topk_finish_kernel(TopkArgs a) {
         if (tid < 32)
             full_row_plan(s.sorted, reinterpret_cast<float*>(s.buf), n < k ? n : k, row, nf != 0, a, z, gbar, sigma,
                           u_row);
+    } else if constexpr (kRowPlan) {
+        // sel_topk_stats: the slice's statistics beside its top k. The sums
+        // of the chunks' exponent sums rescaled to the slice's maximum, in
+        // chunk order (lane-strided, then a fixed butterfly), as above.
+        if (warp == 0) {
+            const float4* fp = a.full_parts + static_cast<size_t>(row) * a.stride;
+            float M = -INFINITY;
+            for (uint32_t c = lane; c < chunks; c += 32) M = fmaxf(M, fp[c].x);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+            const double c2 = static_cast<double>(a.full_cf);
+            double z = 0.0, q = 0.0;
+            for (uint32_t c = lane; c < chunks; c += 32) {
+                const float4 pc = fp[c];
+                const double sh = (static_cast<double>(pc.x) - M) * c2;
+                const double f = ex2_approx(static_cast<float>(sh));
+                const double sc = static_cast<double>(pc.y) + static_cast<double>(pc.z);
+                z += f * sc;
+                q += f * (static_cast<double>(pc.w) + sc * sh);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                z += __shfl_xor_sync(kFull, z, o);
+                q += __shfl_xor_sync(kFull, q, o);
+            }
+            if (lane == 0) {
+                sel_row_stats st;
+                st.max = M;
+                st.flags = nf != 0 ? 1u : 0u;
+                st.x0 = a.logits[static_cast<size_t>(row) * a.V];
+                st.n = a.V;
+                st.s1 = mo1;
+                st.s2 = mo2;
+                st.z = z;
+                st.h = q * 0.6931471805599453;  // natural units
+                a.stats_out[row] = st;
+            }
+        }
+        write_row<false>(s.sorted, reinterpret_cast<float*>(s.buf), a, row, n < k ? n : k, nf != 0, u_row);
     } else {
         write_row<kSample>(s.sorted, reinterpret_cast<float*>(s.buf), a, row, n < k ? n : k, nf != 0, u_row,
                            nsig_thr);
@@ -2051,7 +2182,7 @@ SampleArgs sample_args(const sel_sample_params& p, const float* uniforms, float*
 template <bool kSample>
 sel_status launch_topk(const float* d_logits, uint32_t rows, uint32_t V, uint32_t k, float* d_out_vals,
                        uint32_t* d_out_ids, void* d_ws, size_t ws_bytes, const SampleArgs& sa, cudaStream_t stream,
-                       bool full_row = false) {
+                       bool full_row = false, sel_row_stats* stats = nullptr) {
     const TopkLayout l = topk_layout(rows, V, k);
     if (!d_ws) return SEL_EINVAL;
     if (reinterpret_cast<uintptr_t>(d_ws) % SEL_WS_ALIGN) return SEL_EINVAL;
@@ -2076,8 +2207,9 @@ sel_status launch_topk(const float* d_logits, uint32_t rows, uint32_t V, uint32_
     a.pools = reinterpret_cast<uint32_t*>(ws + l.pools);
     a.chunk_flags = reinterpret_cast<uint32_t*>(ws + l.flags);
     a.moments = reinterpret_cast<float*>(ws + l.moments);
-    a.want_moments = (kSample && sa.top_n_sigma > 0.0f) ? 1u : 0u;
-    a.full_row = (kSample && full_row) ? 1u : 0u;
+    a.want_moments = ((kSample && sa.top_n_sigma > 0.0f) || stats) ? 1u : 0u;
+    a.full_row = ((kSample && full_row) || stats) ? 1u : 0u;
+    a.stats_out = stats;
     a.full_parts = reinterpret_cast<float4*>(ws + l.full_parts);
     a.full_rows = reinterpret_cast<FullRow*>(ws + l.full_rows);
     a.draw_sums = reinterpret_cast<FF*>(ws + l.draw_sums);
@@ -2093,6 +2225,14 @@ sel_status launch_topk(const float* d_logits, uint32_t rows, uint32_t V, uint32_
         const double Tf = sa.order == SEL_ORDER_TEMP_LAST ? 1.0 : static_cast<double>(sa.temperature);
         a.full_cf = static_cast<float>(1.4426950408889634 / Tf);
         a.draw_c = static_cast<float>(1.4426950408889634 / static_cast<double>(sa.temperature));
+    }
+    if (stats) {
+        // a shard's statistics: Tf as in the sampling chain (1 for a greedy
+        // policy, whose statistics nothing reads)
+        const double Tf = (sa.order == SEL_ORDER_TEMP_LAST || !(sa.temperature > 0.0f))
+                              ? 1.0
+                              : static_cast<double>(sa.temperature);
+        a.full_cf = static_cast<float>(1.4426950408889634 / Tf);
     }
     a.lists = reinterpret_cast<uint64_t*>(ws + l.lists);
     a.stride = l.stride;
@@ -2216,19 +2356,65 @@ namespace {
 struct ShardArgs {
     const float* vals;    // [rows][G][k], each shard's list sorted like sel_topk's
     const uint32_t* ids;  // [rows][G][k], shard-local ids
+    const sel_row_stats* stats;  // [rows][G] or null
     uint32_t G;
     uint32_t off[SEL_MAX_SHARDS + 1];  // shard g covers global ids [off[g], off[g+1])
 };
+
+// The whole row's statistics merged from its shards' records, in shard
+// order (every lane of the calling warp computes the same values):
+// the maximum M, the filter mass Z = sum exp((x - M) / Tf), the mean
+// log-weight gbar = sum P (x - M) / Tf, and the population standard
+// deviation, from moments shifted to shard 0's x0.
+struct MergedStats {
+    double M, Z, gbar, sigma;
+    bool bad;  // a shard saw a nonfinite logit, or a record does not fit its shard
+};
+
+__device__ MergedStats merge_stats(const ShardArgs& sh, uint32_t row, double Tf) {
+    const sel_row_stats* st = sh.stats + static_cast<size_t>(row) * sh.G;
+    MergedStats m{};
+    m.M = -INFINITY;
+    for (uint32_t g = 0; g < sh.G; ++g) {
+        const sel_row_stats r = st[g];
+        if ((r.flags & 1u) || r.n != sh.off[g + 1] - sh.off[g] || !(fabsf(r.max) <= FLT_MAX)) m.bad = true;
+        m.M = fmax(m.M, static_cast<double>(r.max));
+    }
+    if (m.bad) return m;
+    const double X0 = static_cast<double>(st[0].x0);
+    double Z = 0.0, H = 0.0, S1 = 0.0, S2 = 0.0, N = 0.0;
+    for (uint32_t g = 0; g < sh.G; ++g) {
+        const sel_row_stats r = st[g];
+        const double d = (static_cast<double>(r.max) - m.M) / Tf;  // log of the rescale, <= 0
+        const double f = exp(d);
+        Z += f * r.z;
+        H += f * (r.h + d * r.z);
+        const double D = static_cast<double>(r.x0) - X0;
+        const double n = static_cast<double>(r.n);
+        S1 += r.s1 + n * D;
+        S2 += r.s2 + 2.0 * D * r.s1 + n * D * D;
+        N += n;
+    }
+    m.Z = Z;
+    m.gbar = Z > 0.0 ? H / Z : 0.0;
+    const double mean_d = S1 / N;
+    m.sigma = sqrt(fmax(S2 / N - mean_d * mean_d, 0.0));
+    return m;
+}
 
 // One block per row. Entry j of shard g becomes the candidate (key(value),
 // off[g] + id), so the merged order is (value desc, global id asc), the order
 // sel_topk gives the unsharded row. A shard whose row failed (nonfinite
 // logits: id 0xFFFFFFFF) or a malformed list (id outside the shard, a
-// nonfinite value, an unsorted list) makes the row fail closed.
+// nonfinite value, an unsorted list) makes the row fail closed. Sampling
+// then runs the chain on the merged candidates (top_k > 0, with the merged
+// standard deviation for top-n-sigma), or plans the row's full-row draw
+// (top_k = 0: a.full_row).
 template <bool kSample>
 __global__ void __launch_bounds__(kNT) merge_shards_kernel(ShardArgs sh, TopkArgs a) {
     __shared__ TopkShared s;
     __shared__ uint32_t s_bad;
+    __shared__ double s_ms[4];  // Z, gbar, sigma, M of the merged statistics
     pdl_wait();
     const uint32_t row = blockIdx.x;
     const uint32_t k = a.k;
@@ -2236,6 +2422,18 @@ __global__ void __launch_bounds__(kNT) merge_shards_kernel(ShardArgs sh, TopkArg
     const float u_row = kSample ? a.sa.uniforms[row] : 0.0f;
     if (threadIdx.x == 0) s_bad = 0u;
     __syncthreads();
+    if (kSample && sh.stats && threadIdx.x < 32) {
+        const bool temp_last = a.sa.order == SEL_ORDER_TEMP_LAST;
+        const double Tf = (temp_last || !(a.sa.temperature > 0.0f)) ? 1.0 : static_cast<double>(a.sa.temperature);
+        const MergedStats m = merge_stats(sh, row, Tf);
+        if (threadIdx.x == 0) {
+            if (m.bad) atomicOr(&s_bad, 1u);
+            s_ms[0] = m.Z;
+            s_ms[1] = m.gbar;
+            s_ms[2] = m.sigma;
+            s_ms[3] = m.M;
+        }
+    }
     auto load = [&](uint32_t i) -> uint64_t {
         const uint32_t g = i / k;
         const uint32_t id = sh.ids[base + i];
@@ -2248,7 +2446,24 @@ __global__ void __launch_bounds__(kNT) merge_shards_kernel(ShardArgs sh, TopkArg
     };
     merge_row_lists(s, load, sh.G, k, &s_bad);
     __syncthreads();
-    write_row<kSample>(s.sorted, reinterpret_cast<float*>(s.buf), a, row, k, s_bad != 0u, u_row);
+    bool bad = s_bad != 0u;
+    if constexpr (kSample) {
+        if (sh.stats && !bad && static_cast<double>(key2f(cand_key(s.sorted[0]))) != s_ms[3])
+            bad = true;  // the lists' maximum is not the statistics' maximum
+        if (a.full_row) {
+            if (threadIdx.x < 32)
+                full_row_plan(s.sorted, reinterpret_cast<float*>(s.buf), k, row, bad, a, s_ms[0], s_ms[1], s_ms[2],
+                              u_row);
+            return;
+        }
+        double nsig_thr = -INFINITY;
+        if (sh.stats && a.sa.top_n_sigma > 0.0f && !bad)
+            nsig_thr = static_cast<double>(key2f(cand_key(s.sorted[0]))) -
+                       static_cast<double>(a.sa.top_n_sigma) * s_ms[2];
+        write_row<true>(s.sorted, reinterpret_cast<float*>(s.buf), a, row, k, bad, u_row, nsig_thr);
+    } else {
+        write_row<false>(s.sorted, reinterpret_cast<float*>(s.buf), a, row, k, bad, u_row);
+    }
 }
 
 sel_status check_shards(const float* d_vals, const uint32_t* d_ids, uint32_t rows, uint32_t G, uint32_t k,
@@ -2263,13 +2478,71 @@ sel_status check_shards(const float* d_vals, const uint32_t* d_ids, uint32_t row
     if (reinterpret_cast<uintptr_t>(d_vals) % 4 || reinterpret_cast<uintptr_t>(d_ids) % 4) return SEL_EINVAL;
     sh.vals = d_vals;
     sh.ids = d_ids;
+    sh.stats = nullptr;
     sh.G = G;
     for (uint32_t g = 0; g <= G; ++g) sh.off[g] = h_offsets[g];
     return SEL_OK;
 }
 
+// The workspace of a shard's draw: the error word, then the chunk sums.
+struct ShardDrawLayout {
+    size_t sums, total;
+    uint32_t chunks;
+};
+ShardDrawLayout shard_draw_layout(uint32_t rows, uint32_t V) {
+    ShardDrawLayout l{};
+    l.chunks = ceil_div(V, kDrawIds);
+    l.sums = kWsHeaderBytes;
+    l.total = l.sums + align_up(static_cast<size_t>(rows) * l.chunks * sizeof(FF), 256);
+    return l;
+}
+
+// Arguments of the two shard-draw calls (the same checks for both).
+sel_status shard_draw_args(const float* d_logits, uint32_t rows, uint32_t V, uint32_t offset,
+                           const sel_shard_plan* d_plan, void* d_ws, size_t ws_bytes, TopkArgs& a, bool& vec) {
+    if (V == 0 || V > SEL_MAX_V || offset > SEL_MAX_V - V) return SEL_EINVAL;
+    if (rows == 0) return SEL_OK;
+    if (!d_logits || !d_plan || !d_ws) return SEL_EINVAL;
+    if (reinterpret_cast<uintptr_t>(d_logits) % 4 || reinterpret_cast<uintptr_t>(d_plan) % 16 ||
+        reinterpret_cast<uintptr_t>(d_ws) % SEL_WS_ALIGN)
+        return SEL_EINVAL;
+    const ShardDrawLayout l = shard_draw_layout(rows, V);
+    if (ws_bytes < l.total) return SEL_EWORKSPACE;
+    if (static_cast<uint64_t>(rows) * l.chunks > 0x7fffffffull) return SEL_EUNSUPPORTED;
+    char* ws = static_cast<char*>(d_ws);
+    a.logits = d_logits;
+    a.V = V;
+    a.id_base = offset;
+    a.full_rows = reinterpret_cast<FullRow*>(const_cast<sel_shard_plan*>(d_plan));
+    a.draw_sums = reinterpret_cast<FF*>(ws + l.sums);
+    a.draw_chunks = l.chunks;
+    a.full_parts = nullptr;  // no chunk maxima from an earlier launch
+    a.err = reinterpret_cast<uint32_t*>(ws);
+    vec = (reinterpret_cast<uintptr_t>(d_logits) % 16 == 0) && (V % 4 == 0);
+    return SEL_OK;
+}
+
 }  // namespace
+
+size_t shard_draw_ws_bytes(uint32_t rows, uint32_t V) { return shard_draw_layout(rows, V).total; }
+
 }  // namespace sel
+
+extern "C" sel_status sel_topk_stats(const float* d_logits, uint32_t rows, uint32_t V, uint32_t k,
+                                     const sel_sample_params* p, float* d_out_vals, uint32_t* d_out_ids,
+                                     sel_row_stats* d_stats, void* d_ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!p || !policy_valid(*p)) return SEL_EINVAL;
+    if (V == 0 || V > SEL_MAX_V || k == 0 || k > V) return SEL_EINVAL;
+    if (k > SEL_MAX_K) return SEL_EUNSUPPORTED;
+    if (rows == 0) return SEL_OK;
+    if (!d_logits || !d_out_vals || !d_out_ids || !d_stats) return SEL_EINVAL;
+    if (reinterpret_cast<uintptr_t>(d_logits) % 4 || reinterpret_cast<uintptr_t>(d_out_vals) % 4 ||
+        reinterpret_cast<uintptr_t>(d_out_ids) % 4 || reinterpret_cast<uintptr_t>(d_stats) % 8)
+        return SEL_EINVAL;
+    const SampleArgs sa = sample_args(*p, nullptr, nullptr);
+    return launch_topk<false>(d_logits, rows, V, k, d_out_vals, d_out_ids, d_ws, ws_bytes, sa, stream, false,
+                              d_stats);
+}
 
 extern "C" sel_status sel_merge_shards(const float* d_vals, const uint32_t* d_ids, uint32_t rows, uint32_t G,
                                        uint32_t k, const uint32_t* h_offsets, float* d_out_vals,
@@ -2289,32 +2562,91 @@ extern "C" sel_status sel_merge_shards(const float* d_vals, const uint32_t* d_id
                : SEL_ECUDA;
 }
 
-extern "C" sel_status sel_sample_shards(const float* d_vals, const uint32_t* d_ids, uint32_t rows, uint32_t G,
-                                        uint32_t k, const uint32_t* h_offsets, const sel_sample_params* p,
-                                        const float* d_uniforms, uint32_t* d_out_ids, float* d_out_probs,
-                                        cudaStream_t stream) {
+extern "C" sel_status sel_sample_shards(const float* d_vals, const uint32_t* d_ids, const sel_row_stats* d_stats,
+                                        uint32_t rows, uint32_t G, uint32_t k, const uint32_t* h_offsets,
+                                        const sel_sample_params* p, const float* d_uniforms, uint32_t* d_out_ids,
+                                        float* d_out_probs, sel_shard_plan* d_plan, cudaStream_t stream) {
     if (!p) return SEL_EINVAL;
     const float T = p->temperature;
     if (!policy_valid(*p)) return SEL_EINVAL;
-    if (T > 0.0f && p->top_k != k) return SEL_EINVAL;  // the lists are the policy's top_k candidates
-    // top-n-sigma needs the whole row's standard deviation, which the
-    // per-shard candidate lists do not carry
-    if (T > 0.0f && p->top_n_sigma > 0.0f) return SEL_EUNSUPPORTED;
+    const bool full_row = T > 0.0f && p->top_k == 0;
+    if (full_row) {
+        // the lists are each shard's most probable candidates
+        if (k > kFullCand || !d_stats || !d_plan) return SEL_EINVAL;
+    } else if (T > 0.0f) {
+        if (p->top_k != k) return SEL_EINVAL;  // the lists are the policy's top_k candidates
+        if (p->top_n_sigma > 0.0f && !d_stats) return SEL_EINVAL;  // the whole row's deviation
+    }
     ShardArgs sh{};
     const sel_status st = check_shards(d_vals, d_ids, rows, G, k, h_offsets, sh);
     if (st != SEL_OK) return st;
     if (rows == 0) return SEL_OK;
-    if (!d_uniforms || !d_out_ids || !d_out_probs) return SEL_EINVAL;
-    if (reinterpret_cast<uintptr_t>(d_uniforms) % 4 || reinterpret_cast<uintptr_t>(d_out_ids) % 4 ||
-        reinterpret_cast<uintptr_t>(d_out_probs) % 4)
-        return SEL_EINVAL;
+    if (!d_uniforms || reinterpret_cast<uintptr_t>(d_uniforms) % 4) return SEL_EINVAL;
+    if (d_stats && reinterpret_cast<uintptr_t>(d_stats) % 8) return SEL_EINVAL;
+    if (full_row) {
+        if (reinterpret_cast<uintptr_t>(d_plan) % 16) return SEL_EINVAL;
+    } else {
+        if (!d_out_ids || !d_out_probs) return SEL_EINVAL;
+        if (reinterpret_cast<uintptr_t>(d_out_ids) % 4 || reinterpret_cast<uintptr_t>(d_out_probs) % 4)
+            return SEL_EINVAL;
+    }
+    sh.stats = T > 0.0f ? d_stats : nullptr;
     TopkArgs a{};
     a.k = k;
     a.out_ids = d_out_ids;
     a.sa = sample_args(*p, d_uniforms, d_out_probs);
+    if (full_row) {
+        const double Tf = p->order == SEL_ORDER_TEMP_LAST ? 1.0 : static_cast<double>(T);
+        a.full_row = 1u;
+        a.full_rows = reinterpret_cast<FullRow*>(d_plan);
+        a.full_cf = static_cast<float>(1.4426950408889634 / Tf);
+        a.draw_c = static_cast<float>(1.4426950408889634 / static_cast<double>(T));
+        a.V = h_offsets[G];
+        a.shard_G = G;  // no cut search: such rows fail closed
+        a.err = nullptr;
+    }
     return launch_pdl(merge_shards_kernel<true>, dim3(rows), dim3(kNT), 0, stream, sh, a) == cudaSuccess
                ? SEL_OK
                : SEL_ECUDA;
+}
+
+extern "C" sel_status sel_shard_draw_mass(const float* d_logits, uint32_t rows, uint32_t V, uint32_t offset,
+                                          const sel_shard_plan* d_plan, double* d_mass, void* d_ws, size_t ws_bytes,
+                                          cudaStream_t stream) {
+    TopkArgs a{};
+    bool vec = false;
+    const sel_status st = shard_draw_args(d_logits, rows, V, offset, d_plan, d_ws, ws_bytes, a, vec);
+    if (st != SEL_OK || rows == 0) return st;
+    if (!d_mass || reinterpret_cast<uintptr_t>(d_mass) % 8) return SEL_EINVAL;
+    const dim3 grid(rows * a.draw_chunks);
+    cudaError_t e = vec ? launch_pdl(full_draw_sum_kernel<true>, grid, dim3(kNT), 0, stream, a)
+                        : launch_pdl(full_draw_sum_kernel<false>, grid, dim3(kNT), 0, stream, a);
+    if (e != cudaSuccess) return SEL_ECUDA;
+    e = launch_pdl(shard_mass_kernel, dim3(rows), dim3(32), 0, stream, a, d_mass);
+    return e == cudaSuccess ? SEL_OK : SEL_ECUDA;
+}
+
+extern "C" sel_status sel_shard_draw(const float* d_logits, uint32_t rows, uint32_t V, uint32_t offset, uint32_t g,
+                                     uint32_t G, const sel_shard_plan* d_plan, const double* d_masses,
+                                     uint32_t* d_out_ids, float* d_out_probs, void* d_ws, size_t ws_bytes,
+                                     cudaStream_t stream) {
+    if (G == 0 || G > SEL_MAX_SHARDS || g >= G) return SEL_EINVAL;
+    TopkArgs a{};
+    bool vec = false;
+    const sel_status st = shard_draw_args(d_logits, rows, V, offset, d_plan, d_ws, ws_bytes, a, vec);
+    if (st != SEL_OK || rows == 0) return st;
+    if (!d_masses || !d_out_ids || !d_out_probs) return SEL_EINVAL;
+    if (reinterpret_cast<uintptr_t>(d_masses) % 8 || reinterpret_cast<uintptr_t>(d_out_ids) % 4 ||
+        reinterpret_cast<uintptr_t>(d_out_probs) % 4)
+        return SEL_EINVAL;
+    a.shard_masses = d_masses;
+    a.shard_g = g;
+    a.shard_G = G;
+    a.out_ids = d_out_ids;
+    a.sa.out_probs = d_out_probs;
+    const cudaError_t e = vec ? launch_pdl(full_draw_find_kernel<true>, dim3(rows), dim3(kNT), 0, stream, a)
+                              : launch_pdl(full_draw_find_kernel<false>, dim3(rows), dim3(kNT), 0, stream, a);
+    return e == cudaSuccess ? SEL_OK : SEL_ECUDA;
 }
 
 // ---------------------------------------------------------------------------

@@ -15,9 +15,24 @@ then runs per shard and merges:
    result equals `sel_topk` / `sel_sample` on the unsharded row.
 
 Only the gather moves data between ranks: G * k (value, id) pairs per row.
+
+Filters that look at the whole row take one more record per row and shard
+(`sel_topk_stats` writes the list and a 48-byte `sel_row_stats` record from
+one read of the slice):
+
+- top-n-sigma (top_k > 0): the gathered statistics give the row's standard
+  deviation; `sel_sample_shards` writes the result directly.
+- top_k = 0 (full-row sampling): `sel_sample_shards` writes a 48-byte plan
+  per row (the survivor set, decided from the merged 64 candidates and the
+  merged normaliser). Each shard then sums its survivors' mass
+  (`sel_shard_draw_mass`), `gather_masses` all-gathers the [rows][G] masses,
+  each shard runs `sel_shard_draw` (the shard the draw falls in writes the
+  global id, the others SEL_OTHER_SHARD and probability 0), and
+  `combine_draws` all-reduces them (minimum id, summed probability).
 """
 from __future__ import annotations
 
+import numpy as np
 import torch
 
 ALIGN = 4  # elements: a 16-byte boundary for fp32
@@ -64,3 +79,75 @@ def gather_lists(vals: torch.Tensor, ids: torch.Tensor, group=None):
     dist.all_gather(vs, vals.contiguous(), group=group)
     dist.all_gather(is_, ids32.contiguous(), group=group)
     return torch.stack(vs, dim=1).contiguous(), torch.stack(is_, dim=1).contiguous()
+
+
+# struct sel_row_stats, as numpy sees it (48 bytes)
+ROW_STATS_DTYPE = np.dtype([("max", "<f4"), ("flags", "<u4"), ("x0", "<f4"), ("n", "<u4"),
+                            ("s1", "<f8"), ("s2", "<f8"), ("z", "<f8"), ("h", "<f8")])
+assert ROW_STATS_DTYPE.itemsize == 48
+FULL_ROW_CANDIDATES = 64
+OTHER_SHARD = 0xFFFFFFFE
+
+
+def stats_records(stats: torch.Tensor) -> np.ndarray:
+    """[..., 48] uint8 statistics (device or host) as a numpy record array."""
+    a = stats.detach().cpu().contiguous().numpy()
+    return a.view(ROW_STATS_DTYPE)[..., 0]
+
+
+def full_row_list_len(offsets: list[int]) -> int:
+    """Entries per shard list for full-row sampling on shards: the 64
+    candidates, or fewer when a shard is narrower."""
+    return min(FULL_ROW_CANDIDATES, min(offsets[g + 1] - offsets[g] for g in range(len(offsets) - 1)))
+
+
+def gather_stats(stats: torch.Tensor, group=None) -> torch.Tensor:
+    """All-gather this rank's [rows][48] statistics into [rows][G][48]."""
+    import torch.distributed as dist
+
+    world = dist.get_world_size(group)
+    if stats.dim() != 2 or stats.shape[1] != ROW_STATS_DTYPE.itemsize or stats.dtype != torch.uint8:
+        raise ValueError("stats must be [rows, 48] uint8")
+    parts = [torch.empty_like(stats) for _ in range(world)]
+    dist.all_gather(parts, stats.contiguous(), group=group)
+    return torch.stack(parts, dim=1).contiguous()
+
+
+def gather_masses(mass: torch.Tensor, group=None) -> torch.Tensor:
+    """All-gather this rank's [rows] float64 survivor masses into [rows][G]."""
+    import torch.distributed as dist
+
+    world = dist.get_world_size(group)
+    if mass.dim() != 1 or mass.dtype != torch.float64:
+        raise ValueError("mass must be [rows] float64")
+    parts = [torch.empty_like(mass) for _ in range(world)]
+    dist.all_gather(parts, mass.contiguous(), group=group)
+    return torch.stack(parts, dim=1).contiguous()
+
+
+def _ids64(ids: torch.Tensor) -> torch.Tensor:
+    # ids as unsigned 32-bit values in int64, so that the minimum orders
+    # SEL_OTHER_SHARD and SEL_INVALID_ID above every real id
+    return ids.view(torch.int32).to(torch.int64) & 0xFFFFFFFF
+
+
+def combine_draws(ids: torch.Tensor, probs: torch.Tensor, group=None):
+    """All-reduce the shards' sel_shard_draw outputs: the row's id (minimum:
+    one shard holds the id, the others SEL_OTHER_SHARD; a failed row is
+    SEL_INVALID_ID everywhere) and probability (sum: the others hold 0).
+    Returns (ids as int64 holding uint32 values, probs float32)."""
+    import torch.distributed as dist
+
+    i = _ids64(ids)
+    p = probs.clone()
+    dist.all_reduce(i, op=dist.ReduceOp.MIN, group=group)
+    dist.all_reduce(p, op=dist.ReduceOp.SUM, group=group)
+    return i, p
+
+
+def combine_draws_local(ids: list[torch.Tensor], probs: list[torch.Tensor]):
+    """combine_draws for shards held by one process (shard g's outputs at
+    index g)."""
+    i = torch.stack([_ids64(t) for t in ids]).min(dim=0).values
+    p = torch.stack(probs).sum(dim=0)
+    return i, p

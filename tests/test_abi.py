@@ -132,18 +132,62 @@ def test_shard_merge_validation_needs_no_gpu(lib):
     assert m(vp(0x10002), fake, 1, 2, 5, good, fake, fake, None) == B.SEL_EINVAL      # misaligned
     s = lib.sel_sample_shards
     p = B.SampleParams(0.7, 5, 0.9, 0.05, 0)
-    assert s(fake, fake, 1, 2, 5, good, None, fake, fake, fake, None) == B.SEL_EINVAL
-    assert s(fake, fake, 1, 2, 5, good, ctypes.byref(B.SampleParams(0.7, 6, 0.9, 0.05, 0)),
-             fake, fake, fake, None) == B.SEL_EINVAL                                   # top_k != k
-    assert s(fake, fake, 1, 2, 5, good, ctypes.byref(B.SampleParams(float("nan"), 5, 0.9, 0.05, 0)),
-             fake, fake, fake, None) == B.SEL_EINVAL
-    assert s(fake, fake, 1, 2, 5, good, ctypes.byref(B.SampleParams(0.7, 5, 1.5, 0.05, 0)),
-             fake, fake, fake, None) == B.SEL_EINVAL
-    assert s(fake, fake, 1, 2, 5, good, ctypes.byref(p), None, fake, fake, None) == B.SEL_EINVAL
-    # top-n-sigma needs the whole row's standard deviation: not from shard lists
-    assert s(fake, fake, 1, 2, 5, good, ctypes.byref(B.SampleParams(0.7, 5, 0.9, 0.05, 0, 1.0, 0.0)),
-             fake, fake, fake, None) == B.SEL_EUNSUPPORTED
-    assert s(fake, fake, 0, 2, 5, good, ctypes.byref(p), None, None, None, None) == B.SEL_OK
+    # (vals, ids, stats, rows, G, k, offsets, params, uniforms, out_ids, out_probs, plan, stream)
+    assert s(fake, fake, None, 1, 2, 5, good, None, fake, fake, fake, None, None) == B.SEL_EINVAL
+    assert s(fake, fake, None, 1, 2, 5, good, ctypes.byref(B.SampleParams(0.7, 6, 0.9, 0.05, 0)),
+             fake, fake, fake, None, None) == B.SEL_EINVAL                             # top_k != k
+    assert s(fake, fake, None, 1, 2, 5, good, ctypes.byref(B.SampleParams(float("nan"), 5, 0.9, 0.05, 0)),
+             fake, fake, fake, None, None) == B.SEL_EINVAL
+    assert s(fake, fake, None, 1, 2, 5, good, ctypes.byref(B.SampleParams(0.7, 5, 1.5, 0.05, 0)),
+             fake, fake, fake, None, None) == B.SEL_EINVAL
+    assert s(fake, fake, None, 1, 2, 5, good, ctypes.byref(p), None, fake, fake, None, None) == B.SEL_EINVAL
+    # top-n-sigma needs the whole row's standard deviation: the shards' statistics
+    nsig = ctypes.byref(B.SampleParams(0.7, 5, 0.9, 0.05, 0, 1.0, 0.0))
+    assert s(fake, fake, None, 1, 2, 5, good, nsig, fake, fake, fake, None, None) == B.SEL_EINVAL
+    assert s(fake, fake, vp(0x10004), 1, 2, 5, good, nsig, fake, fake, fake, None, None) == B.SEL_EINVAL
+    # full-row sampling: statistics, a plan, and at most 64 candidates per list
+    full = ctypes.byref(B.SampleParams(0.7, 0, 0.9, 0.0, 0))
+    assert s(fake, fake, None, 1, 2, 5, good, full, fake, None, None, fake, None) == B.SEL_EINVAL
+    assert s(fake, fake, fake, 1, 2, 5, good, full, fake, None, None, None, None) == B.SEL_EINVAL
+    assert s(fake, fake, fake, 1, 2, 65, offs(0, 100, 200), full, fake, None, None, fake,
+             None) == B.SEL_EINVAL
+    assert s(fake, fake, fake, 1, 2, 5, good, full, fake, None, None, vp(0x10008), None) == B.SEL_EINVAL
+    assert s(fake, fake, None, 0, 2, 5, good, ctypes.byref(p), None, None, None, None, None) == B.SEL_OK
+
+
+def test_shard_stats_and_draw_validation_needs_no_gpu(lib):
+    from sampling_row_fp32_gb300 import binding as B
+    vp = ctypes.c_void_p
+    fake = vp(0x10000)
+    p = B.SampleParams(1.0, 0, 0.9, 0.0, 0)
+    st = lib.sel_topk_stats
+    assert st(fake, 0, 100, 5, ctypes.byref(p), None, None, None, None, 0, None) == B.SEL_OK    # rows = 0
+    assert st(fake, 1, 100, 5, None, fake, fake, fake, fake, 1 << 20, None) == B.SEL_EINVAL     # no policy
+    assert st(fake, 1, 100, 5, ctypes.byref(p), fake, fake, None, fake, 1 << 20, None) == B.SEL_EINVAL
+    assert st(fake, 1, 100, 5, ctypes.byref(p), fake, fake, vp(0x10004), fake, 1 << 20, None) == B.SEL_EINVAL
+    assert st(fake, 1, 100, 0, ctypes.byref(p), fake, fake, fake, fake, 1 << 20, None) == B.SEL_EINVAL
+    assert st(fake, 1, 4, 5, ctypes.byref(p), fake, fake, fake, fake, 1 << 20, None) == B.SEL_EINVAL  # k > V
+    n = B.sel_workspace_bytes(B.SEL_OP_SHARD_DRAW, 3, 100_000, 0)
+    assert n > 0 and n == B.sel_workspace_bytes(B.SEL_OP_SHARD_DRAW, 3, 100_000, 7)
+    assert B.sel_workspace_bytes(B.SEL_OP_SHARD_DRAW, 3, 0, 0) == 0
+    m = lib.sel_shard_draw_mass
+    # (logits, rows, V, offset, plan, mass, ws, ws_bytes, stream)
+    assert m(None, 0, 100, 0, None, None, None, 0, None) == B.SEL_OK                            # rows = 0
+    assert m(fake, 3, 0, 0, fake, fake, fake, n, None) == B.SEL_EINVAL                          # V = 0
+    assert m(fake, 3, 100_000, 0x7FFFFFFF, fake, fake, fake, n, None) == B.SEL_EINVAL           # ids past 2^31
+    assert m(fake, 3, 100_000, 0, None, fake, fake, n, None) == B.SEL_EINVAL                    # no plan
+    assert m(fake, 3, 100_000, 0, vp(0x10008), fake, fake, n, None) == B.SEL_EINVAL             # plan alignment
+    assert m(fake, 3, 100_000, 0, fake, None, fake, n, None) == B.SEL_EINVAL                    # no mass
+    assert m(fake, 3, 100_000, 0, fake, fake, fake, n - 1, None) == B.SEL_EWORKSPACE
+    assert m(fake, 3, 100_000, 0, fake, fake, vp(0x10080), n, None) == B.SEL_EINVAL             # ws alignment
+    d = lib.sel_shard_draw
+    # (logits, rows, V, offset, g, G, plan, masses, out_ids, out_probs, ws, ws_bytes, stream)
+    assert d(fake, 3, 100_000, 0, 2, 2, fake, fake, fake, fake, fake, n, None) == B.SEL_EINVAL  # g >= G
+    assert d(fake, 3, 100_000, 0, 0, 65, fake, fake, fake, fake, fake, n, None) == B.SEL_EINVAL
+    assert d(fake, 3, 100_000, 0, 0, 2, fake, None, fake, fake, fake, n, None) == B.SEL_EINVAL  # no masses
+    assert d(fake, 3, 100_000, 0, 0, 2, fake, vp(0x10004), fake, fake, fake, n, None) == B.SEL_EINVAL
+    assert d(fake, 3, 100_000, 0, 0, 2, fake, fake, fake, fake, fake, 16, None) == B.SEL_EWORKSPACE
+    assert d(fake, 0, 100_000, 0, 0, 2, None, None, None, None, None, 0, None) == B.SEL_OK
 
 
 def test_eog_validation_needs_no_gpu(lib):

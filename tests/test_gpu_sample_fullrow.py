@@ -174,3 +174,37 @@ def test_draw_walks_ascending_ids(orc):
     u = ((np.arange(n) + 0.5) / n).astype(np.float32)
     gi, _, _, _ = check(orc, x, u, 1.0, 1.0, 0.0, decided=np.ones(n, bool))
     assert np.all(np.diff(gi.astype(np.int64)) >= 0)
+
+
+@pytest.mark.parametrize("V,misalign", [(20_001, False), (20_000, True), (16_671, True)])
+def test_typical_on_scalar_path_rows(orc, V, misalign):
+    """A locally typical cut needs the row's mean log-weight; rows that take
+    the scalar loads (V % 4 != 0, or misaligned) end in a chunk where some
+    threads hold only fill values, which must add nothing to it. Rows whose
+    window lies well inside the 64 candidates are decided; rows whose window
+    runs past them fail closed."""
+    x = synth.normal_rows(81, 30, V, 3.0)
+    u = synth.uniforms(82, 30)
+    _, _, _, failed = check(orc, x, u, 0.6, 1.0, 0.0, typ=0.8, misalign=misalign)
+    reach = typical_window_reach(x, 0.6, 0.8)
+    assert not failed[reach < CAND - 8].any() and failed[reach >= CAND].all()
+    assert (reach < CAND - 8).sum() >= 20
+
+
+def typical_window_reach(x, T, typ):
+    """Per row, the largest probability rank (0 = most probable) inside the
+    locally typical window (double precision, ties by id)."""
+    out = np.zeros(x.shape[0], dtype=np.int64)
+    for r in range(x.shape[0]):
+        z = x[r].astype(np.float64) / T
+        z -= z.max()
+        p = np.exp(z)
+        p /= p.sum()
+        lp = np.log(p)
+        score = np.abs(-lp - (-(p * lp).sum()))
+        order = np.lexsort((np.arange(p.size), score))
+        n = int(np.searchsorted(np.cumsum(p[order]), typ) + 1)
+        rank = np.empty(p.size, dtype=np.int64)
+        rank[np.lexsort((np.arange(p.size), -p))] = np.arange(p.size)
+        out[r] = rank[order[:n]].max()
+    return out

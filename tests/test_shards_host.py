@@ -81,3 +81,73 @@ def test_gather_two_ranks_holds_the_row_top_k(tmp_path, V, k):
             order = np.lexsort((glob, -v.astype(np.float64)))[:k]
             assert np.array_equal(glob[order], want_ids[r].astype(np.int64))
             assert np.array_equal(v[order], want_vals[r])
+
+
+def _rank_stats_main(rank, world, port, out_dir):
+    """Each rank: a statistics record per row of its slice (packed as
+    sel_row_stats), its survivor masses, and a draw output in which it holds
+    the id of some rows; then the gathers and the combine."""
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        rows, V = 4, 1000
+        x = synth.normal_rows(22, rows, V, 2.0)
+        lo, hi = shards.shard_range(V, world, rank)
+        rec = np.zeros(rows, dtype=shards.ROW_STATS_DTYPE)
+        xs = x[:, lo:hi].astype(np.float64)
+        rec["max"] = x[:, lo:hi].max(axis=1)
+        rec["x0"] = x[:, lo]
+        rec["n"] = hi - lo
+        rec["s1"] = (xs - xs[:, :1]).sum(axis=1)
+        rec["z"] = np.exp(xs - xs.max(axis=1, keepdims=True)).sum(axis=1)
+        st = torch.from_numpy(rec.view(np.uint8).reshape(rows, 48).copy())
+        gs = shards.gather_stats(st)
+        mass = torch.tensor([float(rank + 1), 0.5 * rank, 2.0, 0.0], dtype=torch.float64)
+        gm = shards.gather_masses(mass)
+        # row 0: rank 1 holds the draw; row 1: rank 0; row 2: failed everywhere;
+        # row 3: rank 0 holds id 0 (the smallest id)
+        ids = torch.tensor([shards.OTHER_SHARD if rank == 0 else 700, 5 if rank == 0 else shards.OTHER_SHARD,
+                            0xFFFFFFFF, 0 if rank == 0 else shards.OTHER_SHARD], dtype=torch.int64)
+        ids = torch.from_numpy(ids.numpy().astype(np.uint32).view(np.int32))
+        probs = torch.tensor([0.0 if rank == 0 else 0.25, 0.125 if rank == 0 else 0.0, float("nan"),
+                              1.0 if rank == 0 else 0.0], dtype=torch.float32)
+        ci, cp = shards.combine_draws(ids, probs)
+        np.save(os.path.join(out_dir, f"stats{rank}.npy"), gs.numpy())
+        np.save(os.path.join(out_dir, f"mass{rank}.npy"), gm.numpy())
+        np.save(os.path.join(out_dir, f"cid{rank}.npy"), ci.numpy())
+        np.save(os.path.join(out_dir, f"cp{rank}.npy"), cp.numpy())
+    finally:
+        dist.destroy_process_group()
+
+
+def test_stats_masses_and_draws_between_two_ranks(tmp_path):
+    world = 2
+    mp.start_processes(_rank_stats_main, args=(world, _free_port(), str(tmp_path)),
+                       nprocs=world, join=True, start_method="spawn")
+    x = synth.normal_rows(22, 4, 1000, 2.0)
+    offs = shards.shard_offsets(1000, world)
+    for rank in range(world):
+        gs = np.load(tmp_path / f"stats{rank}.npy")
+        assert gs.shape == (4, world, 48)
+        rec = gs.view(shards.ROW_STATS_DTYPE)[..., 0]
+        for g in range(world):  # shard order = rank order
+            assert np.all(rec["n"][:, g] == offs[g + 1] - offs[g])
+            assert np.array_equal(rec["x0"][:, g], x[:, offs[g]])
+            assert np.array_equal(rec["max"][:, g], x[:, offs[g]:offs[g + 1]].max(axis=1))
+        gm = np.load(tmp_path / f"mass{rank}.npy")
+        assert np.array_equal(gm, np.array([[1.0, 2.0], [0.0, 0.5], [2.0, 2.0], [0.0, 0.0]]))
+        ci = np.load(tmp_path / f"cid{rank}.npy")
+        cp = np.load(tmp_path / f"cp{rank}.npy")
+        assert list(ci) == [700, 5, 0xFFFFFFFF, 0]
+        assert cp[0] == 0.25 and cp[1] == 0.125 and np.isnan(cp[2]) and cp[3] == 1.0
+
+
+def test_full_row_list_len_and_local_combine():
+    assert shards.full_row_list_len([0, 100, 200]) == 64
+    assert shards.full_row_list_len([0, 40, 200]) == 40
+    ids = [torch.tensor([-2, 3, -1], dtype=torch.int32), torch.tensor([9, -2, -1], dtype=torch.int32)]
+    probs = [torch.tensor([0.0, 0.5, float("nan")]), torch.tensor([0.75, 0.0, float("nan")])]
+    ci, cp = shards.combine_draws_local(ids, probs)
+    assert ci.tolist() == [9, 3, 0xFFFFFFFF]
+    assert cp[0] == 0.75 and cp[1] == 0.5 and torch.isnan(cp[2])
