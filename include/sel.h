@@ -64,7 +64,8 @@ typedef enum sel_status {
 
 /* Operation codes for sel_workspace_bytes. */
 enum { SEL_OP_ARGMAX = 0, SEL_OP_TOPK = 1, SEL_OP_SAMPLE = 2, SEL_OP_SPEC = 3,
-       SEL_OP_SPEC_SAMPLER = 4, SEL_OP_SPEC_DIAG = 5, SEL_OP_SHARD_DRAW = 6 };
+       SEL_OP_SPEC_SAMPLER = 4, SEL_OP_SPEC_DIAG = 5, SEL_OP_SHARD_DRAW = 6,
+       SEL_OP_SPEC_SHARD_DRAW = 7 };
 
 /* Order of temperature and filters in sel_sample. */
 enum {
@@ -92,6 +93,7 @@ enum {
  *                     k = the policy's top_k
  *   op SEL_OP_SPEC_DIAG: rows = S, V, k = K
  *   op SEL_OP_SHARD_DRAW: rows, V = the shard's slice width (k ignored)
+ *   op SEL_OP_SPEC_SHARD_DRAW: rows = S, V = the shard's slice width
  * The size depends only on these arguments, not on the device. Returns 0
  * when the arguments are invalid (the entry point would refuse them anyway).
  */
@@ -535,6 +537,123 @@ sel_status sel_shard_draw(const float *d_logits, uint32_t rows, uint32_t V,
                           const sel_shard_plan *d_plan, const double *d_masses,
                           uint32_t *d_out_ids, float *d_out_probs, void *d_ws,
                           size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Speculative acceptance on vocabulary shards. Under a tensor split each
+ * rank holds one id range of every target and draft row (llama.cpp PR 49,
+ * "Problem"). The acceptance rules ("Speculative-decoding acceptance rules",
+ * Modified rejection sampling and Argmax-against-argmax) need, per row, the
+ * softmax normaliser (or the argmax) of the whole row and the logits at the
+ * draft tokens; the final draw needs the residual's mass on every shard
+ * (one exchange of per-shard totals). The steps, on every rank:
+ *   1. spec_shard_stats on the rank's slices: one spec_shard_part per row;
+ *   2. all-gather the parts into [S][G][2K+1];
+ *   3. spec_accept_shards: the merged statistics, the acceptance chain (the
+ *      same on every rank), accepted counts and emitted tokens, and, in the
+ *      rejection rule, a draw plan per sequence;
+ *   4. (rejection rule) spec_shard_draw_mass on the slices, all-gather the
+ *      [S][2] masses into [S][G][2], spec_shard_draw on the slices, and an
+ *      all-reduce (minimum) of the emitted arrays over the ranks: the shard
+ *      the draw falls in writes the token's global id, the others
+ *      SEL_OTHER_SHARD.
+ */
+typedef struct spec_shard_part {
+    float max;        /* the slice's largest logit */
+    uint32_t idx;     /* argmax rule: global id of the slice's first maximum;
+                         bit 31: the slice holds a NaN or +-Inf logit */
+    float x_tok;      /* rejection rule: the row's logit at its draft token,
+                         when has_tok */
+    uint32_t has_tok; /* 1: the row's draft token lies in this slice */
+    double z;         /* rejection rule: sum of exp((x - max) / T) */
+    uint32_t pad[2];
+} spec_shard_part;    /* 32 bytes */
+
+typedef struct spec_shard_plan {
+    uint32_t opaque[8];
+} spec_shard_plan;    /* 32 bytes */
+
+#define SPEC_SHARD_MAX_K 64u
+
+/*
+ * spec_shard_stats -- step 1 on one shard.
+ *
+ *   d_target   [S][K+1][V] f32: this shard's slice of every target row
+ *   d_draft    [S][K][V] f32: the slices of the draft rows (rejection rule)
+ *   d_draft_tokens [S][K] u32: the draft tokens, GLOBAL ids
+ *   V, offset  the slice's width and first global id
+ *   params     as for spec_accept
+ *   d_parts    [S][2K+1] spec_shard_part: per sequence, target rows 0..K,
+ *              then draft rows 0..K-1 (unused in the argmax rule)
+ *   d_ws       workspace of sel_workspace_bytes(SEL_OP_SPEC, S, V, K)
+ * K <= SPEC_SHARD_MAX_K (else SEL_EUNSUPPORTED).
+ */
+sel_status spec_shard_stats(const float *d_target, const float *d_draft,
+                            const uint32_t *d_draft_tokens, uint32_t S,
+                            uint32_t K, uint32_t V, uint32_t offset,
+                            const spec_params *params, spec_shard_part *d_parts,
+                            void *d_ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * spec_accept_shards -- step 3: the acceptance chain of spec_accept from the
+ * gathered parts.
+ *
+ *   d_parts    [S][G][2K+1]: every shard's spec_shard_stats output, shard
+ *              order = id order
+ *   G, h_offsets  as for sel_merge_shards (h_offsets[G] = V)
+ *   d_draft_tokens, params, d_u_acc, d_u_fin, d_accepted, d_emitted  as for
+ *              spec_accept; in the rejection rule the emitted entry at the
+ *              accepted count is left SEL_INVALID_ID for the draw
+ *   d_plan     [S] spec_shard_plan (rejection rule; may be NULL in the
+ *              argmax rule, which emits its final token here)
+ * Per-sequence errors as for spec_accept; parts that do not fit their shard
+ * (a draft token's logit on no shard or on two) also invalidate the sequence.
+ */
+sel_status spec_accept_shards(const spec_shard_part *d_parts,
+                              const uint32_t *d_draft_tokens, uint32_t S,
+                              uint32_t K, uint32_t G,
+                              const uint32_t *h_offsets,
+                              const spec_params *params, const float *d_u_acc,
+                              const float *d_u_fin, uint32_t *d_accepted,
+                              uint32_t *d_emitted, spec_shard_plan *d_plan,
+                              cudaStream_t stream);
+
+/*
+ * spec_shard_draw_mass -- step 4a on one shard: the residual mass
+ * sum max(p - q, 0) and the target mass sum p over this slice of the rows
+ * each sequence's plan names (the rejecting position's target and draft
+ * rows, or target row K for a bonus draw).
+ *
+ *   d_target, d_draft, S, K, V  as for spec_shard_stats
+ *   d_plan     [S] from spec_accept_shards
+ *   d_mass     [S][2] f64: (residual, target) masses of this slice
+ *   d_ws       workspace of sel_workspace_bytes(SEL_OP_SPEC_SHARD_DRAW, S,
+ *              V, 0), kept untouched until the matching spec_shard_draw
+ */
+sel_status spec_shard_draw_mass(const float *d_target, const float *d_draft,
+                                uint32_t S, uint32_t K, uint32_t V,
+                                const spec_shard_plan *d_plan, double *d_mass,
+                                void *d_ws, size_t ws_bytes,
+                                cudaStream_t stream);
+
+/*
+ * spec_shard_draw -- step 4b on shard g: the draw with u_fin over the
+ * residual (over p when the residual's total is <= 0), in ascending global
+ * id across the shards; writes d_emitted[s][accepted] (the token's global
+ * id on the shard it falls in, SEL_OTHER_SHARD on the others).
+ *
+ *   d_target, d_draft, S, K, V, offset  as for spec_shard_stats
+ *   g, G       this shard and the number of shards
+ *   d_plan     [S] from spec_accept_shards
+ *   d_masses   [S][G][2] f64: every shard's d_mass, gathered in shard order
+ *   d_emitted  [S][K+1] u32: this rank's spec_accept_shards output
+ *   d_ws       this shard's spec_shard_draw_mass workspace
+ */
+sel_status spec_shard_draw(const float *d_target, const float *d_draft,
+                           uint32_t S, uint32_t K, uint32_t V, uint32_t offset,
+                           uint32_t g, uint32_t G,
+                           const spec_shard_plan *d_plan,
+                           const double *d_masses, uint32_t *d_emitted,
+                           void *d_ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Static description of a status code. */
 const char *sel_status_string(sel_status status);

@@ -22,7 +22,7 @@ SEL_OK, SEL_EINVAL, SEL_EWORKSPACE, SEL_ECUDA, SEL_EUNSUPPORTED = range(5)
 SEL_INVALID_ID = 0xFFFFFFFF
 SEL_MAX_K = 1024
 (SEL_OP_ARGMAX, SEL_OP_TOPK, SEL_OP_SAMPLE, SEL_OP_SPEC, SEL_OP_SPEC_SAMPLER, SEL_OP_SPEC_DIAG,
- SEL_OP_SHARD_DRAW) = range(7)
+ SEL_OP_SHARD_DRAW, SEL_OP_SPEC_SHARD_DRAW) = range(8)
 SEL_ORDER_TEMP_FIRST, SEL_ORDER_TEMP_LAST = 0, 1
 SPEC_MODE_REJECTION, SPEC_MODE_ARGMAX = 0, 1
 
@@ -30,7 +30,8 @@ EXPORTED = ("sel_workspace_bytes", "sel_workspace_init", "sel_argmax", "sel_topk
             "sel_sample", "spec_accept", "sel_status_string", "sel_argmax_noalloc",
             "sel_merge_shards", "sel_sample_shards", "sel_argmax_excluding",
             "spec_accept_sampler", "spec_diagnostics", "sel_topk_stats", "sel_shard_draw_mass",
-            "sel_shard_draw")
+            "sel_shard_draw", "spec_shard_stats", "spec_accept_shards", "spec_shard_draw_mass",
+            "spec_shard_draw")
 SEL_NOALLOC_SCRATCH_BYTES = 1 << 20
 SEL_MAX_SHARDS = 64
 SEL_MAX_EXCLUDED = 256
@@ -38,6 +39,9 @@ SEL_OTHER_SHARD = 0xFFFFFFFE
 ROW_STATS_BYTES = 48   # struct sel_row_stats
 SHARD_PLAN_BYTES = 48  # struct sel_shard_plan
 FULL_ROW_CANDIDATES = 64
+SPEC_SHARD_PART_BYTES = 32  # struct spec_shard_part
+SPEC_SHARD_PLAN_BYTES = 32  # struct spec_shard_plan
+SPEC_SHARD_MAX_K = 64
 
 
 class SelError(RuntimeError):
@@ -113,6 +117,16 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.sel_shard_draw_mass.restype = ctypes.c_int
     lib.sel_shard_draw.argtypes = [_vp, _u32, _u32, _u32, _u32, _u32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
     lib.sel_shard_draw.restype = ctypes.c_int
+    lib.spec_shard_stats.argtypes = [_vp, _vp, _vp, _u32, _u32, _u32, _u32, ctypes.POINTER(SpecParams), _vp, _vp,
+                                     _sz, _vp]
+    lib.spec_shard_stats.restype = ctypes.c_int
+    lib.spec_accept_shards.argtypes = [_vp, _vp, _u32, _u32, _u32, _vp, ctypes.POINTER(SpecParams), _vp, _vp, _vp,
+                                       _vp, _vp, _vp]
+    lib.spec_accept_shards.restype = ctypes.c_int
+    lib.spec_shard_draw_mass.argtypes = [_vp, _vp, _u32, _u32, _u32, _vp, _vp, _vp, _sz, _vp]
+    lib.spec_shard_draw_mass.restype = ctypes.c_int
+    lib.spec_shard_draw.argtypes = [_vp, _vp, _u32, _u32, _u32, _u32, _u32, _u32, _vp, _vp, _vp, _vp, _sz, _vp]
+    lib.spec_shard_draw.restype = ctypes.c_int
     lib.sel_sample_shards.restype = ctypes.c_int
     lib.sel_status_string.argtypes = [ctypes.c_int]
     lib.sel_status_string.restype = ctypes.c_char_p
@@ -341,6 +355,72 @@ def sel_shard_draw(logits, offset: int, g: int, G: int, plan, masses, out_ids, o
     _check(load().sel_shard_draw(_ptr(logits), rows, V, int(offset), int(g), int(G), _ptr(plan), _ptr(masses),
                                  _ptr(out_ids), _ptr(out_probs), _ptr(ws), _nbytes(ws), _stream(stream)),
            "sel_shard_draw")
+
+
+def _spec_dims(target, draft):
+    S, K1, V = target.shape
+    if draft is not None and tuple(draft.shape) != (S, K1 - 1, V):
+        raise ValueError("draft must be [S, K, V] with target [S, K+1, V]")
+    return S, K1 - 1, V
+
+
+def spec_shard_stats(target, draft, draft_tokens, offset: int, params: SpecParams, parts, ws=None,
+                     stream=None) -> None:
+    """A shard's slices target [S, K+1, V], draft [S, K, V] (global draft
+    token ids) -> parts [S, 2K+1, 32] uint8 (spec_shard_part records)."""
+    _check_f32(target, "target")
+    _check_f32(draft, "draft")
+    _check_ids(draft_tokens, "draft_tokens")
+    S, K, V = _spec_dims(target, draft)
+    if tuple(parts.shape) != (S, 2 * K + 1, SPEC_SHARD_PART_BYTES):
+        raise ValueError("parts must be [S, 2K+1, 32] bytes")
+    _check(load().spec_shard_stats(_ptr(target), _ptr(draft), _ptr(draft_tokens), S, K, V, int(offset),
+                                   ctypes.byref(params), _ptr(parts), _ptr(ws), _nbytes(ws), _stream(stream)),
+           "spec_shard_stats")
+
+
+def spec_accept_shards(parts, draft_tokens, offsets, params: SpecParams, u_acc, u_fin, accepted, emitted,
+                       plan=None, stream=None) -> None:
+    """Gathered parts [S, G, 2K+1, 32] -> accepted [S], emitted [S, K+1] and
+    (rejection rule) plan [S, 32] uint8."""
+    _check_ids(draft_tokens, "draft_tokens")
+    _check_f32(u_acc, "u_acc")
+    _check_f32(u_fin, "u_fin")
+    _check_ids(accepted, "accepted")
+    _check_ids(emitted, "emitted")
+    S, G, R, nb = parts.shape
+    if nb != SPEC_SHARD_PART_BYTES or R % 2 != 1 or len(offsets) != G + 1:
+        raise ValueError("parts must be [S, G, 2K+1, 32] bytes and offsets G + 1 ints")
+    K = (R - 1) // 2
+    off = _host_offsets(offsets)
+    _check(load().spec_accept_shards(_ptr(parts), _ptr(draft_tokens), S, K, G, ctypes.cast(off, _vp),
+                                     ctypes.byref(params), _ptr(u_acc), _ptr(u_fin), _ptr(accepted), _ptr(emitted),
+                                     _ptr(plan), _stream(stream)), "spec_accept_shards")
+
+
+def spec_shard_draw_mass(target, draft, plan, mass, ws=None, stream=None) -> None:
+    """A shard's slices and the plans -> mass [S, 2] float64 (residual, target)."""
+    _check_f32(target, "target")
+    _check_f32(draft, "draft")
+    if mass.dtype != torch.float64:
+        raise ValueError("mass must be float64")
+    S, K, V = _spec_dims(target, draft)
+    _check(load().spec_shard_draw_mass(_ptr(target), _ptr(draft), S, K, V, _ptr(plan), _ptr(mass), _ptr(ws),
+                                       _nbytes(ws), _stream(stream)), "spec_shard_draw_mass")
+
+
+def spec_shard_draw(target, draft, offset: int, g: int, G: int, plan, masses, emitted, ws=None,
+                    stream=None) -> None:
+    """Shard g's slices, gathered masses [S, G, 2] -> emitted[s][accepted]."""
+    _check_f32(target, "target")
+    _check_f32(draft, "draft")
+    _check_ids(emitted, "emitted")
+    if masses.dtype != torch.float64:
+        raise ValueError("masses must be float64")
+    S, K, V = _spec_dims(target, draft)
+    _check(load().spec_shard_draw(_ptr(target), _ptr(draft), S, K, V, int(offset), int(g), int(G), _ptr(plan),
+                                  _ptr(masses), _ptr(emitted), _ptr(ws), _nbytes(ws), _stream(stream)),
+           "spec_shard_draw")
 
 
 # ---------------------------------------------------------------------------

@@ -45,6 +45,8 @@ extern "C" size_t sel_workspace_bytes(int op, uint32_t rows, uint32_t V, uint32_
             return spec_diag_ws_bytes(rows, V, k);
         case SEL_OP_SHARD_DRAW:
             return shard_draw_ws_bytes(rows, V);
+        case SEL_OP_SPEC_SHARD_DRAW:
+            return spec_shard_draw_ws_bytes(rows, V);
         default:
             return 0;
     }

@@ -25,6 +25,7 @@ size_t spec_ws_bytes(uint32_t S, uint32_t V, uint32_t K);
 size_t spec_diag_ws_bytes(uint32_t S, uint32_t V, uint32_t K);
 size_t spec_sampler_ws_bytes(uint32_t rows_t, uint32_t V, uint32_t top_k);
 size_t shard_draw_ws_bytes(uint32_t rows, uint32_t V);
+size_t spec_shard_draw_ws_bytes(uint32_t S, uint32_t V);
 
 // Candidates of full-row sampling (sel_sample with top_k = 0).
 constexpr uint32_t kFullRowCandidates = 64;

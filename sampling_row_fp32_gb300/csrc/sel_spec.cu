@@ -71,7 +71,8 @@ struct alignas(16) DrawPlan {
     uint32_t kind;   // kDraw*
     float pm, pinv;  // target row j*: max, 1 / sum exp((x - max) / T)
     float qm, qinv;  // draft row j* (residual draws only)
-    uint32_t pad0, pad1;
+    uint32_t uf_bits;  // shard plans: u_fin (float bits)
+    uint32_t c_bits;   // shard plans: log2(e) / T (float bits)
 };
 
 struct alignas(16) DrawPart {
@@ -125,6 +126,8 @@ struct SpecArgs {
     DrawPlan* plans;       // [S]
     uint32_t cmax;
     bool decide;           // run the acceptance chain (false: row statistics only)
+    bool want_tok;         // phase 1 stores the rows' logits at their draft tokens
+    uint32_t id_base;      // global id of the rows' first logit (a vocabulary shard's offset; 0 unsharded)
 };
 
 __device__ __forceinline__ bool beats(float v, uint32_t i, float w, uint32_t j) {
@@ -292,10 +295,11 @@ __global__ void __launch_bounds__(kNT, 6) spec_phase1_kernel(SpecArgs a) {
     // draft row have one); the block whose chunk holds it stores the logit
     // there for the acceptance chain (thread 0, at its end)
     uint32_t tok_t = 0xFFFFFFFFu;
-    if (kRej && a.decide && tid == 0) {
+    if (kRej && a.want_tok && tid == 0) {
         const uint32_t nt = a.S * (a.K + 1u);
         const uint32_t j = t.row < nt ? t.row - seq * (a.K + 1u) : (t.row - nt) - seq * a.K;
-        if (j < a.K) tok_t = a.tokens[static_cast<size_t>(seq) * a.K + j];
+        // on a shard, a token outside the slice wraps to an id past every chunk
+        if (j < a.K) tok_t = a.tokens[static_cast<size_t>(seq) * a.K + j] - a.id_base;
     }
 
     // nonfinite latch over the real quads (sum of x * 0 stays 0 unless some
@@ -591,6 +595,11 @@ struct DrawArgs {
     const DrawPlan* plans;
     DrawPart* parts;  // [S][cmax]
     uint32_t cmax;
+    // vocabulary shards (spec_shard_draw): every shard's residual and target
+    // masses [S][shard_G][2], this shard, and its slice's first global id
+    const double* shard_masses;
+    uint32_t shard_g, shard_G, id_base;
+    bool plan_c;  // take log2(e) / T from the plan (shard plans carry it)
 };
 
 // Phase 2: the inverse-CDF draw from the residual (or from p), in two
@@ -634,7 +643,7 @@ __device__ __forceinline__ void draw_chunk_sum(const DrawArgs& b, uint32_t s, ui
     const bool residual = d.kind == kDrawResidual;
     const float* prow = plan_prow(b, s, d);
     const float* qrow = residual ? plan_qrow(b, s, d) : nullptr;
-    const float c = b.log2e_over_T;
+    const float c = b.plan_c ? __uint_as_float(d.c_bits) : b.log2e_over_T;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr float kNegInf = -INFINITY;
     const float4 none = make_float4(kNegInf, kNegInf, kNegInf, kNegInf);
@@ -796,6 +805,8 @@ __global__ void __launch_bounds__(kNT) spec_draw_find_kernel(DrawArgs a) {
     __shared__ uint32_t s_cstar, s_cross;
     __shared__ int s_clast, s_lastid;
     __shared__ FF s_before, s_before_last;
+    __shared__ FF s_target;
+    __shared__ uint32_t s_other, s_use_p;
 
     const uint32_t chunks = a.chunks;
     const uint32_t s = blockIdx.x;
@@ -807,14 +818,58 @@ __global__ void __launch_bounds__(kNT) spec_draw_find_kernel(DrawArgs a) {
     // the plan, the first kNT chunk sums and u_fin, loaded together
     const DrawPlan d = a.plans[s];
     const DrawPart first = static_cast<uint32_t>(tid) < chunks ? parts[tid] : zero;
-    const float uf = a.u_fin[s];
+    const bool shard = a.shard_masses != nullptr;
+    const float uf = shard ? __uint_as_float(d.uf_bits) : a.u_fin[s];  // a shard plan carries u_fin
     if (d.kind == kDrawNone) return;  // invalid sequence
     const bool residual = d.kind == kDrawResidual;
+    uint32_t* out = a.emitted + static_cast<size_t>(s) * (a.K + 1u) + d.jstar;
     if (tid == 0) {
         s_cstar = kNoIdx;
         s_cross = kNoIdx;
         s_clast = -1;
         s_lastid = -1;
+        if (shard) {
+            // every shard's masses in shard order: the totals, then the
+            // shard the draw falls in (the first with mass whose inclusive
+            // prefix passes u_fin * total, else the last with mass) and the
+            // target relative to its start
+            const double* ms = a.shard_masses + static_cast<size_t>(s) * a.shard_G * 2u;
+            double rt = 0.0, pt = 0.0;
+            for (uint32_t g = 0; g < a.shard_G; ++g) {
+                rt += ms[2u * g];
+                pt += ms[2u * g + 1u];
+            }
+            const bool up = !(rt > 0.0);  // residual empty: draw from p
+            const double tg = static_cast<double>(uf) * (up ? pt : rt);
+            double run = 0.0, before_g = 0.0, before_last = 0.0;
+            uint32_t gstar = a.shard_G, glast = 0u;
+            for (uint32_t g = 0; g < a.shard_G; ++g) {
+                const double m = ms[2u * g + (up ? 1u : 0u)];
+                if (m > 0.0) {
+                    glast = g;
+                    before_last = run;
+                    if (gstar == a.shard_G && tg < run + m) {
+                        gstar = g;
+                        before_g = run;
+                    }
+                }
+                run += m;
+            }
+            if (gstar == a.shard_G) {
+                gstar = glast;
+                before_g = before_last;
+            }
+            s_other = gstar != a.shard_g ? 1u : 0u;
+            s_use_p = up ? 1u : 0u;
+            s_target = ff_from_double(tg - before_g);
+        }
+    }
+    if (shard) {
+        __syncthreads();
+        if (s_other) {
+            if (tid == 0) *out = SEL_OTHER_SHARD;
+            return;
+        }
     }
     FF ir, er, ip, ep, R, P;
     const bool one_group = chunks <= static_cast<uint32_t>(kNT);
@@ -833,8 +888,8 @@ __global__ void __launch_bounds__(kNT) spec_draw_find_kernel(DrawArgs a) {
             P = ff_add(P, tp);
         }
     }
-    const bool use_p = !(R.hi > 0.0f);  // residual empty by rounding: draw from p
-    const FF target = ff_mul_f(use_p ? P : R, uf);
+    const bool use_p = shard ? s_use_p != 0u : !(R.hi > 0.0f);  // residual empty by rounding: draw from p
+    const FF target = shard ? s_target : ff_mul_f(use_p ? P : R, uf);
 
     // the first chunk with mass whose inclusive prefix passes the target
     // (else, by rounding, the last chunk with mass)
@@ -876,7 +931,7 @@ __global__ void __launch_bounds__(kNT) spec_draw_find_kernel(DrawArgs a) {
     // the hit chunk, read again: thread t's ids [e0, e0 + kDrawPer)
     const float* prow = plan_prow(a, s, d);
     const float* qrow = residual ? plan_qrow(a, s, d) : nullptr;
-    const float c = a.log2e_over_T;
+    const float c = a.plan_c ? __uint_as_float(d.c_bits) : a.log2e_over_T;
     const uint32_t clo = cstar * a.chunk_elems;
     const uint32_t chi = min(a.V, clo + a.chunk_elems);
     const uint32_t e0 = clo + kDrawPer * static_cast<uint32_t>(tid);
@@ -920,7 +975,6 @@ __global__ void __launch_bounds__(kNT) spec_draw_find_kernel(DrawArgs a) {
     const uint32_t hit = __ballot_sync(kFull, tsum > 0.0f && ff_lt(target, incl));
     if (lane == 0 && hit) atomicMin(&s_cross, static_cast<uint32_t>(warp * 32 + __ffs(hit) - 1));
     __syncthreads();
-    uint32_t* out = a.emitted + static_cast<size_t>(s) * (a.K + 1u) + d.jstar;
     if (static_cast<uint32_t>(tid) == s_cross) {
         // the target's offset into this thread's mass
         const float off = ff_add(target, FF{-start.hi, -start.lo}).hi;
@@ -930,11 +984,11 @@ __global__ void __launch_bounds__(kNT) spec_draw_find_kernel(DrawArgs a) {
             if (w[j] > 0.0f) last = e0 + j;
             if (pick == kNoIdx && w[j] > 0.0f && off < cs[j]) pick = e0 + j;
         }
-        *out = pick != kNoIdx ? pick : last;
+        *out = (pick != kNoIdx ? pick : last) + a.id_base;
     }
     if (tid == 0 && s_cross == kNoIdx) {
         // no crossing (rounding): the last id with mass in the chunk
-        *out = s_lastid >= 0 ? static_cast<uint32_t>(s_lastid) : clo;
+        *out = (s_lastid >= 0 ? static_cast<uint32_t>(s_lastid) : clo) + a.id_base;
     }
 }
 
@@ -1127,6 +1181,7 @@ extern "C" sel_status spec_accept(const float* d_target, const float* d_draft, c
     a.plans = reinterpret_cast<DrawPlan*>(ws + l.plans);
     a.cmax = l.cmax_a;
     a.decide = true;
+    a.want_tok = true;
     const dim3 grid1(rows1 * chunks1);
     cudaError_t e1;
     if (rej) e1 = vec ? launch_pdl(spec_phase1_kernel<true, true>, grid1, dim3(kNT), 0, stream, a)
@@ -1249,4 +1304,355 @@ extern "C" sel_status spec_diagnostics(const float* d_target, const float* d_dra
     const cudaError_t e2 = vec ? launch_pdl(spec_diag_kernel<true>, grid2, dim3(kNT), 0, stream, d)
                                : launch_pdl(spec_diag_kernel<false>, grid2, dim3(kNT), 0, stream, d);
     return e2 == cudaSuccess ? SEL_OK : SEL_ECUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Speculative acceptance on vocabulary shards: each shard reduces its slice
+// of every row to a spec_shard_part, the gathered parts merge (in shard
+// order) into the row statistics the acceptance chain reads, and the draw
+// runs on the slices with every shard's mass known.
+// ---------------------------------------------------------------------------
+
+namespace sel {
+namespace {
+
+static_assert(sizeof(spec_shard_part) == 32, "spec_shard_part layout");
+static_assert(sizeof(spec_shard_plan) == sizeof(DrawPlan), "a shard plan is a DrawPlan");
+static_assert(SPEC_SHARD_MAX_K <= kPre, "the shard chain reads every position from its staged inputs");
+
+// Step 1's finishing launch: block s writes the parts of sequence s's rows
+// in chain order (target rows 0..K, then draft rows 0..K-1) from the row
+// statistics (rejection rule) or the argmax slots (argmax rule, which it
+// clears for the next call).
+template <bool kRej>
+__global__ void __launch_bounds__(kNT) spec_shard_parts_kernel(SpecArgs a, spec_shard_part* out) {
+    pdl_wait();
+    pdl_trigger();
+    const uint32_t s = blockIdx.x, K = a.K, rows_t = K + 1u, nrows = 2u * K + 1u;
+    for (uint32_t i = threadIdx.x; i < nrows; i += kNT) {
+        spec_shard_part p{};
+        const uint32_t r = seq_row(a, s, i);
+        const uint32_t j = i < rows_t ? i : i - rows_t;  // the row's position
+        if (kRej) {
+            const RowPart m = a.row_stats[r];
+            p.max = m.m;
+            p.idx = m.idx;
+            p.z = static_cast<double>(m.s_hi) + static_cast<double>(m.s_lo);
+            if (j < K) {
+                const uint32_t local = a.tokens[static_cast<size_t>(s) * K + j] - a.id_base;
+                if (local < a.V) {
+                    p.has_tok = 1u;
+                    p.x_tok = a.tok_logit[r];
+                }
+            }
+        } else if (i < rows_t) {
+            const unsigned long long key = a.slots[r];
+            a.slots[r] = 0ull;  // for the next call
+            if (key == ~0ull) {
+                p.max = __uint_as_float(0x7fc00000u);
+                p.idx = kNonfiniteBit;
+            } else {
+                p.max = key2f(static_cast<uint32_t>(key >> 32));
+                p.idx = ~static_cast<uint32_t>(key) + a.id_base;
+            }
+        }
+        out[static_cast<size_t>(s) * nrows + i] = p;
+    }
+}
+
+struct SpecShardArgs {
+    const spec_shard_part* parts;  // [S][G][2K+1]
+    spec_shard_plan* plans;        // [S] (rejection rule)
+    uint32_t G;
+    uint32_t off[SEL_MAX_SHARDS + 1];
+};
+
+// Step 3: block s merges the gathered parts of sequence s's rows (one thread
+// per row, shards in order: the maximum, its lowest global id, the
+// normaliser rescaled to the row's maximum, the token logit from the one
+// shard that holds it), then runs the acceptance chain of spec_accept on
+// them and, in the rejection rule, stores the draw plan with u_fin.
+template <bool kRej>
+__global__ void __launch_bounds__(kNT) spec_accept_shards_kernel(SpecArgs a, SpecShardArgs sh) {
+    __shared__ ChainPre pre;
+    __shared__ RowPart rs[kChainRows];
+    __shared__ float xtok[kChainRows];
+    pdl_wait();
+    pdl_trigger();
+    const uint32_t s = blockIdx.x, K = a.K, rows_t = K + 1u, nrows = 2u * K + 1u;
+    const uint32_t tid = threadIdx.x;
+    const uint32_t nr = kRej ? nrows : rows_t;
+    for (uint32_t i = tid; i < nr; i += kNT) {
+        const spec_shard_part* pp = sh.parts + static_cast<size_t>(s) * sh.G * nrows + i;
+        const uint32_t j = i < rows_t ? i : i - rows_t;
+        float M = -INFINITY;
+        uint32_t idx = kNoIdx, nf = 0u, holders = 0u;
+        float xt = 0.0f;
+        for (uint32_t g = 0; g < sh.G; ++g) {
+            const spec_shard_part p = pp[static_cast<size_t>(g) * nrows];
+            nf |= p.idx & kNonfiniteBit;
+            const uint32_t id = p.idx & ~kNonfiniteBit;
+            if (beats(p.max, id, M, idx)) {
+                M = p.max;
+                idx = id;
+            }
+            if (p.has_tok) {
+                ++holders;
+                xt = p.x_tok;
+            }
+        }
+        double Z = 0.0;
+        if (kRej && !nf) {
+            for (uint32_t g = 0; g < sh.G; ++g) {
+                const spec_shard_part p = pp[static_cast<size_t>(g) * nrows];
+                Z += p.z * exp((static_cast<double>(p.max) - static_cast<double>(M)) / static_cast<double>(a.T));
+            }
+            // a draft token inside the row has its logit on exactly one shard
+            if (j < K && a.tokens[static_cast<size_t>(s) * K + j] < a.V && holders != 1u) nf = kNonfiniteBit;
+        }
+        rs[i] = RowPart{M, idx | nf, static_cast<float>(Z), 0.0f};
+        xtok[i] = xt;
+    }
+    // the chain inputs (K <= kPre: every position reads them from `pre`)
+    if (tid == 0) pre.uf = kRej ? a.u_fin[s] : 0.0f;
+    for (uint32_t j = tid; j < K; j += kNT) pre.tok[j] = a.tokens[static_cast<size_t>(s) * K + j];
+    if (kRej)
+        for (uint32_t j = tid; j < K; j += kNT) pre.u[j] = a.u_acc[static_cast<size_t>(s) * K + j];
+    __syncthreads();
+    if (kRej)
+        for (uint32_t j = tid; j < K; j += kNT) {
+            pre.xt[j] = xtok[j];
+            pre.xd[j] = xtok[rows_t + j];
+        }
+    __syncthreads();
+    if (tid < 32) {
+        const uint32_t n = decide_sequence<kRej>(a, s, pre, rs, rs + rows_t, true);
+        if (kRej && tid == 0) {
+            DrawPlan d = make_plan(n, K, rs, rs + rows_t);
+            d.uf_bits = __float_as_uint(pre.uf);
+            d.c_bits = __float_as_uint(a.log2e_over_T);
+            reinterpret_cast<DrawPlan*>(sh.plans)[s] = d;
+        }
+    }
+}
+
+// Step 4a's finishing launch: sequence s's residual and target masses of
+// this slice, the chunk sums added in chunk order (one warp).
+__global__ void __launch_bounds__(32) spec_shard_mass_kernel(DrawArgs b, double* mass) {
+    pdl_wait();
+    pdl_trigger();
+    const uint32_t s = blockIdx.x;
+    const int lane = threadIdx.x;
+    double* m = mass + 2u * static_cast<size_t>(s);
+    if (b.plans[s].kind == kDrawNone) {
+        if (lane == 0) { m[0] = 0.0; m[1] = 0.0; }
+        return;
+    }
+    const DrawPart* parts = b.parts + static_cast<size_t>(s) * b.cmax;
+    FF R{0.0f, 0.0f}, P{0.0f, 0.0f};
+    for (uint32_t c0 = 0; c0 < b.chunks; c0 += 32u) {
+        const uint32_t ci = c0 + lane;
+        const DrawPart v = ci < b.chunks ? parts[ci] : DrawPart{FF{0.0f, 0.0f}, FF{0.0f, 0.0f}};
+        R = ff_add(R, ff_warp_sum(v.r));
+        P = ff_add(P, ff_warp_sum(v.p));
+    }
+    if (lane == 0) {
+        m[0] = static_cast<double>(R.hi) + static_cast<double>(R.lo);
+        m[1] = static_cast<double>(P.hi) + static_cast<double>(P.lo);
+    }
+}
+
+// The draw workspace of a shard: the error word, then the chunk sums.
+struct SpecShardDrawLayout {
+    size_t parts, total;
+    uint32_t chunks;
+};
+SpecShardDrawLayout spec_shard_draw_layout(uint32_t S, uint32_t V) {
+    SpecShardDrawLayout l{};
+    l.chunks = ceil_div(V, kDrawChunkMax);
+    l.parts = kWsHeaderBytes;
+    l.total = l.parts + align_up(static_cast<size_t>(S) * l.chunks * sizeof(DrawPart), 256);
+    return l;
+}
+
+// Arguments shared by the two draw calls of a shard.
+sel_status spec_shard_draw_args(const float* d_target, const float* d_draft, uint32_t S, uint32_t K, uint32_t V,
+                                const spec_shard_plan* d_plan, void* d_ws, size_t ws_bytes, DrawArgs& b,
+                                bool& vec) {
+    if (V == 0 || V > SEL_MAX_V || K > SPEC_SHARD_MAX_K) return SEL_EINVAL;
+    if (S == 0) return SEL_OK;
+    if (!d_target || !d_plan || !d_ws || (K > 0 && !d_draft)) return SEL_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(d_target) | reinterpret_cast<uintptr_t>(d_draft)) % 4 ||
+        reinterpret_cast<uintptr_t>(d_plan) % 16 || reinterpret_cast<uintptr_t>(d_ws) % SEL_WS_ALIGN)
+        return SEL_EINVAL;
+    const SpecShardDrawLayout l = spec_shard_draw_layout(S, V);
+    if (ws_bytes < l.total) return SEL_EWORKSPACE;
+    if (static_cast<uint64_t>(S) * l.chunks > 0x7fffffffull) return SEL_EUNSUPPORTED;
+    b.target = d_target;
+    b.draft = d_draft;
+    b.S = S;
+    b.K = K;
+    b.V = V;
+    b.chunks = l.chunks;
+    b.chunk_elems = kDrawChunkMax;
+    b.plans = reinterpret_cast<const DrawPlan*>(d_plan);
+    b.parts = reinterpret_cast<DrawPart*>(static_cast<char*>(d_ws) + l.parts);
+    b.cmax = l.chunks;
+    b.plan_c = true;  // log2(e) / T travels in the plan
+    vec = V % 4 == 0 && reinterpret_cast<uintptr_t>(d_target) % 16 == 0 &&
+          (K == 0 || reinterpret_cast<uintptr_t>(d_draft) % 16 == 0);
+    return SEL_OK;
+}
+
+}  // namespace
+
+size_t spec_shard_draw_ws_bytes(uint32_t S, uint32_t V) {
+    if (S == 0 || V == 0) return 0;
+    return spec_shard_draw_layout(S, V).total;
+}
+
+}  // namespace sel
+
+extern "C" sel_status spec_shard_stats(const float* d_target, const float* d_draft, const uint32_t* d_draft_tokens,
+                                       uint32_t S, uint32_t K, uint32_t V, uint32_t offset, const spec_params* p,
+                                       spec_shard_part* d_parts, void* d_ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!p || V == 0 || V > SEL_MAX_V || offset > SEL_MAX_V - V) return SEL_EINVAL;
+    if (!(p->temperature >= 0.0f) || !(p->temperature < INFINITY)) return SEL_EINVAL;
+    if (p->mode != SPEC_MODE_REJECTION && p->mode != SPEC_MODE_ARGMAX) return SEL_EINVAL;
+    if (K > SPEC_SHARD_MAX_K) return SEL_EUNSUPPORTED;
+    if (S == 0) return SEL_OK;
+    const bool rej = p->mode == SPEC_MODE_REJECTION && p->temperature > 0.0f;
+    if (!d_target || !d_parts || (K > 0 && !d_draft_tokens) || (rej && K > 0 && !d_draft)) return SEL_EINVAL;
+    const uintptr_t mis = reinterpret_cast<uintptr_t>(d_target) | reinterpret_cast<uintptr_t>(d_draft_tokens) |
+                          (rej ? reinterpret_cast<uintptr_t>(d_draft) : 0u);
+    if (mis % 4 || reinterpret_cast<uintptr_t>(d_parts) % 8) return SEL_EINVAL;
+    const uint64_t rows_a = static_cast<uint64_t>(S) * (2ull * K + 1ull);
+    if (rows_a > 0x7fffffffull) return SEL_EUNSUPPORTED;
+    const SpecLayout l = spec_layout(S, V, K);
+    if (!d_ws) return SEL_EINVAL;
+    if (reinterpret_cast<uintptr_t>(d_ws) % SEL_WS_ALIGN) return SEL_EINVAL;
+    if (ws_bytes < l.total) return SEL_EWORKSPACE;
+    const int sms = device_sms();
+    if (sms <= 0) return SEL_ECUDA;
+    char* ws = static_cast<char*>(d_ws);
+    const uint32_t rows1 = rej ? static_cast<uint32_t>(rows_a) : S * (K + 1u);
+    const bool vec = V % 4 == 0 && reinterpret_cast<uintptr_t>(d_target) % 16 == 0 &&
+                     (!rej || K == 0 || reinterpret_cast<uintptr_t>(d_draft) % 16 == 0);
+    const uint32_t ce1 = plan_unit(rows1, V, kGrain, kUnitMax, 2ull * static_cast<uint64_t>(sms));
+    const uint32_t chunks1 = ceil_div(V, ce1);
+    if (static_cast<uint64_t>(rows1) * chunks1 > 0x7fffffffull) return SEL_EUNSUPPORTED;
+    SpecArgs a{};
+    a.target = d_target;
+    a.draft = d_draft;
+    a.tokens = d_draft_tokens;
+    a.S = S; a.K = K; a.V = V;
+    a.T = rej ? p->temperature : 1.0f;
+    a.log2e_over_T = static_cast<float>(1.4426950408889634 / static_cast<double>(a.T));
+    a.chunks = chunks1;
+    a.chunk_elems = ce1;
+    a.err = reinterpret_cast<uint32_t*>(ws);
+    a.row_ctr = reinterpret_cast<uint32_t*>(ws + l.row_ctr);
+    a.seq_ctr = reinterpret_cast<uint32_t*>(ws + l.seq_ctr_a);
+    a.row_parts = reinterpret_cast<RowPart*>(ws + l.row_parts);
+    a.row_stats = reinterpret_cast<RowPart*>(ws + l.row_stats);
+    a.slots = reinterpret_cast<unsigned long long*>(ws + l.slots);
+    a.tok_logit = reinterpret_cast<float*>(ws + l.tok_logit);
+    a.plans = reinterpret_cast<DrawPlan*>(ws + l.plans);
+    a.cmax = l.cmax_a;
+    a.decide = false;
+    a.want_tok = true;
+    a.id_base = offset;
+    const dim3 grid1(rows1 * chunks1);
+    cudaError_t e;
+    if (rej) {
+        e = vec ? launch_pdl(spec_phase1_kernel<true, true>, grid1, dim3(kNT), 0, stream, a)
+                : launch_pdl(spec_phase1_kernel<false, true>, grid1, dim3(kNT), 0, stream, a);
+        if (e != cudaSuccess) return SEL_ECUDA;
+        e = launch_pdl(spec_rows_kernel<true>, dim3(S), dim3(kNT), 0, stream, a);  // row statistics only
+        if (e != cudaSuccess) return SEL_ECUDA;
+        e = launch_pdl(spec_shard_parts_kernel<true>, dim3(S), dim3(kNT), 0, stream, a, d_parts);
+    } else {
+        e = vec ? launch_pdl(spec_phase1_kernel<true, false>, grid1, dim3(kNT), 0, stream, a)
+                : launch_pdl(spec_phase1_kernel<false, false>, grid1, dim3(kNT), 0, stream, a);
+        if (e != cudaSuccess) return SEL_ECUDA;
+        e = launch_pdl(spec_shard_parts_kernel<false>, dim3(S), dim3(kNT), 0, stream, a, d_parts);
+    }
+    return e == cudaSuccess ? SEL_OK : SEL_ECUDA;
+}
+
+extern "C" sel_status spec_accept_shards(const spec_shard_part* d_parts, const uint32_t* d_draft_tokens, uint32_t S,
+                                         uint32_t K, uint32_t G, const uint32_t* h_offsets, const spec_params* p,
+                                         const float* d_u_acc, const float* d_u_fin, uint32_t* d_accepted,
+                                         uint32_t* d_emitted, spec_shard_plan* d_plan, cudaStream_t stream) {
+    if (!p || G == 0 || G > SEL_MAX_SHARDS || !h_offsets) return SEL_EINVAL;
+    if (!(p->temperature >= 0.0f) || !(p->temperature < INFINITY)) return SEL_EINVAL;
+    if (p->mode != SPEC_MODE_REJECTION && p->mode != SPEC_MODE_ARGMAX) return SEL_EINVAL;
+    if (h_offsets[0] != 0u) return SEL_EINVAL;
+    for (uint32_t g = 0; g < G; ++g)
+        if (h_offsets[g + 1] <= h_offsets[g]) return SEL_EINVAL;
+    if (h_offsets[G] > SEL_MAX_V) return SEL_EINVAL;
+    if (K > SPEC_SHARD_MAX_K) return SEL_EUNSUPPORTED;
+    if (S == 0) return SEL_OK;
+    const bool rej = p->mode == SPEC_MODE_REJECTION && p->temperature > 0.0f;
+    if (!d_parts || !d_accepted || !d_emitted || (K > 0 && !d_draft_tokens)) return SEL_EINVAL;
+    if (rej && (!d_u_fin || !d_plan || (K > 0 && !d_u_acc))) return SEL_EINVAL;
+    const uintptr_t mis = reinterpret_cast<uintptr_t>(d_accepted) | reinterpret_cast<uintptr_t>(d_emitted) |
+                          reinterpret_cast<uintptr_t>(d_draft_tokens) |
+                          (rej ? reinterpret_cast<uintptr_t>(d_u_acc) | reinterpret_cast<uintptr_t>(d_u_fin) : 0u);
+    if (mis % 4 || reinterpret_cast<uintptr_t>(d_parts) % 8 || (rej && reinterpret_cast<uintptr_t>(d_plan) % 16))
+        return SEL_EINVAL;
+    SpecArgs a{};
+    a.tokens = d_draft_tokens;
+    a.u_acc = d_u_acc;
+    a.u_fin = d_u_fin;
+    a.accepted = d_accepted;
+    a.emitted = d_emitted;
+    a.S = S; a.K = K; a.V = h_offsets[G];
+    a.T = rej ? p->temperature : 1.0f;
+    a.log2e_over_T = static_cast<float>(1.4426950408889634 / static_cast<double>(a.T));
+    SpecShardArgs sh{};
+    sh.parts = d_parts;
+    sh.plans = d_plan;
+    sh.G = G;
+    for (uint32_t g = 0; g <= G; ++g) sh.off[g] = h_offsets[g];
+    const cudaError_t e = rej ? launch_pdl(spec_accept_shards_kernel<true>, dim3(S), dim3(kNT), 0, stream, a, sh)
+                              : launch_pdl(spec_accept_shards_kernel<false>, dim3(S), dim3(kNT), 0, stream, a, sh);
+    return e == cudaSuccess ? SEL_OK : SEL_ECUDA;
+}
+
+extern "C" sel_status spec_shard_draw_mass(const float* d_target, const float* d_draft, uint32_t S, uint32_t K,
+                                           uint32_t V, const spec_shard_plan* d_plan, double* d_mass, void* d_ws,
+                                           size_t ws_bytes, cudaStream_t stream) {
+    DrawArgs b{};
+    bool vec = false;
+    const sel_status st = spec_shard_draw_args(d_target, d_draft, S, K, V, d_plan, d_ws, ws_bytes, b, vec);
+    if (st != SEL_OK || S == 0) return st;
+    if (!d_mass || reinterpret_cast<uintptr_t>(d_mass) % 8) return SEL_EINVAL;
+    cudaError_t e = vec ? launch_pdl(spec_draw_sum_kernel<true>, dim3(S * b.chunks), dim3(kNT), 0, stream, b)
+                        : launch_pdl(spec_draw_sum_kernel<false>, dim3(S * b.chunks), dim3(kNT), 0, stream, b);
+    if (e != cudaSuccess) return SEL_ECUDA;
+    e = launch_pdl(spec_shard_mass_kernel, dim3(S), dim3(32), 0, stream, b, d_mass);
+    return e == cudaSuccess ? SEL_OK : SEL_ECUDA;
+}
+
+extern "C" sel_status spec_shard_draw(const float* d_target, const float* d_draft, uint32_t S, uint32_t K, uint32_t V,
+                                      uint32_t offset, uint32_t g, uint32_t G, const spec_shard_plan* d_plan,
+                                      const double* d_masses, uint32_t* d_emitted, void* d_ws, size_t ws_bytes,
+                                      cudaStream_t stream) {
+    if (G == 0 || G > SEL_MAX_SHARDS || g >= G) return SEL_EINVAL;
+    if (V > 0 && offset > SEL_MAX_V - V) return SEL_EINVAL;
+    DrawArgs b{};
+    bool vec = false;
+    const sel_status st = spec_shard_draw_args(d_target, d_draft, S, K, V, d_plan, d_ws, ws_bytes, b, vec);
+    if (st != SEL_OK || S == 0) return st;
+    if (!d_masses || !d_emitted) return SEL_EINVAL;
+    if (reinterpret_cast<uintptr_t>(d_masses) % 8 || reinterpret_cast<uintptr_t>(d_emitted) % 4) return SEL_EINVAL;
+    b.emitted = d_emitted;
+    b.shard_masses = d_masses;
+    b.shard_g = g;
+    b.shard_G = G;
+    b.id_base = offset;
+    const cudaError_t e = vec ? launch_pdl(spec_draw_find_kernel<true>, dim3(S), dim3(kNT), 0, stream, b)
+                              : launch_pdl(spec_draw_find_kernel<false>, dim3(S), dim3(kNT), 0, stream, b);
+    return e == cudaSuccess ? SEL_OK : SEL_ECUDA;
 }

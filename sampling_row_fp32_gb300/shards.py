@@ -29,6 +29,14 @@ one read of the slice):
   each shard runs `sel_shard_draw` (the shard the draw falls in writes the
   global id, the others SEL_OTHER_SHARD and probability 0), and
   `combine_draws` all-reduces them (minimum id, summed probability).
+
+Speculative acceptance on shards follows the same pattern: `spec_shard_stats`
+reduces each slice of every target and draft row to a 32-byte part (max,
+normaliser, first argmax id, logit at the draft token), `gather_parts`
+all-gathers them, `spec_accept_shards` runs the acceptance chain on every
+rank, and, in the rejection rule, the residual draw runs on the slices
+(`spec_shard_draw_mass`, `gather_masses`, `spec_shard_draw`) before
+`combine_emitted` all-reduces the emitted tokens (minimum).
 """
 from __future__ import annotations
 
@@ -151,3 +159,43 @@ def combine_draws_local(ids: list[torch.Tensor], probs: list[torch.Tensor]):
     i = torch.stack([_ids64(t) for t in ids]).min(dim=0).values
     p = torch.stack(probs).sum(dim=0)
     return i, p
+
+
+def gather_parts(parts: torch.Tensor, group=None) -> torch.Tensor:
+    """All-gather this rank's [S][2K+1][32] spec parts into [S][G][2K+1][32]."""
+    import torch.distributed as dist
+
+    world = dist.get_world_size(group)
+    if parts.dim() != 3 or parts.shape[2] != 32 or parts.dtype != torch.uint8:
+        raise ValueError("parts must be [S, 2K+1, 32] uint8")
+    out = [torch.empty_like(parts) for _ in range(world)]
+    dist.all_gather(out, parts.contiguous(), group=group)
+    return torch.stack(out, dim=1).contiguous()
+
+
+def gather_spec_masses(mass: torch.Tensor, group=None) -> torch.Tensor:
+    """All-gather this rank's [S][2] float64 draw masses into [S][G][2]."""
+    import torch.distributed as dist
+
+    world = dist.get_world_size(group)
+    if mass.dim() != 2 or mass.shape[1] != 2 or mass.dtype != torch.float64:
+        raise ValueError("mass must be [S, 2] float64")
+    out = [torch.empty_like(mass) for _ in range(world)]
+    dist.all_gather(out, mass.contiguous(), group=group)
+    return torch.stack(out, dim=1).contiguous()
+
+
+def combine_emitted(emitted: torch.Tensor, group=None) -> torch.Tensor:
+    """All-reduce (minimum) the ranks' emitted tokens after spec_shard_draw:
+    the drawn token's shard holds its global id, the others SEL_OTHER_SHARD.
+    Returns int64 holding the uint32 values."""
+    import torch.distributed as dist
+
+    e = _ids64(emitted)
+    dist.all_reduce(e, op=dist.ReduceOp.MIN, group=group)
+    return e
+
+
+def combine_emitted_local(emitted: list[torch.Tensor]) -> torch.Tensor:
+    """combine_emitted for shards held by one process."""
+    return torch.stack([_ids64(e) for e in emitted]).min(dim=0).values

@@ -63,7 +63,7 @@ def test_workspace_sizes_are_host_only_and_monotone(lib):
     assert B.sel_workspace_bytes(B.SEL_OP_TOPK, 1, 10, 11) == 0       # k > V
     assert B.sel_workspace_bytes(B.SEL_OP_SAMPLE, 64, 202_048, 40) == \
         B.sel_workspace_bytes(B.SEL_OP_TOPK, 64, 202_048, 40)
-    assert B.sel_workspace_bytes(7, 1, 10, 1) == 0                    # unknown op
+    assert B.sel_workspace_bytes(8, 1, 10, 1) == 0                    # unknown op
 
 
 def test_host_validation_needs_no_gpu(lib):
@@ -188,6 +188,56 @@ def test_shard_stats_and_draw_validation_needs_no_gpu(lib):
     assert d(fake, 3, 100_000, 0, 0, 2, fake, vp(0x10004), fake, fake, fake, n, None) == B.SEL_EINVAL
     assert d(fake, 3, 100_000, 0, 0, 2, fake, fake, fake, fake, fake, 16, None) == B.SEL_EWORKSPACE
     assert d(fake, 0, 100_000, 0, 0, 2, None, None, None, None, None, 0, None) == B.SEL_OK
+
+
+def test_spec_shard_validation_needs_no_gpu(lib):
+    from sampling_row_fp32_gb300 import binding as B
+    vp = ctypes.c_void_p
+    fake = vp(0x10000)
+    U = ctypes.c_uint32
+    rej = ctypes.byref(B.SpecParams(1.0, B.SPEC_MODE_REJECTION))
+    arg = ctypes.byref(B.SpecParams(1.0, B.SPEC_MODE_ARGMAX))
+    n = B.sel_workspace_bytes(B.SEL_OP_SPEC, 4, 1000, 3)
+    st = lib.spec_shard_stats
+    # (target, draft, tokens, S, K, V, offset, params, parts, ws, ws_bytes, stream)
+    assert st(fake, fake, fake, 0, 3, 1000, 0, rej, fake, fake, n, None) == B.SEL_OK             # S = 0
+    assert st(fake, fake, fake, 4, 65, 1000, 0, rej, fake, fake, n, None) == B.SEL_EUNSUPPORTED  # K > 64
+    assert st(fake, fake, fake, 4, 3, 0, 0, rej, fake, fake, n, None) == B.SEL_EINVAL            # V = 0
+    assert st(fake, fake, fake, 4, 3, 1000, 0x7FFFFFFF, rej, fake, fake, n, None) == B.SEL_EINVAL
+    assert st(fake, None, fake, 4, 3, 1000, 0, rej, fake, fake, n, None) == B.SEL_EINVAL         # no draft
+    assert st(fake, fake, fake, 4, 3, 1000, 0, rej, None, fake, n, None) == B.SEL_EINVAL         # no parts
+    assert st(fake, fake, fake, 4, 3, 1000, 0, rej, vp(0x10004), fake, n, None) == B.SEL_EINVAL
+    assert st(fake, fake, fake, 4, 3, 1000, 0, rej, fake, fake, n - 1, None) == B.SEL_EWORKSPACE
+    assert st(fake, fake, fake, 4, 3, 1000, 0, None, fake, fake, n, None) == B.SEL_EINVAL
+    acc = lib.spec_accept_shards
+    offs = ctypes.cast((U * 3)(0, 500, 1000), vp)
+    # (parts, tokens, S, K, G, offsets, params, u_acc, u_fin, accepted, emitted, plan, stream)
+    assert acc(fake, fake, 0, 3, 2, offs, rej, fake, fake, fake, fake, fake, None) == B.SEL_OK
+    assert acc(fake, fake, 4, 3, 0, offs, rej, fake, fake, fake, fake, fake, None) == B.SEL_EINVAL
+    assert acc(fake, fake, 4, 3, 2, ctypes.cast((U * 3)(1, 500, 1000), vp), rej, fake, fake, fake, fake, fake,
+               None) == B.SEL_EINVAL                                                            # not from 0
+    assert acc(fake, fake, 4, 3, 2, ctypes.cast((U * 3)(0, 500, 500), vp), rej, fake, fake, fake, fake, fake,
+               None) == B.SEL_EINVAL                                                            # empty shard
+    assert acc(fake, fake, 4, 65, 2, offs, rej, fake, fake, fake, fake, fake, None) == B.SEL_EUNSUPPORTED
+    assert acc(fake, fake, 4, 3, 2, offs, rej, fake, fake, fake, fake, None, None) == B.SEL_EINVAL  # no plan
+    assert acc(fake, fake, 4, 3, 2, offs, rej, fake, None, fake, fake, fake, None) == B.SEL_EINVAL  # no u_fin
+    assert acc(fake, fake, 4, 3, 2, offs, rej, fake, fake, fake, fake, vp(0x10008), None) == B.SEL_EINVAL
+    n2 = B.sel_workspace_bytes(B.SEL_OP_SPEC_SHARD_DRAW, 4, 500, 0)
+    assert n2 > 0
+    m = lib.spec_shard_draw_mass
+    # (target, draft, S, K, V, plan, mass, ws, ws_bytes, stream)
+    assert m(fake, fake, 0, 3, 500, fake, fake, fake, n2, None) == B.SEL_OK
+    assert m(fake, fake, 4, 3, 500, None, fake, fake, n2, None) == B.SEL_EINVAL
+    assert m(fake, fake, 4, 3, 500, fake, None, fake, n2, None) == B.SEL_EINVAL
+    assert m(fake, fake, 4, 3, 500, fake, fake, fake, n2 - 1, None) == B.SEL_EWORKSPACE
+    assert m(fake, fake, 4, 65, 500, fake, fake, fake, n2, None) == B.SEL_EINVAL
+    d = lib.spec_shard_draw
+    # (target, draft, S, K, V, offset, g, G, plan, masses, emitted, ws, ws_bytes, stream)
+    assert d(fake, fake, 4, 3, 500, 500, 2, 2, fake, fake, fake, fake, n2, None) == B.SEL_EINVAL  # g >= G
+    assert d(fake, fake, 4, 3, 500, 500, 1, 2, fake, None, fake, fake, n2, None) == B.SEL_EINVAL
+    assert d(fake, fake, 4, 3, 500, 500, 1, 2, fake, fake, None, fake, n2, None) == B.SEL_EINVAL
+    assert d(fake, fake, 4, 3, 500, 500, 1, 2, fake, fake, fake, fake, 16, None) == B.SEL_EWORKSPACE
+    assert d(fake, fake, 0, 3, 500, 500, 1, 2, None, None, None, None, 0, None) == B.SEL_OK
 
 
 def test_eog_validation_needs_no_gpu(lib):

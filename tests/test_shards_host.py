@@ -151,3 +151,47 @@ def test_full_row_list_len_and_local_combine():
     ci, cp = shards.combine_draws_local(ids, probs)
     assert ci.tolist() == [9, 3, 0xFFFFFFFF]
     assert cp[0] == 0.75 and cp[1] == 0.5 and torch.isnan(cp[2])
+
+
+def _rank_spec_main(rank, world, port, out_dir):
+    """Each rank: its spec parts (bytes that name the rank), its draw masses,
+    and an emitted array in which it holds the drawn token of some
+    sequences; then the gathers and the combine."""
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        S, K = 3, 2
+        parts = torch.full((S, 2 * K + 1, 32), rank + 1, dtype=torch.uint8)
+        gp = shards.gather_parts(parts)
+        mass = torch.tensor([[0.25 * rank, 1.0], [0.0, 0.5 + rank], [3.0, 3.0]], dtype=torch.float64)
+        gm = shards.gather_spec_masses(mass)
+        # every rank wrote t_0..t_{n-1} the same way; the drawn slot (n) holds
+        # the token on one rank and SEL_OTHER_SHARD on the others
+        other = shards.OTHER_SHARD
+        inv = 0xFFFFFFFF
+        rows = [[11, 12, 900 if rank == 1 else other],
+                [40 if rank == 0 else other, inv, inv],
+                [inv, inv, inv]]
+        em = torch.from_numpy(np.array(rows, dtype=np.uint32).view(np.int32))
+        ce = shards.combine_emitted(em)
+        np.save(os.path.join(out_dir, f"gp{rank}.npy"), gp.numpy())
+        np.save(os.path.join(out_dir, f"gm{rank}.npy"), gm.numpy())
+        np.save(os.path.join(out_dir, f"ce{rank}.npy"), ce.numpy())
+    finally:
+        dist.destroy_process_group()
+
+
+def test_spec_parts_masses_and_emitted_between_two_ranks(tmp_path):
+    world = 2
+    mp.start_processes(_rank_spec_main, args=(world, _free_port(), str(tmp_path)),
+                       nprocs=world, join=True, start_method="spawn")
+    for rank in range(world):
+        gp = np.load(tmp_path / f"gp{rank}.npy")
+        assert gp.shape == (3, world, 5, 32)
+        assert np.all(gp[:, 0] == 1) and np.all(gp[:, 1] == 2)  # shard order = rank order
+        gm = np.load(tmp_path / f"gm{rank}.npy")
+        assert gm.shape == (3, world, 2)
+        assert np.array_equal(gm[0], [[0.0, 1.0], [0.25, 1.0]]) and np.array_equal(gm[1], [[0.0, 0.5], [0.0, 1.5]])
+        ce = np.load(tmp_path / f"ce{rank}.npy")
+        assert ce.tolist() == [[11, 12, 900], [40, 0xFFFFFFFF, 0xFFFFFFFF], [0xFFFFFFFF] * 3]
