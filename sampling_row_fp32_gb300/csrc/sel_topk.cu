@@ -174,6 +174,8 @@ struct TopkArgs {
     uint32_t stride, list_len;
     uint32_t* err;
     uint32_t V, chunks, chunk_elems;
+    unsigned long long chunks_magic;  // b / chunks = (b * chunks_magic) >> (32 + chunks_shift)
+    uint32_t chunks_shift;
     SampleArgs sa;
 };
 
@@ -804,48 +806,21 @@ __device__ __forceinline__ void write_row(const uint64_t* sorted, float* scratch
     }
 }
 
-// The main launch: one block per row chunk. Each stores its chunk list and
-// nonfinite flag, and folds its bound into the row's slot (atomic max). The
-// chunk is staged in shared memory (one bulk copy for aligned rows), so a
-// survivor's value is read back by its offset.
-template <bool kVec, bool kExtra, bool kSmall>
-__global__ void __launch_bounds__(kNT, kSmall ? 6 : 5) topk_kernel(TopkArgs a) {
-    constexpr uint32_t kCapB = kSmall ? kBlockCapSmall : kBlockCap;
-    extern __shared__ float4 stage[];  // the chunk: kUnitMax floats
-    __shared__ ChunkShared<kCapB> s;
-    __shared__ uint64_t bar;
+// The work of the main launch on one row chunk, staged in shared memory
+// (`stage`: the chunk's n_real logits; scalar rows pad the rest of the unit
+// with -FLT_MAX). The block stores the chunk's list, its pool entries and
+// its nonfinite flag, and folds its bound into the row's slot (atomic max);
+// a survivor's value is read back from the stage by its offset. Ends with
+// the stage and `s` still in use by the list store: the caller syncs before
+// reusing them.
+template <bool kVec, bool kExtra, bool kSmall, uint32_t kCapB>
+__device__ __forceinline__ void topk_chunk(const TopkArgs& a, ChunkShared<kCapB>& s, float4* stage,
+                                           const BlockUnit t) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t V = a.V, k = a.k;
-    if (kVec) {
-        if (tid == 0) mbar_init(&bar, 1);
-        __syncthreads();  // the barrier is initialised before anyone polls it
-    }
-    pdl_wait();
-    const BlockUnit t = block_unit(a.chunks, a.chunk_elems, V);
     const uint32_t n_real = t.hi - t.lo;
     const float* rowp = a.logits + static_cast<size_t>(t.row) * V;
     const float* sf = reinterpret_cast<const float*>(stage);
-    if (kVec) {
-        // 16-byte aligned row, V % 4 == 0: the chunk is whole quads
-        if (tid == 0) bulk_load(stage, rowp + t.lo, n_real * 4u, &bar);
-        pdl_trigger();
-        const bool ok = mbar_wait(&bar, 0);
-        if (__syncthreads_or(!ok)) {
-            // the copy engine stopped answering: record it, wait (bounded)
-            // for the copy still in flight, and leave
-            if (tid == 0) {
-                atomicOr(a.err, kErrTimeout);
-                mbar_wait(&bar, 0);
-            }
-            return;
-        }
-    } else {
-        float4 q[kVPT];
-        load_unit<kNT, kVPT, false>(rowp, t.lo, t.hi, -FLT_MAX, q);
-        pdl_trigger();
-#pragma unroll
-        for (int sl = 0; sl < kVPT; ++sl) stage[tid + kNT * sl] = q[sl];
-    }
     if (tid == 0) s.count = 0;
 
     // The thread's largest value and the nonfinite latch (sum of x * 0 stays
@@ -1035,16 +1010,10 @@ __global__ void __launch_bounds__(kNT, kSmall ? 6 : 5) topk_kernel(TopkArgs a) {
             if (o + 4u > n_real) m4 &= o < n_real ? (1u << (n_real - o)) - 1u : 0u;
             marks |= m4 << (4u * sl);
         }
+        // a chunk has few survivors: each thread holding some reserves its
+        // slots with one shared atomic (the list is unordered)
         const uint32_t mine = __popc(marks);
-        uint32_t incl = mine;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t v = __shfl_up_sync(kFull, incl, o);
-            if (lane >= o) incl += v;
-        }
-        uint32_t slot = 0;
-        if (lane == 31 && incl) slot = atomicAdd(&s.count, incl);
-        slot = __shfl_sync(kFull, slot, 31) + incl - mine;
+        uint32_t slot = mine ? atomicAdd(&s.count, mine) : 0u;
         while (marks) {
             const uint32_t b = static_cast<uint32_t>(__ffs(marks) - 1);
             marks &= marks - 1u;
@@ -1083,6 +1052,52 @@ __global__ void __launch_bounds__(kNT, kSmall ? 6 : 5) topk_kernel(TopkArgs a) {
         a.chunk_flags[static_cast<size_t>(t.row) * a.stride + t.chunk] = nf;
         if (tau != 0u) red_max_u32(&a.row_tau[t.row], tau);
     }
+}
+
+// The main launch: one block per row chunk; the chunk is staged in shared
+// memory (one bulk copy for aligned rows, 128-bit register loads
+// otherwise).
+template <bool kVec, bool kExtra, bool kSmall>
+__global__ void __launch_bounds__(kNT, kSmall ? 6 : 5) topk_kernel(TopkArgs a) {
+    constexpr uint32_t kCapB = kSmall ? kBlockCapSmall : kBlockCap;
+    extern __shared__ float4 stage[];  // the chunk: kUnitMax floats
+    __shared__ ChunkShared<kCapB> s;
+    __shared__ uint64_t bar;
+    const int tid = threadIdx.x;
+    if (kVec) {
+        if (tid == 0) mbar_init(&bar, 1);
+        __syncthreads();  // the barrier is initialised before anyone polls it
+    }
+    pdl_wait();
+    BlockUnit t;
+    t.row = static_cast<uint32_t>((static_cast<unsigned long long>(blockIdx.x) * a.chunks_magic) >>
+                                  (32u + a.chunks_shift));  // blockIdx.x / chunks
+    t.chunk = blockIdx.x - t.row * a.chunks;
+    t.lo = t.chunk * a.chunk_elems;
+    t.hi = min(a.V, t.lo + a.chunk_elems);
+    const float* rowp = a.logits + static_cast<size_t>(t.row) * a.V;
+    if (kVec) {
+        // 16-byte aligned row, V % 4 == 0: the chunk is whole quads
+        if (tid == 0) bulk_load(stage, rowp + t.lo, (t.hi - t.lo) * 4u, &bar);
+        pdl_trigger();
+        const bool ok = mbar_wait(&bar, 0);
+        if (__syncthreads_or(!ok)) {
+            // the copy engine stopped answering: record it, wait (bounded)
+            // for the copy still in flight, and leave
+            if (tid == 0) {
+                atomicOr(a.err, kErrTimeout);
+                mbar_wait(&bar, 0);
+            }
+            return;
+        }
+    } else {
+        float4 q[kVPT];
+        load_unit<kNT, kVPT, false>(rowp, t.lo, t.hi, -FLT_MAX, q);
+        pdl_trigger();
+#pragma unroll
+        for (int sl = 0; sl < kVPT; ++sl) stage[tid + kNT * sl] = q[sl];
+    }
+    topk_chunk<kVec, kExtra, kSmall, kCapB>(a, s, stage, t);
 }
 
 // The m-th largest (1 <= m <= 32) of the warp's 32 values: each lane counts
@@ -2241,6 +2256,13 @@ sel_status launch_topk(const float* d_logits, uint32_t rows, uint32_t V, uint32_
     a.V = V;
     a.chunks = chunks;
     a.chunk_elems = ce;
+    {
+        // b / chunks for b < 2^31: m = ceil(2^(32+s) / chunks), 2^s >= chunks
+        uint32_t sh = 0;
+        while ((1u << sh) < chunks) ++sh;
+        a.chunks_shift = sh;
+        a.chunks_magic = ((1ull << (32 + sh)) + chunks - 1) / chunks;
+    }
     a.sa = sa;
     const dim3 grid(static_cast<uint32_t>(blocks));
     constexpr size_t kStage = static_cast<size_t>(kUnitMax) * 4u;
