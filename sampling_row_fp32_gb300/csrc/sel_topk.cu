@@ -199,6 +199,31 @@ __device__ __forceinline__ void warp_append(TopkShared& s, bool p, uint64_t cand
 // The min(n, k) largest of buf[0..n) (distinct, non-zero, n <= kCap) into
 // out[], in descending order. All threads call; buf may be reordered. Ends
 // synced.
+// More than kRankMax candidates: a block bitonic sort of buf (padded with
+// zeros to a power of two, which buf must have room for), top k copied out.
+// Out of line: the rare path.
+__device__ __noinline__ void bitonic_select(uint64_t* buf, uint32_t n, uint32_t k, uint64_t* out) {
+    const uint32_t tid = threadIdx.x;
+    uint32_t m = 1;
+    while (m < n) m <<= 1;
+    for (uint32_t i = n + tid; i < m; i += kNT) buf[i] = 0;
+    __syncthreads();
+    for (uint32_t size = 2; size <= m; size <<= 1) {
+        for (uint32_t stride = size >> 1; stride > 0; stride >>= 1) {
+            for (uint32_t i = tid; i < m / 2; i += kNT) {
+                const uint32_t a = 2 * stride * (i / stride) + (i % stride);
+                const uint32_t b = a + stride;
+                const bool desc = (a & size) == 0;
+                const uint64_t x = buf[a], y = buf[b];
+                if ((x < y) == desc) { buf[a] = y; buf[b] = x; }
+            }
+            __syncthreads();
+        }
+    }
+    const uint32_t kk = n < k ? n : k;
+    for (uint32_t i = tid; i < kk; i += kNT) out[i] = buf[i];
+}
+
 __device__ void block_select_sorted(uint64_t* buf, uint32_t n, uint32_t k, uint64_t* out) {
     const uint32_t tid = threadIdx.x;
     if (n <= kRankMax) {
@@ -223,24 +248,7 @@ __device__ void block_select_sorted(uint64_t* buf, uint32_t n, uint32_t k, uint6
             if (rank < k) out[rank] = c;
         }
     } else {
-        uint32_t m = 1;
-        while (m < n) m <<= 1;
-        for (uint32_t i = n + tid; i < m; i += kNT) buf[i] = 0;
-        __syncthreads();
-        for (uint32_t size = 2; size <= m; size <<= 1) {
-            for (uint32_t stride = size >> 1; stride > 0; stride >>= 1) {
-                for (uint32_t i = tid; i < m / 2; i += kNT) {
-                    const uint32_t a = 2 * stride * (i / stride) + (i % stride);
-                    const uint32_t b = a + stride;
-                    const bool desc = (a & size) == 0;
-                    const uint64_t x = buf[a], y = buf[b];
-                    if ((x < y) == desc) { buf[a] = y; buf[b] = x; }
-                }
-                __syncthreads();
-            }
-        }
-        const uint32_t kk = n < k ? n : k;
-        for (uint32_t i = tid; i < kk; i += kNT) out[i] = buf[i];
+        bitonic_select(buf, n, k, out);
     }
     __syncthreads();
 }
@@ -433,6 +441,10 @@ __device__ float typical_window(const float* wf, const float* g, float* byr, uin
 //  - top-p keeps the shortest prefix of the window with pf >= top_p * its
 //    total; min-p keeps wf_j >= min_p * wf_lo (wf falls, so the survivors
 //    stay a prefix); the draw takes the first j with u * pd_end < pd_j.
+__device__ __noinline__ void sample_epilogue_general(const uint64_t* sorted, float* scratch, uint32_t nc,
+                                                     uint32_t row, float u, const SampleArgs& sa,
+                                                     uint32_t* out_ids);
+
 __device__ void sample_epilogue(const uint64_t* sorted, float* scratch, uint32_t n, uint32_t row, float u,
                                 bool nonfinite, const SampleArgs& sa, double nsig_thr, uint32_t* out_ids) {
     const int lane = threadIdx.x & 31;
@@ -462,7 +474,6 @@ __device__ void sample_epilogue(const uint64_t* sorted, float* scratch, uint32_t
     const float x0 = key2f(cand_key(sorted[0]));
     const float T = sa.temperature;
     const bool temp_last = sa.order == SEL_ORDER_TEMP_LAST;
-    const float Tf = temp_last ? 1.0f : T;
     const bool use_typ = sa.typical_p > 0.0f && sa.typical_p < 1.0f;
     if (nc <= 64u && !use_typ) {
         // At most 64 candidates and no typical cut: the same steps with the
@@ -521,6 +532,21 @@ __device__ void sample_epilogue(const uint64_t* sorted, float* scratch, uint32_t
         }
         return;
     }
+    sample_epilogue_general(sorted, scratch, nc, row, u, sa, out_ids);
+}
+
+// sample_epilogue past 64 candidates or with a typical cut: the weights and
+// prefix sums in shared memory (out of line, so that the common case above
+// keeps a small instruction footprint).
+__device__ __noinline__ void sample_epilogue_general(const uint64_t* sorted, float* scratch, uint32_t nc,
+                                                     uint32_t row, float u, const SampleArgs& sa,
+                                                     uint32_t* out_ids) {
+    const int lane = threadIdx.x & 31;
+    const float x0 = key2f(cand_key(sorted[0]));
+    const float T = sa.temperature;
+    const bool temp_last = sa.order == SEL_ORDER_TEMP_LAST;
+    const float Tf = temp_last ? 1.0f : T;
+    const bool use_typ = sa.typical_p > 0.0f && sa.typical_p < 1.0f;
     float* wf = scratch;                 // [SEL_MAX_K]
     float* wd = wf + SEL_MAX_K;          // [SEL_MAX_K]
     float* pf = wd + SEL_MAX_K;          // [SEL_MAX_K]
