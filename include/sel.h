@@ -196,12 +196,15 @@ typedef struct sel_sample_params {
  * id of the row as a candidate; the draw walks the survivors in ascending
  * token id instead (the same distribution, without sorting the row). The
  * row is read twice. The filters are decided from the row's 64 most probable
- * ids against sums over the whole row; a top-p cut that needs ids beyond
- * those 64 is found by a search over the row (a radix select weighted by
- * probability mass, four more passes that L2 mostly serves), so every top-p
- * row is decided. A locally typical window that needs ids beyond the 64 is
- * not decided: that row fails closed (SEL_INVALID_ID, probability NaN) and
- * bit 3 (8) is set in the workspace's first 32-bit word.
+ * ids against sums over the whole row; a top-p cut or a locally typical
+ * window that needs ids beyond those 64 is found by a search over the row (a
+ * radix select weighted by probability mass, on the value for top-p and on
+ * the distance to the typical logit M + Tf * mean(g) for the typical window,
+ * then top-p inside that window; passes that L2 mostly serves), so every
+ * such row is decided. With top-n-sigma on, a typical window whose
+ * candidate set runs past the 64 is not decided: that row fails closed
+ * (SEL_INVALID_ID, probability NaN) and bit 3 (8) is set in the workspace's
+ * first 32-bit word.
  * Sources: Muser book 21.1 (temperature-scaled softmax, then a draw
  * restricted to top-k / top-p candidates) and 21.7 (top-k truncation before
  * the top-p cutoff); llama.cpp pull 49, "Change" (a chain with top-k first

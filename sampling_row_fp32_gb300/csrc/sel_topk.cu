@@ -127,15 +127,20 @@ struct alignas(16) FullRow {
     unsigned long long key_lo, key_hi;
     float M;         // the row's maximum logit
     float u;         // the row's uniform
-    uint32_t valid;  // 0: the row fails closed; 1: decided; 2: top-p cut to be found over the row
+    uint32_t valid;  // 0: the row fails closed; 1: decided; 2: top-p cut to be found over the row;
+                     // 3: locally typical window (then top-p, min-p) to be found over the row
     uint32_t flags;  // kPlanBeyond: failed closed because a cut lay past the candidates
     float c_floor;   // (valid 2) the candidates C are the ids with x >= c_floor (top-n-sigma; -inf: all)
     float mp_floor;  // (valid 2) min-p keeps x >= mp_floor (-inf: off)
     float draw_c;    // log2(e) / T of the draw
-    uint32_t pad;
+    float x_typ;     // (valid 3) the typical logit M + Tf * gbar, where -ln P equals the entropy
 };
 static_assert(sizeof(FullRow) == sizeof(sel_shard_plan), "a shard plan is a FullRow");
 constexpr uint32_t kPlanBeyond = 1u;
+// the survivors at the top value key_hi are the ids up to cand_id-encoded
+// key_hi's low word (the lowest ids of a run the typical window keeps in
+// part), instead of those from it
+constexpr uint32_t kPlanTopLow = 2u;
 
 struct SampleArgs {
     const float* uniforms;  // [rows]
@@ -1182,7 +1187,9 @@ __device__ void full_row_plan(const uint64_t* sorted, float* scratch, uint32_t n
     out.M = n > 0 ? key2f(cand_key(sorted[0])) : 0.0f;
     bool resolved = !nonfinite && out.u >= 0.0f && out.u < 1.0f && n > 0 && Z > 0.0;
     bool beyond_err = false;
-    bool search = false;  // a top-p cut left to the cut search
+    bool search = false;      // a top-p cut left to the cut search
+    bool typ_search = false;  // a typical window left to the cut search
+    float x_typ = 0.0f;
     if (resolved) {
         const float M = out.M;
         const bool temp_last = sa.order == SEL_ORDER_TEMP_LAST;
@@ -1256,7 +1263,16 @@ __device__ void full_row_plan(const uint64_t* sorted, float* scratch, uint32_t n
             for (int o = 16; o > 0; o >>= 1) mass += __shfl_xor_sync(kFull, mass, o);
             const double beyond_min = fmax(gC - static_cast<double>(gv(nc - 1)), 0.0);
             if (beyond && !(mass >= static_cast<double>(need) && beyond_min >= static_cast<double>(s_last))) {
-                resolved = false;  // the window may run past the candidates
+                // the window may run past the candidates: with every id a
+                // candidate (no top-n-sigma), the cut search finds it over
+                // the row, then top-p and min-p inside it; otherwise the row
+                // fails closed
+                if (sa.top_n_sigma > 0.0f) {
+                    resolved = false;
+                } else {
+                    typ_search = true;
+                    x_typ = static_cast<float>(static_cast<double>(M) + static_cast<double>(Tf) * gC);
+                }
             } else {
                 lo = wlo;
                 hi = whi;
@@ -1265,6 +1281,7 @@ __device__ void full_row_plan(const uint64_t* sorted, float* scratch, uint32_t n
             }
         }
         uint32_t end = hi;
+        if (typ_search) search = true;  // the search also runs top-p and min-p
         if (resolved && !search && topp) {
             // the shortest prefix of the window whose mass reaches top_p
             const double need = static_cast<double>(sa.top_p) * ZW;
@@ -1293,7 +1310,7 @@ __device__ void full_row_plan(const uint64_t* sorted, float* scratch, uint32_t n
             }
         }
         double thr_mp = -INFINITY;
-        if (resolved && sa.min_p > 0.0f) {
+        if (resolved && !typ_search && sa.min_p > 0.0f) {
             // P_j >= min_p * P_max: wf_j >= min_p * wf_lo
             thr_mp = static_cast<double>(M) + static_cast<double>(Tf) * log(static_cast<double>(sa.min_p));
             if (!search && beyond && static_cast<double>(xv(n - 1)) < thr_mp) beyond = false;
@@ -1326,6 +1343,7 @@ __device__ void full_row_plan(const uint64_t* sorted, float* scratch, uint32_t n
             out.key_lo = 1ull;
             out.c_floor = floor_f(thr_ns);
             out.mp_floor = floor_f(thr_mp);
+            out.x_typ = x_typ;
         } else if (resolved) {
             if (!beyond) {
                 out.key_hi = sorted[lo];
@@ -1345,7 +1363,7 @@ __device__ void full_row_plan(const uint64_t* sorted, float* scratch, uint32_t n
             beyond_err = !nonfinite && out.u >= 0.0f && out.u < 1.0f;
         }
     }
-    out.valid = resolved ? (search ? 2u : 1u) : 0u;
+    out.valid = resolved ? (typ_search ? 3u : (search ? 2u : 1u)) : 0u;
     out.flags = beyond_err ? kPlanBeyond : 0u;
     out.draw_c = a.draw_c;
     if (lane == 0) {
@@ -1355,22 +1373,25 @@ __device__ void full_row_plan(const uint64_t* sorted, float* scratch, uint32_t n
 }
 
 // The survivor test of a FullRow by value, with the ids only at the two
-// boundary values: c = (key(x) << 32 | ~id) in [key_lo, key_hi].
+// boundary values: c = (key(x) << 32 | ~id) in [key_lo, key_hi]; with
+// kPlanTopLow the ids at the top value are those up to key_hi's low word
+// instead (a run of equal logits the typical window keeps in part).
 struct Members {
     float vlo, vhi;
     uint32_t idlo, idhi;
-    bool has_lo, has_hi;
+    bool has_lo, has_hi, hi_low;
     __device__ explicit Members(const FullRow& fr) {
         has_lo = (fr.key_lo >> 32) >= kKeyMinFinite;
         has_hi = fr.key_hi != ~0ull;
+        hi_low = (fr.flags & kPlanTopLow) != 0u;
         vlo = has_lo ? key2f(static_cast<uint32_t>(fr.key_lo >> 32)) : -INFINITY;
         vhi = has_hi ? key2f(static_cast<uint32_t>(fr.key_hi >> 32)) : INFINITY;
         idlo = cand_id(fr.key_lo);
-        idhi = cand_id(fr.key_hi);
+        idhi = hi_low ? static_cast<uint32_t>(fr.key_hi) : cand_id(fr.key_hi);
     }
     __device__ __forceinline__ bool operator()(float x, uint32_t id) const {
         const bool above = !has_lo || x > vlo || (x == vlo && id <= idlo);
-        const bool below = !has_hi || x < vhi || (x == vhi && id >= idhi);
+        const bool below = !has_hi || x < vhi || (x == vhi && (hi_low ? id <= idhi : id >= idhi));
         return above && below;
     }
 };
@@ -1473,7 +1494,7 @@ __global__ void __launch_bounds__(kNT) full_draw_find_kernel(TopkArgs a) {
         if (tid == 0) {
             a.out_ids[row] = SEL_INVALID_ID;
             a.sa.out_probs[row] = __uint_as_float(0x7fc00000u);
-            if (a.shard_masses && (fr.valid == 2u || (fr.flags & kPlanBeyond))) atomicOr(a.err, kErrBeyond);
+            if (a.shard_masses && (fr.valid >= 2u || (fr.flags & kPlanBeyond))) atomicOr(a.err, kErrBeyond);
         }
         return;
     }
@@ -1716,6 +1737,8 @@ struct alignas(16) CutShared {
     uint32_t tie_cnt;                       // ids at the cut value in this block's segment
     uint32_t found_id;
     int found;
+    float wr[kCutWarps][4];                 // per warp: the typical window's value range and the cut run's
+    float win[4];                           // ... and per block
 };
 
 __device__ __forceinline__ unsigned long long shfl_down_u64(unsigned long long v, int o) {
@@ -1734,7 +1757,7 @@ __global__ void __launch_bounds__(kCutNT, 1) full_cut_kernel(TopkArgs a) {
     pdl_trigger();
     const uint32_t row = blockIdx.x / kCutCL;
     const FullRow fr = a.full_rows[row];
-    if (fr.valid != 2u) return;  // every block of the cluster reads the same plan
+    if (fr.valid != 2u && fr.valid != 3u) return;  // every block of the cluster reads the same plan
     const uint32_t rank = cl.block_rank();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t V = a.V;
@@ -1762,218 +1785,371 @@ __global__ void __launch_bounds__(kCutNT, 1) full_cut_kernel(TopkArgs a) {
         return ld_quad<kVec>(x, e, hi, -INFINITY);
     };
 
-    uint32_t prefix = 0, pmask = 0;
-    unsigned long long above = 0, hd = 0;
-    double need = 0.0;
-    uint32_t ok = 1;
-    for (int pass = 0; pass < 4; ++pass) {
-        const int shift = 24 - 8 * pass;
-        for (int i = lane; i < 256; i += 32) sh.wh[warp][i] = 0ull;
-        __syncwarp();
-        // every thread runs the same number of iterations: the warp-wide
-        // votes below need all 32 lanes
-        // Lanes with the same digit add their masses (split in two 22-bit
-        // halves so the 32-bit sums cannot overflow), then one lane of each
-        // digit adds them to the warp's histogram. A thread first merges its
-        // four elements when they share a digit (the usual case), so a warp
-        // mostly needs one round per quad; it needs none when no element of
-        // the warp's quads lies under the prefix (most of passes 2-4).
-        auto add_round = [&](uint32_t d, unsigned long long w) {
-            const uint32_t live = __ballot_sync(kFull, d < 256u);
-            if (!live) return;
-            const int first = __ffs(live) - 1;
-            const uint32_t d0 = __shfl_sync(kFull, d, first);
-            uint32_t peers = kFull;
-            int leader = first;
-            if (!__all_sync(kFull, d == d0 || d == 256u)) {
-                peers = __match_any_sync(kFull, d);
-                leader = __ffs(peers) - 1;
+    // The typical window (valid 3) as a value range [wa, wb] of the row,
+    // less the ids above idpart at the value vpart (a run of equal logits
+    // that the window keeps only in part); everything when not in use.
+    float wa = -INFINITY, wb = INFINITY, vpart = NAN;
+    uint32_t idpart = 0xFFFFFFFFu;
+    auto in_set = [&](float v, uint32_t id) {
+        return f2key(v) >= key_floor && v >= wa && v <= wb && !(v == vpart && id > idpart);
+    };
+
+    // One weighted radix search over the set's logits: the shortest run of
+    // the largest sort keys whose mass reaches frac times the set's mass. The
+    // sort key is the value key (a top-p cut) or, with dist, the complement
+    // of the key of |v - xs| (the closest to the typical logit first).
+    // Returns with every block of the cluster holding the decision: the cut
+    // key, the mass above it, the mass of its bucket, and the needed mass.
+    struct Cut {
+        uint32_t prefix;
+        unsigned long long above, hd;
+        double need;
+        uint32_t ok;
+    };
+    auto search = [&](bool dist, float xs, float frac) {
+        Cut r{0u, 0ull, 0ull, 0.0, 1u};
+        uint32_t pmask = 0;
+        for (int pass = 0; pass < 4; ++pass) {
+            const int shift = 24 - 8 * pass;
+            for (int i = lane; i < 256; i += 32) sh.wh[warp][i] = 0ull;
+            __syncwarp();
+            // Lanes with the same digit add their masses (split in two 22-bit
+            // halves so the 32-bit sums cannot overflow), then one lane of
+            // each digit adds them to the warp's histogram. A thread first
+            // merges its four elements when they share a digit (the usual
+            // case), so a warp mostly needs one round per quad; it needs none
+            // when no element of the warp's quads lies under the prefix (most
+            // of passes 2-4).
+            auto add_round = [&](uint32_t d, unsigned long long w) {
+                const uint32_t live = __ballot_sync(kFull, d < 256u);
+                if (!live) return;
+                const int first = __ffs(live) - 1;
+                const uint32_t d0 = __shfl_sync(kFull, d, first);
+                uint32_t peers = kFull;
+                int leader = first;
+                if (!__all_sync(kFull, d == d0 || d == 256u)) {
+                    peers = __match_any_sync(kFull, d);
+                    leader = __ffs(peers) - 1;
+                }
+                const uint32_t whi = __reduce_add_sync(peers, static_cast<uint32_t>(w >> 22));
+                const uint32_t wlo = __reduce_add_sync(peers, static_cast<uint32_t>(w & 0x3FFFFFull));
+                if (d < 256u && lane == leader) sh.wh[warp][d] += (static_cast<unsigned long long>(whi) << 22) + wlo;
+            };
+            // every thread runs the same number of iterations: the warp-wide
+            // votes need all 32 lanes
+            for (uint32_t base = lo; base < hi; base += 4u * kCutNT) {
+                const uint32_t e = base + 4u * static_cast<uint32_t>(tid);
+                const float4 q = e < hi ? quad(e) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                const float f[4] = {q.x, q.y, q.z, q.w};
+                uint32_t d[4];
+                unsigned long long w[4];
+                uint32_t dq = 256u;
+                bool same = true;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t key = dist ? ~f2key(fabsf(f[j] - xs)) : f2key(f[j]);
+                    d[j] = 256u;
+                    w[j] = 0ull;
+                    if (e + j < hi && (key & pmask) == r.prefix && in_set(f[j], e + j)) {
+                        w[j] = mass(f[j]);
+                        if (w[j] != 0ull) d[j] = (key >> shift) & 255u;
+                    }
+                    if (d[j] < 256u) {
+                        same &= dq == 256u || dq == d[j];
+                        dq = d[j];
+                    }
+                }
+                if (!__any_sync(kFull, dq < 256u)) continue;
+                if (__all_sync(kFull, same)) {
+                    add_round(dq, (w[0] + w[1]) + (w[2] + w[3]));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) add_round(d[j], w[j]);
+                }
             }
-            const uint32_t whi = __reduce_add_sync(peers, static_cast<uint32_t>(w >> 22));
-            const uint32_t wlo = __reduce_add_sync(peers, static_cast<uint32_t>(w & 0x3FFFFFull));
-            if (d < 256u && lane == leader) sh.wh[warp][d] += (static_cast<unsigned long long>(whi) << 22) + wlo;
-        };
-        // every thread runs the same number of iterations: the warp-wide
-        // votes need all 32 lanes
+            __syncthreads();
+            if (tid < 256) {
+                unsigned long long sum = 0ull;
+#pragma unroll
+                for (int w = 0; w < kCutWarps; ++w) sum += sh.wh[w][tid];
+                sh.bh[tid] = sum;
+            }
+            cl.sync();  // every block's histogram is complete
+            if (rank == 0 && warp == 0) {
+                // the cluster's histogram; lane l holds buckets 8 l .. 8 l + 7
+                unsigned long long h[8] = {0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull};
+                for (uint32_t b = 0; b < kCutCL; ++b) {
+                    const unsigned long long* rb = cl.map_shared_rank(sh.bh, b);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) h[i] += rb[8 * lane + i];
+                }
+                unsigned long long T = 0ull;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) T += h[i];
+                // U: mass of buckets 8 l and up (suffix over the lanes)
+                unsigned long long U = T;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned long long v = shfl_down_u64(U, o);
+                    if (lane + o < 32) U += v;
+                }
+                // the set's mass, from the first pass
+                if (pass == 0) r.need = static_cast<double>(frac) * static_cast<double>(shfl64(U, 0));
+                // the lane whose buckets hold the crossing: the cumulative
+                // mass from the top reaches need within them
+                const unsigned long long above_l = r.above + (U - T);
+                const bool cross =
+                    static_cast<double>(r.above + U) >= r.need && static_cast<double>(above_l) < r.need;
+                const uint32_t who = __ballot_sync(kFull, cross);
+                if (who == 0u) {
+                    if (lane == 0) sh.dec = CutDecision{r.above, 0ull, r.need, 0u, 0u};
+                } else if (lane == __ffs(who) - 1) {
+                    unsigned long long acc = above_l, hs = 0ull;
+                    int ds = 0;
+                    for (int i = 7; i >= 0; --i) {
+                        if (static_cast<double>(acc + h[i]) >= r.need) {
+                            ds = i;
+                            hs = h[i];
+                            break;
+                        }
+                        acc += h[i];
+                    }
+                    sh.dec = CutDecision{acc, hs, r.need,
+                                         8u * static_cast<uint32_t>(lane) + static_cast<uint32_t>(ds), 1u};
+                }
+            }
+            cl.sync();  // block 0's decision is ready
+            const CutDecision dec = *cl.map_shared_rank(&sh.dec, 0u);
+            r.prefix |= dec.digit << shift;
+            pmask |= 255u << shift;
+            r.above = dec.above;
+            r.hd = dec.hd;
+            r.need = dec.need;
+            r.ok &= dec.ok;
+        }
+        return r;
+    };
+
+    // Of the ids for which at_cut(v, id) holds (a run at the cut), the
+    // tb-th lowest: every block counts its own, then the block holding it
+    // finds it in id order. Returns false when there is no such id.
+    auto nth_at_cut = [&](auto at_cut, uint32_t tn, uint32_t& id_out) {
+        uint32_t mine = 0;
         for (uint32_t base = lo; base < hi; base += 4u * kCutNT) {
             const uint32_t e = base + 4u * static_cast<uint32_t>(tid);
             const float4 q = e < hi ? quad(e) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
             const float f[4] = {q.x, q.y, q.z, q.w};
-            uint32_t d[4];
-            unsigned long long w[4];
-            uint32_t dq = 256u;
-            bool same = true;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) mine += (e + j < hi && at_cut(f[j], e + j)) ? 1u : 0u;
+        }
+        mine = __reduce_add_sync(kFull, mine);
+        if (lane == 0) sh.warp_cnt[warp] = mine;
+        __syncthreads();
+        if (tid == 0) {
+            uint32_t cnt = 0;
+            for (int w = 0; w < kCutWarps; ++w) cnt += sh.warp_cnt[w];
+            sh.tie_cnt = cnt;
+            sh.found = 0;
+        }
+        cl.sync();  // every block's count is ready
+        uint32_t before = 0, bstar = kCutCL, tb = 0;
+        for (uint32_t b = 0; b < kCutCL; ++b) {
+            const uint32_t cnt = *cl.map_shared_rank(&sh.tie_cnt, b);
+            if (bstar == kCutCL && before + cnt >= tn) {
+                bstar = b;
+                tb = tn - before;
+            }
+            before += cnt;
+        }
+        if (rank == bstar) {
+            __syncthreads();  // every warp has read the counts before warp_cnt is reused
+            for (uint32_t tile = lo; tile < hi; tile += 4u * kCutNT) {
+                const uint32_t e = tile + 4u * static_cast<uint32_t>(tid);
+                const float4 q = e < hi ? quad(e) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                const float f[4] = {q.x, q.y, q.z, q.w};
+                uint32_t flags = 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) flags |= (e + j < hi && at_cut(f[j], e + j)) ? (1u << j) : 0u;
+                const uint32_t cnt = __popc(flags);
+                uint32_t incl = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t v = __shfl_up_sync(kFull, incl, o);
+                    if (lane >= o) incl += v;
+                }
+                if (lane == 31) sh.warp_cnt[warp] = incl;
+                __syncthreads();
+                uint32_t woff = 0, total = 0;
+                for (int w = 0; w < kCutWarps; ++w) {
+                    const uint32_t v = sh.warp_cnt[w];
+                    if (w < warp) woff += v;
+                    total += v;
+                }
+                const uint32_t excl = woff + incl - cnt;
+                if (cnt != 0u && excl < tb && tb <= excl + cnt) {
+                    uint32_t m = flags;
+                    for (uint32_t r = tb - excl; r > 1u; --r) m &= m - 1u;
+                    sh.found_id = e + static_cast<uint32_t>(__ffs(m) - 1);
+                    sh.found = 1;
+                }
+                __syncthreads();
+                if (sh.found) break;
+                tb -= total;
+                __syncthreads();  // the counts are read before the next tile's
+            }
+        }
+        cl.sync();  // the finding block's result is ready
+        bool found = false;
+        if (bstar < kCutCL) {
+            found = *cl.map_shared_rank(&sh.found, bstar) != 0;
+            id_out = *cl.map_shared_rank(&sh.found_id, bstar);
+        }
+        cl.sync();  // every block has read it before the shared words are reused
+        return found;
+    };
+
+    uint32_t ok = 1;
+    bool top_low = false;  // the partial run sits at the window's top value
+    const bool typ = fr.valid == 3u;
+    if (typ) {
+        // The locally typical window: the ids closest to the typical logit
+        // xs, up to typical_p of C's mass. |v - xs| rounded is monotone on
+        // either side of xs, so the window is a value range; an exact tie
+        // in distance at the cut is one run of equal logits (on one side),
+        // of which the lowest ids are kept (the chain's order), or a tie
+        // across both sides, which is kept whole.
+        const float xs = fr.x_typ;
+        const Cut t = search(true, xs, a.sa.typical_p);
+        ok &= t.ok;
+        float vmin = INFINITY, vmax = -INFINITY, cmin = INFINITY, cmax = -INFINITY;
+        for (uint32_t base = lo; base < hi; base += 4u * kCutNT) {
+            const uint32_t e = base + 4u * static_cast<uint32_t>(tid);
+            if (e >= hi) continue;
+            const float4 q = quad(e);
+            const float f[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const uint32_t key = f2key(f[j]);
-                d[j] = 256u;
-                w[j] = 0ull;
-                if (e + j < hi && key >= key_floor && (key & pmask) == prefix) {
-                    w[j] = mass(f[j]);
-                    if (w[j] != 0ull) d[j] = (key >> shift) & 255u;
-                }
-                if (d[j] < 256u) {
-                    same &= dq == 256u || dq == d[j];
-                    dq = d[j];
+                if (e + j < hi && f2key(f[j]) >= key_floor && mass(f[j]) != 0ull) {
+                    const uint32_t dk = ~f2key(fabsf(f[j] - xs));
+                    if (dk >= t.prefix) {
+                        vmin = fminf(vmin, f[j]);
+                        vmax = fmaxf(vmax, f[j]);
+                    }
+                    if (dk == t.prefix) {
+                        cmin = fminf(cmin, f[j]);
+                        cmax = fmaxf(cmax, f[j]);
+                    }
                 }
             }
-            if (!__any_sync(kFull, dq < 256u)) continue;
-            if (__all_sync(kFull, same)) {
-                add_round(dq, (w[0] + w[1]) + (w[2] + w[3]));
-            } else {
+        }
 #pragma unroll
-                for (int j = 0; j < 4; ++j) add_round(d[j], w[j]);
-            }
+        for (int o = 16; o > 0; o >>= 1) {
+            vmin = fminf(vmin, __shfl_xor_sync(kFull, vmin, o));
+            vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, o));
+            cmin = fminf(cmin, __shfl_xor_sync(kFull, cmin, o));
+            cmax = fmaxf(cmax, __shfl_xor_sync(kFull, cmax, o));
+        }
+        if (lane == 0) {
+            sh.wr[warp][0] = vmin;
+            sh.wr[warp][1] = vmax;
+            sh.wr[warp][2] = cmin;
+            sh.wr[warp][3] = cmax;
         }
         __syncthreads();
-        if (tid < 256) {
-            unsigned long long sum = 0ull;
-#pragma unroll
-            for (int w = 0; w < kCutWarps; ++w) sum += sh.wh[w][tid];
-            sh.bh[tid] = sum;
+        if (tid < 4) {
+            float m = (tid & 1) ? -INFINITY : INFINITY;
+            for (int w = 0; w < kCutWarps; ++w) m = (tid & 1) ? fmaxf(m, sh.wr[w][tid]) : fminf(m, sh.wr[w][tid]);
+            sh.win[tid] = m;
         }
-        cl.sync();  // every block's histogram is complete
-        if (rank == 0 && warp == 0) {
-            // the cluster's histogram; lane l holds buckets 8 l .. 8 l + 7
-            unsigned long long h[8] = {0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull};
-            for (uint32_t b = 0; b < kCutCL; ++b) {
-                const unsigned long long* rb = cl.map_shared_rank(sh.bh, b);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) h[i] += rb[8 * lane + i];
-            }
-            unsigned long long T = 0ull;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) T += h[i];
-            // U: mass of buckets 8 l and up (suffix over the lanes)
-            unsigned long long U = T;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const unsigned long long v = shfl_down_u64(U, o);
-                if (lane + o < 32) U += v;
-            }
-            if (pass == 0) need = static_cast<double>(top_p) * static_cast<double>(shfl64(U, 0));  // C's mass
-            // the lane whose buckets hold the crossing: the cumulative mass
-            // from the top reaches need within them
-            const unsigned long long above_l = above + (U - T);
-            const bool cross = static_cast<double>(above + U) >= need && static_cast<double>(above_l) < need;
-            const uint32_t who = __ballot_sync(kFull, cross);
-            if (who == 0u) {
-                if (lane == 0) sh.dec = CutDecision{above, 0ull, need, 0u, 0u};
-            } else if (lane == __ffs(who) - 1) {
-                unsigned long long acc = above_l, hs = 0ull;
-                int ds = 0;
-                for (int i = 7; i >= 0; --i) {
-                    if (static_cast<double>(acc + h[i]) >= need) {
-                        ds = i;
-                        hs = h[i];
-                        break;
-                    }
-                    acc += h[i];
-                }
-                sh.dec = CutDecision{acc, hs, need, 8u * static_cast<uint32_t>(lane) + static_cast<uint32_t>(ds), 1u};
+        cl.sync();  // every block's ranges are ready
+        float r4[4] = {INFINITY, -INFINITY, INFINITY, -INFINITY};
+        for (uint32_t b = 0; b < kCutCL; ++b) {
+            const float* rw = cl.map_shared_rank(sh.win, b);
+            r4[0] = fminf(r4[0], rw[0]);
+            r4[1] = fmaxf(r4[1], rw[1]);
+            r4[2] = fminf(r4[2], rw[2]);
+            r4[3] = fmaxf(r4[3], rw[3]);
+        }
+        cl.sync();  // every block has read the ranges
+        wa = r4[0];
+        wb = r4[1];
+        ok &= (wa <= wb) ? 1u : 0u;
+        if (ok && r4[2] == r4[3]) {
+            // one run of equal logits at the cut distance: its lowest ids
+            // until the mass reaches typical_p
+            const float vc = r4[2];
+            const unsigned long long w1 = mass(vc);
+            const uint32_t nt = w1 != 0ull ? static_cast<uint32_t>(t.hd / w1) : 0u;
+            const double tn = ceil((t.need - static_cast<double>(t.above)) / static_cast<double>(w1));
+            const uint32_t tk = tn < 1.0 ? 1u : (tn >= static_cast<double>(nt) ? nt : static_cast<uint32_t>(tn));
+            if (nt > 1u && tk < nt) {
+                uint32_t id = 0;
+                const uint32_t pk = t.prefix;
+                const bool found = nth_at_cut(
+                    [&](float v, uint32_t) { return f2key(v) >= key_floor && ~f2key(fabsf(v - xs)) == pk; }, tk, id);
+                ok &= found ? 1u : 0u;
+                vpart = vc;
+                idpart = id;
+                top_low = vc == wb && wa < wb;
             }
         }
-        cl.sync();  // block 0's decision is ready
-        const CutDecision dec = *cl.map_shared_rank(&sh.dec, 0u);
-        prefix |= dec.digit << shift;
-        pmask |= 255u << shift;
-        above = dec.above;
-        hd = dec.hd;
-        need = dec.need;
-        ok &= dec.ok;
     }
-    // The cut value's key is `prefix`; each id there weighs w1, and the
-    // prefix of C takes t of its nt ids (the lowest).
-    const unsigned long long w1 = mass(key2f(prefix));
-    const uint32_t nt = (ok && w1 != 0ull) ? static_cast<uint32_t>(hd / w1) : 0u;
-    uint32_t t = 0;
-    if (nt != 0u) {
-        const double tn = ceil((need - static_cast<double>(above)) / static_cast<double>(w1));
-        t = tn < 1.0 ? 1u : (tn >= static_cast<double>(nt) ? nt : static_cast<uint32_t>(tn));
+    // The top-p cut, over C or inside the window: the cut value's key is
+    // c.prefix; each id there weighs w1, and the prefix takes tk of its nt
+    // ids (the lowest).
+    unsigned long long cstar = 0ull;
+    if (ok && top_p < 1.0f) {
+        const Cut c = search(false, 0.0f, top_p);
+        ok &= c.ok;
+        const unsigned long long w1 = mass(key2f(c.prefix));
+        const uint32_t nt = (ok && w1 != 0ull) ? static_cast<uint32_t>(c.hd / w1) : 0u;
+        ok &= nt != 0u ? 1u : 0u;
+        uint32_t tk = nt;
+        if (nt != 0u) {
+            const double tn = ceil((c.need - static_cast<double>(c.above)) / static_cast<double>(w1));
+            tk = tn < 1.0 ? 1u : (tn >= static_cast<double>(nt) ? nt : static_cast<uint32_t>(tn));
+        }
+        cstar = static_cast<unsigned long long>(c.prefix) << 32;
+        if (ok && tk < nt) {
+            // only the tk lowest ids at the cut value are kept
+            uint32_t id = 0;
+            const uint32_t pk = c.prefix;
+            const bool found =
+                nth_at_cut([&](float v, uint32_t i) { return f2key(v) == pk && in_set(v, i); }, tk, id);
+            ok &= found ? 1u : 0u;
+            cstar |= static_cast<uint32_t>(~id);
+        }
     }
-    const unsigned long long mp =
-        fr.mp_floor > -INFINITY ? static_cast<unsigned long long>(f2key(fr.mp_floor)) << 32 : 0ull;
-    auto write_plan = [&](bool good, unsigned long long cstar) {
+    if (rank == 0 && tid == 0) {
+        // min-p against the most probable survivor (the row's maximum, or
+        // the window's top value) as a value floor
+        unsigned long long mp =
+            fr.mp_floor > -INFINITY ? static_cast<unsigned long long>(f2key(fr.mp_floor)) << 32 : 0ull;
+        if (typ && a.sa.min_p > 0.0f) {
+            const double thr =
+                static_cast<double>(wb) + log2(static_cast<double>(a.sa.min_p)) / static_cast<double>(cf);
+            float f = static_cast<float>(thr);
+            if (static_cast<double>(f) < thr) f = nextafterf(f, INFINITY);
+            mp = static_cast<unsigned long long>(f2key(f)) << 32;
+        }
         FullRow out = fr;
+        unsigned long long lo_c = cstar > mp ? cstar : mp;
         out.key_hi = ~0ull;
-        out.key_lo = cstar > mp ? cstar : mp;
-        out.valid = good ? 1u : 0u;
+        if (typ) {
+            // the window's ends as candidate keys: its bottom value (the run
+            // kept in part there stops at idpart), its top value (all ids,
+            // or those up to idpart when the partial run is at the top)
+            unsigned long long wlo = static_cast<unsigned long long>(f2key(wa)) << 32;
+            if (vpart == wa && !top_low) wlo |= static_cast<uint32_t>(~idpart);
+            lo_c = lo_c > wlo ? lo_c : wlo;
+            out.key_hi = (static_cast<unsigned long long>(f2key(wb)) << 32) |
+                         (top_low ? static_cast<uint32_t>(idpart) : 0xFFFFFFFFu);
+            out.flags |= top_low ? kPlanTopLow : 0u;
+        }
+        out.key_lo = lo_c;
+        out.valid = ok ? 1u : 0u;
         a.full_rows[row] = out;
-        if (!good) atomicOr(a.err, kErrBeyond);
-    };
-    if (nt == 0u || t >= nt) {
-        // every id at the cut value is kept (or no cut was found)
-        if (rank == 0 && tid == 0) write_plan(nt != 0u, static_cast<unsigned long long>(prefix) << 32);
-        cl.sync();  // no block leaves while block 0's shared memory may still be read
-        return;
-    }
-    // Only the t lowest ids at the cut value are kept: count them per block,
-    // then the block holding the t-th finds it in id order.
-    uint32_t mine = 0;
-    for (uint32_t base = lo; base < hi; base += 4u * kCutNT) {
-        const uint32_t e = base + 4u * static_cast<uint32_t>(tid);
-        const float4 q = e < hi ? quad(e) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        const float f[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) mine += (e + j < hi && f2key(f[j]) == prefix) ? 1u : 0u;
-    }
-    mine = __reduce_add_sync(kFull, mine);
-    if (lane == 0) sh.warp_cnt[warp] = mine;
-    __syncthreads();
-    if (tid == 0) {
-        uint32_t c = 0;
-        for (int w = 0; w < kCutWarps; ++w) c += sh.warp_cnt[w];
-        sh.tie_cnt = c;
-        sh.found = 0;
-    }
-    cl.sync();
-    uint32_t before = 0, bstar = kCutCL, tb = 0;
-    for (uint32_t b = 0; b < kCutCL; ++b) {
-        const uint32_t c = *cl.map_shared_rank(&sh.tie_cnt, b);
-        if (bstar == kCutCL && before + c >= t) {
-            bstar = b;
-            tb = t - before;
-        }
-        before += c;
-    }
-    if (rank == bstar) {
-        for (uint32_t tile = lo; tile < hi; tile += 4u * kCutNT) {
-            const uint32_t e = tile + 4u * static_cast<uint32_t>(tid);
-            const float4 q = e < hi ? quad(e) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-            const float f[4] = {q.x, q.y, q.z, q.w};
-            uint32_t flags = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) flags |= (e + j < hi && f2key(f[j]) == prefix) ? (1u << j) : 0u;
-            const uint32_t cnt = __popc(flags);
-            uint32_t incl = cnt;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t v = __shfl_up_sync(kFull, incl, o);
-                if (lane >= o) incl += v;
-            }
-            if (lane == 31) sh.warp_cnt[warp] = incl;
-            __syncthreads();
-            uint32_t woff = 0, total = 0;
-            for (int w = 0; w < kCutWarps; ++w) {
-                const uint32_t c = sh.warp_cnt[w];
-                if (w < warp) woff += c;
-                total += c;
-            }
-            const uint32_t excl = woff + incl - cnt;
-            if (cnt != 0u && excl < tb && tb <= excl + cnt) {
-                uint32_t m = flags;
-                for (uint32_t r = tb - excl; r > 1u; --r) m &= m - 1u;
-                sh.found_id = e + static_cast<uint32_t>(__ffs(m) - 1);
-                sh.found = 1;
-            }
-            __syncthreads();
-            if (sh.found) break;
-            tb -= total;
-            __syncthreads();  // the counts are read before the next tile's
-        }
-        if (tid == 0)
-            write_plan(sh.found != 0,
-                       (static_cast<unsigned long long>(prefix) << 32) | static_cast<uint32_t>(~sh.found_id));
+        if (!ok) atomicOr(a.err, kErrBeyond);
     }
     cl.sync();  // no block leaves while its shared memory may still be read
 }

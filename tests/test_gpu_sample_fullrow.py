@@ -3,12 +3,13 @@ oracle. The filters act on softmax(x / T) over the whole vocabulary (the
 sampler chain of the Muser book, "Ch 21 -- Sampling, argmax, and grammar",
 21.1 and 21.7, without top-k); the draw walks the survivors in ascending id.
 
-Temperature alone, min-p, top-n-sigma and top-p are decided on every row:
-a top-p cut inside the row's 64 most probable tokens is decided from them,
-one past them by the cut search over the whole row (a radix select on the
-value key weighted by probability mass, exact ties going to the lower ids).
-A locally typical cut is decided from the 64 candidates only; a row whose
-typical window runs past them fails closed (0xFFFFFFFF, NaN) and raises
+Temperature alone, min-p, top-n-sigma, top-p and locally typical sampling
+are decided on every row: a cut inside the row's 64 most probable tokens is
+decided from them, one past them by the cut search over the whole row (a
+radix select weighted by probability mass, on the value key for top-p and
+on the distance to the typical logit for the typical window, exact ties
+going to the lower ids). Only a typical window under top-n-sigma whose
+candidate set runs past the 64 fails closed (0xFFFFFFFF, NaN) and raises
 error bit 8."""
 import numpy as np
 import pytest
@@ -181,14 +182,56 @@ def test_typical_on_scalar_path_rows(orc, V, misalign):
     """A locally typical cut needs the row's mean log-weight; rows that take
     the scalar loads (V % 4 != 0, or misaligned) end in a chunk where some
     threads hold only fill values, which must add nothing to it. Rows whose
-    window lies well inside the 64 candidates are decided; rows whose window
-    runs past them fail closed."""
+    window lies inside the 64 candidates and rows whose window runs past them
+    (the cut search) are all decided."""
     x = synth.normal_rows(81, 30, V, 3.0)
     u = synth.uniforms(82, 30)
-    _, _, _, failed = check(orc, x, u, 0.6, 1.0, 0.0, typ=0.8, misalign=misalign)
     reach = typical_window_reach(x, 0.6, 0.8)
-    assert not failed[reach < CAND - 8].any() and failed[reach >= CAND].all()
-    assert (reach < CAND - 8).sum() >= 20
+    assert (reach < CAND - 8).sum() >= 20 and (reach >= CAND).any()
+    check(orc, x, u, 0.6, 1.0, 0.0, typ=0.8, misalign=misalign, decided=np.ones(30, bool))
+
+
+@pytest.mark.parametrize("T,typ", [(1.0, 0.5), (0.7, 0.9), (1.5, 0.3), (1.0, 0.95)])
+@pytest.mark.parametrize("misalign", [False, True])
+def test_typical_past_the_candidates(orc, T, typ, misalign):
+    """Flat rows (N(0, 1.5^2)): the typical window holds thousands of ids,
+    so the cut search finds it over the row (a radix select on the distance
+    to the typical logit, weighted by mass); every row matches the oracle."""
+    x = synth.normal_rows(83, 32, 30_001, 1.5)
+    u = synth.uniforms(84, 32)
+    assert (typical_window_reach(x[:4], T, typ) >= CAND).all()
+    check(orc, x, u, T, 1.0, 0.0, typ=typ, misalign=misalign, decided=np.ones(32, bool))
+
+
+@pytest.mark.parametrize("top_p,min_p,temp_last", [(0.8, 0.0, False), (1.0, 0.05, False), (0.6, 0.01, True),
+                                                   (0.9, 0.2, True)])
+def test_typical_search_then_top_p_and_min_p(orc, top_p, min_p, temp_last):
+    """After the window, top-p keeps the shortest prefix of the window (a
+    second search inside it) and min-p compares with the window's most
+    probable id; in both temperature orders."""
+    x = synth.normal_rows(85, 24, 40_000, 2.0)
+    u = synth.uniforms(86, 24)
+    check(orc, x, u, 1.2, top_p, min_p, typ=0.7, temp_last=temp_last, decided=np.ones(24, bool))
+
+
+@pytest.mark.parametrize("typ,top_p", [(0.4, 1.0), (0.65, 0.5), (0.9, 1.0)])
+def test_typical_window_inside_a_run_of_equal_logits(orc, typ, top_p):
+    """Integer-valued rows: thousands of ids share each value, so the
+    window's edge falls inside a run of equal logits (one side of the
+    typical logit), of which the lowest ids are kept: the chain's order
+    among ids of equal score."""
+    rng = np.random.default_rng(int(typ * 1000))
+    x = rng.integers(0, 7, size=(12, 24_000)).astype(np.float32)
+    u = synth.uniforms(87, 12)
+    check(orc, x, u, 1.0, top_p, 0.0, typ=typ, decided=np.ones(12, bool))
+
+
+def test_typical_on_verify_batch(orc):
+    """The 49 verify rows at T 0.7 with typical_p 0.9: windows inside and
+    past the 64 candidates, all decided."""
+    x, _ = synth.workload_verify_batch()
+    u = synth.uniforms(88, 49)
+    check(orc, x, u, 0.7, 1.0, 0.0, typ=0.9, decided=np.ones(49, bool))
 
 
 def typical_window_reach(x, T, typ):
