@@ -201,10 +201,8 @@ typedef struct sel_sample_params {
  * radix select weighted by probability mass, on the value for top-p and on
  * the distance to the typical logit M + Tf * mean(g) for the typical window,
  * then top-p inside that window; passes that L2 mostly serves), so every
- * such row is decided. With top-n-sigma on, a typical window whose
- * candidate set runs past the 64 is not decided: that row fails closed
- * (SEL_INVALID_ID, probability NaN) and bit 3 (8) is set in the workspace's
- * first 32-bit word.
+ * such row is decided. (Under top-n-sigma the search first sums the
+ * candidate set's mass and mean log-weight over the row.)
  * Sources: Muser book 21.1 (temperature-scaled softmax, then a draw
  * restricted to top-k / top-p candidates) and 21.7 (top-k truncation before
  * the top-p cutoff); llama.cpp pull 49, "Change" (a chain with top-k first

@@ -133,7 +133,8 @@ struct alignas(16) FullRow {
     float c_floor;   // (valid 2) the candidates C are the ids with x >= c_floor (top-n-sigma; -inf: all)
     float mp_floor;  // (valid 2) min-p keeps x >= mp_floor (-inf: off)
     float draw_c;    // log2(e) / T of the draw
-    float x_typ;     // (valid 3) the typical logit M + Tf * gbar, where -ln P equals the entropy
+    float x_typ;     // (valid 3) the typical logit M + Tf * gbar, where -ln P equals the entropy (NaN: over C,
+                     // to be summed by the search)
 };
 static_assert(sizeof(FullRow) == sizeof(sel_shard_plan), "a shard plan is a FullRow");
 constexpr uint32_t kPlanBeyond = 1u;
@@ -1241,11 +1242,17 @@ __device__ void full_row_plan(const uint64_t* sorted, float* scratch, uint32_t n
         const bool topp = sa.top_p < 1.0f;
         // a top-p cut past the candidates is found over the whole row by the
         // cut search (full_cut_kernel); a typical window past them is not
-        if (!known && typical) resolved = false;
-        else if (!known && topp) search = true;
+        if (!known && typical) {
+            // C runs past the candidates: the cut search computes C's typical
+            // logit over the row, then finds the window
+            typ_search = true;
+            x_typ = NAN;
+        } else if (!known && topp) {
+            search = true;
+        }
         uint32_t lo = 0, hi = nc;
         double ZW = ZC;
-        if (resolved && typical && (nc > 1 || beyond)) {
+        if (resolved && !typ_search && typical && (nc > 1 || beyond)) {
             // the candidates' window; exact when every id past the
             // candidates scores above (or ties, later in position) the last
             // kept one: their g is at most g_{nc-1}, so their score is at
@@ -1263,16 +1270,10 @@ __device__ void full_row_plan(const uint64_t* sorted, float* scratch, uint32_t n
             for (int o = 16; o > 0; o >>= 1) mass += __shfl_xor_sync(kFull, mass, o);
             const double beyond_min = fmax(gC - static_cast<double>(gv(nc - 1)), 0.0);
             if (beyond && !(mass >= static_cast<double>(need) && beyond_min >= static_cast<double>(s_last))) {
-                // the window may run past the candidates: with every id a
-                // candidate (no top-n-sigma), the cut search finds it over
-                // the row, then top-p and min-p inside it; otherwise the row
-                // fails closed
-                if (sa.top_n_sigma > 0.0f) {
-                    resolved = false;
-                } else {
-                    typ_search = true;
-                    x_typ = static_cast<float>(static_cast<double>(M) + static_cast<double>(Tf) * gC);
-                }
+                // the window may run past the candidates: the cut search finds
+                // it over the row, then top-p and min-p inside it
+                typ_search = true;
+                x_typ = static_cast<float>(static_cast<double>(M) + static_cast<double>(Tf) * gC);
             } else {
                 lo = wlo;
                 hi = whi;
@@ -1739,6 +1740,8 @@ struct alignas(16) CutShared {
     int found;
     float wr[kCutWarps][4];                 // per warp: the typical window's value range and the cut run's
     float win[4];                           // ... and per block
+    double ws[kCutWarps][2];                // per warp: C's mass and first moment (typical under top-n-sigma)
+    double bs[2];                           // ... and per block
 };
 
 __device__ __forceinline__ unsigned long long shfl_down_u64(unsigned long long v, int o) {
@@ -2018,7 +2021,48 @@ __global__ void __launch_bounds__(kCutNT, 1) full_cut_kernel(TopkArgs a) {
         // in distance at the cut is one run of equal logits (on one side),
         // of which the lowest ids are kept (the chain's order), or a tie
         // across both sides, which is kept whole.
-        const float xs = fr.x_typ;
+        float xs = fr.x_typ;
+        if (!(xs == xs)) {
+            // C's typical logit M + sum w (x - M) / sum w over C (the ids at
+            // or above the top-n-sigma floor), w = exp((x - M) / Tf), summed
+            // in double in a fixed order (thread, warp, block, cluster)
+            double s0 = 0.0, s1 = 0.0;
+            for (uint32_t base = lo; base < hi; base += 4u * kCutNT) {
+                const uint32_t e = base + 4u * static_cast<uint32_t>(tid);
+                if (e >= hi) continue;
+                const float4 q = quad(e);
+                const float f[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (e + j < hi && f2key(f[j]) >= key_floor) {
+                        const double w = ex2_approx((f[j] - M) * cf);
+                        s0 += w;
+                        s1 += w * (static_cast<double>(f[j]) - static_cast<double>(M));
+                    }
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                s0 += __shfl_xor_sync(kFull, s0, o);
+                s1 += __shfl_xor_sync(kFull, s1, o);
+            }
+            if (lane == 0) { sh.ws[warp][0] = s0; sh.ws[warp][1] = s1; }
+            __syncthreads();
+            if (tid < 2) {
+                double m = 0.0;
+                for (int w = 0; w < kCutWarps; ++w) m += sh.ws[w][tid];
+                sh.bs[tid] = m;
+            }
+            cl.sync();  // every block's sums are ready
+            double c0 = 0.0, c1 = 0.0;
+            for (uint32_t b = 0; b < kCutCL; ++b) {
+                const double* rs = cl.map_shared_rank(sh.bs, b);
+                c0 += rs[0];
+                c1 += rs[1];
+            }
+            cl.sync();  // every block has read them
+            xs = c0 > 0.0 ? static_cast<float>(static_cast<double>(M) + c1 / c0) : M;
+        }
         const Cut t = search(true, xs, a.sa.typical_p);
         ok &= t.ok;
         float vmin = INFINITY, vmax = -INFINITY, cmin = INFINITY, cmax = -INFINITY;

@@ -8,9 +8,8 @@ are decided on every row: a cut inside the row's 64 most probable tokens is
 decided from them, one past them by the cut search over the whole row (a
 radix select weighted by probability mass, on the value key for top-p and
 on the distance to the typical logit for the typical window, exact ties
-going to the lower ids). Only a typical window under top-n-sigma whose
-candidate set runs past the 64 fails closed (0xFFFFFFFF, NaN) and raises
-error bit 8."""
+going to the lower ids; under top-n-sigma the search first sums the
+candidate set's mass and mean log-weight over the row)."""
 import numpy as np
 import pytest
 import torch
@@ -156,7 +155,18 @@ def test_whole_chain_on_short_rows(orc):
 def test_typical_and_top_p_together(orc):
     x = synth.normal_rows(72, 30, 20_000, 3.0)
     u = synth.uniforms(73, 30)
-    check(orc, x, u, 0.6, 0.9, 0.0, nsig=1.0, typ=0.8)
+    check(orc, x, u, 0.6, 0.9, 0.0, nsig=1.0, typ=0.8, decided=np.ones(30, bool))
+
+
+@pytest.mark.parametrize("nsig,typ,top_p,temp_last", [(3.0, 0.6, 1.0, False), (2.0, 0.8, 0.7, False),
+                                                      (4.0, 0.5, 0.9, True)])
+def test_typical_under_top_n_sigma_past_the_candidates(orc, nsig, typ, top_p, temp_last):
+    """Top-n-sigma keeps thousands of ids (a loose n), so the candidate set
+    C runs past the 64: the search sums C's mass and mean log-weight over the
+    row for the typical logit, then finds the window inside C."""
+    x = synth.normal_rows(89, 24, 30_000, 1.5)
+    u = synth.uniforms(90, 24)
+    check(orc, x, u, 1.0, top_p, 0.0, nsig=nsig, typ=typ, temp_last=temp_last, decided=np.ones(24, bool))
 
 
 def test_invalid_rows(orc):
