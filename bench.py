@@ -379,14 +379,41 @@ def full_row_search_rows() -> int:
     return int((((c < POLICY["top_p"]).sum(axis=1) + 1) > 64).sum())
 
 
+TYPICAL_P = 0.9  # the full-row typical line: T as the step's, typical_p 0.9, no other filter
+
+
+def full_row_typical_search_rows() -> int:
+    """Rows of the verify batch whose locally typical window (at the step's
+    T, typical_p TYPICAL_P, over the whole row) reaches past the 64 most
+    probable tokens, so that the cut search decides them (double, host)."""
+    from sampling_row_fp32_gb300 import synth
+    x, _ = synth.workload_verify_batch(ROWS, V)
+    n = 0
+    for r in range(ROWS):
+        z = x[r].astype(np.float64) / POLICY["temperature"]
+        z -= z.max()
+        p = np.exp(z)
+        p /= p.sum()
+        lp = np.log(p, where=p > 0, out=np.full_like(p, -np.inf))
+        h = -(p[p > 0] * lp[p > 0]).sum()
+        score = np.abs(-lp - h)
+        order = np.lexsort((np.arange(p.size), score))
+        k = int(np.searchsorted(np.cumsum(p[order]), TYPICAL_P) + 1)
+        rank = np.empty(p.size, dtype=np.int64)
+        rank[np.lexsort((np.arange(p.size), -p))] = np.arange(p.size)
+        n += int(rank[order[:k]].max() >= 64)
+    return n
+
+
 def extra_ops(B, dev, xs, drafts, tok, stream):
     """The calls beyond the step, on the same batch and copy rotation, each
     timed over OP_REPS graph-replayed launches: the EOG-excluding argmax (8
     ids), sampling with the step's policy plus top-n-sigma 1.0 and typical_p
     0.8, full-row sampling (top_k = 0, the step's T, top_p and min_p),
     sampler-match acceptance (7 x 6, the step's policy), the closed-form
-    diagnostics (7 x 6) and a two-shard top-k (k = 20 per shard on each half
-    of the vocabulary, then the merge)."""
+    diagnostics (7 x 6), a two-shard top-k (k = 20 per shard on each half
+    of the vocabulary, then the merge), and full-row locally typical sampling
+    (top_k = 0, the step's T, typical_p TYPICAL_P)."""
     import torch
     peak, _ = measured_peak()
     ids = torch.empty(ROWS, dtype=torch.int32, device=dev)
@@ -432,13 +459,19 @@ def extra_ops(B, dev, xs, drafts, tok, stream):
     prm_last = B.SampleParams(POLICY["temperature"], POLICY["top_k"], POLICY["top_p"], POLICY["min_p"],
                               B.SEL_ORDER_TEMP_LAST)
     ws_full = B.workspace(B.SEL_OP_SAMPLE, ROWS, V, 0, device=dev)
+    prm_typ = B.SampleParams(POLICY["temperature"], 0, 1.0, 0.0, B.SEL_ORDER_TEMP_FIRST, 0.0, TYPICAL_P)
+    ws_typ = B.workspace(B.SEL_OP_SAMPLE, ROWS, V, 0, device=dev)
+    typ_rows = full_row_typical_search_rows()
     calls = {
         "argmax_excluding_8": (lambda r: B.sel_argmax_excluding(xs[r % N_COPIES], exd, ids, ws_a), ROWS * ROW_BYTES),
         # full-row sampling reads every row twice (candidates and sums, then
-        # the draw); a row whose nucleus runs past the 64 candidates is read
-        # four more times by the cut search (from L2, mostly): counted too
+        # the draw); a row whose cut lies past the 64 candidates is read once
+        # more by the cut search (staged in shared memory, whose passes then
+        # read no more of it): counted too
         "sample_full_row": (lambda r: B.sel_sample(xs[r % N_COPIES], prm_full, uu, sid, spr, ws_full),
-                            (2 * ROWS + 4 * full_row_search_rows()) * ROW_BYTES),
+                            (2 * ROWS + full_row_search_rows()) * ROW_BYTES),
+        "sample_full_row_typical": (lambda r: B.sel_sample(xs[r % N_COPIES], prm_typ, uu, sid, spr, ws_typ),
+                                    (2 * ROWS + typ_rows) * ROW_BYTES),
         "sample_nsigma1_typical08": (lambda r: B.sel_sample(xs[r % N_COPIES], prm_f, uu, sid, spr, ws_f),
                                      ROWS * ROW_BYTES),
         # the step's policy with the filters on the untempered distribution
@@ -478,6 +511,11 @@ def extra_ops(B, dev, xs, drafts, tok, stream):
         B.sel_sample(xs[0], prm_full, uu, sid, spr, ws_full)
     torch.cuda.synchronize()
     out["sample_full_row"]["failed_rows"] = int((B.ids_to_numpy(sid) == 0xFFFFFFFF).sum())
+    out["sample_full_row_typical"]["cut_search_rows"] = typ_rows
+    with torch.cuda.stream(stream):
+        B.sel_sample(xs[0], prm_typ, uu, sid, spr, ws_typ)
+    torch.cuda.synchronize()
+    out["sample_full_row_typical"]["failed_rows"] = int((B.ids_to_numpy(sid) == 0xFFFFFFFF).sum())
     return out
 
 

@@ -143,6 +143,15 @@ def test_top_p_search_on_a_large_row(orc):
     check(orc, x, u, 1.0, 0.9, 0.0, decided=np.ones(2, bool))
 
 
+def test_typical_search_on_a_large_row(orc):
+    """Two flat rows of 2,000,003 logits: the typical window (then top-p
+    inside it) found by the search on segments too long to stage in shared
+    memory, so every pass reads the row from global memory."""
+    x = synth.normal_rows(91, 2, 2_000_003, 4.0)
+    u = synth.uniforms(92, 2)
+    check(orc, x, u, 1.0, 0.9, 0.0, typ=0.6, decided=np.ones(2, bool))
+
+
 def test_whole_chain_on_short_rows(orc):
     """V <= 64: the candidates hold the whole row, so every filter of the
     chain is decided, in both temperature orders."""
