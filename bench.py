@@ -632,7 +632,7 @@ STEP_LAUNCHES = [
     ("sample", "topk_kernel"), ("sample", "topk_finish_kernel<1"),
     ("spec_rejection", "spec_phase1_kernel"), ("spec_rejection", "spec_decide_draw_kernel"),
     ("spec_rejection", "spec_draw_find_kernel"),
-    ("spec_argmax", "spec_phase1_kernel"), ("spec_argmax", "spec_rows_kernel<0"),
+    ("spec_argmax", "argmax_kernel"), ("spec_argmax", "spec_argmax_finish_kernel"),
 ]
 TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
 

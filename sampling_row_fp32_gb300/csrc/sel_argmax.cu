@@ -248,6 +248,30 @@ sel_status launch_argmax(const float* d_logits, uint32_t rows, uint32_t V, const
     return e == cudaSuccess ? SEL_OK : SEL_ECUDA;
 }
 
+// The main launch alone, folding each row's (max, lowest argmax id) key
+// into slots[row] (which must hold 0; a nonfinite row gets the all-ones
+// key): the argmax rule of spec_accept finishes from these slots.
+sel_status argmax_into_slots(const float* d_logits, uint32_t rows, uint32_t V, unsigned long long* slots,
+                             cudaStream_t stream) {
+    const int sms = device_sms();
+    if (sms <= 0) return SEL_ECUDA;
+    const bool vec = (reinterpret_cast<uintptr_t>(d_logits) % 16 == 0) && (V % 4 == 0);
+    const uint32_t ce = plan_unit(rows, V, kGrain, kUnitMax, 2ull * static_cast<uint64_t>(sms));
+    const uint32_t chunks = ceil_div(V, ce);
+    const uint64_t blocks = static_cast<uint64_t>(rows) * chunks;
+    if (blocks > 0x7fffffffull) return SEL_EUNSUPPORTED;
+    ArgmaxArgs a{};
+    a.logits = d_logits;
+    a.slots = slots;
+    a.V = V;
+    a.chunks = chunks;
+    a.chunk_elems = ce;
+    const dim3 grid(static_cast<uint32_t>(blocks));
+    const cudaError_t e = vec ? launch_pdl(argmax_kernel<true, false>, grid, dim3(kNT), 0, stream, a)
+                              : launch_pdl(argmax_kernel<false, false>, grid, dim3(kNT), 0, stream, a);
+    return e == cudaSuccess ? SEL_OK : SEL_ECUDA;
+}
+
 }  // namespace sel
 
 extern "C" sel_status sel_argmax(const float* d_logits, uint32_t rows, uint32_t V, uint32_t* d_out_ids, void* d_ws,

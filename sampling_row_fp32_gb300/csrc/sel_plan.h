@@ -7,6 +7,8 @@
 
 #include <cuda_runtime.h>
 
+#include "sel.h"
+
 namespace sel {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -20,6 +22,10 @@ int device_sms();
 
 // Workspace bytes of each operation (0 when none is needed).
 size_t argmax_ws_bytes(uint32_t rows, uint32_t V);
+// sel_argmax's main launch alone, folding each row's (max, lowest argmax id)
+// key into slots[row] (zero beforehand; all ones for a nonfinite row)
+sel_status argmax_into_slots(const float* d_logits, uint32_t rows, uint32_t V, unsigned long long* slots,
+                             cudaStream_t stream);
 size_t topk_ws_bytes(uint32_t rows, uint32_t V, uint32_t k);
 size_t spec_ws_bytes(uint32_t S, uint32_t V, uint32_t K);
 size_t spec_diag_ws_bytes(uint32_t S, uint32_t V, uint32_t K);

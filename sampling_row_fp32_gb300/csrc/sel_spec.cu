@@ -18,10 +18,11 @@
 // verified position" is the mlxcel cost note). Here:
 //  Phase 1 (one launch over every target and draft row of every sequence):
 //    one block per row chunk (sel_units.cuh) reduces its chunk to (max, sum
-//    of exp((x - max) / T)) and stores it; in the argmax rule it folds
-//    (max, lowest argmax id) into the row's slot with one 64-bit atomic
-//    maximum (no block waits on another). In the rejection rule the block
-//    holding a row's draft token also stores that logit.
+//    of exp((x - max) / T)) and stores it; the block holding a row's draft
+//    token also stores that logit. The argmax rule reads only the target
+//    rows: sel_argmax's main launch folds each row's (max, lowest argmax
+//    id) into the row's slot with one 64-bit atomic maximum per block (no
+//    block waits on another).
 //  Decision: a launch that follows by programmatic dependent launch reads
 //    the slots (argmax rule) or merges each row's chunks in chunk order, and
 //    runs the sequence's acceptance chain. In the rejection rule with
@@ -581,6 +582,37 @@ __global__ void __launch_bounds__(kNT) spec_rows_kernel(SpecArgs a) {
             if (tid == 0) a.plans[s] = make_plan(n, K, tstat, dstat);
         }
     }
+}
+
+// The argmax rule with K < 32, one warp per sequence (kWarps a block): lane
+// j reads position j's slot (target row j's key) and draft token together,
+// the first j < K whose token is not its row's argmax ends the chain, and a
+// nonfinite target row or a token >= V fails the sequence closed. Each slot
+// is cleared for the next call. One round trip from phase 1's keys to the
+// outputs, no block barrier.
+__global__ void __launch_bounds__(kNT) spec_argmax_finish_kernel(SpecArgs a) {
+    pdl_wait();
+    pdl_trigger();
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint32_t s = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (s >= a.S) return;
+    const uint32_t K = a.K, V = a.V;
+    unsigned long long* sl = a.slots + static_cast<size_t>(s) * (K + 1u);
+    unsigned long long key = 0ull;
+    uint32_t t = 0;
+    if (lane <= K) key = sl[lane];
+    if (lane < K) t = a.tokens[static_cast<size_t>(s) * K + lane];
+    if (lane <= K) sl[lane] = 0ull;
+    const uint32_t arg = ~static_cast<uint32_t>(key);
+    const bool bad = __any_sync(kFull, (lane <= K && key == ~0ull) || (lane < K && t >= V));
+    const uint32_t f = __ballot_sync(kFull, lane < K && t != arg);
+    const uint32_t n = f ? static_cast<uint32_t>(__ffs(f) - 1) : K;
+    if (lane <= K) {
+        uint32_t v = SEL_INVALID_ID;
+        if (!bad) v = lane < n ? t : (lane == n ? arg : SEL_INVALID_ID);
+        a.emitted[static_cast<size_t>(s) * (K + 1u) + lane] = v;
+    }
+    if (lane == 0) a.accepted[s] = bad ? SEL_INVALID_ID : n;
 }
 
 struct DrawArgs {
@@ -1182,17 +1214,20 @@ extern "C" sel_status spec_accept(const float* d_target, const float* d_draft, c
     a.cmax = l.cmax_a;
     a.decide = true;
     a.want_tok = true;
-    const dim3 grid1(rows1 * chunks1);
-    cudaError_t e1;
-    if (rej) e1 = vec ? launch_pdl(spec_phase1_kernel<true, true>, grid1, dim3(kNT), 0, stream, a)
-                      : launch_pdl(spec_phase1_kernel<false, true>, grid1, dim3(kNT), 0, stream, a);
-    else e1 = vec ? launch_pdl(spec_phase1_kernel<true, false>, grid1, dim3(kNT), 0, stream, a)
-                  : launch_pdl(spec_phase1_kernel<false, false>, grid1, dim3(kNT), 0, stream, a);
-    if (e1 != cudaSuccess) return SEL_ECUDA;
     if (!rej) {
-        e1 = launch_pdl(spec_rows_kernel<false>, dim3(S), dim3(kNT), 0, stream, a);
-        return e1 == cudaSuccess ? SEL_OK : SEL_ECUDA;
+        // argmax rule: the target rows' argmax keys into their slots by
+        // sel_argmax's main launch (its 16 KB units), then the chains
+        const sel_status st = argmax_into_slots(d_target, S * (K + 1u), V, a.slots, stream);
+        if (st != SEL_OK) return st;
+        const cudaError_t e =
+            K < 32u ? launch_pdl(spec_argmax_finish_kernel, dim3(ceil_div(S, kWarps)), dim3(kNT), 0, stream, a)
+                    : launch_pdl(spec_rows_kernel<false>, dim3(S), dim3(kNT), 0, stream, a);
+        return e == cudaSuccess ? SEL_OK : SEL_ECUDA;
     }
+    const dim3 grid1(rows1 * chunks1);
+    const cudaError_t e1 = vec ? launch_pdl(spec_phase1_kernel<true, true>, grid1, dim3(kNT), 0, stream, a)
+                               : launch_pdl(spec_phase1_kernel<false, true>, grid1, dim3(kNT), 0, stream, a);
+    if (e1 != cudaSuccess) return SEL_ECUDA;
 
     // phase 2: chunks of kDrawChunkMax ids
     const uint32_t ce2 = kDrawChunkMax;

@@ -72,6 +72,22 @@ def test_separate_decision_launch(orc, S, K, V, equal_upto):
     run_both(orc, si, ARG)
 
 
+@pytest.mark.parametrize("K", [1, 31, 32, 40])
+def test_argmax_rule_long_chains(orc, K):
+    """Drafts that match the targets' argmax for a prefix of every length
+    (0 .. K, so some sequences accept all K and emit the bonus argmax):
+    the one-warp decision up to K = 31 and the block decision above it."""
+    S, V = K + 1, 5000
+    si = synth.spec_inputs(S=S, K=K, V=V, seed_target=K + 40, seed_draft=K + 41, seed_u=K + 42)
+    best = si.target.argmax(axis=2).astype(np.uint32)   # first maximum, as the rule's argmax
+    for s_ in range(S):
+        si.draft_tokens[s_, :s_] = best[s_, :s_]
+        if s_ < K:
+            si.draft_tokens[s_, s_] = (best[s_, s_] + 1) % V
+    acc, emi, ref = run_both(orc, si, ARG)
+    assert np.array_equal(acc, np.arange(S))
+
+
 def test_temperature_zero_is_the_argmax_rule(orc):
     si = synth.spec_inputs(S=6, K=4, V=9000, temperature=1.0, sigma_noise=0.1)
     a0, e0 = G.spec(si.target, si.draft, si.draft_tokens, si.u_acc, si.u_fin, 0.0, REJ)
