@@ -486,21 +486,37 @@ __device__ __forceinline__ FF ff_half_sum(FF a) {
     return a;
 }
 
-// Merge the staged chunk statistics of gn rows (st: row i's C chunks at
-// st + i * C) into out[0..gn), block-wide: a half-warp per row, lane l
-// folding chunks l, l + 16, ... in order, then a butterfly over the half.
-// The result depends on the data only, not on timing.
+// Row r of sequence s's rows in chain order: target rows 0..K, then draft
+// rows 0..K-1.
+__device__ __forceinline__ uint32_t seq_row(const SpecArgs& a, uint32_t s, uint32_t i);
+
+// Merge the chunk statistics of rows 0 .. nrows - 1 of sequence s (chain
+// order) straight from global memory into out[]: a half-warp per row (16
+// rows a round), lane l folding chunks l, l + 16, ... in order, then a
+// butterfly over the half (the result depends on the data only, not on
+// timing); the max, the lowest id attaining it, the nonfinite bit, and
+// (rejection rule) the float-float sum of the chunk sums rescaled to the
+// row's max. Every load of a round is issued before its use.
 template <bool kRej>
-__device__ void merge_staged(const RowPart* st, uint32_t gn, uint32_t C, float c, RowPart* out) {
+__device__ void merge_rows_global(const SpecArgs& a, uint32_t s, uint32_t nrows, float c, RowPart* out) {
     const uint32_t tid = threadIdx.x, h = tid >> 4, hl = tid & 15u;
+    const uint32_t C = a.chunks;
     constexpr uint32_t kHalves = kNT / 16;
-    for (uint32_t i0 = 0; i0 < gn; i0 += kHalves) {
+    const RowPart none{-INFINITY, kNoIdx, 0.0f, 0.0f};
+    for (uint32_t i0 = 0; i0 < nrows; i0 += kHalves) {
         const uint32_t i = i0 + h;
-        const bool live = i < gn;
-        const RowPart* parts = st + static_cast<size_t>(live ? i : 0u) * C;
-        float rm = -INFINITY;
-        uint32_t ri = kNoIdx, rnf = 0u;
-        if (live) {
+        const bool live = i < nrows;
+        const RowPart* parts = a.row_parts + static_cast<size_t>(seq_row(a, s, live ? i : 0u)) * a.cmax;
+        // C <= 32 (the usual case): this lane's two chunks, kept in registers
+        RowPart p0 = none, p1 = none;
+        if (live && C <= 32u) {
+            if (hl < C) p0 = parts[hl];
+            if (hl + 16u < C) p1 = parts[hl + 16u];
+        }
+        float rm = p0.m;
+        uint32_t ri = p0.idx & ~kNonfiniteBit, rnf = (p0.idx | p1.idx) & kNonfiniteBit;
+        if (beats(p1.m, p1.idx & ~kNonfiniteBit, rm, ri)) { rm = p1.m; ri = p1.idx & ~kNonfiniteBit; }
+        if (live && C > 32u) {
             for (uint32_t cc = hl; cc < C; cc += 16u) {
                 const float cm = parts[cc].m;
                 const uint32_t ci = parts[cc].idx;
@@ -516,23 +532,23 @@ __device__ void merge_staged(const RowPart* st, uint32_t gn, uint32_t C, float c
             if (beats(ov, oi, rm, ri)) { rm = ov; ri = oi; }
         }
         FF rs{0.0f, 0.0f};
-        if (kRej) {
-            if (live && !rnf) {
+        if (kRej && live && !rnf) {
+            // a chunk of padding only (max -inf) adds nothing
+            if (C <= 32u) {
+                if (p0.m > -INFINITY) rs = ff_add(rs, ff_mul_f(FF{p0.s_hi, p0.s_lo}, ex2_approx((p0.m - rm) * c)));
+                if (p1.m > -INFINITY) rs = ff_add(rs, ff_mul_f(FF{p1.s_hi, p1.s_lo}, ex2_approx((p1.m - rm) * c)));
+            } else {
                 for (uint32_t cc = hl; cc < C; cc += 16u) {
                     const float cm = parts[cc].m;
-                    // a chunk of padding only (max -inf) adds nothing
                     if (cm > -INFINITY)
                         rs = ff_add(rs, ff_mul_f(FF{parts[cc].s_hi, parts[cc].s_lo}, ex2_approx((cm - rm) * c)));
                 }
             }
-            rs = ff_half_sum(rs);
         }
+        if (kRej) rs = ff_half_sum(rs);
         if (live && hl == 0) out[i] = RowPart{rm, ri | rnf, rs.hi, rs.lo};
     }
 }
-
-// Row r of sequence s's rows in chain order: target rows 0..K, then draft
-// rows 0..K-1.
 __device__ __forceinline__ uint32_t seq_row(const SpecArgs& a, uint32_t s, uint32_t i) {
     const uint32_t rows_t = a.K + 1u;
     return i < rows_t ? s * rows_t + i : a.S * rows_t + s * a.K + (i - rows_t);
@@ -725,16 +741,16 @@ __global__ void __launch_bounds__(kNT) spec_draw_sum_kernel(DrawArgs b) {
 
 // Rejection rule with K <= kPre and at most kStage chunk statistics per row:
 // the row merge, the acceptance chain and 2a in one launch. Block (s, chunk)
-// stages sequence s's chunk statistics in shared memory, merges its rows and
-// runs its chain (every block of the sequence reaches the same decision from
-// the same data; chunk 0's block stores it), then sums its chunk of the rows
-// the decision names. This saves a launch and two round trips through L2 on
-// the path from phase 1 to the draw.
-constexpr uint32_t kStage = 1024;               // chunk statistics staged at once (16 KB)
+// merges sequence s's rows from their chunk statistics (a half-warp per row,
+// straight from global memory) and runs its chain (every block of the
+// sequence reaches the same decision from the same data; chunk 0's block
+// stores it), then sums its chunk of the rows the decision names. This saves
+// a launch and two round trips through L2 on the path from phase 1 to the
+// draw.
+constexpr uint32_t kStage = 1024;               // chunk statistics of a row the fused launch takes
 constexpr uint32_t kChainRows = 2u * kPre + 1u;  // rows of a sequence with K <= kPre
 
 struct DecideShared {
-    RowPart st[kStage];
     RowPart rs[kChainRows];
     ChainPre pre;
     FF s_r[kWarps], s_p[kWarps];
@@ -749,33 +765,12 @@ __global__ void __launch_bounds__(kNT) spec_decide_draw_kernel(SpecArgs a, DrawA
     const uint32_t K = a.K, C = a.chunks;
     const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
     const uint32_t rows_t = K + 1u, nrows = 2u * K + 1u;
-    const uint32_t per = kStage / C;  // rows staged at once (C <= kStage)
+    (void)C;
     pdl_wait();
     pdl_trigger();
     load_chain_pre<true>(a, s, sh.pre);
-    for (uint32_t g0 = 0; g0 < nrows; g0 += per) {
-        const uint32_t gn = min(per, nrows - g0);
-        const uint32_t n = gn * C;
-        for (uint32_t e0 = 0; e0 < n; e0 += 4u * kNT) {
-            RowPart v[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t e = e0 + tid + kNT * i;
-                if (e < n) {
-                    const uint32_t ri = e / C;
-                    v[i] = a.row_parts[static_cast<size_t>(seq_row(a, s, g0 + ri)) * a.cmax + (e - ri * C)];
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t e = e0 + tid + kNT * i;
-                if (e < n) sh.st[e] = v[i];
-            }
-        }
-        __syncthreads();
-        merge_staged<true>(sh.st, gn, C, a.log2e_over_T, sh.rs + g0);
-        __syncthreads();
-    }
+    merge_rows_global<true>(a, s, nrows, a.log2e_over_T, sh.rs);
+    __syncthreads();
     if (warp == 0) {
         const uint32_t n = decide_sequence<true>(a, s, sh.pre, sh.rs, sh.rs + rows_t, chunk == 0);
         if (lane == 0) {
