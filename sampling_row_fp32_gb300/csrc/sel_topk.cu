@@ -1176,9 +1176,11 @@ __device__ __forceinline__ void sort_desc8(uint32_t (&e)[8]) {
 // (Z, and the mean log-weight gbar, from the main launch's chunk sums).
 // Decides the survivor set as a range of candidate keys: a prefix or window
 // of the sorted candidates where a top-p or typical cut applies, or every id
-// at or above a value threshold (min-p, top-n-sigma) otherwise. A cut that
-// would need candidates past the kFullCand most probable ones is not
-// decided: the row fails closed and kErrBeyond is raised. One warp.
+// at or above a value threshold (min-p, top-n-sigma) otherwise. A top-p
+// cut or a typical window that would need candidates past the kFullCand
+// most probable ones is left to the cut search over the row (valid 2 or 3);
+// on vocabulary shards, where that search is not run, the row fails closed
+// and kErrBeyond is raised. One warp.
 __device__ void full_row_plan(const uint64_t* sorted, float* scratch, uint32_t n, uint32_t row, bool nonfinite,
                               const TopkArgs& a, double Z, double gbar_all, double sigma, float u) {
     const int lane = threadIdx.x & 31;
@@ -1706,6 +1708,16 @@ __global__ void __launch_bounds__(kNT) full_draw_find_kernel(TopkArgs a) {
 // prefix takes follows from the masses; when it takes only some of them,
 // one more pass finds the last of those in id order (ties go to lower ids,
 // as everywhere). min-p then keeps x >= mp_floor.
+// A locally typical window past the candidates (valid 3) is found the same
+// way on another key first: the score |-ln P - H| of the chain is
+// |x - xs| / Tf with xs = M + Tf * gbar the typical logit, so the window is
+// the ids closest to xs up to typical_p of C's mass (sort key: the
+// complement of the key of |x - xs|), a value range [wa, wb] since rounded
+// |x - xs| is monotone on either side of xs. A run of equal logits at the
+// cut distance keeps its lowest ids (kPlanTopLow marks such a run at the
+// top value). Top-p then searches inside the window, and min-p compares
+// with its top value. Under top-n-sigma with C past the candidates the
+// search first sums C's mass and first moment for xs.
 //
 // One thread-block cluster of kCutCL blocks per row (rows whose plan is
 // already decided return at once): block b of the cluster takes a
