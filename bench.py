@@ -630,8 +630,7 @@ STEP_LAUNCHES = [
     ("argmax", "argmax_kernel"), ("argmax", "argmax_finish_kernel"),
     ("topk", "topk_kernel"), ("topk", "topk_finish_kernel<0"),
     ("sample", "topk_kernel"), ("sample", "topk_finish_kernel<1"),
-    ("spec_rejection", "spec_phase1_kernel"), ("spec_rejection", "spec_decide_draw_kernel"),
-    ("spec_rejection", "spec_draw_find_kernel"),
+    ("spec_rejection", "spec_phase1_kernel"), ("spec_rejection", "spec_decide_draw_cl_kernel"),
     ("spec_argmax", "argmax_kernel"), ("spec_argmax", "spec_argmax_finish_kernel"),
 ]
 TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")

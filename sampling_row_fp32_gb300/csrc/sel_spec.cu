@@ -25,21 +25,27 @@
 //    block waits on another).
 //  Decision: a launch that follows by programmatic dependent launch reads
 //    the slots (argmax rule) or merges each row's chunks in chunk order, and
-//    runs the sequence's acceptance chain. In the rejection rule with
-//    K <= 64 this is fused into phase 2a:
-//    every block of a sequence stages the sequence's chunk statistics in
-//    shared memory and reaches the same decision.
-//  Phase 2 (rejection rule only): 2a blocks stream the one or two rows the
-//    decision names (target and draft row j*, or target row K), summing the
-//    residual (and p, for the fallback) per chunk; 2b, one block per
-//    sequence, finds the chunk where u_fin * total falls and scans it in id
-//    order for the drawn token. Rows are therefore read at most twice, and
-//    only the rejecting position's rows are read again.
+//    runs the sequence's acceptance chain.
+//  Draw (rejection rule only): the rows the decision names (target and
+//    draft row j*, or target row K) are read again and the token is drawn
+//    from the residual (or p) in id order. Small batches (every sequence's
+//    cluster on the GPU at once, K <= 64, V <= 262,144, 16-byte rows) take
+//    one launch of thread-block clusters, one per sequence, that merges,
+//    decides, sums its slices and finds the token, exchanging slice masses
+//    through distributed shared memory. Other batches take two launches:
+//    blocks of 4,096 ids that merge, decide and sum their chunk (K <= 64;
+//    a separate merge launch first beyond), then one block per sequence
+//    that finds the chunk where u_fin * total falls and scans it in id
+//    order. Rows are read at most twice, and only the rejecting position's
+//    rows are read again.
 // exp((x - m) / T) is computed as 2^((x - m) * log2(e) / T) with the SFU's
 // exp2 (relative error about 2^-22). Each thread sums its values in fp32;
 // sums across threads, blocks and chunks are float-float (about 44 bits), so
-// the CDF is accurate to ~1e-7 of its total.
+// the CDF is accurate to ~1e-7 of its total (the cluster draw sums a warp's
+// lanes in fp32 too: within 1e-6).
 #include <cfloat>
+
+#include <cooperative_groups.h>
 
 #include "sel_plan.h"
 #include "sel_units.cuh"
@@ -181,10 +187,11 @@ __device__ __forceinline__ void load_chain_pre(const SpecArgs& a, uint32_t s, Ch
 // and logits from `pre`. Returns, in every lane, the number of accepted
 // positions n (K: all), or kNoIdx for an invalid sequence. With `write` the
 // emitted tokens and the accepted count are stored (the rejection rule's
-// em[n] is left to the draw).
+// em[n] is left to the draw). Without `write_n` em[n] is not stored at all
+// (another block stores the draw there).
 template <bool kRej>
 __device__ uint32_t decide_sequence(const SpecArgs& a, uint32_t s, const ChainPre& pre, const RowPart* tstat,
-                                    const RowPart* dstat, bool write) {
+                                    const RowPart* dstat, bool write, bool write_n = true) {
     const uint32_t lane = threadIdx.x & 31u;
     const uint32_t K = a.K, V = a.V;
     const uint32_t nt = a.S * (K + 1u);
@@ -250,7 +257,7 @@ __device__ uint32_t decide_sequence(const SpecArgs& a, uint32_t s, const ChainPr
             uint32_t v = SEL_INVALID_ID;  // in the rejection rule em[n] is the phase-2 draw
             if (j < n) v = token(j);
             else if (!kRej && j == n) v = tstat[n].idx & ~kNonfiniteBit;
-            em[j] = v;
+            if (write_n || j != n) em[j] = v;
         }
         if (lane == 0) a.accepted[s] = n;
     }
@@ -659,7 +666,8 @@ constexpr uint32_t kDrawPer = 16;                   // ids per thread and chunk
 constexpr uint32_t kDrawChunkMax = kNT * kDrawPer;  // 4,096
 // Weights of 4 elements of the draw distribution: p = exp((x - m_p) / T) / Z_p
 // and the residual max(p - q, 0) (p again for a bonus draw). Padding (-inf)
-// weighs 0.
+// weighs 0. Every operation rounds on its own (no contraction), so the sum
+// and the find passes get the same bits wherever they inline this.
 __device__ __forceinline__ void quad_weights(const float4& xp, const float4& xq, bool residual, float pm,
                                              float pinv, float qm, float qinv, float c, float (&pw)[4],
                                              float (&rw)[4]) {
@@ -667,10 +675,10 @@ __device__ __forceinline__ void quad_weights(const float4& xp, const float4& xq,
     const float fq[4] = {xq.x, xq.y, xq.z, xq.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const float p = ex2_approx((fp[j] - pm) * c) * pinv;
-        const float q = residual ? ex2_approx((fq[j] - qm) * c) * qinv : 0.0f;
+        const float p = __fmul_rn(ex2_approx(__fmul_rn(__fsub_rn(fp[j], pm), c)), pinv);
+        const float q = residual ? __fmul_rn(ex2_approx(__fmul_rn(__fsub_rn(fq[j], qm), c)), qinv) : 0.0f;
         pw[j] = p;
-        rw[j] = residual ? fmaxf(p - q, 0.0f) : p;
+        rw[j] = residual ? fmaxf(__fsub_rn(p, q), 0.0f) : p;
     }
 }
 
@@ -1020,6 +1028,293 @@ __global__ void __launch_bounds__(kNT) spec_draw_find_kernel(DrawArgs a) {
 }
 
 // ---------------------------------------------------------------------------
+// Rejection rule for small batches: the decision and the whole draw in one
+// launch, one thread-block cluster per sequence. CTA r of the cluster takes
+// ids [r R, (r + 1) R) of the vocabulary, warp w of it the R / 32 ids from
+// r R + w R / 32. Every CTA merges the sequence's rows and runs its chain
+// (the same decision everywhere); CTA 0 stores the outputs but the drawn
+// token. Each CTA then loads its slice of the one or two rows the decision
+// names into registers (lane l of a warp: quads l, l + 32, ... of the warp's
+// ids, so every load is coalesced) and sums the weights: fp32 within a warp,
+// float-float across warps. Warp 0 keeps the prefixes of the warps' masses,
+// and the CTA's masses cross the cluster through distributed shared memory:
+// each CTA stores them into every CTA's table before one cluster barrier,
+// so no CTA touches another's memory after it. Every CTA scans the table in
+// rank order and finds the CTA where u_fin * total falls; only that CTA goes
+// on. Its warp 0 finds the warp from the kept prefixes, and that warp finds
+// the row of 128 ids (quad j of every lane), the lane and the id, with the
+// weights recomputed from its registers. Compared with the chunk-sum and
+// find launches this saves a launch, the L2 round trips between the sums
+// and the find, and the second read of the chunk the draw falls in.
+// Accuracy: a lane sums at most 16 weights and a warp 32 lane sums in fp32
+// (at most 9 roundings, below 6e-7 of the warp's mass); the rest is
+// float-float, so the CDF stays within 1e-6 of its total.
+// ---------------------------------------------------------------------------
+constexpr int kClNT = 1024;                           // threads per CTA
+constexpr int kClWarps = kClNT / 32;
+constexpr uint32_t kClMax = 16;                       // CTAs per cluster at most (a non-portable size)
+constexpr uint32_t kClSliceMin = 4u * kClNT;          // ids per CTA: a quad per lane at least
+constexpr uint32_t kClSliceMax = 4u * kClSliceMin;    // ... and four at most (two rows: 32 registers)
+static_assert(kClWarps == 32, "one lane per warp in the CTA-wide sums");
+
+// The slice R (a power of two) for a row of V ids, or 0 when a cluster of
+// kClMax CTAs cannot cover it.
+inline uint32_t cl_slice(uint32_t V) {
+    uint32_t R = kClSliceMin;
+    while (static_cast<uint64_t>(R) * kClMax < V && R < kClSliceMax) R <<= 1;
+    return static_cast<uint64_t>(R) * kClMax >= V ? R : 0u;
+}
+
+struct ClShared {
+    RowPart rs[kChainRows];
+    ChainPre pre;
+    DrawPlan plan;
+    FF wr[kClWarps], wp[kClWarps];    // the warps' residual and target masses
+    FF wir[kClWarps], wip[kClWarps];  // ... and their inclusive prefixes in warp order
+    FF all_r[kClMax], all_p[kClMax];  // every CTA's masses, stored here by each CTA
+    FF target, before;                // u_fin * total; the mass of the CTAs before the drawing one
+    FF wstart;                        // ... and of the warps before the drawing warp
+    uint32_t rstar, use_p, cross;
+};
+
+// Warp sum and inclusive warp scan of floats (a fixed order: the butterfly
+// gives every lane the same sum).
+__device__ __forceinline__ float warp_sum_f32(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_scan_f32(float v) {
+    const uint32_t lane = threadIdx.x & 31u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(kFull, v, o);
+        if (lane >= static_cast<uint32_t>(o)) v += t;
+    }
+    return v;
+}
+
+// The first lane with mass whose inclusive prefix passes the target, else
+// (rounding) the last lane with mass, else kNoIdx; every lane gets it.
+__device__ __forceinline__ uint32_t crossing_lane(bool mass, const FF& target, const FF& incl) {
+    const uint32_t hit = __ballot_sync(kFull, mass && ff_lt(target, incl));
+    const uint32_t has = __ballot_sync(kFull, mass);
+    return hit ? static_cast<uint32_t>(__ffs(hit) - 1) : (has ? 31u - __clz(has) : kNoIdx);
+}
+
+__global__ void __launch_bounds__(kClNT, 1) spec_decide_draw_cl_kernel(SpecArgs a, DrawArgs b, uint32_t R) {
+    __shared__ ClShared sh;
+    namespace cg = cooperative_groups;
+    cg::cluster_group cl = cg::this_cluster();
+    const uint32_t rank = blockIdx.x, s = blockIdx.y, CL = gridDim.x;
+    const uint32_t K = a.K, V = a.V;
+    const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
+    const uint32_t rows_t = K + 1u, nrows = 2u * K + 1u;
+    pdl_wait();
+    pdl_trigger();
+    load_chain_pre<true>(a, s, sh.pre);
+    if (warp < static_cast<uint32_t>(kWarps)) merge_rows_global<true>(a, s, nrows, a.log2e_over_T, sh.rs);
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t n = decide_sequence<true>(a, s, sh.pre, sh.rs, sh.rs + rows_t, rank == 0, false);
+        if (lane == 0) sh.plan = make_plan(n, K, sh.rs, sh.rs + rows_t);
+    }
+    __syncthreads();
+    const DrawPlan d = sh.plan;
+    if (d.kind == kDrawNone) return;  // invalid sequence: every CTA of the cluster leaves here
+
+    // this CTA's slice of the drawn rows, in registers: warp w takes the
+    // R / 32 ids from lo + w R / 32, lane l its quads l, l + 32, ... of them
+    // (every load coalesced)
+    const bool residual = d.kind == kDrawResidual;
+    const uint32_t lo = rank * R, hi = min(V, lo + R);
+    const uint32_t m = R / (4u * kClNT);  // quads per lane
+    const uint32_t sw = lo + warp * (R / kClWarps);
+    const float* prow = plan_prow(b, s, d);
+    const float* qrow = residual ? plan_qrow(b, s, d) : prow;
+    const float c = b.log2e_over_T;
+    const float4 none = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    float4 xp[4], xq[4];
+#pragma unroll
+    for (uint32_t j = 0; j < 4u; ++j) {
+        const uint32_t e = sw + 4u * (lane + 32u * j);
+        xp[j] = j < m ? ld_quad<true>(prow, e, hi, -INFINITY) : none;
+        xq[j] = residual && j < m ? ld_quad<true>(qrow, e, hi, -INFINITY) : none;
+    }
+    float rsum = 0.0f, psum = 0.0f;
+#pragma unroll
+    for (uint32_t j = 0; j < 4u; ++j) {
+        float pw[4], rw[4];
+        quad_weights(xp[j], xq[j], residual, d.pm, d.pinv, d.qm, d.qinv, c, pw, rw);
+        rsum += (rw[0] + rw[1]) + (rw[2] + rw[3]);
+        psum += (pw[0] + pw[1]) + (pw[2] + pw[3]);
+    }
+    // the warps' masses in fp32 (each lane's run is already an fp32 sum),
+    // then float-float across the warps: warp 0 keeps the inclusive prefixes
+    // for the drawing CTA and stores the CTA's masses into every CTA's table
+    {
+        const float wr = warp_sum_f32(rsum), wp = warp_sum_f32(psum);
+        if (lane == 0) {
+            sh.wr[warp] = FF{wr, 0.0f};
+            sh.wp[warp] = FF{wp, 0.0f};
+        }
+        __syncthreads();
+        if (warp == 0) {
+            const FF ir = ff_warp_scan(sh.wr[lane]), ip = ff_warp_scan(sh.wp[lane]);
+            sh.wir[lane] = ir;
+            sh.wip[lane] = ip;
+            const FF r = ff_shfl(ir, 31), p = ff_shfl(ip, 31);
+            if (lane < CL) {
+                cl.map_shared_rank(sh.all_r, lane)[rank] = r;
+                cl.map_shared_rank(sh.all_p, lane)[rank] = p;
+            }
+        }
+    }
+    cl.sync();  // every table is complete; no CTA touches another's memory from here on
+
+    // the CTAs' masses in rank order: the totals and the drawing CTA
+    if (warp == 0) {
+        const FF r = lane < CL ? sh.all_r[lane] : FF{0.0f, 0.0f};
+        const FF p = lane < CL ? sh.all_p[lane] : FF{0.0f, 0.0f};
+        const FF ir = ff_warp_scan(r), ip = ff_warp_scan(p);
+        const FF rt = ff_shfl(ir, 31), pt = ff_shfl(ip, 31);
+        const bool up = !(rt.hi > 0.0f);  // residual empty by rounding: draw from p
+        const FF target = ff_mul_f(up ? pt : rt, sh.pre.uf);
+        const FF w = up ? p : r, incl = up ? ip : ir;
+        const FF prev = ff_shfl_up(incl, 1);
+        const uint32_t rs = crossing_lane(lane < CL && w.hi > 0.0f, target, incl);
+        const uint32_t rr = rs == kNoIdx ? 0u : rs;  // no mass anywhere: CTA 0
+        const FF before = ff_shfl(lane == 0 ? FF{0.0f, 0.0f} : prev, static_cast<int>(rr));
+        if (lane == 0) {
+            sh.rstar = rr;
+            sh.use_p = up ? 1u : 0u;
+            sh.target = target;
+            sh.before = before;
+        }
+    }
+    __syncthreads();
+    if (sh.rstar != rank) return;
+
+    // the drawing CTA: the warp from the prefixes kept above; that warp
+    // takes its rows of 128 ids (quad j of every lane), then the lane, then
+    // the id, recomputing the weights from its registers
+    const bool up = sh.use_p != 0u;
+    const FF target = sh.target;
+    if (warp == 0) {
+        const FF* pre = up ? sh.wip : sh.wir;
+        const FF w = up ? sh.wp[lane] : sh.wr[lane];
+        const FF incl = ff_add(sh.before, pre[lane]);
+        const FF start = lane == 0 ? sh.before : ff_add(sh.before, pre[lane - 1u]);
+        const uint32_t wc = crossing_lane(w.hi > 0.0f, target, incl);
+        if (lane == 0) sh.cross = wc;
+        if (lane == wc) sh.wstart = start;
+    }
+    __syncthreads();
+    uint32_t* out = b.emitted + static_cast<size_t>(s) * (K + 1u) + d.jstar;
+    const uint32_t wc = sh.cross;
+    if (wc == kNoIdx) {
+        if (tid == 0) *out = lo;  // no mass anywhere: the first id, as the chunked find gives
+    } else if (warp == wc) {
+        float wq[4][4], sj[4], tj[4];
+#pragma unroll
+        for (uint32_t j = 0; j < 4u; ++j) {
+            float pw[4], rw[4];
+            quad_weights(xp[j], xq[j], residual, d.pm, d.pinv, d.qm, d.qinv, c, pw, rw);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) wq[j][k] = up ? pw[k] : rw[k];
+            sj[j] = (wq[j][0] + wq[j][1]) + (wq[j][2] + wq[j][3]);
+        }
+#pragma unroll
+        for (uint32_t j = 0; j < 4u; ++j) tj[j] = warp_sum_f32(sj[j]);
+        // the row (j) where the target falls, else the last with mass
+        FF run = sh.wstart, jstart = run, lstart = run;
+        uint32_t js = kNoIdx, jl = kNoIdx;
+#pragma unroll
+        for (uint32_t j = 0; j < 4u; ++j) {
+            const FF nx = ff_add(run, FF{tj[j], 0.0f});
+            if (tj[j] > 0.0f) {
+                if (js == kNoIdx && ff_lt(target, nx)) {
+                    js = j;
+                    jstart = run;
+                }
+                jl = j;
+                lstart = run;
+            }
+            run = nx;
+        }
+        if (js == kNoIdx) {
+            js = jl == kNoIdx ? 0u : jl;
+            jstart = lstart;
+        }
+        // the lane: an fp32 scan of the row's lane sums from the row's start
+        const float sl = js == 0u ? sj[0] : (js == 1u ? sj[1] : (js == 2u ? sj[2] : sj[3]));
+        const float sc = warp_scan_f32(sl);
+        const float ex = __shfl_up_sync(kFull, sc, 1);
+        const FF li = ff_add(jstart, FF{sc, 0.0f});
+        uint32_t tl = crossing_lane(sl > 0.0f, target, li);
+        tl = tl == kNoIdx ? 0u : tl;
+        if (lane == tl) {
+            // the quad's ids in order
+            float w4[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                w4[k] = js == 0u ? wq[0][k] : (js == 1u ? wq[1][k] : (js == 2u ? wq[2][k] : wq[3][k]));
+            const uint32_t e0 = sw + 4u * (lane + 32u * js);
+            FF r2 = lane == 0 ? jstart : ff_add(jstart, FF{ex, 0.0f});
+            uint32_t pick = kNoIdx, last = kNoIdx;
+#pragma unroll
+            for (uint32_t k = 0; k < 4u; ++k) {
+                r2 = ff_add(r2, FF{w4[k], 0.0f});
+                if (w4[k] > 0.0f) {
+                    last = e0 + k;
+                    if (pick == kNoIdx && ff_lt(target, r2)) pick = e0 + k;
+                }
+            }
+            *out = pick != kNoIdx ? pick : (last != kNoIdx ? last : e0);
+        }
+    }
+}
+
+// Host side: how many clusters of `cl` CTAs of spec_decide_draw_cl_kernel
+// the GPU runs at once (each CTA fills an SM's registers, and a cluster must
+// fit in one GPU processing cluster), for cl = 1 .. kClMax, found once; 0
+// when the attribute cannot be set or a query fails, which keeps the
+// chunked path.
+inline uint32_t cl_active_clusters(uint32_t cl) {
+    struct Table {
+        uint32_t n[kClMax + 1] = {};
+    };
+    static const Table t = [] {
+        Table r;
+        if (cudaFuncSetAttribute(spec_decide_draw_cl_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess) {
+            (void)cudaGetLastError();
+            return r;
+        }
+        for (uint32_t c = 1; c <= kClMax; ++c) {
+            cudaLaunchConfig_t cfg{};
+            cfg.gridDim = dim3(c, 1, 1);
+            cfg.blockDim = dim3(kClNT, 1, 1);
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = c;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, spec_decide_draw_cl_kernel, &cfg) != cudaSuccess || n < 0) {
+                (void)cudaGetLastError();
+                n = 0;
+            }
+            r.n[c] = static_cast<uint32_t>(n);
+        }
+        return r;
+    }();
+    return cl <= kClMax ? t.n[cl] : 0u;
+}
+
+// ---------------------------------------------------------------------------
 // Closed-form diagnostics (mlxcel rules, "Verifying the gain"): per verified
 // position, sum_x min(p, q) and sum_x p q from the phase-1 row statistics and
 // one more pass over the target and draft rows of the position.
@@ -1243,6 +1538,15 @@ extern "C" sel_status spec_accept(const float* d_target, const float* d_draft, c
     const dim3 grid2(S * chunks2);
     cudaError_t e2;
     if (K <= kPre && chunks1 <= kStage) {
+        // small batches: one cluster per sequence does the decision and the
+        // whole draw, when every sequence's cluster runs on the GPU at once
+        const uint32_t R = vec ? cl_slice(V) : 0u;
+        const uint32_t CL = R ? ceil_div(V, R) : 0u;
+        if (R && S <= cl_active_clusters(CL)) {
+            e2 = launch_pdl_cluster(spec_decide_draw_cl_kernel, dim3(CL, S), dim3(kClNT), CL, 0,
+                                    stream, a, b, R);
+            return e2 == cudaSuccess ? SEL_OK : SEL_ECUDA;
+        }
         // merge, chain and chunk sums in one launch
         e2 = vec ? launch_pdl(spec_decide_draw_kernel<true>, grid2, dim3(kNT), 0, stream, a, b)
                  : launch_pdl(spec_decide_draw_kernel<false>, grid2, dim3(kNT), 0, stream, a, b);

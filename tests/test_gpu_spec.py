@@ -38,13 +38,34 @@ def test_spec_workload(orc, mode):
 
 
 @pytest.mark.parametrize("S,K,V,T", [(3, 1, 5, 1.0), (4, 3, 1000, 0.8), (5, 4, 8191, 1.0),
-                                     (2, 8, 33_333, 1.3), (6, 2, 248_320, 1.0), (9, 0, 4096, 1.0)])
+                                     (2, 8, 33_333, 1.3), (6, 2, 248_320, 1.0), (9, 0, 4096, 1.0),
+                                     (3, 3, 100_000, 1.0), (4, 2, 50_000, 0.9)])
 @pytest.mark.parametrize("misalign", [False, True])
 @pytest.mark.parametrize("mode", [REJ, ARG])
 def test_shapes(orc, S, K, V, T, misalign, mode):
     si = synth.spec_inputs(S=S, K=K, V=V, temperature=T, seed_target=S + K, seed_draft=V,
                            seed_u=int(T * 10) + 3, sigma_noise=0.7)
     run_both(orc, si, mode, misalign)
+
+
+def _head(si, n, start=0):
+    """Sequences start .. start + n - 1 of a SpecInputs."""
+    sl = slice(start, start + n)
+    return synth.SpecInputs(si.target[sl], si.draft[sl], si.draft_tokens[sl], si.u_acc[sl], si.u_fin[sl],
+                            si.temperature)
+
+
+def test_both_draw_paths_agree(orc):
+    """Twelve sequences over V = 248,320 take the two-launch draw (twelve
+    clusters of 16 CTAs do not fit on the GPU at once); the first seven
+    alone take the one-launch cluster draw. Both match the oracle, and so
+    each other."""
+    si = synth.spec_inputs(S=12, K=3, V=248_320, seed_target=5, seed_draft=6, seed_u=7, sigma_noise=0.7)
+    acc, emi, ref = run_both(orc, si, REJ)
+    assert np.any(acc < 3) and np.any(acc == 3)  # residual and bonus draws both occur
+    acc7, emi7, _ = run_both(orc, _head(si, 7), REJ)
+    np.testing.assert_array_equal(acc7, acc[:7])
+    np.testing.assert_array_equal(emi7, emi[:7])
 
 
 def test_bench_workload(orc):
@@ -139,6 +160,25 @@ def test_stream_matches_target_by_chi_square(orc):
     rate = float(np.mean(acc == 1))
     smin = float(np.minimum(p, q).sum())
     assert abs(rate - smin) < 5 * math.sqrt(smin * (1 - smin) / acc.size)
+
+
+def test_chi_square_on_the_cluster_draw(orc):
+    """The same recipe with the vocabulary padded to 8 ids (two of mass 0,
+    so rows are whole 16-byte quads) in batches of 150 sequences: every
+    batch takes the one-launch cluster draw. The padding is never emitted."""
+    g = oracle_pins.golden("chi_square_recipe.json")
+    rng = np.random.default_rng(61)
+    p = rng.dirichlet(np.ones(6) * 2)
+    q = rng.dirichlet(np.ones(6) * 2)
+    pad = np.zeros(2)
+    si = _rounds(np.concatenate([p, pad]), np.concatenate([q, pad]), g["samples"], 62)
+    first = []
+    for b0 in range(0, g["samples"], 150):
+        _, emi, _ = run_both(orc, _head(si, 150, b0), REJ)
+        first.append(emi[:, 0])
+    counts = np.bincount(np.concatenate(first).astype(np.int64), minlength=8)
+    assert counts[6:].sum() == 0
+    assert oracle_pins.chi_square(counts[:6], p) <= g["critical"]
 
 
 def test_ceiling_example(orc):
