@@ -1040,10 +1040,11 @@ __global__ void __launch_bounds__(kNT) spec_draw_find_kernel(DrawArgs a) {
 // and the CTA's masses cross the cluster through distributed shared memory:
 // each CTA stores them into every CTA's table before one cluster barrier,
 // so no CTA touches another's memory after it. Every CTA scans the table in
-// rank order and finds the CTA where u_fin * total falls; only that CTA goes
-// on. Its warp 0 finds the warp from the kept prefixes, and that warp finds
-// the row of 128 ids (quad j of every lane), the lane and the id, with the
-// weights recomputed from its registers. Compared with the chunk-sum and
+// rank order and finds the CTA where u_fin * total falls (the drawing CTA's
+// warp 0 also finds the warp, from the kept prefixes); only that CTA goes
+// on. The warp finds the row of 128 ids (quad j of every lane) and the lane
+// from row masses the sum pass kept in shared memory, then the id, with the
+// quad's weights recomputed from its registers. Compared with the chunk-sum and
 // find launches this saves a launch, the L2 round trips between the sums
 // and the find, and the second read of the chunk the draw falls in.
 // Accuracy: a lane sums at most 16 weights and a warp 32 lane sums in fp32
@@ -1071,9 +1072,12 @@ struct ClShared {
     DrawPlan plan;
     FF wr[kClWarps], wp[kClWarps];    // the warps' residual and target masses
     FF wir[kClWarps], wip[kClWarps];  // ... and their inclusive prefixes in warp order
+    float rows_r[4][kClWarps][32];    // each lane's residual and target mass in each
+    float rows_p[4][kClWarps][32];    // row of 128 ids of its warp (quad j of the lanes)
+    float tjr[kClWarps][4];           // each warp's residual mass per row
     FF all_r[kClMax], all_p[kClMax];  // every CTA's masses, stored here by each CTA
-    FF target, before;                // u_fin * total; the mass of the CTAs before the drawing one
-    FF wstart;                        // ... and of the warps before the drawing warp
+    FF target;                        // u_fin * total
+    FF wstart;                        // the mass before the drawing warp
     uint32_t rstar, use_p, cross;
 };
 
@@ -1141,21 +1145,31 @@ __global__ void __launch_bounds__(kClNT, 1) spec_decide_draw_cl_kernel(SpecArgs 
         xp[j] = j < m ? ld_quad<true>(prow, e, hi, -INFINITY) : none;
         xq[j] = residual && j < m ? ld_quad<true>(qrow, e, hi, -INFINITY) : none;
     }
-    float rsum = 0.0f, psum = 0.0f;
+    // each lane's mass in each row of 128 ids (kept in shared memory for the
+    // find), the warp's residual mass per row, and the warp's masses, all in
+    // fp32; then float-float across the warps: warp 0 keeps the inclusive
+    // prefixes for the drawing CTA and stores the CTA's masses into every
+    // CTA's table
+    float sjr[4], sjp[4], psum = 0.0f;
 #pragma unroll
     for (uint32_t j = 0; j < 4u; ++j) {
         float pw[4], rw[4];
         quad_weights(xp[j], xq[j], residual, d.pm, d.pinv, d.qm, d.qinv, c, pw, rw);
-        rsum += (rw[0] + rw[1]) + (rw[2] + rw[3]);
-        psum += (pw[0] + pw[1]) + (pw[2] + pw[3]);
+        sjr[j] = (rw[0] + rw[1]) + (rw[2] + rw[3]);
+        sjp[j] = (pw[0] + pw[1]) + (pw[2] + pw[3]);
+        psum += sjp[j];
+        sh.rows_r[j][warp][lane] = sjr[j];
+        sh.rows_p[j][warp][lane] = sjp[j];
     }
-    // the warps' masses in fp32 (each lane's run is already an fp32 sum),
-    // then float-float across the warps: warp 0 keeps the inclusive prefixes
-    // for the drawing CTA and stores the CTA's masses into every CTA's table
     {
-        const float wr = warp_sum_f32(rsum), wp = warp_sum_f32(psum);
+        float tr[4];
+#pragma unroll
+        for (uint32_t j = 0; j < 4u; ++j) tr[j] = warp_sum_f32(sjr[j]);
+        const float wp = warp_sum_f32(psum);
         if (lane == 0) {
-            sh.wr[warp] = FF{wr, 0.0f};
+#pragma unroll
+            for (uint32_t j = 0; j < 4u; ++j) sh.tjr[warp][j] = tr[j];
+            sh.wr[warp] = FF{((tr[0] + tr[1]) + tr[2]) + tr[3], 0.0f};
             sh.wp[warp] = FF{wp, 0.0f};
         }
         __syncthreads();
@@ -1174,13 +1188,16 @@ __global__ void __launch_bounds__(kClNT, 1) spec_decide_draw_cl_kernel(SpecArgs 
 
     // the CTAs' masses in rank order: the totals and the drawing CTA
     if (warp == 0) {
-        const FF r = lane < CL ? sh.all_r[lane] : FF{0.0f, 0.0f};
-        const FF p = lane < CL ? sh.all_p[lane] : FF{0.0f, 0.0f};
-        const FF ir = ff_warp_scan(r), ip = ff_warp_scan(p);
-        const FF rt = ff_shfl(ir, 31), pt = ff_shfl(ip, 31);
-        const bool up = !(rt.hi > 0.0f);  // residual empty by rounding: draw from p
-        const FF target = ff_mul_f(up ? pt : rt, sh.pre.uf);
-        const FF w = up ? p : r, incl = up ? ip : ir;
+        FF w = lane < CL ? sh.all_r[lane] : FF{0.0f, 0.0f};
+        FF incl = ff_warp_scan(w);
+        FF tot = ff_shfl(incl, 31);
+        const bool up = !(tot.hi > 0.0f);  // residual empty by rounding: draw from p
+        if (up) {
+            w = lane < CL ? sh.all_p[lane] : FF{0.0f, 0.0f};
+            incl = ff_warp_scan(w);
+            tot = ff_shfl(incl, 31);
+        }
+        const FF target = ff_mul_f(tot, sh.pre.uf);
         const FF prev = ff_shfl_up(incl, 1);
         const uint32_t rs = crossing_lane(lane < CL && w.hi > 0.0f, target, incl);
         const uint32_t rr = rs == kNoIdx ? 0u : rs;  // no mass anywhere: CTA 0
@@ -1189,43 +1206,34 @@ __global__ void __launch_bounds__(kClNT, 1) spec_decide_draw_cl_kernel(SpecArgs 
             sh.rstar = rr;
             sh.use_p = up ? 1u : 0u;
             sh.target = target;
-            sh.before = before;
+        }
+        if (rr == rank) {
+            // the drawing CTA: the warp, from the prefixes kept above
+            const FF* pre = up ? sh.wip : sh.wir;
+            const FF ww = up ? sh.wp[lane] : sh.wr[lane];
+            const FF wi = ff_add(before, pre[lane]);
+            const FF ws = lane == 0 ? before : ff_add(before, pre[lane - 1u]);
+            const uint32_t wc = crossing_lane(ww.hi > 0.0f, target, wi);
+            if (lane == 0) sh.cross = wc;
+            if (lane == wc) sh.wstart = ws;
         }
     }
     __syncthreads();
     if (sh.rstar != rank) return;
 
-    // the drawing CTA: the warp from the prefixes kept above; that warp
-    // takes its rows of 128 ids (quad j of every lane), then the lane, then
-    // the id, recomputing the weights from its registers
+    // the drawing CTA: its warp takes its row of 128 ids (quad j of every
+    // lane) and the lane from the masses kept above, then the id,
+    // recomputing the quad's weights from its registers
     const bool up = sh.use_p != 0u;
     const FF target = sh.target;
-    if (warp == 0) {
-        const FF* pre = up ? sh.wip : sh.wir;
-        const FF w = up ? sh.wp[lane] : sh.wr[lane];
-        const FF incl = ff_add(sh.before, pre[lane]);
-        const FF start = lane == 0 ? sh.before : ff_add(sh.before, pre[lane - 1u]);
-        const uint32_t wc = crossing_lane(w.hi > 0.0f, target, incl);
-        if (lane == 0) sh.cross = wc;
-        if (lane == wc) sh.wstart = start;
-    }
-    __syncthreads();
     uint32_t* out = b.emitted + static_cast<size_t>(s) * (K + 1u) + d.jstar;
     const uint32_t wc = sh.cross;
     if (wc == kNoIdx) {
         if (tid == 0) *out = lo;  // no mass anywhere: the first id, as the chunked find gives
     } else if (warp == wc) {
-        float wq[4][4], sj[4], tj[4];
+        float tj[4];
 #pragma unroll
-        for (uint32_t j = 0; j < 4u; ++j) {
-            float pw[4], rw[4];
-            quad_weights(xp[j], xq[j], residual, d.pm, d.pinv, d.qm, d.qinv, c, pw, rw);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) wq[j][k] = up ? pw[k] : rw[k];
-            sj[j] = (wq[j][0] + wq[j][1]) + (wq[j][2] + wq[j][3]);
-        }
-#pragma unroll
-        for (uint32_t j = 0; j < 4u; ++j) tj[j] = warp_sum_f32(sj[j]);
+        for (uint32_t j = 0; j < 4u; ++j) tj[j] = up ? warp_sum_f32(sh.rows_p[j][wc][lane]) : sh.tjr[wc][j];
         // the row (j) where the target falls, else the last with mass
         FF run = sh.wstart, jstart = run, lstart = run;
         uint32_t js = kNoIdx, jl = kNoIdx;
@@ -1247,7 +1255,7 @@ __global__ void __launch_bounds__(kClNT, 1) spec_decide_draw_cl_kernel(SpecArgs 
             jstart = lstart;
         }
         // the lane: an fp32 scan of the row's lane sums from the row's start
-        const float sl = js == 0u ? sj[0] : (js == 1u ? sj[1] : (js == 2u ? sj[2] : sj[3]));
+        const float sl = up ? sh.rows_p[js][wc][lane] : sh.rows_r[js][wc][lane];
         const float sc = warp_scan_f32(sl);
         const float ex = __shfl_up_sync(kFull, sc, 1);
         const FF li = ff_add(jstart, FF{sc, 0.0f});
@@ -1255,10 +1263,12 @@ __global__ void __launch_bounds__(kClNT, 1) spec_decide_draw_cl_kernel(SpecArgs 
         tl = tl == kNoIdx ? 0u : tl;
         if (lane == tl) {
             // the quad's ids in order
-            float w4[4];
+            const float4 qp = js == 0u ? xp[0] : (js == 1u ? xp[1] : (js == 2u ? xp[2] : xp[3]));
+            const float4 qq = js == 0u ? xq[0] : (js == 1u ? xq[1] : (js == 2u ? xq[2] : xq[3]));
+            float pw[4], rw[4], w4[4];
+            quad_weights(qp, qq, residual, d.pm, d.pinv, d.qm, d.qinv, c, pw, rw);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                w4[k] = js == 0u ? wq[0][k] : (js == 1u ? wq[1][k] : (js == 2u ? wq[2][k] : wq[3][k]));
+            for (int k = 0; k < 4; ++k) w4[k] = up ? pw[k] : rw[k];
             const uint32_t e0 = sw + 4u * (lane + 32u * js);
             FF r2 = lane == 0 ? jstart : ff_add(jstart, FF{ex, 0.0f});
             uint32_t pick = kNoIdx, last = kNoIdx;
