@@ -361,6 +361,7 @@ def gpu_arm(args, rank, world, local_rank):
         "e2e": e2e,
         "extra_ops": extra,
         "configs": named_configs(B, dev, stream),
+        "rows_sweep": rows_sweep(B, dev, stream),
     }
     return line
 
@@ -516,6 +517,80 @@ def extra_ops(B, dev, xs, drafts, tok, stream):
         B.sel_sample(xs[0], prm_typ, uu, sid, spr, ws_typ)
     torch.cuda.synchronize()
     out["sample_full_row_typical"]["failed_rows"] = int((B.ids_to_numpy(sid) == 0xFFFFFFFF).sum())
+    return out
+
+
+SWEEP_ROWS = (1, 2, 4, 8, 16, 32, 49)
+SWEEP_REPS = 110
+
+
+def rows_sweep(B, dev, stream):
+    """The metric's range: argmax, top-k (k = 20) and sampling (the step's
+    policy) on 1 .. 49 rows of V = 248,320, timed like the step's ops. The
+    verify batch's rows are repeated through a buffer of about 630 MB, and
+    call i reads the block of rows that starts i rows-sizes further on, so a
+    block is read again only after at least ~480 MB of other reads (L2 is
+    129 MB). Below a few MB a call these are bound by launch latency."""
+    import torch
+    from sampling_row_fp32_gb300 import synth
+    peak, _ = measured_peak()
+    x, _ = synth.workload_verify_batch(ROWS, V)
+    reps = 13
+    big = torch.from_numpy(np.ascontiguousarray(x)).to(dev).repeat(reps, 1)  # reps * 49 rows
+    total_rows = big.shape[0]
+    u = torch.from_numpy(synth.uniforms(5, total_rows)).to(dev)
+    prm = B.SampleParams(POLICY["temperature"], POLICY["top_k"], POLICY["top_p"], POLICY["min_p"],
+                         B.SEL_ORDER_TEMP_FIRST)
+    out = {"workload": f"rows of the verify batch, V = {V:,}; argmax, top-k k = {K_TOPK}, sampling "
+                       f"(T {POLICY['temperature']}, top_k {POLICY['top_k']}, top_p {POLICY['top_p']}, "
+                       f"min_p {POLICY['min_p']})",
+           "rows": list(SWEEP_ROWS), "argmax": [], "topk": [], "sample": []}
+    for r in SWEEP_ROWS:
+        n_blocks = total_rows // r
+        ids = torch.empty(r, dtype=torch.int32, device=dev)
+        tv = torch.empty(r, K_TOPK, device=dev)
+        ti = torch.empty(r, K_TOPK, dtype=torch.int32, device=dev)
+        sid = torch.empty(r, dtype=torch.int32, device=dev)
+        sp = torch.empty(r, device=dev)
+        ws_a = B.workspace(B.SEL_OP_ARGMAX, r, V, device=dev)
+        ws_t = B.workspace(B.SEL_OP_TOPK, r, V, K_TOPK, device=dev)
+        ws_s = B.workspace(B.SEL_OP_SAMPLE, r, V, POLICY["top_k"], device=dev)
+
+        def blk(i):
+            b = (i % n_blocks) * r
+            return big[b:b + r]
+
+        calls = {
+            "argmax": lambda i: B.sel_argmax(blk(i), ids, ws_a),
+            "topk": lambda i: B.sel_topk(blk(i), K_TOPK, tv, ti, ws_t),
+            "sample": lambda i: B.sel_sample(blk(i), prm, u[(i % n_blocks) * r:(i % n_blocks) * r + r], sid, sp,
+                                             ws_s),
+        }
+        for op, fn in calls.items():
+            with torch.cuda.stream(stream):
+                for i in range(3):
+                    fn(i)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(SWEEP_REPS):
+                    fn(i)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                g.replay()
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+            torch.cuda.synchronize()
+            us = a.elapsed_time(b) * 1e3 / SWEEP_REPS
+            nbytes = r * V * 4
+            gbs = nbytes / (us * 1e-6) / 1e9
+            out[op].append(dict({"rows": r, "us": round(us, 3), "rows_per_s": round(r / (us * 1e-6), 1),
+                                 "gbs": round(gbs, 1)}, **fracs(gbs, peak)))
+            del g
+    del big
+    torch.cuda.synchronize()
     return out
 
 
