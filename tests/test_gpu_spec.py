@@ -39,7 +39,7 @@ def test_spec_workload(orc, mode):
 
 @pytest.mark.parametrize("S,K,V,T", [(3, 1, 5, 1.0), (4, 3, 1000, 0.8), (5, 4, 8191, 1.0),
                                      (2, 8, 33_333, 1.3), (6, 2, 248_320, 1.0), (9, 0, 4096, 1.0),
-                                     (3, 3, 100_000, 1.0), (4, 2, 50_000, 0.9)])
+                                     (3, 3, 100_000, 1.0), (4, 2, 50_000, 0.9), (2, 2, 300_000, 1.0)])
 @pytest.mark.parametrize("misalign", [False, True])
 @pytest.mark.parametrize("mode", [REJ, ARG])
 def test_shapes(orc, S, K, V, T, misalign, mode):
