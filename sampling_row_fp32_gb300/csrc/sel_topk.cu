@@ -69,6 +69,7 @@ constexpr uint32_t kDrawIds = 4096;          // ids per chunk of the full-row dr
 constexpr int kDrawQ = static_cast<int>(kDrawIds / (4u * kNT));  // quads per thread and draw chunk
 constexpr uint32_t kRankMax = 512;           // rank counting up to this many candidates
 constexpr uint32_t kFastMergeLists = 32;     // one warp lane per chunk list
+constexpr float kLog2eF = 1.4426950408889634f;  // exp(y) = 2^(y log2 e) with the SFU's exp2
 
 static_assert(kBlockCap <= kCap && SEL_MAX_K <= kCap, "selection buffers");
 static_assert(4u * SEL_MAX_K * sizeof(float) <= kCap * sizeof(uint64_t), "sampling scratch fits the merge buffer");
@@ -487,15 +488,16 @@ __device__ void sample_epilogue(const uint64_t* sorted, float* scratch, uint32_t
         // l + 32; the same scans, so the same sums as the path below).
         const uint32_t j0 = lane, j1 = lane + 32u;
         float f0 = 0.0f, w0 = 0.0f, f1 = 0.0f, w1 = 0.0f;
+        const float cT = kLog2eF / T;
         if (j0 < nc) {
             const float d = key2f(cand_key(sorted[j0])) - x0;
-            w0 = expf(d / T);
-            f0 = temp_last ? expf(d) : w0;
+            w0 = ex2_approx(d * cT);
+            f0 = temp_last ? ex2_approx(d * kLog2eF) : w0;
         }
         if (j1 < nc) {
             const float d = key2f(cand_key(sorted[j1])) - x0;
-            w1 = expf(d / T);
-            f1 = temp_last ? expf(d) : w1;
+            w1 = ex2_approx(d * cT);
+            f1 = temp_last ? ex2_approx(d * kLog2eF) : w1;
         }
         float pf0 = f0, pd0 = w0, pf1 = f1, pd1 = w1;
 #pragma unroll
@@ -566,8 +568,8 @@ __device__ __noinline__ void sample_epilogue_general(const uint64_t* sorted, flo
             if (j < hi) {
                 if (weights) {
                     const float d = key2f(cand_key(sorted[j])) - x0;
-                    w = expf(d / T);
-                    f = temp_last ? expf(d) : w;
+                    w = ex2_approx(d * (kLog2eF / T));
+                    f = temp_last ? ex2_approx(d * kLog2eF) : w;
                     wf[j] = f;
                     wd[j] = w;
                 } else {
