@@ -362,6 +362,7 @@ def gpu_arm(args, rank, world, local_rank):
         "extra_ops": extra,
         "configs": named_configs(B, dev, stream),
         "rows_sweep": rows_sweep(B, dev, stream),
+        "spec_sweep": spec_sweep(B, dev, stream),
     }
     return line
 
@@ -590,6 +591,57 @@ def rows_sweep(B, dev, stream):
                                  "gbs": round(gbs, 1)}, **fracs(gbs, peak)))
             del g
     del big
+    torch.cuda.synchronize()
+    return out
+
+
+SPEC_SWEEP = ((1, 1), (1, 4), (1, 8), (2, 4), (4, 4))
+
+
+def spec_sweep(B, dev, stream):
+    """Speculative acceptance on small batches (S sequences x K drafts) at
+    V = 248,320, both rules, timed like the step's ops: each call reads one
+    of several resident copies of its inputs (at least ~500 MB between two
+    reads of a copy, or 64 copies). Latency-bound: a few MB a call."""
+    import torch
+    from sampling_row_fp32_gb300 import synth
+    out = {"workload": f"S sequences x K drafts, V = {V:,}, T = 1, draft = target + N(0, 0.7^2)", "cases": []}
+    for S, K in SPEC_SWEEP:
+        si = synth.spec_inputs(S=S, K=K, V=V, seed_target=S + K, seed_draft=7, seed_u=9, sigma_noise=0.7)
+        n = int(min(64, max(2, 500e6 // (si.target.nbytes + si.draft.nbytes))))
+        t = torch.from_numpy(si.target).to(dev).unsqueeze(0).repeat(n, 1, 1, 1)
+        d = torch.from_numpy(si.draft).to(dev).unsqueeze(0).repeat(n, 1, 1, 1)
+        tok = torch.from_numpy(si.draft_tokens.view(np.int32)).to(dev)
+        ua = torch.from_numpy(si.u_acc).to(dev)
+        uf = torch.from_numpy(si.u_fin).to(dev)
+        acc = torch.empty(S, dtype=torch.int32, device=dev)
+        emi = torch.empty(S, K + 1, dtype=torch.int32, device=dev)
+        ws = B.workspace(B.SEL_OP_SPEC, S, V, K, device=dev)
+        rej = B.SpecParams(1.0, B.SPEC_MODE_REJECTION)
+        arg = B.SpecParams(1.0, B.SPEC_MODE_ARGMAX)
+        case = {"S": S, "K": K}
+        for name, fn in (("rejection_us", lambda i: B.spec_accept(t[i % n], d[i % n], tok, rej, ua, uf, acc, emi, ws)),
+                         ("argmax_us", lambda i: B.spec_accept(t[i % n], None, tok, arg, None, None, acc, emi, ws))):
+            with torch.cuda.stream(stream):
+                for i in range(3):
+                    fn(i)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(SWEEP_REPS):
+                    fn(i)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                g.replay()
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+            torch.cuda.synchronize()
+            case[name] = round(a.elapsed_time(b) * 1e3 / SWEEP_REPS, 3)
+            del g
+        out["cases"].append(case)
+        del t, d
     torch.cuda.synchronize()
     return out
 
