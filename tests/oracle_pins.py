@@ -420,6 +420,34 @@ def pin_spec_stream_is_target(orc):
     assert stat <= g["critical"], stat
 
 
+def pin_spec_chi_square_power(orc):
+    """mlxcel, Regression guards: the stream statistic has power. On the
+    same rounds as the stream pin it rejects two known-wrong rules: argmax
+    against argmax (the oracle's other mode), and the rejection rule's own
+    decisions followed by a redraw from p instead of the residual (built
+    here from the same draft tokens and uniforms; its accept decisions must
+    equal the oracle's)."""
+    g = golden("chi_square_recipe.json")
+    rng = np.random.default_rng(61)
+    p = rng.dirichlet(np.ones(6) * 2)
+    q = rng.dirichlet(np.ones(6) * 2)
+    n = g["samples"]
+    r = _spec_rounds(orc, p, q, n, seed=62, mode=1)
+    counts = np.bincount(r.emitted[:, 0].astype(np.int64), minlength=6)
+    assert chi_square(counts, p) > g["critical"]
+    # the same uniforms and tokens _spec_rounds draws (K = 1)
+    ref = _spec_rounds(orc, p, q, n, seed=62)
+    rng = np.random.default_rng(62)
+    t = _draws_from(rng, q, n)
+    u_acc = rng.random((n, 1), dtype=np.float32)[:, 0].astype(np.float64)
+    u_fin = rng.random(n, dtype=np.float32).astype(np.float64)
+    accept = u_acc * q[t] <= p[t]
+    assert np.array_equal(accept, ref.accepted == 1)
+    redraw = np.searchsorted(np.cumsum(p) / p.sum(), u_fin, side="right")
+    wrong = np.where(accept, t, redraw)
+    assert chi_square(np.bincount(wrong, minlength=6), p) > g["critical"]
+
+
 def pin_spec_support(orc):
     """mlxcel, Regression guards: with a top_k = 2 target no emitted token
     ever lies outside the target's support (accepted drafts, residual draws
@@ -685,7 +713,7 @@ ALL_PINS = [
     pin_sample_closed_forms, pin_sample_cdf_grid, pin_sample_support,
     pin_sample_invalid, pin_sample_margins, pin_filters_closed_forms, pin_filters_reduce,
     pin_spec_closed_forms, pin_spec_ceiling_example, pin_spec_acceptance_law,
-    pin_spec_stream_is_target, pin_spec_support, pin_spec_regimes,
+    pin_spec_stream_is_target, pin_spec_chi_square_power, pin_spec_support, pin_spec_regimes,
     pin_spec_greedy, pin_spec_invalid, pin_spec_margins,
     pin_diag_closed_forms, pin_diag_inequality, pin_diag_is_the_rejection_acceptance,
     pin_sampler_acceptance_law, pin_sampler_stream_is_target, pin_sampler_greedy_and_support,
