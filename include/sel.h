@@ -14,8 +14,8 @@
  *    logits + r * V (a row stride of exactly V floats). The vector path needs
  *    logits 16-byte aligned and V % 4 == 0; any other 4-byte-aligned layout
  *    takes the scalar path, with identical results.
- *  - Workspace. d_ws holds per-row partial results and the counters that
- *    let the last block of a row combine them. Size it with
+ *  - Workspace. d_ws holds per-row partial results, and the slots that the
+ *    finishing launches combine and clear again. Size it with
  *    sel_workspace_bytes() for the largest call it will serve, zero it once
  *    with sel_workspace_init() after allocating it, then reuse it: every call
  *    leaves its counters at zero again. Calls that may run concurrently (on
